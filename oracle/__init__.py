@@ -1,0 +1,184 @@
+"""Float64 CPU oracle for the chunkwise gated delta rule -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it, and it imports nothing from the product.
+
+The forward oracle is the token recurrence itself (page "Diagonal Plus Low
+Rank", section 2, opening equation), run in float64 by ``recurrence.c``:
+
+    S_t = S_{t-1} Diag(alpha_t) (I - b_t a_t^T) + vv_t k_t^T,   o_t = S_t q_t
+
+Every variant is a choice of (a, b, vv, alpha):
+
+* KDA: a = k, b = beta k, vv = beta v, alpha = exp(g) per channel
+  (DPLR page, "relation to KDA"; page "How to make GDN2 more stable", eq. (1)).
+* GDN: as KDA with one scalar log-decay per token (same eq. (1), D = gamma I).
+* DeltaNet: as KDA with alpha = 1 (DeltaNet page, section 4.1).
+* GLA: b = 0 and vv = v (GLA page, section 5.1).
+* DPLR: a, b given, vv = v (DPLR page, section 2).
+
+Parity status of each function is listed in ``PINS`` below; each pin is a test
+under ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from .spectral import factor_norm_exact, rho_closed_form  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "recurrence.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+GATE_NONE, GATE_SCALAR, GATE_CHANNEL = 0, 1, 2
+
+# Which test pins each oracle function to something other than itself.
+PINS = {
+    "recurrence": [
+        "linear-attention closed form (g = 0, beta = 0)",
+        "GLA parallel closed form with decay (beta = 0, vv = v)",
+        "delta-rule write: with unit k and q = k, o_t = (1 - beta) S_{t-1} Diag(alpha) k + beta v",
+        "hand-derived worked example, tests/golden/tiny_kda_worked.txt",
+        "DeltaNet/KDA/DPLR chunk forms of the pages equal the recurrence for several C",
+        "h0 -> ht chaining over split segments equals one call",
+    ],
+    "rho_closed_form": ["numpy SVD", "eq. (5) lower bound", "eq. (6) equality case",
+                        "hand-derived values, tests/golden/spectral_norm_points.txt"],
+    "factor_norm_exact": ["explicit 2x2 reduction of eq. (9)", "D = I reduces to rho"],
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile ``recurrence.c`` with gcc into ``oracle/_build/liboracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.oracle_recurrence_head.restype = ctypes.c_int
+            lib.oracle_recurrence_head.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                dp, dp, ctypes.c_long,
+                dp, ctypes.c_long,
+                dp, ctypes.c_long, ctypes.c_int,
+                dp, dp, ctypes.c_long,
+                dp, ctypes.c_long, ctypes.c_int,
+                dp, dp, ctypes.c_long, dp]
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    return None if x is None else np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(x, offset=0):
+    if x is None:
+        return None
+    return ctypes.cast(x.ctypes.data + 8 * offset, ctypes.POINTER(ctypes.c_double))
+
+
+def recurrence(q, k, v, g=None, gate=GATE_CHANNEL, beta=None, a=None, b=None,
+               scale_v=True, h0=None, threads=None, heads=None):
+    """Run the token recurrence for every (batch, head) of [B, T, H, d] inputs.
+
+    q, k: [B, T, H, dk]; v: [B, T, H, dv]; g: [B, T, H, dk] (GATE_CHANNEL),
+    [B, T, H] (GATE_SCALAR) or None (GATE_NONE); beta: [B, T, H] or None;
+    a, b: [B, T, H, dk] or None (None -> KDA mapping a = k, b = beta k);
+    h0: [B, H, dv, dk] or None.  ``heads`` optionally restricts the work to a
+    list of (b, h) pairs; the other outputs stay zero.
+    Returns (o [B, T, H, dv], ht [B, H, dv, dk]) in float64.
+    """
+    lib = _load()
+    q, k, v, g, beta, a, b, h0 = map(_f64, (q, k, v, g, beta, a, b, h0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if g is None:
+        gate = GATE_NONE
+    if (a is None) != (b is None):
+        raise ValueError("a and b are given together or not at all")
+    o = np.zeros((B, T, H, dv), np.float64)
+    ht = np.zeros((B, H, dv, dk), np.float64)
+    s_qk, s_v, s_o = H * dk, H * dv, H * dv
+    s_g = (H * dk) if gate == GATE_CHANNEL else H
+    pairs = heads if heads is not None else [(bi, hi) for bi in range(B) for hi in range(H)]
+
+    def one(pair):
+        bi, hi = pair
+        base_qk = (bi * T * H + hi) * dk
+        base_v = (bi * T * H + hi) * dv
+        gbase = 0
+        if gate == GATE_CHANNEL:
+            gbase = (bi * T * H + hi) * dk
+        elif gate == GATE_SCALAR:
+            gbase = bi * T * H + hi
+        rc = lib.oracle_recurrence_head(
+            T, dk, dv,
+            _ptr(q, base_qk), _ptr(k, base_qk), s_qk,
+            _ptr(v, base_v), s_v,
+            _ptr(g, gbase) if g is not None else None, s_g, gate,
+            _ptr(a, base_qk) if a is not None else None,
+            _ptr(b, base_qk) if b is not None else None, s_qk,
+            _ptr(beta, bi * T * H + hi) if beta is not None else None, H,
+            1 if scale_v else 0,
+            _ptr(h0, (bi * H + hi) * dv * dk) if h0 is not None else None,
+            _ptr(o, base_v), s_o,
+            _ptr(ht, (bi * H + hi) * dv * dk))
+        if rc != 0:
+            raise MemoryError("oracle scratch allocation failed")
+
+    nthreads = threads or len(os.sched_getaffinity(0))
+    if nthreads <= 1 or len(pairs) == 1:
+        for p in pairs:
+            one(p)
+    else:
+        with ThreadPoolExecutor(max_workers=nthreads) as ex:
+            list(ex.map(one, pairs))
+    return o, ht
+
+
+def kda_fwd(q, k, v, g, beta, h0=None, **kw):
+    """KDA: per-channel log-decay g [B,T,H,dk], a = k, b = beta k, vv = beta v."""
+    return recurrence(q, k, v, g=g, gate=GATE_CHANNEL, beta=beta, scale_v=True, h0=h0, **kw)
+
+
+def gdn_fwd(q, k, v, g, beta, h0=None, **kw):
+    """GDN: one log-decay per token g [B,T,H] broadcast over channels."""
+    return recurrence(q, k, v, g=g, gate=GATE_SCALAR, beta=beta, scale_v=True, h0=h0, **kw)
+
+
+def deltanet_fwd(q, k, v, beta, h0=None, **kw):
+    """DeltaNet: alpha = 1."""
+    return recurrence(q, k, v, g=None, gate=GATE_NONE, beta=beta, scale_v=True, h0=h0, **kw)
+
+
+def gla_fwd(q, k, v, g, h0=None, **kw):
+    """GLA: beta = 0 and vv = v (no delta correction, values unscaled)."""
+    return recurrence(q, k, v, g=g, gate=GATE_CHANNEL, beta=None, scale_v=False, h0=h0, **kw)
+
+
+def dplr_fwd(q, k, v, a, b, g, h0=None, **kw):
+    """General gated DPLR: independent a, b [B,T,H,dk]; vv = v."""
+    return recurrence(q, k, v, g=g, gate=GATE_CHANNEL, a=a, b=b, scale_v=False, h0=h0, **kw)
