@@ -1,0 +1,352 @@
+"""Throughput of the chunkwise KDA forward on GB300 (one JSON line on stdout).
+
+A step is one kda_chunk_fwd call -- the whole forward path: decay cumsum,
+rescaling, WY build, state scan and output -- over the KDA workload
+B=4, T=4096, H=16, dk=dv=128, bf16 inputs, fp32 state, initial state given.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl ours (default): the CUDA library through its C ABI.  `value` is tokens/s
+with the inputs resident in HBM; `e2e` is the same metric with pinned host
+inputs copied in and o / ht copied out inside the timed region; `roofline`
+compares the kernel's algorithmic bytes per launch against the measured HBM
+copy bandwidth; `cpu_baseline` times the float64 oracle on a bounded sample
+of the same workload on the host cores.
+--impl reference: the float64 oracle (the only reference this method has) on
+the host cores, on a bounded sample per step.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload: the
+(batch, head) scans are independent, so there is no collective on the data
+path ("scaling": "weak").  Rank 0 prints the line; times are the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+WORKLOAD = "kda_bf16_b4t4096h16d128"
+METRIC = "tokens/s KDA chunk fwd(+bwd) B4·T4096·H16·d128 bf16; % of roofline"
+KERNEL_SRC = os.path.join(ROOT, "chunkwise_gated_delta_gb300", "csrc", "kda_fwd_tc.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_fwd_tc_b4t4096h16d128_traffic.txt")
+
+
+def algorithmic_bytes(w) -> int:
+    """Inputs read once and outputs written once: q, k, v, g, o (bf16), beta (bf16), h0 and ht (fp32)."""
+    bth = w.B * w.T * w.H
+    seq = bth * (3 * w.dk + w.dv + w.dv) * 2          # q, k, g (dk wide) + v, o (dv wide)
+    beta = bth * 2
+    state = 2 * w.B * w.H * w.dv * w.dk * 4            # h0 + ht
+    return seq + beta + state
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def traffic_per_launch():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    try:
+        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+        vals = {}
+        for line in open(TRAFFIC_FILE):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256_16") != src_hash:
+            return None
+        return int(vals["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while a region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r for t, r in self.rows if self.t0 is not None and self.t0 - 0.15 <= t <= self.t1 + 0.15]
+        if not rows and self.rows:
+            rows = [min(self.rows, key=lambda tr: abs(tr[0] - (self.t1 or tr[0])))[1]]
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_sample(w, x, heads, T):
+    """Time the float64 oracle on `heads` (b, h) pairs over the first T tokens."""
+    import oracle
+    f = lambda t: t[:, :T].double().numpy() if t.dim() >= 3 else t.double().numpy()
+    q, k, v, g, beta = (f(x[n]) for n in ("q", "k", "v", "g", "beta"))
+    h0 = x["h0"].double().numpy() if "h0" in x else None
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    oracle.kda_fwd(q, k, v, g, beta, h0, heads=heads, threads=cores)
+    dt = time.perf_counter() - t0
+    tokens = len(heads) * T / w.H              # head-tokens expressed as workload tokens
+    return tokens, dt, cores
+
+
+def cpu_baseline_leg(w, x, budget_s=12.0):
+    """Oracle on a bounded sample: as many (b, h) pairs over the full T as fit the budget."""
+    cores = len(os.sched_getaffinity(0))
+    pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
+    probe = pairs[:min(cores, len(pairs))]
+    tokens, dt, _ = oracle_sample(w, x, probe, w.T)
+    n = len(probe)
+    scale = max(1, int(budget_s / max(dt, 1e-3)))
+    n = min(len(pairs), n * scale)
+    if n > len(probe):
+        tokens, dt, _ = oracle_sample(w, x, pairs[:n], w.T)
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {len(pairs)} (batch, head) pairs over the full T={w.T}, float64 token "
+                      f"recurrence in C, {cores} threads; tokens counted as head-tokens / H; {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    from chunkwise_gated_delta_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[WORKLOAD]
+    if rank != 0:
+        return
+    x = make_inputs(w, seed=0)
+    cores = len(os.sched_getaffinity(0))
+    pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
+    heads = pairs[:min(cores, len(pairs))]
+    # size each step so the whole run stays within about a minute
+    tokens, dt, _ = oracle_sample(w, x, heads, 256)
+    per_step_budget = max(0.05, 60.0 / max(1, args.steps + args.warmup))
+    T = int(min(w.T, max(64, 256 * per_step_budget / max(dt, 1e-4))))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, heads, T)
+    tot_tokens, tot_dt = 0.0, 0.0
+    for _ in range(args.steps):
+        tk, dt, _ = oracle_sample(w, x, heads, T)
+        tot_tokens += tk
+        tot_dt += dt
+    value = tot_tokens / tot_dt
+    sample = (f"{len(heads)} (batch, head) pairs x {T} tokens per step, float64 token recurrence in C, "
+              f"{cores} threads; tokens counted as head-tokens / H")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+            "h0": w.h0, "inputs": "bf16 q,k,v,g,beta; fp32 h0/ht",
+            "l2": f"no flush: inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.1f} MB per step vs 129 MB)",
+            "parallelism": "replicas (independent (batch, head) scans, no collective)"}
+
+
+def run_ours(args, rank, world, local):
+    from chunkwise_gated_delta_gb300 import HostRunner, kda_chunk_fwd
+    from chunkwise_gated_delta_gb300.inputs import WORKLOADS, make_inputs
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, seed=rank)
+    d = {k: v.to(dev) for k, v in x.items() if isinstance(v, torch.Tensor)}
+    o = torch.empty(w.B, w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    ht = torch.empty(w.B, w.H, w.dv, w.dk, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o=o, ht=ht, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark_begin()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    launch_ms = max_over_ranks(launch_ms, world)
+
+    # end to end from pinned host buffers
+    runner = HostRunner(x, device=dev, scale_v=True, gate="channel")
+    for _ in range(max(3, min(args.warmup, 10))):
+        runner.run(stream)
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 50))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        runner.run(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    barrier(world)
+
+    tokens = w.B * w.T
+    peaks, peak_kind = measured_peaks()
+    abytes = algorithmic_bytes(w)
+    achieved = abytes / (launch_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * tokens * args.steps / (elapsed_ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config_dict(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_per_launch(),
+                     "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+                     "algorithmic_bytes_per_launch": abytes, "kernel_ms_per_launch": launch_ms},
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 or rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_leg(w, x)
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,8 @@
+"""Chunkwise gated delta rule (KDA, GDN, DeltaNet, GLA) on GB300 / sm_103a.
+
+The computation lives in the CUDA library ``_build/libkda.so`` (C ABI in
+``include/kda.h``); :mod:`.api` is its Python binding.  Build the library with
+:func:`.build.build`.
+"""
+from .api import (HostRunner, KdaError, deltanet_fwd, gdn_fwd, gla_fwd,  # noqa: F401
+                  kda_chunk_fwd, status_read)

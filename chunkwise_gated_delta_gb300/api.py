@@ -1,0 +1,169 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every step of the computation runs in the CUDA library (``libkda.so``); this
+module only turns torch tensors into pointers and sizes, picks the current
+stream and keeps a zero-filled workspace per device.  There is no CPU path:
+when the library is missing, :func:`_lib.load` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import KdaError
+
+_GATES = {"none": _lib.KDA_GATE_NONE, "scalar": _lib.KDA_GATE_SCALAR, "channel": _lib.KDA_GATE_CHANNEL}
+_workspaces: dict = {}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.KDA_BF16
+    if t.dtype == torch.float32:
+        return _lib.KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_for(device, nbytes: int) -> torch.Tensor:
+    """A cached, zero-filled workspace of at least ``nbytes`` on ``device``."""
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
+def make_args(q, k, v, g=None, beta=None, h0=None, o=None, ht=None, *, gate=None, scale_v=True,
+              workspace=None) -> _lib.KdaFwdArgs:
+    """Fill the C argument struct from tensors (no validation beyond the C side's)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if gate is None:
+        gate = "none" if g is None else ("scalar" if g.dim() == 3 else "channel")
+    a = _lib.KdaFwdArgs()
+    a.B, a.T, a.H, a.dk, a.dv, a.chunk = B, T, H, dk, dv, 64
+    a.dtype = _dtype_code(q)
+    a.gate_kind = _GATES[gate]
+    a.g_dtype = _dtype_code(g) if g is not None else _lib.KDA_BF16
+    a.flags = _lib.KDA_FLAG_BETA_SCALES_V if scale_v else 0
+    a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
+    a.h0, a.o, a.ht = _ptr(h0), _ptr(o), _ptr(ht)
+    if workspace is not None:
+        a.workspace = _ptr(workspace)
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def kda_chunk_fwd(q, k, v, g=None, beta=None, h0=None, *, gate=None, scale_v=True,
+                  output_final_state=True, o=None, ht=None, workspace=None, stream=None):
+    """Chunkwise gated delta-rule forward through ``kda_chunk_fwd`` of the C ABI.
+
+    q, k: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, same dtype);
+    g: log-decay [B, T, H, dk] (per channel), [B, T, H] (scalar) or None;
+    beta: [B, T, H] in the dtype of q, or None (beta = 0);
+    h0: [B, H, dv, dk] fp32 or None.
+    Returns (o [B, T, H, dv] in q's dtype, ht [B, H, dv, dk] fp32 or None).
+    """
+    lib = _lib.load()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (h0, "h0")):
+        _check(t, name)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    if ht is None and output_final_state:
+        ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device)
+    args = make_args(q, k, v, g, beta, h0, o, ht, gate=gate, scale_v=scale_v)
+    need = lib.kda_chunk_fwd_workspace(ctypes.byref(args))
+    if need == 0:
+        # invalid arguments: let the launch entry point report which status
+        rc = lib.kda_chunk_fwd(ctypes.byref(args), None)
+        raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "kda_chunk_fwd")
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    args.workspace = _ptr(workspace)
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = lib.kda_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd")
+    return o, ht
+
+
+def status_read(workspace=None, device=None, stream=None) -> int:
+    """Device status word of the workspace (waits for the stream, then clears it)."""
+    lib = _lib.load()
+    if workspace is None:
+        workspace = workspace_for(device or torch.cuda.current_device(), 256)
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    return lib.kda_status_read(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+
+
+def gdn_fwd(q, k, v, g, beta, h0=None, **kw):
+    """GDN: one log-decay per token and head, g [B, T, H]."""
+    return kda_chunk_fwd(q, k, v, g, beta, h0, gate="scalar", scale_v=True, **kw)
+
+
+def deltanet_fwd(q, k, v, beta, h0=None, **kw):
+    """DeltaNet: no decay."""
+    return kda_chunk_fwd(q, k, v, None, beta, h0, gate="none", scale_v=True, **kw)
+
+
+def gla_fwd(q, k, v, g, h0=None, **kw):
+    """GLA: per-channel decay, no delta term, v unscaled."""
+    return kda_chunk_fwd(q, k, v, g, None, h0, gate="channel", scale_v=False, **kw)
+
+
+class HostRunner:
+    """End-to-end call from pinned host buffers.
+
+    Each :meth:`run` copies the inputs host->device, runs ``kda_chunk_fwd`` and
+    copies o (and ht) back device->host, all on one stream.  Device buffers
+    are allocated once and reused.
+    """
+
+    def __init__(self, host: dict, device="cuda", scale_v=True, gate=None):
+        self.host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        self.dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()
+                    if isinstance(v, torch.Tensor)}
+        q = self.dev["q"]
+        B, T, H, _ = q.shape
+        dv, dk = self.dev["v"].shape[-1], q.shape[-1]
+        self.o = torch.empty(B, T, H, dv, dtype=q.dtype, device=device)
+        self.ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)
+        self.o_host = torch.empty_like(self.o, device="cpu").pin_memory()
+        self.ht_host = torch.empty_like(self.ht, device="cpu").pin_memory()
+        self.scale_v, self.gate = scale_v, gate
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.dev.values())
+        self.d2h_bytes = self.o.numel() * self.o.element_size() + self.ht.numel() * 4
+
+    def run(self, stream=None):
+        stream = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(stream):
+            for k, v in self.dev.items():
+                v.copy_(self.host[k], non_blocking=True)
+            d = self.dev
+            kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"),
+                          gate=self.gate, scale_v=self.scale_v, o=self.o, ht=self.ht, stream=stream)
+            self.o_host.copy_(self.o, non_blocking=True)
+            self.ht_host.copy_(self.ht, non_blocking=True)
+        return self.o_host, self.ht_host

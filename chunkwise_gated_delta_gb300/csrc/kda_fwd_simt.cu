@@ -1,0 +1,207 @@
+// float32 CUDA-core kernel for the chunkwise gated delta rule.
+//
+// Computes the chunk form recapped on page "Kimi Delta Attention backward"
+// ("forward recap") in float32 throughout, one CTA per (value slice, head,
+// batch).  It serves float32 inputs, whose tolerance (1e-5 relative) no
+// tensor-core precision below fp32 meets.  Per chunk [t]:
+//
+//   G = in-chunk cumsum of g, Gamma = exp(G); Q<- = Q*Gamma, K<- = K*Gamma,
+//   K-> = K/Gamma (page "Diagonal Plus Low Rank", definition of Gamma);
+//   L = Diag(beta)(K<- K->^T * M_{-1});  A~ = (I + L)^{-1} by forward
+//   substitution, one column per thread (page "DeltaNet", section 4.2 gives
+//   the unit-lower-triangular inverse);
+//   W = A~ Diag(beta) K<-,  U = A~ Diag(beta) V  (or A~ V when beta does not
+//   scale v);  V_new = U - W S^T;  O = Q<- S^T + (Q<- K->^T * M) V_new;
+//   S <- (S + V_new^T K->) Diag(gamma^C)  (page "Gated Linear Attention",
+//   section 5.2 writes the state step in this factored form).
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kC = 64;      // chunk length
+constexpr int kDVS = 32;    // value channels per CTA
+constexpr int kThreads = 256;
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <int DK, typename Tg>
+__global__ void __launch_bounds__(kThreads)
+fwd_simt_kernel(const FwdParams p) {
+    constexpr int SK = DK + 1;     // padded row stride of [C][DK] tiles
+    constexpr int SC = kC + 1;     // padded row stride of [C][C] tiles
+    constexpr int SV = kDVS + 1;
+    extern __shared__ float smem[];
+    float *Ql = smem;                 // [C][SK]
+    float *Kl = Ql + kC * SK;         // [C][SK]
+    float *Kr = Kl + kC * SK;         // [C][SK]
+    float *Lm = Kr + kC * SK;         // [C][SC]  strictly lower Gram, beta rows
+    float *Pm = Lm + kC * SC;         // [C][SC]  inclusive-lower Q<- K->^T
+    float *Ym = Pm + kC * SC;         // [C][SC]  A~ = (I + L)^{-1}
+    float *Wm = Ym + kC * SC;         // [C][SK]
+    float *Vm = Wm + kC * SK;         // [C][SV]  raw v slice
+    float *Um = Vm + kC * SV;         // [C][SV]  U, then V_new
+    float *Sm = Um + kC * SV;         // [DVS][SK] state slice
+    float *bet = Sm + kDVS * SK;      // [C]
+    float *gC = bet + kC;             // [DK]
+
+    const int tid = threadIdx.x;
+    const int e0 = blockIdx.x * kDVS;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, H = p.H, dv = p.dv;
+    const float *q = static_cast<const float *>(p.q);
+    const float *k = static_cast<const float *>(p.k);
+    const float *v = static_cast<const float *>(p.v);
+    const Tg *g = static_cast<const Tg *>(p.g);
+    const float *beta = static_cast<const float *>(p.beta);
+    float *o = static_cast<float *>(p.o);
+
+    for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+        int e = idx / DK, d = idx % DK;
+        float s0 = 0.f;
+        if (p.h0) s0 = p.h0[(((size_t)b * H + h) * dv + e0 + e) * DK + d];
+        Sm[e * SK + d] = s0;
+    }
+
+    for (int t0 = 0; t0 < T; t0 += kC) {
+        const int nvalid = min(kC, T - t0);
+        __syncthreads();
+        // ---- prologue: Gamma, rescaled tiles (one key channel per thread)
+        if (tid < DK) {
+            const int d = tid;
+            float G = 0.f, gam = 1.f;
+            for (int c = 0; c < kC; ++c) {
+                float qv = 0.f, kv = 0.f;
+                if (c < nvalid) {
+                    size_t row = ((size_t)b * T + t0 + c) * H + h;
+                    qv = q[row * DK + d];
+                    kv = k[row * DK + d];
+                    if (p.gate_kind == KDA_GATE_CHANNEL) G += to_f(g[row * DK + d]);
+                    else if (p.gate_kind == KDA_GATE_SCALAR) G += to_f(g[row]);
+                    gam = expf(G);
+                }
+                Ql[c * SK + d] = qv * gam;
+                Kl[c * SK + d] = kv * gam;
+                Kr[c * SK + d] = kv / gam;
+            }
+            gC[d] = gam;
+        }
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            int c = idx / kDVS, e = idx % kDVS;
+            float vv = 0.f;
+            if (c < nvalid) vv = v[(((size_t)b * T + t0 + c) * H + h) * dv + e0 + e];
+            Vm[c * SV + e] = vv;
+        }
+        if (tid < kC) {
+            float bv = 0.f;
+            if (p.has_beta && tid < nvalid) bv = beta[((size_t)b * T + t0 + tid) * H + h];
+            bet[tid] = bv;
+        }
+        __syncthreads();
+        // ---- Gram matrices: L = Diag(beta)(K<- K->^T * M_{-1}), P = Q<- K->^T * M
+        for (int idx = tid; idx < kC * kC; idx += kThreads) {
+            int i = idx / kC, j = idx % kC;
+            float l = 0.f, pp = 0.f;
+            if (j <= i) {
+                for (int d = 0; d < DK; ++d) {
+                    float kr = Kr[j * SK + d];
+                    l += Kl[i * SK + d] * kr;
+                    pp += Ql[i * SK + d] * kr;
+                }
+            }
+            Lm[i * SC + j] = (j < i) ? bet[i] * l : 0.f;
+            Pm[i * SC + j] = pp;
+        }
+        __syncthreads();
+        // ---- A~ = (I + L)^{-1}: column c solved by forward substitution
+        if (tid < kC) {
+            const int c = tid;
+            for (int i = 0; i < kC; ++i) {
+                float y = 0.f;
+                if (i == c) y = 1.f;
+                else if (i > c) {
+                    for (int j = c; j < i; ++j) y -= Lm[i * SC + j] * Ym[j * SC + c];
+                }
+                Ym[i * SC + c] = y;
+            }
+        }
+        __syncthreads();
+        // ---- W = A~ Diag(beta) K<-,  U = A~ Diag(beta) V  (or A~ V)
+        for (int idx = tid; idx < kC * DK; idx += kThreads) {
+            int i = idx / DK, d = idx % DK;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j) acc += Ym[i * SC + j] * bet[j] * Kl[j * SK + d];
+            Wm[i * SK + d] = acc;
+        }
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            int i = idx / kDVS, e = idx % kDVS;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j)
+                acc += Ym[i * SC + j] * (p.scale_v ? bet[j] : 1.f) * Vm[j * SV + e];
+            Um[i * SV + e] = acc;
+        }
+        __syncthreads();
+        // ---- V_new = U - W S^T
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            int i = idx / kDVS, e = idx % kDVS;
+            float acc = Um[i * SV + e];
+            for (int d = 0; d < DK; ++d) acc -= Wm[i * SK + d] * Sm[e * SK + d];
+            Um[i * SV + e] = acc;
+        }
+        __syncthreads();
+        // ---- O = Q<- S^T + P V_new
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            int i = idx / kDVS, e = idx % kDVS;
+            float acc = 0.f;
+            for (int d = 0; d < DK; ++d) acc += Ql[i * SK + d] * Sm[e * SK + d];
+            for (int j = 0; j <= i; ++j) acc += Pm[i * SC + j] * Um[j * SV + e];
+            if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = acc;
+        }
+        __syncthreads();
+        // ---- S <- (S + V_new^T K->) Diag(gamma^C)
+        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+            int e = idx / DK, d = idx % DK;
+            float acc = Sm[e * SK + d];
+            for (int c = 0; c < kC; ++c) acc += Um[c * SV + e] * Kr[c * SK + d];
+            Sm[e * SK + d] = acc * gC[d];
+        }
+    }
+    __syncthreads();
+    if (p.ht) {
+        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+            int e = idx / DK, d = idx % DK;
+            p.ht[(((size_t)b * H + h) * dv + e0 + e) * DK + d] = Sm[e * SK + d];
+        }
+    }
+}
+
+template <int DK>
+constexpr size_t simt_smem_bytes() {
+    return sizeof(float) * (size_t)(3 * kC * (DK + 1) + 3 * kC * (kC + 1) + kC * (DK + 1) +
+                                    2 * kC * (kDVS + 1) + kDVS * (DK + 1) + kC + DK);
+}
+
+template <int DK, typename Tg>
+cudaError_t launch_dk(const FwdParams &p, cudaStream_t s) {
+    const size_t smem = simt_smem_bytes<DK>();
+    cudaError_t e = cudaFuncSetAttribute(fwd_simt_kernel<DK, Tg>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.dv / kDVS, p.H, p.B);
+    fwd_simt_kernel<DK, Tg><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt_f32(const FwdParams &p, int g_is_bf16, cudaStream_t s) {
+    if (p.dk == 64) return g_is_bf16 ? launch_dk<64, __nv_bfloat16>(p, s) : launch_dk<64, float>(p, s);
+    if (p.dk == 128) return g_is_bf16 ? launch_dk<128, __nv_bfloat16>(p, s) : launch_dk<128, float>(p, s);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace kda

@@ -1,0 +1,735 @@
+// Fused tcgen05 kernel for the chunkwise KDA forward (bf16 in, fp32 accumulate,
+// fp32 state), GB300 / sm_103a.
+//
+// One CTA owns one (batch, head, 64-wide value slice) and walks its chunks in
+// order.  The chunk form it evaluates is the one recapped on page "Kimi Delta
+// Attention backward" ("forward recap"), regrouped so every tensor-core
+// product has M = 128 rows:
+//
+//   [beta K<- ; Q<-] K->^T      = [L ; P]          (Gram, one MMA)
+//   T  = (I + L_{strict})^{-1} Diag(beta)          (CUDA cores, 16x16 blocks,
+//        page "DeltaNet" 4.2, block form 1 applied twice)
+//   [I ; P] T                   = Z = [T ; P T]
+//   Z K<-                       = [W ; P W]
+//   Z V                         = [U ; P U]        (into the accumulator D1)
+//   D1 += [-W ; Q<- - P W] S^T  = [V_new ; O]      (state-dependent, one MMA)
+//   K~^T V_new                  = dS^T,  S <- S Diag(gamma^C) + dS
+//
+// O = Q<- S^T + (Q<- K->^T * M) V_new expands to (Q<- - P W) S^T + P U, which
+// is why the output rides in the lower half of the state-dependent product.
+// K~ = K * exp(G_C - G) is K-> Diag(gamma^C) written without the division.
+//
+// Warp roles (384 threads):
+//   warps 0-3  "chain": the serial part -- the state S^T (dk x 64 slice) lives
+//              in fp32 registers, one key channel per thread.
+//   warps 4-11 "WY": everything that does not depend on S, one chunk ahead.
+// Every wait on an mbarrier is bounded; on timeout the kernel writes the
+// status word, turns every later wait into a no-op and runs to its end.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kda_internal.h"
+#include "tc_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;        // chunk length
+constexpr int kDK = 128;      // key dim
+constexpr int kDVS = 64;      // value channels per CTA
+constexpr int kChainThreads = 128;
+constexpr int kWyThreads = 256;
+constexpr int kThreads = kChainThreads + kWyThreads;
+
+// ---- shared memory map (byte offsets from a 1024-aligned base)
+constexpr uint32_t OFF_RAWQ = 0;         // q tile, 2 column blocks of [64][64] bf16, SW128
+constexpr uint32_t OFF_RAWK = 16384;     // k tile
+constexpr uint32_t OFF_RAWG = 32768;     // g tile (per-channel gate)
+constexpr uint32_t OFF_V0 = 49152;       // v slice [64 rows][64] bf16, SW128 (MN-major B), slot 0
+constexpr uint32_t OFF_V1 = 57344;       // slot 1
+constexpr uint32_t OFF_AG = 65536;       // [beta K<- ; Q<-] 128 x 128 K-major; later Y (fp32) / T
+constexpr uint32_t OFF_KR = 98304;       // K-> 64 x 128 (K-major B); later L (fp32), [I;P], Z
+constexpr uint32_t OFF_KL = 114688;      // K<- 64 x 128 (MN-major B)
+constexpr uint32_t OFF_ACH = 131072;     // [-W ; Q'] 128 x 128 K-major
+constexpr uint32_t OFF_KT0 = 163840;     // K~ 64 x 128 (MN-major A), slot 0
+constexpr uint32_t OFF_KT1 = 180224;     // slot 1
+constexpr uint32_t OFF_ST = 196608;      // S^T 128 x 64 bf16 (MN-major B); V_new / O staging
+constexpr uint32_t OFF_MISC = 212992;
+constexpr uint32_t MISC_GC = 0;          // gamma^C [2][128] f32
+constexpr uint32_t MISC_BETA = 1024;     // beta [2][64] f32
+constexpr uint32_t MISC_GS = 1536;       // scalar gate [2][64] f32
+constexpr uint32_t MISC_TOT = 2048;      // cumsum partials [4][128] f32
+constexpr uint32_t MISC_BAR = 4096;      // mbarriers
+constexpr uint32_t MISC_TSLOT = 4352;    // TMEM base address
+constexpr uint32_t MISC_ABORT = 4356;    // abort flag
+constexpr uint32_t kSmemBytes = OFF_MISC + 4608 + 1024;
+
+// ---- TMEM columns
+constexpr uint32_t TM_G = 0;      // Gram [L ; P], 64 cols
+constexpr uint32_t TM_Z = 64;     // Z, 64 cols
+constexpr uint32_t TM_WQ = 128;   // [W ; P W], 128 cols
+constexpr uint32_t TM_D1 = 256;   // [U ; P U] -> [V_new ; O], 2 slots x 64 cols
+constexpr uint32_t TM_S = 384;    // dS^T, 64 cols
+constexpr uint32_t kTmemCols = 512;
+
+// mbarrier indices
+enum {
+    B_RAW = 0, B_V0, B_V1, B_GRAM, B_Z, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
+    B_FIN0, B_FIN1, kNumBars
+};
+
+struct Ctx {
+    uint8_t *base;
+    uint64_t *bars;
+    volatile int *abort;
+    int *status;
+    uint32_t tmem;
+};
+
+__device__ __forceinline__ void record_timeout(const Ctx &c) {
+    *c.abort = 1;
+    atomicCAS(c.status, kDevOk, kDevTimeout);
+}
+
+// Bounded wait that becomes a no-op once any thread has given up.
+__device__ __forceinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
+    uint64_t *bar = c.bars + idx;
+    for (uint32_t i = 0; i < kWaitBound; ++i) {
+        if (mbar_try_wait(bar, parity)) return;
+        if (*c.abort) return;
+    }
+    record_timeout(c);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ float2 ld_bf16x2(const uint8_t *p) {
+    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(p);
+    return __bfloat1622float2(h);
+}
+__device__ __forceinline__ void st_u32(uint8_t *p, uint32_t v) { *reinterpret_cast<uint32_t *>(p) = v; }
+__device__ __forceinline__ void st_u128(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
+}
+
+// fp32 [64][64] scratch with an XOR swizzle on the low 5 column bits: row and
+// column walks across a warp both hit 32 distinct banks.
+__device__ __forceinline__ uint32_t lidx(uint32_t i, uint32_t j) { return i * 64u + (j ^ (i & 31u)); }
+
+// Y (the inverse) lives in the dead beta K<- rows of the A_G tile, which are
+// two 8 KB pieces: rows 0-31 at +0, rows 32-63 at +16 KB.
+__device__ __forceinline__ float *yptr(uint8_t *base, uint32_t i, uint32_t j) {
+    float *y = reinterpret_cast<float *>(base + OFF_AG + (i >= 32 ? 16384u : 0u));
+    return y + lidx(i & 31u, j);
+}
+
+template <typename T> __device__ __forceinline__ float ldg_f(const T *p);
+template <> __device__ __forceinline__ float ldg_f<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+}
+template <> __device__ __forceinline__ float ldg_f<float>(const float *p) { return *p; }
+
+// ============================================================================
+// WY warps: everything of chunk n that does not depend on the state.
+// ============================================================================
+template <int GATE, bool GLA, typename Tg>
+__device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                        const CUtensorMap *tm_g, const CUtensorMap *tm_v, int e0, int h, int b, int nchunks) {
+    uint8_t *base = c.base;
+    const int wt = threadIdx.x - kChainThreads;          // 0..255
+    const int warp = threadIdx.x >> 5;                   // 4..11
+    const int lane = threadIdx.x & 31;
+    const int quarter = warp & 3;                        // TMEM lane quarter
+    const int half = (warp - 4) >> 2;                    // column half
+    const bool leader = wt == 0;
+    const int T = p.T, H = p.H;
+    float *gC = reinterpret_cast<float *>(base + OFF_MISC + MISC_GC);
+    float *betas = reinterpret_cast<float *>(base + OFF_MISC + MISC_BETA);
+    float *gss = reinterpret_cast<float *>(base + OFF_MISC + MISC_GS);
+    float *tot = reinterpret_cast<float *>(base + OFF_MISC + MISC_TOT);
+    const __nv_bfloat16 *betag = static_cast<const __nv_bfloat16 *>(p.beta);
+    const Tg *gsg = static_cast<const Tg *>(p.g);
+    const uint32_t raw_bytes = (GATE == KDA_GATE_CHANNEL ? 3u : 2u) * 16384u;
+
+    auto issue_raw = [&](int n) {
+        mbar_arrive_expect_tx(c.bars + B_RAW, raw_bytes);
+        for (int blk = 0; blk < 2; ++blk) {
+            tma_load_4d(base + OFF_RAWQ + blk * 8192, tm_q, c.bars + B_RAW, blk * 64, h, n * kC, b);
+            tma_load_4d(base + OFF_RAWK + blk * 8192, tm_k, c.bars + B_RAW, blk * 64, h, n * kC, b);
+            if (GATE == KDA_GATE_CHANNEL)
+                tma_load_4d(base + OFF_RAWG + blk * 8192, tm_g, c.bars + B_RAW, blk * 64, h, n * kC, b);
+        }
+    };
+    auto issue_v = [&](int n) {
+        const int s = n & 1;
+        mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
+        tma_load_4d(base + (s ? OFF_V1 : OFF_V0), tm_v, c.bars + B_V0 + s, e0, h, n * kC, b);
+    };
+    // per-token scalars of chunk n: beta and (GDN) the scalar log-decay
+    auto load_scalars = [&](int n, float &bv, float &gv) {
+        bv = 0.f; gv = 0.f;
+        const int t = n * kC + wt;
+        if (wt < kC && t < T) {
+            const size_t row = ((size_t)b * T + t) * H + h;
+            if (p.has_beta) bv = __bfloat162float(betag[row]);
+            if (GATE == KDA_GATE_SCALAR) gv = ldg_f<Tg>(gsg + row);
+        }
+    };
+
+    if (leader) {
+        issue_raw(0);
+        issue_v(0);
+        if (nchunks > 1) issue_v(1);
+    }
+    {
+        float bv, gv;
+        load_scalars(0, bv, gv);
+        if (wt < kC) { betas[wt] = bv; gss[wt] = gv; }
+    }
+    named_sync(2, kWyThreads);
+
+    for (int n = 0; n < nchunks; ++n) {
+        const int s = n & 1;
+        const uint32_t ph = (uint32_t)(n & 1);
+        const uint32_t ph2 = (uint32_t)((n >> 1) & 1);
+        const float *bet = betas + s * kC;
+        // prefetch next chunk's scalars
+        float nb = 0.f, ng = 0.f;
+        if (n + 1 < nchunks) load_scalars(n + 1, nb, ng);
+
+        wait_bar(c, B_RAW, ph);
+        if (n >= 2) wait_bar(c, B_C20 + s, (uint32_t)(((n - 2) >> 1) & 1));   // K~[s] and gamma^C[s] free
+
+        // ---------------- prologue: Gamma and the rescaled tiles
+        {
+            const int cp = wt & 63, rq = wt >> 6;
+            const int col = 2 * cp;
+            float G0[16], G1[16];
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int row = rq * 16 + r;
+                float x0 = 0.f, x1 = 0.f;
+                if (GATE == KDA_GATE_CHANNEL) {
+                    float2 gg = ld_bf16x2(base + OFF_RAWG + sw128_offset(64, row, col));
+                    x0 = gg.x; x1 = gg.y;
+                } else if (GATE == KDA_GATE_SCALAR) {
+                    x0 = x1 = gss[s * kC + row];
+                }
+                a0 += x0; a1 += x1;
+                G0[r] = a0; G1[r] = a1;
+            }
+            tot[rq * kDK + col] = a0;
+            tot[rq * kDK + col + 1] = a1;
+            named_sync(2, kWyThreads);
+            float pre0 = 0.f, pre1 = 0.f, all0 = 0.f, all1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float t0 = tot[q * kDK + col], t1 = tot[q * kDK + col + 1];
+                if (q < rq) { pre0 += t0; pre1 += t1; }
+                all0 += t0; all1 += t1;
+            }
+            if (rq == 0) {
+                gC[s * kDK + col] = __expf(all0);
+                gC[s * kDK + col + 1] = __expf(all1);
+            }
+            uint8_t *kt = base + (s ? OFF_KT1 : OFF_KT0);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int row = rq * 16 + r;
+                const float g0 = G0[r] + pre0, g1 = G1[r] + pre1;
+                const float e0v = __expf(g0), e1v = __expf(g1);
+                const float i0 = __expf(-g0), i1 = __expf(-g1);
+                const float t0 = __expf(all0 - g0), t1 = __expf(all1 - g1);
+                const uint32_t o64 = sw128_offset(64, row, col);
+                const float2 qq = ld_bf16x2(base + OFF_RAWQ + o64);
+                const float2 kk = ld_bf16x2(base + OFF_RAWK + o64);
+                const float bb = bet[row];
+                st_u32(base + OFF_AG + sw128_offset(128, row, col), pack_bf16(bb * kk.x * e0v, bb * kk.y * e1v));
+                st_u32(base + OFF_AG + sw128_offset(128, 64 + row, col), pack_bf16(qq.x * e0v, qq.y * e1v));
+                st_u32(base + OFF_KR + o64, pack_bf16(kk.x * i0, kk.y * i1));
+                st_u32(base + OFF_KL + o64, pack_bf16(kk.x * e0v, kk.y * e1v));
+                st_u32(kt + o64, pack_bf16(kk.x * t0, kk.y * t1));
+            }
+        }
+        fence_proxy_async_smem();
+        named_sync(2, kWyThreads);
+        if (leader && n + 1 < nchunks) issue_raw(n + 1);   // raw tiles consumed
+
+        // ---------------- Gram: D_G = [beta K<- ; Q<-] K->^T   (M128 N64 K128)
+        if (leader) {
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(base + OFF_AG), b0 = smem_u32(base + OFF_KR);
+            const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(c.tmem + TM_G, desc_kmajor(a0, 128, ks), desc_kmajor(b0, 64, ks), id, ks > 0);
+            mma_commit(c.bars + B_GRAM);
+        }
+        wait_bar(c, B_GRAM, ph);
+        tc_fence_after();
+
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const int row = quarter * 32 + lane;   // TMEM lane owned by this thread
+
+        if (!GLA) {
+            // ---- L (strictly lower, rows carry beta) to fp32 scratch in the K-> tile (dead now)
+            float *L = reinterpret_cast<float *>(base + OFF_KR);
+            if (quarter < 2) {
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float r16[16];
+                    tmem_ld16(c.tmem + TM_G + lane_base + half * 32 + cc * 16, r16);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = half * 32 + cc * 16 + j;
+                        L[lidx(row, col)] = col < row ? r16[j] : 0.f;
+                    }
+                }
+            }
+            named_sync(2, kWyThreads);
+
+            // ---- Y = (I + L)^{-1}, level 0: the four 16x16 diagonal blocks, one column per thread
+            if (wt < 64) {
+                const int blk = wt >> 4, cl = wt & 15, o = blk * 16;
+                float y[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float acc = (r == cl) ? 1.f : 0.f;
+#pragma unroll
+                    for (int j = 0; j < r; ++j) acc -= L[lidx(o + r, o + j)] * y[j];
+                    y[r] = acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) *yptr(base, o + r, o + cl) = y[r];
+            }
+            named_sync(2, kWyThreads);
+            // ---- level 1: Y10 = -Y11 L10 Y00 and Y32 = -Y33 L32 Y22 (block form 1 on 16x16 blocks)
+            {
+                const int which = wt >> 7;            // 0: rows 16-31 / cols 0-15, 1: rows 48-63 / cols 32-47
+                const int o = which * 32;
+                const int idx = (wt & 127) * 2;       // two outputs per thread
+                const int r = idx >> 4, cl = idx & 15;
+                float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float l = L[lidx(o + 16 + r, o + k)];
+                    m0 += l * *yptr(base, o + k, o + cl);
+                    m1 += l * *yptr(base, o + k, o + cl + 1);
+                }
+                // M goes into the (still unused) lower-left block of this 32x32 pair
+                *yptr(base, o + 16 + r, o + cl) = m0;
+                *yptr(base, o + 16 + r, o + cl + 1) = m1;
+                named_sync(2, kWyThreads);
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float yy = *yptr(base, o + 16 + r, o + 16 + k);   // Y11 / Y33, lower triangular
+                    if (k <= r) {
+                        y0 -= yy * *yptr(base, o + 16 + k, o + cl);
+                        y1 -= yy * *yptr(base, o + 16 + k, o + cl + 1);
+                    }
+                }
+                named_sync(2, kWyThreads);
+                *yptr(base, o + 16 + r, o + cl) = y0;
+                *yptr(base, o + 16 + r, o + cl + 1) = y1;
+            }
+            named_sync(2, kWyThreads);
+            // ---- level 2: Y_BL = -Y_BB L_BL Y_TT on 32x32 blocks
+            {
+                const int r = wt >> 3;                // 0..31
+                const int c0 = (wt & 7) * 4;          // 4 columns
+                float m[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    const float l = L[lidx(32 + r, k)];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (k >= c0 + q) m[q] += l * *yptr(base, k, c0 + q);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) *yptr(base, 32 + r, c0 + q) = m[q];
+                named_sync(2, kWyThreads);
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    if (k <= r) {
+                        const float yy = *yptr(base, 32 + r, 32 + k);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) y[q] -= yy * *yptr(base, 32 + k, c0 + q);
+                    }
+                }
+                named_sync(2, kWyThreads);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) *yptr(base, 32 + r, c0 + q) = y[q];
+            }
+            named_sync(2, kWyThreads);
+            // ---- T = Y Diag(beta) -> bf16 MN-major B tile at the start of A_G
+            {
+                const int i = wt >> 2, cs = (wt & 3) * 16;
+                float t[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = cs + j;
+                    t[j] = col <= i ? *yptr(base, i, col) * bet[col] : 0.f;
+                }
+                named_sync(2, kWyThreads);
+                uint8_t *tt = base + OFF_AG;
+                st_u128(tt + sw128_offset(64, i, cs), pack_bf16(t[0], t[1]), pack_bf16(t[2], t[3]),
+                        pack_bf16(t[4], t[5]), pack_bf16(t[6], t[7]));
+                st_u128(tt + sw128_offset(64, i, cs + 8), pack_bf16(t[8], t[9]), pack_bf16(t[10], t[11]),
+                        pack_bf16(t[12], t[13]), pack_bf16(t[14], t[15]));
+            }
+            named_sync(2, kWyThreads);   // L reads finished before [I;P] overwrites it
+        }
+
+        // ---- [I ; P] into the K-> tile (K-major, 128 rows x 64): for GLA this is Z itself
+        {
+            uint8_t *zp = base + OFF_KR;
+            float v[32];
+            if (quarter < 2) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = (half * 32 + j == row) ? 1.f : 0.f;
+            } else {
+                const int i = row - 64;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float r16[16];
+                    tmem_ld16(c.tmem + TM_G + lane_base + half * 32 + cc * 16, r16);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[cc * 16 + j] = (half * 32 + cc * 16 + j <= i) ? r16[j] : 0.f;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_u128(zp + sw128_offset(128, row, half * 32 + q * 8), pack_bf16(v[8 * q], v[8 * q + 1]),
+                        pack_bf16(v[8 * q + 2], v[8 * q + 3]), pack_bf16(v[8 * q + 4], v[8 * q + 5]),
+                        pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(2, kWyThreads);
+
+        if (!GLA) {
+            // ---------------- Z = [I ; P] T   (M128 N64 K64)
+            if (leader) {
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(base + OFF_KR), b0 = smem_u32(base + OFF_AG);
+                const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(c.tmem + TM_Z, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
+                mma_commit(c.bars + B_Z);
+            }
+            wait_bar(c, B_Z, ph);
+            tc_fence_after();
+            {
+                uint8_t *zp = base + OFF_KR;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float r16[16];
+                    tmem_ld16(c.tmem + TM_Z + lane_base + half * 32 + cc * 16, r16);
+                    const int col = half * 32 + cc * 16;
+                    st_u128(zp + sw128_offset(128, row, col), pack_bf16(r16[0], r16[1]), pack_bf16(r16[2], r16[3]),
+                            pack_bf16(r16[4], r16[5]), pack_bf16(r16[6], r16[7]));
+                    st_u128(zp + sw128_offset(128, row, col + 8), pack_bf16(r16[8], r16[9]),
+                            pack_bf16(r16[10], r16[11]), pack_bf16(r16[12], r16[13]), pack_bf16(r16[14], r16[15]));
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(2, kWyThreads);
+        }
+
+        // ---------------- Z K<- -> [W ; P W],  Z V -> D1[s] = [U ; P U]
+        if (leader) {
+            wait_bar(c, B_V0 + s, ph2);
+            if (n >= 2) wait_bar(c, B_E10 + s, (uint32_t)(((n - 2) >> 1) & 1));   // D1[s] drained
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(base + OFF_KR);
+            if (!GLA) {
+                const uint32_t bk = smem_u32(base + OFF_KL);
+                const uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(c.tmem + TM_WQ, desc_kmajor(a0, 128, ks), desc_mnmajor(bk, 64, ks), id, ks > 0);
+            }
+            const uint32_t bv = smem_u32(base + (s ? OFF_V1 : OFF_V0));
+            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(c.tmem + TM_D1 + s * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(bv, 64, ks), id, ks > 0);
+            mma_commit(c.bars + B_W2);
+        }
+        wait_bar(c, B_W2, ph);
+        tc_fence_after();
+        if (leader && n + 2 < nchunks) issue_v(n + 2);           // v[s] consumed
+        if (n >= 1) wait_bar(c, B_C10 + ((n - 1) & 1), (uint32_t)(((n - 1) >> 1) & 1));   // A_chain free
+
+        // ---------------- A_chain = [-W ; Q<- - P W]  (K-major 128 x 128)
+        {
+            uint8_t *ach = base + OFF_ACH;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col = half * 64 + cc * 16;
+                float r16[16];
+                if (!GLA) {
+                    tmem_ld16(c.tmem + TM_WQ + lane_base + col, r16);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r16[j] = 0.f;
+                }
+                float o16[16];
+                if (quarter < 2) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o16[j] = -r16[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 qq = ld_bf16x2(base + OFF_AG + sw128_offset(128, row, col + j));
+                        o16[j] = qq.x - r16[j];
+                        o16[j + 1] = qq.y - r16[j + 1];
+                    }
+                }
+                st_u128(ach + sw128_offset(128, row, col), pack_bf16(o16[0], o16[1]), pack_bf16(o16[2], o16[3]),
+                        pack_bf16(o16[4], o16[5]), pack_bf16(o16[6], o16[7]));
+                st_u128(ach + sw128_offset(128, row, col + 8), pack_bf16(o16[8], o16[9]),
+                        pack_bf16(o16[10], o16[11]), pack_bf16(o16[12], o16[13]), pack_bf16(o16[14], o16[15]));
+            }
+        }
+        if (wt < kC && n + 1 < nchunks) {
+            betas[(s ^ 1) * kC + wt] = nb;
+            gss[(s ^ 1) * kC + wt] = ng;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(2, kWyThreads);
+        if (leader) mbar_arrive(c.bars + B_WYR0 + s);
+    }
+    // drain: every MMA this thread issued has completed before TMEM is freed
+    if (leader) {
+        mma_commit(c.bars + B_FIN1);
+        wait_bar(c, B_FIN1, 0);
+    }
+}
+
+// ============================================================================
+// Chain warps: the serial state scan and the output.
+// ============================================================================
+__device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_o, int e0, int h, int b,
+                           int nchunks) {
+    uint8_t *base = c.base;
+    const int j = threadIdx.x;                  // key channel == TMEM lane
+    const int warp = j >> 5;
+    const bool leader = j == 0;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float *gC = reinterpret_cast<const float *>(base + OFF_MISC + MISC_GC);
+    const int H = p.H, dv = p.dv;
+
+    float S[kDVS];
+#pragma unroll
+    for (int e = 0; e < kDVS; ++e)
+        S[e] = p.h0 ? p.h0[(((size_t)b * H + h) * dv + e0 + e) * kDK + j] : 0.f;
+
+    auto write_state = [&]() {
+        uint8_t *st = base + OFF_ST;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            st_u128(st + sw128_offset(128, j, q * 8), pack_bf16(S[8 * q], S[8 * q + 1]),
+                    pack_bf16(S[8 * q + 2], S[8 * q + 3]), pack_bf16(S[8 * q + 4], S[8 * q + 5]),
+                    pack_bf16(S[8 * q + 6], S[8 * q + 7]));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(1, kChainThreads);
+    };
+    write_state();
+
+    for (int n = 0; n < nchunks; ++n) {
+        const int s = n & 1;
+        const uint32_t ph2 = (uint32_t)((n >> 1) & 1);
+        wait_bar(c, B_WYR0 + s, ph2);
+        tc_fence_after();
+        const float gam = gC[s * kDK + j];
+
+        // ---- D1[s] += [-W ; Q'] S^T   (M128 N64 K128)
+        if (leader) {
+            const uint32_t a0 = smem_u32(base + OFF_ACH), b0 = smem_u32(base + OFF_ST);
+            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(c.tmem + TM_D1 + s * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 128, ks), id, 1);
+            mma_commit(c.bars + B_C10 + s);
+        }
+        wait_bar(c, B_C10 + s, ph2);
+        tc_fence_after();
+
+        // ---- rows 0-63: V_new -> bf16 MN-major B tile; rows 64-127: O -> staging tile
+        {
+            uint8_t *dst = base + OFF_ST + (warp < 2 ? 0u : 8192u);
+            const int r = (warp & 1) * 32 + (j & 31);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float r16[16];
+                tmem_ld16(c.tmem + TM_D1 + s * 64 + lane_base + cc * 16, r16);
+                st_u128(dst + sw128_offset(64, r, cc * 16), pack_bf16(r16[0], r16[1]), pack_bf16(r16[2], r16[3]),
+                        pack_bf16(r16[4], r16[5]), pack_bf16(r16[6], r16[7]));
+                st_u128(dst + sw128_offset(64, r, cc * 16 + 8), pack_bf16(r16[8], r16[9]),
+                        pack_bf16(r16[10], r16[11]), pack_bf16(r16[12], r16[13]), pack_bf16(r16[14], r16[15]));
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(1, kChainThreads);
+
+        if (leader) {
+            tc_fence_after();
+            mbar_arrive(c.bars + B_E10 + s);                        // D1[s] drained
+            tma_store_4d(tm_o, base + OFF_ST + 8192, e0, h, n * kC, b);
+            tma_store_commit();
+            // ---- dS^T = K~^T V_new   (M128 N64 K64)
+            const uint32_t a0 = smem_u32(base + (s ? OFF_KT1 : OFF_KT0)), b0 = smem_u32(base + OFF_ST);
+            const uint32_t id = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(c.tmem + TM_S, desc_mnmajor(a0, 64, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
+            mma_commit(c.bars + B_C20 + s);
+        }
+        wait_bar(c, B_C20 + s, ph2);
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            float r16[16];
+            tmem_ld16(c.tmem + TM_S + lane_base + cc * 16, r16);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) S[cc * 16 + e] = fmaf(gam, S[cc * 16 + e], r16[e]);
+        }
+        if (leader) tma_store_wait_read0();
+        named_sync(1, kChainThreads);    // the staged O tile has been read
+        write_state();
+    }
+    if (p.ht) {
+#pragma unroll
+        for (int e = 0; e < kDVS; ++e) p.ht[(((size_t)b * H + h) * dv + e0 + e) * kDK + j] = S[e];
+    }
+    if (leader) {
+        tma_store_wait_all0();
+        mma_commit(c.bars + B_FIN0);
+        wait_bar(c, B_FIN0, 0);
+    }
+}
+
+template <int GATE, bool GLA, typename Tg>
+__global__ void __launch_bounds__(kThreads, 1)
+kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctx c;
+    c.base = base;
+    c.bars = reinterpret_cast<uint64_t *>(base + OFF_MISC + MISC_BAR);
+    c.abort = reinterpret_cast<volatile int *>(base + OFF_MISC + MISC_ABORT);
+    c.status = p.status;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + OFF_MISC + MISC_TSLOT);
+
+    const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
+    const int nchunks = (p.T + kC - 1) / kC;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNumBars; ++i) mbar_init(c.bars + i, 1);
+        *c.abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(tslot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    c.tmem = *tslot;
+
+    if (threadIdx.x < kChainThreads)
+        chain_role(c, p, &tm_o, e0, h, b, nchunks);
+    else
+        wy_role<GATE, GLA, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, b, nchunks);
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x < 32) tmem_dealloc(c.tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// [B, T, H, D] tensor as a 4-D map (D, H, T, B) with 64 x 1 x 64 x 1 boxes, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t es, int B, int T, int H, int D) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es, (cuuint64_t)T * H * D * es};
+    cuuint32_t box[4] = {64, 1, 64, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int GATE, bool GLA, typename Tg>
+cudaError_t launch_variant(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
+                           const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
+    auto kern = kda_fwd_tc_kernel<GATE, GLA, Tg>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.dv / kDVS, p.H, p.B);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(p, q, k, g, v, o);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc_bf16(const FwdParams &p, int g_is_bf16, cudaStream_t s) {
+    if (p.dk != kDK || p.dv % kDVS != 0) return cudaErrorNotSupported;
+    const bool gla = !p.scale_v;
+    if (gla && p.has_beta) return cudaErrorNotSupported;     // unscaled v with a delta term: DPLR entry
+    if (p.gate_kind == KDA_GATE_CHANNEL && !g_is_bf16) return cudaErrorNotSupported;
+    CUtensorMap mq, mk, mg, mv, mo;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map(&mq, p.q, bf, 2, p.B, p.T, p.H, p.dk) || !make_map(&mk, p.k, bf, 2, p.B, p.T, p.H, p.dk) ||
+        !make_map(&mv, p.v, bf, 2, p.B, p.T, p.H, p.dv) || !make_map(&mo, p.o, bf, 2, p.B, p.T, p.H, p.dv))
+        return cudaErrorInvalidValue;
+    mg = mq;
+    if (p.gate_kind == KDA_GATE_CHANNEL && !make_map(&mg, p.g, bf, 2, p.B, p.T, p.H, p.dk))
+        return cudaErrorInvalidValue;
+    if (p.gate_kind == KDA_GATE_CHANNEL) {
+        return gla ? launch_variant<KDA_GATE_CHANNEL, true, __nv_bfloat16>(p, mq, mk, mg, mv, mo, s)
+                   : launch_variant<KDA_GATE_CHANNEL, false, __nv_bfloat16>(p, mq, mk, mg, mv, mo, s);
+    }
+    if (p.gate_kind == KDA_GATE_SCALAR) {
+        if (gla) return cudaErrorNotSupported;
+        return g_is_bf16 ? launch_variant<KDA_GATE_SCALAR, false, __nv_bfloat16>(p, mq, mk, mg, mv, mo, s)
+                         : launch_variant<KDA_GATE_SCALAR, false, float>(p, mq, mk, mg, mv, mo, s);
+    }
+    if (gla) return cudaErrorNotSupported;
+    return launch_variant<KDA_GATE_NONE, false, __nv_bfloat16>(p, mq, mk, mg, mv, mo, s);
+}
+
+}  // namespace kda

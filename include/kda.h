@@ -1,0 +1,116 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) chunkwise gated delta-rule library.
+ *
+ * Recurrence (page "Diagonal Plus Low Rank", section 2, opening equation):
+ *
+ *     S_t = S_{t-1} Diag(alpha_t) (I - b_t a_t^T) + v_t k_t^T,   o_t = S_t q_t,
+ *     S in R^{dv x dk},  alpha_t = exp(g_t),  S_{-1} = h0 (0 when absent).
+ *
+ * kda_chunk_fwd evaluates the KDA specialisation a = k, b = beta k with beta
+ * scaling v (same page, "relation to KDA"; page "How to make GDN2 more
+ * stable", eq. (1)) by the chunkwise form recapped on page "Kimi Delta
+ * Attention backward" ("forward recap"):
+ *
+ *     Gamma = exp(in-chunk cumsum g),  Q<- = Q*Gamma, K<- = K*Gamma, K-> = K/Gamma,
+ *     A~ = (I + Diag(beta)(K<- K->^T * M_{-1}))^{-1},
+ *     W = A~ Diag(beta) K<-,  U = A~ Diag(beta) V,
+ *     V_new = U - W S^T,  O = Q<- S^T + (Q<- K->^T * M) V_new,
+ *     S <- S Diag(gamma^C) + V_new^T K-> Diag(gamma^C).
+ *
+ * The same call covers GDN (gate_kind = KDA_GATE_SCALAR), DeltaNet
+ * (gate_kind = KDA_GATE_NONE) and GLA (beta = NULL and the flag
+ * KDA_FLAG_BETA_SCALES_V cleared, so S_t = S_{t-1} Diag(alpha_t) + v_t k_t^T;
+ * page "Gated Linear Attention", section 5.1).
+ *
+ * Conventions
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates or frees device memory.
+ *   - Sequence tensors are contiguous [B, T, H, d] (d fastest); the state
+ *     tensors h0 / ht are contiguous [B, H, dv, dk] float32 (row = value
+ *     channel, column = key channel).  Device pointers must be 16-byte
+ *     aligned.
+ *   - Calls are asynchronous on the given stream.  Argument errors are
+ *     detected on the host before anything is launched and nothing is
+ *     written; the return value says which.  Errors found on the device
+ *     (a bounded wait that ran out) are recorded in the first word of the
+ *     workspace and read back with kda_status_read.
+ *   - Outputs must not alias inputs.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kda_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misalignment, bad enum */
+    KDA_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. dk = 96) */
+    KDA_ERR_WORKSPACE = -3,    /* workspace missing or smaller than the query */
+    KDA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
+    KDA_ERR_TIMEOUT = -5       /* a device-side bounded wait gave up */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+typedef enum {
+    KDA_GATE_NONE = 0,     /* alpha = 1 (DeltaNet); g must be NULL */
+    KDA_GATE_SCALAR = 1,   /* g [B, T, H]: one log-decay per token and head (GDN) */
+    KDA_GATE_CHANNEL = 2   /* g [B, T, H, dk]: per-channel log-decay (KDA, GLA) */
+} kda_gate;
+
+/* beta scales v (KDA, GDN, DeltaNet).  Cleared: v enters unscaled (GLA). */
+#define KDA_FLAG_BETA_SCALES_V 1u
+
+typedef struct {
+    int B, T, H;           /* batch, sequence length (any T >= 1), heads */
+    int dk, dv;            /* key / value head dims: 64 or 128 each */
+    int chunk;             /* chunk length C; 64 (0 selects 64) */
+    kda_dtype dtype;       /* dtype of q, k, v, beta and o */
+    kda_gate gate_kind;
+    kda_dtype g_dtype;     /* dtype of g (log-decay, g <= 0 expected) */
+    unsigned flags;        /* KDA_FLAG_* */
+    const void *q;         /* [B, T, H, dk] */
+    const void *k;         /* [B, T, H, dk] */
+    const void *v;         /* [B, T, H, dv] */
+    const void *g;         /* see kda_gate; NULL iff gate_kind == KDA_GATE_NONE */
+    const void *beta;      /* [B, T, H] in dtype; NULL means beta = 0 */
+    const float *h0;       /* [B, H, dv, dk] initial state, or NULL (zero) */
+    void *o;               /* [B, T, H, dv] output, dtype */
+    float *ht;             /* [B, H, dv, dk] final state, or NULL (not written) */
+    void *workspace;       /* device buffer, zero-filled before its first use */
+    size_t workspace_bytes;
+} kda_fwd_args;
+
+/* Bytes of workspace kda_chunk_fwd needs for these arguments (0 on bad args). */
+size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
+
+/*
+ * Chunkwise forward of the gated delta rule (KDA and its special cases).
+ * Writes o, and ht when non-NULL.  float32 inputs run a float32 CUDA-core
+ * kernel; bfloat16 inputs run the tcgen05 tensor-core kernel (bf16 operands,
+ * fp32 accumulation, fp32 state).
+ */
+kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
+
+/*
+ * Reads the device status word that kernels set on a device-side error,
+ * waits for the stream, clears the word and returns the code (KDA_OK when
+ * no error was recorded).
+ */
+kda_status kda_status_read(void *workspace, kda_stream_t stream);
+
+/* Static English text for a status code. */
+const char *kda_status_string(kda_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

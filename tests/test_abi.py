@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads,
+exports every symbol include/kda.h declares, and rejects bad arguments before
+anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunkwise_gated_delta_gb300 import _lib
+from chunkwise_gated_delta_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", src))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert declared == set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.kda_status_string(code)
+    assert _lib.status_string(_lib.KDA_ERR_TIMEOUT) == "device-side wait timed out"
+
+
+def _args(**over):
+    a = _lib.KdaFwdArgs()
+    a.B, a.T, a.H, a.dk, a.dv, a.chunk = 2, 100, 4, 128, 128, 64
+    a.dtype, a.gate_kind, a.g_dtype, a.flags = _lib.KDA_BF16, _lib.KDA_GATE_CHANNEL, _lib.KDA_BF16, 1
+    base = 1 << 40          # fake, well-separated 16-byte aligned device addresses (never dereferenced)
+    for i, f in enumerate(("q", "k", "v", "g", "beta", "h0", "o", "ht", "workspace")):
+        setattr(a, f, base + i * (1 << 32))
+    a.workspace_bytes = 256
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def _call(lib, a):
+    return lib.kda_chunk_fwd(ctypes.byref(a), None)
+
+
+def test_workspace_query(lib):
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args())) >= 4
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(dk=96))) == 0
+    assert lib.kda_chunk_fwd_workspace(None) == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(o=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(B=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(T=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(H=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dtype=7), _lib.KDA_ERR_INVALID_ARG),
+    (dict(gate_kind=9), _lib.KDA_ERR_INVALID_ARG),
+    (dict(gate_kind=_lib.KDA_GATE_NONE), _lib.KDA_ERR_INVALID_ARG),      # g given with no gate
+    (dict(g=None), _lib.KDA_ERR_INVALID_ARG),                            # gate without g
+    (dict(flags=6), _lib.KDA_ERR_INVALID_ARG),
+    (dict(q=(1 << 40) + 8), _lib.KDA_ERR_INVALID_ARG),                   # misaligned
+    (dict(o=(1 << 40) + 1 * (1 << 32)), _lib.KDA_ERR_INVALID_ARG),       # o aliases k
+    (dict(dk=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dv=32), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=32), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(workspace=None, workspace_bytes=0), _lib.KDA_ERR_WORKSPACE),
+    (dict(workspace_bytes=16), _lib.KDA_ERR_WORKSPACE),
+])
+def test_rejects_bad_arguments_before_launch(lib, over, code):
+    assert _call(lib, _args(**over)) == code
+
+
+def test_null_args_pointer(lib):
+    assert lib.kda_chunk_fwd(None, None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_status_read(None, None) == _lib.KDA_ERR_INVALID_ARG

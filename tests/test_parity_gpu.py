@@ -1,0 +1,161 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI.
+
+Tolerances (relative Frobenius norm, on o and on the final state):
+  * float32 inputs: 1e-5  (CUDA-core fp32 kernel)
+  * bfloat16 inputs, fp32 accumulation: 5e-3  (tcgen05 kernel)
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunkwise_gated_delta_gb300 import kda_chunk_fwd
+from chunkwise_gated_delta_gb300.inputs import WORKLOADS, custom, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 5e-3}
+DEV = "cuda:0"
+
+
+def rel(x, ref):
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def f64(t):
+    return None if t is None else t.double().numpy()
+
+
+def run_gpu(x, variant):
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    gate = {"kda": "channel", "gla": "channel", "gdn": "scalar", "deltanet": "none"}[variant]
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"),
+                          gate=gate, scale_v=x["scale_v"])
+    torch.cuda.synchronize()
+    return o.double().cpu().numpy(), ht.double().cpu().numpy()
+
+
+def run_oracle(x, variant, heads=None):
+    args = dict(h0=f64(x.get("h0")), heads=heads)
+    q, k, v = f64(x["q"]), f64(x["k"]), f64(x["v"])
+    if variant == "kda":
+        return oracle.kda_fwd(q, k, v, f64(x["g"]), f64(x["beta"]), **args)
+    if variant == "gdn":
+        return oracle.gdn_fwd(q, k, v, f64(x["g"]), f64(x["beta"]), **args)
+    if variant == "deltanet":
+        return oracle.deltanet_fwd(q, k, v, f64(x["beta"]), **args)
+    if variant == "gla":
+        return oracle.gla_fwd(q, k, v, f64(x["g"]), **args)
+    raise ValueError(variant)
+
+
+def check(variant, dtype, B, T, H, dk, dv, h0, seed=0):
+    w = custom(variant, B, T, H, dk, dv, dtype=dtype, h0=h0)
+    x = make_inputs(w, seed=seed)
+    o, ht = run_gpu(x, variant)
+    ro, rh = run_oracle(x, variant)
+    eo, eh = rel(o, ro), rel(ht, rh)
+    assert eo <= TOL[dtype] and eh <= TOL[dtype], f"o {eo:.3e} ht {eh:.3e}"
+    return eo, eh
+
+
+# ---------------------------------------------------------------- fp32 path
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 256])
+def test_fp32_kda_lengths(T):
+    check("kda", torch.float32, 1, T, 2, 64, 64, h0=True)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_fp32_kda_dims(dk, dv):
+    check("kda", torch.float32, 2, 100, 2, dk, dv, h0=True)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "gla"])
+def test_fp32_special_cases(variant):
+    check(variant, torch.float32, 1, 150, 2, 64, 64, h0=True)
+
+
+def test_fp32_workload_small():
+    """The fp32 KDA workload: B1 T256 H1 d64, no initial state."""
+    w = WORKLOADS["kda_fp32_b1t256h1d64"]
+    x = make_inputs(w, seed=0)
+    o, ht = run_gpu(x, "kda")
+    ro, rh = run_oracle(x, "kda")
+    assert rel(o, ro) <= 1e-5 and rel(ht, rh) <= 1e-5
+
+
+# ---------------------------------------------------------------- bf16 tensor-core path
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 200, 512])
+def test_bf16_kda_lengths(T):
+    check("kda", torch.bfloat16, 1, T, 2, 128, 128, h0=True)
+
+
+@pytest.mark.parametrize("dv", [64, 128])
+def test_bf16_kda_value_dims(dv):
+    check("kda", torch.bfloat16, 2, 130, 2, 128, dv, h0=True)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "gla"])
+def test_bf16_special_cases(variant):
+    check(variant, torch.bfloat16, 2, 300, 3, 128, 128, h0=True)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_bf16_kda_seeds(seed):
+    check("kda", torch.bfloat16, 2, 700, 2, 128, 128, h0=True, seed=seed)
+
+
+def test_bf16_no_h0_no_ht():
+    w = custom("kda", 1, 150, 2, 128, 128, dtype=torch.bfloat16, h0=False)
+    x = make_inputs(w, seed=3)
+    d = {k: v.to(DEV) for k, v in x.items() if isinstance(v, torch.Tensor)}
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], output_final_state=False)
+    torch.cuda.synchronize()
+    assert ht is None
+    ro, _ = run_oracle(x, "kda")
+    assert rel(o.double().cpu().numpy(), ro) <= 5e-3
+
+
+def test_bf16_chaining_matches_one_call():
+    """h0 -> ht chaining: two calls over halves equal one call (the state is the resume point)."""
+    w = custom("kda", 1, 512, 2, 128, 128, dtype=torch.bfloat16, h0=True)
+    x = make_inputs(w, seed=4)
+    d = {k: v.to(DEV) for k, v in x.items() if isinstance(v, torch.Tensor)}
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    sl = lambda t, a, b: t[:, a:b].contiguous()
+    o1, h1 = kda_chunk_fwd(*(sl(d[n], 0, 256) for n in ("q", "k", "v", "g", "beta")), d["h0"])
+    o2, h2 = kda_chunk_fwd(*(sl(d[n], 256, 512) for n in ("q", "k", "v", "g", "beta")), h1)
+    torch.cuda.synchronize()
+    ro, rh = run_oracle(x, "kda")
+    oc = torch.cat([o1, o2], 1).double().cpu().numpy()
+    assert rel(oc, ro) <= 5e-3 and rel(h2.double().cpu().numpy(), rh) <= 5e-3
+
+
+def test_bf16_deterministic():
+    w = custom("kda", 2, 300, 2, 128, 128, dtype=torch.bfloat16, h0=True)
+    x = make_inputs(w, seed=5)
+    a = run_gpu(x, "kda")
+    b = run_gpu(x, "kda")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled heads
+def _full(name, heads):
+    w = WORKLOADS[name]
+    x = make_inputs(w, seed=0)
+    o, ht = run_gpu(x, w.variant)
+    ro, rh = run_oracle(x, w.variant, heads=heads)
+    for (b, h) in heads:
+        eo, eh = rel(o[b, :, h], ro[b, :, h]), rel(ht[b, h], rh[b, h])
+        assert eo <= 5e-3 and eh <= 5e-3, f"{name} head {(b, h)}: o {eo:.3e} ht {eh:.3e}"
+    assert np.isfinite(o).all() and np.isfinite(ht).all()
+
+
+def test_full_kda_b4t4096h16d128_sampled_heads():
+    _full("kda_bf16_b4t4096h16d128", [(0, 0), (1, 7), (3, 15)])
+
+
+@pytest.mark.parametrize("name", ["gdn_bf16_b8t2048h32d128", "deltanet_bf16_b8t2048h32d128",
+                                  "gla_bf16_b8t2048h32d128"])
+def test_full_special_cases_sampled_heads(name):
+    _full(name, [(0, 0), (7, 31)])
