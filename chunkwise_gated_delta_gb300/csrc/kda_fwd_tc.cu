@@ -57,14 +57,23 @@ constexpr uint32_t OFF_KT0 = 163840;     // K~ 64 x 128 (MN-major A), slot 0
 constexpr uint32_t OFF_KT1 = 180224;     // slot 1
 constexpr uint32_t OFF_ST = 196608;      // S^T 128 x 64 bf16 (MN-major B); V_new / O staging
 constexpr uint32_t OFF_MISC = 212992;
-constexpr uint32_t MISC_GC = 0;          // gamma^C [2][128] f32
-constexpr uint32_t MISC_BETA = 1024;     // beta [2][64] f32
-constexpr uint32_t MISC_GS = 1536;       // scalar gate [2][64] f32
-constexpr uint32_t MISC_TOT = 2048;      // cumsum partials [4][128] f32
-constexpr uint32_t MISC_BAR = 4096;      // mbarriers
-constexpr uint32_t MISC_TSLOT = 4352;    // TMEM base address
-constexpr uint32_t MISC_ABORT = 4356;    // abort flag
-constexpr uint32_t kSmemBytes = OFF_MISC + 4608 + 1024;
+constexpr uint32_t MISC_GC = 0;          // gamma^C [2][128] f32            (1024 B)
+constexpr uint32_t MISC_BETA = 1024;     // beta [2][64] f32                 (512 B)
+constexpr uint32_t MISC_GS = 1536;       // scalar gate [2][64] f32          (512 B)
+constexpr uint32_t MISC_TOT = 2048;      // cumsum partials [8][128] f32     (4096 B)
+constexpr uint32_t MISC_BAR = 6144;      // mbarriers [16] u64               (128 B)
+constexpr uint32_t MISC_TSLOT = 6400;    // TMEM base address
+constexpr uint32_t MISC_ABORT = 6404;    // abort flag
+constexpr uint32_t kMiscBytes = 7168;
+constexpr uint32_t kSmemBytes = OFF_MISC + kMiscBytes + 1024;   // + alignment slack of the dynamic base
+static_assert(MISC_GC + 2 * 128 * 4 <= MISC_BETA, "misc layout");
+static_assert(MISC_BETA + 2 * 64 * 4 <= MISC_GS, "misc layout");
+static_assert(MISC_GS + 2 * 64 * 4 <= MISC_TOT, "misc layout");
+static_assert(MISC_TOT + 8 * 128 * 4 <= MISC_BAR, "misc layout");
+static_assert(MISC_BAR + 16 * 8 <= MISC_TSLOT, "misc layout");
+static_assert(MISC_ABORT + 4 <= kMiscBytes, "misc layout");
+static_assert(OFF_ST + 16384 <= OFF_MISC, "tile layout");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // ---- TMEM columns
 constexpr uint32_t TM_G = 0;      // Gram [L ; P], 64 cols
@@ -79,6 +88,7 @@ enum {
     B_RAW = 0, B_V0, B_V1, B_GRAM, B_Z, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
     B_FIN0, B_FIN1, kNumBars
 };
+static_assert(kNumBars <= 16, "mbarrier slots");
 
 struct Ctx {
     uint8_t *base;
@@ -116,17 +126,6 @@ __device__ __forceinline__ void st_u128(uint8_t *p, uint32_t a, uint32_t b, uint
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
 
-// fp32 [64][64] scratch with an XOR swizzle on the low 5 column bits: row and
-// column walks across a warp both hit 32 distinct banks.
-__device__ __forceinline__ uint32_t lidx(uint32_t i, uint32_t j) { return i * 64u + (j ^ (i & 31u)); }
-
-// Y (the inverse) lives in the dead beta K<- rows of the A_G tile, which are
-// two 8 KB pieces: rows 0-31 at +0, rows 32-63 at +16 KB.
-__device__ __forceinline__ float *yptr(uint8_t *base, uint32_t i, uint32_t j) {
-    float *y = reinterpret_cast<float *>(base + OFF_AG + (i >= 32 ? 16384u : 0u));
-    return y + lidx(i & 31u, j);
-}
-
 template <typename T> __device__ __forceinline__ float ldg_f(const T *p);
 template <> __device__ __forceinline__ float ldg_f<__nv_bfloat16>(const __nv_bfloat16 *p) {
     return __bfloat162float(*p);
@@ -136,11 +135,86 @@ template <> __device__ __forceinline__ float ldg_f<float>(const float *p) { retu
 // ============================================================================
 // WY warps: everything of chunk n that does not depend on the state.
 // ============================================================================
+
+// fp32 [64][64] scratch with an XOR swizzle on column bits 2-4: float4 groups
+// stay contiguous, and row walks (lanes over rows) spread over the banks.
+__device__ __forceinline__ uint32_t sidx(uint32_t i, uint32_t j) { return i * 64u + (j ^ ((i & 7u) << 2)); }
+
+struct Scratch {
+    uint8_t *base;
+    __device__ __forceinline__ float *L(uint32_t i, uint32_t j) const {
+        return reinterpret_cast<float *>(base + OFF_KR) + sidx(i, j);
+    }
+    // Y lives in the dead beta K<- rows of the A_G tile: rows 0-31 at +0, rows 32-63 at +16 KB.
+    __device__ __forceinline__ float *Y(uint32_t i, uint32_t j) const {
+        return reinterpret_cast<float *>(base + OFF_AG + (i >= 32 ? 16384u : 0u)) + sidx(i & 31u, j);
+    }
+};
+
+// acc (16x16 as two 16x8 halves) += X[rx:rx+16, cx:cx+16] * Z[rz:rz+16, cz:cz+16], tf32 tensor cores.
+template <bool XL, bool ZL>
+__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const Scratch &sc, int rx, int cx, int rz, int cz,
+                                        int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    auto X = [&](int i, int j) { return XL ? *sc.L(i, j) : *sc.Y(i, j); };
+    auto Z = [&](int i, int j) { return ZL ? *sc.L(i, j) : *sc.Y(i, j); };
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t a[4] = {to_tf32(X(rx + g, cx + 8 * ks + t)), to_tf32(X(rx + g + 8, cx + 8 * ks + t)),
+                               to_tf32(X(rx + g, cx + 8 * ks + t + 4)), to_tf32(X(rx + g + 8, cx + 8 * ks + t + 4))};
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+            const uint32_t bb[2] = {to_tf32(Z(rz + 8 * ks + t, cz + 8 * nh + g)),
+                                    to_tf32(Z(rz + 8 * ks + t + 4, cz + 8 * nh + g))};
+            mma_tf32_16x8x8(acc[nh], a, bb);
+        }
+    }
+}
+__device__ __forceinline__ void blk_store_y(const float (&acc)[2][4], const Scratch &sc, int r0, int c0, float sign,
+                                            int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nh = 0; nh < 2; ++nh) {
+        *sc.Y(r0 + g, c0 + 8 * nh + 2 * t) = sign * acc[nh][0];
+        *sc.Y(r0 + g, c0 + 8 * nh + 2 * t + 1) = sign * acc[nh][1];
+        *sc.Y(r0 + g + 8, c0 + 8 * nh + 2 * t) = sign * acc[nh][2];
+        *sc.Y(r0 + g + 8, c0 + 8 * nh + 2 * t + 1) = sign * acc[nh][3];
+    }
+}
+__device__ __forceinline__ void zero_acc(float (&acc)[2][4]) {
+#pragma unroll
+    for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nh][e] = 0.f;
+}
+
+__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
+    return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
+}
+__device__ __forceinline__ float4 ld_bf16x4(const uint8_t *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ void st_u64(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
+
+// 32 fp32 values -> 64 bytes of bf16 at (row, col .. col+31) of a SW128 tile with `rows` rows.
+__device__ __forceinline__ void store_row32_bf16(uint8_t *tile, uint32_t rows, uint32_t row, uint32_t col,
+                                                 const float *v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        st_u128(tile + sw128_offset(rows, row, col + 8 * q), pack_bf16(v[8 * q], v[8 * q + 1]),
+                pack_bf16(v[8 * q + 2], v[8 * q + 3]), pack_bf16(v[8 * q + 4], v[8 * q + 5]),
+                pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
 template <int GATE, bool GLA, typename Tg>
 __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                         const CUtensorMap *tm_g, const CUtensorMap *tm_v, int e0, int h, int b, int nchunks) {
     uint8_t *base = c.base;
     const int wt = threadIdx.x - kChainThreads;          // 0..255
+    const int ww = wt >> 5;                              // WY warp 0..7
     const int warp = threadIdx.x >> 5;                   // 4..11
     const int lane = threadIdx.x & 31;
     const int quarter = warp & 3;                        // TMEM lane quarter
@@ -154,6 +228,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     const __nv_bfloat16 *betag = static_cast<const __nv_bfloat16 *>(p.beta);
     const Tg *gsg = static_cast<const Tg *>(p.g);
     const uint32_t raw_bytes = (GATE == KDA_GATE_CHANNEL ? 3u : 2u) * 16384u;
+    const Scratch sc{base};
 
     auto issue_raw = [&](int n) {
         mbar_arrive_expect_tx(c.bars + B_RAW, raw_bytes);
@@ -197,63 +272,72 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         const uint32_t ph = (uint32_t)(n & 1);
         const uint32_t ph2 = (uint32_t)((n >> 1) & 1);
         const float *bet = betas + s * kC;
-        // prefetch next chunk's scalars
         float nb = 0.f, ng = 0.f;
-        if (n + 1 < nchunks) load_scalars(n + 1, nb, ng);
+        if (n + 1 < nchunks) load_scalars(n + 1, nb, ng);   // prefetch next chunk's scalars
 
         wait_bar(c, B_RAW, ph);
         if (n >= 2) wait_bar(c, B_C20 + s, (uint32_t)(((n - 2) >> 1) & 1));   // K~[s] and gamma^C[s] free
 
-        // ---------------- prologue: Gamma and the rescaled tiles
+        // ---------------- prologue: Gamma and the rescaled tiles; 4 columns x 8 rows per thread
         {
-            const int cp = wt & 63, rq = wt >> 6;
-            const int col = 2 * cp;
-            float G0[16], G1[16];
-            float a0 = 0.f, a1 = 0.f;
+            const int cg = wt & 31, rg = wt >> 5;
+            const int col = 4 * cg;
+            float G[8][4];
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int row = rq * 16 + r;
-                float x0 = 0.f, x1 = 0.f;
+            for (int r = 0; r < 8; ++r) {
+                const int row = rg * 8 + r;
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
                 if (GATE == KDA_GATE_CHANNEL) {
-                    float2 gg = ld_bf16x2(base + OFF_RAWG + sw128_offset(64, row, col));
-                    x0 = gg.x; x1 = gg.y;
+                    const float4 gg = ld_bf16x4(base + OFF_RAWG + sw128_offset(64, row, col));
+                    x[0] = gg.x; x[1] = gg.y; x[2] = gg.z; x[3] = gg.w;
                 } else if (GATE == KDA_GATE_SCALAR) {
-                    x0 = x1 = gss[s * kC + row];
+                    x[0] = x[1] = x[2] = x[3] = gss[s * kC + row];
                 }
-                a0 += x0; a1 += x1;
-                G0[r] = a0; G1[r] = a1;
-            }
-            tot[rq * kDK + col] = a0;
-            tot[rq * kDK + col + 1] = a1;
-            named_sync(2, kWyThreads);
-            float pre0 = 0.f, pre1 = 0.f, all0 = 0.f, all1 = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float t0 = tot[q * kDK + col], t1 = tot[q * kDK + col + 1];
-                if (q < rq) { pre0 += t0; pre1 += t1; }
-                all0 += t0; all1 += t1;
+                for (int e = 0; e < 4; ++e) { a[e] += x[e]; G[r][e] = a[e]; }
             }
-            if (rq == 0) {
-                gC[s * kDK + col] = __expf(all0);
-                gC[s * kDK + col + 1] = __expf(all1);
+            *reinterpret_cast<float4 *>(tot + rg * kDK + col) = make_float4(a[0], a[1], a[2], a[3]);
+            named_sync(2, kWyThreads);
+            float pre[4] = {0.f, 0.f, 0.f, 0.f}, all[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(tot + q * kDK + col);
+                const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (q < rg) pre[e] += tv[e];
+                    all[e] += tv[e];
+                }
             }
+            float gcv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gcv[e] = __expf(all[e]);
+            if (rg == 0) *reinterpret_cast<float4 *>(gC + s * kDK + col) = make_float4(gcv[0], gcv[1], gcv[2], gcv[3]);
             uint8_t *kt = base + (s ? OFF_KT1 : OFF_KT0);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int row = rq * 16 + r;
-                const float g0 = G0[r] + pre0, g1 = G1[r] + pre1;
-                const float e0v = __expf(g0), e1v = __expf(g1);
-                const float i0 = __expf(-g0), i1 = __expf(-g1);
-                const float t0 = __expf(all0 - g0), t1 = __expf(all1 - g1);
+            for (int r = 0; r < 8; ++r) {
+                const int row = rg * 8 + r;
                 const uint32_t o64 = sw128_offset(64, row, col);
-                const float2 qq = ld_bf16x2(base + OFF_RAWQ + o64);
-                const float2 kk = ld_bf16x2(base + OFF_RAWK + o64);
+                const float4 q4 = ld_bf16x4(base + OFF_RAWQ + o64);
+                const float4 k4 = ld_bf16x4(base + OFF_RAWK + o64);
+                const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
                 const float bb = bet[row];
-                st_u32(base + OFF_AG + sw128_offset(128, row, col), pack_bf16(bb * kk.x * e0v, bb * kk.y * e1v));
-                st_u32(base + OFF_AG + sw128_offset(128, 64 + row, col), pack_bf16(qq.x * e0v, qq.y * e1v));
-                st_u32(base + OFF_KR + o64, pack_bf16(kk.x * i0, kk.y * i1));
-                st_u32(base + OFF_KL + o64, pack_bf16(kk.x * e0v, kk.y * e1v));
-                st_u32(kt + o64, pack_bf16(kk.x * t0, kk.y * t1));
+                float ev[4], iv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float gg = G[r][e] + pre[e];
+                    ev[e] = __expf(gg);
+                    iv[e] = __expf(-gg);
+                }
+                st_u64(base + OFF_AG + sw128_offset(128, row, col),
+                       pack4(bb * kv[0] * ev[0], bb * kv[1] * ev[1], bb * kv[2] * ev[2], bb * kv[3] * ev[3]));
+                st_u64(base + OFF_AG + sw128_offset(128, 64 + row, col),
+                       pack4(qv[0] * ev[0], qv[1] * ev[1], qv[2] * ev[2], qv[3] * ev[3]));
+                st_u64(base + OFF_KR + o64, pack4(kv[0] * iv[0], kv[1] * iv[1], kv[2] * iv[2], kv[3] * iv[3]));
+                st_u64(base + OFF_KL + o64, pack4(kv[0] * ev[0], kv[1] * ev[1], kv[2] * ev[2], kv[3] * ev[3]));
+                st_u64(kt + o64, pack4(kv[0] * iv[0] * gcv[0], kv[1] * iv[1] * gcv[1], kv[2] * iv[2] * gcv[2],
+                                       kv[3] * iv[3] * gcv[3]));
             }
         }
         fence_proxy_async_smem();
@@ -278,94 +362,87 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 
         if (!GLA) {
             // ---- L (strictly lower, rows carry beta) to fp32 scratch in the K-> tile (dead now)
-            float *L = reinterpret_cast<float *>(base + OFF_KR);
             if (quarter < 2) {
+                float v[32];
+                tmem_ld32(c.tmem + TM_G + lane_base + half * 32, v);
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float r16[16];
-                    tmem_ld16(c.tmem + TM_G + lane_base + half * 32 + cc * 16, r16);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = half * 32 + cc * 16 + j;
-                        L[lidx(row, col)] = col < row ? r16[j] : 0.f;
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    const int col = half * 32 + 4 * q;
+                    float4 f;
+                    f.x = col + 0 < row ? v[4 * q + 0] : 0.f;
+                    f.y = col + 1 < row ? v[4 * q + 1] : 0.f;
+                    f.z = col + 2 < row ? v[4 * q + 2] : 0.f;
+                    f.w = col + 3 < row ? v[4 * q + 3] : 0.f;
+                    *reinterpret_cast<float4 *>(sc.L(row, col)) = f;
                 }
             }
             named_sync(2, kWyThreads);
 
-            // ---- Y = (I + L)^{-1}, level 0: the four 16x16 diagonal blocks, one column per thread
+            // ---- Y = (I + L)^{-1}; level 0: the four 16x16 diagonal blocks, one column per thread
             if (wt < 64) {
                 const int blk = wt >> 4, cl = wt & 15, o = blk * 16;
                 float y[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
-                    float acc = (r == cl) ? 1.f : 0.f;
+                    float acc0 = (r == cl) ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
-                    for (int j = 0; j < r; ++j) acc -= L[lidx(o + r, o + j)] * y[j];
-                    y[r] = acc;
+                    for (int j4 = 0; j4 < r; j4 += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(sc.L(o + r, o + j4));
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (j4 + e < r) {
+                                if (e & 1) acc1 -= lv[e] * y[j4 + e];
+                                else acc0 -= lv[e] * y[j4 + e];
+                            }
+                    }
+                    y[r] = acc0 + acc1;
                 }
 #pragma unroll
-                for (int r = 0; r < 16; ++r) *yptr(base, o + r, o + cl) = y[r];
+                for (int r = 0; r < 16; ++r) *sc.Y(o + r, o + cl) = y[r];
             }
             named_sync(2, kWyThreads);
-            // ---- level 1: Y10 = -Y11 L10 Y00 and Y32 = -Y33 L32 Y22 (block form 1 on 16x16 blocks)
-            {
-                const int which = wt >> 7;            // 0: rows 16-31 / cols 0-15, 1: rows 48-63 / cols 32-47
-                const int o = which * 32;
-                const int idx = (wt & 127) * 2;       // two outputs per thread
-                const int r = idx >> 4, cl = idx & 15;
-                float m0 = 0.f, m1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float l = L[lidx(o + 16 + r, o + k)];
-                    m0 += l * *yptr(base, o + k, o + cl);
-                    m1 += l * *yptr(base, o + k, o + cl + 1);
-                }
-                // M goes into the (still unused) lower-left block of this 32x32 pair
-                *yptr(base, o + 16 + r, o + cl) = m0;
-                *yptr(base, o + 16 + r, o + cl + 1) = m1;
-                named_sync(2, kWyThreads);
-                float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float yy = *yptr(base, o + 16 + r, o + 16 + k);   // Y11 / Y33, lower triangular
-                    if (k <= r) {
-                        y0 -= yy * *yptr(base, o + 16 + k, o + cl);
-                        y1 -= yy * *yptr(base, o + 16 + k, o + cl + 1);
-                    }
-                }
-                named_sync(2, kWyThreads);
-                *yptr(base, o + 16 + r, o + cl) = y0;
-                *yptr(base, o + 16 + r, o + cl + 1) = y1;
+            // ---- level 1 (block form 1 on 16x16 blocks): Y10 = -Y11 L10 Y00, Y32 = -Y33 L32 Y22
+            if (ww < 2) {
+                const int o = ww * 32;
+                float acc[2][4];
+                zero_acc(acc);
+                blk_mma<true, false>(acc, sc, o + 16, o, o, o, lane);          // M = L10 Y00
+                __syncwarp();
+                blk_store_y(acc, sc, o + 16, o, 1.f, lane);
+                __syncwarp();
+                zero_acc(acc);
+                blk_mma<false, false>(acc, sc, o + 16, o + 16, o + 16, o, lane);   // Y11 M
+                __syncwarp();
+                blk_store_y(acc, sc, o + 16, o, -1.f, lane);
             }
             named_sync(2, kWyThreads);
-            // ---- level 2: Y_BL = -Y_BB L_BL Y_TT on 32x32 blocks
+            // ---- level 2 (block form 1 on 32x32 blocks): Y_BL = -Y_BB (L_BL Y_TT)
             {
-                const int r = wt >> 3;                // 0..31
-                const int c0 = (wt & 7) * 4;          // 4 columns
-                float m[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-                for (int k = 0; k < 32; ++k) {
-                    const float l = L[lidx(32 + r, k)];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (k >= c0 + q) m[q] += l * *yptr(base, k, c0 + q);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) *yptr(base, 32 + r, c0 + q) = m[q];
-                named_sync(2, kWyThreads);
-                float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-                for (int k = 0; k < 32; ++k) {
-                    if (k <= r) {
-                        const float yy = *yptr(base, 32 + r, 32 + k);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) y[q] -= yy * *yptr(base, 32 + k, c0 + q);
-                    }
+                float acc[2][4];
+                zero_acc(acc);
+                if (ww < 4) {
+                    const int bi = 2 + (ww >> 1), bj = ww & 1;   // output block (bi, bj), bi in {2,3}, bj in {0,1}
+                    // M_{bi,bj} = sum_{k=bj}^{1} L_{bi,k} Y_{k,bj}
+                    for (int k = bj; k < 2; ++k) blk_mma<true, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
                 }
                 named_sync(2, kWyThreads);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) *yptr(base, 32 + r, c0 + q) = y[q];
+                if (ww < 4) {
+                    const int bi = 2 + (ww >> 1), bj = ww & 1;
+                    blk_store_y(acc, sc, 16 * bi, 16 * bj, 1.f, lane);
+                }
+                named_sync(2, kWyThreads);
+                zero_acc(acc);
+                if (ww < 4) {
+                    const int bi = 2 + (ww >> 1), bj = ww & 1;
+                    // Y_{bi,bj} = -sum_{k=2}^{bi} Y_{bi,k} M_{k,bj}
+                    for (int k = 2; k <= bi; ++k) blk_mma<false, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
+                }
+                named_sync(2, kWyThreads);
+                if (ww < 4) {
+                    const int bi = 2 + (ww >> 1), bj = ww & 1;
+                    blk_store_y(acc, sc, 16 * bi, 16 * bj, -1.f, lane);
+                }
             }
             named_sync(2, kWyThreads);
             // ---- T = Y Diag(beta) -> bf16 MN-major B tile at the start of A_G
@@ -373,9 +450,14 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 const int i = wt >> 2, cs = (wt & 3) * 16;
                 float t[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = cs + j;
-                    t[j] = col <= i ? *yptr(base, i, col) * bet[col] : 0.f;
+                for (int q = 0; q < 4; ++q) {
+                    const float4 y4 = *reinterpret_cast<const float4 *>(sc.Y(i, cs + 4 * q));
+                    const float4 b4 = *reinterpret_cast<const float4 *>(bet + cs + 4 * q);
+                    const int c0 = cs + 4 * q;
+                    t[4 * q + 0] = c0 + 0 <= i ? y4.x * b4.x : 0.f;
+                    t[4 * q + 1] = c0 + 1 <= i ? y4.y * b4.y : 0.f;
+                    t[4 * q + 2] = c0 + 2 <= i ? y4.z * b4.z : 0.f;
+                    t[4 * q + 3] = c0 + 3 <= i ? y4.w * b4.w : 0.f;
                 }
                 named_sync(2, kWyThreads);
                 uint8_t *tt = base + OFF_AG;
@@ -389,26 +471,17 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 
         // ---- [I ; P] into the K-> tile (K-major, 128 rows x 64): for GLA this is Z itself
         {
-            uint8_t *zp = base + OFF_KR;
             float v[32];
             if (quarter < 2) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = (half * 32 + j == row) ? 1.f : 0.f;
             } else {
                 const int i = row - 64;
+                tmem_ld32(c.tmem + TM_G + lane_base + half * 32, v);
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float r16[16];
-                    tmem_ld16(c.tmem + TM_G + lane_base + half * 32 + cc * 16, r16);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[cc * 16 + j] = (half * 32 + cc * 16 + j <= i) ? r16[j] : 0.f;
-                }
+                for (int j = 0; j < 32; ++j) v[j] = (half * 32 + j <= i) ? v[j] : 0.f;
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                st_u128(zp + sw128_offset(128, row, half * 32 + q * 8), pack_bf16(v[8 * q], v[8 * q + 1]),
-                        pack_bf16(v[8 * q + 2], v[8 * q + 3]), pack_bf16(v[8 * q + 4], v[8 * q + 5]),
-                        pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+            store_row32_bf16(base + OFF_KR, 128, row, half * 32, v);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -428,17 +501,9 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             wait_bar(c, B_Z, ph);
             tc_fence_after();
             {
-                uint8_t *zp = base + OFF_KR;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float r16[16];
-                    tmem_ld16(c.tmem + TM_Z + lane_base + half * 32 + cc * 16, r16);
-                    const int col = half * 32 + cc * 16;
-                    st_u128(zp + sw128_offset(128, row, col), pack_bf16(r16[0], r16[1]), pack_bf16(r16[2], r16[3]),
-                            pack_bf16(r16[4], r16[5]), pack_bf16(r16[6], r16[7]));
-                    st_u128(zp + sw128_offset(128, row, col + 8), pack_bf16(r16[8], r16[9]),
-                            pack_bf16(r16[10], r16[11]), pack_bf16(r16[12], r16[13]), pack_bf16(r16[14], r16[15]));
-                }
+                float v[32];
+                tmem_ld32(c.tmem + TM_Z + lane_base + half * 32, v);
+                store_row32_bf16(base + OFF_KR, 128, row, half * 32, v);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -470,35 +535,36 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         if (leader && n + 2 < nchunks) issue_v(n + 2);           // v[s] consumed
         if (n >= 1) wait_bar(c, B_C10 + ((n - 1) & 1), (uint32_t)(((n - 1) >> 1) & 1));   // A_chain free
 
-        // ---------------- A_chain = [-W ; Q<- - P W]  (K-major 128 x 128)
+        // ---------------- A_chain = [-W ; Q<- - P W]  (K-major 128 x 128), 64 columns per thread
         {
             uint8_t *ach = base + OFF_ACH;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col = half * 64 + cc * 16;
-                float r16[16];
+            for (int cc = 0; cc < 2; ++cc) {
+                const int col = half * 64 + cc * 32;
+                float v[32];
                 if (!GLA) {
-                    tmem_ld16(c.tmem + TM_WQ + lane_base + col, r16);
+                    tmem_ld32(c.tmem + TM_WQ + lane_base + col, v);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r16[j] = 0.f;
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
-                float o16[16];
                 if (quarter < 2) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) o16[j] = -r16[j];
+                    for (int j = 0; j < 32; ++j) v[j] = -v[j];
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float2 qq = ld_bf16x2(base + OFF_AG + sw128_offset(128, row, col + j));
-                        o16[j] = qq.x - r16[j];
-                        o16[j + 1] = qq.y - r16[j + 1];
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(base + OFF_AG + sw128_offset(128, row, col + 8 * q));
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                            v[8 * q + 2 * e] = f.x - v[8 * q + 2 * e];
+                            v[8 * q + 2 * e + 1] = f.y - v[8 * q + 2 * e + 1];
+                        }
                     }
                 }
-                st_u128(ach + sw128_offset(128, row, col), pack_bf16(o16[0], o16[1]), pack_bf16(o16[2], o16[3]),
-                        pack_bf16(o16[4], o16[5]), pack_bf16(o16[6], o16[7]));
-                st_u128(ach + sw128_offset(128, row, col + 8), pack_bf16(o16[8], o16[9]),
-                        pack_bf16(o16[10], o16[11]), pack_bf16(o16[12], o16[13]), pack_bf16(o16[14], o16[15]));
+                store_row32_bf16(ach, 128, row, col, v);
             }
         }
         if (wt < kC && n + 1 < nchunks) {
