@@ -5,4 +5,4 @@ The computation lives in the CUDA library ``_build/libkda.so`` (C ABI in
 :func:`.build.build`.
 """
 from .api import (HostRunner, KdaError, deltanet_fwd, gdn_fwd, gla_fwd,  # noqa: F401
-                  kda_chunk_fwd, status_read)
+                  kda_chunk_fwd, kda_chunk_fwd_noalloc, status_read)

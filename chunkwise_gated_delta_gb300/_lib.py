@@ -24,7 +24,8 @@ KDA_GATE_CHANNEL = 2
 KDA_FLAG_BETA_SCALES_V = 1
 
 # Every symbol include/kda.h declares.
-EXPORTS = ("kda_chunk_fwd_workspace", "kda_chunk_fwd", "kda_status_read", "kda_status_string")
+EXPORTS = ("kda_chunk_fwd_workspace", "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_status_read",
+           "kda_status_string")
 
 
 class KdaFwdArgs(ctypes.Structure):
@@ -62,6 +63,8 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_workspace.argtypes = [ctypes.POINTER(KdaFwdArgs)]
         lib.kda_chunk_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd.argtypes = [ctypes.POINTER(KdaFwdArgs), ctypes.c_void_p]
+        lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(KdaFwdArgs), ctypes.c_void_p]
         lib.kda_status_read.restype = ctypes.c_int
         lib.kda_status_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
         lib.kda_status_string.restype = ctypes.c_char_p

@@ -108,6 +108,35 @@ def kda_chunk_fwd(q, k, v, g=None, beta=None, h0=None, *, gate=None, scale_v=Tru
     return o, ht
 
 
+def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, scale_v=True,
+                          output_final_state=True, o=None, ht=None, stream=None):
+    """``kda_chunk_fwd_noalloc`` of the C ABI: the forward without a workspace.
+
+    For callers that cannot allocate device memory at the call (for instance
+    inside CUDA-graph capture): the library uses its own 256-byte array in
+    place of the workspace.  o / ht may be passed in preallocated; when they
+    are not, this binding allocates them with torch before the call (the C
+    entry point itself allocates nothing).  Calls sharing the library array
+    must not overlap on the GPU.
+    """
+    lib = _lib.load()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (h0, "h0")):
+        _check(t, name)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    if ht is None and output_final_state:
+        ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device)
+    args = make_args(q, k, v, g, beta, h0, o, ht, gate=gate, scale_v=scale_v)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_noalloc")
+    return o, ht
+
+
 def status_read(workspace=None, device=None, stream=None) -> int:
     """Device status word of the workspace (waits for the stream, then clears it)."""
     lib = _lib.load()

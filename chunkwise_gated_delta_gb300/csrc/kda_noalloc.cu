@@ -1,0 +1,64 @@
+// kda_chunk_fwd_noalloc: the forward for callers that cannot allocate device
+// memory at the point of the call.
+//
+// kda_chunk_fwd needs one piece of memory besides its inputs and outputs: a
+// workspace whose first word the kernels use to report a device-side error.
+// Callers that cannot provide it -- code running while a stream is captured
+// into a CUDA graph, frameworks whose allocator forbids allocations outside
+// its own arenas, hosts that only hand over the input and output tensors --
+// use this entry point instead.  The workspace then lives in a small array
+// owned by the library, defined below; every GPU that loads the library
+// holds it until the process exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kda.h"
+
+namespace {
+
+// Library-owned replacement for the caller's workspace (the forward needs
+// 256 bytes: its status word, padded to an aligned block).
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// In host code `g_noalloc_scratch` names a host-side stand-in, not the device
+// array, so its device address is looked up once per device, with that
+// device current, and cached here.
+constexpr int kMaxDevices = 64;
+std::mutex g_lock;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+cudaError_t scratch_address(int dev, void **out) {
+    std::lock_guard<std::mutex> guard(g_lock);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" kda_status kda_chunk_fwd_noalloc(const kda_fwd_args *args, kda_stream_t stream) {
+    if (!args) return KDA_ERR_INVALID_ARG;
+    kda_fwd_args a = *args;
+    a.workspace = nullptr;          // the caller's workspace fields are ignored
+    a.workspace_bytes = 0;
+    const size_t need = kda_chunk_fwd_workspace(&a);
+    if (need == 0) return kda_chunk_fwd(&a, stream);          // reports the argument error, launches nothing
+    if (need > kNoAllocScratchBytes) return KDA_ERR_WORKSPACE;  // more scratch than the library array holds
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    void *scratch = nullptr;
+    if (scratch_address(dev, &scratch) != cudaSuccess) return KDA_ERR_CUDA;
+    // The array keeps the previous call's contents: the status word must start at zero.
+    if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    a.workspace = scratch;
+    a.workspace_bytes = kNoAllocScratchBytes;
+    return kda_chunk_fwd(&a, stream);
+}

@@ -100,6 +100,31 @@ size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd without a workspace from the caller.  The papers have no
+ * counterpart: this is library plumbing.
+ *
+ * Some callers cannot allocate device memory where they call the forward:
+ * code running while a stream is being captured into a CUDA graph,
+ * frameworks whose allocator forbids allocations outside its own arenas, or
+ * hosts that hand the library nothing but the input and output tensors.
+ * This entry point takes the same arguments as kda_chunk_fwd (workspace and
+ * workspace_bytes are ignored) and uses instead an array owned by the
+ * library: 256 bytes per device, held from library load until process exit.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call clears the array's status word on `stream`, then launches.
+ *     All calls share the array, so calls that overlap on the GPU (unordered
+ *     streams) race on it.
+ *   - Returns KDA_ERR_WORKSPACE if the forward would need more scratch than
+ *     the array holds (the current kernels need all of 256 bytes, no more).
+ *   - A device-side wait that runs out is recorded in the shared array and
+ *     cleared by the next call; to observe it, use kda_chunk_fwd with your
+ *     own workspace and kda_status_read.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+kda_status kda_chunk_fwd_noalloc(const kda_fwd_args *args, kda_stream_t stream);
+
+/*
  * Reads the device status word that kernels set on a device-side error,
  * waits for the stream, clears the word and returns the code (KDA_OK when
  * no error was recorded).

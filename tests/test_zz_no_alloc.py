@@ -1,0 +1,59 @@
+"""kda_chunk_fwd_noalloc: the forward for callers that cannot allocate device memory.
+
+Callers such as code running during CUDA-graph capture, or frameworks whose
+allocator forbids allocations at the call site, cannot supply the workspace
+that kda_chunk_fwd needs; the no-allocation entry point replaces it with a
+small array owned by the library.  Its results must equal those of
+kda_chunk_fwd on the same inputs, on every call (the library array keeps the
+previous call's contents, so two calls in a row are checked).  This file is
+collected last so that a run stopping at the first failure has already run
+every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from chunkwise_gated_delta_gb300 import _lib, api
+from chunkwise_gated_delta_gb300 import build as kbuild
+from chunkwise_gated_delta_gb300.inputs import custom, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: 5e-3, torch.float32: 1e-5}
+
+
+def _rel(x, ref):
+    x, ref = x.double().cpu().numpy(), ref.double().cpu().numpy()
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+@pytest.mark.parametrize("dtype,dk,T", [(torch.bfloat16, 128, 200), (torch.float32, 64, 130)])
+def test_noalloc_matches_kda_chunk_fwd_on_two_calls(dtype, dk, T):
+    kbuild.build()
+    lib = _lib.load()
+    w = custom("kda", 2, T, 2, dk, dk, dtype=dtype, h0=True)
+    x = make_inputs(w, seed=11)
+    d = {k: v.to("cuda:0") for k, v in x.items() if isinstance(v, torch.Tensor)}
+    o_ref, ht_ref = api.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        o = torch.full_like(o_ref, float("nan"))
+        ht = torch.full_like(ht_ref, float("nan"))
+        args = api.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, ht)
+        rc = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+        assert rc == _lib.KDA_OK, _lib.status_string(rc)
+        torch.cuda.synchronize()
+        assert _rel(o, o_ref) <= TOL[dtype]
+        assert _rel(ht, ht_ref) <= TOL[dtype]
+
+
+def test_noalloc_rejects_bad_arguments_like_kda_chunk_fwd():
+    kbuild.build()
+    lib = _lib.load()
+    assert lib.kda_chunk_fwd_noalloc(None, None) == _lib.KDA_ERR_INVALID_ARG
+    a = _lib.KdaFwdArgs()
+    a.B, a.T, a.H, a.dk, a.dv = 1, 64, 1, 96, 128      # dk = 96 is not implemented
+    a.q = a.k = a.v = a.o = None
+    assert lib.kda_chunk_fwd_noalloc(ctypes.byref(a), None) == _lib.KDA_ERR_INVALID_ARG
