@@ -7,22 +7,32 @@
 // product has M = 128 rows:
 //
 //   [beta K<- ; Q<-] K->^T      = [L ; P]          (Gram, one MMA)
-//   T  = (I + L_{strict})^{-1} Diag(beta)          (CUDA cores, 16x16 blocks,
-//        page "DeltaNet" 4.2, block form 1 applied twice)
+//   T  = (I + L_{strict})^{-1} Diag(beta)          (page "DeltaNet" 4.2,
+//        block form 1 applied twice: 16x16 diagonal blocks on CUDA cores,
+//        the off-diagonal blocks as tf32 warp MMAs)
 //   [I ; P] T                   = Z = [T ; P T]
 //   Z K<-                       = [W ; P W]
 //   Z V                         = [U ; P U]        (into the accumulator D1)
 //   D1 += [-W ; Q<- - P W] S^T  = [V_new ; O]      (state-dependent, one MMA)
-//   K~^T V_new                  = dS^T,  S <- S Diag(gamma^C) + dS
+//   K->^T V_new                 = dS^T,  S <- (S + dS) Diag(gamma^C)
 //
 // O = Q<- S^T + (Q<- K->^T * M) V_new expands to (Q<- - P W) S^T + P U, which
-// is why the output rides in the lower half of the state-dependent product.
-// K~ = K * exp(G_C - G) is K-> Diag(gamma^C) written without the division.
+// is why the output rides in the lower half of the state-dependent product;
+// the state step uses the factored form of page "Gated Linear Attention" 5.2.
 //
 // Warp roles (384 threads):
-//   warps 0-3  "chain": the serial part -- the state S^T (dk x 64 slice) lives
-//              in fp32 registers, one key channel per thread.
-//   warps 4-11 "WY": everything that does not depend on S, one chunk ahead.
+//   warps 0-3  "chain": the serial part -- the state S^T (128 key channels x
+//              64 values) in fp32 registers, one key channel per thread.
+//   warps 4-11 "WY": everything that does not depend on S.
+//
+// Pairs.  With dv = 128 the two value-slice CTAs of a head form a cluster and
+// split the state-independent work by chunk parity: CTA r builds the WY
+// operands of the chunks n with n % 2 == r and copies them (A_chain, K->,
+// gamma^C, Z) into the other CTA's shared memory with bulk copies; each CTA
+// still runs the state scan of every chunk for its own value slice, and forms
+// its own [U ; P U] = Z V from its own v slice.  With dv = 64 one CTA does it
+// all.
+//
 // Every wait on an mbarrier is bounded; on timeout the kernel writes the
 // status word, turns every later wait into a no-op and runs to its end.
 #include <cuda.h>
@@ -43,37 +53,44 @@ constexpr int kChainThreads = 128;
 constexpr int kWyThreads = 256;
 constexpr int kThreads = kChainThreads + kWyThreads;
 
-// ---- shared memory map (byte offsets from a 1024-aligned base)
-constexpr uint32_t OFF_RAWQ = 0;         // q tile, 2 column blocks of [64][64] bf16, SW128
-constexpr uint32_t OFF_RAWK = 16384;     // k tile
-constexpr uint32_t OFF_RAWG = 32768;     // g tile (per-channel gate)
-constexpr uint32_t OFF_V0 = 49152;       // v slice [64 rows][64] bf16, SW128 (MN-major B), slot 0
-constexpr uint32_t OFF_V1 = 57344;       // slot 1
-constexpr uint32_t OFF_AG = 65536;       // [beta K<- ; Q<-] 128 x 128 K-major; later Y (fp32) / T
-constexpr uint32_t OFF_KR = 98304;       // K-> 64 x 128 (K-major B); later L (fp32), [I;P], Z
-constexpr uint32_t OFF_KL = 114688;      // K<- 64 x 128 (MN-major B)
-constexpr uint32_t OFF_ACH = 131072;     // [-W ; Q'] 128 x 128 K-major
-constexpr uint32_t OFF_KT0 = 163840;     // K~ 64 x 128 (MN-major A), slot 0
-constexpr uint32_t OFF_KT1 = 180224;     // slot 1
-constexpr uint32_t OFF_ST = 196608;      // S^T 128 x 64 bf16 (MN-major B); V_new / O staging
-constexpr uint32_t OFF_MISC = 212992;
+// ---- shared memory map (byte offsets from a 1024-aligned base).  Operand
+// tiles are bf16 column blocks of 64 with 128-byte swizzle.
+constexpr uint32_t OFF_AG = 0;           // [beta K<- ; Q<-] 128 x 128 K-major.  Raw g lands in its
+                                         // rows 0-63 and raw q in rows 64-127; after the Gram,
+                                         // rows 0-63 hold Y (fp32) and then T.
+constexpr uint32_t OFF_KR = 32768;       // K-> 64 x 128 (K-major B); then L (fp32), [I;P], Z
+constexpr uint32_t OFF_KL = 49152;       // raw k, then K<- 64 x 128 (MN-major B)
+constexpr uint32_t OFF_V0 = 65536;       // v slice [64][64] (MN-major B), slot 0
+constexpr uint32_t OFF_V1 = 73728;       // slot 1
+constexpr uint32_t OFF_ACH0 = 81920;     // [-W ; Q'] 128 x 128 K-major, slot 0
+constexpr uint32_t OFF_ACH1 = 114688;    // slot 1
+constexpr uint32_t OFF_KT0 = 147456;     // K-> 64 x 128 (MN-major A of dS), slot 0
+constexpr uint32_t OFF_KT1 = 163840;     // slot 1
+constexpr uint32_t OFF_ZIN = 180224;     // Z received from the other CTA of the pair
+constexpr uint32_t OFF_ST = 196608;      // S^T 128 x 64 (MN-major B); V_new in its first 8 KB
+constexpr uint32_t OFF_OST = 212992;     // O staging [64][64] for the TMA store
+constexpr uint32_t OFF_MISC = 221184;
 constexpr uint32_t MISC_GC = 0;          // gamma^C [2][128] f32            (1024 B)
 constexpr uint32_t MISC_BETA = 1024;     // beta [2][64] f32                 (512 B)
 constexpr uint32_t MISC_GS = 1536;       // scalar gate [2][64] f32          (512 B)
 constexpr uint32_t MISC_TOT = 2048;      // cumsum partials [8][128] f32     (4096 B)
-constexpr uint32_t MISC_BAR = 6144;      // mbarriers [16] u64               (128 B)
+constexpr uint32_t MISC_BAR = 6144;      // mbarriers [24] u64               (192 B)
 constexpr uint32_t MISC_TSLOT = 6400;    // TMEM base address
 constexpr uint32_t MISC_ABORT = 6404;    // abort flag
-constexpr uint32_t kMiscBytes = 7168;
+constexpr uint32_t kMiscBytes = 6656;
 constexpr uint32_t kSmemBytes = OFF_MISC + kMiscBytes + 1024;   // + alignment slack of the dynamic base
 static_assert(MISC_GC + 2 * 128 * 4 <= MISC_BETA, "misc layout");
 static_assert(MISC_BETA + 2 * 64 * 4 <= MISC_GS, "misc layout");
 static_assert(MISC_GS + 2 * 64 * 4 <= MISC_TOT, "misc layout");
 static_assert(MISC_TOT + 8 * 128 * 4 <= MISC_BAR, "misc layout");
-static_assert(MISC_BAR + 16 * 8 <= MISC_TSLOT, "misc layout");
+static_assert(MISC_BAR + 24 * 8 <= MISC_TSLOT, "misc layout");
 static_assert(MISC_ABORT + 4 <= kMiscBytes, "misc layout");
-static_assert(OFF_ST + 16384 <= OFF_MISC, "tile layout");
+static_assert(OFF_OST + 8192 <= OFF_MISC, "tile layout");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+
+// bytes of the slot buffers one CTA copies into the other per chunk it builds
+constexpr uint32_t kSlotPushBytes = 32768 + 16384 + 512;
 
 // ---- TMEM columns
 constexpr uint32_t TM_G = 0;      // Gram [L ; P], 64 cols
@@ -86,9 +103,13 @@ constexpr uint32_t kTmemCols = 512;
 // mbarrier indices
 enum {
     B_RAW = 0, B_V0, B_V1, B_GRAM, B_Z, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
-    B_FIN0, B_FIN1, kNumBars
+    B_RX, B_PFREE, B_FIN0, B_FIN1, kNumBars
 };
-static_assert(kNumBars <= 16, "mbarrier slots");
+static_assert(kNumBars <= 24, "mbarrier slots");
+
+__device__ __forceinline__ uint32_t off_ach(int s) { return s ? OFF_ACH1 : OFF_ACH0; }
+__device__ __forceinline__ uint32_t off_kt(int s) { return s ? OFF_KT1 : OFF_KT0; }
+__device__ __forceinline__ uint32_t off_v(int s) { return s ? OFF_V1 : OFF_V0; }
 
 struct Ctx {
     uint8_t *base;
@@ -96,6 +117,7 @@ struct Ctx {
     volatile int *abort;
     int *status;
     uint32_t tmem;
+    uint32_t rank;     // rank in the pair (0 without a pair)
 };
 
 __device__ __forceinline__ void record_timeout(const Ctx &c) {
@@ -103,11 +125,20 @@ __device__ __forceinline__ void record_timeout(const Ctx &c) {
     atomicCAS(c.status, kDevOk, kDevTimeout);
 }
 
-// Bounded wait that becomes a no-op once any thread has given up.
+// Bounded wait that becomes a no-op once any thread of the CTA has given up.
 __device__ __forceinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
     uint64_t *bar = c.bars + idx;
     for (uint32_t i = 0; i < kWaitBound; ++i) {
         if (mbar_try_wait(bar, parity)) return;
+        if (*c.abort) return;
+    }
+    record_timeout(c);
+}
+// The same for barriers completed from the other CTA of the pair.
+__device__ __forceinline__ void wait_bar_cluster(const Ctx &c, int idx, uint32_t parity) {
+    uint64_t *bar = c.bars + idx;
+    for (uint32_t i = 0; i < kWaitBound; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return;
         if (*c.abort) return;
     }
     record_timeout(c);
@@ -117,13 +148,41 @@ __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ float2 ld_bf16x2(const uint8_t *p) {
-    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(p);
-    return __bfloat1622float2(h);
-}
-__device__ __forceinline__ void st_u32(uint8_t *p, uint32_t v) { *reinterpret_cast<uint32_t *>(p) = v; }
 __device__ __forceinline__ void st_u128(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
+}
+__device__ __forceinline__ void st_u64(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
+__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
+    return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
+}
+__device__ __forceinline__ float4 ld_bf16x4(const uint8_t *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+// 32 fp32 values -> 64 bytes of bf16 at (row, col .. col+31) of a SW128 tile with `rows` rows.
+__device__ __forceinline__ void store_row32_bf16(uint8_t *tile, uint32_t rows, uint32_t row, uint32_t col,
+                                                 const float *v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        st_u128(tile + sw128_offset(rows, row, col + 8 * q), pack_bf16(v[8 * q], v[8 * q + 1]),
+                pack_bf16(v[8 * q + 2], v[8 * q + 3]), pack_bf16(v[8 * q + 4], v[8 * q + 5]),
+                pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// The same, also written to the other CTA of the pair at `remote` (its address of `tile`).
+template <bool REMOTE>
+__device__ __forceinline__ void store_row32_bf16_x2(uint8_t *tile, uint32_t remote, uint32_t rows, uint32_t row,
+                                                    uint32_t col, const float *v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t off = sw128_offset(rows, row, col + 8 * q);
+        const uint32_t a = pack_bf16(v[8 * q], v[8 * q + 1]), b = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+        const uint32_t c = pack_bf16(v[8 * q + 4], v[8 * q + 5]), d = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+        st_u128(tile + off, a, b, c, d);
+        if (REMOTE) st_cluster_u128(remote + off, a, b, c, d);
+    }
 }
 
 template <typename T> __device__ __forceinline__ float ldg_f(const T *p);
@@ -132,12 +191,8 @@ template <> __device__ __forceinline__ float ldg_f<__nv_bfloat16>(const __nv_bfl
 }
 template <> __device__ __forceinline__ float ldg_f<float>(const float *p) { return *p; }
 
-// ============================================================================
-// WY warps: everything of chunk n that does not depend on the state.
-// ============================================================================
-
-// fp32 [64][64] scratch with an XOR swizzle on column bits 2-4: float4 groups
-// stay contiguous, and row walks (lanes over rows) spread over the banks.
+// ---- fp32 [64][64] scratch for the inverse, with an XOR swizzle on column
+// bits 2-4: float4 groups stay contiguous, and row walks spread over the banks.
 __device__ __forceinline__ uint32_t sidx(uint32_t i, uint32_t j) { return i * 64u + (j ^ ((i & 7u) << 2)); }
 
 struct Scratch {
@@ -188,28 +243,68 @@ __device__ __forceinline__ void zero_acc(float (&acc)[2][4]) {
         for (int e = 0; e < 4; ++e) acc[nh][e] = 0.f;
 }
 
-__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
-    return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
-}
-__device__ __forceinline__ float4 ld_bf16x4(const uint8_t *p) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(p);
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-    return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
-__device__ __forceinline__ void st_u64(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
-
-// 32 fp32 values -> 64 bytes of bf16 at (row, col .. col+31) of a SW128 tile with `rows` rows.
-__device__ __forceinline__ void store_row32_bf16(uint8_t *tile, uint32_t rows, uint32_t row, uint32_t col,
-                                                 const float *v) {
+// Y = (I + L)^{-1} for the strictly lower L in the scratch, all 256 WY threads.
+__device__ __forceinline__ void invert_unit_lower(const Scratch &sc, int wt, int ww, int lane) {
+    // level 0: the four 16x16 diagonal blocks, forward substitution, one column per thread
+    if (wt < 64) {
+        const int blk = wt >> 4, cl = wt & 15, o = blk * 16;
+        float y[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-        st_u128(tile + sw128_offset(rows, row, col + 8 * q), pack_bf16(v[8 * q], v[8 * q + 1]),
-                pack_bf16(v[8 * q + 2], v[8 * q + 3]), pack_bf16(v[8 * q + 4], v[8 * q + 5]),
-                pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+        for (int r = 0; r < 16; ++r) {
+            float acc0 = (r == cl) ? 1.f : 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int j4 = 0; j4 < r; j4 += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(sc.L(o + r, o + j4));
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (j4 + e < r) {
+                        if (e & 1) acc1 -= lv[e] * y[j4 + e];
+                        else acc0 -= lv[e] * y[j4 + e];
+                    }
+            }
+            y[r] = acc0 + acc1;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) *sc.Y(o + r, o + cl) = y[r];
+    }
+    named_sync(2, kWyThreads);
+    // level 1 (block form 1 on 16x16 blocks): Y10 = -Y11 L10 Y00, Y32 = -Y33 L32 Y22
+    if (ww < 2) {
+        const int o = ww * 32;
+        float acc[2][4];
+        zero_acc(acc);
+        blk_mma<true, false>(acc, sc, o + 16, o, o, o, lane);              // M = L10 Y00
+        __syncwarp();
+        blk_store_y(acc, sc, o + 16, o, 1.f, lane);
+        __syncwarp();
+        zero_acc(acc);
+        blk_mma<false, false>(acc, sc, o + 16, o + 16, o + 16, o, lane);   // Y11 M
+        __syncwarp();
+        blk_store_y(acc, sc, o + 16, o, -1.f, lane);
+    }
+    named_sync(2, kWyThreads);
+    // level 2 (block form 1 on 32x32 blocks): Y_BL = -Y_BB (L_BL Y_TT)
+    float acc[2][4];
+    zero_acc(acc);
+    const int bi = 2 + (ww >> 1), bj = ww & 1;   // output block of warps 0-3
+    if (ww < 4)
+        for (int k = bj; k < 2; ++k) blk_mma<true, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
+    named_sync(2, kWyThreads);
+    if (ww < 4) blk_store_y(acc, sc, 16 * bi, 16 * bj, 1.f, lane);
+    named_sync(2, kWyThreads);
+    zero_acc(acc);
+    if (ww < 4)
+        for (int k = 2; k <= bi; ++k) blk_mma<false, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
+    named_sync(2, kWyThreads);
+    if (ww < 4) blk_store_y(acc, sc, 16 * bi, 16 * bj, -1.f, lane);
+    named_sync(2, kWyThreads);
 }
 
-template <int GATE, bool GLA, typename Tg>
+// ============================================================================
+// WY warps: everything of a chunk that does not depend on the state.
+// ============================================================================
+template <int GATE, bool GLA, bool PAIR, typename Tg>
 __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                         const CUtensorMap *tm_g, const CUtensorMap *tm_v, int e0, int h, int b, int nchunks) {
     uint8_t *base = c.base;
@@ -229,20 +324,25 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     const Tg *gsg = static_cast<const Tg *>(p.g);
     const uint32_t raw_bytes = (GATE == KDA_GATE_CHANNEL ? 3u : 2u) * 16384u;
     const Scratch sc{base};
+    const int step = PAIR ? 2 : 1;                       // distance between chunks this CTA builds
+    const int first = PAIR ? (int)c.rank : 0;
+    auto owns = [&](int n) { return !PAIR || (n & 1) == (int)c.rank; };
 
+    // raw tiles land where their rescaled versions go: g -> A_G rows 0-63,
+    // q -> A_G rows 64-127, k -> K<- tile
     auto issue_raw = [&](int n) {
         mbar_arrive_expect_tx(c.bars + B_RAW, raw_bytes);
         for (int blk = 0; blk < 2; ++blk) {
-            tma_load_4d(base + OFF_RAWQ + blk * 8192, tm_q, c.bars + B_RAW, blk * 64, h, n * kC, b);
-            tma_load_4d(base + OFF_RAWK + blk * 8192, tm_k, c.bars + B_RAW, blk * 64, h, n * kC, b);
+            tma_load_4d(base + OFF_AG + blk * 16384 + 8192, tm_q, c.bars + B_RAW, blk * 64, h, n * kC, b);
+            tma_load_4d(base + OFF_KL + blk * 8192, tm_k, c.bars + B_RAW, blk * 64, h, n * kC, b);
             if (GATE == KDA_GATE_CHANNEL)
-                tma_load_4d(base + OFF_RAWG + blk * 8192, tm_g, c.bars + B_RAW, blk * 64, h, n * kC, b);
+                tma_load_4d(base + OFF_AG + blk * 16384, tm_g, c.bars + B_RAW, blk * 64, h, n * kC, b);
         }
     };
     auto issue_v = [&](int n) {
         const int s = n & 1;
         mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
-        tma_load_4d(base + (s ? OFF_V1 : OFF_V0), tm_v, c.bars + B_V0 + s, e0, h, n * kC, b);
+        tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, n * kC, b);
     };
     // per-token scalars of chunk n: beta and (GDN) the scalar log-decay
     auto load_scalars = [&](int n, float &bv, float &gv) {
@@ -256,29 +356,38 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     };
 
     if (leader) {
-        issue_raw(0);
+        if (first < nchunks) issue_raw(first);
         issue_v(0);
         if (nchunks > 1) issue_v(1);
     }
     {
         float bv, gv;
-        load_scalars(0, bv, gv);
+        load_scalars(first, bv, gv);
         if (wt < kC) { betas[wt] = bv; gss[wt] = gv; }
     }
     named_sync(2, kWyThreads);
 
     for (int n = 0; n < nchunks; ++n) {
         const int s = n & 1;
-        const uint32_t ph = (uint32_t)(n & 1);
         const uint32_t ph2 = (uint32_t)((n >> 1) & 1);
-        const float *bet = betas + s * kC;
+
+        if (!owns(n)) continue;              // the chain warps take the other CTA's chunks
+
+        // ---------------- a chunk this CTA builds
+        const int m = PAIR ? (n >> 1) : n;                   // index among the chunks built here
+        const uint32_t phm = (uint32_t)(m & 1);
+        const int sb = m & 1;                                // scalar buffer
+        const float *bet = betas + sb * kC;
         float nb = 0.f, ng = 0.f;
-        if (n + 1 < nchunks) load_scalars(n + 1, nb, ng);   // prefetch next chunk's scalars
+        if (n + step < nchunks) load_scalars(n + step, nb, ng);   // prefetch next built chunk's scalars
 
-        wait_bar(c, B_RAW, ph);
-        if (n >= 2) wait_bar(c, B_C20 + s, (uint32_t)(((n - 2) >> 1) & 1));   // K~[s] and gamma^C[s] free
+        wait_bar(c, B_RAW, phm);
+        const uint32_t peer_base = PAIR ? map_to_rank(smem_u32(base), c.rank ^ 1u) : 0u;
 
-        // ---------------- prologue: Gamma and the rescaled tiles; 4 columns x 8 rows per thread
+        // ---------------- prologue: Gamma and the rescaled tiles, in place; 4 columns x 8 rows per thread.
+        // K-> and gamma^C also go to the chunk's slot, written at the end (the slot may still be in use).
+        uint2 krv[8];
+        float4 gcv;
         {
             const int cg = wt & 31, rg = wt >> 5;
             const int col = 4 * cg;
@@ -289,10 +398,10 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 const int row = rg * 8 + r;
                 float x[4] = {0.f, 0.f, 0.f, 0.f};
                 if (GATE == KDA_GATE_CHANNEL) {
-                    const float4 gg = ld_bf16x4(base + OFF_RAWG + sw128_offset(64, row, col));
+                    const float4 gg = ld_bf16x4(base + OFF_AG + sw128_offset(128, row, col));
                     x[0] = gg.x; x[1] = gg.y; x[2] = gg.z; x[3] = gg.w;
                 } else if (GATE == KDA_GATE_SCALAR) {
-                    x[0] = x[1] = x[2] = x[3] = gss[s * kC + row];
+                    x[0] = x[1] = x[2] = x[3] = gss[sb * kC + row];
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) { a[e] += x[e]; G[r][e] = a[e]; }
@@ -310,17 +419,14 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                     all[e] += tv[e];
                 }
             }
-            float gcv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) gcv[e] = __expf(all[e]);
-            if (rg == 0) *reinterpret_cast<float4 *>(gC + s * kDK + col) = make_float4(gcv[0], gcv[1], gcv[2], gcv[3]);
-            uint8_t *kt = base + (s ? OFF_KT1 : OFF_KT0);
+            gcv = make_float4(__expf(all[0]), __expf(all[1]), __expf(all[2]), __expf(all[3]));
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int row = rg * 8 + r;
                 const uint32_t o64 = sw128_offset(64, row, col);
-                const float4 q4 = ld_bf16x4(base + OFF_RAWQ + o64);
-                const float4 k4 = ld_bf16x4(base + OFF_RAWK + o64);
+                const uint32_t otop = sw128_offset(128, row, col), obot = sw128_offset(128, 64 + row, col);
+                const float4 q4 = ld_bf16x4(base + OFF_AG + obot);
+                const float4 k4 = ld_bf16x4(base + OFF_KL + o64);
                 const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
                 const float bb = bet[row];
                 float ev[4], iv[4];
@@ -330,19 +436,17 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                     ev[e] = __expf(gg);
                     iv[e] = __expf(-gg);
                 }
-                st_u64(base + OFF_AG + sw128_offset(128, row, col),
+                const uint2 kr = pack4(kv[0] * iv[0], kv[1] * iv[1], kv[2] * iv[2], kv[3] * iv[3]);
+                st_u64(base + OFF_AG + otop,
                        pack4(bb * kv[0] * ev[0], bb * kv[1] * ev[1], bb * kv[2] * ev[2], bb * kv[3] * ev[3]));
-                st_u64(base + OFF_AG + sw128_offset(128, 64 + row, col),
-                       pack4(qv[0] * ev[0], qv[1] * ev[1], qv[2] * ev[2], qv[3] * ev[3]));
-                st_u64(base + OFF_KR + o64, pack4(kv[0] * iv[0], kv[1] * iv[1], kv[2] * iv[2], kv[3] * iv[3]));
+                st_u64(base + OFF_AG + obot, pack4(qv[0] * ev[0], qv[1] * ev[1], qv[2] * ev[2], qv[3] * ev[3]));
+                st_u64(base + OFF_KR + o64, kr);
                 st_u64(base + OFF_KL + o64, pack4(kv[0] * ev[0], kv[1] * ev[1], kv[2] * ev[2], kv[3] * ev[3]));
-                st_u64(kt + o64, pack4(kv[0] * iv[0] * gcv[0], kv[1] * iv[1] * gcv[1], kv[2] * iv[2] * gcv[2],
-                                       kv[3] * iv[3] * gcv[3]));
+                krv[r] = kr;
             }
         }
         fence_proxy_async_smem();
         named_sync(2, kWyThreads);
-        if (leader && n + 1 < nchunks) issue_raw(n + 1);   // raw tiles consumed
 
         // ---------------- Gram: D_G = [beta K<- ; Q<-] K->^T   (M128 N64 K128)
         if (leader) {
@@ -354,7 +458,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 mma_bf16(c.tmem + TM_G, desc_kmajor(a0, 128, ks), desc_kmajor(b0, 64, ks), id, ks > 0);
             mma_commit(c.bars + B_GRAM);
         }
-        wait_bar(c, B_GRAM, ph);
+        wait_bar(c, B_GRAM, phm);
         tc_fence_after();
 
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -377,74 +481,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 }
             }
             named_sync(2, kWyThreads);
-
-            // ---- Y = (I + L)^{-1}; level 0: the four 16x16 diagonal blocks, one column per thread
-            if (wt < 64) {
-                const int blk = wt >> 4, cl = wt & 15, o = blk * 16;
-                float y[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc0 = (r == cl) ? 1.f : 0.f, acc1 = 0.f;
-#pragma unroll
-                    for (int j4 = 0; j4 < r; j4 += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(sc.L(o + r, o + j4));
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (j4 + e < r) {
-                                if (e & 1) acc1 -= lv[e] * y[j4 + e];
-                                else acc0 -= lv[e] * y[j4 + e];
-                            }
-                    }
-                    y[r] = acc0 + acc1;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) *sc.Y(o + r, o + cl) = y[r];
-            }
-            named_sync(2, kWyThreads);
-            // ---- level 1 (block form 1 on 16x16 blocks): Y10 = -Y11 L10 Y00, Y32 = -Y33 L32 Y22
-            if (ww < 2) {
-                const int o = ww * 32;
-                float acc[2][4];
-                zero_acc(acc);
-                blk_mma<true, false>(acc, sc, o + 16, o, o, o, lane);          // M = L10 Y00
-                __syncwarp();
-                blk_store_y(acc, sc, o + 16, o, 1.f, lane);
-                __syncwarp();
-                zero_acc(acc);
-                blk_mma<false, false>(acc, sc, o + 16, o + 16, o + 16, o, lane);   // Y11 M
-                __syncwarp();
-                blk_store_y(acc, sc, o + 16, o, -1.f, lane);
-            }
-            named_sync(2, kWyThreads);
-            // ---- level 2 (block form 1 on 32x32 blocks): Y_BL = -Y_BB (L_BL Y_TT)
-            {
-                float acc[2][4];
-                zero_acc(acc);
-                if (ww < 4) {
-                    const int bi = 2 + (ww >> 1), bj = ww & 1;   // output block (bi, bj), bi in {2,3}, bj in {0,1}
-                    // M_{bi,bj} = sum_{k=bj}^{1} L_{bi,k} Y_{k,bj}
-                    for (int k = bj; k < 2; ++k) blk_mma<true, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
-                }
-                named_sync(2, kWyThreads);
-                if (ww < 4) {
-                    const int bi = 2 + (ww >> 1), bj = ww & 1;
-                    blk_store_y(acc, sc, 16 * bi, 16 * bj, 1.f, lane);
-                }
-                named_sync(2, kWyThreads);
-                zero_acc(acc);
-                if (ww < 4) {
-                    const int bi = 2 + (ww >> 1), bj = ww & 1;
-                    // Y_{bi,bj} = -sum_{k=2}^{bi} Y_{bi,k} M_{k,bj}
-                    for (int k = 2; k <= bi; ++k) blk_mma<false, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
-                }
-                named_sync(2, kWyThreads);
-                if (ww < 4) {
-                    const int bi = 2 + (ww >> 1), bj = ww & 1;
-                    blk_store_y(acc, sc, 16 * bi, 16 * bj, -1.f, lane);
-                }
-            }
-            named_sync(2, kWyThreads);
+            invert_unit_lower(sc, wt, ww, lane);
             // ---- T = Y Diag(beta) -> bf16 MN-major B tile at the start of A_G
             {
                 const int i = wt >> 2, cs = (wt & 3) * 16;
@@ -481,7 +518,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = (half * 32 + j <= i) ? v[j] : 0.f;
             }
-            store_row32_bf16(base + OFF_KR, 128, row, half * 32, v);
+            if (GLA && PAIR && m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));   // peer done with n-2
+            store_row32_bf16_x2<GLA && PAIR>(base + OFF_KR, peer_base + OFF_ZIN, 128, row, half * 32, v);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -498,12 +536,13 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                     mma_bf16(c.tmem + TM_Z, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
                 mma_commit(c.bars + B_Z);
             }
-            wait_bar(c, B_Z, ph);
+            if (PAIR && m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));   // peer done with n-2
+            wait_bar(c, B_Z, phm);
             tc_fence_after();
             {
                 float v[32];
                 tmem_ld32(c.tmem + TM_Z + lane_base + half * 32, v);
-                store_row32_bf16(base + OFF_KR, 128, row, half * 32, v);
+                store_row32_bf16_x2<PAIR>(base + OFF_KR, peer_base + OFF_ZIN, 128, row, half * 32, v);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -523,21 +562,21 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(c.tmem + TM_WQ, desc_kmajor(a0, 128, ks), desc_mnmajor(bk, 64, ks), id, ks > 0);
             }
-            const uint32_t bv = smem_u32(base + (s ? OFF_V1 : OFF_V0));
+            const uint32_t bv = smem_u32(base + off_v(s));
             const uint32_t id = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(c.tmem + TM_D1 + s * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(bv, 64, ks), id, ks > 0);
             mma_commit(c.bars + B_W2);
         }
-        wait_bar(c, B_W2, ph);
+        wait_bar(c, B_W2, phm);
         tc_fence_after();
         if (leader && n + 2 < nchunks) issue_v(n + 2);           // v[s] consumed
-        if (n >= 1) wait_bar(c, B_C10 + ((n - 1) & 1), (uint32_t)(((n - 1) >> 1) & 1));   // A_chain free
+        if (n >= 2) wait_bar(c, B_C20 + s, (uint32_t)(((n - 2) >> 1) & 1));   // own scan done with slot s
 
-        // ---------------- A_chain = [-W ; Q<- - P W]  (K-major 128 x 128), 64 columns per thread
+        // ---------------- A_chain[s] = [-W ; Q<- - P W]  (K-major 128 x 128), 64 columns per thread
         {
-            uint8_t *ach = base + OFF_ACH;
+            uint8_t *ach = base + off_ach(s);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int col = half * 64 + cc * 32;
@@ -554,7 +593,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(base + OFF_AG + sw128_offset(128, row, col + 8 * q));
+                        const uint4 u =
+                            *reinterpret_cast<const uint4 *>(base + OFF_AG + sw128_offset(128, row, col + 8 * q));
                         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -567,14 +607,44 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 store_row32_bf16(ach, 128, row, col, v);
             }
         }
-        if (wt < kC && n + 1 < nchunks) {
-            betas[(s ^ 1) * kC + wt] = nb;
-            gss[(s ^ 1) * kC + wt] = ng;
+        // ---------------- K-> and gamma^C into slot s (and the other CTA's slot s)
+        {
+            const int cg = wt & 31, rg = wt >> 5;
+            const int col = 4 * cg;
+            uint8_t *kt = base + off_kt(s);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const uint32_t o64 = sw128_offset(64, rg * 8 + r, col);
+                st_u64(kt + o64, krv[r]);
+            }
+            if (rg == 0) *reinterpret_cast<float4 *>(gC + s * kDK + col) = gcv;
+        }
+        if (wt < kC && n + step < nchunks) {
+            betas[(sb ^ 1) * kC + wt] = nb;
+            gss[(sb ^ 1) * kC + wt] = ng;
         }
         fence_proxy_async_smem();
+        if (PAIR) {
+            // release this thread's Z rows written into the other CTA (long since performed)
+            fence_proxy_async_cluster();
+            mbar_arrive_remote_release(peer_base + OFF_MISC + MISC_BAR + 8u * B_RX);
+        }
         tc_fence_before();
         named_sync(2, kWyThreads);
-        if (leader) mbar_arrive(c.bars + B_WYR0 + s);
+        if (leader) {
+            mbar_arrive(c.bars + B_WYR0 + s);
+            if (n + step < nchunks) issue_raw(n + step);     // A_G and the K<- tile are free again
+            if (PAIR) {
+                // the slot buffers go to the other CTA's slot s by bulk copy; they are rewritten here
+                // only after that CTA has finished chunk n (checked before the next Z epilogue)
+                const uint32_t rbar = peer_base + OFF_MISC + MISC_BAR + 8u * B_RX;
+                const uint32_t gc_off = OFF_MISC + MISC_GC + (uint32_t)s * 512u;
+                mbar_arrive_expect_tx_remote(rbar, kSlotPushBytes);
+                bulk_copy_to_peer(peer_base + off_ach(s), base + off_ach(s), 32768u, rbar);
+                bulk_copy_to_peer(peer_base + off_kt(s), base + off_kt(s), 16384u, rbar);
+                bulk_copy_to_peer(peer_base + gc_off, base + gc_off, 512u, rbar);
+            }
+        }
     }
     // drain: every MMA this thread issued has completed before TMEM is freed
     if (leader) {
@@ -586,8 +656,9 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 // ============================================================================
 // Chain warps: the serial state scan and the output.
 // ============================================================================
-__device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_o, int e0, int h, int b,
-                           int nchunks) {
+template <bool PAIR>
+__device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_v, const CUtensorMap *tm_o,
+                           int e0, int h, int b, int nchunks) {
     uint8_t *base = c.base;
     const int j = threadIdx.x;                  // key channel == TMEM lane
     const int warp = j >> 5;
@@ -617,14 +688,29 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     for (int n = 0; n < nchunks; ++n) {
         const int s = n & 1;
         const uint32_t ph2 = (uint32_t)((n >> 1) & 1);
-        wait_bar(c, B_WYR0 + s, ph2);
+        const bool peer_chunk = PAIR && (n & 1) != (int)c.rank;
+        if (peer_chunk) {
+            // built by the other CTA: wait until its WY warps have written A_chain, K->, gamma^C
+            // and Z here, and for this slice's v; [U ; P U] = Z V goes right before the state product
+            if (leader) wait_bar(c, B_V0 + s, ph2);
+            wait_bar_cluster(c, B_RX, (uint32_t)((n >> 1) & 1));
+        } else {
+            wait_bar(c, B_WYR0 + s, ph2);
+        }
         tc_fence_after();
         const float gam = gC[s * kDK + j];
 
-        // ---- D1[s] += [-W ; Q'] S^T   (M128 N64 K128)
+        // ---- D1[s] (+)= [-W ; Q'] S^T   (M128 N64 K128)
         if (leader) {
-            const uint32_t a0 = smem_u32(base + OFF_ACH), b0 = smem_u32(base + OFF_ST);
             const uint32_t id = idesc_bf16(128, 64, 0, 1);
+            if (peer_chunk) {
+                const uint32_t az = smem_u32(base + OFF_ZIN), bv = smem_u32(base + off_v(s));
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(c.tmem + TM_D1 + s * 64, desc_kmajor(az, 128, ks), desc_mnmajor(bv, 64, ks), id,
+                             ks > 0);
+            }
+            const uint32_t a0 = smem_u32(base + off_ach(s)), b0 = smem_u32(base + OFF_ST);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16(c.tmem + TM_D1 + s * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 128, ks), id, 1);
@@ -632,50 +718,60 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
         }
         wait_bar(c, B_C10 + s, ph2);
         tc_fence_after();
+        if (peer_chunk && leader && n + 2 < nchunks) {
+            // v[s] has been read: fetch the slice of chunk n + 2
+            mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
+            tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, (n + 2) * kC, b);
+        }
 
-        // ---- rows 0-63: V_new -> bf16 MN-major B tile; rows 64-127: O -> staging tile
+        // ---- rows 0-63: V_new -> bf16 MN-major B tile in the first half of the S^T tile (its
+        //      product is done), then dS^T = K->^T V_new.  Rows 64-127: O -> staging tile.
         {
-            uint8_t *dst = base + OFF_ST + (warp < 2 ? 0u : 8192u);
             const int r = (warp & 1) * 32 + (j & 31);
+            uint8_t *dst = base + (warp < 2 ? OFF_ST : OFF_OST);
+            float v[32];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float r16[16];
-                tmem_ld16(c.tmem + TM_D1 + s * 64 + lane_base + cc * 16, r16);
-                st_u128(dst + sw128_offset(64, r, cc * 16), pack_bf16(r16[0], r16[1]), pack_bf16(r16[2], r16[3]),
-                        pack_bf16(r16[4], r16[5]), pack_bf16(r16[6], r16[7]));
-                st_u128(dst + sw128_offset(64, r, cc * 16 + 8), pack_bf16(r16[8], r16[9]),
-                        pack_bf16(r16[10], r16[11]), pack_bf16(r16[12], r16[13]), pack_bf16(r16[14], r16[15]));
+            for (int cc = 0; cc < 2; ++cc) {
+                tmem_ld32(c.tmem + TM_D1 + s * 64 + lane_base + cc * 32, v);
+                store_row32_bf16(dst, 64, r, cc * 32, v);
+            }
+            fence_proxy_async_smem();
+            if (warp < 2) {
+                named_sync(3, 64);
+                if (leader) {
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(base + off_kt(s)), b0 = smem_u32(base + OFF_ST);
+                    const uint32_t id = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(c.tmem + TM_S, desc_mnmajor(a0, 64, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
+                    mma_commit(c.bars + B_C20 + s);
+                }
             }
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         named_sync(1, kChainThreads);
-
         if (leader) {
             tc_fence_after();
             mbar_arrive(c.bars + B_E10 + s);                        // D1[s] drained
-            tma_store_4d(tm_o, base + OFF_ST + 8192, e0, h, n * kC, b);
+            tma_store_4d(tm_o, base + OFF_OST, e0, h, n * kC, b);
             tma_store_commit();
-            // ---- dS^T = K~^T V_new   (M128 N64 K64)
-            const uint32_t a0 = smem_u32(base + (s ? OFF_KT1 : OFF_KT0)), b0 = smem_u32(base + OFF_ST);
-            const uint32_t id = idesc_bf16(128, 64, 1, 1);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(c.tmem + TM_S, desc_mnmajor(a0, 64, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
-            mma_commit(c.bars + B_C20 + s);
         }
         wait_bar(c, B_C20 + s, ph2);
         tc_fence_after();
+        {
+            float v[32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            float r16[16];
-            tmem_ld16(c.tmem + TM_S + lane_base + cc * 16, r16);
+            for (int cc = 0; cc < 2; ++cc) {
+                tmem_ld32(c.tmem + TM_S + lane_base + cc * 32, v);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) S[cc * 16 + e] = fmaf(gam, S[cc * 16 + e], r16[e]);
+                for (int e = 0; e < 32; ++e) S[cc * 32 + e] = gam * (S[cc * 32 + e] + v[e]);
+            }
         }
-        if (leader) tma_store_wait_read0();
-        named_sync(1, kChainThreads);    // the staged O tile has been read
+        if (leader) tma_store_wait_read0();                       // staging tile free for the next chunk
         write_state();
+        if (peer_chunk && leader)                                  // done with the other CTA's chunk n
+            mbar_arrive_remote(map_to_rank(smem_u32(c.bars + B_PFREE), c.rank ^ 1u));
     }
     if (p.ht) {
 #pragma unroll
@@ -688,7 +784,7 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     }
 }
 
-template <int GATE, bool GLA, typename Tg>
+template <int GATE, bool GLA, bool PAIR, typename Tg>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
@@ -700,13 +796,14 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     c.bars = reinterpret_cast<uint64_t *>(base + OFF_MISC + MISC_BAR);
     c.abort = reinterpret_cast<volatile int *>(base + OFF_MISC + MISC_ABORT);
     c.status = p.status;
+    c.rank = PAIR ? cluster_ctarank() : 0u;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + OFF_MISC + MISC_TSLOT);
 
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
     const int nchunks = (p.T + kC - 1) / kC;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(c.bars + i, 1);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(c.bars + i, i == B_RX ? (uint32_t)kWyThreads + 1u : 1u);
         *c.abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -717,16 +814,18 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();           // the peer's barriers exist before any remote access
     tc_fence_after();
     c.tmem = *tslot;
 
     if (threadIdx.x < kChainThreads)
-        chain_role(c, p, &tm_o, e0, h, b, nchunks);
+        chain_role<PAIR>(c, p, &tm_v, &tm_o, e0, h, b, nchunks);
     else
-        wy_role<GATE, GLA, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, b, nchunks);
+        wy_role<GATE, GLA, PAIR, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, b, nchunks);
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();           // no remote access into a CTA that has exited
     tc_fence_after();
     if (threadIdx.x < 32) tmem_dealloc(c.tmem, kTmemCols);
 }
@@ -762,10 +861,29 @@ bool make_map(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t 
 template <int GATE, bool GLA, typename Tg>
 cudaError_t launch_variant(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
                            const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
-    auto kern = kda_fwd_tc_kernel<GATE, GLA, Tg>;
+    const bool pair = p.dv == 2 * kDVS;
+    dim3 grid(p.dv / kDVS, p.H, p.B);
+    if (pair) {
+        auto kern = kda_fwd_tc_kernel<GATE, GLA, true, Tg>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, p, q, k, g, v, o);
+    }
+    auto kern = kda_fwd_tc_kernel<GATE, GLA, false, Tg>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.dv / kDVS, p.H, p.B);
     kern<<<grid, kThreads, kSmemBytes, s>>>(p, q, k, g, v, o);
     return cudaGetLastError();
 }
@@ -773,7 +891,7 @@ cudaError_t launch_variant(const FwdParams &p, const CUtensorMap &q, const CUten
 }  // namespace
 
 cudaError_t launch_fwd_tc_bf16(const FwdParams &p, int g_is_bf16, cudaStream_t s) {
-    if (p.dk != kDK || p.dv % kDVS != 0) return cudaErrorNotSupported;
+    if (p.dk != kDK || (p.dv != kDVS && p.dv != 2 * kDVS)) return cudaErrorNotSupported;
     const bool gla = !p.scale_v;
     if (gla && p.has_beta) return cudaErrorNotSupported;     // unscaled v with a delta term: DPLR entry
     if (p.gate_kind == KDA_GATE_CHANNEL && !g_is_bf16) return cudaErrorNotSupported;
