@@ -52,6 +52,7 @@ constexpr int kDVS = 64;      // value channels per CTA
 constexpr int kChainThreads = 128;
 constexpr int kWyThreads = 256;
 constexpr int kThreads = kChainThreads + kWyThreads;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- shared memory map (byte offsets from a 1024-aligned base).  Operand
 // tiles are bf16 column blocks of 64 with 128-byte swizzle.
@@ -89,8 +90,8 @@ static_assert(OFF_OST + 8192 <= OFF_MISC, "tile layout");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 
-// bytes of the slot buffers one CTA copies into the other per chunk it builds
-constexpr uint32_t kSlotPushBytes = 32768 + 16384 + 512;
+// bytes one CTA sends the other per chunk it builds: Z (st.async) and the slot tiles (bulk copies)
+constexpr uint32_t kPushBytes = 16384 + 32768 + 16384 + 512;
 
 // ---- TMEM columns
 constexpr uint32_t TM_G = 0;      // Gram [L ; P], 64 cols
@@ -171,17 +172,18 @@ __device__ __forceinline__ void store_row32_bf16(uint8_t *tile, uint32_t rows, u
                 pack_bf16(v[8 * q + 6], v[8 * q + 7]));
 }
 
-// The same, also written to the other CTA of the pair at `remote` (its address of `tile`).
+// A row of Z (128 x 64 K-major tile): also sent to the other CTA of the pair at `remote`
+// (its address of `tile`) by asynchronous stores that complete on its barrier `rbar`.
 template <bool REMOTE>
-__device__ __forceinline__ void store_row32_bf16_x2(uint8_t *tile, uint32_t remote, uint32_t rows, uint32_t row,
-                                                    uint32_t col, const float *v) {
+__device__ __forceinline__ void store_row32_z(uint8_t *tile, uint32_t remote, uint32_t rbar, uint32_t row, uint32_t col,
+                                              const float *v) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint32_t off = sw128_offset(rows, row, col + 8 * q);
+        const uint32_t off = sw128_offset(128, row, col + 8 * q);
         const uint32_t a = pack_bf16(v[8 * q], v[8 * q + 1]), b = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
         const uint32_t c = pack_bf16(v[8 * q + 4], v[8 * q + 5]), d = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
         st_u128(tile + off, a, b, c, d);
-        if (REMOTE) st_cluster_u128(remote + off, a, b, c, d);
+        if (REMOTE) st_async_u128(remote + off, a, b, c, d, rbar);
     }
 }
 
@@ -243,32 +245,10 @@ __device__ __forceinline__ void zero_acc(float (&acc)[2][4]) {
         for (int e = 0; e < 4; ++e) acc[nh][e] = 0.f;
 }
 
-// Y = (I + L)^{-1} for the strictly lower L in the scratch, all 256 WY threads.
+// Y = (I + L)^{-1} for the strictly lower L in the scratch, all 256 WY threads,
+// given the inverses of the four 16x16 diagonal blocks already in Y.
 __device__ __forceinline__ void invert_unit_lower(const Scratch &sc, int wt, int ww, int lane) {
-    // level 0: the four 16x16 diagonal blocks, forward substitution, one column per thread
-    if (wt < 64) {
-        const int blk = wt >> 4, cl = wt & 15, o = blk * 16;
-        float y[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc0 = (r == cl) ? 1.f : 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int j4 = 0; j4 < r; j4 += 4) {
-                const float4 l4 = *reinterpret_cast<const float4 *>(sc.L(o + r, o + j4));
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (j4 + e < r) {
-                        if (e & 1) acc1 -= lv[e] * y[j4 + e];
-                        else acc0 -= lv[e] * y[j4 + e];
-                    }
-            }
-            y[r] = acc0 + acc1;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) *sc.Y(o + r, o + cl) = y[r];
-    }
-    named_sync(2, kWyThreads);
+    // level 0 (the diagonal 16x16 blocks) is done by the warps that load L
     // level 1 (block form 1 on 16x16 blocks): Y10 = -Y11 L10 Y00, Y32 = -Y33 L32 Y22
     if (ww < 2) {
         const int o = ww * 32;
@@ -429,19 +409,20 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 const float4 k4 = ld_bf16x4(base + OFF_KL + o64);
                 const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
                 const float bb = bet[row];
-                float ev[4], iv[4];
+                float kl[4], kr4[4], ql[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float gg = G[r][e] + pre[e];
-                    ev[e] = __expf(gg);
-                    iv[e] = __expf(-gg);
+                    const float g2 = (G[r][e] + pre[e]) * kLog2e;   // G in base-2 units
+                    const float ev = ex2_approx(g2), iv = ex2_approx(-g2);
+                    kl[e] = kv[e] * ev;
+                    kr4[e] = kv[e] * iv;
+                    ql[e] = qv[e] * ev;
                 }
-                const uint2 kr = pack4(kv[0] * iv[0], kv[1] * iv[1], kv[2] * iv[2], kv[3] * iv[3]);
-                st_u64(base + OFF_AG + otop,
-                       pack4(bb * kv[0] * ev[0], bb * kv[1] * ev[1], bb * kv[2] * ev[2], bb * kv[3] * ev[3]));
-                st_u64(base + OFF_AG + obot, pack4(qv[0] * ev[0], qv[1] * ev[1], qv[2] * ev[2], qv[3] * ev[3]));
+                const uint2 kr = pack4(kr4[0], kr4[1], kr4[2], kr4[3]);
+                st_u64(base + OFF_AG + otop, pack4(bb * kl[0], bb * kl[1], bb * kl[2], bb * kl[3]));
+                st_u64(base + OFF_AG + obot, pack4(ql[0], ql[1], ql[2], ql[3]));
                 st_u64(base + OFF_KR + o64, kr);
-                st_u64(base + OFF_KL + o64, pack4(kv[0] * ev[0], kv[1] * ev[1], kv[2] * ev[2], kv[3] * ev[3]));
+                st_u64(base + OFF_KL + o64, pack4(kl[0], kl[1], kl[2], kl[3]));
                 krv[r] = kr;
             }
         }
@@ -478,6 +459,32 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                     f.z = col + 2 < row ? v[4 * q + 2] : 0.f;
                     f.w = col + 3 < row ? v[4 * q + 3] : 0.f;
                     *reinterpret_cast<float4 *>(sc.L(row, col)) = f;
+                }
+                if (quarter == half) {
+                    // Level 0 of the inverse: this warp holds the two 16x16 diagonal blocks of its
+                    // 32 rows (one row per lane).  Row-wise forward substitution,
+                    // Y[r] = e_r - sum_{j<r} L[r][j] Y[j], rows of the block exchanged by shuffles.
+                    const int seg = lane >> 4, r = lane & 15;
+                    float lr[16], y[16];
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) {
+                        lr[cc] = seg ? v[16 + cc] : v[cc];
+                        y[cc] = (cc == r) ? 1.f : 0.f;
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 15; ++jj) {
+                        const float lj = (r > jj) ? lr[jj] : 0.f;
+#pragma unroll
+                        for (int cc = 0; cc <= jj; ++cc) {
+                            const float yj = __shfl_sync(0xffffffffu, y[cc], jj, 16);
+                            y[cc] -= lj * yj;
+                        }
+                    }
+                    const int o = quarter * 32 + seg * 16;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        *reinterpret_cast<float4 *>(sc.Y(row, o + 4 * c4)) =
+                            make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
                 }
             }
             named_sync(2, kWyThreads);
@@ -519,7 +526,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 for (int j = 0; j < 32; ++j) v[j] = (half * 32 + j <= i) ? v[j] : 0.f;
             }
             if (GLA && PAIR && m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));   // peer done with n-2
-            store_row32_bf16_x2<GLA && PAIR>(base + OFF_KR, peer_base + OFF_ZIN, 128, row, half * 32, v);
+            store_row32_z<GLA && PAIR>(base + OFF_KR, peer_base + OFF_ZIN,
+                                       peer_base + OFF_MISC + MISC_BAR + 8u * B_RX, row, half * 32, v);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -542,7 +550,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             {
                 float v[32];
                 tmem_ld32(c.tmem + TM_Z + lane_base + half * 32, v);
-                store_row32_bf16_x2<PAIR>(base + OFF_KR, peer_base + OFF_ZIN, 128, row, half * 32, v);
+                store_row32_z<PAIR>(base + OFF_KR, peer_base + OFF_ZIN, peer_base + OFF_MISC + MISC_BAR + 8u * B_RX,
+                                    row, half * 32, v);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -624,11 +633,6 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             gss[(sb ^ 1) * kC + wt] = ng;
         }
         fence_proxy_async_smem();
-        if (PAIR) {
-            // release this thread's Z rows written into the other CTA (long since performed)
-            fence_proxy_async_cluster();
-            mbar_arrive_remote_release(peer_base + OFF_MISC + MISC_BAR + 8u * B_RX);
-        }
         tc_fence_before();
         named_sync(2, kWyThreads);
         if (leader) {
@@ -639,7 +643,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 // only after that CTA has finished chunk n (checked before the next Z epilogue)
                 const uint32_t rbar = peer_base + OFF_MISC + MISC_BAR + 8u * B_RX;
                 const uint32_t gc_off = OFF_MISC + MISC_GC + (uint32_t)s * 512u;
-                mbar_arrive_expect_tx_remote(rbar, kSlotPushBytes);
+                mbar_arrive_expect_tx_remote(rbar, kPushBytes);
                 bulk_copy_to_peer(peer_base + off_ach(s), base + off_ach(s), 32768u, rbar);
                 bulk_copy_to_peer(peer_base + off_kt(s), base + off_kt(s), 16384u, rbar);
                 bulk_copy_to_peer(peer_base + gc_off, base + gc_off, 512u, rbar);
@@ -694,6 +698,7 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
             // and Z here, and for this slice's v; [U ; P U] = Z V goes right before the state product
             if (leader) wait_bar(c, B_V0 + s, ph2);
             wait_bar_cluster(c, B_RX, (uint32_t)((n >> 1) & 1));
+            fence_proxy_async_smem();    // the received tiles are read by the tensor core next
         } else {
             wait_bar(c, B_WYR0 + s, ph2);
         }
@@ -803,7 +808,7 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     const int nchunks = (p.T + kC - 1) / kC;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(c.bars + i, i == B_RX ? (uint32_t)kWyThreads + 1u : 1u);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(c.bars + i, 1);
         *c.abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();

@@ -113,6 +113,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t remote_bar
                  "r"(bytes)
                  : "memory");
 }
+// Asynchronous 16-byte store into another CTA's shared memory; its bytes
+// complete on that CTA's mbarrier `remote_bar` (st.async, complete_tx).
+__device__ __forceinline__ void st_async_u128(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                              uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+                 : "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -269,6 +278,13 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, uint32_t rows, ui
 // Descriptor of K-step `ks` of an MN-major tile with `krows` K rows.
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, uint32_t krows, uint32_t ks) {
     return sdesc_sw128(base + ks * 2048u, krows * 128u, 1024u);
+}
+
+// 2^x on the special-function unit (flush-to-zero), the exponential base of the gates.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
