@@ -7,10 +7,11 @@
 // product has M = 128 rows:
 //
 //   [beta K<- ; Q<-] K->^T      = [L ; P]          (Gram, one MMA)
-//   T  = (I + L_{strict})^{-1} Diag(beta)          (page "DeltaNet" 4.2,
-//        block form 1 applied twice: 16x16 diagonal blocks on CUDA cores,
-//        the off-diagonal blocks as tf32 warp MMAs)
-//   [I ; P] T                   = Z = [T ; P T]
+//   Z' (I + L_{strict}) = [I ; P],  Z = Z' Diag(beta) = [T ; P T]
+//        with T = (I + L)^{-1} Diag(beta): block back-substitution over
+//        16-column blocks (page "DeltaNet" 4.2, block form 2), the 16x16
+//        diagonal blocks inverted by warp shuffles, the block products as
+//        tf32 warp MMAs, 16 rows of Z' per warp
 //   Z K<-                       = [W ; P W]
 //   Z V                         = [U ; P U]        (into the accumulator D1)
 //   D1 += [-W ; Q<- - P W] S^T  = [V_new ; O]      (state-dependent, one MMA)
@@ -58,8 +59,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // tiles are bf16 column blocks of 64 with 128-byte swizzle.
 constexpr uint32_t OFF_AG = 0;           // [beta K<- ; Q<-] 128 x 128 K-major.  Raw g lands in its
                                          // rows 0-63 and raw q in rows 64-127; after the Gram,
-                                         // rows 0-63 hold Y (fp32) and then T.
-constexpr uint32_t OFF_KR = 32768;       // K-> 64 x 128 (K-major B); then L (fp32), [I;P], Z
+                                         // rows 0-63 hold the diagonal-block inverses (fp32).
+constexpr uint32_t OFF_KR = 32768;       // K-> 64 x 128 (K-major B); then L (fp32), then Z
 constexpr uint32_t OFF_KL = 49152;       // raw k, then K<- 64 x 128 (MN-major B)
 constexpr uint32_t OFF_V0 = 65536;       // v slice [64][64] (MN-major B), slot 0
 constexpr uint32_t OFF_V1 = 73728;       // slot 1
@@ -95,7 +96,6 @@ constexpr uint32_t kPushBytes = 16384 + 32768 + 16384 + 512;
 
 // ---- TMEM columns
 constexpr uint32_t TM_G = 0;      // Gram [L ; P], 64 cols
-constexpr uint32_t TM_Z = 64;     // Z, 64 cols
 constexpr uint32_t TM_WQ = 128;   // [W ; P W], 128 cols
 constexpr uint32_t TM_D1 = 256;   // [U ; P U] -> [V_new ; O], 2 slots x 64 cols
 constexpr uint32_t TM_S = 384;    // dS^T, 64 cols
@@ -103,7 +103,7 @@ constexpr uint32_t kTmemCols = 512;
 
 // mbarrier indices
 enum {
-    B_RAW = 0, B_V0, B_V1, B_GRAM, B_Z, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
+    B_RAW = 0, B_V0, B_V1, B_GRAM, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
     B_RX, B_PFREE, B_FIN0, B_FIN1, kNumBars
 };
 static_assert(kNumBars <= 24, "mbarrier slots");
@@ -208,77 +208,23 @@ struct Scratch {
     }
 };
 
-// acc (16x16 as two 16x8 halves) += X[rx:rx+16, cx:cx+16] * Z[rz:rz+16, cz:cz+16], tf32 tensor cores.
-template <bool XL, bool ZL>
-__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const Scratch &sc, int rx, int cx, int rz, int cz,
-                                        int lane) {
+// Accumulator fragments of a 16x16 block (two 16x8 halves) -> tf32 A fragments of the
+// same block (k-steps 0 and 1), times `sign`, by shuffles within the warp.
+__device__ __forceinline__ void frag_c_to_a(const float (&x)[2][4], uint32_t (&a)[2][4], int lane, float sign) {
     const int g = lane >> 2, t = lane & 3;
-    auto X = [&](int i, int j) { return XL ? *sc.L(i, j) : *sc.Y(i, j); };
-    auto Z = [&](int i, int j) { return ZL ? *sc.L(i, j) : *sc.Y(i, j); };
+    const int s0 = 4 * g + (t >> 1), s1 = s0 + 2;
+    const bool odd = (t & 1) != 0;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t a[4] = {to_tf32(X(rx + g, cx + 8 * ks + t)), to_tf32(X(rx + g + 8, cx + 8 * ks + t)),
-                               to_tf32(X(rx + g, cx + 8 * ks + t + 4)), to_tf32(X(rx + g + 8, cx + 8 * ks + t + 4))};
-#pragma unroll
-        for (int nh = 0; nh < 2; ++nh) {
-            const uint32_t bb[2] = {to_tf32(Z(rz + 8 * ks + t, cz + 8 * nh + g)),
-                                    to_tf32(Z(rz + 8 * ks + t + 4, cz + 8 * nh + g))};
-            mma_tf32_16x8x8(acc[nh], a, bb);
-        }
+        const float v0 = __shfl_sync(0xffffffffu, x[ks][0], s0), v1 = __shfl_sync(0xffffffffu, x[ks][1], s0);
+        const float v2 = __shfl_sync(0xffffffffu, x[ks][2], s0), v3 = __shfl_sync(0xffffffffu, x[ks][3], s0);
+        const float w0 = __shfl_sync(0xffffffffu, x[ks][0], s1), w1 = __shfl_sync(0xffffffffu, x[ks][1], s1);
+        const float w2 = __shfl_sync(0xffffffffu, x[ks][2], s1), w3 = __shfl_sync(0xffffffffu, x[ks][3], s1);
+        a[ks][0] = to_tf32(sign * (odd ? v1 : v0));
+        a[ks][1] = to_tf32(sign * (odd ? v3 : v2));
+        a[ks][2] = to_tf32(sign * (odd ? w1 : w0));
+        a[ks][3] = to_tf32(sign * (odd ? w3 : w2));
     }
-}
-__device__ __forceinline__ void blk_store_y(const float (&acc)[2][4], const Scratch &sc, int r0, int c0, float sign,
-                                            int lane) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nh = 0; nh < 2; ++nh) {
-        *sc.Y(r0 + g, c0 + 8 * nh + 2 * t) = sign * acc[nh][0];
-        *sc.Y(r0 + g, c0 + 8 * nh + 2 * t + 1) = sign * acc[nh][1];
-        *sc.Y(r0 + g + 8, c0 + 8 * nh + 2 * t) = sign * acc[nh][2];
-        *sc.Y(r0 + g + 8, c0 + 8 * nh + 2 * t + 1) = sign * acc[nh][3];
-    }
-}
-__device__ __forceinline__ void zero_acc(float (&acc)[2][4]) {
-#pragma unroll
-    for (int nh = 0; nh < 2; ++nh)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nh][e] = 0.f;
-}
-
-// Y = (I + L)^{-1} for the strictly lower L in the scratch, all 256 WY threads,
-// given the inverses of the four 16x16 diagonal blocks already in Y.
-__device__ __forceinline__ void invert_unit_lower(const Scratch &sc, int wt, int ww, int lane) {
-    // level 0 (the diagonal 16x16 blocks) is done by the warps that load L
-    // level 1 (block form 1 on 16x16 blocks): Y10 = -Y11 L10 Y00, Y32 = -Y33 L32 Y22
-    if (ww < 2) {
-        const int o = ww * 32;
-        float acc[2][4];
-        zero_acc(acc);
-        blk_mma<true, false>(acc, sc, o + 16, o, o, o, lane);              // M = L10 Y00
-        __syncwarp();
-        blk_store_y(acc, sc, o + 16, o, 1.f, lane);
-        __syncwarp();
-        zero_acc(acc);
-        blk_mma<false, false>(acc, sc, o + 16, o + 16, o + 16, o, lane);   // Y11 M
-        __syncwarp();
-        blk_store_y(acc, sc, o + 16, o, -1.f, lane);
-    }
-    named_sync(2, kWyThreads);
-    // level 2 (block form 1 on 32x32 blocks): Y_BL = -Y_BB (L_BL Y_TT)
-    float acc[2][4];
-    zero_acc(acc);
-    const int bi = 2 + (ww >> 1), bj = ww & 1;   // output block of warps 0-3
-    if (ww < 4)
-        for (int k = bj; k < 2; ++k) blk_mma<true, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
-    named_sync(2, kWyThreads);
-    if (ww < 4) blk_store_y(acc, sc, 16 * bi, 16 * bj, 1.f, lane);
-    named_sync(2, kWyThreads);
-    zero_acc(acc);
-    if (ww < 4)
-        for (int k = 2; k <= bi; ++k) blk_mma<false, false>(acc, sc, 16 * bi, 16 * k, 16 * k, 16 * bj, lane);
-    named_sync(2, kWyThreads);
-    if (ww < 4) blk_store_y(acc, sc, 16 * bi, 16 * bj, -1.f, lane);
-    named_sync(2, kWyThreads);
 }
 
 // ============================================================================
@@ -488,75 +434,109 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 }
             }
             named_sync(2, kWyThreads);
-            invert_unit_lower(sc, wt, ww, lane);
-            // ---- T = Y Diag(beta) -> bf16 MN-major B tile at the start of A_G
-            {
-                const int i = wt >> 2, cs = (wt & 3) * 16;
-                float t[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 y4 = *reinterpret_cast<const float4 *>(sc.Y(i, cs + 4 * q));
-                    const float4 b4 = *reinterpret_cast<const float4 *>(bet + cs + 4 * q);
-                    const int c0 = cs + 4 * q;
-                    t[4 * q + 0] = c0 + 0 <= i ? y4.x * b4.x : 0.f;
-                    t[4 * q + 1] = c0 + 1 <= i ? y4.y * b4.y : 0.f;
-                    t[4 * q + 2] = c0 + 2 <= i ? y4.z * b4.z : 0.f;
-                    t[4 * q + 3] = c0 + 3 <= i ? y4.w * b4.w : 0.f;
-                }
-                named_sync(2, kWyThreads);
-                uint8_t *tt = base + OFF_AG;
-                st_u128(tt + sw128_offset(64, i, cs), pack_bf16(t[0], t[1]), pack_bf16(t[2], t[3]),
-                        pack_bf16(t[4], t[5]), pack_bf16(t[6], t[7]));
-                st_u128(tt + sw128_offset(64, i, cs + 8), pack_bf16(t[8], t[9]), pack_bf16(t[10], t[11]),
-                        pack_bf16(t[12], t[13]), pack_bf16(t[14], t[15]));
-            }
-            named_sync(2, kWyThreads);   // L reads finished before [I;P] overwrites it
         }
 
-        // ---- [I ; P] into the K-> tile (K-major, 128 rows x 64): for GLA this is Z itself
+        // ---------------- Z' (I + L) = [I ; P] by block back-substitution over 16-column blocks,
+        // 16 rows of Z' per warp: Z'_b = ([I ; P]_b - sum_{b' > b} Z'_{b'} L_{b'b}) Y_bb with
+        // Y_bb = (I + L_bb)^{-1} (block form 2 of page "DeltaNet" 4.2, on the transposed system).
+        // Then Z = Z' Diag(beta) = [T ; P T].  For GLA (beta = 0, v unscaled) Z = [I ; P].
+        float zb[4][2][4];                                     // Z' blocks, accumulator-fragment layout
+        const int r0 = quarter * 32 + half * 16;               // first row of Z' owned by this warp
         {
-            float v[32];
-            if (quarter < 2) {
+            const int g = lane >> 2, t = lane & 3;
+            uint32_t za[4][2][4];                              // -Z' blocks as tf32 A fragments
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = (half * 32 + j == row) ? 1.f : 0.f;
-            } else {
-                const int i = row - 64;
-                tmem_ld32(c.tmem + TM_G + lane_base + half * 32, v);
+            for (int bb = 3; bb >= 0; --bb) {
+                float acc[2][4];
+                if (quarter < 2) {                             // identity rows
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = (half * 32 + j <= i) ? v[j] : 0.f;
+                    for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc[nh][e] = (r0 + g + 8 * (e >> 1) == 16 * bb + 8 * nh + 2 * t + (e & 1)) ? 1.f : 0.f;
+                } else {                                       // rows of P = Q<- K->^T * M (inclusive)
+                    float pv[8];
+                    tmem_ld16x256b_x2(c.tmem + TM_G + ((uint32_t)r0 << 16) + 16 * bb, pv);
+                    const int i0 = r0 - 64;
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc[nh][e] = (16 * bb + 8 * nh + 2 * t + (e & 1) <= i0 + g + 8 * (e >> 1)) ? pv[4 * nh + e]
+                                                                                                      : 0.f;
+                }
+                if (!GLA) {
+#pragma unroll
+                    for (int bp = bb + 1; bp < 4; ++bp)
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                            for (int nh = 0; nh < 2; ++nh) {
+                                const uint32_t bf[2] = {to_tf32(*sc.L(16 * bp + 8 * ks + t, 16 * bb + 8 * nh + g)),
+                                                        to_tf32(*sc.L(16 * bp + 8 * ks + t + 4, 16 * bb + 8 * nh + g))};
+                                mma_tf32_16x8x8(acc[nh], za[bp][ks], bf);
+                            }
+                    uint32_t af[2][4];
+                    frag_c_to_a(acc, af, lane, 1.f);
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) zb[bb][nh][e] = 0.f;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                        for (int nh = 0; nh < 2; ++nh) {
+                            const uint32_t bf[2] = {to_tf32(*sc.Y(16 * bb + 8 * ks + t, 16 * bb + 8 * nh + g)),
+                                                    to_tf32(*sc.Y(16 * bb + 8 * ks + t + 4, 16 * bb + 8 * nh + g))};
+                            mma_tf32_16x8x8(zb[bb][nh], af[ks], bf);
+                        }
+                    if (bb > 0) frag_c_to_a(zb[bb], za[bb], lane, -1.f);
+                } else {
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) zb[bb][nh][e] = acc[nh][e];
+                }
             }
-            if (GLA && PAIR && m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));   // peer done with n-2
-            store_row32_z<GLA && PAIR>(base + OFF_KR, peer_base + OFF_ZIN,
-                                       peer_base + OFF_MISC + MISC_BAR + 8u * B_RX, row, half * 32, v);
+        }
+        if (!GLA) named_sync(2, kWyThreads);                   // every warp is done with L in the K-> tile
+        // ---------------- Z = Z' Diag(beta) -> bf16 K-major 128 x 64 tile in the K-> tile
+        {
+            const int g = lane >> 2, t = lane & 3;
+            uint8_t *zt = base + OFF_KR;
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh) {
+                    const int c0 = 16 * bb + 8 * nh + 2 * t;
+                    float b0 = 1.f, b1 = 1.f;
+                    if (!GLA) {
+                        const float2 b2 = *reinterpret_cast<const float2 *>(bet + c0);
+                        b0 = b2.x;
+                        b1 = b2.y;
+                    }
+                    *reinterpret_cast<uint32_t *>(zt + sw128_offset(128, r0 + g, c0)) =
+                        pack_bf16(zb[bb][nh][0] * b0, zb[bb][nh][1] * b1);
+                    *reinterpret_cast<uint32_t *>(zt + sw128_offset(128, r0 + g + 8, c0)) =
+                        pack_bf16(zb[bb][nh][2] * b0, zb[bb][nh][3] * b1);
+                }
+            if (PAIR) {
+                // the other CTA forms its own [U ; P U] = Z V: send this warp's 16 rows of Z
+                if (m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));   // it is done with n - 2
+                __syncwarp();
+                const uint32_t rbar = peer_base + OFF_MISC + MISC_BAR + 8u * B_RX;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int id = lane + 32 * k4;
+                    const uint32_t off = sw128_offset(128, r0 + (id >> 3), (id & 7) * 8);
+                    const uint4 u = *reinterpret_cast<const uint4 *>(zt + off);
+                    st_async_u128(peer_base + OFF_ZIN + off, u.x, u.y, u.z, u.w, rbar);
+                }
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         named_sync(2, kWyThreads);
-
-        if (!GLA) {
-            // ---------------- Z = [I ; P] T   (M128 N64 K64)
-            if (leader) {
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(base + OFF_KR), b0 = smem_u32(base + OFF_AG);
-                const uint32_t id = idesc_bf16(128, 64, 0, 1);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(c.tmem + TM_Z, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
-                mma_commit(c.bars + B_Z);
-            }
-            if (PAIR && m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));   // peer done with n-2
-            wait_bar(c, B_Z, phm);
-            tc_fence_after();
-            {
-                float v[32];
-                tmem_ld32(c.tmem + TM_Z + lane_base + half * 32, v);
-                store_row32_z<PAIR>(base + OFF_KR, peer_base + OFF_ZIN, peer_base + OFF_MISC + MISC_BAR + 8u * B_RX,
-                                    row, half * 32, v);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_sync(2, kWyThreads);
-        }
 
         // ---------------- Z K<- -> [W ; P W],  Z V -> D1[s] = [U ; P U]
         if (leader) {

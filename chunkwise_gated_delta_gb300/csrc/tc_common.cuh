@@ -220,6 +220,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
         : "memory");
 }
 
+// 16 lanes x 256 bit, twice (16 rows x 16 columns of 32 bit), delivered in the
+// accumulator-fragment layout of mma.m16n8: with g = lane / 4, t = lane % 4,
+// r[4h + {0,1,2,3}] = (row g, col 8h+2t), (g, 8h+2t+1), (g+8, 8h+2t), (g+8, 8h+2t+1).
+__device__ __forceinline__ void tmem_ld16x256b_x2(uint32_t taddr, float (&r)[8]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+        : "r"(taddr)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- warp-level tf32 MMA
 // m16n8k8, A row-major 16x8, B column-major 8x8, fp32 accumulate.  With g = lane / 4
 // and t = lane % 4: a = {A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]},
