@@ -127,7 +127,7 @@ __device__ __forceinline__ void record_timeout(const Ctx &c) {
 }
 
 // Bounded wait that becomes a no-op once any thread of the CTA has given up.
-__device__ __forceinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
+__device__ __noinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
     uint64_t *bar = c.bars + idx;
     for (uint32_t i = 0; i < kWaitBound; ++i) {
         if (mbar_try_wait(bar, parity)) return;
@@ -136,7 +136,7 @@ __device__ __forceinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity)
     record_timeout(c);
 }
 // The same for barriers completed from the other CTA of the pair.
-__device__ __forceinline__ void wait_bar_cluster(const Ctx &c, int idx, uint32_t parity) {
+__device__ __noinline__ void wait_bar_cluster(const Ctx &c, int idx, uint32_t parity) {
     uint64_t *bar = c.bars + idx;
     for (uint32_t i = 0; i < kWaitBound; ++i) {
         if (mbar_try_wait_cluster(bar, parity)) return;
