@@ -137,6 +137,84 @@ def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, sca
     return o, ht
 
 
+def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None,
+                   workspace=None) -> _lib.DplrFwdArgs:
+    """Fill the C DPLR argument struct from tensors (q, k, v, o may be None for the norm report)."""
+    B, T, H, dk = a.shape
+    dv = v.shape[-1] if v is not None else 0
+    if gate is None:
+        gate = "none" if g is None else ("scalar" if g.dim() == 3 else "channel")
+    x = _lib.DplrFwdArgs()
+    x.B, x.T, x.H, x.dk, x.dv, x.chunk = B, T, H, dk, dv, 0
+    x.dtype = _dtype_code(a)
+    x.gate_kind = _GATES[gate]
+    x.g_dtype = _dtype_code(g) if g is not None else _lib.KDA_BF16
+    x.q, x.k, x.v, x.a, x.b, x.g = _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(g)
+    x.h0, x.o, x.ht = _ptr(h0), _ptr(o), _ptr(ht)
+    if workspace is not None:
+        x.workspace = _ptr(workspace)
+        x.workspace_bytes = workspace.numel() * workspace.element_size()
+    return x
+
+
+def dplr_chunk_fwd(q, k, v, a, b, g=None, h0=None, *, gate=None, output_final_state=True,
+                   o=None, ht=None, workspace=None, stream=None):
+    """General gated DPLR forward through ``dplr_chunk_fwd`` of the C ABI.
+
+    q, k, a, b: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, one dtype);
+    g: log-decay [B, T, H, dk], [B, T, H] or None; h0: [B, H, dv, dk] fp32 or None.
+    Returns (o [B, T, H, dv] in q's dtype, ht [B, H, dv, dk] fp32 or None).
+    """
+    lib = _lib.load()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (g, "g"), (h0, "h0")):
+        _check(t, name)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    if ht is None and output_final_state:
+        ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device)
+    args = make_dplr_args(q, k, v, a, b, g, h0, o, ht, gate=gate)
+    need = lib.dplr_chunk_fwd_workspace(ctypes.byref(args))
+    if need == 0:
+        rc = lib.dplr_chunk_fwd(ctypes.byref(args), None)
+        raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "dplr_chunk_fwd")
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    args.workspace = _ptr(workspace)
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = lib.dplr_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.KDA_OK:
+        raise KdaError(rc, "dplr_chunk_fwd")
+    return o, ht
+
+
+def dplr_factor_norms(a, b, g=None, *, gate=None, stream=None):
+    """Per-token transition norms through ``dplr_factor_norms`` of the C ABI.
+
+    Returns (rho [B, T, H], norm [B, T, H], maxes [2]) float32 on a's device:
+    rho = ||I - b a^T||_2 by the closed form, norm = ||Diag(alpha)(I - b a^T)||_2,
+    maxes = (max rho, max norm).
+    """
+    lib = _lib.load()
+    for t, name in ((a, "a"), (b, "b"), (g, "g")):
+        _check(t, name)
+    B, T, H, _ = a.shape
+    rho = torch.empty(B, T, H, dtype=torch.float32, device=a.device)
+    nrm = torch.empty_like(rho)
+    maxes = torch.empty(4, dtype=torch.float32, device=a.device)
+    args = make_dplr_args(None, None, None, a, b, g, gate=gate)
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    rc = lib.dplr_factor_norms(ctypes.byref(args), _ptr(rho), _ptr(nrm), _ptr(maxes),
+                               ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.KDA_OK:
+        raise KdaError(rc, "dplr_factor_norms")
+    return rho, nrm, maxes[:2]
+
+
 def status_read(workspace=None, device=None, stream=None) -> int:
     """Device status word of the workspace (waits for the stream, then clears it)."""
     lib = _lib.load()

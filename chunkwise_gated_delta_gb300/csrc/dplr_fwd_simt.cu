@@ -1,0 +1,366 @@
+// float32 CUDA-core kernels for the general gated DPLR recurrence
+//
+//     S_t = S_{t-1} Diag(alpha_t) (I - b_t a_t^T) + v_t k_t^T,   o_t = S_t q_t
+//
+// (page "Diagonal Plus Low Rank", section 2), evaluated in the chunk form
+// that page derives.  Per chunk [t] (length C = 32, so every tile of a
+// (value slice, head, batch) fits in shared memory; the chunk length does not
+// change the result):
+//
+//   Gamma = exp(in-chunk cumsum g);  Q<- = Q*Gamma, K-> = K/Gamma,
+//   A-> = A/Gamma, B<- = B*Gamma;
+//   E = (I + (B<- A->^T * M_{-1}))^{-1};   W = E B<-;
+//   C = -E (B<- K->^T * M_{-1}) V;          X = C - W S^T;
+//   O = Q<- S^T + (Q<- K->^T * M) V + (Q<- A->^T * M) X;
+//   S <- (S + V^T K-> + X^T A->) Diag(gamma^C).
+//
+// Also the per-token transition norms of page "How to make GDN2 more stable":
+// eq. (4) for I - b a^T, and the largest singular value of the full factor
+// Diag(alpha)(I - b a^T), for which the page has no closed form, by
+// bisection on inertia counts of its Gram matrix.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kC = 32;      // chunk length
+constexpr int kDVS = 32;    // value channels per CTA
+constexpr int kThreads = 256;
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+template <int DK, typename Tin, typename Tg>
+__global__ void __launch_bounds__(kThreads)
+dplr_fwd_simt_kernel(const DplrParams p) {
+    constexpr int SK = DK + 1;     // padded row stride of [C][DK] tiles
+    constexpr int SC = kC + 1;     // padded row stride of [C][C] tiles
+    constexpr int SV = kDVS + 1;
+    extern __shared__ float smem[];
+    float *Ql = smem;                 // [C][SK]
+    float *Kr = Ql + kC * SK;         // [C][SK]
+    float *Ar = Kr + kC * SK;         // [C][SK]
+    float *Bl = Ar + kC * SK;         // [C][SK]
+    float *Wm = Bl + kC * SK;         // [C][SK]
+    float *Lab = Wm + kC * SK;        // [C][SC]  B<- A->^T * M_{-1}
+    float *Lbk = Lab + kC * SC;       // [C][SC]  B<- K->^T * M_{-1}
+    float *Pk = Lbk + kC * SC;        // [C][SC]  Q<- K->^T * M
+    float *Pa = Pk + kC * SC;         // [C][SC]  Q<- A->^T * M
+    float *Em = Pa + kC * SC;         // [C][SC]  E
+    float *Vm = Em + kC * SC;         // [C][SV]  v slice
+    float *Tm = Vm + kC * SV;         // [C][SV]  (B<- K->^T * M_{-1}) V
+    float *Xm = Tm + kC * SV;         // [C][SV]  X
+    float *Sm = Xm + kC * SV;         // [DVS][SK] state slice
+    float *gC = Sm + kDVS * SK;       // [DK]
+
+    const int tid = threadIdx.x;
+    const int e0 = blockIdx.x * kDVS;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, H = p.H, dv = p.dv;
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    const Tin *a = static_cast<const Tin *>(p.a);
+    const Tin *bb = static_cast<const Tin *>(p.b);
+    const Tg *g = static_cast<const Tg *>(p.g);
+    Tin *o = static_cast<Tin *>(p.o);
+
+    for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+        const int e = idx / DK, d = idx % DK;
+        Sm[e * SK + d] = p.h0 ? p.h0[(((size_t)b * H + h) * dv + e0 + e) * DK + d] : 0.f;
+    }
+
+    for (int t0 = 0; t0 < T; t0 += kC) {
+        const int nvalid = min(kC, T - t0);
+        __syncthreads();
+        // ---- Gamma and the rescaled tiles, one key channel per thread
+        if (tid < DK) {
+            const int d = tid;
+            float G = 0.f, gam = 1.f;
+            for (int c = 0; c < kC; ++c) {
+                float qv = 0.f, kv = 0.f, av = 0.f, bv = 0.f;
+                if (c < nvalid) {
+                    const size_t row = ((size_t)b * T + t0 + c) * H + h;
+                    qv = to_f(q[row * DK + d]);
+                    kv = to_f(k[row * DK + d]);
+                    av = to_f(a[row * DK + d]);
+                    bv = to_f(bb[row * DK + d]);
+                    if (p.gate_kind == KDA_GATE_CHANNEL) G += to_f(g[row * DK + d]);
+                    else if (p.gate_kind == KDA_GATE_SCALAR) G += to_f(g[row]);
+                    gam = expf(G);
+                }
+                Ql[c * SK + d] = qv * gam;
+                Kr[c * SK + d] = kv / gam;
+                Ar[c * SK + d] = av / gam;
+                Bl[c * SK + d] = bv * gam;
+            }
+            gC[d] = gam;
+        }
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            const int c = idx / kDVS, e = idx % kDVS;
+            Vm[c * SV + e] = c < nvalid ? to_f(v[(((size_t)b * T + t0 + c) * H + h) * dv + e0 + e]) : 0.f;
+        }
+        __syncthreads();
+        // ---- the four chunk Gram matrices
+        for (int idx = tid; idx < kC * kC; idx += kThreads) {
+            const int i = idx / kC, j = idx % kC;
+            float lab = 0.f, lbk = 0.f, pk = 0.f, pa = 0.f;
+            if (j <= i) {
+                for (int d = 0; d < DK; ++d) {
+                    const float kr = Kr[j * SK + d], ar = Ar[j * SK + d];
+                    const float bl = Bl[i * SK + d], ql = Ql[i * SK + d];
+                    lab += bl * ar;
+                    lbk += bl * kr;
+                    pk += ql * kr;
+                    pa += ql * ar;
+                }
+            }
+            Lab[i * SC + j] = j < i ? lab : 0.f;
+            Lbk[i * SC + j] = j < i ? lbk : 0.f;
+            Pk[i * SC + j] = pk;
+            Pa[i * SC + j] = pa;
+        }
+        __syncthreads();
+        // ---- E = (I + Lab)^{-1}: column c by forward substitution
+        if (tid < kC) {
+            const int c = tid;
+            for (int i = 0; i < kC; ++i) {
+                float y = 0.f;
+                if (i == c) y = 1.f;
+                else if (i > c)
+                    for (int j = c; j < i; ++j) y -= Lab[i * SC + j] * Em[j * SC + c];
+                Em[i * SC + c] = y;
+            }
+        }
+        // ---- Lbk V (independent of E)
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            const int i = idx / kDVS, e = idx % kDVS;
+            float acc = 0.f;
+            for (int j = 0; j < i; ++j) acc += Lbk[i * SC + j] * Vm[j * SV + e];
+            Tm[i * SV + e] = acc;
+        }
+        __syncthreads();
+        // ---- W = E B<-,  C = -E (Lbk V)  (C is kept in X for now)
+        for (int idx = tid; idx < kC * DK; idx += kThreads) {
+            const int i = idx / DK, d = idx % DK;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j) acc += Em[i * SC + j] * Bl[j * SK + d];
+            Wm[i * SK + d] = acc;
+        }
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            const int i = idx / kDVS, e = idx % kDVS;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j) acc -= Em[i * SC + j] * Tm[j * SV + e];
+            Xm[i * SV + e] = acc;
+        }
+        __syncthreads();
+        // ---- X = C - W S^T
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            const int i = idx / kDVS, e = idx % kDVS;
+            float acc = Xm[i * SV + e];
+            for (int d = 0; d < DK; ++d) acc -= Wm[i * SK + d] * Sm[e * SK + d];
+            Xm[i * SV + e] = acc;
+        }
+        __syncthreads();
+        // ---- O = Q<- S^T + (Q<- K->^T * M) V + (Q<- A->^T * M) X
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            const int i = idx / kDVS, e = idx % kDVS;
+            float acc = 0.f;
+            for (int d = 0; d < DK; ++d) acc += Ql[i * SK + d] * Sm[e * SK + d];
+            for (int j = 0; j <= i; ++j) acc += Pk[i * SC + j] * Vm[j * SV + e] + Pa[i * SC + j] * Xm[j * SV + e];
+            if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = from_f<Tin>(acc);
+        }
+        __syncthreads();
+        // ---- S <- (S + V^T K-> + X^T A->) Diag(gamma^C)
+        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+            const int e = idx / DK, d = idx % DK;
+            float acc = Sm[e * SK + d];
+            for (int c = 0; c < kC; ++c) acc += Vm[c * SV + e] * Kr[c * SK + d] + Xm[c * SV + e] * Ar[c * SK + d];
+            Sm[e * SK + d] = acc * gC[d];
+        }
+    }
+    __syncthreads();
+    if (p.ht) {
+        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+            const int e = idx / DK, d = idx % DK;
+            p.ht[(((size_t)b * H + h) * dv + e0 + e) * DK + d] = Sm[e * SK + d];
+        }
+    }
+}
+
+template <int DK>
+constexpr size_t dplr_smem_bytes() {
+    return sizeof(float) * (size_t)(5 * kC * (DK + 1) + 5 * kC * (kC + 1) + 3 * kC * (kDVS + 1) +
+                                    kDVS * (DK + 1) + DK);
+}
+
+template <int DK, typename Tin, typename Tg>
+cudaError_t launch_dk(const DplrParams &p, cudaStream_t s) {
+    const size_t smem = dplr_smem_bytes<DK>();
+    cudaError_t e = cudaFuncSetAttribute(dplr_fwd_simt_kernel<DK, Tin, Tg>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.dv / kDVS, p.H, p.B);
+    dplr_fwd_simt_kernel<DK, Tin, Tg><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tg>
+cudaError_t launch_typed(const DplrParams &p, cudaStream_t s) {
+    if (p.dk == 64) return launch_dk<64, Tin, Tg>(p, s);
+    if (p.dk == 128) return launch_dk<128, Tin, Tg>(p, s);
+    return cudaErrorNotSupported;
+}
+
+// ---------------------------------------------------------------- factor norms
+// One warp per token; lane l holds channels l, l+32, l+64, l+96 (dk <= 128).
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+    return x;
+}
+
+// Largest singular value of M = D - u a^T with D = Diag(alpha), u = D b.
+// M^T M = D^2 + P K P^T with P = [a, r], r = D u, K = [[s, -1], [-1, 0]],
+// s = u^T u: a diagonal matrix plus a rank-2 term of either sign.  For a
+// shift lambda that is no alpha_i^2, Haynsworth's inertia additivity applied
+// to [[D^2 - lambda, P], [P^T, -K^{-1}]] counts the eigenvalues of M^T M
+// above lambda:
+//     #{i : alpha_i^2 > lambda} + pos(N) - pos(-K^{-1}),
+//     N = -K^{-1} - P^T (D^2 - lambda)^{-1} P = [[-R11, 1 - R12], [1 - R12, s - R22]],
+// with pos(-K^{-1}) = 1 (its determinant is -1).  The count is monotone in
+// lambda, so bisection on "count >= 1" over [0, (max alpha + |u||a|)^2]
+// brackets the largest eigenvalue (the spectral-bisection method of Sturm
+// counts, with the count taken from the inertia of a 2x2 matrix).
+template <int R>
+__device__ float factor_norm_inertia(const float (&av)[R], const float (&al)[R], const float (&bv)[R]) {
+    float r[R], d2[R];
+    float dmax = 0.f, su = 0.f, sa = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const float u = al[i] * bv[i];
+        r[i] = al[i] * u;
+        d2[i] = al[i] * al[i];
+        dmax = fmaxf(dmax, al[i]);
+        su += u * u;
+        sa += av[i] * av[i];
+    }
+    dmax = warp_max(dmax);
+    const float s = warp_sum(su);
+    sa = warp_sum(sa);
+    const float top = dmax + sqrtf(s * sa);
+    float lo = 0.f, hi = top * top * (1.f + 1e-6f) + 1e-30f;
+    for (int it = 0; it < 64; ++it) {
+        float mid = 0.5f * (lo + hi);
+        if (!(mid > lo && mid < hi)) break;
+        bool pole = false;
+#pragma unroll
+        for (int i = 0; i < R; ++i) pole |= d2[i] == mid;
+        if (__any_sync(0xffffffffu, pole)) mid = nextafterf(mid, hi);
+        float r11 = 0.f, r12 = 0.f, r22 = 0.f, above = 0.f;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const float w = 1.f / (d2[i] - mid);
+            r11 += av[i] * av[i] * w;
+            r12 += av[i] * r[i] * w;
+            r22 += r[i] * r[i] * w;
+            above += d2[i] > mid ? 1.f : 0.f;
+        }
+        r11 = warp_sum(r11);
+        r12 = warp_sum(r12);
+        r22 = warp_sum(r22);
+        above = warp_sum(above);
+        const float n11 = -r11, n12 = 1.f - r12, n22 = s - r22;
+        const float det = n11 * n22 - n12 * n12, tr = n11 + n22;
+        const float pos = det < 0.f ? 1.f : (tr > 0.f ? (det > 0.f ? 2.f : 1.f) : 0.f);
+        if (above + pos - 1.f >= 1.f) lo = mid;
+        else hi = mid;
+    }
+    return sqrtf(0.5f * (lo + hi));
+}
+
+template <typename Tin, typename Tg>
+__global__ void __launch_bounds__(256)
+dplr_factor_norm_kernel(const DplrParams p, float *rho, float *nrm, float *maxes) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long ntok = (long)p.B * p.T * p.H;
+    if (warp >= ntok) return;
+    const int dk = p.dk;
+    const Tin *a = static_cast<const Tin *>(p.a);
+    const Tin *bb = static_cast<const Tin *>(p.b);
+    const Tg *g = static_cast<const Tg *>(p.g);
+    float av[4], bv[4], al[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int d = lane + 32 * r;
+        const bool ok = d < dk;
+        av[r] = ok ? to_f(a[(size_t)warp * dk + d]) : 0.f;
+        bv[r] = ok ? to_f(bb[(size_t)warp * dk + d]) : 0.f;
+        float gv = 0.f;
+        if (p.gate_kind == KDA_GATE_CHANNEL) gv = ok ? to_f(g[(size_t)warp * dk + d]) : 0.f;
+        else if (p.gate_kind == KDA_GATE_SCALAR) gv = to_f(g[warp]);
+        al[r] = ok ? expf(gv) : 0.f;
+    }
+    // eq. (4): ||I - eta k j^T||_2 for unit k, j with eta = |a||b| and c = cos(a, b)
+    const float na = sqrtf(warp_sum(av[0] * av[0] + av[1] * av[1] + av[2] * av[2] + av[3] * av[3]));
+    const float nb = sqrtf(warp_sum(bv[0] * bv[0] + bv[1] * bv[1] + bv[2] * bv[2] + bv[3] * bv[3]));
+    const float ab = warp_sum(av[0] * bv[0] + av[1] * bv[1] + av[2] * bv[2] + av[3] * bv[3]);
+    const float eta = na * nb;
+    const float cosv = eta > 0.f ? ab / eta : 1.f;
+    const float r4 = 0.5f * (eta + sqrtf(fmaxf(eta * eta - 4.f * eta * cosv + 4.f, 0.f)));
+    const float sig = factor_norm_inertia(av, al, bv);
+    if (lane == 0) {
+        if (rho) rho[warp] = r4;
+        if (nrm) nrm[warp] = sig;
+        if (maxes) {   // non-negative floats order like their bit patterns
+            atomicMax(reinterpret_cast<int *>(maxes), __float_as_int(r4));
+            atomicMax(reinterpret_cast<int *>(maxes) + 1, __float_as_int(sig));
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s) {
+    if (in_bf16)
+        return g_is_bf16 ? launch_typed<__nv_bfloat16, __nv_bfloat16>(p, s) : launch_typed<__nv_bfloat16, float>(p, s);
+    return g_is_bf16 ? launch_typed<float, __nv_bfloat16>(p, s) : launch_typed<float, float>(p, s);
+}
+
+cudaError_t launch_dplr_factor_norms(const DplrParams &p, int in_bf16, int g_is_bf16, float *rho, float *nrm,
+                                     float *maxes, cudaStream_t s) {
+    const long ntok = (long)p.B * p.T * p.H;
+    const long blocks = (ntok * 32 + 255) / 256;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+    if (maxes) {
+        cudaError_t e = cudaMemsetAsync(maxes, 0, 2 * sizeof(float), s);
+        if (e != cudaSuccess) return e;
+    }
+    if (in_bf16) {
+        if (g_is_bf16)
+            dplr_factor_norm_kernel<__nv_bfloat16, __nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(p, rho, nrm, maxes);
+        else
+            dplr_factor_norm_kernel<__nv_bfloat16, float><<<(unsigned)blocks, 256, 0, s>>>(p, rho, nrm, maxes);
+    } else {
+        if (g_is_bf16)
+            dplr_factor_norm_kernel<float, __nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(p, rho, nrm, maxes);
+        else
+            dplr_factor_norm_kernel<float, float><<<(unsigned)blocks, 256, 0, s>>>(p, rho, nrm, maxes);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

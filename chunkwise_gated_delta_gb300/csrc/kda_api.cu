@@ -60,6 +60,66 @@ kda_status validate(const kda_fwd_args *a) {
     return KDA_OK;
 }
 
+kda_status validate_dplr_common(const dplr_fwd_args *a) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->B < 1 || a->T < 1 || a->H < 1) return KDA_ERR_INVALID_ARG;
+    if (a->dk < 1) return KDA_ERR_INVALID_ARG;
+    if (a->chunk != 0 && a->chunk < 1) return KDA_ERR_INVALID_ARG;
+    if (a->dtype != KDA_BF16 && a->dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (a->g_dtype != KDA_BF16 && a->g_dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (a->gate_kind != KDA_GATE_NONE && a->gate_kind != KDA_GATE_SCALAR && a->gate_kind != KDA_GATE_CHANNEL)
+        return KDA_ERR_INVALID_ARG;
+    if ((a->gate_kind == KDA_GATE_NONE) != (a->g == nullptr)) return KDA_ERR_INVALID_ARG;
+    if (!a->a || !a->b) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->q, a->k, a->v, a->a, a->b, a->g, a->h0, a->o, a->ht, a->workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const double elems = (double)a->B * a->T * a->H * (a->dk > 256 ? a->dk : 256);
+    if (elems > 9.0e18 / 8 || (double)a->B * a->T * a->H > 2.0e9) return KDA_ERR_INVALID_ARG;
+    if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+kda_status validate_dplr(const dplr_fwd_args *a) {
+    kda_status st = validate_dplr_common(a);
+    if (st != KDA_OK) return st;
+    if (!a->q || !a->k || !a->v || !a->o || a->dv < 1) return KDA_ERR_INVALID_ARG;
+    if (a->dv % 32 != 0 || a->dv > 256) return KDA_ERR_UNSUPPORTED;
+    if (a->chunk != 0 && a->chunk != 32) return KDA_ERR_UNSUPPORTED;
+    const size_t es = dtype_size(a->dtype);
+    const size_t nbt = (size_t)a->B * a->T * a->H;
+    const size_t o_bytes = nbt * a->dv * es;
+    const size_t state_bytes = (size_t)a->B * a->H * a->dv * a->dk * 4;
+    const size_t ht_bytes = a->ht ? state_bytes : 0;
+    const size_t g_bytes = a->gate_kind == KDA_GATE_CHANNEL ? nbt * a->dk * dtype_size(a->g_dtype)
+                           : a->gate_kind == KDA_GATE_SCALAR ? nbt * dtype_size(a->g_dtype) : 0;
+    struct R { const void *p; size_t n; } ins[] = {
+        {a->q, nbt * a->dk * es}, {a->k, nbt * a->dk * es}, {a->v, nbt * a->dv * es},
+        {a->a, nbt * a->dk * es}, {a->b, nbt * a->dk * es}, {a->g, g_bytes},
+        {a->h0, a->h0 ? state_bytes : 0}, {a->workspace, a->workspace_bytes}};
+    for (const R &r : ins) {
+        if (overlaps(a->o, o_bytes, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+        if (overlaps(a->ht, ht_bytes, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+    }
+    if (overlaps(a->o, o_bytes, a->ht, ht_bytes)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+kda::DplrParams dplr_params(const dplr_fwd_args *args) {
+    kda::DplrParams p{};
+    p.B = args->B; p.T = args->T; p.H = args->H; p.dk = args->dk; p.dv = args->dv;
+    p.gate_kind = args->gate_kind;
+    p.q = args->q; p.k = args->k; p.v = args->v; p.a = args->a; p.b = args->b; p.g = args->g;
+    p.h0 = args->h0; p.o = args->o; p.ht = args->ht;
+    p.status = static_cast<int *>(args->workspace);
+    return p;
+}
+
+kda_status from_cuda(cudaError_t e) {
+    if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -92,6 +152,46 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
         e = kda::launch_fwd_tc_bf16(p, g_bf16, s);
     if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+size_t dplr_chunk_fwd_workspace(const dplr_fwd_args *args) {
+    if (validate_dplr(args) != KDA_OK) return 0;
+    return kStatusBytes;
+}
+
+kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream) {
+    kda_status st = validate_dplr(args);
+    if (st != KDA_OK) return st;
+    if (!args->workspace || args->workspace_bytes < kStatusBytes) return KDA_ERR_WORKSPACE;
+    return from_cuda(kda::launch_dplr_fwd_simt(dplr_params(args), args->dtype == KDA_BF16,
+                                               args->g_dtype == KDA_BF16,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status dplr_factor_norms(const dplr_fwd_args *args, float *rho, float *norm, float *maxes,
+                             kda_stream_t stream) {
+    kda_status st = validate_dplr_common(args);
+    if (st != KDA_OK) return st;
+    const size_t nbt = (size_t)args->B * args->T * args->H;
+    const void *outs[] = {rho, norm, maxes};
+    for (const void *p : outs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const size_t in_bytes = nbt * args->dk * dtype_size(args->dtype);
+    const size_t g_bytes = args->gate_kind == KDA_GATE_CHANNEL ? nbt * args->dk * dtype_size(args->g_dtype)
+                           : args->gate_kind == KDA_GATE_SCALAR ? nbt * dtype_size(args->g_dtype) : 0;
+    struct R { const void *p; size_t n; } outr[] = {{rho, rho ? nbt * 4 : 0}, {norm, norm ? nbt * 4 : 0},
+                                                     {maxes, maxes ? 8 : 0}};
+    for (const R &o : outr) {
+        if (overlaps(o.p, o.n, args->a, in_bytes) || overlaps(o.p, o.n, args->b, in_bytes) ||
+            overlaps(o.p, o.n, args->g, g_bytes))
+            return KDA_ERR_INVALID_ARG;
+    }
+    if (overlaps(rho, outr[0].n, norm, outr[1].n) || overlaps(rho, outr[0].n, maxes, outr[2].n) ||
+        overlaps(norm, outr[1].n, maxes, outr[2].n))
+        return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_dplr_factor_norms(dplr_params(args), args->dtype == KDA_BF16,
+                                                   args->g_dtype == KDA_BF16, rho, norm, maxes,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_status_read(void *workspace, kda_stream_t stream) {

@@ -124,6 +124,70 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  */
 kda_status kda_chunk_fwd_noalloc(const kda_fwd_args *args, kda_stream_t stream);
 
+/* ------------------------------------------------------------------ DPLR */
+
+/*
+ * General gated DPLR recurrence (page "Diagonal Plus Low Rank", section 2):
+ *
+ *     S_t = S_{t-1} Diag(alpha_t) (I - b_t a_t^T) + v_t k_t^T,   o_t = S_t q_t,
+ *
+ * with a_t, b_t given independently and v unscaled.  Evaluated by that
+ * section's chunk form: per chunk, Gamma = exp(in-chunk cumsum g),
+ * Q<- = Q*Gamma, K-> = K/Gamma, A-> = A/Gamma, B<- = B*Gamma;
+ *     E = (I + (B<- A->^T * M_{-1}))^{-1},  W = E B<-,
+ *     C = -E (B<- K->^T * M_{-1}) V,        X = C - W S^T,
+ *     O = Q<- S^T + (Q<- K->^T * M) V + (Q<- A->^T * M) X,
+ *     S <- (S + V^T K-> + X^T A->) Diag(gamma^C).
+ * Layouts, ownership, stream semantics and error reporting are those of
+ * kda_chunk_fwd.
+ */
+typedef struct {
+    int B, T, H;           /* batch, sequence length (any T >= 1), heads */
+    int dk, dv;            /* key head dim 64 or 128; value head dim a multiple of 32, <= 256 */
+    int chunk;             /* 0 (library's choice) or 32; the result does not depend on it */
+    kda_dtype dtype;       /* dtype of q, k, v, a, b and o */
+    kda_gate gate_kind;
+    kda_dtype g_dtype;     /* dtype of g */
+    const void *q;         /* [B, T, H, dk] */
+    const void *k;         /* [B, T, H, dk] */
+    const void *v;         /* [B, T, H, dv] */
+    const void *a;         /* [B, T, H, dk] */
+    const void *b;         /* [B, T, H, dk] */
+    const void *g;         /* see kda_gate; NULL iff gate_kind == KDA_GATE_NONE */
+    const float *h0;       /* [B, H, dv, dk] initial state, or NULL (zero) */
+    void *o;               /* [B, T, H, dv] output, dtype */
+    float *ht;             /* [B, H, dv, dk] final state, or NULL (not written) */
+    void *workspace;       /* device buffer, zero-filled before its first use */
+    size_t workspace_bytes;
+} dplr_fwd_args;
+
+/* Bytes of workspace dplr_chunk_fwd needs for these arguments (0 on bad args). */
+size_t dplr_chunk_fwd_workspace(const dplr_fwd_args *args);
+
+/*
+ * Chunkwise forward of the general gated DPLR recurrence.  Writes o, and ht
+ * when non-NULL.  float32 CUDA-core kernel; bfloat16 inputs are widened to
+ * float32 on load and o is rounded to bfloat16 on store.
+ */
+kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream);
+
+/*
+ * Per-token norms of the DPLR transition factors (page "How to make GDN2
+ * more stable", eqs. (4) and (12)), for every (b, t, h) of args:
+ *   rho  [B, T, H] float32: ||I - b a^T||_2 by eq. (4), with
+ *        eta = |a| |b| and c = a.b / (|a| |b|)  (c = 1 when eta = 0);
+ *   norm [B, T, H] float32: ||Diag(alpha)(I - b a^T)||_2, the largest
+ *        singular value of the full factor, for which the page gives no
+ *        closed form: the largest eigenvalue of its Gram matrix
+ *        (Diag(alpha^2) plus a rank-2 term) by bisection on eigenvalue
+ *        counts from Haynsworth's inertia additivity, in float32;
+ *   maxes [2] float32: max over all tokens of rho and of norm.
+ * Reads a, b, g and the sizes B, T, H, dk of args (q, k, v, o, h0, ht, dv
+ * and the workspace are not used; the pointers may be NULL).  Any of rho, norm, maxes may be NULL (not written).
+ */
+kda_status dplr_factor_norms(const dplr_fwd_args *args, float *rho, float *norm, float *maxes,
+                             kda_stream_t stream);
+
 /*
  * Reads the device status word that kernels set on a device-side error,
  * waits for the stream, clears the word and returns the code (KDA_OK when

@@ -22,7 +22,7 @@ def lib():
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "kda.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", src))
+    return set(re.findall(r"\b((?:kda|dplr)_[a-z_0-9]+)\s*\(", src))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -87,3 +87,55 @@ def test_rejects_bad_arguments_before_launch(lib, over, code):
 def test_null_args_pointer(lib):
     assert lib.kda_chunk_fwd(None, None) == _lib.KDA_ERR_INVALID_ARG
     assert lib.kda_status_read(None, None) == _lib.KDA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- DPLR entry points
+def _dplr_args(**over):
+    a = _lib.DplrFwdArgs()
+    a.B, a.T, a.H, a.dk, a.dv, a.chunk = 2, 100, 4, 128, 128, 0
+    a.dtype, a.gate_kind, a.g_dtype = _lib.KDA_BF16, _lib.KDA_GATE_CHANNEL, _lib.KDA_BF16
+    base = 1 << 40
+    for i, f in enumerate(("q", "k", "v", "a", "b", "g", "h0", "o", "ht", "workspace")):
+        setattr(a, f, base + i * (1 << 32))
+    a.workspace_bytes = 256
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_dplr_workspace_query(lib):
+    assert lib.dplr_chunk_fwd_workspace(ctypes.byref(_dplr_args())) >= 4
+    assert lib.dplr_chunk_fwd_workspace(ctypes.byref(_dplr_args(dv=48))) == 0
+    assert lib.dplr_chunk_fwd_workspace(None) == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(a=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(b=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(q=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(o=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(T=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dtype=3), _lib.KDA_ERR_INVALID_ARG),
+    (dict(g=None), _lib.KDA_ERR_INVALID_ARG),                            # gate without g
+    (dict(b=(1 << 40) + 4 * (1 << 32) + 4), _lib.KDA_ERR_INVALID_ARG),   # misaligned
+    (dict(o=(1 << 40) + 3 * (1 << 32)), _lib.KDA_ERR_INVALID_ARG),       # o aliases a
+    (dict(dk=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dv=48), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dv=288), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=64), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(workspace=None, workspace_bytes=0), _lib.KDA_ERR_WORKSPACE),
+])
+def test_dplr_rejects_bad_arguments_before_launch(lib, over, code):
+    assert lib.dplr_chunk_fwd(ctypes.byref(_dplr_args(**over)), None) == code
+
+
+def test_dplr_factor_norms_rejects_bad_arguments(lib):
+    a = _dplr_args()
+    out = (1 << 40) + 20 * (1 << 32)
+    assert lib.dplr_factor_norms(None, out, None, None, None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.dplr_factor_norms(ctypes.byref(_dplr_args(a=None)), out, None, None, None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.dplr_factor_norms(ctypes.byref(a), out + 4, None, None, None) == _lib.KDA_ERR_INVALID_ARG
+    # the per-token output may not alias the input a
+    assert lib.dplr_factor_norms(ctypes.byref(a), (1 << 40) + 3 * (1 << 32), None, None, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    assert lib.dplr_factor_norms(ctypes.byref(_dplr_args(dk=96)), out, None, None, None) == _lib.KDA_ERR_UNSUPPORTED
