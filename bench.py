@@ -1,10 +1,14 @@
-"""Throughput of the chunkwise KDA forward on GB300 (one JSON line on stdout).
+"""Throughput of the chunkwise gated delta-rule forward on GB300 (one JSON line on stdout).
 
-A step is one kda_chunk_fwd call -- the whole forward path: decay cumsum,
-rescaling, WY build, state scan and output -- over the KDA workload
-B=4, T=4096, H=16, dk=dv=128, bf16 inputs, fp32 state, initial state given.
+A step is one forward call -- the whole path: decay cumsum, rescaling, WY
+build, state scan and output.  The default workload is KDA at B=4, T=4096,
+H=16, dk=dv=128, bf16 inputs, fp32 state, initial state given (one
+kda_chunk_fwd call per step).  --workload picks another of the seeded
+workloads: the GDN / DeltaNet / GLA sweep at B=8, T=2048, H=32, d=128 (same
+entry point) or general DPLR at B=2, T=8192, H=16, d=128 (one dplr_chunk_fwd
+call per step; the line also carries the transition-norm report).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 --impl ours (default): the CUDA library through its C ABI.  `value` is tokens/s
 with the inputs resident in HBM; `e2e` is the same metric with pinned host
@@ -38,17 +42,44 @@ import torch  # noqa: E402
 
 WORKLOAD = "kda_bf16_b4t4096h16d128"
 METRIC = "tokens/s KDA chunk fwd(+bwd) B4·T4096·H16·d128 bf16; % of roofline"
-KERNEL_SRC = os.path.join(ROOT, "chunkwise_gated_delta_gb300", "csrc", "kda_fwd_tc.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_fwd_tc_b4t4096h16d128_traffic.txt")
+CSRC = os.path.join(ROOT, "chunkwise_gated_delta_gb300", "csrc")
+
+# kernel that runs each variant's step: (name, source file)
+KERNELS = {"kda": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gdn": ("kda_fwd_tc", "kda_fwd_tc.cu"),
+           "deltanet": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gla": ("kda_fwd_tc", "kda_fwd_tc.cu"),
+           "dplr": ("dplr_fwd_simt", "dplr_fwd_simt.cu")}
+GATES = {"kda": "channel", "gla": "channel", "dplr": "channel", "gdn": "scalar", "deltanet": "none"}
+
+
+def metric_for(w) -> str:
+    if w.name == WORKLOAD:
+        return METRIC
+    shape = f"B{w.B}·T{w.T}·H{w.H}·d{w.dk}"
+    return f"tokens/s {w.variant.upper() if w.variant != 'deltanet' else 'DeltaNet'} chunk fwd {shape} bf16; % of roofline"
 
 
 def algorithmic_bytes(w) -> int:
-    """Inputs read once and outputs written once: q, k, v, g, o (bf16), beta (bf16), h0 and ht (fp32)."""
+    """Inputs read once and outputs written once (bf16 sequences, fp32 states).
+
+    KDA: q, k, g (dk wide), v, o (dv wide), beta, h0, ht.  GDN: g is one value
+    per token and head.  DeltaNet: no g.  GLA: no beta.  DPLR: q, k, a, b, g
+    (dk wide), v, o (dv wide), h0 when given, ht.
+    """
     bth = w.B * w.T * w.H
-    seq = bth * (3 * w.dk + w.dv + w.dv) * 2          # q, k, g (dk wide) + v, o (dv wide)
-    beta = bth * 2
-    state = 2 * w.B * w.H * w.dv * w.dk * 4            # h0 + ht
-    return seq + beta + state
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    state = w.B * w.H * w.dv * w.dk * 4
+    states = state * (2 if w.h0 else 1)
+    if w.variant == "dplr":
+        return bth * (5 * w.dk + 2 * w.dv) * es + states
+    seq = bth * (2 * w.dk + 2 * w.dv) * es
+    g = {"kda": bth * w.dk, "gla": bth * w.dk, "gdn": bth, "deltanet": 0}[w.variant] * es
+    beta = 0 if w.variant == "gla" else bth * es
+    return seq + g + beta + states
+
+
+def traffic_file(w) -> str:
+    shape = w.name.split("_", 2)[-1]
+    return os.path.join(ROOT, "profiles", f"{KERNELS[w.variant][0]}_{w.variant}_{shape}_traffic.txt")
 
 
 def measured_peaks():
@@ -59,12 +90,13 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def traffic_per_launch():
+def traffic_per_launch(w):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
     try:
-        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+        src = os.path.join(CSRC, KERNELS[w.variant][1])
+        src_hash = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         vals = {}
-        for line in open(TRAFFIC_FILE):
+        for line in open(traffic_file(w)):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
@@ -168,12 +200,22 @@ def barrier(world):
 def oracle_sample(w, x, heads, T):
     """Time the float64 oracle on `heads` (b, h) pairs over the first T tokens."""
     import oracle
-    f = lambda t: t[:, :T].double().numpy() if t.dim() >= 3 else t.double().numpy()
-    q, k, v, g, beta = (f(x[n]) for n in ("q", "k", "v", "g", "beta"))
+    f = lambda n: (x[n][:, :T].double().numpy() if n in x else None)
+    q, k, v, g, beta, a, b = (f(n) for n in ("q", "k", "v", "g", "beta", "a", "b"))
     h0 = x["h0"].double().numpy() if "h0" in x else None
     cores = len(os.sched_getaffinity(0))
+    kw = dict(h0=h0, heads=heads, threads=cores)
     t0 = time.perf_counter()
-    oracle.kda_fwd(q, k, v, g, beta, h0, heads=heads, threads=cores)
+    if w.variant == "kda":
+        oracle.kda_fwd(q, k, v, g, beta, **kw)
+    elif w.variant == "gdn":
+        oracle.gdn_fwd(q, k, v, g, beta, **kw)
+    elif w.variant == "deltanet":
+        oracle.deltanet_fwd(q, k, v, beta, **kw)
+    elif w.variant == "gla":
+        oracle.gla_fwd(q, k, v, g, **kw)
+    else:
+        oracle.dplr_fwd(q, k, v, a, b, g, **kw)
     dt = time.perf_counter() - t0
     tokens = len(heads) * T / w.H              # head-tokens expressed as workload tokens
     return tokens, dt, cores
@@ -197,7 +239,7 @@ def cpu_baseline_leg(w, x, budget_s=12.0):
 
 def run_reference(args, rank, world):
     from chunkwise_gated_delta_gb300.inputs import WORKLOADS, make_inputs
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     if rank != 0:
         return
     x = make_inputs(w, seed=0)
@@ -219,7 +261,7 @@ def run_reference(args, rank, world):
     sample = (f"{len(heads)} (batch, head) pairs x {T} tokens per step, float64 token recurrence in C, "
               f"{cores} threads; tokens counted as head-tokens / H")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "impl": "reference", "metric": metric_for(w), "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(w),
@@ -230,26 +272,37 @@ def run_reference(args, rank, world):
 
 
 def config_dict(w):
-    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
-            "h0": w.h0, "inputs": "bf16 q,k,v,g,beta; fp32 h0/ht",
+    inputs = {"kda": "bf16 q,k,v,g,beta", "gdn": "bf16 q,k,v,beta, g [B,T,H]", "deltanet": "bf16 q,k,v,beta",
+              "gla": "bf16 q,k,v,g; beta = 0, v unscaled", "dplr": "bf16 q,k,v,a,b,g"}[w.variant]
+    inputs += "; fp32 h0/ht" if w.h0 else "; fp32 ht, no h0"
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+            "chunk": 32 if w.variant == "dplr" else w.chunk, "h0": w.h0, "inputs": inputs,
             "l2": f"no flush: inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.1f} MB per step vs 129 MB)",
             "parallelism": "replicas (independent (batch, head) scans, no collective)"}
 
 
 def run_ours(args, rank, world, local):
-    from chunkwise_gated_delta_gb300 import HostRunner, kda_chunk_fwd
+    from chunkwise_gated_delta_gb300 import HostRunner, dplr_chunk_fwd, dplr_factor_norms, kda_chunk_fwd
     from chunkwise_gated_delta_gb300.inputs import WORKLOADS, make_inputs
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     x = make_inputs(w, seed=rank)
+    x = {k: v for k, v in x.items() if k in ("q", "k", "v", "g", "beta", "h0", "a", "b", "scale_v")}
     d = {k: v.to(dev) for k, v in x.items() if isinstance(v, torch.Tensor)}
-    o = torch.empty(w.B, w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    o = torch.empty(w.B, w.T, w.H, w.dv, dtype=w.dtype, device=dev)
     ht = torch.empty(w.B, w.H, w.dv, w.dk, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    gate = GATES[w.variant]
 
-    def step():
-        kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o=o, ht=ht, stream=stream)
+    if w.variant == "dplr":
+        def step():
+            dplr_chunk_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"), gate=gate,
+                           o=o, ht=ht, stream=stream)
+    else:
+        def step():
+            kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), gate=gate,
+                          scale_v=x["scale_v"], o=o, ht=ht, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -282,7 +335,8 @@ def run_ours(args, rank, world, local):
     # end to end from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        runner = HostRunner(x, device=dev, scale_v=True, gate="channel")
+        runner = HostRunner(x, device=dev, scale_v=x["scale_v"], gate=gate,
+                            kind="dplr" if w.variant == "dplr" else "kda")
         for _ in range(max(3, min(args.warmup, 10))):
             runner.run(stream)
         torch.cuda.synchronize()
@@ -306,7 +360,7 @@ def run_ours(args, rank, world, local):
     abytes = algorithmic_bytes(w)
     achieved = abytes / (launch_ms * 1e-3) / 1e9
     line = {
-        "metric": METRIC,
+        "metric": metric_for(w),
         "value": world * tokens * args.steps / (elapsed_ms * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -320,13 +374,20 @@ def run_ours(args, rank, world, local):
         "data": "synthetic",
         "config": config_dict(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_per_launch(),
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_per_launch(w),
+                     "kernel": KERNELS[w.variant][0],
                      "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                      "algorithmic_bytes_per_launch": abytes, "kernel_ms_per_launch": launch_ms},
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clk,
     }
+    if w.variant == "dplr":
+        # transition-norm report (outside the timed region)
+        _, _, mx = dplr_factor_norms(d["a"], d["b"], d.get("g"), gate=gate, stream=stream)
+        torch.cuda.synchronize()
+        line["factor_norms"] = {"max_rho_eq4": float(mx[0]), "max_factor_norm": float(mx[1]),
+                                "tokens": w.B * w.T * w.H}
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline_leg(w, x)
@@ -339,6 +400,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["kda_bf16_b4t4096h16d128", "gdn_bf16_b8t2048h32d128", "deltanet_bf16_b8t2048h32d128",
+                             "gla_bf16_b8t2048h32d128", "dplr_bf16_b2t8192h16d128"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()

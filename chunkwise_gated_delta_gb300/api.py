@@ -243,15 +243,18 @@ def gla_fwd(q, k, v, g, h0=None, **kw):
 class HostRunner:
     """End-to-end call from pinned host buffers.
 
-    Each :meth:`run` copies the inputs host->device, runs ``kda_chunk_fwd`` and
-    copies o (and ht) back device->host, all on one stream.  Device buffers
-    are allocated once and reused.
+    Each :meth:`run` copies the inputs host->device, runs the forward
+    (``kda_chunk_fwd``, or ``dplr_chunk_fwd`` when ``kind="dplr"``) and copies
+    o and ht back device->host, all on one stream.  Device buffers are
+    allocated once and reused.
     """
 
-    def __init__(self, host: dict, device="cuda", scale_v=True, gate=None):
-        self.host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-        self.dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()
-                    if isinstance(v, torch.Tensor)}
+    def __init__(self, host: dict, device="cuda", scale_v=True, gate=None, kind="kda"):
+        if kind not in ("kda", "dplr"):
+            raise ValueError(f"unknown kind {kind}")
+        self.host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()
+                     if k in ("q", "k", "v", "g", "beta", "h0", "a", "b")}
+        self.dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()}
         q = self.dev["q"]
         B, T, H, _ = q.shape
         dv, dk = self.dev["v"].shape[-1], q.shape[-1]
@@ -259,7 +262,7 @@ class HostRunner:
         self.ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)
         self.o_host = torch.empty_like(self.o, device="cpu").pin_memory()
         self.ht_host = torch.empty_like(self.ht, device="cpu").pin_memory()
-        self.scale_v, self.gate = scale_v, gate
+        self.scale_v, self.gate, self.kind = scale_v, gate, kind
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.dev.values())
         self.d2h_bytes = self.o.numel() * self.o.element_size() + self.ht.numel() * 4
 
@@ -269,8 +272,12 @@ class HostRunner:
             for k, v in self.dev.items():
                 v.copy_(self.host[k], non_blocking=True)
             d = self.dev
-            kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"),
-                          gate=self.gate, scale_v=self.scale_v, o=self.o, ht=self.ht, stream=stream)
+            if self.kind == "dplr":
+                dplr_chunk_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"),
+                               gate=self.gate, o=self.o, ht=self.ht, stream=stream)
+            else:
+                kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"),
+                              gate=self.gate, scale_v=self.scale_v, o=self.o, ht=self.ht, stream=stream)
             self.o_host.copy_(self.o, non_blocking=True)
             self.ht_host.copy_(self.ht, non_blocking=True)
         return self.o_host, self.ht_host
