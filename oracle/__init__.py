@@ -18,8 +18,11 @@ Every variant is a choice of (a, b, vv, alpha):
 * GLA: b = 0 and vv = v (GLA page, section 5.1).
 * DPLR: a, b given, vv = v (DPLR page, section 2).
 
+The reverse mode of the same loop (``recurrence_bwd.c``) gives the gradients
+of L = <do, o> + <dht, ht> with respect to every input.
+
 Parity status of each function is listed in ``PINS`` below; each pin is a test
-under ``tests/test_oracle_pins.py``.
+under ``tests/test_oracle_pins.py`` or ``tests/test_oracle_bwd_pins.py``.
 """
 from __future__ import annotations
 
@@ -35,6 +38,7 @@ from .spectral import factor_norm_exact, rho_closed_form  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "recurrence.c")
+_SRC_BWD = os.path.join(_HERE, "recurrence_bwd.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
@@ -55,6 +59,13 @@ PINS = {
     "rho_closed_form": ["numpy SVD", "eq. (5) lower bound", "eq. (6) equality case",
                         "hand-derived values, tests/golden/spectral_norm_points.txt"],
     "factor_norm_exact": ["explicit 2x2 reduction of eq. (9)", "D = I reduces to rho"],
+    "recurrence_bwd": [
+        "central finite differences of the forward oracle on every input entry (T = 64, all five variants)",
+        "central finite differences on sampled entries across four checkpoint segments",
+        "chunk backward of page 'Kimi Delta Attention backward' restated in numpy, C in {16, 32, 64}",
+        "closed-form gradients of the GLA parallel form (page 'Gated Linear Attention', section 6.3)",
+        "scalar-gate gradient equals the channel sum at equal decays",
+    ],
 }
 
 
@@ -62,11 +73,11 @@ def build(force: bool = False) -> str:
     """Compile ``recurrence.c`` with gcc into ``oracle/_build/liboracle.so``."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+             or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_BWD)))
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared",
-                               "-o", tmp, _SRC, "-lm"])
+                               "-o", tmp, _SRC, _SRC_BWD, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -86,6 +97,17 @@ def _load():
                 dp, dp, ctypes.c_long,
                 dp, ctypes.c_long, ctypes.c_int,
                 dp, dp, ctypes.c_long, dp]
+            lib.oracle_recurrence_head_bwd.restype = ctypes.c_int
+            lib.oracle_recurrence_head_bwd.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                dp, dp, ctypes.c_long,
+                dp, ctypes.c_long,
+                dp, ctypes.c_long, ctypes.c_int,
+                dp, dp, ctypes.c_long,
+                dp, ctypes.c_long, ctypes.c_int,
+                dp,
+                dp, ctypes.c_long, dp,
+                dp, dp, dp, dp, dp, dp, dp, dp]
             _lib = lib
     return _lib
 
@@ -157,6 +179,96 @@ def recurrence(q, k, v, g=None, gate=GATE_CHANNEL, beta=None, a=None, b=None,
         with ThreadPoolExecutor(max_workers=nthreads) as ex:
             list(ex.map(one, pairs))
     return o, ht
+
+
+def recurrence_bwd(q, k, v, do, g=None, gate=GATE_CHANNEL, beta=None, a=None, b=None,
+                   scale_v=True, h0=None, dht=None, threads=None, heads=None):
+    """Reverse mode of :func:`recurrence` for L = <do, o> + <dht, ht>.
+
+    Same inputs as :func:`recurrence` plus do [B, T, H, dv] and dht
+    [B, H, dv, dk] (None -> 0).  Returns a dict of float64 gradients: dq, dk,
+    dv, dh0, and dg (shape of g) when g is given, dbeta when beta is given,
+    da and db when a and b are given.  With the KDA mapping (a, b None) the
+    a- and b-paths are folded into dk and dbeta.  ``heads`` restricts the work
+    to a list of (b, h) pairs; the other entries stay zero.
+    """
+    lib = _load()
+    q, k, v, do, g, beta, a, b, h0, dht = map(_f64, (q, k, v, do, g, beta, a, b, h0, dht))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if g is None:
+        gate = GATE_NONE
+    if (a is None) != (b is None):
+        raise ValueError("a and b are given together or not at all")
+    out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v),
+           "dh0": np.zeros((B, H, dv, dk))}
+    if g is not None:
+        out["dg"] = np.zeros_like(g)
+    if beta is not None:
+        out["dbeta"] = np.zeros_like(beta)
+    if a is not None:
+        out["da"], out["db"] = np.zeros_like(a), np.zeros_like(b)
+    s_qk, s_v = H * dk, H * dv
+    s_g = (H * dk) if gate == GATE_CHANNEL else H
+    pairs = heads if heads is not None else [(bi, hi) for bi in range(B) for hi in range(H)]
+
+    def one(pair):
+        bi, hi = pair
+        base_qk = (bi * T * H + hi) * dk
+        base_v = (bi * T * H + hi) * dv
+        base_s = (bi * H + hi) * dv * dk
+        gbase = (bi * T * H + hi) * dk if gate == GATE_CHANNEL else bi * T * H + hi
+        o_g = (_ptr(g, gbase), _ptr(out.get("dg"), gbase)) if g is not None else (None, None)
+        bb = bi * T * H + hi
+        rc = lib.oracle_recurrence_head_bwd(
+            T, dk, dv,
+            _ptr(q, base_qk), _ptr(k, base_qk), s_qk,
+            _ptr(v, base_v), s_v,
+            o_g[0], s_g, gate,
+            _ptr(a, base_qk), _ptr(b, base_qk), s_qk,
+            _ptr(beta, bb), H,
+            1 if scale_v else 0,
+            _ptr(h0, base_s),
+            _ptr(do, base_v), s_v, _ptr(dht, base_s),
+            _ptr(out["dq"], base_qk), _ptr(out["dk"], base_qk), _ptr(out["dv"], base_v), o_g[1],
+            _ptr(out.get("da"), base_qk), _ptr(out.get("db"), base_qk),
+            _ptr(out.get("dbeta"), bb), _ptr(out["dh0"], base_s))
+        if rc != 0:
+            raise MemoryError("oracle scratch allocation failed")
+
+    nthreads = threads or len(os.sched_getaffinity(0))
+    if nthreads <= 1 or len(pairs) == 1:
+        for p in pairs:
+            one(p)
+    else:
+        with ThreadPoolExecutor(max_workers=nthreads) as ex:
+            list(ex.map(one, pairs))
+    return out
+
+
+def kda_bwd(q, k, v, g, beta, do, h0=None, dht=None, **kw):
+    """KDA backward: gradients dq, dk, dv, dg, dbeta, dh0."""
+    return recurrence_bwd(q, k, v, do, g=g, gate=GATE_CHANNEL, beta=beta, scale_v=True, h0=h0, dht=dht, **kw)
+
+
+def gdn_bwd(q, k, v, g, beta, do, h0=None, dht=None, **kw):
+    """GDN backward (g [B, T, H])."""
+    return recurrence_bwd(q, k, v, do, g=g, gate=GATE_SCALAR, beta=beta, scale_v=True, h0=h0, dht=dht, **kw)
+
+
+def deltanet_bwd(q, k, v, beta, do, h0=None, dht=None, **kw):
+    """DeltaNet backward."""
+    return recurrence_bwd(q, k, v, do, g=None, gate=GATE_NONE, beta=beta, scale_v=True, h0=h0, dht=dht, **kw)
+
+
+def gla_bwd(q, k, v, g, do, h0=None, dht=None, **kw):
+    """GLA backward."""
+    return recurrence_bwd(q, k, v, do, g=g, gate=GATE_CHANNEL, beta=None, scale_v=False, h0=h0, dht=dht, **kw)
+
+
+def dplr_bwd(q, k, v, a, b, g, do, h0=None, dht=None, **kw):
+    """General gated DPLR backward: dq, dk, dv, da, db, dg, dh0."""
+    return recurrence_bwd(q, k, v, do, g=g, gate=GATE_CHANNEL, a=a, b=b, scale_v=False, h0=h0, dht=dht, **kw)
 
 
 def kda_fwd(q, k, v, g, beta, h0=None, **kw):

@@ -101,3 +101,107 @@ def dplr_wy_product(a, b, alpha):
     for i in range(C):
         acc -= np.outer(w[i], a[i] / gam[i])
     return acc @ np.diag(gam[-1])
+
+
+def kda_chunk_bwd_form(q, k, v, g, beta, do, h0=None, dht=None, C=64, scale_v=True):
+    """KDA chunk backward of page "Kimi Delta Attention backward" (one head).
+
+    Forward per chunk as kda_chunk_form; backward per chunk, in reverse, with
+    dS the gradient of the state after the chunk:
+      dU = K-> Diag(gamma^C) dS^T + (Q<- K->^T * M)^T dO;   dW = -dU S_prev;
+      dQ<- = dO S_prev + (dO V_new^T * M) K->;   dV = Diag(beta) A~^T dU;
+      dA~ = dW K<-^T Diag(beta) + dU V^T Diag(beta);   dX~ = -A~^T dA~ A~^T;
+      dK<- = Diag(beta) A~^T dW + (Diag(beta) dX~ * M_{-1}) K->;
+      dK-> = V_new dS Diag(gamma^C) + (dO V_new^T * M)^T Q<- + (Diag(beta) dX~ * M_{-1})^T K<-;
+      dK = dK<- * Gamma + dK-> / Gamma;   dQ = dQ<- * Gamma;
+      dbeta = diag(A~^T dW K<-^T) + diag(A~^T dU V^T) + diag(dX~ (K<- K->^T * M_{-1})^T);
+      dlogGamma = dQ * Q + (dK<- * Gamma) * K - (dK-> / Gamma) * K, last row + diag(S^T dS);
+      dg = in-chunk suffix sum of dlogGamma;
+      dS_prev = dS Diag(gamma^C) + dO^T Q<- - dU^T W.
+    (The page's dS recursion, its dW with S_[t-1] and its dK-> with the
+    output term of the final combination.)  With scale_v False (beta = 0,
+    GLA) U = A~ V and the beta-terms of dV, dA~ and dbeta drop.
+    Returns dq, dk, dv, dg, dbeta, dh0.
+    """
+    T, dk = q.shape
+    dv = v.shape[1]
+    g = np.zeros((T, dk)) if g is None else g
+    beta = np.zeros(T) if beta is None else beta
+    S = np.zeros((dv, dk)) if h0 is None else h0.copy()
+    starts = list(range(0, T, C))
+    prev = []
+    for s in starts:                       # forward: states before each chunk
+        e = min(s + C, T)
+        n = e - s
+        _, M1 = _masks(n)
+        Gam = np.exp(np.cumsum(g[s:e], axis=0))
+        Kl, Kr = k[s:e] * Gam, k[s:e] / Gam
+        Db = np.diag(beta[s:e])
+        At = np.linalg.inv(np.eye(n) + Db @ ((Kl @ Kr.T) * M1))
+        W = At @ Db @ Kl
+        U = At @ Db @ v[s:e] if scale_v else At @ v[s:e]
+        prev.append(S.copy())
+        S = (S + (U - W @ S.T).T @ Kr) * Gam[-1][None, :]
+    out = {n: np.zeros_like(x) for n, x in (("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta))}
+    dS = np.zeros((dv, dk)) if dht is None else dht.copy()
+    for idx in reversed(range(len(starts))):
+        s = starts[idx]
+        e = min(s + C, T)
+        n = e - s
+        M, M1 = _masks(n)
+        Sp = prev[idx]
+        Gam = np.exp(np.cumsum(g[s:e], axis=0))
+        gC = Gam[-1]
+        Q, K, V, dO = q[s:e], k[s:e], v[s:e], do[s:e]
+        Ql, Kl, Kr = Q * Gam, K * Gam, K / Gam
+        Db = np.diag(beta[s:e])
+        N = (Kl @ Kr.T) * M1
+        At = np.linalg.inv(np.eye(n) + Db @ N)
+        W = At @ Db @ Kl
+        U = At @ Db @ V if scale_v else At @ V
+        Vn = U - W @ Sp.T
+        P = (Ql @ Kr.T) * M
+        St = (Sp + Vn.T @ Kr) * gC[None, :]
+        dU = (Kr * gC[None, :]) @ dS.T + P.T @ dO
+        dW = -dU @ Sp
+        dOV = (dO @ Vn.T) * M
+        dQl = dO @ Sp + dOV @ Kr
+        dV = (Db @ At.T @ dU) if scale_v else At.T @ dU
+        dAt = dW @ Kl.T @ Db + (dU @ V.T @ Db if scale_v else dU @ V.T)
+        dXt = -At.T @ dAt @ At.T
+        E = (Db @ dXt) * M1
+        dKl = Db @ At.T @ dW + E @ Kr
+        dKr = Vn @ dS * gC[None, :] + dOV.T @ Ql + E.T @ Kl
+        dq = dQl * Gam
+        dk_ = dKl * Gam + dKr / Gam
+        dbeta = np.diag(At.T @ dW @ Kl.T) + np.diag(dXt @ N.T)
+        if scale_v:
+            dbeta = dbeta + np.diag(At.T @ dU @ V.T)
+        dlg = dq * Q + dKl * Gam * K - dKr / Gam * K
+        dlg[-1] += (St * dS).sum(0)
+        out["dq"][s:e], out["dk"][s:e], out["dv"][s:e] = dq, dk_, dV
+        out["dg"][s:e] = np.cumsum(dlg[::-1], axis=0)[::-1]
+        out["dbeta"][s:e] = dbeta
+        dS = dS * gC[None, :] + dO.T @ Ql - dU.T @ W
+    out["dh0"] = dS
+    return out
+
+
+def gla_parallel_grads(q, k, v, g, do):
+    """Gradients of the GLA parallel form o = (Q<- K->^T * M) V, whole sequence as one chunk.
+
+    Page "Gated Linear Attention", section 6.3 with zero initial state and no
+    final-state gradient: with A = (Q<- K->^T) * M and dA = (dO V^T) * M,
+    dQ = (dA K->) * Gamma, dK = (dA^T Q<-) / Gamma, dV = A^T dO,
+    dlogGamma = Q * dQ - K * dK and dg its suffix sum.
+    """
+    Gam = np.exp(np.cumsum(g, axis=0))
+    M, _ = _masks(q.shape[0])
+    Ql, Kr = q * Gam, k / Gam
+    A = (Ql @ Kr.T) * M
+    dA = (do @ v.T) * M
+    dq = (dA @ Kr) * Gam
+    dk = (dA.T @ Ql) / Gam
+    dv = A.T @ do
+    dlg = q * dq - k * dk
+    return dq, dk, dv, np.cumsum(dlg[::-1], axis=0)[::-1]
