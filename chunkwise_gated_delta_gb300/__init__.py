@@ -5,4 +5,4 @@ The computation lives in the CUDA library ``_build/libkda.so`` (C ABI in
 :func:`.build.build`.
 """
 from .api import (HostRunner, KdaError, deltanet_fwd, dplr_chunk_fwd, dplr_factor_norms,  # noqa: F401
-                  gdn_fwd, gla_fwd, kda_chunk_fwd, kda_chunk_fwd_noalloc, status_read)
+                  gdn_fwd, gla_fwd, kda_chunk_bwd, kda_chunk_fwd, kda_chunk_fwd_noalloc, status_read)

@@ -45,6 +45,7 @@ def workspace_for(device, nbytes: int) -> torch.Tensor:
     key = dev.index if dev.index is not None else torch.cuda.current_device()
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
+        _workspaces.pop(key, None)
         ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
         _workspaces[key] = ws
     return ws
@@ -135,6 +136,70 @@ def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, sca
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_noalloc")
     return o, ht
+
+
+def make_bwd_args(q, k, v, g, beta, h0, do, dht, grads: dict, *, gate=None, scale_v=True,
+                  workspace=None) -> _lib.KdaBwdArgs:
+    """Fill the C backward argument struct (grads: dq, dk, dv, dg, dbeta, dh0 tensors or None)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if gate is None:
+        gate = "none" if g is None else ("scalar" if g.dim() == 3 else "channel")
+    x = _lib.KdaBwdArgs()
+    x.B, x.T, x.H, x.dk, x.dv, x.chunk = B, T, H, dk, dv, 0
+    x.dtype = _dtype_code(q)
+    x.gate_kind = _GATES[gate]
+    x.g_dtype = _dtype_code(g) if g is not None else _lib.KDA_BF16
+    x.flags = _lib.KDA_FLAG_BETA_SCALES_V if scale_v else 0
+    x.q, x.k, x.v, x.g, x.beta, x.h0 = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0)
+    x.grad_o, x.grad_ht = _ptr(do), _ptr(dht)
+    x.grad_q, x.grad_k, x.grad_v = _ptr(grads.get("dq")), _ptr(grads.get("dk")), _ptr(grads.get("dv"))
+    x.grad_g, x.grad_beta, x.grad_h0 = _ptr(grads.get("dg")), _ptr(grads.get("dbeta")), _ptr(grads.get("dh0"))
+    if workspace is not None:
+        x.workspace = _ptr(workspace)
+        x.workspace_bytes = workspace.numel() * workspace.element_size()
+    return x
+
+
+def kda_chunk_bwd(q, k, v, g, beta, h0, do, dht=None, *, gate=None, scale_v=True, grads=None,
+                  workspace=None, stream=None):
+    """Backward of :func:`kda_chunk_fwd` through ``kda_chunk_bwd`` of the C ABI.
+
+    Inputs are those of the forward plus do [B, T, H, dv] (dtype of q) and dht
+    [B, H, dv, dk] fp32 or None.  Returns a dict with dq, dk, dv (dtype of q),
+    dg (dtype and layout of g) when g is given, dbeta when beta is given, and
+    dh0 (fp32).  ``grads`` may supply preallocated output tensors by those names.
+    """
+    lib = _lib.load()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (h0, "h0"), (do, "do"),
+                    (dht, "dht")):
+        _check(t, name)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    out = dict(grads or {})
+    out.setdefault("dq", torch.empty_like(q))
+    out.setdefault("dk", torch.empty_like(k))
+    out.setdefault("dv", torch.empty_like(v))
+    if g is not None:
+        out.setdefault("dg", torch.empty_like(g))
+    if beta is not None:
+        out.setdefault("dbeta", torch.empty_like(beta))
+    out.setdefault("dh0", torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device))
+    args = make_bwd_args(q, k, v, g, beta, h0, do, dht, out, gate=gate, scale_v=scale_v)
+    need = lib.kda_chunk_bwd_workspace(ctypes.byref(args))
+    if need == 0:
+        rc = lib.kda_chunk_bwd(ctypes.byref(args), None)
+        raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "kda_chunk_bwd")
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    args.workspace = _ptr(workspace)
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = lib.kda_chunk_bwd(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.KDA_OK:
+        raise KdaError(rc, "kda_chunk_bwd")
+    return out
 
 
 def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None,

@@ -105,6 +105,55 @@ kda_status validate_dplr(const dplr_fwd_args *a) {
     return KDA_OK;
 }
 
+kda_status validate_bwd(const kda_bwd_args *a) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->B < 1 || a->T < 1 || a->H < 1 || a->dk < 1 || a->dv < 1) return KDA_ERR_INVALID_ARG;
+    if (a->chunk != 0 && a->chunk < 1) return KDA_ERR_INVALID_ARG;
+    if (a->dtype != KDA_BF16 && a->dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (a->g_dtype != KDA_BF16 && a->g_dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (a->gate_kind != KDA_GATE_NONE && a->gate_kind != KDA_GATE_SCALAR && a->gate_kind != KDA_GATE_CHANNEL)
+        return KDA_ERR_INVALID_ARG;
+    if ((a->gate_kind == KDA_GATE_NONE) != (a->g == nullptr)) return KDA_ERR_INVALID_ARG;
+    if ((a->g == nullptr) != (a->grad_g == nullptr)) return KDA_ERR_INVALID_ARG;
+    if ((a->beta == nullptr) != (a->grad_beta == nullptr)) return KDA_ERR_INVALID_ARG;
+    if (a->flags & ~KDA_FLAG_BETA_SCALES_V) return KDA_ERR_INVALID_ARG;
+    if (!a->q || !a->k || !a->v || !a->grad_o || !a->grad_q || !a->grad_k || !a->grad_v)
+        return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->q, a->k, a->v, a->g, a->beta, a->h0, a->grad_o, a->grad_ht, a->grad_q,
+                          a->grad_k, a->grad_v, a->grad_g, a->grad_beta, a->grad_h0, a->workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const double elems = (double)a->B * a->T * a->H * (a->dk > a->dv ? a->dk : a->dv);
+    if (elems > 9.0e18 / 8 || (double)a->B * a->T * a->H > 2.0e9) return KDA_ERR_INVALID_ARG;
+    if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
+    if (a->dv != 64 && a->dv != 128) return KDA_ERR_UNSUPPORTED;
+    if (a->chunk != 0 && a->chunk != 32) return KDA_ERR_UNSUPPORTED;
+    const size_t es = dtype_size(a->dtype);
+    const size_t nbt = (size_t)a->B * a->T * a->H;
+    const size_t state_bytes = (size_t)a->B * a->H * a->dv * a->dk * 4;
+    const size_t g_bytes = a->gate_kind == KDA_GATE_CHANNEL ? nbt * a->dk * dtype_size(a->g_dtype)
+                           : a->gate_kind == KDA_GATE_SCALAR ? nbt * dtype_size(a->g_dtype) : 0;
+    struct R { const void *p; size_t n; };
+    const R ins[] = {{a->q, nbt * a->dk * es}, {a->k, nbt * a->dk * es}, {a->v, nbt * a->dv * es},
+                     {a->g, g_bytes}, {a->beta, a->beta ? nbt * es : 0}, {a->h0, a->h0 ? state_bytes : 0},
+                     {a->grad_o, nbt * a->dv * es}, {a->grad_ht, a->grad_ht ? state_bytes : 0},
+                     {a->workspace, a->workspace_bytes}};
+    const R outs[] = {{a->grad_q, nbt * a->dk * es}, {a->grad_k, nbt * a->dk * es},
+                      {a->grad_v, nbt * a->dv * es}, {a->grad_g, g_bytes},
+                      {a->grad_beta, a->grad_beta ? nbt * es : 0}, {a->grad_h0, a->grad_h0 ? state_bytes : 0}};
+    for (const R &o : outs) {
+        for (const R &r : ins)
+            if (overlaps(o.p, o.n, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+        for (const R &o2 : outs)
+            if (&o2 != &o && overlaps(o.p, o.n, o2.p, o2.n)) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
+size_t bwd_workspace_bytes(const kda_bwd_args *a) {
+    return kStatusBytes + kda::bwd_state_bytes(a->B, a->T, a->H, a->dk, a->dv);
+}
+
 kda::DplrParams dplr_params(const dplr_fwd_args *args) {
     kda::DplrParams p{};
     p.B = args->B; p.T = args->T; p.H = args->H; p.dk = args->dk; p.dv = args->dv;
@@ -192,6 +241,34 @@ kda_status dplr_factor_norms(const dplr_fwd_args *args, float *rho, float *norm,
     return from_cuda(kda::launch_dplr_factor_norms(dplr_params(args), args->dtype == KDA_BF16,
                                                    args->g_dtype == KDA_BF16, rho, norm, maxes,
                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_chunk_bwd_workspace(const kda_bwd_args *args) {
+    if (validate_bwd(args) != KDA_OK) return 0;
+    return bwd_workspace_bytes(args);
+}
+
+kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream) {
+    kda_status st = validate_bwd(args);
+    if (st != KDA_OK) return st;
+    if (!args->workspace || args->workspace_bytes < bwd_workspace_bytes(args)) return KDA_ERR_WORKSPACE;
+    kda::BwdParams p{};
+    p.B = args->B; p.T = args->T; p.H = args->H; p.dk = args->dk; p.dv = args->dv;
+    p.gate_kind = args->gate_kind;
+    p.scale_v = (args->flags & KDA_FLAG_BETA_SCALES_V) ? 1 : 0;
+    p.has_beta = args->beta != nullptr;
+    p.q = args->q; p.k = args->k; p.v = args->v; p.g = args->g; p.beta = args->beta; p.h0 = args->h0;
+    p.grad_o = args->grad_o; p.grad_ht = args->grad_ht;
+    p.grad_q = args->grad_q; p.grad_k = args->grad_k; p.grad_v = args->grad_v;
+    p.grad_g = args->grad_g; p.grad_beta = args->grad_beta; p.grad_h0 = args->grad_h0;
+    unsigned char *ws = static_cast<unsigned char *>(args->workspace);
+    const size_t N = (size_t)(args->T + 31) / 32;
+    const size_t per_state = (size_t)args->B * args->H * args->dv * args->dk;
+    p.status = reinterpret_cast<int *>(ws);
+    p.ws_S = reinterpret_cast<float *>(ws + kStatusBytes);
+    p.ws_dS = p.ws_S + (N + 1) * per_state;
+    return from_cuda(kda::launch_bwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_status_read(void *workspace, kda_stream_t stream) {

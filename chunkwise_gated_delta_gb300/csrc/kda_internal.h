@@ -32,6 +32,23 @@ struct DplrParams {
     int *status;            // first word of the workspace
 };
 
+// Device-side copy of the validated backward arguments.
+struct BwdParams {
+    int B, T, H, dk, dv;
+    int gate_kind;          // kda_gate
+    int scale_v;            // beta scales v
+    int has_beta;
+    const void *q, *k, *v, *g, *beta;
+    const float *h0;
+    const void *grad_o;     // [B, T, H, dv]
+    const float *grad_ht;   // [B, H, dv, dk] or null
+    void *grad_q, *grad_k, *grad_v, *grad_g, *grad_beta;
+    float *grad_h0;
+    float *ws_S;            // [B, H, N + 1, dv, dk] states before each chunk, then the final state
+    float *ws_dS;           // [B, H, N, dv, dk] gradients of the state after each chunk
+    int *status;
+};
+
 // Device status codes written into the workspace word (first error wins).
 enum : int { kDevOk = 0, kDevTimeout = 1 };
 
@@ -47,5 +64,11 @@ cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16
 // Per-token transition norms; maxes (2 floats) is cleared on the stream first.
 cudaError_t launch_dplr_factor_norms(const DplrParams &p, int in_bf16, int g_is_bf16, float *rho, float *nrm,
                                      float *maxes, cudaStream_t s);
+
+// Backward: bytes of chunk states the three kernels keep in the workspace.
+size_t bwd_state_bytes(int B, int T, int H, int dk, int dv);
+
+// float32 CUDA-core backward (inputs float32 or bf16).
+cudaError_t launch_bwd_simt(const BwdParams &p, int in_bf16, int g_is_bf16, cudaStream_t s);
 
 }  // namespace kda

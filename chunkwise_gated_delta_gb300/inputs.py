@@ -6,8 +6,9 @@ storage dtype.  Both the CUDA path and the CPU oracle receive the same cast
 values (the oracle upcasts them to float64).
 
 Draws come from a CPU ``torch.Generator`` seeded with ``seed`` in a fixed
-order -- q, k, v, beta logits, g logits, h0, then (DPLR only) a, the noise for
-a', the cosines and the eta logits -- all in float64 before the cast.
+order -- q, k, v, beta logits, g logits, h0, then (backward workloads only) the
+output gradient dO and the final-state gradient dht, then (DPLR only) a, the
+noise for a', the cosines and the eta logits -- all in float64 before the cast.
 
 Distributions (one per workload family):
 
@@ -17,6 +18,7 @@ Distributions (one per workload family):
 * g = -softplus(N(0, 1)) * 0.1 per channel (KDA, GLA, DPLR) or one value per
   token and head (GDN); absent for DeltaNet;
 * h0 ~ 0.1 N(0, 1) in float32 when requested;
+* backward: dO ~ N(0, 1) in the storage dtype, dht ~ N(0, 1) in float32;
 * DPLR: a unit; a' unit with cos(a, a') ~ U[0.9, 1]; b = eta a' with
   eta = 2 sigmoid(N(0, 1)).
 """
@@ -41,6 +43,7 @@ class Workload:
     dtype: torch.dtype
     h0: bool
     chunk: int = 64
+    grads: bool = False        # backward workload: also draw dO and dht
 
     @property
     def tokens(self) -> int:
@@ -50,8 +53,8 @@ class Workload:
         return replace(self, **kw)
 
 
-# The five workloads: a small fp32 KDA case, the KDA throughput case, the
-# special-case sweep and the general DPLR case.
+# The workloads: a small fp32 KDA case, the KDA throughput case, the
+# special-case sweep, the general DPLR case and the KDA backward case.
 WORKLOADS = {
     "kda_fp32_b1t256h1d64": Workload("kda_fp32_b1t256h1d64", "kda", 1, 256, 1, 64, 64, torch.float32, False),
     "kda_bf16_b4t4096h16d128": Workload("kda_bf16_b4t4096h16d128", "kda", 4, 4096, 16, 128, 128, torch.bfloat16, True),
@@ -59,6 +62,8 @@ WORKLOADS = {
     "deltanet_bf16_b8t2048h32d128": Workload("deltanet_bf16_b8t2048h32d128", "deltanet", 8, 2048, 32, 128, 128, torch.bfloat16, False),
     "gla_bf16_b8t2048h32d128": Workload("gla_bf16_b8t2048h32d128", "gla", 8, 2048, 32, 128, 128, torch.bfloat16, False),
     "dplr_bf16_b2t8192h16d128": Workload("dplr_bf16_b2t8192h16d128", "dplr", 2, 8192, 16, 128, 128, torch.bfloat16, False),
+    "kda_bwd_bf16_b4t4096h16d128": Workload("kda_bwd_bf16_b4t4096h16d128", "kda", 4, 4096, 16, 128, 128,
+                                            torch.bfloat16, True, grads=True),
 }
 
 
@@ -87,6 +92,9 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     gshape = (B, T, H) if w.variant == "gdn" else (B, T, H, dk)
     g_logits = torch.randn(*gshape, **f64)
     h0 = (0.1 * torch.randn(B, H, dv, dk, **f64)) if w.h0 else None
+    if w.grads:
+        do = torch.randn(B, T, H, dv, **f64)
+        dht = torch.randn(B, H, dv, dk, **f64)
 
     out = {"q": q, "k": k, "v": v}
     if w.variant in ("kda", "gdn", "deltanet"):
@@ -108,7 +116,10 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
         out["eta"] = eta[..., 0]
         out["a_prime"] = a_prime
 
-    for key in ("q", "k", "v", "g", "beta", "a", "b"):
+    if w.grads:
+        out["do"] = do
+        out["dht"] = dht.to(torch.float32)
+    for key in ("q", "k", "v", "g", "beta", "a", "b", "do"):
         if key in out:
             out[key] = out[key].to(w.dtype)
     if h0 is not None:
@@ -117,6 +128,6 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
 
 
 def custom(variant: str, B: int, T: int, H: int, dk: int, dv: int,
-           dtype=torch.bfloat16, h0: bool = False) -> Workload:
+           dtype=torch.bfloat16, h0: bool = False, grads: bool = False) -> Workload:
     """A workload of arbitrary shape with the distributions above (tests)."""
-    return Workload(f"{variant}_custom", variant, B, T, H, dk, dv, dtype, h0)
+    return Workload(f"{variant}_custom", variant, B, T, H, dk, dv, dtype, h0, grads=grads)

@@ -124,6 +124,52 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  */
 kda_status kda_chunk_fwd_noalloc(const kda_fwd_args *args, kda_stream_t stream);
 
+/* -------------------------------------------------------------- backward */
+
+/*
+ * Backward of kda_chunk_fwd: given dL/do (grad_o) and dL/dht (grad_ht), the
+ * gradients of L with respect to q, k, v, g, beta and h0.  It follows the
+ * chunk backward of page "Kimi Delta Attention backward": per chunk, in
+ * reverse, with dS the gradient of the state after the chunk,
+ *     dU = K-> Diag(gamma^C) dS^T + (Q<- K->^T * M)^T dO,   dW = -dU S_[t-1],
+ *     dS_[t-1] = dS Diag(gamma^C) + dO^T Q<- - dU^T W,
+ * then dQ, dK (both the K<- and K-> paths, with the output term), dV,
+ * dbeta (the form without beta^{-1}), dlog Gamma and its in-chunk suffix sum
+ * for dg.  The forward states are recomputed, not read from the forward call.
+ * Same variants as kda_chunk_fwd (gate kinds, beta NULL, the v-scaling flag).
+ */
+typedef struct {
+    int B, T, H;           /* as kda_fwd_args */
+    int dk, dv;            /* 64 or 128 each */
+    int chunk;             /* 0 (library's choice) or 32; the result does not depend on it */
+    kda_dtype dtype;       /* dtype of q, k, v, beta, grad_o and of grad_q, grad_k, grad_v, grad_beta */
+    kda_gate gate_kind;
+    kda_dtype g_dtype;     /* dtype of g and of grad_g */
+    unsigned flags;        /* KDA_FLAG_* */
+    const void *q, *k, *v, *g, *beta;   /* the forward's inputs, layouts of kda_fwd_args */
+    const float *h0;       /* [B, H, dv, dk] or NULL */
+    const void *grad_o;    /* [B, T, H, dv] dL/do */
+    const float *grad_ht;  /* [B, H, dv, dk] dL/dht, or NULL (zero) */
+    void *grad_q;          /* [B, T, H, dk] out */
+    void *grad_k;          /* [B, T, H, dk] out */
+    void *grad_v;          /* [B, T, H, dv] out */
+    void *grad_g;          /* layout of g, out; NULL iff g is NULL */
+    void *grad_beta;       /* [B, T, H] out; NULL iff beta is NULL */
+    float *grad_h0;        /* [B, H, dv, dk] out, or NULL (not written) */
+    void *workspace;       /* device buffer of kda_chunk_bwd_workspace bytes; its first 256
+                              bytes zero-filled before the first use */
+    size_t workspace_bytes;
+} kda_bwd_args;
+
+/*
+ * Bytes of workspace kda_chunk_bwd needs (0 on bad args): 256 for the status
+ * word plus the float32 chunk states, (2 ceil(T/32) + 1) B H dv dk 4 bytes.
+ */
+size_t kda_chunk_bwd_workspace(const kda_bwd_args *args);
+
+/* Backward of the chunkwise gated delta rule; float32 CUDA-core kernels. */
+kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream);
+
 /* ------------------------------------------------------------------ DPLR */
 
 /*

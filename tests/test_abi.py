@@ -139,3 +139,47 @@ def test_dplr_factor_norms_rejects_bad_arguments(lib):
     assert lib.dplr_factor_norms(ctypes.byref(a), (1 << 40) + 3 * (1 << 32), None, None, None) == \
         _lib.KDA_ERR_INVALID_ARG
     assert lib.dplr_factor_norms(ctypes.byref(_dplr_args(dk=96)), out, None, None, None) == _lib.KDA_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- backward entry points
+def _bwd_args(**over):
+    a = _lib.KdaBwdArgs()
+    a.B, a.T, a.H, a.dk, a.dv, a.chunk = 2, 100, 4, 128, 128, 0
+    a.dtype, a.gate_kind, a.g_dtype, a.flags = _lib.KDA_BF16, _lib.KDA_GATE_CHANNEL, _lib.KDA_BF16, 1
+    base = 1 << 40
+    names = ("q", "k", "v", "g", "beta", "h0", "grad_o", "grad_ht", "grad_q", "grad_k", "grad_v", "grad_g",
+             "grad_beta", "grad_h0", "workspace")
+    for i, f in enumerate(names):
+        setattr(a, f, base + i * (1 << 32))
+    a.workspace_bytes = 1 << 31
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_bwd_workspace_query(lib):
+    need = lib.kda_chunk_bwd_workspace(ctypes.byref(_bwd_args()))
+    n_chunks = (100 + 31) // 32
+    assert need == 256 + 4 * 2 * 4 * (2 * n_chunks + 1) * 128 * 128
+    assert lib.kda_chunk_bwd_workspace(ctypes.byref(_bwd_args(dk=96))) == 0
+    assert lib.kda_chunk_bwd_workspace(None) == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(grad_o=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(grad_q=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(grad_g=None), _lib.KDA_ERR_INVALID_ARG),                       # g given, no grad_g
+    (dict(grad_beta=None), _lib.KDA_ERR_INVALID_ARG),                    # beta given, no grad_beta
+    (dict(beta=None), _lib.KDA_ERR_INVALID_ARG),                         # grad_beta without beta
+    (dict(g=None, gate_kind=_lib.KDA_GATE_NONE), _lib.KDA_ERR_INVALID_ARG),
+    (dict(grad_k=(1 << 40) + 8 * (1 << 32)), _lib.KDA_ERR_INVALID_ARG),  # grad_k aliases grad_q
+    (dict(grad_v=(1 << 40) + 2 * (1 << 32)), _lib.KDA_ERR_INVALID_ARG),  # grad_v aliases v
+    (dict(grad_q=(1 << 40) + 8 * (1 << 32) + 2), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dk=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dv=32), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=64), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(workspace_bytes=4096), _lib.KDA_ERR_WORKSPACE),
+    (dict(workspace=None, workspace_bytes=0), _lib.KDA_ERR_WORKSPACE),
+])
+def test_bwd_rejects_bad_arguments_before_launch(lib, over, code):
+    assert lib.kda_chunk_bwd(ctypes.byref(_bwd_args(**over)), None) == code

@@ -1,0 +1,120 @@
+"""Backward of the chunkwise gated delta rule, CUDA (through the C ABI) vs the float64 oracle.
+
+The oracle is the reverse mode of the token recurrence (``oracle.recurrence_bwd``),
+for L = <dO, o> + <dht, ht>.  Every gradient (dq, dk, dv, dg, dbeta, dh0) is
+compared by relative Frobenius norm: 1e-5 for float32 inputs; 5e-3 for
+bfloat16 inputs (float32 arithmetic, gradients rounded to bf16 on store).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunkwise_gated_delta_gb300 import kda_chunk_bwd
+from chunkwise_gated_delta_gb300.inputs import WORKLOADS, custom, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 5e-3}
+DEV = "cuda:0"
+GATE = {"kda": "channel", "gla": "channel", "gdn": "scalar", "deltanet": "none"}
+
+
+def rel(x, ref):
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def f64(t):
+    return None if t is None else t.double().numpy()
+
+
+def run_gpu(x, variant, with_dht=True):
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    out = kda_chunk_bwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), d["do"],
+                        d["dht"] if with_dht else None, gate=GATE[variant], scale_v=x["scale_v"])
+    torch.cuda.synchronize()
+    return {k: v.double().cpu().numpy() for k, v in out.items()}
+
+
+def run_oracle(x, variant, with_dht=True, heads=None):
+    kw = dict(h0=f64(x.get("h0")), dht=f64(x["dht"]) if with_dht else None, heads=heads)
+    q, k, v, do = f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"])
+    if variant == "kda":
+        return oracle.kda_bwd(q, k, v, f64(x["g"]), f64(x["beta"]), do, **kw)
+    if variant == "gdn":
+        return oracle.gdn_bwd(q, k, v, f64(x["g"]), f64(x["beta"]), do, **kw)
+    if variant == "deltanet":
+        return oracle.deltanet_bwd(q, k, v, f64(x["beta"]), do, **kw)
+    return oracle.gla_bwd(q, k, v, f64(x["g"]), do, **kw)
+
+
+def compare(got, ref, tol, heads=None):
+    errs = {}
+    for key, r in ref.items():
+        g = got[key]
+        if heads is not None:
+            if key == "dh0":
+                g, r = np.stack([g[b, h] for b, h in heads]), np.stack([r[b, h] for b, h in heads])
+            else:
+                g, r = np.stack([g[b, :, h] for b, h in heads]), np.stack([r[b, :, h] for b, h in heads])
+        errs[key] = rel(g, r)
+    bad = {k: f"{e:.2e}" for k, e in errs.items() if not e <= tol}
+    assert not bad, f"over {tol}: {bad} (all: { {k: f'{e:.1e}' for k, e in errs.items()} })"
+    return errs
+
+
+def check(variant, dtype, B, T, H, dk, dv, h0=True, seed=0, with_dht=True):
+    x = make_inputs(custom(variant, B, T, H, dk, dv, dtype=dtype, h0=h0, grads=True), seed=seed)
+    got = run_gpu(x, variant, with_dht)
+    ref = run_oracle(x, variant, with_dht)
+    return compare(got, ref, TOL[dtype])
+
+
+# ---------------------------------------------------------------- float32
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 100, 256])
+def test_fp32_kda_lengths(T):
+    check("kda", torch.float32, 1, T, 2, 64, 64)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_fp32_kda_dims(dk, dv):
+    check("kda", torch.float32, 2, 90, 2, dk, dv)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "gla"])
+def test_fp32_special_cases(variant):
+    check(variant, torch.float32, 1, 130, 2, 64, 64)
+
+
+def test_fp32_no_h0_no_dht():
+    check("kda", torch.float32, 1, 97, 2, 64, 64, h0=False, with_dht=False)
+
+
+# ---------------------------------------------------------------- bfloat16
+@pytest.mark.parametrize("T", [1, 64, 65, 300])
+def test_bf16_kda_lengths(T):
+    check("kda", torch.bfloat16, 1, T, 2, 128, 128)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "gla"])
+def test_bf16_special_cases(variant):
+    check(variant, torch.bfloat16, 2, 200, 2, 128, 128)
+
+
+def test_bf16_deterministic():
+    x = make_inputs(custom("kda", 2, 150, 2, 128, 128, dtype=torch.bfloat16, h0=True, grads=True), seed=5)
+    a, b = run_gpu(x, "kda"), run_gpu(x, "kda")
+    for key in a:
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_full_kda_bwd_b4t4096h16d128_sampled_heads():
+    """The backward workload B4 T4096 H16 d128 bf16: every gradient of three sampled heads."""
+    w = WORKLOADS["kda_bwd_bf16_b4t4096h16d128"]
+    x = make_inputs(w, seed=0)
+    got = run_gpu(x, "kda")
+    heads = [(0, 0), (2, 9), (3, 15)]
+    ref = run_oracle(x, "kda", heads=heads)
+    compare(got, ref, 5e-3, heads=heads)
+    for v in got.values():
+        assert np.isfinite(v).all()
