@@ -47,7 +47,12 @@ CSRC = os.path.join(ROOT, "chunkwise_gated_delta_gb300", "csrc")
 # kernel that runs each variant's step: (name, source file)
 KERNELS = {"kda": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gdn": ("kda_fwd_tc", "kda_fwd_tc.cu"),
            "deltanet": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gla": ("kda_fwd_tc", "kda_fwd_tc.cu"),
-           "dplr": ("dplr_fwd_simt", "dplr_fwd_simt.cu")}
+           "dplr": ("dplr_fwd_simt", "dplr_fwd_simt.cu"), "kda_bwd": ("kda_bwd_simt", "kda_bwd_simt.cu")}
+LAUNCHES_PER_STEP = {"kda_bwd": 3}
+
+
+def kind_of(w) -> str:
+    return "kda_bwd" if w.grads else w.variant
 GATES = {"kda": "channel", "gla": "channel", "dplr": "channel", "gdn": "scalar", "deltanet": "none"}
 
 
@@ -55,6 +60,8 @@ def metric_for(w) -> str:
     if w.name == WORKLOAD:
         return METRIC
     shape = f"B{w.B}·T{w.T}·H{w.H}·d{w.dk}"
+    if w.grads:
+        return f"tokens/s KDA chunk bwd {shape} bf16; % of roofline"
     return f"tokens/s {w.variant.upper() if w.variant != 'deltanet' else 'DeltaNet'} chunk fwd {shape} bf16; % of roofline"
 
 
@@ -69,6 +76,11 @@ def algorithmic_bytes(w) -> int:
     es = 2 if w.dtype == torch.bfloat16 else 4
     state = w.B * w.H * w.dv * w.dk * 4
     states = state * (2 if w.h0 else 1)
+    if w.grads:
+        # reads q, k, v, g, beta, h0, dO, dht; writes dq, dk, dv, dg, dbeta, dh0
+        reads = bth * (3 * w.dk + 2 * w.dv + 1) * es + state * (2 if w.h0 else 1)
+        writes = bth * (3 * w.dk + w.dv + 1) * es + state
+        return reads + writes
     if w.variant == "dplr":
         return bth * (5 * w.dk + 2 * w.dv) * es + states
     seq = bth * (2 * w.dk + 2 * w.dv) * es
@@ -78,8 +90,8 @@ def algorithmic_bytes(w) -> int:
 
 
 def traffic_file(w) -> str:
-    shape = w.name.split("_", 2)[-1]
-    return os.path.join(ROOT, "profiles", f"{KERNELS[w.variant][0]}_{w.variant}_{shape}_traffic.txt")
+    shape = w.name.split("_")[-1]
+    return os.path.join(ROOT, "profiles", f"{KERNELS[kind_of(w)][0]}_{w.variant}_{shape}_traffic.txt")
 
 
 def measured_peaks():
@@ -93,7 +105,7 @@ def measured_peaks():
 def traffic_per_launch(w):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
     try:
-        src = os.path.join(CSRC, KERNELS[w.variant][1])
+        src = os.path.join(CSRC, KERNELS[kind_of(w)][1])
         src_hash = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         vals = {}
         for line in open(traffic_file(w)):
@@ -206,7 +218,10 @@ def oracle_sample(w, x, heads, T):
     cores = len(os.sched_getaffinity(0))
     kw = dict(h0=h0, heads=heads, threads=cores)
     t0 = time.perf_counter()
-    if w.variant == "kda":
+    if w.grads:
+        dht = x["dht"].double().numpy() if "dht" in x else None
+        oracle.kda_bwd(q, k, v, g, beta, f("do"), dht=dht, **kw)
+    elif w.variant == "kda":
         oracle.kda_fwd(q, k, v, g, beta, **kw)
     elif w.variant == "gdn":
         oracle.gdn_fwd(q, k, v, g, beta, **kw)
@@ -234,7 +249,8 @@ def cpu_baseline_leg(w, x, budget_s=12.0):
         tokens, dt, _ = oracle_sample(w, x, pairs[:n], w.T)
     return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {len(pairs)} (batch, head) pairs over the full T={w.T}, float64 token "
-                      f"recurrence in C, {cores} threads; tokens counted as head-tokens / H; {dt:.1f} s"}
+                      f"recurrence{' reverse mode' if w.grads else ''} in C, {cores} threads; tokens counted as "
+                      f"head-tokens / H; {dt:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -274,28 +290,40 @@ def run_reference(args, rank, world):
 def config_dict(w):
     inputs = {"kda": "bf16 q,k,v,g,beta", "gdn": "bf16 q,k,v,beta, g [B,T,H]", "deltanet": "bf16 q,k,v,beta",
               "gla": "bf16 q,k,v,g; beta = 0, v unscaled", "dplr": "bf16 q,k,v,a,b,g"}[w.variant]
-    inputs += "; fp32 h0/ht" if w.h0 else "; fp32 ht, no h0"
+    if w.grads:
+        inputs += ", dO; fp32 h0, dht; outputs bf16 dq,dk,dv,dg,dbeta, fp32 dh0"
+    else:
+        inputs += "; fp32 h0/ht" if w.h0 else "; fp32 ht, no h0"
     return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-            "chunk": 32 if w.variant == "dplr" else w.chunk, "h0": w.h0, "inputs": inputs,
+            "chunk": 32 if (w.variant == "dplr" or w.grads) else w.chunk, "h0": w.h0, "inputs": inputs,
             "l2": f"no flush: inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.1f} MB per step vs 129 MB)",
             "parallelism": "replicas (independent (batch, head) scans, no collective)"}
 
 
 def run_ours(args, rank, world, local):
-    from chunkwise_gated_delta_gb300 import HostRunner, dplr_chunk_fwd, dplr_factor_norms, kda_chunk_fwd
+    from chunkwise_gated_delta_gb300 import (HostRunner, dplr_chunk_fwd, dplr_factor_norms, kda_chunk_bwd,
+                                             kda_chunk_fwd)
     from chunkwise_gated_delta_gb300.inputs import WORKLOADS, make_inputs
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.workload]
     x = make_inputs(w, seed=rank)
-    x = {k: v for k, v in x.items() if k in ("q", "k", "v", "g", "beta", "h0", "a", "b", "scale_v")}
+    x = {k: v for k, v in x.items() if k in ("q", "k", "v", "g", "beta", "h0", "a", "b", "do", "dht", "scale_v")}
     d = {k: v.to(dev) for k, v in x.items() if isinstance(v, torch.Tensor)}
     o = torch.empty(w.B, w.T, w.H, w.dv, dtype=w.dtype, device=dev)
     ht = torch.empty(w.B, w.H, w.dv, w.dk, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     gate = GATES[w.variant]
 
-    if w.variant == "dplr":
+    if w.grads:
+        grads = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+                 "dg": torch.empty_like(d["g"]), "dbeta": torch.empty_like(d["beta"]),
+                 "dh0": torch.empty(w.B, w.H, w.dv, w.dk, dtype=torch.float32, device=dev)}
+
+        def step():
+            kda_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), d["do"], d["dht"], gate=gate,
+                          scale_v=x["scale_v"], grads=grads, stream=stream)
+    elif w.variant == "dplr":
         def step():
             dplr_chunk_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"), gate=gate,
                            o=o, ht=ht, stream=stream)
@@ -336,7 +364,7 @@ def run_ours(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         runner = HostRunner(x, device=dev, scale_v=x["scale_v"], gate=gate,
-                            kind="dplr" if w.variant == "dplr" else "kda")
+                            kind=kind_of(w) if kind_of(w) in ("dplr", "kda_bwd") else "kda")
         for _ in range(max(3, min(args.warmup, 10))):
             runner.run(stream)
         torch.cuda.synchronize()
@@ -375,11 +403,11 @@ def run_ours(args, rank, world, local):
         "config": config_dict(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_per_launch(w),
-                     "kernel": KERNELS[w.variant][0],
+                     "kernel": KERNELS[kind_of(w)][0],
                      "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                      "algorithmic_bytes_per_launch": abytes, "kernel_ms_per_launch": launch_ms},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * LAUNCHES_PER_STEP.get(kind_of(w), 1),
         "clocks": clk,
     }
     if w.variant == "dplr":
@@ -402,7 +430,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["kda_bf16_b4t4096h16d128", "gdn_bf16_b8t2048h32d128", "deltanet_bf16_b8t2048h32d128",
-                             "gla_bf16_b8t2048h32d128", "dplr_bf16_b2t8192h16d128"])
+                             "gla_bf16_b8t2048h32d128", "dplr_bf16_b2t8192h16d128", "kda_bwd_bf16_b4t4096h16d128"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()

@@ -308,28 +308,38 @@ def gla_fwd(q, k, v, g, h0=None, **kw):
 class HostRunner:
     """End-to-end call from pinned host buffers.
 
-    Each :meth:`run` copies the inputs host->device, runs the forward
-    (``kda_chunk_fwd``, or ``dplr_chunk_fwd`` when ``kind="dplr"``) and copies
-    o and ht back device->host, all on one stream.  Device buffers are
-    allocated once and reused.
+    Each :meth:`run` copies the inputs host->device, runs the call
+    (``kda_chunk_fwd``; ``dplr_chunk_fwd`` when ``kind="dplr"``;
+    ``kda_chunk_bwd`` when ``kind="kda_bwd"``) and copies its results back
+    device->host (o and ht, or every gradient), all on one stream.  Device
+    buffers are allocated once and reused.
     """
 
+    _INPUTS = ("q", "k", "v", "g", "beta", "h0", "a", "b", "do", "dht")
+
     def __init__(self, host: dict, device="cuda", scale_v=True, gate=None, kind="kda"):
-        if kind not in ("kda", "dplr"):
+        if kind not in ("kda", "dplr", "kda_bwd"):
             raise ValueError(f"unknown kind {kind}")
-        self.host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()
-                     if k in ("q", "k", "v", "g", "beta", "h0", "a", "b")}
+        self.host = {k: v.pin_memory() for k, v in host.items() if k in self._INPUTS and isinstance(v, torch.Tensor)}
         self.dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()}
         q = self.dev["q"]
-        B, T, H, _ = q.shape
-        dv, dk = self.dev["v"].shape[-1], q.shape[-1]
-        self.o = torch.empty(B, T, H, dv, dtype=q.dtype, device=device)
-        self.ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)
-        self.o_host = torch.empty_like(self.o, device="cpu").pin_memory()
-        self.ht_host = torch.empty_like(self.ht, device="cpu").pin_memory()
+        B, T, H, dk = q.shape
+        dv = self.dev["v"].shape[-1]
         self.scale_v, self.gate, self.kind = scale_v, gate, kind
+        if kind == "kda_bwd":
+            d = self.dev
+            self.outs = {"dq": torch.empty_like(q), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+                         "dh0": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
+            if "g" in d:
+                self.outs["dg"] = torch.empty_like(d["g"])
+            if "beta" in d:
+                self.outs["dbeta"] = torch.empty_like(d["beta"])
+        else:
+            self.outs = {"o": torch.empty(B, T, H, dv, dtype=q.dtype, device=device),
+                         "ht": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
+        self.outs_host = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in self.outs.items()}
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.dev.values())
-        self.d2h_bytes = self.o.numel() * self.o.element_size() + self.ht.numel() * 4
+        self.d2h_bytes = sum(v.numel() * v.element_size() for v in self.outs.values())
 
     def run(self, stream=None):
         stream = stream or torch.cuda.current_stream()
@@ -339,10 +349,14 @@ class HostRunner:
             d = self.dev
             if self.kind == "dplr":
                 dplr_chunk_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"),
-                               gate=self.gate, o=self.o, ht=self.ht, stream=stream)
+                               gate=self.gate, o=self.outs["o"], ht=self.outs["ht"], stream=stream)
+            elif self.kind == "kda_bwd":
+                kda_chunk_bwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), d["do"],
+                              d.get("dht"), gate=self.gate, scale_v=self.scale_v, grads=self.outs, stream=stream)
             else:
                 kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"),
-                              gate=self.gate, scale_v=self.scale_v, o=self.o, ht=self.ht, stream=stream)
-            self.o_host.copy_(self.o, non_blocking=True)
-            self.ht_host.copy_(self.ht, non_blocking=True)
-        return self.o_host, self.ht_host
+                              gate=self.gate, scale_v=self.scale_v, o=self.outs["o"], ht=self.outs["ht"],
+                              stream=stream)
+            for k, v in self.outs.items():
+                self.outs_host[k].copy_(v, non_blocking=True)
+        return self.outs_host
