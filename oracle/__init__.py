@@ -34,7 +34,7 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-from .spectral import factor_norm_exact, rho_closed_form  # noqa: F401
+from .spectral import clip_gate, clip_gate_bwd, factor_norm_exact, rho_closed_form, rho_of  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "recurrence.c")
@@ -59,6 +59,10 @@ PINS = {
     "rho_closed_form": ["numpy SVD", "eq. (5) lower bound", "eq. (6) equality case",
                         "hand-derived values, tests/golden/spectral_norm_points.txt"],
     "factor_norm_exact": ["explicit 2x2 reduction of eq. (9)", "D = I reduces to rho"],
+    "clip_gate": ["after the clip every factor norm (numpy SVD) is at most 1",
+                  "eq. (6): the KDA mapping (a = k unit, b = beta k, beta <= 2) leaves g unchanged",
+                  "only channels above -log rho change"],
+    "clip_gate_bwd / dplr_bwd(clip=True)": ["central finite differences of dplr_fwd(clip=True)"],
     "recurrence_bwd": [
         "central finite differences of the forward oracle on every input entry (T = 64, all five variants)",
         "central finite differences on sampled entries across four checkpoint segments",
@@ -266,9 +270,29 @@ def gla_bwd(q, k, v, g, do, h0=None, dht=None, **kw):
     return recurrence_bwd(q, k, v, do, g=g, gate=GATE_CHANNEL, beta=None, scale_v=False, h0=h0, dht=dht, **kw)
 
 
-def dplr_bwd(q, k, v, a, b, g, do, h0=None, dht=None, **kw):
-    """General gated DPLR backward: dq, dk, dv, da, db, dg, dh0."""
-    return recurrence_bwd(q, k, v, do, g=g, gate=GATE_CHANNEL, a=a, b=b, scale_v=False, h0=h0, dht=dht, **kw)
+def dplr_bwd(q, k, v, a, b, g, do, h0=None, dht=None, clip=False, **kw):
+    """General gated DPLR backward: dq, dk, dv, da, db, dg, dh0.
+
+    clip=True differentiates the forward with the eq. (7) clip applied to g
+    (page "How to make GDN2 more stable"): the reverse mode runs on the
+    clipped gate and the clip's chain rule maps its gate gradient back onto
+    g, a and b.
+    """
+    if not clip:
+        return recurrence_bwd(q, k, v, do, g=g, gate=GATE_CHANNEL, a=a, b=b, scale_v=False, h0=h0, dht=dht, **kw)
+    gc = clip_gate(g, a, b)
+    out = recurrence_bwd(q, k, v, do, g=gc, gate=GATE_CHANNEL, a=a, b=b, scale_v=False, h0=h0, dht=dht, **kw)
+    dg, da, db = clip_gate_bwd(g, a, b, out["dg"])
+    heads = kw.get("heads")
+    if heads is not None:          # keep the untouched heads at zero, as recurrence_bwd does
+        mask = np.zeros(np.asarray(g).shape[:3], dtype=bool)
+        for bi, hi in heads:
+            mask[bi, :, hi] = True
+        dg, da, db = (np.where(mask[..., None], x, 0.0) for x in (dg, da, db))
+    out["dg"] = dg
+    out["da"] = out["da"] + da
+    out["db"] = out["db"] + db
+    return out
 
 
 def kda_fwd(q, k, v, g, beta, h0=None, **kw):
@@ -291,6 +315,12 @@ def gla_fwd(q, k, v, g, h0=None, **kw):
     return recurrence(q, k, v, g=g, gate=GATE_CHANNEL, beta=None, scale_v=False, h0=h0, **kw)
 
 
-def dplr_fwd(q, k, v, a, b, g, h0=None, **kw):
-    """General gated DPLR: independent a, b [B,T,H,dk]; vv = v."""
+def dplr_fwd(q, k, v, a, b, g, h0=None, clip=False, **kw):
+    """General gated DPLR: independent a, b [B,T,H,dk]; vv = v.
+
+    clip=True applies the eq. (7) clip of page "How to make GDN2 more stable"
+    to the gate first: g -> min(g, -log ||I - b a^T||_2) token by token.
+    """
+    if clip:
+        g = clip_gate(g, a, b)
     return recurrence(q, k, v, g=g, gate=GATE_CHANNEL, a=a, b=b, scale_v=False, h0=h0, **kw)

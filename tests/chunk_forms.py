@@ -205,3 +205,83 @@ def gla_parallel_grads(q, k, v, g, do):
     dv = A.T @ do
     dlg = q * dq - k * dk
     return dq, dk, dv, np.cumsum(dlg[::-1], axis=0)[::-1]
+
+
+def dplr_chunk_bwd_form(q, k, v, a, b, g, do, h0=None, dht=None, C=64):
+    """Gated DPLR chunk backward of page "Diagonal Plus Low Rank", section 3 (one head).
+
+    Forward per chunk as dplr_chunk_form, with F = I + (B<- A->^T * M_{-1}),
+    E = F^{-1}, V_1 = V, V_2 = C - W S^T.  Backward per chunk, in reverse,
+    dS the gradient of the state after the chunk:
+      dC = dV_2 = A-> Diag(gamma^C) dS^T + (Q<- A->^T * M)^T dO;
+      dV_1 = K-> Diag(gamma^C) dS^T + (Q<- K->^T * M)^T dO;   dW = -dC S_prev;
+      dE = -dC V^T (B<- K->^T * M_{-1})^T + dW B<-^T;   dF = -E^T dE E^T;
+      dQ<- = dO S_prev + (dO V_1^T * M) K-> + (dO V_2^T * M) A->;
+      dB<- = E^T dW - (E^T dC V^T * M_{-1}) K-> + (dF * M_{-1}) A->;
+      dK-> = (dO V_1^T * M)^T Q<- - (E^T dC V^T * M_{-1})^T B<- + V_1 dS Diag(gamma^C);
+      dA-> = (dO V_2^T * M)^T Q<- + (dF * M_{-1})^T B<- + V_2 dS Diag(gamma^C);
+      dV = dV_1 - (B<- K->^T * M_{-1})^T E^T dC;
+      dq = dQ<- * Gamma, db = dB<- * Gamma, dk = dK-> / Gamma, da = dA-> / Gamma;
+      dlogGamma = dQ<- * Q<- + dB<- * B<- - dK-> * K-> - dA-> * A->, last row + diag(S^T dS);
+      dS_prev = dS Diag(gamma^C) + dO^T Q<- - dC^T W.
+    Readings: dW against S_[t-1] (the page writes S_[t]); dB = dB<- * Gamma
+    (the page writes dQ<-); dK-> and dA-> carry the state-update terms
+    V_1 dS Diag(gamma^C) and V_2 dS Diag(gamma^C), which the page's lines omit.
+    Returns dq, dk, dv, da, db, dg, dh0.
+    """
+    T, dk = q.shape
+    dv = v.shape[1]
+    S = np.zeros((dv, dk)) if h0 is None else h0.copy()
+    starts = list(range(0, T, C))
+    prev = []
+    for s in starts:
+        e = min(s + C, T)
+        n = e - s
+        _, M1 = _masks(n)
+        Gam = np.exp(np.cumsum(g[s:e], axis=0))
+        Kr, Ar, Bl = k[s:e] / Gam, a[s:e] / Gam, b[s:e] * Gam
+        E = np.linalg.inv(np.eye(n) + (Bl @ Ar.T) * M1)
+        W = E @ Bl
+        Cm = -E @ ((Bl @ Kr.T) * M1) @ v[s:e]
+        prev.append(S.copy())
+        S = (S + v[s:e].T @ Kr + (Cm - W @ S.T).T @ Ar) * Gam[-1][None, :]
+    out = {n: np.zeros_like(x) for n, x in (("dq", q), ("dk", k), ("dv", v), ("da", a), ("db", b), ("dg", g))}
+    dS = np.zeros((dv, dk)) if dht is None else dht.copy()
+    for idx in reversed(range(len(starts))):
+        s = starts[idx]
+        e = min(s + C, T)
+        n = e - s
+        M, M1 = _masks(n)
+        Sp = prev[idx]
+        Gam = np.exp(np.cumsum(g[s:e], axis=0))
+        gC = Gam[-1]
+        V, dO = v[s:e], do[s:e]
+        Ql, Kr, Ar, Bl = q[s:e] * Gam, k[s:e] / Gam, a[s:e] / Gam, b[s:e] * Gam
+        Nbk = (Bl @ Kr.T) * M1
+        E = np.linalg.inv(np.eye(n) + (Bl @ Ar.T) * M1)
+        W = E @ Bl
+        Cm = -E @ Nbk @ V
+        V2 = Cm - W @ Sp.T
+        Pk, Pa = (Ql @ Kr.T) * M, (Ql @ Ar.T) * M
+        St = (Sp + V.T @ Kr + V2.T @ Ar) * gC[None, :]
+        dC = (Ar * gC[None, :]) @ dS.T + Pa.T @ dO
+        dV1 = (Kr * gC[None, :]) @ dS.T + Pk.T @ dO
+        dW = -dC @ Sp
+        dE = -dC @ V.T @ Nbk.T + dW @ Bl.T
+        dF = -E.T @ dE @ E.T
+        O1, O2 = (dO @ V.T) * M, (dO @ V2.T) * M
+        G = (E.T @ dC @ V.T) * M1
+        dQl = dO @ Sp + O1 @ Kr + O2 @ Ar
+        dBl = E.T @ dW - G @ Kr + (dF * M1) @ Ar
+        dKr = O1.T @ Ql - G.T @ Bl + (V @ dS) * gC[None, :]
+        dAr = O2.T @ Ql + (dF * M1).T @ Bl + (V2 @ dS) * gC[None, :]
+        dV = dV1 - Nbk.T @ E.T @ dC
+        dlg = dQl * Ql + dBl * Bl - dKr * Kr - dAr * Ar
+        dlg[-1] += (St * dS).sum(0)
+        out["dq"][s:e], out["db"][s:e] = dQl * Gam, dBl * Gam
+        out["dk"][s:e], out["da"][s:e] = dKr / Gam, dAr / Gam
+        out["dv"][s:e] = dV
+        out["dg"][s:e] = np.cumsum(dlg[::-1], axis=0)[::-1]
+        dS = dS * gC[None, :] + dO.T @ Ql - dC.T @ W
+    out["dh0"] = dS
+    return out

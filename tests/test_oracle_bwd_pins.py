@@ -8,6 +8,11 @@ The backward oracle is checked against things that are not itself:
   numpy (``chunk_forms.kda_chunk_bwd_form``) for several chunk sizes;
 * the closed-form gradients of the GLA parallel form (page "Gated Linear
   Attention", section 6.3) when beta = 0;
+* the DPLR chunk backward of page "Diagonal Plus Low Rank", section 3,
+  restated in numpy (``chunk_forms.dplr_chunk_bwd_form``, with its readings);
+* the eq. (7) clip of page "How to make GDN2 more stable": after it every
+  factor norm (numpy SVD) is at most 1, eq. (6)'s KDA case is left alone, and
+  the clip's chain rule agrees with central differences;
 * and mutated copies of the reverse mode (a dropped term, a wrong sign, the
   gate gradient taken against the wrong state) fail the finite-difference pin.
 """
@@ -216,3 +221,60 @@ def test_fd_pin_catches_planted_mistakes(mode):
             fd = _fd(fwd, x, do, dht, name, idx)
             worst = max(worst, abs(bad[_grad_key(name)][idx[1]][idx[3]] - fd))
     assert worst > 1e-4
+
+
+# --------------------------------------------------------------------------
+# DPLR: the page's chunk backward and the eq. (7) clip
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("C", [16, 32, 64])
+def test_dplr_chunk_backward_of_the_page_equals_reverse_mode(C):
+    from chunk_forms import dplr_chunk_bwd_form
+    x, do, dht = _case(9, T=150, dk=8, dv=6)
+    one = lambda n: x[n][0, :, 0]
+    ref = dplr_chunk_bwd_form(one("q"), one("k"), one("v"), one("a"), one("b"), one("g"), do[0, :, 0],
+                              x["h0"][0, 0], dht[0, 0], C=C)
+    got = oracle.dplr_bwd(x["q"], x["k"], x["v"], x["a"], x["b"], x["g"], do, x["h0"], dht)
+    for key in ("dq", "dk", "dv", "da", "db", "dg", "dh0"):
+        g_ = got[key][0, :, 0] if key != "dh0" else got[key][0, 0]
+        np.testing.assert_allclose(g_, ref[key], rtol=1e-9, atol=1e-11, err_msg=key)
+
+
+def test_clip_bounds_every_factor_norm_by_one():
+    """Eq. (7): after g -> min(g, -log rho) every ||Diag(alpha)(I - b a^T)||_2 <= 1 (numpy SVD)."""
+    x, _, _ = _case(10, T=50, dk=8)
+    a, b = x["a"][0, :, 0], 1.6 * x["b"][0, :, 0]
+    g = x["g"][0, :, 0] * 0.2                      # weak decay: the unclipped factors exceed 1
+    before = oracle.factor_norm_exact(np.exp(g), a, b)
+    after = oracle.factor_norm_exact(np.exp(oracle.clip_gate(g, a, b)), a, b)
+    assert before.max() > 1.05
+    assert after.max() <= 1 + 1e-12
+
+
+def test_clip_leaves_kda_mapping_and_small_channels_alone():
+    """Eq. (6): a = k unit, b = beta k with beta <= 2 gives rho = 1, so the clip changes nothing;
+    in general only channels above -log rho change."""
+    x, _, _ = _case(11, T=40, dk=8)
+    k, beta, g = x["k"][0, :, 0], x["beta"][0, :, 0], x["g"][0, :, 0]
+    np.testing.assert_array_equal(oracle.clip_gate(g, k, 2 * beta[:, None] * k), g)
+    a, b = x["a"][0, :, 0], x["b"][0, :, 0]
+    gc = oracle.clip_gate(g, a, b)
+    lim = -np.log(oracle.rho_of(a, b))[:, None]
+    np.testing.assert_array_equal(gc[g <= lim], g[g <= lim])
+    assert np.all(gc[g > lim] == np.broadcast_to(lim, g.shape)[g > lim])
+
+
+def test_dplr_clip_backward_finite_differences():
+    """dplr_bwd(clip=True) against central differences of dplr_fwd(clip=True) on every entry."""
+    x, do, dht = _case(12, T=40, dk=5, dv=4)
+    x["b"] = 1.5 * x["b"]                          # rho well above 1 on many tokens: the clip is active
+    names = ("q", "k", "v", "a", "b", "g", "h0")
+    fwd = lambda y: oracle.dplr_fwd(y["q"], y["k"], y["v"], y["a"], y["b"], y["g"], y["h0"], clip=True, threads=1)
+    grads = oracle.dplr_bwd(x["q"], x["k"], x["v"], x["a"], x["b"], x["g"], do, x["h0"], dht, clip=True)
+    gc = oracle.clip_gate(x["g"], x["a"], x["b"])
+    assert (gc < x["g"]).mean() > 0.2               # the clip acts on a good share of the channels
+    for name in names:
+        fd = np.zeros_like(x[name])
+        for idx in np.ndindex(*x[name].shape):
+            fd[idx] = _fd(fwd, x, do, dht, name, idx)
+        err = np.linalg.norm(grads[_grad_key(name)] - fd) / np.linalg.norm(fd)
+        assert err <= 1e-6, f"d{name}: {err:.2e}"
