@@ -26,7 +26,9 @@ KDA_FLAG_BETA_SCALES_V = 1
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_fwd_workspace", "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_status_read",
            "kda_status_string", "kda_chunk_bwd_workspace", "kda_chunk_bwd", "dplr_chunk_fwd_workspace",
-           "dplr_chunk_fwd", "dplr_factor_norms")
+           "dplr_chunk_fwd", "dplr_factor_norms", "dplr_chunk_bwd_workspace", "dplr_chunk_bwd")
+
+DPLR_FLAG_CLIP_GATE = 1
 
 
 class KdaFwdArgs(ctypes.Structure):
@@ -62,9 +64,26 @@ class DplrFwdArgs(ctypes.Structure):
         ("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
         ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("chunk", ctypes.c_int),
         ("dtype", ctypes.c_int), ("gate_kind", ctypes.c_int), ("g_dtype", ctypes.c_int),
+        ("flags", ctypes.c_uint),
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("g", ctypes.c_void_p),
         ("h0", ctypes.c_void_p), ("o", ctypes.c_void_p), ("ht", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class DplrBwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+        ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("chunk", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("gate_kind", ctypes.c_int), ("g_dtype", ctypes.c_int),
+        ("flags", ctypes.c_uint),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("g", ctypes.c_void_p),
+        ("h0", ctypes.c_void_p), ("grad_o", ctypes.c_void_p), ("grad_ht", ctypes.c_void_p),
+        ("grad_q", ctypes.c_void_p), ("grad_k", ctypes.c_void_p), ("grad_v", ctypes.c_void_p),
+        ("grad_a", ctypes.c_void_p), ("grad_b", ctypes.c_void_p), ("grad_g", ctypes.c_void_p),
+        ("grad_h0", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -104,6 +123,10 @@ def load() -> ctypes.CDLL:
         lib.dplr_factor_norms.restype = ctypes.c_int
         lib.dplr_factor_norms.argtypes = [ctypes.POINTER(DplrFwdArgs), ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p]
+        lib.dplr_chunk_bwd_workspace.restype = ctypes.c_size_t
+        lib.dplr_chunk_bwd_workspace.argtypes = [ctypes.POINTER(DplrBwdArgs)]
+        lib.dplr_chunk_bwd.restype = ctypes.c_int
+        lib.dplr_chunk_bwd.argtypes = [ctypes.POINTER(DplrBwdArgs), ctypes.c_void_p]
         lib.kda_status_read.restype = ctypes.c_int
         lib.kda_status_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
         lib.kda_status_string.restype = ctypes.c_char_p

@@ -202,7 +202,7 @@ def kda_chunk_bwd(q, k, v, g, beta, h0, do, dht=None, *, gate=None, scale_v=True
     return out
 
 
-def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None,
+def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None, clip=False,
                    workspace=None) -> _lib.DplrFwdArgs:
     """Fill the C DPLR argument struct from tensors (q, k, v, o may be None for the norm report)."""
     B, T, H, dk = a.shape
@@ -214,6 +214,7 @@ def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None
     x.dtype = _dtype_code(a)
     x.gate_kind = _GATES[gate]
     x.g_dtype = _dtype_code(g) if g is not None else _lib.KDA_BF16
+    x.flags = _lib.DPLR_FLAG_CLIP_GATE if clip else 0
     x.q, x.k, x.v, x.a, x.b, x.g = _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(g)
     x.h0, x.o, x.ht = _ptr(h0), _ptr(o), _ptr(ht)
     if workspace is not None:
@@ -222,12 +223,13 @@ def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None
     return x
 
 
-def dplr_chunk_fwd(q, k, v, a, b, g=None, h0=None, *, gate=None, output_final_state=True,
+def dplr_chunk_fwd(q, k, v, a, b, g=None, h0=None, *, gate=None, clip=False, output_final_state=True,
                    o=None, ht=None, workspace=None, stream=None):
     """General gated DPLR forward through ``dplr_chunk_fwd`` of the C ABI.
 
     q, k, a, b: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, one dtype);
     g: log-decay [B, T, H, dk], [B, T, H] or None; h0: [B, H, dv, dk] fp32 or None.
+    clip=True applies the eq. (7) gate clip (``DPLR_FLAG_CLIP_GATE``).
     Returns (o [B, T, H, dv] in q's dtype, ht [B, H, dv, dk] fp32 or None).
     """
     lib = _lib.load()
@@ -239,7 +241,7 @@ def dplr_chunk_fwd(q, k, v, a, b, g=None, h0=None, *, gate=None, output_final_st
         o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
     if ht is None and output_final_state:
         ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device)
-    args = make_dplr_args(q, k, v, a, b, g, h0, o, ht, gate=gate)
+    args = make_dplr_args(q, k, v, a, b, g, h0, o, ht, gate=gate, clip=clip)
     need = lib.dplr_chunk_fwd_workspace(ctypes.byref(args))
     if need == 0:
         rc = lib.dplr_chunk_fwd(ctypes.byref(args), None)
@@ -256,7 +258,7 @@ def dplr_chunk_fwd(q, k, v, a, b, g=None, h0=None, *, gate=None, output_final_st
     return o, ht
 
 
-def dplr_factor_norms(a, b, g=None, *, gate=None, stream=None):
+def dplr_factor_norms(a, b, g=None, *, gate=None, clip=False, stream=None):
     """Per-token transition norms through ``dplr_factor_norms`` of the C ABI.
 
     Returns (rho [B, T, H], norm [B, T, H], maxes [2]) float32 on a's device:
@@ -270,7 +272,7 @@ def dplr_factor_norms(a, b, g=None, *, gate=None, stream=None):
     rho = torch.empty(B, T, H, dtype=torch.float32, device=a.device)
     nrm = torch.empty_like(rho)
     maxes = torch.empty(4, dtype=torch.float32, device=a.device)
-    args = make_dplr_args(None, None, None, a, b, g, gate=gate)
+    args = make_dplr_args(None, None, None, a, b, g, gate=gate, clip=clip)
     if stream is None:
         stream = torch.cuda.current_stream(a.device)
     rc = lib.dplr_factor_norms(ctypes.byref(args), _ptr(rho), _ptr(nrm), _ptr(maxes),
@@ -278,6 +280,54 @@ def dplr_factor_norms(a, b, g=None, *, gate=None, stream=None):
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "dplr_factor_norms")
     return rho, nrm, maxes[:2]
+
+
+def dplr_chunk_bwd(q, k, v, a, b, g, h0, do, dht=None, *, gate=None, clip=False, grads=None,
+                   workspace=None, stream=None):
+    """Backward of :func:`dplr_chunk_fwd` through ``dplr_chunk_bwd`` of the C ABI.
+
+    Returns a dict with dq, dk, dv, da, db (dtype of q), dg (dtype and layout
+    of g) when g is given, and dh0 (fp32).  ``grads`` may supply preallocated
+    outputs by those names.
+    """
+    lib = _lib.load()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (g, "g"), (h0, "h0"), (do, "do"),
+                    (dht, "dht")):
+        _check(t, name)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    out = dict(grads or {})
+    for name, like in (("dq", q), ("dk", k), ("dv", v), ("da", a), ("db", b)):
+        out.setdefault(name, torch.empty_like(like))
+    if g is not None:
+        out.setdefault("dg", torch.empty_like(g))
+    out.setdefault("dh0", torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device))
+    if gate is None:
+        gate = "none" if g is None else ("scalar" if g.dim() == 3 else "channel")
+    x = _lib.DplrBwdArgs()
+    x.B, x.T, x.H, x.dk, x.dv, x.chunk = B, T, H, dk, dv, 0
+    x.dtype = _dtype_code(q)
+    x.gate_kind = _GATES[gate]
+    x.g_dtype = _dtype_code(g) if g is not None else _lib.KDA_BF16
+    x.flags = _lib.DPLR_FLAG_CLIP_GATE if clip else 0
+    x.q, x.k, x.v, x.a, x.b, x.g, x.h0 = (_ptr(t) for t in (q, k, v, a, b, g, h0))
+    x.grad_o, x.grad_ht = _ptr(do), _ptr(dht)
+    x.grad_q, x.grad_k, x.grad_v = _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"])
+    x.grad_a, x.grad_b, x.grad_g, x.grad_h0 = _ptr(out["da"]), _ptr(out["db"]), _ptr(out.get("dg")), _ptr(out["dh0"])
+    need = lib.dplr_chunk_bwd_workspace(ctypes.byref(x))
+    if need == 0:
+        rc = lib.dplr_chunk_bwd(ctypes.byref(x), None)
+        raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "dplr_chunk_bwd")
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    x.workspace = _ptr(workspace)
+    x.workspace_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = lib.dplr_chunk_bwd(ctypes.byref(x), ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.KDA_OK:
+        raise KdaError(rc, "dplr_chunk_bwd")
+    return out
 
 
 def status_read(workspace=None, device=None, stream=None) -> int:

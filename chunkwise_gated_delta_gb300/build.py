@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
 
-SOURCES = ["kda_api.cu", "kda_fwd_simt.cu", "kda_fwd_tc.cu", "kda_noalloc.cu", "dplr_fwd_simt.cu", "kda_bwd_simt.cu"]
+SOURCES = ["kda_api.cu", "kda_fwd_simt.cu", "kda_fwd_tc.cu", "kda_noalloc.cu", "dplr_fwd_simt.cu", "kda_bwd_simt.cu", "dplr_bwd_simt.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -1,0 +1,145 @@
+// Device helpers shared by the DPLR forward and backward kernels.
+//
+// The gated DPLR recurrence S_t = S_{t-1} Diag(alpha_t)(I - b_t a_t^T) + v_t k_t^T
+// (page "Diagonal Plus Low Rank", section 2) in its chunk form needs, per
+// chunk, Gamma = exp(in-chunk cumsum of the log-decay) and the rescaled tiles
+// Q<- = Q * Gamma, K-> = K / Gamma, A-> = A / Gamma, B<- = B * Gamma.
+//
+// With the clip of page "How to make GDN2 more stable", eq. (7), the decay of
+// token t is min(D_t, 1/rho_t), rho_t = ||I - b_t a_t^T||_2 from eq. (4):
+// in log space g'_t = min(g_t, -log rho_t), with eta = |a||b| and
+// c = a.b / eta, rho = (eta + sqrt(eta^2 - 4 eta c + 4)) / 2.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace dplr {
+
+template <typename T> __device__ __forceinline__ float ldf(const T *p, size_t i);
+template <> __device__ __forceinline__ float ldf<float>(const float *p, size_t i) { return p[i]; }
+template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+template <typename T> __device__ __forceinline__ void stf(T *p, size_t i, float x);
+template <> __device__ __forceinline__ void stf<float>(float *p, size_t i, float x) { p[i] = x; }
+template <> __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Eq. (4) for one token from |a|^2, |b|^2 and a.b.
+__device__ __forceinline__ float rho_eq4(float na2, float nb2, float ab) {
+    const float eta = sqrtf(na2 * nb2);
+    const float cosv = eta > 0.f ? ab / eta : 1.f;
+    return 0.5f * (eta + sqrtf(fmaxf(eta * eta - 4.f * eta * cosv + 4.f, 0.f)));
+}
+
+// Per row c < C of the chunk starting at t0: rows[c] = (|a|^2, |b|^2, a.b, -log rho)
+// (zeros past nvalid).  One warp per row; no barrier inside.
+template <int DK, int C, typename Tin>
+__device__ void row_rho(const DplrParams &p, int b, int h, int t0, int nvalid, float4 *rows) {
+    const Tin *a = static_cast<const Tin *>(p.a);
+    const Tin *bb = static_cast<const Tin *>(p.b);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int c = warp; c < C; c += nwarps) {
+        float na2 = 0.f, nb2 = 0.f, ab = 0.f;
+        if (c < nvalid) {
+            const size_t row = (((size_t)b * p.T + t0 + c) * p.H + h) * DK;
+            for (int d = lane; d < DK; d += 32) {
+                const float av = ldf(a, row + d), bv = ldf(bb, row + d);
+                na2 += av * av;
+                nb2 += bv * bv;
+                ab += av * bv;
+            }
+        }
+        na2 = warp_sum(na2);
+        nb2 = warp_sum(nb2);
+        ab = warp_sum(ab);
+        if (lane == 0) rows[c] = make_float4(na2, nb2, ab, c < nvalid ? -logf(rho_eq4(na2, nb2, ab)) : 0.f);
+    }
+}
+
+// The (optionally clipped) log-decay of token row `row` (flattened (b, t, h)), channel d.
+template <typename Tg>
+__device__ __forceinline__ float gate_of(const DplrParams &p, size_t row, int d, int dk, const float4 *rows, int c) {
+    const Tg *g = static_cast<const Tg *>(p.g);
+    float gv = 0.f;
+    if (p.gate_kind == KDA_GATE_CHANNEL) gv = ldf(g, row * dk + d);
+    else if (p.gate_kind == KDA_GATE_SCALAR) gv = ldf(g, row);
+    if (p.clip) gv = fminf(gv, rows[c].w);
+    return gv;
+}
+
+// Gamma and the rescaled tiles of one chunk, one key channel per thread
+// (rows past nvalid are zero, Gamma held at its last value); any tile pointer
+// may be null; gam[d] = gamma^C.  `rows` comes from row_rho when p.clip is set
+// (a barrier must separate the two).
+template <int DK, int C, typename Tin, typename Tg>
+__device__ void load_rescaled(const DplrParams &p, int b, int h, int t0, int nvalid, const float4 *rows, float *Gm,
+                              float *Ql, float *Kr, float *Ar, float *Bl, float *gam) {
+    constexpr int SK = DK + 1;
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *a = static_cast<const Tin *>(p.a);
+    const Tin *bb = static_cast<const Tin *>(p.b);
+    for (int d = threadIdx.x; d < DK; d += blockDim.x) {
+        float G = 0.f, gm = 1.f;
+        for (int c = 0; c < C; ++c) {
+            float qv = 0.f, kv = 0.f, av = 0.f, bv = 0.f;
+            if (c < nvalid) {
+                const size_t row = ((size_t)b * p.T + t0 + c) * p.H + h;
+                if (Ql) qv = ldf(q, row * DK + d);
+                if (Kr) kv = ldf(k, row * DK + d);
+                if (Ar) av = ldf(a, row * DK + d);
+                if (Bl) bv = ldf(bb, row * DK + d);
+                G += gate_of<Tg>(p, row, d, DK, rows, c);
+                gm = expf(G);
+            }
+            if (Gm) Gm[c * SK + d] = gm;
+            if (Ql) Ql[c * SK + d] = qv * gm;
+            if (Kr) Kr[c * SK + d] = kv / gm;
+            if (Ar) Ar[c * SK + d] = av / gm;
+            if (Bl) Bl[c * SK + d] = bv * gm;
+        }
+        gam[d] = gm;
+    }
+}
+
+// E = (I + (B<- A->^T * M_{-1}))^{-1}: the strict-lower Gram into Nm, then
+// forward substitution, one column per thread of the first warp.  Starts and
+// ends with a barrier.
+template <int DK, int C>
+__device__ void inverse_e(const float *Bl, const float *Ar, float *Nm, float *Em) {
+    constexpr int SK = DK + 1, SC = C + 1;
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
+        const int i = idx / C, j = idx % C;
+        float acc = 0.f;
+        if (j < i)
+            for (int d = 0; d < DK; ++d) acc += Bl[i * SK + d] * Ar[j * SK + d];
+        Nm[i * SC + j] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x < C) {
+        const int c = threadIdx.x;
+        for (int i = 0; i < C; ++i) {
+            float y = 0.f;
+            if (i == c) y = 1.f;
+            else if (i > c)
+                for (int j = c; j < i; ++j) y -= Nm[i * SC + j] * Em[j * SC + c];
+            Em[i * SC + c] = y;
+        }
+    }
+    __syncthreads();
+}
+
+}  // namespace dplr
+}  // namespace kda

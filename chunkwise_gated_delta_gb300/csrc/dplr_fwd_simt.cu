@@ -20,6 +20,7 @@
 // bisection on inertia counts of its Gram matrix.
 #include <cuda_bf16.h>
 
+#include "dplr_common.cuh"
 #include "kda_internal.h"
 
 namespace kda {
@@ -58,17 +59,14 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     float *Xm = Tm + kC * SV;         // [C][SV]  X
     float *Sm = Xm + kC * SV;         // [DVS][SK] state slice
     float *gC = Sm + kDVS * SK;       // [DK]
+    float4 *rows = reinterpret_cast<float4 *>(gC + DK);   // [C] eq. (4) data per row (clip)
+    static_assert((5 * kC * SK + 5 * kC * SC + 3 * kC * SV + kDVS * SK + DK) % 4 == 0, "float4 rows alignment");
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS;
     const int h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, H = p.H, dv = p.dv;
-    const Tin *q = static_cast<const Tin *>(p.q);
-    const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
-    const Tin *a = static_cast<const Tin *>(p.a);
-    const Tin *bb = static_cast<const Tin *>(p.b);
-    const Tg *g = static_cast<const Tg *>(p.g);
     Tin *o = static_cast<Tin *>(p.o);
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
@@ -79,29 +77,12 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     for (int t0 = 0; t0 < T; t0 += kC) {
         const int nvalid = min(kC, T - t0);
         __syncthreads();
-        // ---- Gamma and the rescaled tiles, one key channel per thread
-        if (tid < DK) {
-            const int d = tid;
-            float G = 0.f, gam = 1.f;
-            for (int c = 0; c < kC; ++c) {
-                float qv = 0.f, kv = 0.f, av = 0.f, bv = 0.f;
-                if (c < nvalid) {
-                    const size_t row = ((size_t)b * T + t0 + c) * H + h;
-                    qv = to_f(q[row * DK + d]);
-                    kv = to_f(k[row * DK + d]);
-                    av = to_f(a[row * DK + d]);
-                    bv = to_f(bb[row * DK + d]);
-                    if (p.gate_kind == KDA_GATE_CHANNEL) G += to_f(g[row * DK + d]);
-                    else if (p.gate_kind == KDA_GATE_SCALAR) G += to_f(g[row]);
-                    gam = expf(G);
-                }
-                Ql[c * SK + d] = qv * gam;
-                Kr[c * SK + d] = kv / gam;
-                Ar[c * SK + d] = av / gam;
-                Bl[c * SK + d] = bv * gam;
-            }
-            gC[d] = gam;
+        // ---- Gamma (from the clipped gate when asked) and the rescaled tiles
+        if (p.clip) {
+            dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
+            __syncthreads();
         }
+        dplr::load_rescaled<DK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, nullptr, Ql, Kr, Ar, Bl, gC);
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             const int c = idx / kDVS, e = idx % kDVS;
             Vm[c * SV + e] = c < nvalid ? to_f(v[(((size_t)b * T + t0 + c) * H + h) * dv + e0 + e]) : 0.f;
@@ -197,7 +178,7 @@ dplr_fwd_simt_kernel(const DplrParams p) {
 template <int DK>
 constexpr size_t dplr_smem_bytes() {
     return sizeof(float) * (size_t)(5 * kC * (DK + 1) + 5 * kC * (kC + 1) + 3 * kC * (kDVS + 1) +
-                                    kDVS * (DK + 1) + DK);
+                                    kDVS * (DK + 1) + DK + 4 * kC);
 }
 
 template <int DK, typename Tin, typename Tg>
@@ -302,25 +283,28 @@ dplr_factor_norm_kernel(const DplrParams p, float *rho, float *nrm, float *maxes
     const Tin *a = static_cast<const Tin *>(p.a);
     const Tin *bb = static_cast<const Tin *>(p.b);
     const Tg *g = static_cast<const Tg *>(p.g);
-    float av[4], bv[4], al[4];
+    float av[4], bv[4], gv[4], al[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int d = lane + 32 * r;
         const bool ok = d < dk;
         av[r] = ok ? to_f(a[(size_t)warp * dk + d]) : 0.f;
         bv[r] = ok ? to_f(bb[(size_t)warp * dk + d]) : 0.f;
-        float gv = 0.f;
-        if (p.gate_kind == KDA_GATE_CHANNEL) gv = ok ? to_f(g[(size_t)warp * dk + d]) : 0.f;
-        else if (p.gate_kind == KDA_GATE_SCALAR) gv = to_f(g[warp]);
-        al[r] = ok ? expf(gv) : 0.f;
+        gv[r] = 0.f;
+        if (p.gate_kind == KDA_GATE_CHANNEL) gv[r] = ok ? to_f(g[(size_t)warp * dk + d]) : 0.f;
+        else if (p.gate_kind == KDA_GATE_SCALAR) gv[r] = to_f(g[warp]);
     }
     // eq. (4): ||I - eta k j^T||_2 for unit k, j with eta = |a||b| and c = cos(a, b)
-    const float na = sqrtf(warp_sum(av[0] * av[0] + av[1] * av[1] + av[2] * av[2] + av[3] * av[3]));
-    const float nb = sqrtf(warp_sum(bv[0] * bv[0] + bv[1] * bv[1] + bv[2] * bv[2] + bv[3] * bv[3]));
+    const float na2 = warp_sum(av[0] * av[0] + av[1] * av[1] + av[2] * av[2] + av[3] * av[3]);
+    const float nb2 = warp_sum(bv[0] * bv[0] + bv[1] * bv[1] + bv[2] * bv[2] + bv[3] * bv[3]);
     const float ab = warp_sum(av[0] * bv[0] + av[1] * bv[1] + av[2] * bv[2] + av[3] * bv[3]);
-    const float eta = na * nb;
-    const float cosv = eta > 0.f ? ab / eta : 1.f;
-    const float r4 = 0.5f * (eta + sqrtf(fmaxf(eta * eta - 4.f * eta * cosv + 4.f, 0.f)));
+    const float r4 = dplr::rho_eq4(na2, nb2, ab);
+    // decay, clipped to 1/rho by eq. (7) when asked
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const float gc = p.clip ? fminf(gv[r], -logf(r4)) : gv[r];
+        al[r] = (lane + 32 * r < dk) ? expf(gc) : 0.f;
+    }
     const float sig = factor_norm_inertia(av, al, bv);
     if (lane == 0) {
         if (rho) rho[warp] = r4;

@@ -71,6 +71,7 @@ kda_status validate_dplr_common(const dplr_fwd_args *a) {
         return KDA_ERR_INVALID_ARG;
     if ((a->gate_kind == KDA_GATE_NONE) != (a->g == nullptr)) return KDA_ERR_INVALID_ARG;
     if (!a->a || !a->b) return KDA_ERR_INVALID_ARG;
+    if (a->flags & ~DPLR_FLAG_CLIP_GATE) return KDA_ERR_INVALID_ARG;
     const void *ptrs[] = {a->q, a->k, a->v, a->a, a->b, a->g, a->h0, a->o, a->ht, a->workspace};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
@@ -158,10 +159,61 @@ kda::DplrParams dplr_params(const dplr_fwd_args *args) {
     kda::DplrParams p{};
     p.B = args->B; p.T = args->T; p.H = args->H; p.dk = args->dk; p.dv = args->dv;
     p.gate_kind = args->gate_kind;
+    p.clip = (args->flags & DPLR_FLAG_CLIP_GATE) ? 1 : 0;
     p.q = args->q; p.k = args->k; p.v = args->v; p.a = args->a; p.b = args->b; p.g = args->g;
     p.h0 = args->h0; p.o = args->o; p.ht = args->ht;
     p.status = static_cast<int *>(args->workspace);
     return p;
+}
+
+kda_status validate_dplr_bwd(const dplr_bwd_args *a) {
+    if (!a) return KDA_ERR_INVALID_ARG;
+    if (a->B < 1 || a->T < 1 || a->H < 1 || a->dk < 1 || a->dv < 1) return KDA_ERR_INVALID_ARG;
+    if (a->chunk != 0 && a->chunk < 1) return KDA_ERR_INVALID_ARG;
+    if (a->dtype != KDA_BF16 && a->dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (a->g_dtype != KDA_BF16 && a->g_dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (a->gate_kind != KDA_GATE_NONE && a->gate_kind != KDA_GATE_SCALAR && a->gate_kind != KDA_GATE_CHANNEL)
+        return KDA_ERR_INVALID_ARG;
+    if ((a->gate_kind == KDA_GATE_NONE) != (a->g == nullptr)) return KDA_ERR_INVALID_ARG;
+    if ((a->g == nullptr) != (a->grad_g == nullptr)) return KDA_ERR_INVALID_ARG;
+    if (a->flags & ~DPLR_FLAG_CLIP_GATE) return KDA_ERR_INVALID_ARG;
+    if (!a->q || !a->k || !a->v || !a->a || !a->b || !a->grad_o || !a->grad_q || !a->grad_k || !a->grad_v ||
+        !a->grad_a || !a->grad_b)
+        return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {a->q, a->k, a->v, a->a, a->b, a->g, a->h0, a->grad_o, a->grad_ht, a->grad_q, a->grad_k,
+                          a->grad_v, a->grad_a, a->grad_b, a->grad_g, a->grad_h0, a->workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const double elems = (double)a->B * a->T * a->H * (a->dk > a->dv ? a->dk : a->dv);
+    if (elems > 9.0e18 / 8 || (double)a->B * a->T * a->H > 2.0e9) return KDA_ERR_INVALID_ARG;
+    if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
+    if (a->dv != 64 && a->dv != 128) return KDA_ERR_UNSUPPORTED;
+    if (a->chunk != 0 && a->chunk != 16) return KDA_ERR_UNSUPPORTED;
+    const size_t es = dtype_size(a->dtype);
+    const size_t nbt = (size_t)a->B * a->T * a->H;
+    const size_t state_bytes = (size_t)a->B * a->H * a->dv * a->dk * 4;
+    const size_t g_bytes = a->gate_kind == KDA_GATE_CHANNEL ? nbt * a->dk * dtype_size(a->g_dtype)
+                           : a->gate_kind == KDA_GATE_SCALAR ? nbt * dtype_size(a->g_dtype) : 0;
+    struct R { const void *p; size_t n; };
+    const R ins[] = {{a->q, nbt * a->dk * es}, {a->k, nbt * a->dk * es}, {a->v, nbt * a->dv * es},
+                     {a->a, nbt * a->dk * es}, {a->b, nbt * a->dk * es}, {a->g, g_bytes},
+                     {a->h0, a->h0 ? state_bytes : 0}, {a->grad_o, nbt * a->dv * es},
+                     {a->grad_ht, a->grad_ht ? state_bytes : 0}, {a->workspace, a->workspace_bytes}};
+    const R outs[] = {{a->grad_q, nbt * a->dk * es}, {a->grad_k, nbt * a->dk * es},
+                      {a->grad_v, nbt * a->dv * es}, {a->grad_a, nbt * a->dk * es},
+                      {a->grad_b, nbt * a->dk * es}, {a->grad_g, g_bytes},
+                      {a->grad_h0, a->grad_h0 ? state_bytes : 0}};
+    for (const R &o : outs) {
+        for (const R &r : ins)
+            if (overlaps(o.p, o.n, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+        for (const R &o2 : outs)
+            if (&o2 != &o && overlaps(o.p, o.n, o2.p, o2.n)) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
+size_t dplr_bwd_workspace_bytes(const dplr_bwd_args *a) {
+    return kStatusBytes + kda::dplr_bwd_state_bytes(a->B, a->T, a->H, a->dk, a->dv);
 }
 
 kda_status from_cuda(cudaError_t e) {
@@ -214,6 +266,33 @@ kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream) {
     if (!args->workspace || args->workspace_bytes < kStatusBytes) return KDA_ERR_WORKSPACE;
     return from_cuda(kda::launch_dplr_fwd_simt(dplr_params(args), args->dtype == KDA_BF16,
                                                args->g_dtype == KDA_BF16,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t dplr_chunk_bwd_workspace(const dplr_bwd_args *args) {
+    if (validate_dplr_bwd(args) != KDA_OK) return 0;
+    return dplr_bwd_workspace_bytes(args);
+}
+
+kda_status dplr_chunk_bwd(const dplr_bwd_args *args, kda_stream_t stream) {
+    kda_status st = validate_dplr_bwd(args);
+    if (st != KDA_OK) return st;
+    if (!args->workspace || args->workspace_bytes < dplr_bwd_workspace_bytes(args)) return KDA_ERR_WORKSPACE;
+    kda::DplrParams p{};
+    p.B = args->B; p.T = args->T; p.H = args->H; p.dk = args->dk; p.dv = args->dv;
+    p.gate_kind = args->gate_kind;
+    p.clip = (args->flags & DPLR_FLAG_CLIP_GATE) ? 1 : 0;
+    p.q = args->q; p.k = args->k; p.v = args->v; p.a = args->a; p.b = args->b; p.g = args->g; p.h0 = args->h0;
+    p.grad_o = args->grad_o; p.grad_ht = args->grad_ht;
+    p.grad_q = args->grad_q; p.grad_k = args->grad_k; p.grad_v = args->grad_v;
+    p.grad_a = args->grad_a; p.grad_b = args->grad_b; p.grad_g = args->grad_g; p.grad_h0 = args->grad_h0;
+    unsigned char *ws = static_cast<unsigned char *>(args->workspace);
+    const size_t N = (size_t)(args->T + 15) / 16;
+    const size_t per_state = (size_t)args->B * args->H * args->dv * args->dk;
+    p.status = reinterpret_cast<int *>(ws);
+    p.ws_S = reinterpret_cast<float *>(ws + kStatusBytes);
+    p.ws_dS = p.ws_S + (N + 1) * per_state;
+    return from_cuda(kda::launch_dplr_bwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -25,11 +25,19 @@ struct FwdParams {
 struct DplrParams {
     int B, T, H, dk, dv;
     int gate_kind;          // kda_gate
+    int clip;               // clip the decay to 1/rho (eq. (7) of "How to make GDN2 more stable")
     const void *q, *k, *v, *a, *b, *g;
     const float *h0;
     void *o;
     float *ht;
     int *status;            // first word of the workspace
+    // backward only
+    const void *grad_o;
+    const float *grad_ht;
+    void *grad_q, *grad_k, *grad_v, *grad_a, *grad_b, *grad_g;
+    float *grad_h0;
+    float *ws_S;            // [B, H, N + 1, dv, dk] states before each chunk, then the final state
+    float *ws_dS;           // [B, H, N, dv, dk] gradients of the state after each chunk
 };
 
 // Device-side copy of the validated backward arguments.
@@ -60,6 +68,10 @@ cudaError_t launch_fwd_tc_bf16(const FwdParams &p, int g_is_bf16, cudaStream_t s
 
 // float32 CUDA-core DPLR chunk forward (inputs float32 or bf16).
 cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s);
+
+// float32 CUDA-core DPLR backward (inputs float32 or bf16) and its workspace bytes.
+cudaError_t launch_dplr_bwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s);
+size_t dplr_bwd_state_bytes(int B, int T, int H, int dk, int dv);
 
 // Per-token transition norms; maxes (2 floats) is cleared on the stream first.
 cudaError_t launch_dplr_factor_norms(const DplrParams &p, int in_bf16, int g_is_bf16, float *rho, float *nrm,

@@ -64,6 +64,8 @@ WORKLOADS = {
     "dplr_bf16_b2t8192h16d128": Workload("dplr_bf16_b2t8192h16d128", "dplr", 2, 8192, 16, 128, 128, torch.bfloat16, False),
     "kda_bwd_bf16_b4t4096h16d128": Workload("kda_bwd_bf16_b4t4096h16d128", "kda", 4, 4096, 16, 128, 128,
                                             torch.bfloat16, True, grads=True),
+    "dplr_bwd_bf16_b2t8192h16d128": Workload("dplr_bwd_bf16_b2t8192h16d128", "dplr", 2, 8192, 16, 128, 128,
+                                             torch.bfloat16, False, grads=True),
 }
 
 

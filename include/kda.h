@@ -186,7 +186,15 @@ kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream);
  *     S <- (S + V^T K-> + X^T A->) Diag(gamma^C).
  * Layouts, ownership, stream semantics and error reporting are those of
  * kda_chunk_fwd.
+ *
+ * DPLR_FLAG_CLIP_GATE applies the stabilising clip of page "How to make GDN2
+ * more stable", eq. (7), token by token before the recurrence:
+ * Diag(alpha_t) -> min(Diag(alpha_t), 1/rho_t) with rho_t = ||I - b_t a_t^T||_2
+ * from eq. (4), i.e. g -> min(g, -log rho_t) (with no gate, g = 0 is clipped).
+ * It bounds every step's factor norm by 1.
  */
+#define DPLR_FLAG_CLIP_GATE 1u
+
 typedef struct {
     int B, T, H;           /* batch, sequence length (any T >= 1), heads */
     int dk, dv;            /* key head dim 64 or 128; value head dim a multiple of 32, <= 256 */
@@ -194,6 +202,7 @@ typedef struct {
     kda_dtype dtype;       /* dtype of q, k, v, a, b and o */
     kda_gate gate_kind;
     kda_dtype g_dtype;     /* dtype of g */
+    unsigned flags;        /* DPLR_FLAG_* */
     const void *q;         /* [B, T, H, dk] */
     const void *k;         /* [B, T, H, dk] */
     const void *v;         /* [B, T, H, dv] */
@@ -228,11 +237,50 @@ kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream);
  *        (Diag(alpha^2) plus a rank-2 term) by bisection on eigenvalue
  *        counts from Haynsworth's inertia additivity, in float32;
  *   maxes [2] float32: max over all tokens of rho and of norm.
- * Reads a, b, g and the sizes B, T, H, dk of args (q, k, v, o, h0, ht, dv
- * and the workspace are not used; the pointers may be NULL).  Any of rho, norm, maxes may be NULL (not written).
+ * With DPLR_FLAG_CLIP_GATE in args->flags, norm is that of the clipped
+ * factor min(Diag(alpha), 1/rho)(I - b a^T), which is at most 1.
+ * Reads a, b, g, flags and the sizes B, T, H, dk of args (q, k, v, o, h0, ht,
+ * dv and the workspace are not used; the pointers may be NULL).  Any of rho, norm, maxes may be NULL (not written).
  */
 kda_status dplr_factor_norms(const dplr_fwd_args *args, float *rho, float *norm, float *maxes,
                              kda_stream_t stream);
+
+/*
+ * Backward of dplr_chunk_fwd: given dL/do and dL/dht, the gradients of L with
+ * respect to q, k, v, a, b, g and h0.  It follows the chunk backward of page
+ * "Diagonal Plus Low Rank", section 3 (dC, dV_1, dW, dE, dF, dQ<-, dB<-,
+ * dK->, dA->, dV, dlog Gamma with the gamma^C row, and the dS recursion),
+ * with dW taken against S_[t-1], dB from dB<-, and the state-update terms
+ * V_1 dS Diag(gamma^C) and V_2 dS Diag(gamma^C) in dK-> and dA->.  With
+ * DPLR_FLAG_CLIP_GATE the forward's clip is differentiated too: the gate's
+ * gradient reaches g where g < -log rho and a, b through eq. (4) elsewhere.
+ */
+typedef struct {
+    int B, T, H;           /* as dplr_fwd_args */
+    int dk, dv;            /* 64 or 128 each */
+    int chunk;             /* 0 (library's choice) or 16; the result does not depend on it */
+    kda_dtype dtype;       /* dtype of q, k, v, a, b, grad_o and of their gradients */
+    kda_gate gate_kind;
+    kda_dtype g_dtype;     /* dtype of g and of grad_g */
+    unsigned flags;        /* DPLR_FLAG_* */
+    const void *q, *k, *v, *a, *b, *g;   /* the forward's inputs */
+    const float *h0;       /* [B, H, dv, dk] or NULL */
+    const void *grad_o;    /* [B, T, H, dv] dL/do */
+    const float *grad_ht;  /* [B, H, dv, dk] dL/dht, or NULL (zero) */
+    void *grad_q, *grad_k; /* [B, T, H, dk] out */
+    void *grad_v;          /* [B, T, H, dv] out */
+    void *grad_a, *grad_b; /* [B, T, H, dk] out */
+    void *grad_g;          /* layout of g, out; NULL iff g is NULL */
+    float *grad_h0;        /* [B, H, dv, dk] out, or NULL */
+    void *workspace;       /* dplr_chunk_bwd_workspace bytes; first 256 zero-filled before first use */
+    size_t workspace_bytes;
+} dplr_bwd_args;
+
+/* Workspace bytes for dplr_chunk_bwd: 256 + (2 ceil(T/16) + 1) B H dv dk 4 (0 on bad args). */
+size_t dplr_chunk_bwd_workspace(const dplr_bwd_args *args);
+
+/* Backward of the general gated DPLR recurrence; float32 CUDA-core kernels. */
+kda_status dplr_chunk_bwd(const dplr_bwd_args *args, kda_stream_t stream);
 
 /*
  * Reads the device status word that kernels set on a device-side error,

@@ -183,3 +183,43 @@ def test_bwd_workspace_query(lib):
 ])
 def test_bwd_rejects_bad_arguments_before_launch(lib, over, code):
     assert lib.kda_chunk_bwd(ctypes.byref(_bwd_args(**over)), None) == code
+
+
+def _dplr_bwd_args(**over):
+    a = _lib.DplrBwdArgs()
+    a.B, a.T, a.H, a.dk, a.dv, a.chunk = 2, 100, 4, 128, 128, 0
+    a.dtype, a.gate_kind, a.g_dtype, a.flags = _lib.KDA_BF16, _lib.KDA_GATE_CHANNEL, _lib.KDA_BF16, 1
+    base = 1 << 40
+    names = ("q", "k", "v", "a", "b", "g", "h0", "grad_o", "grad_ht", "grad_q", "grad_k", "grad_v", "grad_a",
+             "grad_b", "grad_g", "grad_h0", "workspace")
+    for i, f in enumerate(names):
+        setattr(a, f, base + i * (1 << 32))
+    a.workspace_bytes = 1 << 31
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_dplr_bwd_workspace_query(lib):
+    need = lib.dplr_chunk_bwd_workspace(ctypes.byref(_dplr_bwd_args()))
+    n_chunks = (100 + 15) // 16
+    assert need == 256 + 4 * 2 * 4 * (2 * n_chunks + 1) * 128 * 128
+    assert lib.dplr_chunk_bwd_workspace(ctypes.byref(_dplr_bwd_args(dv=32))) == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(grad_a=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(b=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(grad_g=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(flags=2), _lib.KDA_ERR_INVALID_ARG),
+    (dict(grad_b=(1 << 40) + 3 * (1 << 32)), _lib.KDA_ERR_INVALID_ARG),    # grad_b aliases a
+    (dict(chunk=32), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dk=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(workspace_bytes=1024), _lib.KDA_ERR_WORKSPACE),
+])
+def test_dplr_bwd_rejects_bad_arguments_before_launch(lib, over, code):
+    assert lib.dplr_chunk_bwd(ctypes.byref(_dplr_bwd_args(**over)), None) == code
+
+
+def test_dplr_fwd_rejects_unknown_flags(lib):
+    assert lib.dplr_chunk_fwd(ctypes.byref(_dplr_args(flags=4)), None) == _lib.KDA_ERR_INVALID_ARG
