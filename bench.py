@@ -47,12 +47,15 @@ CSRC = os.path.join(ROOT, "chunkwise_gated_delta_gb300", "csrc")
 # kernel that runs each variant's step: (name, source file)
 KERNELS = {"kda": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gdn": ("kda_fwd_tc", "kda_fwd_tc.cu"),
            "deltanet": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gla": ("kda_fwd_tc", "kda_fwd_tc.cu"),
-           "dplr": ("dplr_fwd_simt", "dplr_fwd_simt.cu"), "kda_bwd": ("kda_bwd_simt", "kda_bwd_simt.cu")}
-LAUNCHES_PER_STEP = {"kda_bwd": 3}
+           "dplr": ("dplr_fwd_simt", "dplr_fwd_simt.cu"), "kda_bwd": ("kda_bwd_simt", "kda_bwd_simt.cu"),
+           "dplr_bwd": ("dplr_bwd_simt", "dplr_bwd_simt.cu")}
+LAUNCHES_PER_STEP = {"kda_bwd": 3, "dplr_bwd": 3}
 
 
 def kind_of(w) -> str:
-    return "kda_bwd" if w.grads else w.variant
+    if w.grads:
+        return "dplr_bwd" if w.variant == "dplr" else "kda_bwd"
+    return w.variant
 GATES = {"kda": "channel", "gla": "channel", "dplr": "channel", "gdn": "scalar", "deltanet": "none"}
 
 
@@ -61,7 +64,7 @@ def metric_for(w) -> str:
         return METRIC
     shape = f"B{w.B}·T{w.T}·H{w.H}·d{w.dk}"
     if w.grads:
-        return f"tokens/s KDA chunk bwd {shape} bf16; % of roofline"
+        return f"tokens/s {'DPLR' if w.variant == 'dplr' else 'KDA'} chunk bwd {shape} bf16; % of roofline"
     return f"tokens/s {w.variant.upper() if w.variant != 'deltanet' else 'DeltaNet'} chunk fwd {shape} bf16; % of roofline"
 
 
@@ -76,6 +79,11 @@ def algorithmic_bytes(w) -> int:
     es = 2 if w.dtype == torch.bfloat16 else 4
     state = w.B * w.H * w.dv * w.dk * 4
     states = state * (2 if w.h0 else 1)
+    if w.grads and w.variant == "dplr":
+        # reads q, k, a, b, g, v, dO, h0 when given, dht; writes dq, dk, da, db, dg, dv, dh0
+        reads = bth * (5 * w.dk + 2 * w.dv) * es + state * (2 if w.h0 else 1)
+        writes = bth * (5 * w.dk + w.dv) * es + state
+        return reads + writes
     if w.grads:
         # reads q, k, v, g, beta, h0, dO, dht; writes dq, dk, dv, dg, dbeta, dh0
         reads = bth * (3 * w.dk + 2 * w.dv + 1) * es + state * (2 if w.h0 else 1)
@@ -220,7 +228,10 @@ def oracle_sample(w, x, heads, T):
     t0 = time.perf_counter()
     if w.grads:
         dht = x["dht"].double().numpy() if "dht" in x else None
-        oracle.kda_bwd(q, k, v, g, beta, f("do"), dht=dht, **kw)
+        if w.variant == "dplr":
+            oracle.dplr_bwd(q, k, v, a, b, g, f("do"), dht=dht, **kw)
+        else:
+            oracle.kda_bwd(q, k, v, g, beta, f("do"), dht=dht, **kw)
     elif w.variant == "kda":
         oracle.kda_fwd(q, k, v, g, beta, **kw)
     elif w.variant == "gdn":
@@ -290,19 +301,21 @@ def run_reference(args, rank, world):
 def config_dict(w):
     inputs = {"kda": "bf16 q,k,v,g,beta", "gdn": "bf16 q,k,v,beta, g [B,T,H]", "deltanet": "bf16 q,k,v,beta",
               "gla": "bf16 q,k,v,g; beta = 0, v unscaled", "dplr": "bf16 q,k,v,a,b,g"}[w.variant]
-    if w.grads:
+    if w.grads and w.variant == "dplr":
+        inputs += ", dO; fp32 dht, no h0; outputs bf16 dq,dk,dv,da,db,dg, fp32 dh0"
+    elif w.grads:
         inputs += ", dO; fp32 h0, dht; outputs bf16 dq,dk,dv,dg,dbeta, fp32 dh0"
     else:
         inputs += "; fp32 h0/ht" if w.h0 else "; fp32 ht, no h0"
     return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-            "chunk": 32 if (w.variant == "dplr" or w.grads) else w.chunk, "h0": w.h0, "inputs": inputs,
+            "chunk": 16 if kind_of(w) == "dplr_bwd" else 32 if (w.variant == "dplr" or w.grads) else w.chunk, "h0": w.h0, "inputs": inputs,
             "l2": f"no flush: inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.1f} MB per step vs 129 MB)",
             "parallelism": "replicas (independent (batch, head) scans, no collective)"}
 
 
 def run_ours(args, rank, world, local):
-    from chunkwise_gated_delta_gb300 import (HostRunner, dplr_chunk_fwd, dplr_factor_norms, kda_chunk_bwd,
-                                             kda_chunk_fwd)
+    from chunkwise_gated_delta_gb300 import (HostRunner, dplr_chunk_bwd, dplr_chunk_fwd, dplr_factor_norms,
+                                             kda_chunk_bwd, kda_chunk_fwd)
     from chunkwise_gated_delta_gb300.inputs import WORKLOADS, make_inputs
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -315,7 +328,15 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     gate = GATES[w.variant]
 
-    if w.grads:
+    if kind_of(w) == "dplr_bwd":
+        grads = {n: torch.empty_like(d[src]) for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"), ("da", "a"),
+                                                            ("db", "b"), ("dg", "g"))}
+        grads["dh0"] = torch.empty(w.B, w.H, w.dv, w.dk, dtype=torch.float32, device=dev)
+
+        def step():
+            dplr_chunk_bwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["g"], d.get("h0"), d["do"], d["dht"],
+                           gate=gate, grads=grads, stream=stream)
+    elif w.grads:
         grads = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
                  "dg": torch.empty_like(d["g"]), "dbeta": torch.empty_like(d["beta"]),
                  "dh0": torch.empty(w.B, w.H, w.dv, w.dk, dtype=torch.float32, device=dev)}
@@ -364,7 +385,7 @@ def run_ours(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         runner = HostRunner(x, device=dev, scale_v=x["scale_v"], gate=gate,
-                            kind=kind_of(w) if kind_of(w) in ("dplr", "kda_bwd") else "kda")
+                            kind=kind_of(w) if kind_of(w) in ("dplr", "kda_bwd", "dplr_bwd") else "kda")
         for _ in range(max(3, min(args.warmup, 10))):
             runner.run(stream)
         torch.cuda.synchronize()
@@ -410,12 +431,13 @@ def run_ours(args, rank, world, local):
         "gpu_launches": args.steps * LAUNCHES_PER_STEP.get(kind_of(w), 1),
         "clocks": clk,
     }
-    if w.variant == "dplr":
-        # transition-norm report (outside the timed region)
+    if kind_of(w) == "dplr":
+        # transition-norm report (outside the timed region), without and with the eq. (7) clip
         _, _, mx = dplr_factor_norms(d["a"], d["b"], d.get("g"), gate=gate, stream=stream)
+        _, _, mxc = dplr_factor_norms(d["a"], d["b"], d.get("g"), gate=gate, clip=True, stream=stream)
         torch.cuda.synchronize()
         line["factor_norms"] = {"max_rho_eq4": float(mx[0]), "max_factor_norm": float(mx[1]),
-                                "tokens": w.B * w.T * w.H}
+                                "max_factor_norm_clipped": float(mxc[1]), "tokens": w.B * w.T * w.H}
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline_leg(w, x)
@@ -430,7 +452,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["kda_bf16_b4t4096h16d128", "gdn_bf16_b8t2048h32d128", "deltanet_bf16_b8t2048h32d128",
-                             "gla_bf16_b8t2048h32d128", "dplr_bf16_b2t8192h16d128", "kda_bwd_bf16_b4t4096h16d128"])
+                             "gla_bf16_b8t2048h32d128", "dplr_bf16_b2t8192h16d128", "kda_bwd_bf16_b4t4096h16d128",
+                             "dplr_bwd_bf16_b2t8192h16d128"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()

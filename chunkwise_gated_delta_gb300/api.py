@@ -360,7 +360,7 @@ class HostRunner:
 
     Each :meth:`run` copies the inputs host->device, runs the call
     (``kda_chunk_fwd``; ``dplr_chunk_fwd`` when ``kind="dplr"``;
-    ``kda_chunk_bwd`` when ``kind="kda_bwd"``) and copies its results back
+    ``kda_chunk_bwd`` / ``dplr_chunk_bwd`` when ``kind="kda_bwd"`` / ``"dplr_bwd"``) and copies its results back
     device->host (o and ht, or every gradient), all on one stream.  Device
     buffers are allocated once and reused.
     """
@@ -368,7 +368,7 @@ class HostRunner:
     _INPUTS = ("q", "k", "v", "g", "beta", "h0", "a", "b", "do", "dht")
 
     def __init__(self, host: dict, device="cuda", scale_v=True, gate=None, kind="kda"):
-        if kind not in ("kda", "dplr", "kda_bwd"):
+        if kind not in ("kda", "dplr", "kda_bwd", "dplr_bwd"):
             raise ValueError(f"unknown kind {kind}")
         self.host = {k: v.pin_memory() for k, v in host.items() if k in self._INPUTS and isinstance(v, torch.Tensor)}
         self.dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()}
@@ -376,14 +376,16 @@ class HostRunner:
         B, T, H, dk = q.shape
         dv = self.dev["v"].shape[-1]
         self.scale_v, self.gate, self.kind = scale_v, gate, kind
-        if kind == "kda_bwd":
+        if kind in ("kda_bwd", "dplr_bwd"):
             d = self.dev
             self.outs = {"dq": torch.empty_like(q), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
                          "dh0": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
             if "g" in d:
                 self.outs["dg"] = torch.empty_like(d["g"])
-            if "beta" in d:
+            if "beta" in d and kind == "kda_bwd":
                 self.outs["dbeta"] = torch.empty_like(d["beta"])
+            if kind == "dplr_bwd":
+                self.outs["da"], self.outs["db"] = torch.empty_like(d["a"]), torch.empty_like(d["b"])
         else:
             self.outs = {"o": torch.empty(B, T, H, dv, dtype=q.dtype, device=device),
                          "ht": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
@@ -400,6 +402,9 @@ class HostRunner:
             if self.kind == "dplr":
                 dplr_chunk_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"),
                                gate=self.gate, o=self.outs["o"], ht=self.outs["ht"], stream=stream)
+            elif self.kind == "dplr_bwd":
+                dplr_chunk_bwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"), d["do"],
+                               d.get("dht"), gate=self.gate, grads=self.outs, stream=stream)
             elif self.kind == "kda_bwd":
                 kda_chunk_bwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), d["do"],
                               d.get("dht"), gate=self.gate, scale_v=self.scale_v, grads=self.outs, stream=stream)
