@@ -3,17 +3,21 @@
 // Computes the chunk form recapped on page "Kimi Delta Attention backward"
 // ("forward recap") in float32 throughout, one CTA per (value slice, head,
 // batch).  It serves float32 inputs, whose tolerance (1e-5 relative) no
-// tensor-core precision below fp32 meets.  Per chunk [t]:
+// tensor-core precision below fp32 meets.  Per chunk [t], with
+// G = in-chunk cumsum of g:
 //
-//   G = in-chunk cumsum of g, Gamma = exp(G); Q<- = Q*Gamma, K<- = K*Gamma,
-//   K-> = K/Gamma (page "Diagonal Plus Low Rank", definition of Gamma);
-//   L = Diag(beta)(K<- K->^T * M_{-1});  A~ = (I + L)^{-1} by forward
-//   substitution, one column per thread (page "DeltaNet", section 4.2 gives
-//   the unit-lower-triangular inverse);
-//   W = A~ Diag(beta) K<-,  U = A~ Diag(beta) V  (or A~ V when beta does not
-//   scale v);  V_new = U - W S^T;  O = Q<- S^T + (Q<- K->^T * M) V_new;
-//   S <- (S + V_new^T K->) Diag(gamma^C)  (page "Gated Linear Attention",
-//   section 5.2 writes the state step in this factored form).
+//   L = Diag(beta)(K<- K->^T * M_{-1}),  P = Q<- K->^T * M,  whose entries
+//       sum_d k_id k_jd exp(G_id - G_jd) and q_id k_jd exp(G_id - G_jd)
+//       (i >= j) are formed in the log domain, as page "Gated Linear
+//       Attention", section 5.3 does for strong decay: no factor exceeds 1,
+//       where K-> = K / Gamma alone would overflow once G < -88;
+//   A~ = (I + L)^{-1} by forward substitution, one column per thread (page
+//       "DeltaNet", section 4.2 gives the unit-lower-triangular inverse);
+//   V_new = U - W S^T = A~ (Diag(beta) V - Diag(beta) (K<- S^T))  (or A~ V -
+//       A~ Diag(beta) (K<- S^T) when beta does not scale v), K<- = K exp(G);
+//   O = Q<- S^T + P V_new,  Q<- = Q exp(G);
+//   S <- S Diag(gamma^C) + V_new^T (K exp(G_C - G))  (page "Gated Linear
+//       Attention", section 5.2 writes the state step in this factored form).
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -36,18 +40,19 @@ fwd_simt_kernel(const FwdParams p) {
     constexpr int SC = kC + 1;     // padded row stride of [C][C] tiles
     constexpr int SV = kDVS + 1;
     extern __shared__ float smem[];
-    float *Ql = smem;                 // [C][SK]
-    float *Kl = Ql + kC * SK;         // [C][SK]
-    float *Kr = Kl + kC * SK;         // [C][SK]
-    float *Lm = Kr + kC * SK;         // [C][SC]  strictly lower Gram, beta rows
+    float *Qm = smem;                 // [C][SK]  raw q
+    float *Km = Qm + kC * SK;         // [C][SK]  raw k
+    float *Gm = Km + kC * SK;         // [C][SK]  G (in-chunk cumsum of g)
+    float *Lm = Gm + kC * SK;         // [C][SC]  strictly lower Gram, beta rows
     float *Pm = Lm + kC * SC;         // [C][SC]  inclusive-lower Q<- K->^T
     float *Ym = Pm + kC * SC;         // [C][SC]  A~ = (I + L)^{-1}
-    float *Wm = Ym + kC * SC;         // [C][SK]
-    float *Vm = Wm + kC * SK;         // [C][SV]  raw v slice
-    float *Um = Vm + kC * SV;         // [C][SV]  U, then V_new
-    float *Sm = Um + kC * SV;         // [DVS][SK] state slice
+    float *Vm = Ym + kC * SC;         // [C][SV]  raw v slice
+    float *Um = Vm + kC * SV;         // [C][SV]  V_new
+    float *KS = Um + kC * SV;         // [C][SV]  K<- S^T
+    float *Sm = KS + kC * SV;         // [DVS][SK] state slice
     float *bet = Sm + kDVS * SK;      // [C]
-    float *gC = bet + kC;             // [DK]
+    float *gC = bet + kC;             // [DK] gamma^C
+    float *GC = gC + DK;              // [DK] log gamma^C
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS;
@@ -70,10 +75,10 @@ fwd_simt_kernel(const FwdParams p) {
     for (int t0 = 0; t0 < T; t0 += kC) {
         const int nvalid = min(kC, T - t0);
         __syncthreads();
-        // ---- prologue: Gamma, rescaled tiles (one key channel per thread)
+        // ---- prologue: raw q, k and G, one key channel per thread (G held past nvalid)
         if (tid < DK) {
             const int d = tid;
-            float G = 0.f, gam = 1.f;
+            float G = 0.f;
             for (int c = 0; c < kC; ++c) {
                 float qv = 0.f, kv = 0.f;
                 if (c < nvalid) {
@@ -82,13 +87,13 @@ fwd_simt_kernel(const FwdParams p) {
                     kv = k[row * DK + d];
                     if (p.gate_kind == KDA_GATE_CHANNEL) G += to_f(g[row * DK + d]);
                     else if (p.gate_kind == KDA_GATE_SCALAR) G += to_f(g[row]);
-                    gam = expf(G);
                 }
-                Ql[c * SK + d] = qv * gam;
-                Kl[c * SK + d] = kv * gam;
-                Kr[c * SK + d] = kv / gam;
+                Qm[c * SK + d] = qv;
+                Km[c * SK + d] = kv;
+                Gm[c * SK + d] = G;
             }
-            gC[d] = gam;
+            gC[d] = expf(G);
+            GC[d] = G;
         }
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             int c = idx / kDVS, e = idx % kDVS;
@@ -102,19 +107,25 @@ fwd_simt_kernel(const FwdParams p) {
             bet[tid] = bv;
         }
         __syncthreads();
-        // ---- Gram matrices: L = Diag(beta)(K<- K->^T * M_{-1}), P = Q<- K->^T * M
+        // ---- Gram matrices in the log domain; K<- S^T
         for (int idx = tid; idx < kC * kC; idx += kThreads) {
             int i = idx / kC, j = idx % kC;
             float l = 0.f, pp = 0.f;
             if (j <= i) {
                 for (int d = 0; d < DK; ++d) {
-                    float kr = Kr[j * SK + d];
-                    l += Kl[i * SK + d] * kr;
-                    pp += Ql[i * SK + d] * kr;
+                    const float f = expf(Gm[i * SK + d] - Gm[j * SK + d]) * Km[j * SK + d];
+                    l += Km[i * SK + d] * f;
+                    pp += Qm[i * SK + d] * f;
                 }
             }
             Lm[i * SC + j] = (j < i) ? bet[i] * l : 0.f;
             Pm[i * SC + j] = pp;
+        }
+        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
+            int i = idx / kDVS, e = idx % kDVS;
+            float acc = 0.f;
+            for (int d = 0; d < DK; ++d) acc += Km[i * SK + d] * expf(Gm[i * SK + d]) * Sm[e * SK + d];
+            KS[i * SV + e] = acc;
         }
         __syncthreads();
         // ---- A~ = (I + L)^{-1}: column c solved by forward substitution
@@ -130,26 +141,12 @@ fwd_simt_kernel(const FwdParams p) {
             }
         }
         __syncthreads();
-        // ---- W = A~ Diag(beta) K<-,  U = A~ Diag(beta) V  (or A~ V)
-        for (int idx = tid; idx < kC * DK; idx += kThreads) {
-            int i = idx / DK, d = idx % DK;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Ym[i * SC + j] * bet[j] * Kl[j * SK + d];
-            Wm[i * SK + d] = acc;
-        }
+        // ---- V_new = A~ (Diag(beta) V - Diag(beta) K<- S^T)  (Diag(beta) V -> V when beta does not scale v)
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             int i = idx / kDVS, e = idx % kDVS;
             float acc = 0.f;
             for (int j = 0; j <= i; ++j)
-                acc += Ym[i * SC + j] * (p.scale_v ? bet[j] : 1.f) * Vm[j * SV + e];
-            Um[i * SV + e] = acc;
-        }
-        __syncthreads();
-        // ---- V_new = U - W S^T
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            int i = idx / kDVS, e = idx % kDVS;
-            float acc = Um[i * SV + e];
-            for (int d = 0; d < DK; ++d) acc -= Wm[i * SK + d] * Sm[e * SK + d];
+                acc += Ym[i * SC + j] * ((p.scale_v ? bet[j] : 1.f) * Vm[j * SV + e] - bet[j] * KS[j * SV + e]);
             Um[i * SV + e] = acc;
         }
         __syncthreads();
@@ -157,17 +154,17 @@ fwd_simt_kernel(const FwdParams p) {
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             int i = idx / kDVS, e = idx % kDVS;
             float acc = 0.f;
-            for (int d = 0; d < DK; ++d) acc += Ql[i * SK + d] * Sm[e * SK + d];
+            for (int d = 0; d < DK; ++d) acc += Qm[i * SK + d] * expf(Gm[i * SK + d]) * Sm[e * SK + d];
             for (int j = 0; j <= i; ++j) acc += Pm[i * SC + j] * Um[j * SV + e];
             if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = acc;
         }
         __syncthreads();
-        // ---- S <- (S + V_new^T K->) Diag(gamma^C)
+        // ---- S <- S Diag(gamma^C) + V_new^T (K exp(G_C - G))
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             int e = idx / DK, d = idx % DK;
-            float acc = Sm[e * SK + d];
-            for (int c = 0; c < kC; ++c) acc += Um[c * SV + e] * Kr[c * SK + d];
-            Sm[e * SK + d] = acc * gC[d];
+            float acc = 0.f;
+            for (int c = 0; c < kC; ++c) acc += Um[c * SV + e] * Km[c * SK + d] * expf(GC[d] - Gm[c * SK + d]);
+            Sm[e * SK + d] = Sm[e * SK + d] * gC[d] + acc;
         }
     }
     __syncthreads();
@@ -181,8 +178,8 @@ fwd_simt_kernel(const FwdParams p) {
 
 template <int DK>
 constexpr size_t simt_smem_bytes() {
-    return sizeof(float) * (size_t)(3 * kC * (DK + 1) + 3 * kC * (kC + 1) + kC * (DK + 1) +
-                                    2 * kC * (kDVS + 1) + kDVS * (DK + 1) + kC + DK);
+    return sizeof(float) * (size_t)(3 * kC * (DK + 1) + 3 * kC * (kC + 1) + 3 * kC * (kDVS + 1) +
+                                    kDVS * (DK + 1) + kC + 2 * DK);
 }
 
 template <int DK, typename Tg>
