@@ -41,6 +41,7 @@ class KdaFwdArgs(ctypes.Structure):
         ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p),
         ("o", ctypes.c_void_p), ("ht", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("cu_seqlens", ctypes.c_void_p),
     ]
 
 

@@ -52,10 +52,16 @@ def workspace_for(device, nbytes: int) -> torch.Tensor:
 
 
 def make_args(q, k, v, g=None, beta=None, h0=None, o=None, ht=None, *, gate=None, scale_v=True,
-              workspace=None) -> _lib.KdaFwdArgs:
-    """Fill the C argument struct from tensors (no validation beyond the C side's)."""
+              workspace=None, cu_seqlens=None) -> _lib.KdaFwdArgs:
+    """Fill the C argument struct from tensors (no validation beyond the C side's).
+
+    With ``cu_seqlens`` (int32 device tensor [N + 1]) the batch is packed:
+    q is [1, T, H, dk] and B is the number of sequences N.
+    """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
     if gate is None:
         gate = "none" if g is None else ("scalar" if g.dim() == 3 else "channel")
     a = _lib.KdaFwdArgs()
@@ -66,6 +72,7 @@ def make_args(q, k, v, g=None, beta=None, h0=None, o=None, ht=None, *, gate=None
     a.flags = _lib.KDA_FLAG_BETA_SCALES_V if scale_v else 0
     a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
     a.h0, a.o, a.ht = _ptr(h0), _ptr(o), _ptr(ht)
+    a.cu_seqlens = _ptr(cu_seqlens)
     if workspace is not None:
         a.workspace = _ptr(workspace)
         a.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -73,25 +80,31 @@ def make_args(q, k, v, g=None, beta=None, h0=None, o=None, ht=None, *, gate=None
 
 
 def kda_chunk_fwd(q, k, v, g=None, beta=None, h0=None, *, gate=None, scale_v=True,
-                  output_final_state=True, o=None, ht=None, workspace=None, stream=None):
+                  output_final_state=True, o=None, ht=None, workspace=None, stream=None, cu_seqlens=None):
     """Chunkwise gated delta-rule forward through ``kda_chunk_fwd`` of the C ABI.
 
     q, k: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, same dtype);
     g: log-decay [B, T, H, dk] (per channel), [B, T, H] (scalar) or None;
     beta: [B, T, H] in the dtype of q, or None (beta = 0);
     h0: [B, H, dv, dk] fp32 or None.
+    cu_seqlens: int32 CUDA tensor [N + 1] for a packed batch of N sequences
+    (then q is [1, T, H, dk], h0 / ht are [N, H, dv, dk]), or None.
     Returns (o [B, T, H, dv] in q's dtype, ht [B, H, dv, dk] fp32 or None).
     """
     lib = _lib.load()
-    for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (h0, "h0")):
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (h0, "h0"),
+                    (cu_seqlens, "cu_seqlens")):
         _check(t, name)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    nseq = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if o is None:
         o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
     if ht is None and output_final_state:
-        ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device)
-    args = make_args(q, k, v, g, beta, h0, o, ht, gate=gate, scale_v=scale_v)
+        ht = torch.empty(nseq, H, dv, dk, dtype=torch.float32, device=q.device)
+    args = make_args(q, k, v, g, beta, h0, o, ht, gate=gate, scale_v=scale_v, cu_seqlens=cu_seqlens)
     need = lib.kda_chunk_fwd_workspace(ctypes.byref(args))
     if need == 0:
         # invalid arguments: let the launch entry point report which status

@@ -34,15 +34,16 @@ kda_status validate(const kda_fwd_args *a) {
     const void *ptrs[] = {a->q, a->k, a->v, a->g, a->beta, a->h0, a->o, a->ht, a->workspace};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (a->cu_seqlens && (reinterpret_cast<uintptr_t>(a->cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
     // sizes: reject products that overflow 63 bits
     const double elems = (double)a->B * a->T * a->H * (a->dk > a->dv ? a->dk : a->dv);
     if (elems > 9.0e18 / 8 || (double)a->B * a->T * a->H > 2.0e9) return KDA_ERR_INVALID_ARG;
     if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
     if (a->dv != 64 && a->dv != 128) return KDA_ERR_UNSUPPORTED;
     if (a->chunk != 0 && a->chunk != 64) return KDA_ERR_UNSUPPORTED;
-    // outputs must not alias inputs
+    // outputs must not alias inputs (packed sequences: one [1, T, H, d] batch)
     const size_t es = dtype_size(a->dtype);
-    const size_t nbt = (size_t)a->B * a->T * a->H;
+    const size_t nbt = (size_t)(a->cu_seqlens ? 1 : a->B) * a->T * a->H;
     const size_t o_bytes = nbt * a->dv * es;
     const size_t state_bytes = (size_t)a->B * a->H * a->dv * a->dk * 4;
     const size_t ht_bytes = a->ht ? state_bytes : 0;
@@ -51,7 +52,7 @@ kda_status validate(const kda_fwd_args *a) {
     struct R { const void *p; size_t n; } ins[] = {
         {a->q, nbt * a->dk * es}, {a->k, nbt * a->dk * es}, {a->v, nbt * a->dv * es}, {a->g, g_bytes},
         {a->beta, a->beta ? nbt * es : 0}, {a->h0, a->h0 ? state_bytes : 0},
-        {a->workspace, a->workspace_bytes}};
+        {a->workspace, a->workspace_bytes}, {a->cu_seqlens, a->cu_seqlens ? (size_t)(a->B + 1) * 4 : 0}};
     for (const R &r : ins) {
         if (overlaps(a->o, o_bytes, r.p, r.n)) return KDA_ERR_INVALID_ARG;
         if (overlaps(a->ht, ht_bytes, r.p, r.n)) return KDA_ERR_INVALID_ARG;
@@ -243,6 +244,7 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
     p.q = args->q; p.k = args->k; p.v = args->v; p.g = args->g; p.beta = args->beta;
     p.h0 = args->h0; p.o = args->o; p.ht = args->ht;
     p.status = static_cast<int *>(args->workspace);
+    p.cu_seqlens = args->cu_seqlens;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int g_bf16 = args->g_dtype == KDA_BF16;

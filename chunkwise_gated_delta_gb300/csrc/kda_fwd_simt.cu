@@ -58,6 +58,13 @@ fwd_simt_kernel(const FwdParams p) {
     const int e0 = blockIdx.x * kDVS;
     const int h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, H = p.H, dv = p.dv;
+    // rows of this sequence: dense batches (b, 0, T); packed sequences (0, cu[b], cu[b+1] - cu[b])
+    int rb = b, tb = 0, len = T;
+    if (p.cu_seqlens) {
+        const int lo = min(max(p.cu_seqlens[b], 0), T);
+        const int hi = min(max(p.cu_seqlens[b + 1], lo), T);
+        rb = 0; tb = lo; len = hi - lo;
+    }
     const float *q = static_cast<const float *>(p.q);
     const float *k = static_cast<const float *>(p.k);
     const float *v = static_cast<const float *>(p.v);
@@ -72,8 +79,8 @@ fwd_simt_kernel(const FwdParams p) {
         Sm[e * SK + d] = s0;
     }
 
-    for (int t0 = 0; t0 < T; t0 += kC) {
-        const int nvalid = min(kC, T - t0);
+    for (int t0 = 0; t0 < len; t0 += kC) {
+        const int nvalid = min(kC, len - t0);
         __syncthreads();
         // ---- prologue: raw q, k and G, one key channel per thread (G held past nvalid)
         if (tid < DK) {
@@ -82,7 +89,7 @@ fwd_simt_kernel(const FwdParams p) {
             for (int c = 0; c < kC; ++c) {
                 float qv = 0.f, kv = 0.f;
                 if (c < nvalid) {
-                    size_t row = ((size_t)b * T + t0 + c) * H + h;
+                    size_t row = ((size_t)rb * T + tb + t0 + c) * H + h;
                     qv = q[row * DK + d];
                     kv = k[row * DK + d];
                     if (p.gate_kind == KDA_GATE_CHANNEL) G += to_f(g[row * DK + d]);
@@ -98,12 +105,12 @@ fwd_simt_kernel(const FwdParams p) {
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             int c = idx / kDVS, e = idx % kDVS;
             float vv = 0.f;
-            if (c < nvalid) vv = v[(((size_t)b * T + t0 + c) * H + h) * dv + e0 + e];
+            if (c < nvalid) vv = v[(((size_t)rb * T + tb + t0 + c) * H + h) * dv + e0 + e];
             Vm[c * SV + e] = vv;
         }
         if (tid < kC) {
             float bv = 0.f;
-            if (p.has_beta && tid < nvalid) bv = beta[((size_t)b * T + t0 + tid) * H + h];
+            if (p.has_beta && tid < nvalid) bv = beta[((size_t)rb * T + tb + t0 + tid) * H + h];
             bet[tid] = bv;
         }
         __syncthreads();
@@ -156,7 +163,7 @@ fwd_simt_kernel(const FwdParams p) {
             float acc = 0.f;
             for (int d = 0; d < DK; ++d) acc += Qm[i * SK + d] * expf(Gm[i * SK + d]) * Sm[e * SK + d];
             for (int j = 0; j <= i; ++j) acc += Pm[i * SC + j] * Um[j * SV + e];
-            if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = acc;
+            if (i < nvalid) o[(((size_t)rb * T + tb + t0 + i) * H + h) * dv + e0 + e] = acc;
         }
         __syncthreads();
         // ---- S <- S Diag(gamma^C) + V_new^T (K exp(G_C - G))

@@ -208,6 +208,13 @@ struct Scratch {
     }
 };
 
+// Where a (batch, head) sequence lives: tensor-map batch coordinate, first row
+// and length.  Dense batches: (b, 0, T).  Packed variable-length batches
+// (cu_seqlens): (0, cu_seqlens[b], cu_seqlens[b + 1] - cu_seqlens[b]).
+struct Seq {
+    int bt, t0, len;
+};
+
 // Accumulator fragments of a 16x16 block (two 16x8 halves) -> tf32 A fragments of the
 // same block (k-steps 0 and 1), times `sign`, by shuffles within the warp.
 __device__ __forceinline__ void frag_c_to_a(const float (&x)[2][4], uint32_t (&a)[2][4], int lane, float sign) {
@@ -232,7 +239,7 @@ __device__ __forceinline__ void frag_c_to_a(const float (&x)[2][4], uint32_t (&a
 // ============================================================================
 template <int GATE, bool GLA, bool PAIR, typename Tg>
 __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                        const CUtensorMap *tm_g, const CUtensorMap *tm_v, int e0, int h, int b, int nchunks) {
+                        const CUtensorMap *tm_g, const CUtensorMap *tm_v, int e0, int h, Seq sq, int nchunks) {
     uint8_t *base = c.base;
     const int wt = threadIdx.x - kChainThreads;          // 0..255
     const int ww = wt >> 5;                              // WY warp 0..7
@@ -259,23 +266,23 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     auto issue_raw = [&](int n) {
         mbar_arrive_expect_tx(c.bars + B_RAW, raw_bytes);
         for (int blk = 0; blk < 2; ++blk) {
-            tma_load_4d(base + OFF_AG + blk * 16384 + 8192, tm_q, c.bars + B_RAW, blk * 64, h, n * kC, b);
-            tma_load_4d(base + OFF_KL + blk * 8192, tm_k, c.bars + B_RAW, blk * 64, h, n * kC, b);
+            tma_load_4d(base + OFF_AG + blk * 16384 + 8192, tm_q, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
+            tma_load_4d(base + OFF_KL + blk * 8192, tm_k, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
             if (GATE == KDA_GATE_CHANNEL)
-                tma_load_4d(base + OFF_AG + blk * 16384, tm_g, c.bars + B_RAW, blk * 64, h, n * kC, b);
+                tma_load_4d(base + OFF_AG + blk * 16384, tm_g, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
         }
     };
     auto issue_v = [&](int n) {
         const int s = n & 1;
         mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
-        tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, n * kC, b);
+        tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, sq.t0 + n * kC, sq.bt);
     };
     // per-token scalars of chunk n: beta and (GDN) the scalar log-decay
     auto load_scalars = [&](int n, float &bv, float &gv) {
         bv = 0.f; gv = 0.f;
         const int t = n * kC + wt;
-        if (wt < kC && t < T) {
-            const size_t row = ((size_t)b * T + t) * H + h;
+        if (wt < kC && t < sq.len) {
+            const size_t row = ((size_t)sq.bt * T + sq.t0 + t) * H + h;
             if (p.has_beta) bv = __bfloat162float(betag[row]);
             if (GATE == KDA_GATE_SCALAR) gv = ldg_f<Tg>(gsg + row);
         }
@@ -283,7 +290,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 
     if (leader) {
         if (first < nchunks) issue_raw(first);
-        issue_v(0);
+        issue_v(0);                          // nchunks >= 1: empty sequences return before the roles
         if (nchunks > 1) issue_v(1);
     }
     {
@@ -319,11 +326,13 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             const int col = 4 * cg;
             float G[8][4];
             float a[4] = {0.f, 0.f, 0.f, 0.f};
+            const int live_rows = sq.len - n * kC;          // rows of this chunk inside the sequence
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int row = rg * 8 + r;
                 float x[4] = {0.f, 0.f, 0.f, 0.f};
-                if (GATE == KDA_GATE_CHANNEL) {
+                if (row >= live_rows) {
+                } else if (GATE == KDA_GATE_CHANNEL) {
                     const float4 gg = ld_bf16x4(base + OFF_AG + sw128_offset(128, row, col));
                     x[0] = gg.x; x[1] = gg.y; x[2] = gg.z; x[3] = gg.w;
                 } else if (GATE == KDA_GATE_SCALAR) {
@@ -351,8 +360,9 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 const int row = rg * 8 + r;
                 const uint32_t o64 = sw128_offset(64, row, col);
                 const uint32_t otop = sw128_offset(128, row, col), obot = sw128_offset(128, 64 + row, col);
-                const float4 q4 = ld_bf16x4(base + OFF_AG + obot);
-                const float4 k4 = ld_bf16x4(base + OFF_KL + o64);
+                const bool live = row < live_rows;
+                const float4 q4 = live ? ld_bf16x4(base + OFF_AG + obot) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 k4 = live ? ld_bf16x4(base + OFF_KL + o64) : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
                 const float bb = bet[row];
                 float kl[4], kr4[4], ql[4];
@@ -642,7 +652,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 // ============================================================================
 template <bool PAIR>
 __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_v, const CUtensorMap *tm_o,
-                           int e0, int h, int b, int nchunks) {
+                           int e0, int h, int b, Seq sq, int nchunks) {
     uint8_t *base = c.base;
     const int j = threadIdx.x;                  // key channel == TMEM lane
     const int warp = j >> 5;
@@ -706,11 +716,14 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
         if (peer_chunk && leader && n + 2 < nchunks) {
             // v[s] has been read: fetch the slice of chunk n + 2
             mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
-            tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, (n + 2) * kC, b);
+            tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, sq.t0 + (n + 2) * kC, sq.bt);
         }
 
         // ---- rows 0-63: V_new -> bf16 MN-major B tile in the first half of the S^T tile (its
-        //      product is done), then dS^T = K->^T V_new.  Rows 64-127: O -> staging tile.
+        //      product is done), then dS^T = K->^T V_new.  Rows 64-127: O -> staging tile, or,
+        //      for the last chunk of a packed sequence, straight to its rows (a 64-row TMA store
+        //      would run into the next sequence).
+        const bool direct_o = p.cu_seqlens != nullptr && (n + 1) * kC > sq.len;
         {
             const int r = (warp & 1) * 32 + (j & 31);
             uint8_t *dst = base + (warp < 2 ? OFF_ST : OFF_OST);
@@ -718,7 +731,19 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 tmem_ld32(c.tmem + TM_D1 + s * 64 + lane_base + cc * 32, v);
-                store_row32_bf16(dst, 64, r, cc * 32, v);
+                if (warp >= 2 && direct_o) {
+                    if (n * kC + r < sq.len) {
+                        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
+                                              (((size_t)sq.t0 + n * kC + r) * p.H + h) * p.dv + e0 + cc * 32;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(orow + 8 * q) =
+                                make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                                           pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+                    }
+                } else {
+                    store_row32_bf16(dst, 64, r, cc * 32, v);
+                }
             }
             fence_proxy_async_smem();
             if (warp < 2) {
@@ -739,8 +764,10 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
         if (leader) {
             tc_fence_after();
             mbar_arrive(c.bars + B_E10 + s);                        // D1[s] drained
-            tma_store_4d(tm_o, base + OFF_OST, e0, h, n * kC, b);
-            tma_store_commit();
+            if (!direct_o) {
+                tma_store_4d(tm_o, base + OFF_OST, e0, h, sq.t0 + n * kC, sq.bt);
+                tma_store_commit();
+            }
         }
         wait_bar(c, B_C20 + s, ph2);
         tc_fence_after();
@@ -785,7 +812,21 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + OFF_MISC + MISC_TSLOT);
 
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
-    const int nchunks = (p.T + kC - 1) / kC;
+    Seq sq{b, 0, p.T};
+    if (p.cu_seqlens) {                     // packed sequences; offsets clamped into [0, T]
+        const int lo = min(max(p.cu_seqlens[b], 0), p.T);
+        const int hi = min(max(p.cu_seqlens[b + 1], lo), p.T);
+        sq = Seq{0, lo, hi - lo};
+    }
+    const int nchunks = (sq.len + kC - 1) / kC;
+    if (nchunks == 0) {                     // empty sequence: ht = h0; nothing else is set up
+        if (p.ht)
+            for (int i = threadIdx.x; i < kDVS * kDK; i += kThreads) {
+                const size_t off = (((size_t)b * p.H + h) * p.dv + e0 + i / kDK) * kDK + i % kDK;
+                p.ht[off] = p.h0 ? p.h0[off] : 0.f;
+            }
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) mbar_init(c.bars + i, 1);
@@ -804,9 +845,9 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     c.tmem = *tslot;
 
     if (threadIdx.x < kChainThreads)
-        chain_role<PAIR>(c, p, &tm_v, &tm_o, e0, h, b, nchunks);
+        chain_role<PAIR>(c, p, &tm_v, &tm_o, e0, h, b, sq, nchunks);
     else
-        wy_role<GATE, GLA, PAIR, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, b, nchunks);
+        wy_role<GATE, GLA, PAIR, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, sq, nchunks);
 
     tc_fence_before();
     __syncthreads();
@@ -882,11 +923,12 @@ cudaError_t launch_fwd_tc_bf16(const FwdParams &p, int g_is_bf16, cudaStream_t s
     if (p.gate_kind == KDA_GATE_CHANNEL && !g_is_bf16) return cudaErrorNotSupported;
     CUtensorMap mq, mk, mg, mv, mo;
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!make_map(&mq, p.q, bf, 2, p.B, p.T, p.H, p.dk) || !make_map(&mk, p.k, bf, 2, p.B, p.T, p.H, p.dk) ||
-        !make_map(&mv, p.v, bf, 2, p.B, p.T, p.H, p.dv) || !make_map(&mo, p.o, bf, 2, p.B, p.T, p.H, p.dv))
+    const int mb = p.cu_seqlens ? 1 : p.B;          // packed sequences: one [1, T, H, d] tensor
+    if (!make_map(&mq, p.q, bf, 2, mb, p.T, p.H, p.dk) || !make_map(&mk, p.k, bf, 2, mb, p.T, p.H, p.dk) ||
+        !make_map(&mv, p.v, bf, 2, mb, p.T, p.H, p.dv) || !make_map(&mo, p.o, bf, 2, mb, p.T, p.H, p.dv))
         return cudaErrorInvalidValue;
     mg = mq;
-    if (p.gate_kind == KDA_GATE_CHANNEL && !make_map(&mg, p.g, bf, 2, p.B, p.T, p.H, p.dk))
+    if (p.gate_kind == KDA_GATE_CHANNEL && !make_map(&mg, p.g, bf, 2, mb, p.T, p.H, p.dk))
         return cudaErrorInvalidValue;
     if (p.gate_kind == KDA_GATE_CHANNEL) {
         return gla ? launch_variant<KDA_GATE_CHANNEL, true, __nv_bfloat16>(p, mq, mk, mg, mv, mo, s)

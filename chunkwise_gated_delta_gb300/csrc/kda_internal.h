@@ -19,6 +19,7 @@ struct FwdParams {
     void *o;
     float *ht;
     int *status;            // first word of the workspace
+    const int *cu_seqlens;  // packed sequences: [B + 1] row offsets into a [1, T, H, d] batch, or null
 };
 
 // Device-side copy of the validated DPLR arguments.

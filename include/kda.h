@@ -86,6 +86,18 @@ typedef struct {
     float *ht;             /* [B, H, dv, dk] final state, or NULL (not written) */
     void *workspace;       /* device buffer, zero-filled before its first use */
     size_t workspace_bytes;
+    /*
+     * Packed variable-length batches, or NULL.  When given: B sequences lie
+     * back to back in [1, T, H, d] tensors (q, k, v, g, beta, o), sequence i
+     * in rows cu_seqlens[i] .. cu_seqlens[i + 1] - 1; h0 / ht stay [B, H, dv, dk],
+     * one state per sequence.  A DEVICE array of B + 1 int32 with
+     * 0 = cu_seqlens[0] <= ... <= cu_seqlens[B] = T, read by the kernels
+     * (offsets outside [0, T] are clamped there); empty sequences are allowed
+     * (their ht is h0).  Each sequence is independent: no state crosses a
+     * boundary.  The pages batch only dense [B, T] sequences; this is a
+     * boundary extension.
+     */
+    const int32_t *cu_seqlens;
 } kda_fwd_args;
 
 /* Bytes of workspace kda_chunk_fwd needs for these arguments (0 on bad args). */

@@ -173,3 +173,61 @@ def test_full_kda_b4t4096h16d128_sampled_heads():
                                   "gla_bf16_b8t2048h32d128"])
 def test_full_special_cases_sampled_heads(name):
     _full(name, [(0, 0), (7, 31)])
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+def _varlen_case(dtype, lens, dk, dv, variant="kda", seed=8):
+    """Sequences of the given lengths, packed into one [1, T, H, d] batch, with their oracle outputs."""
+    H = 2
+    parts = [make_inputs(custom(variant, 1, max(n, 1), H, dk, dv, dtype=dtype, h0=True), seed=seed + i)
+             for i, n in enumerate(lens)]
+    cat = lambda name: torch.cat([p_[name][:, :n] for p_, n in zip(parts, lens)], 1).contiguous()
+    x = {name: cat(name) for name in ("q", "k", "v", "g", "beta") if name in parts[0]}
+    x["h0"] = torch.cat([p_["h0"] for p_ in parts], 0).contiguous()
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    refs = []
+    for p_, n in zip(parts, lens):
+        if n == 0:
+            refs.append((np.zeros((1, 0, H, dv)), f64(p_["h0"])))
+            continue
+        sub = {name: (p_[name][:, :n] if name not in ("h0",) else p_[name]) for name in p_ if name != "scale_v"}
+        sub["scale_v"] = p_["scale_v"]
+        refs.append(run_oracle(sub, variant))
+    return x, cu, refs, parts[0]["scale_v"]
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.bfloat16, 128, 64),
+                                         (torch.float32, 64, 64)])
+def test_varlen_packed_sequences(dtype, dk, dv):
+    """Packed sequences (cu_seqlens) equal separate calls: ragged lengths, an empty sequence,
+    lengths below, at and above a chunk; no state crosses a boundary."""
+    lens = [100, 64, 0, 1, 193, 37]
+    x, cu, refs, scale_v = _varlen_case(dtype, lens, dk, dv)
+    d = {k_: v_.to(DEV) for k_, v_ in x.items()}
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], gate="channel", scale_v=scale_v,
+                          cu_seqlens=cu.to(DEV))
+    torch.cuda.synchronize()
+    o, ht = o.double().cpu().numpy(), ht.double().cpu().numpy()
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    for i, (ro, rh) in enumerate(refs):
+        oi = o[:, starts[i]:starts[i + 1]]
+        if lens[i]:
+            assert rel(oi, ro) <= TOL[dtype], (i, rel(oi, ro))
+        assert rel(ht[i], rh[0]) <= TOL[dtype], (i, rel(ht[i], rh[0]))
+
+
+def test_varlen_special_cases_bf16():
+    for variant in ("gdn", "deltanet", "gla"):
+        lens = [70, 0, 130]
+        x, cu, refs, scale_v = _varlen_case(torch.bfloat16, lens, 128, 128, variant=variant)
+        d = {k_: v_.to(DEV) for k_, v_ in x.items()}
+        gate = {"gdn": "scalar", "deltanet": "none", "gla": "channel"}[variant]
+        o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d["h0"], gate=gate,
+                              scale_v=scale_v, cu_seqlens=cu.to(DEV))
+        torch.cuda.synchronize()
+        o, ht = o.double().cpu().numpy(), ht.double().cpu().numpy()
+        starts = np.concatenate([[0], np.cumsum(lens)])
+        for i, (ro, rh) in enumerate(refs):
+            if lens[i]:
+                assert rel(o[:, starts[i]:starts[i + 1]], ro) <= 5e-3, (variant, i)
+            assert rel(ht[i], rh[0]) <= 5e-3, (variant, i)
