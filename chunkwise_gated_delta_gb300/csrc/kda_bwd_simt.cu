@@ -27,12 +27,12 @@
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
+#include "warp_gemm.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kC = 32;       // chunk length
-constexpr int kSC = kC + 1;  // padded row stride of [C][C] tiles
 constexpr int kDVS = 32;     // value rows per CTA in the scans
 constexpr int kThreads = 256;
 
@@ -47,38 +47,6 @@ template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, 
     p[i] = __float2bfloat16_rn(x);
 }
 
-// Gamma, Q<-, K<-, K-> of one chunk (rows past nvalid are zero, Gamma held at
-// its last value), one key channel per thread; gam[d] = gamma^C.
-template <int DK, typename Tin, typename Tg>
-__device__ void load_rescaled(const BwdParams &p, int b, int h, int t0, int nvalid, float *Gm, float *Ql,
-                              float *Kl, float *Kr, float *gam) {
-    constexpr int SK = DK + 1;
-    const Tin *q = static_cast<const Tin *>(p.q);
-    const Tin *k = static_cast<const Tin *>(p.k);
-    const Tg *g = static_cast<const Tg *>(p.g);
-    const int tid = threadIdx.x;
-    if (tid < DK) {
-        const int d = tid;
-        float G = 0.f, gm = 1.f;
-        for (int c = 0; c < kC; ++c) {
-            float qv = 0.f, kv = 0.f;
-            if (c < nvalid) {
-                const size_t row = ((size_t)b * p.T + t0 + c) * p.H + h;
-                if (Ql) qv = ld(q, row * DK + d);
-                kv = ld(k, row * DK + d);
-                if (p.gate_kind == KDA_GATE_CHANNEL) G += ld(g, row * DK + d);
-                else if (p.gate_kind == KDA_GATE_SCALAR) G += ld(g, row);
-                gm = expf(G);
-            }
-            if (Gm) Gm[c * SK + d] = gm;
-            if (Ql) Ql[c * SK + d] = qv * gm;
-            Kl[c * SK + d] = kv * gm;
-            Kr[c * SK + d] = kv / gm;
-        }
-        gam[d] = gm;
-    }
-}
-
 template <typename Tin>
 __device__ void load_beta(const BwdParams &p, int b, int h, int t0, int nvalid, float *beta) {
     const Tin *bp = static_cast<const Tin *>(p.beta);
@@ -86,48 +54,115 @@ __device__ void load_beta(const BwdParams &p, int b, int h, int t0, int nvalid, 
     if (tid < kC) beta[tid] = (p.has_beta && tid < nvalid) ? ld(bp, ((size_t)b * p.T + t0 + tid) * p.H + h) : 0.f;
 }
 
-// A~ = (I + Diag(beta) N)^{-1} with N = K<- K->^T * M_{-1}: N into Nm (strict
-// lower part, zero elsewhere), then the inverse by forward substitution, one
-// column per thread of the first warp.  Ends with a barrier.
-template <int DK>
-__device__ void wy_inverse(const float *Kl, const float *Kr, const float *beta, float *Nm, float *Am) {
-    constexpr int SK = DK + 1;
+// Gamma, Q<-, K<-, K-> of one chunk with row stride SK: all threads load the raw
+// tiles, then one thread per key channel runs the in-chunk cumsum of g down
+// its column in shared memory (rows past nvalid are zero, Gamma held at its
+// last value); gam[d] = gamma^C.  Gm and Ql may be null (the raw g then waits
+// in Kr); gsc holds C floats (scalar gates).  Contains one barrier; the
+// caller synchronises before reading the tiles.
+template <int DK, int SK, typename Tin, typename Tg>
+__device__ void load_rescaled_par(const BwdParams &p, int b, int h, int t0, int nvalid, float *Gm, float *Ql,
+                                  float *Kl, float *Kr, float *gam, float *gsc) {
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tg *g = static_cast<const Tg *>(p.g);
     const int tid = threadIdx.x;
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float acc = 0.f;
-        if (j < i)
-            for (int d = 0; d < DK; ++d) acc += Kl[i * SK + d] * Kr[j * SK + d];
-        Nm[i * kSC + j] = acc;
+    float *graw = Gm ? Gm : Kr;
+    for (int idx = tid; idx < kC * DK; idx += kThreads) {
+        const int c = idx / DK, d = idx % DK;
+        const bool ok = c < nvalid;
+        const size_t off = (((size_t)b * p.T + t0 + c) * p.H + h) * DK + d;
+        Kl[c * SK + d] = ok ? ld(k, off) : 0.f;
+        if (Ql) Ql[c * SK + d] = ok ? ld(q, off) : 0.f;
+        if (p.gate_kind == KDA_GATE_CHANNEL) graw[c * SK + d] = ok ? ld(g, off) : 0.f;
     }
+    if (p.gate_kind == KDA_GATE_SCALAR && tid < kC)
+        gsc[tid] = tid < nvalid ? ld(g, ((size_t)b * p.T + t0 + tid) * p.H + h) : 0.f;
     __syncthreads();
+    if (tid < DK) {
+        const int d = tid;
+        float G = 0.f, gm = 1.f;
+        for (int c = 0; c < kC; ++c) {
+            const float gv = p.gate_kind == KDA_GATE_CHANNEL ? graw[c * SK + d]
+                             : p.gate_kind == KDA_GATE_SCALAR ? gsc[c] : 0.f;
+            if (c < nvalid) {
+                G += gv;
+                gm = expf(G);
+            }
+            const float kv = Kl[c * SK + d];
+            Kl[c * SK + d] = kv * gm;
+            Kr[c * SK + d] = kv / gm;
+            if (Ql) Ql[c * SK + d] *= gm;
+            if (Gm) Gm[c * SK + d] = gm;
+        }
+        gam[d] = gm;
+    }
+}
+
+// A~ = (I + Diag(beta) N)^{-1} for a strictly lower N in Nm (row stride SC):
+// the unit lower triangular inverse in two levels (page "DeltaNet", section
+// 4.2, block form): the two 16x16 diagonal blocks by forward substitution
+// side by side (one column per thread of the first warp), then the
+// off-diagonal block A21 = -A22 L21 A11 by two parallel products (Tm is a
+// [C][SC] scratch).  Starts after, and ends with, a barrier.
+template <int SC>
+__device__ void block_inverse(const float *beta, const float *Nm, float *Am, float *Tm) {
+    constexpr int HB = kC / 2;
+    const int tid = threadIdx.x;
     if (tid < kC) {
-        const int c = tid;
-        for (int i = 0; i < kC; ++i) {
+        const int blk = tid / HB, c = blk * HB + tid % HB;     // column c of diagonal block blk
+        for (int i = blk * HB; i < blk * HB + HB; ++i) {
             float y = 0.f;
             if (i == c) y = 1.f;
             else if (i > c)
-                for (int j = c; j < i; ++j) y -= beta[i] * Nm[i * kSC + j] * Am[j * kSC + c];
-            Am[i * kSC + c] = y;
+                for (int j = c; j < i; ++j) y -= beta[i] * Nm[i * SC + j] * Am[j * SC + c];
+            Am[i * SC + c] = y;
         }
+        for (int i = 0; i < HB; ++i) Am[(blk == 0 ? i : HB + i) * SC + (blk == 0 ? HB : 0) + tid % HB] = 0.f;
+    }
+    __syncthreads();
+    // Tm = L21 A11 (rows HB.., cols ..HB), L21 = Diag(beta) N21
+    for (int idx = tid; idx < HB * HB; idx += kThreads) {
+        const int i = HB + idx / HB, j = idx % HB;
+        float acc = 0.f;
+        for (int l = j; l < HB; ++l) acc += beta[i] * Nm[i * SC + l] * Am[l * SC + j];
+        Tm[i * SC + j] = acc;
+    }
+    __syncthreads();
+    // A21 = -A22 Tm
+    for (int idx = tid; idx < HB * HB; idx += kThreads) {
+        const int i = HB + idx / HB, j = idx % HB;
+        float acc = 0.f;
+        for (int l = HB; l <= i; ++l) acc -= Am[i * SC + l] * Tm[l * SC + j];
+        Am[i * SC + j] = acc;
     }
     __syncthreads();
 }
 
+// Row strides of the shared tiles: = 4 (mod 32), so that the 8 x 4 fragment
+// reads of the warp-tiled products mostly avoid bank conflicts.
+__host__ __device__ constexpr int pad4(int n) { return n + 4; }
+constexpr int kSC4 = pad4(kC);
+
 // ------------------------------------------------------------------ kernel A
-template <int DK, typename Tin, typename Tg>
+// Products run as warp-tiled 32 x N blocks (warp_gemm.cuh): tf32 tensor-core
+// MMAs for bf16 inputs (TF32), exact float32 for float32 inputs.
+template <int DK, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParams p) {
-    constexpr int SK = DK + 1, SV = kDVS + 1;
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
     extern __shared__ float smem[];
     float *Kl = smem;                  // [C][SK]
     float *Kr = Kl + kC * SK;          // [C][SK]
     float *Wm = Kr + kC * SK;          // [C][SK]
     float *Sm = Wm + kC * SK;          // [DVS][SK]
     float *Nm = Sm + kDVS * SK;        // [C][SC]
-    float *Am = Nm + kC * kSC;         // [C][SC]
-    float *Vm = Am + kC * kSC;         // [C][SV]  v slice, then U, then V_new
-    float *gam = Vm + kC * SV;         // [DK]
+    float *Am = Nm + kC * SC;          // [C][SC]
+    float *Tm = Am + kC * SC;          // [C][SC]  scratch of the inverse
+    float *Vm = Tm + kC * SC;          // [C][SV]  v slice
+    float *Um = Vm + kC * SV;          // [C][SV]  U, then V_new
+    float *gam = Um + kC * SV;         // [DK]
     float *beta = gam + DK;            // [C]
+    float *gsc = beta + kC;            // [C]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -135,6 +170,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
     const Tin *v = static_cast<const Tin *>(p.v);
     const size_t head = (size_t)b * H + h;
     float *Sws = p.ws_S + head * (size_t)(N + 1) * dv * DK;
+    const bool sv = p.scale_v != 0;
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
@@ -147,46 +183,36 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
             const int e = idx / DK, d = idx % DK;
             Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
         }
-        load_rescaled<DK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, nullptr, Kl, Kr, gam);
-        load_beta<Tin>(p, b, h, t0, nvalid, beta);
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             const int c = idx / kDVS, e = idx % kDVS;
             Vm[c * SV + e] = c < nvalid ? ld(v, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
         }
+        load_beta<Tin>(p, b, h, t0, nvalid, beta);
+        load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, nullptr, Kl, Kr, gam, gsc);
         __syncthreads();
-        wy_inverse<DK>(Kl, Kr, beta, Nm, Am);
-        // W = A~ Diag(beta) K<-
-        for (int idx = tid; idx < kC * DK; idx += kThreads) {
-            const int i = idx / DK, d = idx % DK;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Am[i * kSC + j] * beta[j] * Kl[j * SK + d];
-            Wm[i * SK + d] = acc;
-        }
-        // U = A~ Diag(beta) V (or A~ V), column by column in place: row i needs rows j <= i
-        if (tid < kDVS) {
-            const int e = tid;
-            for (int i = kC - 1; i >= 0; --i) {
-                float acc = 0.f;
-                for (int j = 0; j <= i; ++j) acc += Am[i * kSC + j] * (p.scale_v ? beta[j] : 1.f) * Vm[j * SV + e];
-                Vm[i * SV + e] = acc;
-            }
-        }
+        // N = K<- K->^T * M_{-1}, then A~
+        wg::gemm<kC, TF32>(
+            DK, [&](int i, int d) { return Kl[i * SK + d]; }, [&](int d, int j) { return Kr[j * SK + d]; },
+            [&](int i, int j, float x) { Nm[i * SC + j] = j < i ? x : 0.f; });
+        __syncthreads();
+        block_inverse<SC>(beta, Nm, Am, Tm);
+        // W = A~ Diag(beta) K<- ; U = A~ Diag(beta) V (or A~ V)
+        wg::gemm<DK, TF32>(
+            kC, [&](int i, int j) { return Am[i * SC + j] * beta[j]; }, [&](int j, int d) { return Kl[j * SK + d]; },
+            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+        wg::gemm<kDVS, TF32>(
+            kC, [&](int i, int j) { return Am[i * SC + j] * (sv ? beta[j] : 1.f); },
+            [&](int j, int e) { return Vm[j * SV + e]; }, [&](int i, int e, float x) { Um[i * SV + e] = x; });
         __syncthreads();
         // V_new = U - W S^T
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = Vm[i * SV + e];
-            for (int d = 0; d < DK; ++d) acc -= Wm[i * SK + d] * Sm[e * SK + d];
-            Vm[i * SV + e] = acc;
-        }
+        wg::gemm<kDVS, TF32>(
+            DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
+            [&](int i, int e, float x) { Um[i * SV + e] -= x; });
         __syncthreads();
         // S <- (S + V_new^T K->) Diag(gamma^C)
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            float acc = Sm[e * SK + d];
-            for (int c = 0; c < kC; ++c) acc += Vm[c * SV + e] * Kr[c * SK + d];
-            Sm[e * SK + d] = acc * gam[d];
-        }
+        wg::gemm<DK, TF32>(
+            kC, [&](int e, int c) { return Um[c * SV + e]; }, [&](int c, int d) { return Kr[c * SK + d]; },
+            [&](int e, int d, float x) { Sm[e * SK + d] = (Sm[e * SK + d] + x) * gam[d]; });
     }
     __syncthreads();
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
@@ -196,9 +222,9 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
 }
 
 // ------------------------------------------------------------------ kernel B
-template <int DK, typename Tin, typename Tg>
+template <int DK, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParams p) {
-    constexpr int SK = DK + 1, SV = kDVS + 1;
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
     extern __shared__ float smem[];
     float *Ql = smem;                  // [C][SK]
     float *Kl = Ql + kC * SK;          // [C][SK]
@@ -206,12 +232,14 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
     float *Wm = Kr + kC * SK;          // [C][SK]
     float *dS = Wm + kC * SK;          // [DVS][SK]
     float *Nm = dS + kDVS * SK;        // [C][SC]
-    float *Am = Nm + kC * kSC;         // [C][SC]
-    float *Pm = Am + kC * kSC;         // [C][SC]
-    float *dO = Pm + kC * kSC;         // [C][SV]
+    float *Am = Nm + kC * SC;          // [C][SC]
+    float *Pm = Am + kC * SC;          // [C][SC]
+    float *Tm = Pm + kC * SC;          // [C][SC]  scratch of the inverse
+    float *dO = Tm + kC * SC;          // [C][SV]
     float *dU = dO + kC * SV;          // [C][SV]
     float *gam = dU + kC * SV;         // [DK]
     float *beta = gam + DK;            // [C]
+    float *gsc = beta + kC;            // [C]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -231,45 +259,39 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
             const int e = idx / DK, d = idx % DK;
             dSws[((size_t)n * dv + e0 + e) * DK + d] = dS[e * SK + d];
         }
-        load_rescaled<DK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, Ql, Kl, Kr, gam);
-        load_beta<Tin>(p, b, h, t0, nvalid, beta);
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             const int c = idx / kDVS, e = idx % kDVS;
             dO[c * SV + e] = c < nvalid ? ld(dop, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
         }
+        load_beta<Tin>(p, b, h, t0, nvalid, beta);
+        load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, Ql, Kl, Kr, gam, gsc);
         __syncthreads();
-        // P = Q<- K->^T * M
-        for (int idx = tid; idx < kC * kC; idx += kThreads) {
-            const int i = idx / kC, j = idx % kC;
-            float acc = 0.f;
-            if (j <= i)
-                for (int d = 0; d < DK; ++d) acc += Ql[i * SK + d] * Kr[j * SK + d];
-            Pm[i * kSC + j] = acc;
+        // P = Q<- K->^T * M ; N = K<- K->^T * M_{-1}
+        {
+            auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
+            wg::gemm_pair<kC, TF32>(
+                DK, [&](int i, int d) { return Ql[i * SK + d]; }, bKr, DK,
+                [&](int i, int d) { return Kl[i * SK + d]; }, bKr, [&](int i, int j, float pv, float nv) {
+                    Pm[i * SC + j] = j <= i ? pv : 0.f;
+                    Nm[i * SC + j] = j < i ? nv : 0.f;
+                });
         }
-        wy_inverse<DK>(Kl, Kr, beta, Nm, Am);
-        // W = A~ Diag(beta) K<-
-        for (int idx = tid; idx < kC * DK; idx += kThreads) {
-            const int i = idx / DK, d = idx % DK;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Am[i * kSC + j] * beta[j] * Kl[j * SK + d];
-            Wm[i * SK + d] = acc;
-        }
-        // dU = K-> Diag(gamma^C) dS^T + P^T dO
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = 0.f;
-            for (int d = 0; d < DK; ++d) acc += Kr[i * SK + d] * gam[d] * dS[e * SK + d];
-            for (int j = i; j < kC; ++j) acc += Pm[j * kSC + i] * dO[j * SV + e];
-            dU[i * SV + e] = acc;
-        }
+        __syncthreads();
+        block_inverse<SC>(beta, Nm, Am, Tm);
+        // W = A~ Diag(beta) K<- ; dU = K-> Diag(gamma^C) dS^T + P^T dO
+        wg::gemm<DK, TF32>(
+            kC, [&](int i, int j) { return Am[i * SC + j] * beta[j]; }, [&](int j, int d) { return Kl[j * SK + d]; },
+            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+        wg::gemm2<kDVS, TF32>(
+            DK, [&](int i, int d) { return Kr[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[e * SK + d]; },
+            kC, [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
+            [&](int i, int e, float x) { dU[i * SV + e] = x; });
         __syncthreads();
         // dS <- dS Diag(gamma^C) + dO^T Q<- - dU^T W
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            float acc = dS[e * SK + d] * gam[d];
-            for (int c = 0; c < kC; ++c) acc += dO[c * SV + e] * Ql[c * SK + d] - dU[c * SV + e] * Wm[c * SK + d];
-            dS[e * SK + d] = acc;
-        }
+        wg::gemm2<DK, TF32>(
+            kC, [&](int e, int c) { return dO[c * SV + e]; }, [&](int c, int d) { return Ql[c * SK + d]; }, kC,
+            [&](int e, int c) { return -dU[c * SV + e]; }, [&](int c, int d) { return Wm[c * SK + d]; },
+            [&](int e, int d, float x) { dS[e * SK + d] = dS[e * SK + d] * gam[d] + x; });
     }
     __syncthreads();
     if (p.grad_h0) {
@@ -281,14 +303,17 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
 }
 
 // ------------------------------------------------------------------ kernel C
+
 template <int DK, int DV>
 constexpr size_t grad_smem_floats() {
-    return (size_t)8 * kC * (DK + 1) + (size_t)4 * kC * (DV + 1) + (size_t)5 * kC * kSC + 2 * kC + DK;
+    return (size_t)8 * kC * pad4(DK) + (size_t)4 * kC * pad4(DV) + (size_t)5 * kC * kSC4 + 2 * kC + DK;
 }
 
-template <int DK, int DV, typename Tin, typename Tg>
+// Products run as warp-tiled 32 x N blocks (warp_gemm.cuh): tf32 tensor-core
+// MMAs for bf16 inputs (TF32), exact float32 for float32 inputs.
+template <int DK, int DV, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams p) {
-    constexpr int SK = DK + 1, SV = DV + 1;
+    constexpr int SK = pad4(DK), SV = pad4(DV), SC = kSC4;
     extern __shared__ float smem[];
     float *Gm = smem;                  // [C][SK]  Gamma
     float *Ql = Gm + kC * SK;          // [C][SK]
@@ -303,11 +328,11 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     float *Vn = dO + kC * SV;          // [C][SV]  U, V_new, then A~^T dU
     float *dU = Vn + kC * SV;          // [C][SV]
     float *Nm = dU + kC * SV;          // [C][SC]  K<- K->^T * M_{-1}
-    float *Am = Nm + kC * kSC;         // [C][SC]  A~
-    float *Pm = Am + kC * kSC;         // [C][SC]  P, then dO V_new^T * M
-    float *dA = Pm + kC * kSC;         // [C][SC]  dA~, then dX~
-    float *Tm = dA + kC * kSC;         // [C][SC]  scratch
-    float *beta = Tm + kC * kSC;       // [C]
+    float *Am = Nm + kC * SC;          // [C][SC]  A~
+    float *Pm = Am + kC * SC;          // [C][SC]  P, then dO V_new^T * M
+    float *dA = Pm + kC * SC;          // [C][SC]  dA~, then dX~
+    float *Tm = dA + kC * SC;          // [C][SC]  scratch
+    float *beta = Tm + kC * SC;        // [C]
     float *dbeta = beta + kC;          // [C]
     float *gam = dbeta + kC;           // [DK]
 
@@ -321,8 +346,10 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     const float *Sp = p.ws_S + (head * (N + 1) + n) * (size_t)DV * DK;      // state before the chunk
     const float *Sn = Sp + (size_t)DV * DK;                                 // state after the chunk
     const float *dS = p.ws_dS + (head * N + n) * (size_t)DV * DK;           // gradient of the state after
+    const bool sv = p.scale_v != 0;
 
-    load_rescaled<DK, Tin, Tg>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam);
+    // ---- loads: Gamma and the rescaled tiles, v, dO, beta
+    load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, dbeta);
     load_beta<Tin>(p, b, h, t0, nvalid, beta);
     for (int idx = tid; idx < kC * DV; idx += kThreads) {
         const int c = idx / DV, e = idx % DV;
@@ -331,126 +358,92 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
         dO[c * SV + e] = c < nvalid ? ld(dop, off) : 0.f;
     }
     __syncthreads();
-    // P = Q<- K->^T * M ; N and A~
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float acc = 0.f;
-        if (j <= i)
-            for (int d = 0; d < DK; ++d) acc += Ql[i * SK + d] * Kr[j * SK + d];
-        Pm[i * kSC + j] = acc;
-    }
-    wy_inverse<DK>(Kl, Kr, beta, Nm, Am);
-    const float vscale = p.scale_v ? 1.f : 0.f;   // beta scales v: U = A~ Diag(beta) V, else A~ V
-    // W = A~ Diag(beta) K<- ; U = A~ Diag(beta) V
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int i = idx / DK, d = idx % DK;
-        float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc += Am[i * kSC + j] * beta[j] * Kl[j * SK + d];
-        Wm[i * SK + d] = acc;
-    }
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int i = idx / DV, e = idx % DV;
-        float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc += Am[i * kSC + j] * (vscale != 0.f ? beta[j] : 1.f) * Vm[j * SV + e];
-        Vn[i * SV + e] = acc;
+    // ---- P = Q<- K->^T * M and N = K<- K->^T * M_{-1}
+    {
+        auto bKr = [&](int k, int j) { return Kr[j * SK + k]; };
+        wg::gemm_pair<kC, TF32>(
+            DK, [&](int i, int d) { return Ql[i * SK + d]; }, bKr, DK, [&](int i, int d) { return Kl[i * SK + d]; },
+            bKr, [&](int i, int j, float pv, float nv) {
+                Pm[i * SC + j] = j <= i ? pv : 0.f;
+                Nm[i * SC + j] = j < i ? nv : 0.f;
+            });
     }
     __syncthreads();
-    // V_new = U - W S_prev^T ; dU = K-> Diag(gamma^C) dS^T + P^T dO
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int i = idx / DV, e = idx % DV;
-        float acc = Vn[i * SV + e], au = 0.f;
-        for (int d = 0; d < DK; ++d) {
-            acc -= Wm[i * SK + d] * Sp[(size_t)e * DK + d];
-            au += Kr[i * SK + d] * gam[d] * dS[(size_t)e * DK + d];
-        }
-        for (int j = i; j < kC; ++j) au += Pm[j * kSC + i] * dO[j * SV + e];
-        Vn[i * SV + e] = acc;
-        dU[i * SV + e] = au;
+    block_inverse<SC>(beta, Nm, Am, Tm);
+    // ---- W = A~ Diag(beta) K<- ; U = A~ Diag(beta) V (or A~ V)
+    wg::gemm<DK, TF32>(
+        kC, [&](int i, int j) { return Am[i * SC + j] * beta[j]; }, [&](int j, int d) { return Kl[j * SK + d]; },
+        [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+    wg::gemm<DV, TF32>(
+        kC, [&](int i, int j) { return Am[i * SC + j] * (sv ? beta[j] : 1.f); },
+        [&](int j, int e) { return Vm[j * SV + e]; }, [&](int i, int e, float x) { Vn[i * SV + e] = x; });
+    __syncthreads();
+    // ---- V_new = U - W S_prev^T ; dU = K-> Diag(gamma^C) dS^T + P^T dO
+    wg::gemm<DV, TF32>(
+        DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sp[(size_t)e * DK + d]; },
+        [&](int i, int e, float x) { Vn[i * SV + e] -= x; });
+    wg::gemm2<DV, TF32>(
+        DK, [&](int i, int d) { return Kr[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[(size_t)e * DK + d]; },
+        kC, [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
+        [&](int i, int e, float x) { dU[i * SV + e] = x; });
+    __syncthreads();
+    // ---- dO V_new^T * M (into Pm)
+    wg::gemm<kC, TF32>(
+        DV, [&](int i, int e) { return dO[i * SV + e]; }, [&](int e, int j) { return Vn[j * SV + e]; },
+        [&](int i, int j, float x) { Pm[i * SC + j] = j <= i ? x : 0.f; });
+    __syncthreads();
+    // ---- dW = -dU S_prev ; dQ<- = dO S_prev + (dO V_new^T * M) K-> ;
+    //      dK-> = V_new dS Diag(gamma^C) + (dO V_new^T * M)^T Q<-
+    {
+        auto bSp = [&](int e, int d) { return Sp[(size_t)e * DK + d]; };
+        wg::gemm<DK, TF32>(
+            DV, [&](int i, int e) { return dU[i * SV + e]; }, bSp, [&](int i, int d, float x) { Wm[i * SK + d] = -x; });
+        wg::gemm2<DK, TF32>(
+            DV, [&](int i, int e) { return dO[i * SV + e]; }, bSp, kC, [&](int i, int j) { return Pm[i * SC + j]; },
+            [&](int j, int d) { return Kr[j * SK + d]; }, [&](int i, int d, float x) { dQl[i * SK + d] = x; });
+        wg::gemm_pair<DK, TF32>(
+            DV, [&](int i, int e) { return Vn[i * SV + e]; }, [&](int e, int d) { return dS[(size_t)e * DK + d]; },
+            kC, [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int d) { return Ql[j * SK + d]; },
+            [&](int i, int d, float x1, float x2) { dKr[i * SK + d] = x1 * gam[d] + x2; });
     }
     __syncthreads();
-    // dO V_new^T * M (into Pm)
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float acc = 0.f;
-        if (j <= i)
-            for (int e = 0; e < DV; ++e) acc += dO[i * SV + e] * Vn[j * SV + e];
-        Pm[i * kSC + j] = acc;
-    }
+    // ---- A~^T dW (into dKl), A~^T dU (into Vn), dA~ = dW K<-^T Diag(beta) + dU V^T Diag(beta) (or dU V^T)
+    auto aAt = [&](int i, int j) { return Am[j * SC + i]; };
+    wg::gemm<DK, TF32>(
+        kC, aAt, [&](int j, int d) { return Wm[j * SK + d]; }, [&](int i, int d, float x) { dKl[i * SK + d] = x; });
+    wg::gemm<DV, TF32>(
+        kC, aAt, [&](int j, int e) { return dU[j * SV + e]; }, [&](int i, int e, float x) { Vn[i * SV + e] = x; });
+    wg::gemm_pair<kC, TF32>(
+        DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int j) { return Kl[j * SK + d]; }, DV,
+        [&](int i, int e) { return dU[i * SV + e]; }, [&](int e, int j) { return Vm[j * SV + e]; },
+        [&](int i, int j, float xw, float xu) { dA[i * SC + j] = xw * beta[j] + xu * (sv ? beta[j] : 1.f); });
     __syncthreads();
-    // dW = -dU S_prev ; dQ<- = dO S_prev + (dO V_new^T * M) K-> ;
-    // dK-> = V_new dS Diag(gamma^C) + (dO V_new^T * M)^T Q<-
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int i = idx / DK, d = idx % DK;
-        float aw = 0.f, aq = 0.f, ak = 0.f;
-        for (int e = 0; e < DV; ++e) {
-            const float sp = Sp[(size_t)e * DK + d], ds = dS[(size_t)e * DK + d];
-            aw -= dU[i * SV + e] * sp;
-            aq += dO[i * SV + e] * sp;
-            ak += Vn[i * SV + e] * ds;
-        }
-        ak *= gam[d];
-        for (int j = 0; j <= i; ++j) aq += Pm[i * kSC + j] * Kr[j * SK + d];
-        for (int j = i; j < kC; ++j) ak += Pm[j * kSC + i] * Ql[j * SK + d];
-        Wm[i * SK + d] = aw;
-        dQl[i * SK + d] = aq;
-        dKr[i * SK + d] = ak;
-    }
-    __syncthreads();
-    // A~^T dW (into dKl) and A~^T dU (into Vn)
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int i = idx / DK, d = idx % DK;
-        float acc = 0.f;
-        for (int j = i; j < kC; ++j) acc += Am[j * kSC + i] * Wm[j * SK + d];
-        dKl[i * SK + d] = acc;
-    }
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int i = idx / DV, e = idx % DV;
-        float acc = 0.f;
-        for (int j = i; j < kC; ++j) acc += Am[j * kSC + i] * dU[j * SV + e];
-        Vn[i * SV + e] = acc;
-    }
-    // dA~ = dW K<-^T Diag(beta) + dU V^T Diag(beta)  (dU V^T unscaled when beta does not scale v)
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float aw = 0.f, au = 0.f;
-        for (int d = 0; d < DK; ++d) aw += Wm[i * SK + d] * Kl[j * SK + d];
-        for (int e = 0; e < DV; ++e) au += dU[i * SV + e] * Vm[j * SV + e];
-        dA[i * kSC + j] = aw * beta[j] + au * (vscale != 0.f ? beta[j] : 1.f);
-    }
-    __syncthreads();
-    // dbeta, first two terms: diag(A~^T dW K<-^T) + diag(A~^T dU V^T)
+    // ---- dbeta, first two terms: diag(A~^T dW K<-^T) + diag(A~^T dU V^T) ; Tm = dA~ A~^T
     {
         const int warp = tid >> 5, lane = tid & 31;
         for (int i = warp; i < kC; i += kThreads / 32) {
             float acc = 0.f;
             for (int d = lane; d < DK; d += 32) acc += dKl[i * SK + d] * Kl[i * SK + d];
-            if (vscale != 0.f)
+            if (sv)
                 for (int e = lane; e < DV; e += 32) acc += Vn[i * SV + e] * Vm[i * SV + e];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) dbeta[i] = acc;
         }
     }
-    // dX~ = -A~^T dA~ A~^T: Tm = dA~ A~^T, then dA = -A~^T Tm
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float acc = 0.f;
-        for (int l = 0; l <= j; ++l) acc += dA[i * kSC + l] * Am[j * kSC + l];
-        Tm[i * kSC + j] = acc;
-    }
+    wg::gemm<kC, TF32>(
+        kC, [&](int i, int l) { return dA[i * SC + l]; }, [&](int l, int j) { return Am[j * SC + l]; },
+        [&](int i, int j, float x) { Tm[i * SC + j] = x; });
     __syncthreads();
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float acc = 0.f;
-        for (int l = i; l < kC; ++l) acc -= Am[l * kSC + i] * Tm[l * kSC + j];
-        dA[i * kSC + j] = acc;
-    }
+    // ---- dX~ = -A~^T (dA~ A~^T)
+    wg::gemm<kC, TF32>(
+        kC, aAt, [&](int l, int j) { return Tm[l * SC + j]; }, [&](int i, int j, float x) { dA[i * SC + j] = -x; });
     __syncthreads();
-    // dbeta third term diag(dX~ N^T); E = (Diag(beta) dX~) * M_{-1} into Tm
+    // ---- dbeta third term diag(dX~ N^T); E = (Diag(beta) dX~) * M_{-1} into Tm
     {
         const int warp = tid >> 5, lane = tid & 31;
         for (int i = warp; i < kC; i += kThreads / 32) {
-            float acc = dA[i * kSC + lane] * Nm[i * kSC + lane];
+            float acc = dA[i * SC + lane] * Nm[i * SC + lane];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) dbeta[i] += acc;
@@ -458,20 +451,18 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     }
     for (int idx = tid; idx < kC * kC; idx += kThreads) {
         const int i = idx / kC, j = idx % kC;
-        Tm[i * kSC + j] = j < i ? beta[i] * dA[i * kSC + j] : 0.f;
+        Tm[i * SC + j] = j < i ? beta[i] * dA[i * SC + j] : 0.f;
     }
     __syncthreads();
-    // dK<- = Diag(beta) A~^T dW + E K-> ; dK-> += E^T K<-
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int i = idx / DK, d = idx % DK;
-        float al = beta[i] * dKl[i * SK + d], ar = dKr[i * SK + d];
-        for (int j = 0; j < i; ++j) al += Tm[i * kSC + j] * Kr[j * SK + d];
-        for (int j = i + 1; j < kC; ++j) ar += Tm[j * kSC + i] * Kl[j * SK + d];
-        dKl[i * SK + d] = al;
-        dKr[i * SK + d] = ar;
-    }
+    // ---- dK<- = Diag(beta) A~^T dW + E K-> ; dK-> += E^T K<-
+    wg::gemm<DK, TF32>(
+        kC, [&](int i, int j) { return Tm[i * SC + j]; }, [&](int j, int d) { return Kr[j * SK + d]; },
+        [&](int i, int d, float x) { dKl[i * SK + d] = beta[i] * dKl[i * SK + d] + x; });
+    wg::gemm<DK, TF32>(
+        kC, [&](int i, int j) { return Tm[j * SC + i]; }, [&](int j, int d) { return Kl[j * SK + d]; },
+        [&](int i, int d, float x) { dKr[i * SK + d] += x; });
     __syncthreads();
-    // outputs: dq, dk, dv, dbeta, and dg from the suffix sums of dlogGamma
+    // ---- outputs: dq, dk, dv, dbeta, and dg from the suffix sums of dlogGamma
     Tin *gq = static_cast<Tin *>(p.grad_q);
     Tin *gk = static_cast<Tin *>(p.grad_k);
     Tin *gv = static_cast<Tin *>(p.grad_v);
@@ -487,7 +478,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     for (int idx = tid; idx < kC * DV; idx += kThreads) {
         const int i = idx / DV, e = idx % DV;
         if (i < nvalid)
-            st(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, (vscale != 0.f ? beta[i] : 1.f) * Vn[i * SV + e]);
+            st(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, (sv ? beta[i] : 1.f) * Vn[i * SV + e]);
     }
     if (p.has_beta && tid < nvalid)
         st(static_cast<Tin *>(p.grad_beta), ((size_t)b * T + t0 + tid) * H + h, dbeta[tid]);
@@ -539,12 +530,13 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
 
 template <int DK>
 constexpr size_t states_smem_bytes() {
-    return sizeof(float) * ((size_t)3 * kC * (DK + 1) + kDVS * (DK + 1) + 2 * kC * kSC + kC * (kDVS + 1) + DK + kC);
+    return sizeof(float) *
+           ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * kSC4 + 2 * kC * pad4(kDVS) + DK + 2 * kC);
 }
 template <int DK>
 constexpr size_t dstate_smem_bytes() {
     return sizeof(float) *
-           ((size_t)4 * kC * (DK + 1) + kDVS * (DK + 1) + 3 * kC * kSC + 2 * kC * (kDVS + 1) + DK + kC);
+           ((size_t)4 * kC * pad4(DK) + kDVS * pad4(DK) + 4 * kC * kSC4 + 2 * kC * pad4(kDVS) + DK + 2 * kC);
 }
 
 template <typename F>
@@ -554,18 +546,19 @@ cudaError_t set_smem(F *fn, size_t bytes) {
 
 template <int DK, int DV, typename Tin, typename Tg>
 cudaError_t launch_all(const BwdParams &p, cudaStream_t s) {
+    constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const int N = (p.T + kC - 1) / kC;
     cudaError_t e;
     const size_t sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
     static_assert(sizeof(float) * grad_smem_floats<128, 128>() <= 227 * 1024, "kernel C shared memory");
-    if ((e = set_smem(kda_bwd_states_kernel<DK, Tin, Tg>, sa)) != cudaSuccess) return e;
-    if ((e = set_smem(kda_bwd_dstate_kernel<DK, Tin, Tg>, sb)) != cudaSuccess) return e;
-    if ((e = set_smem(kda_bwd_grad_kernel<DK, DV, Tin, Tg>, sc)) != cudaSuccess) return e;
+    if ((e = set_smem(kda_bwd_states_kernel<DK, Tin, Tg, kTf32>, sa)) != cudaSuccess) return e;
+    if ((e = set_smem(kda_bwd_dstate_kernel<DK, Tin, Tg, kTf32>, sb)) != cudaSuccess) return e;
+    if ((e = set_smem(kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
     const dim3 gscan(p.dv / kDVS, p.H, p.B), ggrad(N, p.H, p.B);
-    kda_bwd_states_kernel<DK, Tin, Tg><<<gscan, kThreads, sa, s>>>(p);
-    kda_bwd_dstate_kernel<DK, Tin, Tg><<<gscan, kThreads, sb, s>>>(p);
-    kda_bwd_grad_kernel<DK, DV, Tin, Tg><<<ggrad, kThreads, sc, s>>>(p);
+    kda_bwd_states_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sa, s>>>(p);
+    kda_bwd_dstate_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sb, s>>>(p);
+    kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<ggrad, kThreads, sc, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,112 @@
+// Warp-tiled products for the chunk-parallel backward kernels.
+//
+// A CTA of 8 warps computes a 32 x N block (N in {32, 64, 128}) of a product
+// sum_k A(i, k) B(k, n): warp w owns rows 16 (w & 1) .. +16 and columns
+// (w >> 1) N / 4 .. + N / 4, i.e. N / 32 tiles of 16 x 8.  Operands come
+// through accessor functors (shared or global memory, any layout or
+// transform).  TF32 = true issues warp-level m16n8k8 tf32 tensor-core MMAs
+// with float32 accumulation (operands rounded to tf32); TF32 = false computes
+// the same fragment elements exactly in float32 on the CUDA cores.
+#pragma once
+
+#include "tc_common.cuh"
+
+namespace kda {
+namespace wg {
+
+using tc::mma_tf32_16x8x8;
+using tc::to_tf32;
+
+// acc[nt][q] is element (row0 + g + 8 (q >> 1), col0 + 8 nt + 2 t + (q & 1)) of the tile,
+// g = lane / 4, t = lane % 4 (the m16n8 accumulator layout).
+template <int NT, bool TF32, typename FA, typename FB>
+__device__ __forceinline__ void tile(float (&acc)[NT][4], int row0, int col0, int K, const FA &A, const FB &B) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    if constexpr (TF32) {
+#pragma unroll 2
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            const uint32_t a[4] = {to_tf32(A(row0 + g, k0 + t)), to_tf32(A(row0 + g + 8, k0 + t)),
+                                   to_tf32(A(row0 + g, k0 + t + 4)), to_tf32(A(row0 + g + 8, k0 + t + 4))};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int n = col0 + 8 * nt + g;
+                const uint32_t b[2] = {to_tf32(B(k0 + t, n)), to_tf32(B(k0 + t + 4, n))};
+                mma_tf32_16x8x8(acc[nt], a, b);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = row0 + g + 8 * (q >> 1), n = col0 + 8 * nt + 2 * t + (q & 1);
+                float s = 0.f;
+#pragma unroll 4
+                for (int k = 0; k < K; ++k) s += A(r, k) * B(k, n);
+                acc[nt][q] += s;
+            }
+    }
+}
+
+// Calls epi(row, col, value) for every element of this thread's fragments.
+template <int NT, typename FE>
+__device__ __forceinline__ void store(const float (&acc)[NT][4], int row0, int col0, const FE &epi) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) epi(row0 + g + 8 * (q >> 1), col0 + 8 * nt + 2 * t + (q & 1), acc[nt][q]);
+}
+
+// This warp's tile origin in a 32 x N block.
+template <int N>
+__device__ __forceinline__ void origin(int &row0, int &col0) {
+    const int w = threadIdx.x >> 5;
+    row0 = 16 * (w & 1);
+    col0 = (w >> 1) * (N / 4);
+}
+
+// out(i, n) = epi(i, n, sum_k A(i, k) B(k, n)) over a 32 x N block.
+template <int N, bool TF32, typename FA, typename FB, typename FE>
+__device__ __forceinline__ void gemm(int K, const FA &A, const FB &B, const FE &epi) {
+    constexpr int NT = N / 32;
+    int r0, c0;
+    origin<N>(r0, c0);
+    float acc[NT][4] = {};
+    tile<NT, TF32>(acc, r0, c0, K, A, B);
+    store<NT>(acc, r0, c0, epi);
+}
+
+// out(i, n) = epi(i, n, sum_k A1 B1 + sum_k A2 B2).
+template <int N, bool TF32, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
+__device__ __forceinline__ void gemm2(int K1, const FA1 &A1, const FB1 &B1, int K2, const FA2 &A2, const FB2 &B2,
+                                      const FE &epi) {
+    constexpr int NT = N / 32;
+    int r0, c0;
+    origin<N>(r0, c0);
+    float acc[NT][4] = {};
+    tile<NT, TF32>(acc, r0, c0, K1, A1, B1);
+    tile<NT, TF32>(acc, r0, c0, K2, A2, B2);
+    store<NT>(acc, r0, c0, epi);
+}
+
+// out(i, n) = epi(i, n, sum_k A1 B1, sum_k A2 B2): two products kept apart.
+template <int N, bool TF32, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
+__device__ __forceinline__ void gemm_pair(int K1, const FA1 &A1, const FB1 &B1, int K2, const FA2 &A2,
+                                          const FB2 &B2, const FE &epi) {
+    constexpr int NT = N / 32;
+    int r0, c0;
+    origin<N>(r0, c0);
+    float a1[NT][4] = {}, a2[NT][4] = {};
+    tile<NT, TF32>(a1, r0, c0, K1, A1, B1);
+    tile<NT, TF32>(a2, r0, c0, K2, A2, B2);
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            epi(r0 + g + 8 * (q >> 1), c0 + 8 * nt + 2 * t + (q & 1), a1[nt][q], a2[nt][q]);
+}
+
+}  // namespace wg
+}  // namespace kda
