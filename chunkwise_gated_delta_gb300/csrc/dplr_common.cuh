@@ -141,5 +141,92 @@ __device__ void inverse_e(const float *Bl, const float *Ar, float *Nm, float *Em
     __syncthreads();
 }
 
+// load_rescaled with all threads loading the raw tiles first (coalesced), then
+// one thread per key channel running the cumsum down its column in shared
+// memory.  Gm is required here (it holds the raw gate in between); Ql, Kr, Ar,
+// Bl may be null; gsc holds C floats (scalar gates).  Contains one barrier;
+// the caller synchronises before reading the tiles.
+template <int DK, int SK, int C, typename Tin, typename Tg>
+__device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int nvalid, const float4 *rows,
+                                  float *Gm, float *Ql, float *Kr, float *Ar, float *Bl, float *gam, float *gsc) {
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *a = static_cast<const Tin *>(p.a);
+    const Tin *bb = static_cast<const Tin *>(p.b);
+    const Tg *g = static_cast<const Tg *>(p.g);
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int idx = tid; idx < C * DK; idx += nt) {
+        const int c = idx / DK, d = idx % DK;
+        const bool ok = c < nvalid;
+        const size_t off = (((size_t)b * p.T + t0 + c) * p.H + h) * DK + d;
+        if (Ql) Ql[c * SK + d] = ok ? ldf(q, off) : 0.f;
+        if (Kr) Kr[c * SK + d] = ok ? ldf(k, off) : 0.f;
+        if (Ar) Ar[c * SK + d] = ok ? ldf(a, off) : 0.f;
+        if (Bl) Bl[c * SK + d] = ok ? ldf(bb, off) : 0.f;
+        float gv = 0.f;
+        if (ok && p.gate_kind == KDA_GATE_CHANNEL) gv = ldf(g, off);
+        Gm[c * SK + d] = gv;
+    }
+    if (tid < C) {
+        float gv = 0.f;
+        if (tid < nvalid && p.gate_kind == KDA_GATE_SCALAR) gv = ldf(g, ((size_t)b * p.T + t0 + tid) * p.H + h);
+        gsc[tid] = gv;
+    }
+    __syncthreads();
+    for (int d = tid; d < DK; d += nt) {
+        float G = 0.f, gm = 1.f;
+        for (int c = 0; c < C; ++c) {
+            if (c < nvalid) {
+                float gv = p.gate_kind == KDA_GATE_CHANNEL ? Gm[c * SK + d] : gsc[c];
+                if (p.clip) gv = fminf(gv, rows[c].w);
+                G += gv;
+                gm = expf(G);
+            }
+            Gm[c * SK + d] = gm;
+            if (Ql) Ql[c * SK + d] *= gm;
+            if (Kr) Kr[c * SK + d] /= gm;
+            if (Ar) Ar[c * SK + d] /= gm;
+            if (Bl) Bl[c * SK + d] *= gm;
+        }
+        gam[d] = gm;
+    }
+}
+
+// E = (I + Nm)^{-1} for a strictly lower Nm (row stride SC, C = 32): the two
+// 16x16 diagonal blocks by forward substitution side by side, then
+// E21 = -E22 N21 E11 by two parallel products (Tm: [C][SC] scratch).  Starts
+// after, and ends with, a barrier.
+template <int SC>
+__device__ void block_inverse32(const float *Nm, float *Em, float *Tm) {
+    constexpr int C = 32, HB = 16;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    if (tid < C) {
+        const int blk = tid / HB, c = blk * HB + tid % HB;
+        for (int i = blk * HB; i < blk * HB + HB; ++i) {
+            float y = 0.f;
+            if (i == c) y = 1.f;
+            else if (i > c)
+                for (int j = c; j < i; ++j) y -= Nm[i * SC + j] * Em[j * SC + c];
+            Em[i * SC + c] = y;
+        }
+        for (int i = 0; i < HB; ++i) Em[(blk == 0 ? i : HB + i) * SC + (blk == 0 ? HB : 0) + tid % HB] = 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < HB * HB; idx += nt) {
+        const int i = HB + idx / HB, j = idx % HB;
+        float acc = 0.f;
+        for (int l = j; l < HB; ++l) acc += Nm[i * SC + l] * Em[l * SC + j];
+        Tm[i * SC + j] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < HB * HB; idx += nt) {
+        const int i = HB + idx / HB, j = idx % HB;
+        float acc = 0.f;
+        for (int l = HB; l <= i; ++l) acc -= Em[i * SC + l] * Tm[l * SC + j];
+        Em[i * SC + j] = acc;
+    }
+    __syncthreads();
+}
+
 }  // namespace dplr
 }  // namespace kda

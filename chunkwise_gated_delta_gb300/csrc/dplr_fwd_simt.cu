@@ -22,6 +22,7 @@
 
 #include "dplr_common.cuh"
 #include "kda_internal.h"
+#include "warp_gemm.cuh"
 
 namespace kda {
 namespace {
@@ -37,14 +38,19 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-template <int DK, typename Tin, typename Tg>
+// Row strides = 4 (mod 32) for the fragment reads of the warp-tiled products.
+__host__ __device__ constexpr int pad4(int n) { return n + 4; }
+
+// Products run as warp-tiled 32 x N blocks (warp_gemm.cuh): tf32 tensor-core
+// MMAs for bf16 inputs (TF32), exact float32 for float32 inputs.
+template <int DK, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads)
 dplr_fwd_simt_kernel(const DplrParams p) {
-    constexpr int SK = DK + 1;     // padded row stride of [C][DK] tiles
-    constexpr int SC = kC + 1;     // padded row stride of [C][C] tiles
-    constexpr int SV = kDVS + 1;
+    constexpr int SK = pad4(DK), SC = pad4(kC), SV = pad4(kDVS);
     extern __shared__ float smem[];
-    float *Ql = smem;                 // [C][SK]
+    float4 *rows = reinterpret_cast<float4 *>(smem);   // [C] eq. (4) data per row (clip)
+    float *Gm = smem + 4 * kC;        // [C][SK]  raw gate, then Gamma
+    float *Ql = Gm + kC * SK;         // [C][SK]
     float *Kr = Ql + kC * SK;         // [C][SK]
     float *Ar = Kr + kC * SK;         // [C][SK]
     float *Bl = Ar + kC * SK;         // [C][SK]
@@ -54,13 +60,13 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     float *Pk = Lbk + kC * SC;        // [C][SC]  Q<- K->^T * M
     float *Pa = Pk + kC * SC;         // [C][SC]  Q<- A->^T * M
     float *Em = Pa + kC * SC;         // [C][SC]  E
-    float *Vm = Em + kC * SC;         // [C][SV]  v slice
+    float *Ts = Em + kC * SC;         // [C][SC]  scratch of the inverse
+    float *Vm = Ts + kC * SC;         // [C][SV]  v slice
     float *Tm = Vm + kC * SV;         // [C][SV]  (B<- K->^T * M_{-1}) V
     float *Xm = Tm + kC * SV;         // [C][SV]  X
     float *Sm = Xm + kC * SV;         // [DVS][SK] state slice
     float *gC = Sm + kDVS * SK;       // [DK]
-    float4 *rows = reinterpret_cast<float4 *>(gC + DK);   // [C] eq. (4) data per row (clip)
-    static_assert((5 * kC * SK + 5 * kC * SC + 3 * kC * SV + kDVS * SK + DK) % 4 == 0, "float4 rows alignment");
+    float *gsc = gC + DK;             // [C]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS;
@@ -77,94 +83,69 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     for (int t0 = 0; t0 < T; t0 += kC) {
         const int nvalid = min(kC, T - t0);
         __syncthreads();
-        // ---- Gamma (from the clipped gate when asked) and the rescaled tiles
+        // ---- Gamma (from the clipped gate when asked) and the rescaled tiles; the v slice
         if (p.clip) {
             dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
             __syncthreads();
         }
-        dplr::load_rescaled<DK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, nullptr, Ql, Kr, Ar, Bl, gC);
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             const int c = idx / kDVS, e = idx % kDVS;
             Vm[c * SV + e] = c < nvalid ? to_f(v[(((size_t)b * T + t0 + c) * H + h) * dv + e0 + e]) : 0.f;
         }
+        dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gC, gsc);
         __syncthreads();
         // ---- the four chunk Gram matrices
-        for (int idx = tid; idx < kC * kC; idx += kThreads) {
-            const int i = idx / kC, j = idx % kC;
-            float lab = 0.f, lbk = 0.f, pk = 0.f, pa = 0.f;
-            if (j <= i) {
-                for (int d = 0; d < DK; ++d) {
-                    const float kr = Kr[j * SK + d], ar = Ar[j * SK + d];
-                    const float bl = Bl[i * SK + d], ql = Ql[i * SK + d];
-                    lab += bl * ar;
-                    lbk += bl * kr;
-                    pk += ql * kr;
-                    pa += ql * ar;
-                }
-            }
-            Lab[i * SC + j] = j < i ? lab : 0.f;
-            Lbk[i * SC + j] = j < i ? lbk : 0.f;
-            Pk[i * SC + j] = pk;
-            Pa[i * SC + j] = pa;
+        {
+            auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
+            auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
+            auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
+            auto aQl = [&](int i, int d) { return Ql[i * SK + d]; };
+            wg::gemm_pair<kC, TF32>(DK, aBl, bAr, DK, aBl, bKr, [&](int i, int j, float x, float y) {
+                Lab[i * SC + j] = j < i ? x : 0.f;
+                Lbk[i * SC + j] = j < i ? y : 0.f;
+            });
+            wg::gemm_pair<kC, TF32>(DK, aQl, bKr, DK, aQl, bAr, [&](int i, int j, float x, float y) {
+                Pk[i * SC + j] = j <= i ? x : 0.f;
+                Pa[i * SC + j] = j <= i ? y : 0.f;
+            });
         }
         __syncthreads();
-        // ---- E = (I + Lab)^{-1}: column c by forward substitution
-        if (tid < kC) {
-            const int c = tid;
-            for (int i = 0; i < kC; ++i) {
-                float y = 0.f;
-                if (i == c) y = 1.f;
-                else if (i > c)
-                    for (int j = c; j < i; ++j) y -= Lab[i * SC + j] * Em[j * SC + c];
-                Em[i * SC + c] = y;
-            }
-        }
-        // ---- Lbk V (independent of E)
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = 0.f;
-            for (int j = 0; j < i; ++j) acc += Lbk[i * SC + j] * Vm[j * SV + e];
-            Tm[i * SV + e] = acc;
-        }
+        // ---- E = (I + Lab)^{-1} ; (B<- K->^T * M_{-1}) V ; W = E B<-
+        dplr::block_inverse32<SC>(Lab, Em, Ts);
+        wg::gemm<kDVS, TF32>(
+            kC, [&](int i, int j) { return Lbk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
+            [&](int i, int e, float x) { Tm[i * SV + e] = x; });
+        wg::gemm<DK, TF32>(
+            kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
+            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
         __syncthreads();
-        // ---- W = E B<-,  C = -E (Lbk V)  (C is kept in X for now)
-        for (int idx = tid; idx < kC * DK; idx += kThreads) {
-            const int i = idx / DK, d = idx % DK;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Em[i * SC + j] * Bl[j * SK + d];
-            Wm[i * SK + d] = acc;
-        }
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc -= Em[i * SC + j] * Tm[j * SV + e];
-            Xm[i * SV + e] = acc;
-        }
-        __syncthreads();
-        // ---- X = C - W S^T
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = Xm[i * SV + e];
-            for (int d = 0; d < DK; ++d) acc -= Wm[i * SK + d] * Sm[e * SK + d];
-            Xm[i * SV + e] = acc;
-        }
+        // ---- X = C - W S^T with C = -E (B<- K->^T * M_{-1}) V
+        wg::gemm2<kDVS, TF32>(
+            kC, [&](int i, int j) { return -Em[i * SC + j]; }, [&](int j, int e) { return Tm[j * SV + e]; }, DK,
+            [&](int i, int d) { return -Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
+            [&](int i, int e, float x) { Xm[i * SV + e] = x; });
         __syncthreads();
         // ---- O = Q<- S^T + (Q<- K->^T * M) V + (Q<- A->^T * M) X
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = 0.f;
-            for (int d = 0; d < DK; ++d) acc += Ql[i * SK + d] * Sm[e * SK + d];
-            for (int j = 0; j <= i; ++j) acc += Pk[i * SC + j] * Vm[j * SV + e] + Pa[i * SC + j] * Xm[j * SV + e];
-            if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = from_f<Tin>(acc);
+        {
+            int r0, c0;
+            wg::origin<kDVS>(r0, c0);
+            float acc[kDVS / 32][4] = {};
+            wg::tile<kDVS / 32, TF32>(acc, r0, c0, DK, [&](int i, int d) { return Ql[i * SK + d]; },
+                                      [&](int d, int e) { return Sm[e * SK + d]; });
+            wg::tile<kDVS / 32, TF32>(acc, r0, c0, kC, [&](int i, int j) { return Pk[i * SC + j]; },
+                                      [&](int j, int e) { return Vm[j * SV + e]; });
+            wg::tile<kDVS / 32, TF32>(acc, r0, c0, kC, [&](int i, int j) { return Pa[i * SC + j]; },
+                                      [&](int j, int e) { return Xm[j * SV + e]; });
+            wg::store<kDVS / 32>(acc, r0, c0, [&](int i, int e, float x) {
+                if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = from_f<Tin>(x);
+            });
         }
         __syncthreads();
         // ---- S <- (S + V^T K-> + X^T A->) Diag(gamma^C)
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            float acc = Sm[e * SK + d];
-            for (int c = 0; c < kC; ++c) acc += Vm[c * SV + e] * Kr[c * SK + d] + Xm[c * SV + e] * Ar[c * SK + d];
-            Sm[e * SK + d] = acc * gC[d];
-        }
+        wg::gemm2<DK, TF32>(
+            kC, [&](int e, int c) { return Vm[c * SV + e]; }, [&](int c, int d) { return Kr[c * SK + d]; }, kC,
+            [&](int e, int c) { return Xm[c * SV + e]; }, [&](int c, int d) { return Ar[c * SK + d]; },
+            [&](int e, int d, float x) { Sm[e * SK + d] = (Sm[e * SK + d] + x) * gC[d]; });
     }
     __syncthreads();
     if (p.ht) {
@@ -177,18 +158,20 @@ dplr_fwd_simt_kernel(const DplrParams p) {
 
 template <int DK>
 constexpr size_t dplr_smem_bytes() {
-    return sizeof(float) * (size_t)(5 * kC * (DK + 1) + 5 * kC * (kC + 1) + 3 * kC * (kDVS + 1) +
-                                    kDVS * (DK + 1) + DK + 4 * kC);
+    return sizeof(float) * (size_t)(4 * kC + 6 * kC * pad4(DK) + 6 * kC * pad4(kC) + 3 * kC * pad4(kDVS) +
+                                    kDVS * pad4(DK) + DK + kC);
 }
 
 template <int DK, typename Tin, typename Tg>
 cudaError_t launch_dk(const DplrParams &p, cudaStream_t s) {
+    constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const size_t smem = dplr_smem_bytes<DK>();
-    cudaError_t e = cudaFuncSetAttribute(dplr_fwd_simt_kernel<DK, Tin, Tg>,
+    static_assert(dplr_smem_bytes<128>() <= 227 * 1024, "shared memory");
+    cudaError_t e = cudaFuncSetAttribute(dplr_fwd_simt_kernel<DK, Tin, Tg, kTf32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.dv / kDVS, p.H, p.B);
-    dplr_fwd_simt_kernel<DK, Tin, Tg><<<grid, kThreads, smem, s>>>(p);
+    dplr_fwd_simt_kernel<DK, Tin, Tg, kTf32><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
