@@ -30,6 +30,7 @@
 
 #include "dplr_common.cuh"
 #include "kda_internal.h"
+#include "warp_gemm.cuh"
 
 namespace kda {
 namespace {
@@ -38,28 +39,52 @@ using dplr::ldf;
 using dplr::stf;
 
 constexpr int kC = 16;       // chunk length
-constexpr int kSC = kC + 1;
 constexpr int kDVS = 32;
 constexpr int kThreads = 256;
 
+// Row strides = 4 (mod 32) for the fragment reads of the warp-tiled products.
+__host__ __device__ constexpr int pad4(int n) { return n + 4; }
+constexpr int kSC4 = pad4(kC);
+
+// E = (I + Nm)^{-1} for a strictly lower 16 x 16 Nm: forward substitution,
+// one column per thread of the first warp.  Starts after, ends with, a barrier.
+template <int SC>
+__device__ void inverse16(const float *Nm, float *Em) {
+    if (threadIdx.x < kC) {
+        const int c = threadIdx.x;
+        for (int i = 0; i < kC; ++i) {
+            float y = 0.f;
+            if (i == c) y = 1.f;
+            else if (i > c)
+                for (int j = c; j < i; ++j) y -= Nm[i * SC + j] * Em[j * SC + c];
+            Em[i * SC + c] = y;
+        }
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------------ kernel A
-template <int DK, typename Tin, typename Tg>
+// Products run as warp-tiled blocks (warp_gemm.cuh): tf32 tensor-core MMAs for
+// bf16 inputs (TF32), exact float32 for float32 inputs.
+template <int DK, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrParams p) {
-    constexpr int SK = DK + 1, SV = kDVS + 1;
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
     extern __shared__ float smem[];
     float4 *rows = reinterpret_cast<float4 *>(smem);      // [C]
-    float *Kr = smem + 4 * kC;           // [C][SK]
+    float *Gm = smem + 4 * kC;           // [C][SK]  gate scratch
+    float *Kr = Gm + kC * SK;
     float *Ar = Kr + kC * SK;
     float *Bl = Ar + kC * SK;
     float *Wm = Bl + kC * SK;
     float *Sm = Wm + kC * SK;            // [DVS][SK]
-    float *Nm = Sm + kDVS * SK;          // [C][SC]
-    float *Em = Nm + kC * kSC;
-    float *Nk = Em + kC * kSC;
-    float *Vm = Nk + kC * kSC;           // [C][SV]
+    float *Nm = Sm + kDVS * SK;          // [C][SC]  B<- A->^T * M_{-1}
+    float *Em = Nm + kC * SC;
+    float *Nk = Em + kC * SC;            // B<- K->^T * M_{-1}
+    float *Vm = Nk + kC * SC;            // [C][SV]
     float *T1 = Vm + kC * SV;
     float *Xm = T1 + kC * SV;
     float *gam = Xm + kC * SV;           // [DK]
+    float *gsc = gam + DK;               // [C]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -83,50 +108,42 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
             dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
             __syncthreads();
         }
-        dplr::load_rescaled<DK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, nullptr, nullptr, Kr, Ar, Bl, gam);
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             const int c = idx / kDVS, e = idx % kDVS;
             Vm[c * SV + e] = c < nvalid ? ldf(v, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
         }
-        dplr::inverse_e<DK, kC>(Bl, Ar, Nm, Em);
-        // B<- K->^T * M_{-1} ; W = E B<-
-        for (int idx = tid; idx < kC * kC; idx += kThreads) {
-            const int i = idx / kC, j = idx % kC;
-            float acc = 0.f;
-            if (j < i)
-                for (int d = 0; d < DK; ++d) acc += Bl[i * SK + d] * Kr[j * SK + d];
-            Nk[i * kSC + j] = acc;
-        }
-        for (int idx = tid; idx < kC * DK; idx += kThreads) {
-            const int i = idx / DK, d = idx % DK;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Em[i * kSC + j] * Bl[j * SK + d];
-            Wm[i * SK + d] = acc;
+        dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, nullptr, Kr, Ar, Bl, gam, gsc);
+        __syncthreads();
+        {
+            auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
+            wg::gemm16_pair<kC, TF32>(
+                DK, aBl, [&](int d, int j) { return Ar[j * SK + d]; }, DK, aBl,
+                [&](int d, int j) { return Kr[j * SK + d]; }, [&](int i, int j, float x, float y) {
+                    Nm[i * SC + j] = j < i ? x : 0.f;
+                    Nk[i * SC + j] = j < i ? y : 0.f;
+                });
         }
         __syncthreads();
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = 0.f;
-            for (int j = 0; j < i; ++j) acc += Nk[i * kSC + j] * Vm[j * SV + e];
-            T1[i * SV + e] = acc;
-        }
+        inverse16<SC>(Nm, Em);
+        // W = E B<- ; Nk V
+        wg::gemm16<DK, TF32>(
+            kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
+            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+        wg::gemm16<kDVS, TF32>(
+            kC, [&](int i, int j) { return Nk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
+            [&](int i, int e, float x) { T1[i * SV + e] = x; });
         __syncthreads();
         // V_2 = -E (Nk V) - W S^T
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc -= Em[i * kSC + j] * T1[j * SV + e];
-            for (int d = 0; d < DK; ++d) acc -= Wm[i * SK + d] * Sm[e * SK + d];
-            Xm[i * SV + e] = acc;
-        }
+        wg::gemm16_2<kDVS, TF32>(
+            kC, [&](int i, int j) { return -Em[i * SC + j]; }, [&](int j, int e) { return T1[j * SV + e]; }, DK,
+            [&](int i, int d) { return -Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
+            [&](int i, int e, float x) { Xm[i * SV + e] = x; });
         __syncthreads();
         // S <- (S + V^T K-> + V_2^T A->) Diag(gamma^C)
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            float acc = Sm[e * SK + d];
-            for (int c = 0; c < kC; ++c) acc += Vm[c * SV + e] * Kr[c * SK + d] + Xm[c * SV + e] * Ar[c * SK + d];
-            Sm[e * SK + d] = acc * gam[d];
-        }
+        wg::gemm2<DK, TF32>(
+            kC, [&](int e, int c) { return Vm[c * SV + e]; }, [&](int c, int d) { return Kr[c * SK + d]; }, kC,
+            [&](int e, int c) { return Xm[c * SV + e]; }, [&](int c, int d) { return Ar[c * SK + d]; },
+            [&](int e, int d, float x) { Sm[e * SK + d] = (Sm[e * SK + d] + x) * gam[d]; });
     }
     __syncthreads();
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
@@ -136,22 +153,24 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
 }
 
 // ------------------------------------------------------------------ kernel B
-template <int DK, typename Tin, typename Tg>
+template <int DK, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrParams p) {
-    constexpr int SK = DK + 1, SV = kDVS + 1;
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
     extern __shared__ float smem[];
     float4 *rows = reinterpret_cast<float4 *>(smem);
-    float *Ql = smem + 4 * kC;           // [C][SK]
+    float *Gm = smem + 4 * kC;           // [C][SK]  gate scratch
+    float *Ql = Gm + kC * SK;
     float *Ar = Ql + kC * SK;
     float *Bl = Ar + kC * SK;
     float *Wm = Bl + kC * SK;
     float *dS = Wm + kC * SK;            // [DVS][SK]
     float *Nm = dS + kDVS * SK;          // [C][SC]
-    float *Em = Nm + kC * kSC;
-    float *Pa = Em + kC * kSC;
-    float *dO = Pa + kC * kSC;           // [C][SV]
+    float *Em = Nm + kC * SC;
+    float *Pa = Em + kC * SC;
+    float *dO = Pa + kC * SC;            // [C][SV]
     float *dC = dO + kC * SV;
     float *gam = dC + kC * SV;           // [DK]
+    float *gsc = gam + DK;               // [C]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -175,43 +194,37 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
             dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
             __syncthreads();
         }
-        dplr::load_rescaled<DK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, nullptr, Ql, nullptr, Ar, Bl, gam);
         for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
             const int c = idx / kDVS, e = idx % kDVS;
             dO[c * SV + e] = c < nvalid ? ldf(dop, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
         }
-        dplr::inverse_e<DK, kC>(Bl, Ar, Nm, Em);
-        // P_a = Q<- A->^T * M ; W = E B<-
-        for (int idx = tid; idx < kC * kC; idx += kThreads) {
-            const int i = idx / kC, j = idx % kC;
-            float acc = 0.f;
-            if (j <= i)
-                for (int d = 0; d < DK; ++d) acc += Ql[i * SK + d] * Ar[j * SK + d];
-            Pa[i * kSC + j] = acc;
-        }
-        for (int idx = tid; idx < kC * DK; idx += kThreads) {
-            const int i = idx / DK, d = idx % DK;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc += Em[i * kSC + j] * Bl[j * SK + d];
-            Wm[i * SK + d] = acc;
+        dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, nullptr, Ar, Bl, gam, gsc);
+        __syncthreads();
+        {
+            auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
+            wg::gemm16_pair<kC, TF32>(
+                DK, [&](int i, int d) { return Bl[i * SK + d]; }, bAr, DK, [&](int i, int d) { return Ql[i * SK + d]; },
+                bAr, [&](int i, int j, float x, float y) {
+                    Nm[i * SC + j] = j < i ? x : 0.f;
+                    Pa[i * SC + j] = j <= i ? y : 0.f;
+                });
         }
         __syncthreads();
-        // dC = A-> Diag(gamma^C) dS^T + P_a^T dO
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int i = idx / kDVS, e = idx % kDVS;
-            float acc = 0.f;
-            for (int d = 0; d < DK; ++d) acc += Ar[i * SK + d] * gam[d] * dS[e * SK + d];
-            for (int j = i; j < kC; ++j) acc += Pa[j * kSC + i] * dO[j * SV + e];
-            dC[i * SV + e] = acc;
-        }
+        inverse16<SC>(Nm, Em);
+        // W = E B<- ; dC = A-> Diag(gamma^C) dS^T + P_a^T dO
+        wg::gemm16<DK, TF32>(
+            kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
+            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+        wg::gemm16_2<kDVS, TF32>(
+            DK, [&](int i, int d) { return Ar[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[e * SK + d]; },
+            kC, [&](int i, int j) { return Pa[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
+            [&](int i, int e, float x) { dC[i * SV + e] = x; });
         __syncthreads();
         // dS <- dS Diag(gamma^C) + dO^T Q<- - dC^T W
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            float acc = dS[e * SK + d] * gam[d];
-            for (int c = 0; c < kC; ++c) acc += dO[c * SV + e] * Ql[c * SK + d] - dC[c * SV + e] * Wm[c * SK + d];
-            dS[e * SK + d] = acc;
-        }
+        wg::gemm2<DK, TF32>(
+            kC, [&](int e, int c) { return dO[c * SV + e]; }, [&](int c, int d) { return Ql[c * SK + d]; }, kC,
+            [&](int e, int c) { return -dC[c * SV + e]; }, [&](int c, int d) { return Wm[c * SK + d]; },
+            [&](int e, int d, float x) { dS[e * SK + d] = dS[e * SK + d] * gam[d] + x; });
     }
     __syncthreads();
     if (p.grad_h0) {
@@ -225,12 +238,13 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
 // ------------------------------------------------------------------ kernel C
 template <int DK, int DV>
 constexpr size_t grad_smem_floats() {
-    return (size_t)4 * kC + (size_t)10 * kC * (DK + 1) + (size_t)5 * kC * (DV + 1) + (size_t)12 * kC * kSC + DK + 2 * kC;
+    return (size_t)4 * kC + (size_t)10 * kC * pad4(DK) + (size_t)5 * kC * pad4(DV) + (size_t)12 * kC * kSC4 + DK +
+           3 * kC;
 }
 
-template <int DK, int DV, typename Tin, typename Tg>
+template <int DK, int DV, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParams p) {
-    constexpr int SK = DK + 1, SV = DV + 1;
+    constexpr int SK = pad4(DK), SV = pad4(DV), SC = kSC4;
     extern __shared__ float smem[];
     float4 *rows = reinterpret_cast<float4 *>(smem);      // [C] (|a|^2, |b|^2, a.b, -log rho)
     float *Gm = smem + 4 * kC;           // [C][SK] Gamma
@@ -249,20 +263,21 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     float *dC = V2 + kC * SV;
     float *Ym = dC + kC * SV;            // Nk V, then E^T dC
     float *Nm = Ym + kC * SV;            // [C][SC] B<- A->^T * M_{-1}
-    float *Em = Nm + kC * kSC;
-    float *Nk = Em + kC * kSC;           // B<- K->^T * M_{-1}
-    float *Pk = Nk + kC * kSC;           // Q<- K->^T * M
-    float *Pa = Pk + kC * kSC;           // Q<- A->^T * M
-    float *O1 = Pa + kC * kSC;           // dO V^T * M
-    float *O2 = O1 + kC * kSC;           // dO V_2^T * M
-    float *Z1 = O2 + kC * kSC;           // dC V^T
-    float *dE = Z1 + kC * kSC;
-    float *Gx = dE + kC * kSC;           // E^T dC V^T * M_{-1}
-    float *dF = Gx + kC * kSC;
-    float *Tt = dF + kC * kSC;
-    float *gam = Tt + kC * kSC;          // [DK]
+    float *Em = Nm + kC * SC;
+    float *Nk = Em + kC * SC;            // B<- K->^T * M_{-1}
+    float *Pk = Nk + kC * SC;            // Q<- K->^T * M
+    float *Pa = Pk + kC * SC;            // Q<- A->^T * M
+    float *O1 = Pa + kC * SC;            // dO V^T * M
+    float *O2 = O1 + kC * SC;            // dO V_2^T * M
+    float *Z1 = O2 + kC * SC;            // dC V^T
+    float *dE = Z1 + kC * SC;
+    float *Gx = dE + kC * SC;            // E^T dC V^T * M_{-1}
+    float *dF = Gx + kC * SC;
+    float *Tt = dF + kC * SC;
+    float *gam = Tt + kC * SC;           // [DK]
     float *rsum = gam + DK;              // [C] row sums / dL/d(-log rho)
     float *aux = rsum + kC;              // [C]
+    float *gsc = aux + kC;               // [C]
 
     const int tid = threadIdx.x;
     const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -279,151 +294,127 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
         dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
         __syncthreads();
     }
-    dplr::load_rescaled<DK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam);
     for (int idx = tid; idx < kC * DV; idx += kThreads) {
         const int c = idx / DV, e = idx % DV;
         const size_t off = (((size_t)b * T + t0 + c) * H + h) * DV + e;
         Vm[c * SV + e] = c < nvalid ? ldf(v, off) : 0.f;
         dO[c * SV + e] = c < nvalid ? ldf(dop, off) : 0.f;
     }
-    dplr::inverse_e<DK, kC>(Bl, Ar, Nm, Em);
-    // Nk, Pk, Pa ; W = E B<-
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float nk = 0.f, pk = 0.f, pa = 0.f;
-        for (int d = 0; d < DK; ++d) {
-            const float kr = Kr[j * SK + d], ar = Ar[j * SK + d];
-            nk += Bl[i * SK + d] * kr;
-            pk += Ql[i * SK + d] * kr;
-            pa += Ql[i * SK + d] * ar;
-        }
-        Nk[i * kSC + j] = j < i ? nk : 0.f;
-        Pk[i * kSC + j] = j <= i ? pk : 0.f;
-        Pa[i * kSC + j] = j <= i ? pa : 0.f;
-    }
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int i = idx / DK, d = idx % DK;
-        float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc += Em[i * kSC + j] * Bl[j * SK + d];
-        Wm[i * SK + d] = acc;
+    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
+    __syncthreads();
+    // Grams: N_ab, N_bk, P_k, P_a
+    {
+        auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
+        auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
+        auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
+        auto aQl = [&](int i, int d) { return Ql[i * SK + d]; };
+        wg::gemm16_pair<kC, TF32>(DK, aBl, bAr, DK, aBl, bKr, [&](int i, int j, float x, float y) {
+            Nm[i * SC + j] = j < i ? x : 0.f;
+            Nk[i * SC + j] = j < i ? y : 0.f;
+        });
+        wg::gemm16_pair<kC, TF32>(DK, aQl, bKr, DK, aQl, bAr, [&](int i, int j, float x, float y) {
+            Pk[i * SC + j] = j <= i ? x : 0.f;
+            Pa[i * SC + j] = j <= i ? y : 0.f;
+        });
     }
     __syncthreads();
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int i = idx / DV, e = idx % DV;
-        float acc = 0.f;
-        for (int j = 0; j < i; ++j) acc += Nk[i * kSC + j] * Vm[j * SV + e];
-        Ym[i * SV + e] = acc;
-    }
+    inverse16<SC>(Nm, Em);
+    // W = E B<- ; Nk V
+    wg::gemm16<DK, TF32>(
+        kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
+        [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+    wg::gemm16<DV, TF32>(
+        kC, [&](int i, int j) { return Nk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
+        [&](int i, int e, float x) { Ym[i * SV + e] = x; });
     __syncthreads();
     // V_2 = -E (Nk V) - W S_prev^T ; dC = A-> Diag(gamma^C) dS^T + P_a^T dO
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int i = idx / DV, e = idx % DV;
-        float x = 0.f, c = 0.f;
-        for (int j = 0; j <= i; ++j) x -= Em[i * kSC + j] * Ym[j * SV + e];
-        for (int d = 0; d < DK; ++d) {
-            x -= Wm[i * SK + d] * Sp[(size_t)e * DK + d];
-            c += Ar[i * SK + d] * gam[d] * dS[(size_t)e * DK + d];
-        }
-        for (int j = i; j < kC; ++j) c += Pa[j * kSC + i] * dO[j * SV + e];
-        V2[i * SV + e] = x;
-        dC[i * SV + e] = c;
-    }
+    wg::gemm16_2<DV, TF32>(
+        kC, [&](int i, int j) { return -Em[i * SC + j]; }, [&](int j, int e) { return Ym[j * SV + e]; }, DK,
+        [&](int i, int d) { return -Wm[i * SK + d]; }, [&](int d, int e) { return Sp[(size_t)e * DK + d]; },
+        [&](int i, int e, float x) { V2[i * SV + e] = x; });
+    wg::gemm16_2<DV, TF32>(
+        DK, [&](int i, int d) { return Ar[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[(size_t)e * DK + d]; },
+        kC, [&](int i, int j) { return Pa[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
+        [&](int i, int e, float x) { dC[i * SV + e] = x; });
     __syncthreads();
     // O1 = dO V^T * M ; O2 = dO V_2^T * M ; Z1 = dC V^T
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float o1 = 0.f, o2 = 0.f, z = 0.f;
-        for (int e = 0; e < DV; ++e) {
-            const float vj = Vm[j * SV + e];
-            o1 += dO[i * SV + e] * vj;
-            o2 += dO[i * SV + e] * V2[j * SV + e];
-            z += dC[i * SV + e] * vj;
-        }
-        O1[i * kSC + j] = j <= i ? o1 : 0.f;
-        O2[i * kSC + j] = j <= i ? o2 : 0.f;
-        Z1[i * kSC + j] = z;
+    {
+        auto aDO = [&](int i, int e) { return dO[i * SV + e]; };
+        auto bV = [&](int e, int j) { return Vm[j * SV + e]; };
+        wg::gemm16_pair<kC, TF32>(DV, aDO, bV, DV, aDO, [&](int e, int j) { return V2[j * SV + e]; },
+                                  [&](int i, int j, float x, float y) {
+                                      O1[i * SC + j] = j <= i ? x : 0.f;
+                                      O2[i * SC + j] = j <= i ? y : 0.f;
+                                  });
+        wg::gemm16<kC, TF32>(DV, [&](int i, int e) { return dC[i * SV + e]; }, bV,
+                             [&](int i, int j, float x) { Z1[i * SC + j] = x; });
     }
     __syncthreads();
     // dW = -dC S_prev ; dQ<- ; dK-> and dA-> without their F/G terms ; Y = E^T dC
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int i = idx / DK, d = idx % DK;
-        float aw = 0.f, aq = 0.f, ak = 0.f, aa = 0.f;
-        for (int e = 0; e < DV; ++e) {
-            const float sp = Sp[(size_t)e * DK + d], ds = dS[(size_t)e * DK + d];
-            aw -= dC[i * SV + e] * sp;
-            aq += dO[i * SV + e] * sp;
-            ak += Vm[i * SV + e] * ds;
-            aa += V2[i * SV + e] * ds;
-        }
-        ak *= gam[d];
-        aa *= gam[d];
-        for (int j = 0; j <= i; ++j) aq += O1[i * kSC + j] * Kr[j * SK + d] + O2[i * kSC + j] * Ar[j * SK + d];
-        for (int j = i; j < kC; ++j) {
-            ak += O1[j * kSC + i] * Ql[j * SK + d];
-            aa += O2[j * kSC + i] * Ql[j * SK + d];
-        }
-        Wm[i * SK + d] = aw;
-        dQl[i * SK + d] = aq;
-        dKr[i * SK + d] = ak;
-        dAr[i * SK + d] = aa;
+    {
+        auto bSp = [&](int e, int d) { return Sp[(size_t)e * DK + d]; };
+        auto bdS = [&](int e, int d) { return dS[(size_t)e * DK + d]; };
+        wg::gemm16<DK, TF32>(
+            DV, [&](int i, int e) { return dC[i * SV + e]; }, bSp, [&](int i, int d, float x) { Wm[i * SK + d] = -x; });
+        wg::gemm16_3<DK, TF32>(
+            DV, [&](int i, int e) { return dO[i * SV + e]; }, bSp, kC, [&](int i, int j) { return O1[i * SC + j]; },
+            [&](int j, int d) { return Kr[j * SK + d]; }, kC, [&](int i, int j) { return O2[i * SC + j]; },
+            [&](int j, int d) { return Ar[j * SK + d]; }, [&](int i, int d, float x) { dQl[i * SK + d] = x; });
+        auto bQl = [&](int j, int d) { return Ql[j * SK + d]; };
+        wg::gemm16_pair<DK, TF32>(
+            DV, [&](int i, int e) { return Vm[i * SV + e]; }, bdS, kC, [&](int i, int j) { return O1[j * SC + i]; }, bQl,
+            [&](int i, int d, float x1, float x2) { dKr[i * SK + d] = x1 * gam[d] + x2; });
+        wg::gemm16_pair<DK, TF32>(
+            DV, [&](int i, int e) { return V2[i * SV + e]; }, bdS, kC, [&](int i, int j) { return O2[j * SC + i]; }, bQl,
+            [&](int i, int d, float x1, float x2) { dAr[i * SK + d] = x1 * gam[d] + x2; });
     }
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int i = idx / DV, e = idx % DV;
-        float acc = 0.f;
-        for (int j = i; j < kC; ++j) acc += Em[j * kSC + i] * dC[j * SV + e];
-        Ym[i * SV + e] = acc;
-    }
+    wg::gemm16<DV, TF32>(
+        kC, [&](int i, int j) { return Em[j * SC + i]; }, [&](int j, int e) { return dC[j * SV + e]; },
+        [&](int i, int e, float x) { Ym[i * SV + e] = x; });
     __syncthreads();
     // dE = -Z1 Nk^T + dW B<-^T ; G = (Y V^T) * M_{-1}
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float de = 0.f, gx = 0.f;
-        for (int l = 0; l < j; ++l) de -= Z1[i * kSC + l] * Nk[j * kSC + l];
-        for (int d = 0; d < DK; ++d) de += Wm[i * SK + d] * Bl[j * SK + d];
-        if (j < i)
-            for (int e = 0; e < DV; ++e) gx += Ym[i * SV + e] * Vm[j * SV + e];
-        dE[i * kSC + j] = de;
-        Gx[i * kSC + j] = gx;
-    }
+    wg::gemm16_2<kC, TF32>(
+        kC, [&](int i, int l) { return -Z1[i * SC + l]; }, [&](int l, int j) { return Nk[j * SC + l]; }, DK,
+        [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int j) { return Bl[j * SK + d]; },
+        [&](int i, int j, float x) { dE[i * SC + j] = x; });
+    wg::gemm16<kC, TF32>(
+        DV, [&](int i, int e) { return Ym[i * SV + e]; }, [&](int e, int j) { return Vm[j * SV + e]; },
+        [&](int i, int j, float x) { Gx[i * SC + j] = j < i ? x : 0.f; });
     __syncthreads();
-    // dF = -E^T dE E^T
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float acc = 0.f;
-        for (int l = 0; l <= j; ++l) acc += dE[i * kSC + l] * Em[j * kSC + l];
-        Tt[i * kSC + j] = acc;
-    }
+    // dF = -E^T dE E^T (only dF * M_{-1} is used)
+    wg::gemm16<kC, TF32>(
+        kC, [&](int i, int l) { return dE[i * SC + l]; }, [&](int l, int j) { return Em[j * SC + l]; },
+        [&](int i, int j, float x) { Tt[i * SC + j] = x; });
     __syncthreads();
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
-        const int i = idx / kC, j = idx % kC;
-        float acc = 0.f;
-        for (int l = i; l < kC; ++l) acc -= Em[l * kSC + i] * Tt[l * kSC + j];
-        dF[i * kSC + j] = j < i ? acc : 0.f;      // only dF * M_{-1} is used
-    }
+    wg::gemm16<kC, TF32>(
+        kC, [&](int i, int l) { return Em[l * SC + i]; }, [&](int l, int j) { return Tt[l * SC + j]; },
+        [&](int i, int j, float x) { dF[i * SC + j] = j < i ? -x : 0.f; });
     __syncthreads();
     // dB<- = E^T dW - G K-> + (dF * M_{-1}) A-> ; dK-> -= G^T B<- ; dA-> += (dF * M_{-1})^T B<-
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int i = idx / DK, d = idx % DK;
-        float ab = 0.f, ak = dKr[i * SK + d], aa = dAr[i * SK + d];
-        for (int j = i; j < kC; ++j) ab += Em[j * kSC + i] * Wm[j * SK + d];
-        for (int j = 0; j < i; ++j) ab += -Gx[i * kSC + j] * Kr[j * SK + d] + dF[i * kSC + j] * Ar[j * SK + d];
-        for (int j = i + 1; j < kC; ++j) {
-            ak -= Gx[j * kSC + i] * Bl[j * SK + d];
-            aa += dF[j * kSC + i] * Bl[j * SK + d];
-        }
-        dBl[i * SK + d] = ab;
-        dKr[i * SK + d] = ak;
-        dAr[i * SK + d] = aa;
+    wg::gemm16_3<DK, TF32>(
+        kC, [&](int i, int j) { return Em[j * SC + i]; }, [&](int j, int d) { return Wm[j * SK + d]; }, kC,
+        [&](int i, int j) { return -Gx[i * SC + j]; }, [&](int j, int d) { return Kr[j * SK + d]; }, kC,
+        [&](int i, int j) { return dF[i * SC + j]; }, [&](int j, int d) { return Ar[j * SK + d]; },
+        [&](int i, int d, float x) { dBl[i * SK + d] = x; });
+    {
+        auto bBl = [&](int j, int d) { return Bl[j * SK + d]; };
+        wg::gemm16_pair<DK, TF32>(
+            kC, [&](int i, int j) { return Gx[j * SC + i]; }, bBl, kC, [&](int i, int j) { return dF[j * SC + i]; }, bBl,
+            [&](int i, int d, float xg, float xf) {
+                dKr[i * SK + d] -= xg;
+                dAr[i * SK + d] += xf;
+            });
     }
     // dV = K-> Diag(gamma^C) dS^T + P_k^T dO - Nk^T (E^T dC)
-    Tin *gv = static_cast<Tin *>(p.grad_v);
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int i = idx / DV, e = idx % DV;
-        float acc = 0.f;
-        for (int d = 0; d < DK; ++d) acc += Kr[i * SK + d] * gam[d] * dS[(size_t)e * DK + d];
-        for (int j = i; j < kC; ++j) acc += Pk[j * kSC + i] * dO[j * SV + e];
-        for (int j = i + 1; j < kC; ++j) acc -= Nk[j * kSC + i] * Ym[j * SV + e];
-        if (i < nvalid) stf(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, acc);
+    {
+        Tin *gv = static_cast<Tin *>(p.grad_v);
+        wg::gemm16_3<DV, TF32>(
+            DK, [&](int i, int d) { return Kr[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[(size_t)e * DK + d]; },
+            kC, [&](int i, int j) { return Pk[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; }, kC,
+            [&](int i, int j) { return -Nk[j * SC + i]; }, [&](int j, int e) { return Ym[j * SV + e]; },
+            [&](int i, int e, float x) {
+                if (i < nvalid) stf(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, x);
+            });
     }
     __syncthreads();
     // dq, dk ; dlogGamma into dQl
@@ -532,13 +523,13 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
 
 template <int DK>
 constexpr size_t states_smem_bytes() {
-    return sizeof(float) *
-           ((size_t)4 * kC + 4 * kC * (DK + 1) + kDVS * (DK + 1) + 3 * kC * kSC + 3 * kC * (kDVS + 1) + DK);
+    return sizeof(float) * ((size_t)4 * kC + 5 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * kSC4 +
+                            3 * kC * pad4(kDVS) + DK + kC);
 }
 template <int DK>
 constexpr size_t dstate_smem_bytes() {
-    return sizeof(float) *
-           ((size_t)4 * kC + 4 * kC * (DK + 1) + kDVS * (DK + 1) + 3 * kC * kSC + 2 * kC * (kDVS + 1) + DK);
+    return sizeof(float) * ((size_t)4 * kC + 5 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * kSC4 +
+                            2 * kC * pad4(kDVS) + DK + kC);
 }
 
 template <typename F>
@@ -548,18 +539,19 @@ cudaError_t set_smem(F *fn, size_t bytes) {
 
 template <int DK, int DV, typename Tin, typename Tg>
 cudaError_t launch_all(const DplrParams &p, cudaStream_t s) {
+    constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const int N = (p.T + kC - 1) / kC;
     cudaError_t e;
     const size_t sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
     static_assert(sizeof(float) * grad_smem_floats<128, 128>() <= 227 * 1024, "kernel C shared memory");
-    if ((e = set_smem(dplr_bwd_states_kernel<DK, Tin, Tg>, sa)) != cudaSuccess) return e;
-    if ((e = set_smem(dplr_bwd_dstate_kernel<DK, Tin, Tg>, sb)) != cudaSuccess) return e;
-    if ((e = set_smem(dplr_bwd_grad_kernel<DK, DV, Tin, Tg>, sc)) != cudaSuccess) return e;
+    if ((e = set_smem(dplr_bwd_states_kernel<DK, Tin, Tg, kTf32>, sa)) != cudaSuccess) return e;
+    if ((e = set_smem(dplr_bwd_dstate_kernel<DK, Tin, Tg, kTf32>, sb)) != cudaSuccess) return e;
+    if ((e = set_smem(dplr_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
     const dim3 gscan(p.dv / kDVS, p.H, p.B), ggrad(N, p.H, p.B);
-    dplr_bwd_states_kernel<DK, Tin, Tg><<<gscan, kThreads, sa, s>>>(p);
-    dplr_bwd_dstate_kernel<DK, Tin, Tg><<<gscan, kThreads, sb, s>>>(p);
-    dplr_bwd_grad_kernel<DK, DV, Tin, Tg><<<ggrad, kThreads, sc, s>>>(p);
+    dplr_bwd_states_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sa, s>>>(p);
+    dplr_bwd_dstate_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sb, s>>>(p);
+    dplr_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<ggrad, kThreads, sc, s>>>(p);
     return cudaGetLastError();
 }
 

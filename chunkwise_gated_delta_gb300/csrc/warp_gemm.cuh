@@ -108,5 +108,74 @@ __device__ __forceinline__ void gemm_pair(int K1, const FA1 &A1, const FB1 &B1, 
             epi(r0 + g + 8 * (q >> 1), c0 + 8 * nt + 2 * t + (q & 1), a1[nt][q], a2[nt][q]);
 }
 
+// ---- 16-row blocks (16-token chunks): warp w owns columns w N / 8 .. + N / 8 (N >= 64),
+// or one 16 x 8 tile for N in {16, 32} (warps past N / 8 sit out).
+template <int N>
+__host__ __device__ constexpr int nt16() { return N >= 64 ? N / 64 : 1; }
+
+template <int N>
+__device__ __forceinline__ bool origin16(int &col0) {
+    const int w = threadIdx.x >> 5;
+    if constexpr (N >= 64) {
+        col0 = w * (N / 8);
+        return true;
+    } else {
+        col0 = w * 8;
+        return w < N / 8;
+    }
+}
+
+template <int N, bool TF32, typename FA, typename FB, typename FE>
+__device__ __forceinline__ void gemm16(int K, const FA &A, const FB &B, const FE &epi) {
+    constexpr int NT = nt16<N>();
+    int c0;
+    if (!origin16<N>(c0)) return;
+    float acc[NT][4] = {};
+    tile<NT, TF32>(acc, 0, c0, K, A, B);
+    store<NT>(acc, 0, c0, epi);
+}
+
+template <int N, bool TF32, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
+__device__ __forceinline__ void gemm16_2(int K1, const FA1 &A1, const FB1 &B1, int K2, const FA2 &A2, const FB2 &B2,
+                                         const FE &epi) {
+    constexpr int NT = nt16<N>();
+    int c0;
+    if (!origin16<N>(c0)) return;
+    float acc[NT][4] = {};
+    tile<NT, TF32>(acc, 0, c0, K1, A1, B1);
+    tile<NT, TF32>(acc, 0, c0, K2, A2, B2);
+    store<NT>(acc, 0, c0, epi);
+}
+
+template <int N, bool TF32, typename FA1, typename FB1, typename FA2, typename FB2, typename FA3, typename FB3,
+          typename FE>
+__device__ __forceinline__ void gemm16_3(int K1, const FA1 &A1, const FB1 &B1, int K2, const FA2 &A2, const FB2 &B2,
+                                         int K3, const FA3 &A3, const FB3 &B3, const FE &epi) {
+    constexpr int NT = nt16<N>();
+    int c0;
+    if (!origin16<N>(c0)) return;
+    float acc[NT][4] = {};
+    tile<NT, TF32>(acc, 0, c0, K1, A1, B1);
+    tile<NT, TF32>(acc, 0, c0, K2, A2, B2);
+    tile<NT, TF32>(acc, 0, c0, K3, A3, B3);
+    store<NT>(acc, 0, c0, epi);
+}
+
+template <int N, bool TF32, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
+__device__ __forceinline__ void gemm16_pair(int K1, const FA1 &A1, const FB1 &B1, int K2, const FA2 &A2,
+                                            const FB2 &B2, const FE &epi) {
+    constexpr int NT = nt16<N>();
+    int c0;
+    if (!origin16<N>(c0)) return;
+    float a1[NT][4] = {}, a2[NT][4] = {};
+    tile<NT, TF32>(a1, 0, c0, K1, A1, B1);
+    tile<NT, TF32>(a2, 0, c0, K2, A2, B2);
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) epi(g + 8 * (q >> 1), c0 + 8 * nt + 2 * t + (q & 1), a1[nt][q], a2[nt][q]);
+}
+
 }  // namespace wg
 }  // namespace kda
