@@ -123,7 +123,7 @@ def kda_chunk_fwd(q, k, v, g=None, beta=None, h0=None, *, gate=None, scale_v=Tru
 
 
 def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, scale_v=True,
-                          output_final_state=True, o=None, ht=None, stream=None):
+                          output_final_state=True, o=None, ht=None, stream=None, cu_seqlens=None):
     """``kda_chunk_fwd_noalloc`` of the C ABI: the forward without a workspace.
 
     For callers that cannot allocate device memory at the call (for instance
@@ -138,11 +138,12 @@ def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, sca
         _check(t, name)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    nseq = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if o is None:
         o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
     if ht is None and output_final_state:
-        ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device)
-    args = make_args(q, k, v, g, beta, h0, o, ht, gate=gate, scale_v=scale_v)
+        ht = torch.empty(nseq, H, dv, dk, dtype=torch.float32, device=q.device)
+    args = make_args(q, k, v, g, beta, h0, o, ht, gate=gate, scale_v=scale_v, cu_seqlens=cu_seqlens)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     rc = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))

@@ -231,3 +231,31 @@ def test_varlen_special_cases_bf16():
             if lens[i]:
                 assert rel(o[:, starts[i]:starts[i + 1]], ro) <= 5e-3, (variant, i)
             assert rel(ht[i], rh[0]) <= 5e-3, (variant, i)
+
+
+def test_long_sequence_sampled_head():
+    """A long sequence: T = 65536 (1024 chunks) for one head pair, bf16, against the oracle."""
+    w = custom("kda", 1, 65536, 2, 128, 128, dtype=torch.bfloat16, h0=True)
+    x = make_inputs(w, seed=12)
+    o, ht = run_gpu(x, "kda")
+    ro, rh = run_oracle(x, "kda", heads=[(0, 1)])
+    assert rel(o[0, :, 1], ro[0, :, 1]) <= 5e-3 and rel(ht[0, 1], rh[0, 1]) <= 5e-3
+    assert np.isfinite(o).all()
+
+
+def test_varlen_noalloc_and_many_sequences():
+    """64 packed sequences of mixed lengths through the no-allocation entry point."""
+    from chunkwise_gated_delta_gb300 import kda_chunk_fwd_noalloc
+    rng = np.random.default_rng(3)
+    lens = [int(n) for n in rng.integers(0, 300, size=64)]
+    x, cu, refs, scale_v = _varlen_case(torch.bfloat16, lens, 128, 128, seed=20)
+    d = {k_: v_.to(DEV) for k_, v_ in x.items()}
+    o, ht = kda_chunk_fwd_noalloc(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], gate="channel",
+                                  scale_v=scale_v, cu_seqlens=cu.to(DEV))
+    torch.cuda.synchronize()
+    o, ht = o.double().cpu().numpy(), ht.double().cpu().numpy()
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    for i, (ro, rh) in enumerate(refs):
+        if lens[i]:
+            assert rel(o[:, starts[i]:starts[i + 1]], ro) <= 5e-3, i
+        assert rel(ht[i], rh[0]) <= 5e-3, i
