@@ -108,10 +108,8 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
             dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
             __syncthreads();
         }
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int c = idx / kDVS, e = idx % kDVS;
-            Vm[c * SV + e] = c < nvalid ? ldf(v, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
-        }
+        wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
+                                              Vm);
         dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, nullptr, Kr, Ar, Bl, gam, gsc);
         __syncthreads();
         {
@@ -194,10 +192,8 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
             dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
             __syncthreads();
         }
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int c = idx / kDVS, e = idx % kDVS;
-            dO[c * SV + e] = c < nvalid ? ldf(dop, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
-        }
+        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv,
+                                              nvalid, dO);
         dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, nullptr, Ar, Bl, gam, gsc);
         __syncthreads();
         {
@@ -294,11 +290,10 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
         dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
         __syncthreads();
     }
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int c = idx / DV, e = idx % DV;
-        const size_t off = (((size_t)b * T + t0 + c) * H + h) * DV + e;
-        Vm[c * SV + e] = c < nvalid ? ldf(v, off) : 0.f;
-        dO[c * SV + e] = c < nvalid ? ldf(dop, off) : 0.f;
+    {
+        const size_t r0 = (((size_t)b * T + t0) * H + h) * DV, rs = (size_t)H * DV;
+        wg::load_tile<kC, DV, SV, kThreads>(v + r0, rs, nvalid, Vm);
+        wg::load_tile<kC, DV, SV, kThreads>(dop + r0, rs, nvalid, dO);
     }
     dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
     __syncthreads();

@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
+#include "warp_gemm.cuh"
 
 namespace kda {
 namespace dplr {
@@ -141,11 +142,11 @@ __device__ void inverse_e(const float *Bl, const float *Ar, float *Nm, float *Em
     __syncthreads();
 }
 
-// load_rescaled with all threads loading the raw tiles first (coalesced), then
-// one thread per key channel running the cumsum down its column in shared
-// memory.  Gm is required here (it holds the raw gate in between); Ql, Kr, Ar,
-// Bl may be null; gsc holds C floats (scalar gates).  Contains one barrier;
-// the caller synchronises before reading the tiles.
+// load_rescaled with all threads loading the raw tiles first (16-byte vector
+// loads, 256 threads), then one thread per key channel running the cumsum down
+// its column in shared memory.  Gm is required here (it holds the raw gate in
+// between); Ql, Kr, Ar, Bl may be null; gsc holds C floats (scalar gates).
+// Contains one barrier; the caller synchronises before reading the tiles.
 template <int DK, int SK, int C, typename Tin, typename Tg>
 __device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int nvalid, const float4 *rows,
                                   float *Gm, float *Ql, float *Kr, float *Ar, float *Bl, float *gam, float *gsc) {
@@ -155,18 +156,12 @@ __device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int
     const Tin *bb = static_cast<const Tin *>(p.b);
     const Tg *g = static_cast<const Tg *>(p.g);
     const int tid = threadIdx.x, nt = blockDim.x;
-    for (int idx = tid; idx < C * DK; idx += nt) {
-        const int c = idx / DK, d = idx % DK;
-        const bool ok = c < nvalid;
-        const size_t off = (((size_t)b * p.T + t0 + c) * p.H + h) * DK + d;
-        if (Ql) Ql[c * SK + d] = ok ? ldf(q, off) : 0.f;
-        if (Kr) Kr[c * SK + d] = ok ? ldf(k, off) : 0.f;
-        if (Ar) Ar[c * SK + d] = ok ? ldf(a, off) : 0.f;
-        if (Bl) Bl[c * SK + d] = ok ? ldf(bb, off) : 0.f;
-        float gv = 0.f;
-        if (ok && p.gate_kind == KDA_GATE_CHANNEL) gv = ldf(g, off);
-        Gm[c * SK + d] = gv;
-    }
+    const size_t r0 = (((size_t)b * p.T + t0) * p.H + h) * DK, rs = (size_t)p.H * DK;
+    if (Ql) wg::load_tile<C, DK, SK, 256>(q + r0, rs, nvalid, Ql);
+    if (Kr) wg::load_tile<C, DK, SK, 256>(k + r0, rs, nvalid, Kr);
+    if (Ar) wg::load_tile<C, DK, SK, 256>(a + r0, rs, nvalid, Ar);
+    if (Bl) wg::load_tile<C, DK, SK, 256>(bb + r0, rs, nvalid, Bl);
+    if (p.gate_kind == KDA_GATE_CHANNEL) wg::load_tile<C, DK, SK, 256>(g + r0, rs, nvalid, Gm);
     if (tid < C) {
         float gv = 0.f;
         if (tid < nvalid && p.gate_kind == KDA_GATE_SCALAR) gv = ldf(g, ((size_t)b * p.T + t0 + tid) * p.H + h);
@@ -177,7 +172,7 @@ __device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int
         float G = 0.f, gm = 1.f;
         for (int c = 0; c < C; ++c) {
             if (c < nvalid) {
-                float gv = p.gate_kind == KDA_GATE_CHANNEL ? Gm[c * SK + d] : gsc[c];
+                float gv = p.gate_kind == KDA_GATE_CHANNEL ? Gm[c * SK + d] : gsc[c];   // channel: staged above
                 if (p.clip) gv = fminf(gv, rows[c].w);
                 G += gv;
                 gm = expf(G);

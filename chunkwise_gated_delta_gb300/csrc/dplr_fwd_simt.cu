@@ -88,10 +88,8 @@ dplr_fwd_simt_kernel(const DplrParams p) {
             dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
             __syncthreads();
         }
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int c = idx / kDVS, e = idx % kDVS;
-            Vm[c * SV + e] = c < nvalid ? to_f(v[(((size_t)b * T + t0 + c) * H + h) * dv + e0 + e]) : 0.f;
-        }
+        wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
+                                              Vm);
         dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gC, gsc);
         __syncthreads();
         // ---- the four chunk Gram matrices

@@ -68,14 +68,10 @@ __device__ void load_rescaled_par(const BwdParams &p, int b, int h, int t0, int 
     const Tg *g = static_cast<const Tg *>(p.g);
     const int tid = threadIdx.x;
     float *graw = Gm ? Gm : Kr;
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
-        const int c = idx / DK, d = idx % DK;
-        const bool ok = c < nvalid;
-        const size_t off = (((size_t)b * p.T + t0 + c) * p.H + h) * DK + d;
-        Kl[c * SK + d] = ok ? ld(k, off) : 0.f;
-        if (Ql) Ql[c * SK + d] = ok ? ld(q, off) : 0.f;
-        if (p.gate_kind == KDA_GATE_CHANNEL) graw[c * SK + d] = ok ? ld(g, off) : 0.f;
-    }
+    const size_t r0 = (((size_t)b * p.T + t0) * p.H + h) * DK, rs = (size_t)p.H * DK;
+    wg::load_tile<kC, DK, SK, kThreads>(k + r0, rs, nvalid, Kl);
+    if (Ql) wg::load_tile<kC, DK, SK, kThreads>(q + r0, rs, nvalid, Ql);
+    if (p.gate_kind == KDA_GATE_CHANNEL) wg::load_tile<kC, DK, SK, kThreads>(g + r0, rs, nvalid, graw);
     if (p.gate_kind == KDA_GATE_SCALAR && tid < kC)
         gsc[tid] = tid < nvalid ? ld(g, ((size_t)b * p.T + t0 + tid) * p.H + h) : 0.f;
     __syncthreads();
@@ -183,10 +179,8 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
             const int e = idx / DK, d = idx % DK;
             Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
         }
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int c = idx / kDVS, e = idx % kDVS;
-            Vm[c * SV + e] = c < nvalid ? ld(v, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
-        }
+        wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
+                                              Vm);
         load_beta<Tin>(p, b, h, t0, nvalid, beta);
         load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, nullptr, Kl, Kr, gam, gsc);
         __syncthreads();
@@ -259,10 +253,8 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
             const int e = idx / DK, d = idx % DK;
             dSws[((size_t)n * dv + e0 + e) * DK + d] = dS[e * SK + d];
         }
-        for (int idx = tid; idx < kC * kDVS; idx += kThreads) {
-            const int c = idx / kDVS, e = idx % kDVS;
-            dO[c * SV + e] = c < nvalid ? ld(dop, (((size_t)b * T + t0 + c) * H + h) * dv + e0 + e) : 0.f;
-        }
+        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
+                                              dO);
         load_beta<Tin>(p, b, h, t0, nvalid, beta);
         load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, Ql, Kl, Kr, gam, gsc);
         __syncthreads();
@@ -351,11 +343,10 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     // ---- loads: Gamma and the rescaled tiles, v, dO, beta
     load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, dbeta);
     load_beta<Tin>(p, b, h, t0, nvalid, beta);
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
-        const int c = idx / DV, e = idx % DV;
-        const size_t off = (((size_t)b * T + t0 + c) * H + h) * DV + e;
-        Vm[c * SV + e] = c < nvalid ? ld(v, off) : 0.f;
-        dO[c * SV + e] = c < nvalid ? ld(dop, off) : 0.f;
+    {
+        const size_t r0 = (((size_t)b * T + t0) * H + h) * DV, rs = (size_t)H * DV;
+        wg::load_tile<kC, DV, SV, kThreads>(v + r0, rs, nvalid, Vm);
+        wg::load_tile<kC, DV, SV, kThreads>(dop + r0, rs, nvalid, dO);
     }
     __syncthreads();
     // ---- P = Q<- K->^T * M and N = K<- K->^T * M_{-1}

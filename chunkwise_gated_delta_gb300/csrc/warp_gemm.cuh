@@ -9,6 +9,8 @@
 // the same fragment elements exactly in float32 on the CUDA cores.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "tc_common.cuh"
 
 namespace kda {
@@ -175,6 +177,54 @@ __device__ __forceinline__ void gemm16_pair(int K1, const FA1 &A1, const FB1 &B1
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) epi(g + 8 * (q >> 1), c0 + 8 * nt + 2 * t + (q & 1), a1[nt][q], a2[nt][q]);
+}
+
+// ---- staging of [rows][D] tiles from global memory
+// 8 consecutive elements as floats: one 16-byte load for bf16, two for fp32.
+__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void ld8(const float *p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// Rows c < R of a row-major source (row c at src + c * rs elements, D columns,
+// 16-byte aligned) into dst[c * SD + d] as floats; rows >= nvalid become zero.
+// Every thread issues all of its loads before its shared-memory stores.
+template <int R, int D, int SD, int NT, typename T>
+__device__ __forceinline__ void load_tile(const T *src, size_t rs, int nvalid, float *dst) {
+    static_assert(D % 8 == 0 && SD % 4 == 0, "tile shape");
+    constexpr int V = D / 8, TOT = R * V, IT = (TOT + NT - 1) / NT;
+    float x[IT][8];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int idx = threadIdx.x + it * NT;
+        const int c = idx / V, d0 = (idx % V) * 8;
+        if (idx < TOT && c < nvalid) {
+            ld8(src + (size_t)c * rs + d0, x[it]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[it][j] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int idx = threadIdx.x + it * NT;
+        if (idx < TOT) {
+            const int c = idx / V, d0 = (idx % V) * 8;
+            float4 *q = reinterpret_cast<float4 *>(dst + c * SD + d0);
+            q[0] = make_float4(x[it][0], x[it][1], x[it][2], x[it][3]);
+            q[1] = make_float4(x[it][4], x[it][5], x[it][6], x[it][7]);
+        }
+    }
 }
 
 }  // namespace wg
