@@ -348,6 +348,11 @@ kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream) {
     p.status = reinterpret_cast<int *>(ws);
     p.ws_S = reinterpret_cast<float *>(ws + kStatusBytes);
     p.ws_dS = p.ws_S + (N + 1) * per_state;
+    p.ws_prep = p.ws_dS + N * per_state;
+    const size_t recs = N * (size_t)args->B * args->H * (3 * 32 * 32 + 3 * 32 * (size_t)args->dk + 32 * (size_t)args->dv +
+                                                          args->dk);
+    p.ws_vnew = p.ws_prep + recs;
+    p.ws_du = p.ws_vnew + N * (size_t)args->B * args->H * 32 * args->dv;
     return from_cuda(kda::launch_bwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -17,13 +17,17 @@
 //   dS_prev = dS Diag(gamma^C) + dO^T Q<- - dU^T W
 //
 // (dW against S_[t-1]; dK-> with the output term the page's final
-// combination carries.)  Three kernels:
-//   A  forward scan per (value slice, head, batch): the state before every
-//      chunk and the final state, into the workspace;
-//   B  reverse scan per (value slice, head, batch): dS after every chunk into
-//      the workspace, and dh0;
-//   C  one CTA per (chunk, head, batch): every other gradient of the chunk,
-//      from the stored S_prev, S_next and dS.
+// combination carries.)  Four kernels:
+//   prep  one CTA per (chunk, head, batch): everything of a chunk that does
+//         not depend on the state (A~, P, N, W, U, K~, Q<-, gamma^C) into a
+//         chunk record in the workspace;
+//   A     forward scan per (value slice, head, batch) from the records: the
+//         state before every chunk, the final state and V_new, into the
+//         workspace;
+//   B     reverse scan per (value slice, head, batch) from the records: dS
+//         after every chunk and dU into the workspace, and dh0;
+//   C     one CTA per (chunk, head, batch): every other gradient of the chunk,
+//         from its record, V_new, dU and the stored S_prev, S_next and dS.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -140,73 +144,134 @@ __device__ void block_inverse(const float *beta, const float *Nm, float *Am, flo
 __host__ __device__ constexpr int pad4(int n) { return n + 4; }
 constexpr int kSC4 = pad4(kC);
 
-// ------------------------------------------------------------------ kernel A
-// Products run as warp-tiled 32 x N blocks (warp_gemm.cuh): tf32 tensor-core
-// MMAs for bf16 inputs (TF32), exact float32 for float32 inputs.
-template <int DK, typename Tin, typename Tg, bool TF32>
-__global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
+// ------------------------------------------------------------------ chunk records
+// Everything of a chunk that does not depend on the state, written once by the
+// prep kernel (float32): A~, P = Q<- K->^T * M, N = K<- K->^T * M_{-1},
+// W = A~ Diag(beta) K<-, U = A~ Diag(beta) V (or A~ V), K~ = K-> Diag(gamma^C),
+// Q<- and gamma^C.
+__host__ __device__ constexpr size_t rec_floats(int dk, int dv) {
+    return (size_t)3 * kC * kC + (size_t)3 * kC * dk + (size_t)kC * dv + dk;
+}
+template <int DK, int DV>
+struct Rec {
+    static constexpr int A = 0, P = kC * kC, N = 2 * kC * kC, W = 3 * kC * kC, U = W + kC * DK, KT = U + kC * DV,
+                         QL = KT + kC * DK, GC = QL + kC * DK;
+    static_assert(rec_floats(DK, DV) == (size_t)GC + DK && rec_floats(DK, DV) % 4 == 0, "record layout");
+};
+
+// ------------------------------------------------------------------ prep kernel
+// One CTA per (chunk, head, batch).
+template <int DK, int DV, typename Tin, typename Tg, bool TF32>
+__global__ void __launch_bounds__(kThreads) kda_bwd_prep_kernel(const BwdParams p) {
+    constexpr int SK = pad4(DK), SV = pad4(DV), SC = kSC4;
+    using R = Rec<DK, DV>;
     extern __shared__ float smem[];
-    float *Kl = smem;                  // [C][SK]
+    float *Gm = smem;                  // [C][SK]  raw gate, then Gamma
+    float *Ql = Gm + kC * SK;          // [C][SK]
+    float *Kl = Ql + kC * SK;          // [C][SK]
     float *Kr = Kl + kC * SK;          // [C][SK]
-    float *Wm = Kr + kC * SK;          // [C][SK]
-    float *Sm = Wm + kC * SK;          // [DVS][SK]
-    float *Nm = Sm + kDVS * SK;        // [C][SC]
+    float *Vm = Kr + kC * SK;          // [C][SV]
+    float *Nm = Vm + kC * SV;          // [C][SC]
     float *Am = Nm + kC * SC;          // [C][SC]
-    float *Tm = Am + kC * SC;          // [C][SC]  scratch of the inverse
-    float *Vm = Tm + kC * SC;          // [C][SV]  v slice
-    float *Um = Vm + kC * SV;          // [C][SV]  U, then V_new
-    float *gam = Um + kC * SV;         // [DK]
-    float *beta = gam + DK;            // [C]
+    float *Tm = Am + kC * SC;          // [C][SC]
+    float *beta = Tm + kC * SC;        // [C]
     float *gsc = beta + kC;            // [C]
+    float *gam = gsc + kC;             // [DK]
+
+    const int tid = threadIdx.x;
+    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
+    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    float *rec = p.ws_prep + (((size_t)b * H + h) * N + n) * rec_floats(DK, DV);
+    const bool sv = p.scale_v != 0;
+
+    load_beta<Tin>(p, b, h, t0, nvalid, beta);
+    wg::load_tile<kC, DV, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * DV, (size_t)H * DV, nvalid, Vm);
+    load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, gsc);
+    __syncthreads();
+    {
+        auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
+        wg::gemm_pair<kC, TF32>(
+            DK, [&](int i, int d) { return Ql[i * SK + d]; }, bKr, DK, [&](int i, int d) { return Kl[i * SK + d]; },
+            bKr, [&](int i, int j, float pv, float nv) {
+                rec[R::P + i * kC + j] = j <= i ? pv : 0.f;
+                const float nn = j < i ? nv : 0.f;
+                Nm[i * SC + j] = nn;
+                rec[R::N + i * kC + j] = nn;
+            });
+    }
+    for (int idx = tid; idx < kC * DK; idx += kThreads) {
+        const int i = idx / DK, d = idx % DK;
+        rec[R::KT + idx] = Kr[i * SK + d] * gam[d];
+        rec[R::QL + idx] = Ql[i * SK + d];
+    }
+    for (int d = tid; d < DK; d += kThreads) rec[R::GC + d] = gam[d];
+    __syncthreads();
+    block_inverse<SC>(beta, Nm, Am, Tm);
+    for (int idx = tid; idx < kC * kC; idx += kThreads) rec[R::A + idx] = Am[(idx / kC) * SC + idx % kC];
+    wg::gemm<DK, TF32>(
+        kC, [&](int i, int j) { return Am[i * SC + j] * beta[j]; }, [&](int j, int d) { return Kl[j * SK + d]; },
+        [&](int i, int d, float x) { rec[R::W + i * DK + d] = x; });
+    wg::gemm<DV, TF32>(
+        kC, [&](int i, int j) { return Am[i * SC + j] * (sv ? beta[j] : 1.f); },
+        [&](int j, int e) { return Vm[j * SV + e]; }, [&](int i, int e, float x) { rec[R::U + i * DV + e] = x; });
+}
+
+template <int DK, int DV>
+constexpr size_t prep_smem_bytes() {
+    return sizeof(float) * ((size_t)4 * kC * pad4(DK) + kC * pad4(DV) + 3 * kC * kSC4 + 2 * kC + DK);
+}
+
+// ------------------------------------------------------------------ kernel A
+// The forward state scan from the chunk records: V_new = U - W S^T,
+// S <- S Diag(gamma^C) + V_new^T K~.  One CTA per (32-wide value slice, head, batch).
+template <int DK, int DV, bool TF32>
+__global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParams p) {
+    constexpr int SK = pad4(DK), SV = pad4(kDVS);
+    using R = Rec<DK, DV>;
+    extern __shared__ float smem[];
+    float *Wm = smem;                  // [C][SK]
+    float *KT = Wm + kC * SK;          // [C][SK]
+    float *Sm = KT + kC * SK;          // [DVS][SK]
+    float *Um = Sm + kDVS * SK;        // [C][SV]  U, then V_new
+    float *gam = Um + kC * SV;         // [DK]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, H = p.H, dv = p.dv, N = (T + kC - 1) / kC;
-    const Tin *v = static_cast<const Tin *>(p.v);
     const size_t head = (size_t)b * H + h;
     float *Sws = p.ws_S + head * (size_t)(N + 1) * dv * DK;
-    const bool sv = p.scale_v != 0;
+    const float *recs = p.ws_prep + head * N * rec_floats(DK, DV);
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         Sm[e * SK + d] = p.h0 ? p.h0[(head * dv + e0 + e) * DK + d] : 0.f;
     }
     for (int n = 0; n < N; ++n) {
-        const int t0 = n * kC, nvalid = min(kC, T - t0);
+        const float *rec = recs + (size_t)n * rec_floats(DK, DV);
         __syncthreads();
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
         }
-        wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
-                                              Vm);
-        load_beta<Tin>(p, b, h, t0, nvalid, beta);
-        load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, nullptr, Kl, Kr, gam, gsc);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KT, DK, kC, KT);
+        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::U + e0, DV, kC, Um);
+        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
         __syncthreads();
-        // N = K<- K->^T * M_{-1}, then A~
-        wg::gemm<kC, TF32>(
-            DK, [&](int i, int d) { return Kl[i * SK + d]; }, [&](int d, int j) { return Kr[j * SK + d]; },
-            [&](int i, int j, float x) { Nm[i * SC + j] = j < i ? x : 0.f; });
-        __syncthreads();
-        block_inverse<SC>(beta, Nm, Am, Tm);
-        // W = A~ Diag(beta) K<- ; U = A~ Diag(beta) V (or A~ V)
-        wg::gemm<DK, TF32>(
-            kC, [&](int i, int j) { return Am[i * SC + j] * beta[j]; }, [&](int j, int d) { return Kl[j * SK + d]; },
-            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
-        wg::gemm<kDVS, TF32>(
-            kC, [&](int i, int j) { return Am[i * SC + j] * (sv ? beta[j] : 1.f); },
-            [&](int j, int e) { return Vm[j * SV + e]; }, [&](int i, int e, float x) { Um[i * SV + e] = x; });
-        __syncthreads();
-        // V_new = U - W S^T
+        float *vn = p.ws_vnew + ((head * N + n) * kC) * (size_t)dv + e0;     // V_new rows of this chunk
         wg::gemm<kDVS, TF32>(
             DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
-            [&](int i, int e, float x) { Um[i * SV + e] -= x; });
+            [&](int i, int e, float x) {
+                const float y = Um[i * SV + e] - x;
+                Um[i * SV + e] = y;
+                vn[(size_t)i * dv + e] = y;
+            });
         __syncthreads();
-        // S <- (S + V_new^T K->) Diag(gamma^C)
         wg::gemm<DK, TF32>(
-            kC, [&](int e, int c) { return Um[c * SV + e]; }, [&](int c, int d) { return Kr[c * SK + d]; },
-            [&](int e, int d, float x) { Sm[e * SK + d] = (Sm[e * SK + d] + x) * gam[d]; });
+            kC, [&](int e, int c) { return Um[c * SV + e]; }, [&](int c, int d) { return KT[c * SK + d]; },
+            [&](int e, int d, float x) { Sm[e * SK + d] = Sm[e * SK + d] * gam[d] + x; });
     }
     __syncthreads();
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
@@ -216,24 +281,21 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
 }
 
 // ------------------------------------------------------------------ kernel B
-template <int DK, typename Tin, typename Tg, bool TF32>
+// The reverse scan from the chunk records: dU = K~ dS^T + P^T dO,
+// dS <- dS Diag(gamma^C) + dO^T Q<- - dU^T W.
+template <int DK, int DV, typename Tin, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParams p) {
     constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
+    using R = Rec<DK, DV>;
     extern __shared__ float smem[];
-    float *Ql = smem;                  // [C][SK]
-    float *Kl = Ql + kC * SK;          // [C][SK]
-    float *Kr = Kl + kC * SK;          // [C][SK]
-    float *Wm = Kr + kC * SK;          // [C][SK]
-    float *dS = Wm + kC * SK;          // [DVS][SK]
-    float *Nm = dS + kDVS * SK;        // [C][SC]
-    float *Am = Nm + kC * SC;          // [C][SC]
-    float *Pm = Am + kC * SC;          // [C][SC]
-    float *Tm = Pm + kC * SC;          // [C][SC]  scratch of the inverse
-    float *dO = Tm + kC * SC;          // [C][SV]
+    float *Wm = smem;                  // [C][SK]
+    float *QL = Wm + kC * SK;          // [C][SK]
+    float *KT = QL + kC * SK;          // [C][SK]
+    float *dS = KT + kC * SK;          // [DVS][SK]
+    float *Pm = dS + kDVS * SK;        // [C][SC]
+    float *dO = Pm + kC * SC;          // [C][SV]
     float *dU = dO + kC * SV;          // [C][SV]
     float *gam = dU + kC * SV;         // [DK]
-    float *beta = gam + DK;            // [C]
-    float *gsc = beta + kC;            // [C]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -241,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
     const Tin *dop = static_cast<const Tin *>(p.grad_o);
     const size_t head = (size_t)b * H + h;
     float *dSws = p.ws_dS + head * (size_t)N * dv * DK;
+    const float *recs = p.ws_prep + head * N * rec_floats(DK, DV);
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
@@ -248,40 +311,31 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
     }
     for (int n = N - 1; n >= 0; --n) {
         const int t0 = n * kC, nvalid = min(kC, T - t0);
+        const float *rec = recs + (size_t)n * rec_floats(DK, DV);
         __syncthreads();
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             dSws[((size_t)n * dv + e0 + e) * DK + d] = dS[e * SK + d];
         }
-        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
-                                              dO);
-        load_beta<Tin>(p, b, h, t0, nvalid, beta);
-        load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, nullptr, Ql, Kl, Kr, gam, gsc);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::QL, DK, kC, QL);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KT, DK, kC, KT);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::P, kC, kC, Pm);
+        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv,
+                                              nvalid, dO);
+        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
         __syncthreads();
-        // P = Q<- K->^T * M ; N = K<- K->^T * M_{-1}
-        {
-            auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
-            wg::gemm_pair<kC, TF32>(
-                DK, [&](int i, int d) { return Ql[i * SK + d]; }, bKr, DK,
-                [&](int i, int d) { return Kl[i * SK + d]; }, bKr, [&](int i, int j, float pv, float nv) {
-                    Pm[i * SC + j] = j <= i ? pv : 0.f;
-                    Nm[i * SC + j] = j < i ? nv : 0.f;
-                });
-        }
-        __syncthreads();
-        block_inverse<SC>(beta, Nm, Am, Tm);
-        // W = A~ Diag(beta) K<- ; dU = K-> Diag(gamma^C) dS^T + P^T dO
-        wg::gemm<DK, TF32>(
-            kC, [&](int i, int j) { return Am[i * SC + j] * beta[j]; }, [&](int j, int d) { return Kl[j * SK + d]; },
-            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+        float *du = p.ws_du + ((head * N + n) * kC) * (size_t)dv + e0;       // dU rows of this chunk
         wg::gemm2<kDVS, TF32>(
-            DK, [&](int i, int d) { return Kr[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[e * SK + d]; },
-            kC, [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
-            [&](int i, int e, float x) { dU[i * SV + e] = x; });
+            DK, [&](int i, int d) { return KT[i * SK + d]; }, [&](int d, int e) { return dS[e * SK + d]; }, kC,
+            [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
+            [&](int i, int e, float x) {
+                dU[i * SV + e] = x;
+                du[(size_t)i * dv + e] = x;
+            });
         __syncthreads();
-        // dS <- dS Diag(gamma^C) + dO^T Q<- - dU^T W
         wg::gemm2<DK, TF32>(
-            kC, [&](int e, int c) { return dO[c * SV + e]; }, [&](int c, int d) { return Ql[c * SK + d]; }, kC,
+            kC, [&](int e, int c) { return dO[c * SV + e]; }, [&](int c, int d) { return QL[c * SK + d]; }, kC,
             [&](int e, int c) { return -dU[c * SV + e]; }, [&](int c, int d) { return Wm[c * SK + d]; },
             [&](int e, int d, float x) { dS[e * SK + d] = dS[e * SK + d] * gam[d] + x; });
     }
@@ -349,34 +403,18 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
         wg::load_tile<kC, DV, SV, kThreads>(dop + r0, rs, nvalid, dO);
     }
     __syncthreads();
-    // ---- P = Q<- K->^T * M and N = K<- K->^T * M_{-1}
+    // ---- A~, P, N, W and U from the chunk record
     {
-        auto bKr = [&](int k, int j) { return Kr[j * SK + k]; };
-        wg::gemm_pair<kC, TF32>(
-            DK, [&](int i, int d) { return Ql[i * SK + d]; }, bKr, DK, [&](int i, int d) { return Kl[i * SK + d]; },
-            bKr, [&](int i, int j, float pv, float nv) {
-                Pm[i * SC + j] = j <= i ? pv : 0.f;
-                Nm[i * SC + j] = j < i ? nv : 0.f;
-            });
+        using R = Rec<DK, DV>;
+        const float *rec = p.ws_prep + (head * N + n) * rec_floats(DK, DV);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::A, kC, kC, Am);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::P, kC, kC, Pm);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::N, kC, kC, Nm);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        // V_new and dU of this chunk, from the two scans
+        wg::load_tile<kC, DV, SV, kThreads>(p.ws_vnew + (head * N + n) * (size_t)kC * DV, DV, kC, Vn);
+        wg::load_tile<kC, DV, SV, kThreads>(p.ws_du + (head * N + n) * (size_t)kC * DV, DV, kC, dU);
     }
-    __syncthreads();
-    block_inverse<SC>(beta, Nm, Am, Tm);
-    // ---- W = A~ Diag(beta) K<- ; U = A~ Diag(beta) V (or A~ V)
-    wg::gemm<DK, TF32>(
-        kC, [&](int i, int j) { return Am[i * SC + j] * beta[j]; }, [&](int j, int d) { return Kl[j * SK + d]; },
-        [&](int i, int d, float x) { Wm[i * SK + d] = x; });
-    wg::gemm<DV, TF32>(
-        kC, [&](int i, int j) { return Am[i * SC + j] * (sv ? beta[j] : 1.f); },
-        [&](int j, int e) { return Vm[j * SV + e]; }, [&](int i, int e, float x) { Vn[i * SV + e] = x; });
-    __syncthreads();
-    // ---- V_new = U - W S_prev^T ; dU = K-> Diag(gamma^C) dS^T + P^T dO
-    wg::gemm<DV, TF32>(
-        DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sp[(size_t)e * DK + d]; },
-        [&](int i, int e, float x) { Vn[i * SV + e] -= x; });
-    wg::gemm2<DV, TF32>(
-        DK, [&](int i, int d) { return Kr[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[(size_t)e * DK + d]; },
-        kC, [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
-        [&](int i, int e, float x) { dU[i * SV + e] = x; });
     __syncthreads();
     // ---- dO V_new^T * M (into Pm)
     wg::gemm<kC, TF32>(
@@ -521,13 +559,11 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
 
 template <int DK>
 constexpr size_t states_smem_bytes() {
-    return sizeof(float) *
-           ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * kSC4 + 2 * kC * pad4(kDVS) + DK + 2 * kC);
+    return sizeof(float) * ((size_t)2 * kC * pad4(DK) + kDVS * pad4(DK) + kC * pad4(kDVS) + DK);
 }
 template <int DK>
 constexpr size_t dstate_smem_bytes() {
-    return sizeof(float) *
-           ((size_t)4 * kC * pad4(DK) + kDVS * pad4(DK) + 4 * kC * kSC4 + 2 * kC * pad4(kDVS) + DK + 2 * kC);
+    return sizeof(float) * ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + kC * kSC4 + 2 * kC * pad4(kDVS) + DK);
 }
 
 template <typename F>
@@ -540,16 +576,18 @@ cudaError_t launch_all(const BwdParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const int N = (p.T + kC - 1) / kC;
     cudaError_t e;
-    const size_t sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
+    const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
     static_assert(sizeof(float) * grad_smem_floats<128, 128>() <= 227 * 1024, "kernel C shared memory");
-    if ((e = set_smem(kda_bwd_states_kernel<DK, Tin, Tg, kTf32>, sa)) != cudaSuccess) return e;
-    if ((e = set_smem(kda_bwd_dstate_kernel<DK, Tin, Tg, kTf32>, sb)) != cudaSuccess) return e;
+    if ((e = set_smem(kda_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32>, sp)) != cudaSuccess) return e;
+    if ((e = set_smem(kda_bwd_states_kernel<DK, DV, kTf32>, sa)) != cudaSuccess) return e;
+    if ((e = set_smem(kda_bwd_dstate_kernel<DK, DV, Tin, kTf32>, sb)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
-    const dim3 gscan(p.dv / kDVS, p.H, p.B), ggrad(N, p.H, p.B);
-    kda_bwd_states_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sa, s>>>(p);
-    kda_bwd_dstate_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sb, s>>>(p);
-    kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<ggrad, kThreads, sc, s>>>(p);
+    const dim3 gscan(p.dv / kDVS, p.H, p.B), gchunk(N, p.H, p.B);
+    kda_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sp, s>>>(p);
+    kda_bwd_states_kernel<DK, DV, kTf32><<<gscan, kThreads, sa, s>>>(p);
+    kda_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sb, s>>>(p);
+    kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sc, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -566,7 +604,7 @@ cudaError_t launch_typed(const BwdParams &p, cudaStream_t s) {
 
 size_t bwd_state_bytes(int B, int T, int H, int dk, int dv) {
     const size_t N = (T + kC - 1) / kC;
-    return sizeof(float) * (size_t)B * H * (2 * N + 1) * dv * dk;
+    return sizeof(float) * (size_t)B * H * ((2 * N + 1) * dv * dk + N * rec_floats(dk, dv) + 2 * N * kC * dv);
 }
 
 cudaError_t launch_bwd_simt(const BwdParams &p, int in_bf16, int g_is_bf16, cudaStream_t s) {

@@ -55,6 +55,9 @@ struct BwdParams {
     float *grad_h0;
     float *ws_S;            // [B, H, N + 1, dv, dk] states before each chunk, then the final state
     float *ws_dS;           // [B, H, N, dv, dk] gradients of the state after each chunk
+    float *ws_prep;         // [B, H, N] chunk records (state-independent operands)
+    float *ws_vnew;         // [B, H, N, C, dv] V_new of every chunk
+    float *ws_du;           // [B, H, N, C, dv] dU of every chunk
     int *status;
 };
 

@@ -175,7 +175,11 @@ typedef struct {
 
 /*
  * Bytes of workspace kda_chunk_bwd needs (0 on bad args): 256 for the status
- * word plus the float32 chunk states, (2 ceil(T/32) + 1) B H dv dk 4 bytes.
+ * word, the float32 chunk states and state gradients,
+ * (2 N + 1) B H dv dk 4 bytes with N = ceil(T/32), and one float32 record of
+ * state-independent chunk operands per chunk,
+ * N B H (3 32 32 + 3 32 dk + 32 dv + dk) 4 bytes, and the chunk products
+ * V_new and dU, 2 N B H 32 dv 4 bytes.
  */
 size_t kda_chunk_bwd_workspace(const kda_bwd_args *args);
 

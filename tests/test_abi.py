@@ -160,7 +160,8 @@ def _bwd_args(**over):
 def test_bwd_workspace_query(lib):
     need = lib.kda_chunk_bwd_workspace(ctypes.byref(_bwd_args()))
     n_chunks = (100 + 31) // 32
-    assert need == 256 + 4 * 2 * 4 * (2 * n_chunks + 1) * 128 * 128
+    record = 3 * 32 * 32 + 3 * 32 * 128 + 32 * 128 + 128
+    assert need == 256 + 4 * 2 * 4 * ((2 * n_chunks + 1) * 128 * 128 + n_chunks * record + 2 * n_chunks * 32 * 128)
     assert lib.kda_chunk_bwd_workspace(ctypes.byref(_bwd_args(dk=96))) == 0
     assert lib.kda_chunk_bwd_workspace(None) == 0
 
