@@ -39,6 +39,7 @@ namespace {
 constexpr int kC = 32;       // chunk length
 constexpr int kDVS = 32;     // value rows per CTA in the scans
 constexpr int kThreads = 256;
+constexpr int kThreadsC = 512;   // the gradient kernel: 16 warps to hide the latency of its L2 reads
 
 template <typename T> __device__ __forceinline__ float ld(const T *p, size_t i);
 template <> __device__ __forceinline__ float ld<float>(const float *p, size_t i) { return p[i]; }
@@ -64,7 +65,7 @@ __device__ void load_beta(const BwdParams &p, int b, int h, int t0, int nvalid, 
 // last value); gam[d] = gamma^C.  Gm and Ql may be null (the raw g then waits
 // in Kr); gsc holds C floats (scalar gates).  Contains one barrier; the
 // caller synchronises before reading the tiles.
-template <int DK, int SK, typename Tin, typename Tg>
+template <int DK, int SK, typename Tin, typename Tg, int NT = kThreads>
 __device__ void load_rescaled_par(const BwdParams &p, int b, int h, int t0, int nvalid, float *Gm, float *Ql,
                                   float *Kl, float *Kr, float *gam, float *gsc) {
     const Tin *q = static_cast<const Tin *>(p.q);
@@ -73,9 +74,9 @@ __device__ void load_rescaled_par(const BwdParams &p, int b, int h, int t0, int 
     const int tid = threadIdx.x;
     float *graw = Gm ? Gm : Kr;
     const size_t r0 = (((size_t)b * p.T + t0) * p.H + h) * DK, rs = (size_t)p.H * DK;
-    wg::load_tile<kC, DK, SK, kThreads>(k + r0, rs, nvalid, Kl);
-    if (Ql) wg::load_tile<kC, DK, SK, kThreads>(q + r0, rs, nvalid, Ql);
-    if (p.gate_kind == KDA_GATE_CHANNEL) wg::load_tile<kC, DK, SK, kThreads>(g + r0, rs, nvalid, graw);
+    wg::load_tile<kC, DK, SK, NT>(k + r0, rs, nvalid, Kl);
+    if (Ql) wg::load_tile<kC, DK, SK, NT>(q + r0, rs, nvalid, Ql);
+    if (p.gate_kind == KDA_GATE_CHANNEL) wg::load_tile<kC, DK, SK, NT>(g + r0, rs, nvalid, graw);
     if (p.gate_kind == KDA_GATE_SCALAR && tid < kC)
         gsc[tid] = tid < nvalid ? ld(g, ((size_t)b * p.T + t0 + tid) * p.H + h) : 0.f;
     __syncthreads();
@@ -122,7 +123,7 @@ __device__ void block_inverse(const float *beta, const float *Nm, float *Am, flo
     }
     __syncthreads();
     // Tm = L21 A11 (rows HB.., cols ..HB), L21 = Diag(beta) N21
-    for (int idx = tid; idx < HB * HB; idx += kThreads) {
+    for (int idx = tid; idx < HB * HB; idx += blockDim.x) {
         const int i = HB + idx / HB, j = idx % HB;
         float acc = 0.f;
         for (int l = j; l < HB; ++l) acc += beta[i] * Nm[i * SC + l] * Am[l * SC + j];
@@ -130,7 +131,7 @@ __device__ void block_inverse(const float *beta, const float *Nm, float *Am, flo
     }
     __syncthreads();
     // A21 = -A22 Tm
-    for (int idx = tid; idx < HB * HB; idx += kThreads) {
+    for (int idx = tid; idx < HB * HB; idx += blockDim.x) {
         const int i = HB + idx / HB, j = idx % HB;
         float acc = 0.f;
         for (int l = HB; l <= i; ++l) acc -= Am[i * SC + l] * Tm[l * SC + j];
@@ -352,13 +353,13 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
 
 template <int DK, int DV>
 constexpr size_t grad_smem_floats() {
-    return (size_t)8 * kC * pad4(DK) + (size_t)4 * kC * pad4(DV) + (size_t)5 * kC * kSC4 + 2 * kC + DK;
+    return (size_t)8 * kC * pad4(DK) + (size_t)4 * kC * pad4(DV) + (size_t)5 * kC * kSC4 + 2 * kC + 2 * DK;
 }
 
 // Products run as warp-tiled 32 x N blocks (warp_gemm.cuh): tf32 tensor-core
 // MMAs for bf16 inputs (TF32), exact float32 for float32 inputs.
 template <int DK, int DV, typename Tin, typename Tg, bool TF32>
-__global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams p) {
     constexpr int SK = pad4(DK), SV = pad4(DV), SC = kSC4;
     extern __shared__ float smem[];
     float *Gm = smem;                  // [C][SK]  Gamma
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     float *beta = Tm + kC * SC;        // [C]
     float *dbeta = beta + kC;          // [C]
     float *gam = dbeta + kC;           // [DK]
+    float *lastrow = gam + DK;         // [DK] diag(S_next^T dS)
 
     const int tid = threadIdx.x;
     const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -395,54 +397,82 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     const bool sv = p.scale_v != 0;
 
     // ---- loads: Gamma and the rescaled tiles, v, dO, beta
-    load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, dbeta);
+    load_rescaled_par<DK, SK, Tin, Tg, kThreadsC>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, dbeta);
     load_beta<Tin>(p, b, h, t0, nvalid, beta);
     {
         const size_t r0 = (((size_t)b * T + t0) * H + h) * DV, rs = (size_t)H * DV;
-        wg::load_tile<kC, DV, SV, kThreads>(v + r0, rs, nvalid, Vm);
-        wg::load_tile<kC, DV, SV, kThreads>(dop + r0, rs, nvalid, dO);
+        wg::load_tile<kC, DV, SV, kThreadsC>(v + r0, rs, nvalid, Vm);
+        wg::load_tile<kC, DV, SV, kThreadsC>(dop + r0, rs, nvalid, dO);
     }
     __syncthreads();
     // ---- A~, P, N, W and U from the chunk record
     {
         using R = Rec<DK, DV>;
         const float *rec = p.ws_prep + (head * N + n) * rec_floats(DK, DV);
-        wg::load_tile<kC, kC, SC, kThreads>(rec + R::A, kC, kC, Am);
-        wg::load_tile<kC, kC, SC, kThreads>(rec + R::P, kC, kC, Pm);
-        wg::load_tile<kC, kC, SC, kThreads>(rec + R::N, kC, kC, Nm);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::A, kC, kC, Am);
+        wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::P, kC, kC, Pm);
+        wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::N, kC, kC, Nm);
+        wg::load_tile<kC, DK, SK, kThreadsC>(rec + R::W, DK, kC, Wm);
         // V_new and dU of this chunk, from the two scans
-        wg::load_tile<kC, DV, SV, kThreads>(p.ws_vnew + (head * N + n) * (size_t)kC * DV, DV, kC, Vn);
-        wg::load_tile<kC, DV, SV, kThreads>(p.ws_du + (head * N + n) * (size_t)kC * DV, DV, kC, dU);
+        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_vnew + (head * N + n) * (size_t)kC * DV, DV, kC, Vn);
+        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_du + (head * N + n) * (size_t)kC * DV, DV, kC, dU);
     }
     __syncthreads();
     // ---- dO V_new^T * M (into Pm)
-    wg::gemm<kC, TF32>(
+    wg::gemm<kC, TF32, 16>(
         DV, [&](int i, int e) { return dO[i * SV + e]; }, [&](int e, int j) { return Vn[j * SV + e]; },
         [&](int i, int j, float x) { Pm[i * SC + j] = j <= i ? x : 0.f; });
     __syncthreads();
     // ---- dW = -dU S_prev ; dQ<- = dO S_prev + (dO V_new^T * M) K-> ;
-    //      dK-> = V_new dS Diag(gamma^C) + (dO V_new^T * M)^T Q<-
+    //      dK-> = V_new dS Diag(gamma^C) + (dO V_new^T * M)^T Q<- ; and diag(S_next^T dS)
+    //      for the gamma^C row.  The stored states stream through shared memory 32
+    //      rows at a time (16-byte loads into the dK<- tile, free until A~^T dW).
     {
-        auto bSp = [&](int e, int d) { return Sp[(size_t)e * DK + d]; };
-        wg::gemm<DK, TF32>(
-            DV, [&](int i, int e) { return dU[i * SV + e]; }, bSp, [&](int i, int d, float x) { Wm[i * SK + d] = -x; });
-        wg::gemm2<DK, TF32>(
-            DV, [&](int i, int e) { return dO[i * SV + e]; }, bSp, kC, [&](int i, int j) { return Pm[i * SC + j]; },
-            [&](int j, int d) { return Kr[j * SK + d]; }, [&](int i, int d, float x) { dQl[i * SK + d] = x; });
-        wg::gemm_pair<DK, TF32>(
-            DV, [&](int i, int e) { return Vn[i * SV + e]; }, [&](int e, int d) { return dS[(size_t)e * DK + d]; },
-            kC, [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int d) { return Ql[j * SK + d]; },
-            [&](int i, int d, float x1, float x2) { dKr[i * SK + d] = x1 * gam[d] + x2; });
+        constexpr int NT = wg::ntiles<DK, 16>();
+        int r0, c0;
+        wg::origin<DK, 16>(r0, c0);
+        float aW[NT][4] = {}, aQ[NT][4] = {}, aK[NT][4] = {}, aK2[NT][4] = {};
+        float *slab = dKl;
+        for (int s0 = 0; s0 < DV; s0 += kC) {
+            wg::load_tile<kC, DK, SK, kThreadsC>(Sp + (size_t)s0 * DK, DK, kC, slab);
+            __syncthreads();
+            auto bS = [&](int e, int d) { return slab[e * SK + d]; };
+            wg::tile<NT, TF32>(aW, r0, c0, kC, [&](int i, int e) { return dU[i * SV + s0 + e]; }, bS);
+            wg::tile<NT, TF32>(aQ, r0, c0, kC, [&](int i, int e) { return dO[i * SV + s0 + e]; }, bS);
+            __syncthreads();
+        }
+        float last = 0.f;                  // diag(S_next^T dS), column tid
+        for (int s0 = 0; s0 < DV; s0 += kC) {
+            wg::load_tile<kC, DK, SK, kThreadsC>(dS + (size_t)s0 * DK, DK, kC, slab);
+            float sn[kC];
+            if (tid < DK)
+#pragma unroll
+                for (int e = 0; e < kC; ++e) sn[e] = Sn[(size_t)(s0 + e) * DK + tid];
+            __syncthreads();
+            wg::tile<NT, TF32>(aK, r0, c0, kC, [&](int i, int e) { return Vn[i * SV + s0 + e]; },
+                               [&](int e, int d) { return slab[e * SK + d]; });
+            if (tid < DK)
+#pragma unroll
+                for (int e = 0; e < kC; ++e) last += sn[e] * slab[e * SK + tid];
+            __syncthreads();
+        }
+        if (tid < DK) lastrow[tid] = last;
+        wg::tile<NT, TF32>(aQ, r0, c0, kC, [&](int i, int j) { return Pm[i * SC + j]; },
+                           [&](int j, int d) { return Kr[j * SK + d]; });
+        wg::tile<NT, TF32>(aK2, r0, c0, kC, [&](int i, int j) { return Pm[j * SC + i]; },
+                           [&](int j, int d) { return Ql[j * SK + d]; });
+        wg::store<NT>(aW, r0, c0, [&](int i, int d, float x) { Wm[i * SK + d] = -x; });
+        wg::store<NT>(aQ, r0, c0, [&](int i, int d, float x) { dQl[i * SK + d] = x; });
+        wg::store_pair<NT>(aK, aK2, r0, c0, [&](int i, int d, float x1, float x2) { dKr[i * SK + d] = x1 * gam[d] + x2; });
     }
     __syncthreads();
     // ---- A~^T dW (into dKl), A~^T dU (into Vn), dA~ = dW K<-^T Diag(beta) + dU V^T Diag(beta) (or dU V^T)
     auto aAt = [&](int i, int j) { return Am[j * SC + i]; };
-    wg::gemm<DK, TF32>(
+    wg::gemm<DK, TF32, 16>(
         kC, aAt, [&](int j, int d) { return Wm[j * SK + d]; }, [&](int i, int d, float x) { dKl[i * SK + d] = x; });
-    wg::gemm<DV, TF32>(
+    wg::gemm<DV, TF32, 16>(
         kC, aAt, [&](int j, int e) { return dU[j * SV + e]; }, [&](int i, int e, float x) { Vn[i * SV + e] = x; });
-    wg::gemm_pair<kC, TF32>(
+    wg::gemm_pair<kC, TF32, 16>(
         DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int j) { return Kl[j * SK + d]; }, DV,
         [&](int i, int e) { return dU[i * SV + e]; }, [&](int e, int j) { return Vm[j * SV + e]; },
         [&](int i, int j, float xw, float xu) { dA[i * SC + j] = xw * beta[j] + xu * (sv ? beta[j] : 1.f); });
@@ -450,7 +480,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     // ---- dbeta, first two terms: diag(A~^T dW K<-^T) + diag(A~^T dU V^T) ; Tm = dA~ A~^T
     {
         const int warp = tid >> 5, lane = tid & 31;
-        for (int i = warp; i < kC; i += kThreads / 32) {
+        for (int i = warp; i < kC; i += kThreadsC / 32) {
             float acc = 0.f;
             for (int d = lane; d < DK; d += 32) acc += dKl[i * SK + d] * Kl[i * SK + d];
             if (sv)
@@ -460,34 +490,34 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
             if (lane == 0) dbeta[i] = acc;
         }
     }
-    wg::gemm<kC, TF32>(
+    wg::gemm<kC, TF32, 16>(
         kC, [&](int i, int l) { return dA[i * SC + l]; }, [&](int l, int j) { return Am[j * SC + l]; },
         [&](int i, int j, float x) { Tm[i * SC + j] = x; });
     __syncthreads();
     // ---- dX~ = -A~^T (dA~ A~^T)
-    wg::gemm<kC, TF32>(
+    wg::gemm<kC, TF32, 16>(
         kC, aAt, [&](int l, int j) { return Tm[l * SC + j]; }, [&](int i, int j, float x) { dA[i * SC + j] = -x; });
     __syncthreads();
     // ---- dbeta third term diag(dX~ N^T); E = (Diag(beta) dX~) * M_{-1} into Tm
     {
         const int warp = tid >> 5, lane = tid & 31;
-        for (int i = warp; i < kC; i += kThreads / 32) {
+        for (int i = warp; i < kC; i += kThreadsC / 32) {
             float acc = dA[i * SC + lane] * Nm[i * SC + lane];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) dbeta[i] += acc;
         }
     }
-    for (int idx = tid; idx < kC * kC; idx += kThreads) {
+    for (int idx = tid; idx < kC * kC; idx += kThreadsC) {
         const int i = idx / kC, j = idx % kC;
         Tm[i * SC + j] = j < i ? beta[i] * dA[i * SC + j] : 0.f;
     }
     __syncthreads();
     // ---- dK<- = Diag(beta) A~^T dW + E K-> ; dK-> += E^T K<-
-    wg::gemm<DK, TF32>(
+    wg::gemm<DK, TF32, 16>(
         kC, [&](int i, int j) { return Tm[i * SC + j]; }, [&](int j, int d) { return Kr[j * SK + d]; },
         [&](int i, int d, float x) { dKl[i * SK + d] = beta[i] * dKl[i * SK + d] + x; });
-    wg::gemm<DK, TF32>(
+    wg::gemm<DK, TF32, 16>(
         kC, [&](int i, int j) { return Tm[j * SC + i]; }, [&](int j, int d) { return Kl[j * SK + d]; },
         [&](int i, int d, float x) { dKr[i * SK + d] += x; });
     __syncthreads();
@@ -495,7 +525,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     Tin *gq = static_cast<Tin *>(p.grad_q);
     Tin *gk = static_cast<Tin *>(p.grad_k);
     Tin *gv = static_cast<Tin *>(p.grad_v);
-    for (int idx = tid; idx < kC * DK; idx += kThreads) {
+    for (int idx = tid; idx < kC * DK; idx += kThreadsC) {
         const int i = idx / DK, d = idx % DK;
         if (i < nvalid) {
             const size_t off = (((size_t)b * T + t0 + i) * H + h) * DK + d;
@@ -504,7 +534,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
             st(gk, off, dKl[i * SK + d] * gm + dKr[i * SK + d] / gm);
         }
     }
-    for (int idx = tid; idx < kC * DV; idx += kThreads) {
+    for (int idx = tid; idx < kC * DV; idx += kThreadsC) {
         const int i = idx / DV, e = idx % DV;
         if (i < nvalid)
             st(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, (sv ? beta[i] : 1.f) * Vn[i * SV + e]);
@@ -514,15 +544,9 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
     if (p.gate_kind != KDA_GATE_NONE) {
         // diag(S_next^T dS) for the gamma^C row, then suffix sums down each channel
         Tg *gg = static_cast<Tg *>(p.grad_g);
-        float *acc_last = Tm;          // DK floats (Tm is free now)
-        for (int d = tid; d < DK; d += kThreads) {
-            float acc = 0.f;
-            for (int e = 0; e < DV; ++e) acc += Sn[(size_t)e * DK + d] * dS[(size_t)e * DK + d];
-            acc_last[d] = acc;
-        }
-        __syncthreads();
+        const float *acc_last = lastrow;   // diag(S_next^T dS), from the state pass above
         if (p.gate_kind == KDA_GATE_CHANNEL) {
-            for (int d = tid; d < DK; d += kThreads) {
+            for (int d = tid; d < DK; d += kThreadsC) {
                 float run = acc_last[d];
                 for (int i = kC - 1; i >= 0; --i) {
                     run += dQl[i * SK + d] * Ql[i * SK + d] + dKl[i * SK + d] * Kl[i * SK + d] -
@@ -535,7 +559,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_grad_kernel(const BwdParams 
             const int warp = tid >> 5, lane = tid & 31;
             float *rowsum = dbeta;     // reuse: C floats (dbeta was already written out)
             __syncthreads();
-            for (int i = warp; i < kC; i += kThreads / 32) {
+            for (int i = warp; i < kC; i += kThreadsC / 32) {
                 float acc = 0.f;
                 for (int d = lane; d < DK; d += 32)
                     acc += dQl[i * SK + d] * Ql[i * SK + d] + dKl[i * SK + d] * Kl[i * SK + d] -
@@ -587,7 +611,7 @@ cudaError_t launch_all(const BwdParams &p, cudaStream_t s) {
     kda_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sp, s>>>(p);
     kda_bwd_states_kernel<DK, DV, kTf32><<<gscan, kThreads, sa, s>>>(p);
     kda_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sb, s>>>(p);
-    kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sc, s>>>(p);
+    kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreadsC, sc, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -1,8 +1,8 @@
 // Warp-tiled products for the chunk-parallel backward kernels.
 //
-// A CTA of 8 warps computes a 32 x N block (N in {32, 64, 128}) of a product
-// sum_k A(i, k) B(k, n): warp w owns rows 16 (w & 1) .. +16 and columns
-// (w >> 1) N / 4 .. + N / 4, i.e. N / 32 tiles of 16 x 8.  Operands come
+// A CTA of 8 (or 16) warps computes a 32 x N block (N in {32, 64, 128}) of a
+// product sum_k A(i, k) B(k, n): warp w owns rows 16 (w & 1) .. +16 and a
+// column range of N / 4 (or N / 8), i.e. tiles of 16 x 8.  Operands come
 // through accessor functors (shared or global memory, any layout or
 // transform).  TF32 = true issues warp-level m16n8k8 tf32 tensor-core MMAs
 // with float32 accumulation (operands rounded to tf32); TF32 = false computes
@@ -60,32 +60,53 @@ __device__ __forceinline__ void store(const float (&acc)[NT][4], int row0, int c
         for (int q = 0; q < 4; ++q) epi(row0 + g + 8 * (q >> 1), col0 + 8 * nt + 2 * t + (q & 1), acc[nt][q]);
 }
 
-// This warp's tile origin in a 32 x N block.
-template <int N>
-__device__ __forceinline__ void origin(int &row0, int &col0) {
+// Tiles of a 32 x N block over NW warps (8 or 16): warp w owns rows
+// 16 (w & 1) .. +16 and columns (w >> 1) N / (NW / 2) .. + N / (NW / 2); when
+// that is narrower than one 8-column tile (N = 32 with 16 warps) the warps
+// past the tiles sit out.
+template <int N, int NW>
+__host__ __device__ constexpr int ntiles() { return N / (NW / 2) >= 8 ? N / (NW / 2) / 8 : 1; }
+
+// Calls epi(row, col, a1, a2) for two accumulators of the same tile shape.
+template <int NT, typename FE>
+__device__ __forceinline__ void store_pair(const float (&a1)[NT][4], const float (&a2)[NT][4], int row0, int col0,
+                                           const FE &epi) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            epi(row0 + g + 8 * (q >> 1), col0 + 8 * nt + 2 * t + (q & 1), a1[nt][q], a2[nt][q]);
+}
+
+// This warp's tile origin in a 32 x N block; false when the warp has no tile.
+template <int N, int NW = 8>
+__device__ __forceinline__ bool origin(int &row0, int &col0) {
     const int w = threadIdx.x >> 5;
+    constexpr int W = N / (NW / 2) >= 8 ? N / (NW / 2) : 8;     // columns per warp pair
     row0 = 16 * (w & 1);
-    col0 = (w >> 1) * (N / 4);
+    col0 = (w >> 1) * W;
+    return col0 < N;
 }
 
 // out(i, n) = epi(i, n, sum_k A(i, k) B(k, n)) over a 32 x N block.
-template <int N, bool TF32, typename FA, typename FB, typename FE>
+template <int N, bool TF32, int NW = 8, typename FA, typename FB, typename FE>
 __device__ __forceinline__ void gemm(int K, const FA &A, const FB &B, const FE &epi) {
-    constexpr int NT = N / 32;
+    constexpr int NT = ntiles<N, NW>();
     int r0, c0;
-    origin<N>(r0, c0);
+    if (!origin<N, NW>(r0, c0)) return;
     float acc[NT][4] = {};
     tile<NT, TF32>(acc, r0, c0, K, A, B);
     store<NT>(acc, r0, c0, epi);
 }
 
 // out(i, n) = epi(i, n, sum_k A1 B1 + sum_k A2 B2).
-template <int N, bool TF32, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
+template <int N, bool TF32, int NW = 8, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
 __device__ __forceinline__ void gemm2(int K1, const FA1 &A1, const FB1 &B1, int K2, const FA2 &A2, const FB2 &B2,
                                       const FE &epi) {
-    constexpr int NT = N / 32;
+    constexpr int NT = ntiles<N, NW>();
     int r0, c0;
-    origin<N>(r0, c0);
+    if (!origin<N, NW>(r0, c0)) return;
     float acc[NT][4] = {};
     tile<NT, TF32>(acc, r0, c0, K1, A1, B1);
     tile<NT, TF32>(acc, r0, c0, K2, A2, B2);
@@ -93,12 +114,12 @@ __device__ __forceinline__ void gemm2(int K1, const FA1 &A1, const FB1 &B1, int 
 }
 
 // out(i, n) = epi(i, n, sum_k A1 B1, sum_k A2 B2): two products kept apart.
-template <int N, bool TF32, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
+template <int N, bool TF32, int NW = 8, typename FA1, typename FB1, typename FA2, typename FB2, typename FE>
 __device__ __forceinline__ void gemm_pair(int K1, const FA1 &A1, const FB1 &B1, int K2, const FA2 &A2,
                                           const FB2 &B2, const FE &epi) {
-    constexpr int NT = N / 32;
+    constexpr int NT = ntiles<N, NW>();
     int r0, c0;
-    origin<N>(r0, c0);
+    if (!origin<N, NW>(r0, c0)) return;
     float a1[NT][4] = {}, a2[NT][4] = {};
     tile<NT, TF32>(a1, r0, c0, K1, A1, B1);
     tile<NT, TF32>(a2, r0, c0, K2, A2, B2);
