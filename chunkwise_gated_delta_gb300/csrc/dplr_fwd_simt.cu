@@ -14,6 +14,11 @@
 //   O = Q<- S^T + (Q<- K->^T * M) V + (Q<- A->^T * M) X;
 //   S <- (S + V^T K-> + X^T A->) Diag(gamma^C).
 //
+// Two kernels: a chunk-parallel prep kernel writes, per chunk, everything that
+// does not depend on the state (W, Q<- - P_a W, K-> and A-> times gamma^C, C
+// and the chunk-local output P_k V + P_a C) into the workspace; the scan then
+// needs three products per chunk.
+//
 // Also the per-token transition norms of page "How to make GDN2 more stable":
 // eq. (4) for I - b a^T, and the largest singular value of the full factor
 // Diag(alpha)(I - b a^T), for which the page has no closed form, by
@@ -41,12 +46,30 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // Row strides = 4 (mod 32) for the fragment reads of the warp-tiled products.
 __host__ __device__ constexpr int pad4(int n) { return n + 4; }
 
-// Products run as warp-tiled 32 x N blocks (warp_gemm.cuh): tf32 tensor-core
-// MMAs for bf16 inputs (TF32), exact float32 for float32 inputs.
-template <int DK, typename Tin, typename Tg, bool TF32>
+// ------------------------------------------------------------------ chunk records
+// Everything of a chunk that does not depend on the state (float32), written
+// once by the prep kernel: W = E B<-, Qt = Q<- - P_a W, K~ = K-> Diag(gamma^C),
+// A~ = A-> Diag(gamma^C), C = -E (B<- K->^T * M_{-1}) V, the chunk-local output
+// O_loc = P_k V + P_a C, and gamma^C; so that per chunk
+//   X = C - W S^T,  O = Qt S^T + O_loc,  S <- S Diag(gamma^C) + V^T K~ + X^T A~.
+__host__ __device__ constexpr size_t dplr_rec_floats(int dk, int dv) {
+    return (size_t)4 * kC * dk + (size_t)2 * kC * dv + dk;
+}
+template <int DK, int DV>
+struct DRec {
+    static constexpr int W = 0, QT = kC * DK, KG = 2 * kC * DK, AG = 3 * kC * DK, CC = 4 * kC * DK,
+                         OL = CC + kC * DV, GC = OL + kC * DV;
+    static_assert(dplr_rec_floats(DK, DV) == (size_t)GC + DK && dplr_rec_floats(DK, DV) % 4 == 0, "record");
+};
+
+// One CTA per (chunk, head, batch).  Products run as warp-tiled 32 x N blocks
+// (warp_gemm.cuh): tf32 tensor-core MMAs for bf16 inputs (TF32), exact float32
+// for float32 inputs.
+template <int DK, int DV, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads)
-dplr_fwd_simt_kernel(const DplrParams p) {
-    constexpr int SK = pad4(DK), SC = pad4(kC), SV = pad4(kDVS);
+dplr_fwd_prep_kernel(const DplrParams p) {
+    constexpr int SK = pad4(DK), SC = pad4(kC), SV = pad4(DV);
+    using R = DRec<DK, DV>;
     extern __shared__ float smem[];
     float4 *rows = reinterpret_cast<float4 *>(smem);   // [C] eq. (4) data per row (clip)
     float *Gm = smem + 4 * kC;        // [C][SK]  raw gate, then Gamma
@@ -54,96 +77,151 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     float *Kr = Ql + kC * SK;         // [C][SK]
     float *Ar = Kr + kC * SK;         // [C][SK]
     float *Bl = Ar + kC * SK;         // [C][SK]
-    float *Wm = Bl + kC * SK;         // [C][SK]
-    float *Lab = Wm + kC * SK;        // [C][SC]  B<- A->^T * M_{-1}
+    float *Vm = Bl + kC * SK;         // [C][SV]
+    float *Lab = Vm + kC * SV;        // [C][SC]  B<- A->^T * M_{-1}
     float *Lbk = Lab + kC * SC;       // [C][SC]  B<- K->^T * M_{-1}
     float *Pk = Lbk + kC * SC;        // [C][SC]  Q<- K->^T * M
     float *Pa = Pk + kC * SC;         // [C][SC]  Q<- A->^T * M
     float *Em = Pa + kC * SC;         // [C][SC]  E
-    float *Ts = Em + kC * SC;         // [C][SC]  scratch of the inverse
-    float *Vm = Ts + kC * SC;         // [C][SV]  v slice
-    float *Tm = Vm + kC * SV;         // [C][SV]  (B<- K->^T * M_{-1}) V
-    float *Xm = Tm + kC * SV;         // [C][SV]  X
-    float *Sm = Xm + kC * SV;         // [DVS][SK] state slice
-    float *gC = Sm + kDVS * SK;       // [DK]
-    float *gsc = gC + DK;             // [C]
+    float *Ts = Em + kC * SC;         // [C][SC]  scratch of the inverse, then P_a E
+    float *M1 = Ts + kC * SC;         // [C][SC]  E (B<- K->^T * M_{-1})
+    float *gam = M1 + kC * SC;        // [DK]
+    float *gsc = gam + DK;            // [C]
+
+    const int tid = threadIdx.x;
+    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
+    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    float *rec = p.ws_prep + (((size_t)b * H + h) * N + n) * dplr_rec_floats(DK, DV);
+
+    if (p.clip) {
+        dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
+        __syncthreads();
+    }
+    wg::load_tile<kC, DV, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * DV, (size_t)H * DV, nvalid, Vm);
+    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
+    __syncthreads();
+    {
+        auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
+        auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
+        auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
+        auto aQl = [&](int i, int d) { return Ql[i * SK + d]; };
+        wg::gemm_pair<kC, TF32>(DK, aBl, bAr, DK, aBl, bKr, [&](int i, int j, float x, float y) {
+            Lab[i * SC + j] = j < i ? x : 0.f;
+            Lbk[i * SC + j] = j < i ? y : 0.f;
+        });
+        wg::gemm_pair<kC, TF32>(DK, aQl, bKr, DK, aQl, bAr, [&](int i, int j, float x, float y) {
+            Pk[i * SC + j] = j <= i ? x : 0.f;
+            Pa[i * SC + j] = j <= i ? y : 0.f;
+        });
+    }
+    for (int idx = tid; idx < kC * DK; idx += kThreads) {
+        const int i = idx / DK, d = idx % DK;
+        rec[R::KG + idx] = Kr[i * SK + d] * gam[d];
+        rec[R::AG + idx] = Ar[i * SK + d] * gam[d];
+    }
+    for (int d = tid; d < DK; d += kThreads) rec[R::GC + d] = gam[d];
+    __syncthreads();
+    dplr::block_inverse32<SC>(Lab, Em, Ts);
+    // M1 = E Lbk ; P_a E (into Ts)
+    wg::gemm_pair<kC, TF32>(
+        kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int l) { return Lbk[j * SC + l]; }, kC,
+        [&](int i, int j) { return Pa[i * SC + j]; }, [&](int j, int l) { return Em[j * SC + l]; },
+        [&](int i, int l, float x, float y) {
+            M1[i * SC + l] = x;
+            Ts[i * SC + l] = y;
+        });
+    __syncthreads();
+    // P_k - (P_a E) Lbk (into Pk)
+    wg::gemm<kC, TF32>(
+        kC, [&](int i, int j) { return Ts[i * SC + j]; }, [&](int j, int l) { return Lbk[j * SC + l]; },
+        [&](int i, int l, float x) { Pk[i * SC + l] -= x; });
+    // W = E B<- ; Qt = Q<- - (P_a E) B<-
+    wg::gemm_pair<DK, TF32>(
+        kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; }, kC,
+        [&](int i, int j) { return Ts[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
+        [&](int i, int d, float w, float pw) {
+            rec[R::W + i * DK + d] = w;
+            rec[R::QT + i * DK + d] = Ql[i * SK + d] - pw;
+        });
+    __syncthreads();
+    // C = -M1 V ; O_loc = (P_k - P_a E Lbk) V
+    wg::gemm_pair<DV, TF32>(
+        kC, [&](int i, int j) { return M1[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; }, kC,
+        [&](int i, int j) { return Pk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
+        [&](int i, int e, float c, float ol) {
+            rec[R::CC + i * DV + e] = -c;
+            rec[R::OL + i * DV + e] = ol;
+        });
+}
+
+template <int DK, int DV>
+constexpr size_t prep_smem_bytes() {
+    return sizeof(float) * (size_t)(4 * kC + 5 * kC * pad4(DK) + kC * pad4(DV) + 7 * kC * pad4(kC) + DK + kC);
+}
+
+// One CTA per (32-wide value slice, head, batch): the serial scan over the
+// chunk records.
+template <int DK, int DV, typename Tin, bool TF32>
+__global__ void __launch_bounds__(kThreads)
+dplr_fwd_simt_kernel(const DplrParams p) {
+    constexpr int SK = pad4(DK), SV = pad4(kDVS);
+    using R = DRec<DK, DV>;
+    extern __shared__ float smem[];
+    float *Wm = smem;                 // [C][SK]
+    float *QT = Wm + kC * SK;         // [C][SK]
+    float *KG = QT + kC * SK;         // [C][SK]
+    float *AG = KG + kC * SK;         // [C][SK]
+    float *Sm = AG + kC * SK;         // [DVS][SK] state slice
+    float *Cs = Sm + kDVS * SK;       // [C][SV]  C slice
+    float *Os = Cs + kC * SV;         // [C][SV]  O_loc slice
+    float *Vm = Os + kC * SV;         // [C][SV]  v slice
+    float *Xm = Vm + kC * SV;         // [C][SV]  X
+    float *gC = Xm + kC * SV;         // [DK]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS;
     const int h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, dv = p.dv;
+    const int T = p.T, H = p.H, dv = p.dv, N = (T + kC - 1) / kC;
     const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
+    const float *recs = p.ws_prep + ((size_t)b * H + h) * N * dplr_rec_floats(DK, DV);
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         Sm[e * SK + d] = p.h0 ? p.h0[(((size_t)b * H + h) * dv + e0 + e) * DK + d] : 0.f;
     }
-
-    for (int t0 = 0; t0 < T; t0 += kC) {
-        const int nvalid = min(kC, T - t0);
+    for (int n = 0; n < N; ++n) {
+        const int t0 = n * kC, nvalid = min(kC, T - t0);
+        const float *rec = recs + (size_t)n * dplr_rec_floats(DK, DV);
         __syncthreads();
-        // ---- Gamma (from the clipped gate when asked) and the rescaled tiles; the v slice
-        if (p.clip) {
-            dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
-            __syncthreads();
-        }
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::QT, DK, kC, QT);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KG, DK, kC, KG);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::AG, DK, kC, AG);
+        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, kC, Cs);
+        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::OL + e0, DV, kC, Os);
         wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
                                               Vm);
-        dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gC, gsc);
+        for (int d = tid; d < DK; d += kThreads) gC[d] = rec[R::GC + d];
         __syncthreads();
-        // ---- the four chunk Gram matrices
+        // X = C - W S^T ; O = Qt S^T + O_loc
         {
-            auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
-            auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
-            auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
-            auto aQl = [&](int i, int d) { return Ql[i * SK + d]; };
-            wg::gemm_pair<kC, TF32>(DK, aBl, bAr, DK, aBl, bKr, [&](int i, int j, float x, float y) {
-                Lab[i * SC + j] = j < i ? x : 0.f;
-                Lbk[i * SC + j] = j < i ? y : 0.f;
-            });
-            wg::gemm_pair<kC, TF32>(DK, aQl, bKr, DK, aQl, bAr, [&](int i, int j, float x, float y) {
-                Pk[i * SC + j] = j <= i ? x : 0.f;
-                Pa[i * SC + j] = j <= i ? y : 0.f;
-            });
+            auto bS = [&](int d, int e) { return Sm[e * SK + d]; };
+            wg::gemm_pair<kDVS, TF32>(
+                DK, [&](int i, int d) { return Wm[i * SK + d]; }, bS, DK, [&](int i, int d) { return QT[i * SK + d]; },
+                bS, [&](int i, int e, float ws, float qs) {
+                    Xm[i * SV + e] = Cs[i * SV + e] - ws;
+                    if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = from_f<Tin>(Os[i * SV + e] + qs);
+                });
         }
         __syncthreads();
-        // ---- E = (I + Lab)^{-1} ; (B<- K->^T * M_{-1}) V ; W = E B<-
-        dplr::block_inverse32<SC>(Lab, Em, Ts);
-        wg::gemm<kDVS, TF32>(
-            kC, [&](int i, int j) { return Lbk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
-            [&](int i, int e, float x) { Tm[i * SV + e] = x; });
-        wg::gemm<DK, TF32>(
-            kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
-            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
-        __syncthreads();
-        // ---- X = C - W S^T with C = -E (B<- K->^T * M_{-1}) V
-        wg::gemm2<kDVS, TF32>(
-            kC, [&](int i, int j) { return -Em[i * SC + j]; }, [&](int j, int e) { return Tm[j * SV + e]; }, DK,
-            [&](int i, int d) { return -Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
-            [&](int i, int e, float x) { Xm[i * SV + e] = x; });
-        __syncthreads();
-        // ---- O = Q<- S^T + (Q<- K->^T * M) V + (Q<- A->^T * M) X
-        {
-            int r0, c0;
-            wg::origin<kDVS>(r0, c0);
-            float acc[kDVS / 32][4] = {};
-            wg::tile<kDVS / 32, TF32>(acc, r0, c0, DK, [&](int i, int d) { return Ql[i * SK + d]; },
-                                      [&](int d, int e) { return Sm[e * SK + d]; });
-            wg::tile<kDVS / 32, TF32>(acc, r0, c0, kC, [&](int i, int j) { return Pk[i * SC + j]; },
-                                      [&](int j, int e) { return Vm[j * SV + e]; });
-            wg::tile<kDVS / 32, TF32>(acc, r0, c0, kC, [&](int i, int j) { return Pa[i * SC + j]; },
-                                      [&](int j, int e) { return Xm[j * SV + e]; });
-            wg::store<kDVS / 32>(acc, r0, c0, [&](int i, int e, float x) {
-                if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = from_f<Tin>(x);
-            });
-        }
-        __syncthreads();
-        // ---- S <- (S + V^T K-> + X^T A->) Diag(gamma^C)
+        // S <- S Diag(gamma^C) + V^T K~ + X^T A~
         wg::gemm2<DK, TF32>(
-            kC, [&](int e, int c) { return Vm[c * SV + e]; }, [&](int c, int d) { return Kr[c * SK + d]; }, kC,
-            [&](int e, int c) { return Xm[c * SV + e]; }, [&](int c, int d) { return Ar[c * SK + d]; },
-            [&](int e, int d, float x) { Sm[e * SK + d] = (Sm[e * SK + d] + x) * gC[d]; });
+            kC, [&](int e, int c) { return Vm[c * SV + e]; }, [&](int c, int d) { return KG[c * SK + d]; }, kC,
+            [&](int e, int c) { return Xm[c * SV + e]; }, [&](int c, int d) { return AG[c * SK + d]; },
+            [&](int e, int d, float x) { Sm[e * SK + d] = Sm[e * SK + d] * gC[d] + x; });
     }
     __syncthreads();
     if (p.ht) {
@@ -156,21 +234,39 @@ dplr_fwd_simt_kernel(const DplrParams p) {
 
 template <int DK>
 constexpr size_t dplr_smem_bytes() {
-    return sizeof(float) * (size_t)(4 * kC + 6 * kC * pad4(DK) + 6 * kC * pad4(kC) + 3 * kC * pad4(kDVS) +
-                                    kDVS * pad4(DK) + DK + kC);
+    return sizeof(float) * (size_t)(4 * kC * pad4(DK) + kDVS * pad4(DK) + 4 * kC * pad4(kDVS) + DK);
+}
+
+template <int DK, int DV, typename Tin, typename Tg>
+cudaError_t launch_dkv(const DplrParams &p, cudaStream_t s) {
+    constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
+    const int N = (p.T + kC - 1) / kC;
+    const size_t sp = prep_smem_bytes<DK, DV>(), sm = dplr_smem_bytes<DK>();
+    static_assert(prep_smem_bytes<128, 256>() <= 227 * 1024, "shared memory");
+    cudaError_t e = cudaFuncSetAttribute(dplr_fwd_prep_kernel<DK, DV, Tin, Tg, kTf32>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dplr_fwd_simt_kernel<DK, DV, Tin, kTf32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm);
+    if (e != cudaSuccess) return e;
+    dplr_fwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<dim3(N, p.H, p.B), kThreads, sp, s>>>(p);
+    dplr_fwd_simt_kernel<DK, DV, Tin, kTf32><<<dim3(p.dv / kDVS, p.H, p.B), kThreads, sm, s>>>(p);
+    return cudaGetLastError();
 }
 
 template <int DK, typename Tin, typename Tg>
 cudaError_t launch_dk(const DplrParams &p, cudaStream_t s) {
-    constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
-    const size_t smem = dplr_smem_bytes<DK>();
-    static_assert(dplr_smem_bytes<128>() <= 227 * 1024, "shared memory");
-    cudaError_t e = cudaFuncSetAttribute(dplr_fwd_simt_kernel<DK, Tin, Tg, kTf32>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid(p.dv / kDVS, p.H, p.B);
-    dplr_fwd_simt_kernel<DK, Tin, Tg, kTf32><<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    switch (p.dv) {
+    case 32: return launch_dkv<DK, 32, Tin, Tg>(p, s);
+    case 64: return launch_dkv<DK, 64, Tin, Tg>(p, s);
+    case 96: return launch_dkv<DK, 96, Tin, Tg>(p, s);
+    case 128: return launch_dkv<DK, 128, Tin, Tg>(p, s);
+    case 160: return launch_dkv<DK, 160, Tin, Tg>(p, s);
+    case 192: return launch_dkv<DK, 192, Tin, Tg>(p, s);
+    case 224: return launch_dkv<DK, 224, Tin, Tg>(p, s);
+    case 256: return launch_dkv<DK, 256, Tin, Tg>(p, s);
+    }
+    return cudaErrorNotSupported;
 }
 
 template <typename Tin, typename Tg>
@@ -298,6 +394,10 @@ dplr_factor_norm_kernel(const DplrParams p, float *rho, float *nrm, float *maxes
 }
 
 }  // namespace
+
+size_t dplr_fwd_record_bytes(int B, int T, int H, int dk, int dv) {
+    return sizeof(float) * (size_t)B * H * ((T + kC - 1) / kC) * dplr_rec_floats(dk, dv);
+}
 
 cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s) {
     if (in_bf16)

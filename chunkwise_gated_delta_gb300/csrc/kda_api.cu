@@ -259,15 +259,17 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
 
 size_t dplr_chunk_fwd_workspace(const dplr_fwd_args *args) {
     if (validate_dplr(args) != KDA_OK) return 0;
-    return kStatusBytes;
+    return kStatusBytes + kda::dplr_fwd_record_bytes(args->B, args->T, args->H, args->dk, args->dv);
 }
 
 kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream) {
     kda_status st = validate_dplr(args);
     if (st != KDA_OK) return st;
-    if (!args->workspace || args->workspace_bytes < kStatusBytes) return KDA_ERR_WORKSPACE;
-    return from_cuda(kda::launch_dplr_fwd_simt(dplr_params(args), args->dtype == KDA_BF16,
-                                               args->g_dtype == KDA_BF16,
+    const size_t need = kStatusBytes + kda::dplr_fwd_record_bytes(args->B, args->T, args->H, args->dk, args->dv);
+    if (!args->workspace || args->workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    kda::DplrParams p = dplr_params(args);
+    p.ws_prep = reinterpret_cast<float *>(static_cast<unsigned char *>(args->workspace) + kStatusBytes);
+    return from_cuda(kda::launch_dplr_fwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -39,6 +39,7 @@ struct DplrParams {
     float *grad_h0;
     float *ws_S;            // [B, H, N + 1, dv, dk] states before each chunk, then the final state
     float *ws_dS;           // [B, H, N, dv, dk] gradients of the state after each chunk
+    float *ws_prep;         // forward: [B, H, N] chunk records (state-independent operands)
 };
 
 // Device-side copy of the validated backward arguments.
@@ -70,7 +71,9 @@ cudaError_t launch_fwd_simt_f32(const FwdParams &p, int g_is_bf16, cudaStream_t 
 // bf16 tcgen05 path; returns cudaErrorNotSupported for shapes it does not take.
 cudaError_t launch_fwd_tc_bf16(const FwdParams &p, int g_is_bf16, cudaStream_t s);
 
-// float32 CUDA-core DPLR chunk forward (inputs float32 or bf16).
+// float32 CUDA-core DPLR chunk forward (inputs float32 or bf16) and the bytes
+// of chunk records it keeps in the workspace.
+size_t dplr_fwd_record_bytes(int B, int T, int H, int dk, int dv);
 cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s);
 
 // float32 CUDA-core DPLR backward (inputs float32 or bf16) and its workspace bytes.

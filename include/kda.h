@@ -232,13 +232,18 @@ typedef struct {
     size_t workspace_bytes;
 } dplr_fwd_args;
 
-/* Bytes of workspace dplr_chunk_fwd needs for these arguments (0 on bad args). */
+/*
+ * Bytes of workspace dplr_chunk_fwd needs for these arguments (0 on bad args):
+ * 256 for the status word plus one float32 record of state-independent chunk
+ * operands per 32-token chunk, ceil(T/32) B H (4 32 dk + 2 32 dv + dk) 4 bytes.
+ */
 size_t dplr_chunk_fwd_workspace(const dplr_fwd_args *args);
 
 /*
  * Chunkwise forward of the general gated DPLR recurrence.  Writes o, and ht
- * when non-NULL.  float32 CUDA-core kernel; bfloat16 inputs are widened to
- * float32 on load and o is rounded to bfloat16 on store.
+ * when non-NULL.  Two kernels (chunk-parallel operands, then the state scan);
+ * float32 arithmetic with tf32 tensor-core products for bfloat16 inputs,
+ * exact float32 products for float32 inputs; o is rounded to the input dtype.
  */
 kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream);
 
