@@ -23,8 +23,10 @@
 // to g where g < -log rho, and to -log rho elsewhere, from where it reaches a
 // and b through the derivative of eq. (4).
 //
-// Three kernels, as for the KDA backward: the forward state pass and the
-// reverse dS scan per (32-wide value slice, head, batch), then one CTA per
+// Four kernels, as for the KDA backward: a chunk-parallel prep kernel writes the
+// state-independent operands of every chunk (W, K-> and A-> times gamma^C,
+// Q<-, C, E, N_bk, P_k, P_a) once; the forward state scan and the reverse dS
+// scan per (32-wide value slice, head, batch) keep X and dC; then one CTA per
 // (chunk, head, batch) for every other gradient.
 #include <cuda_bf16.h>
 
@@ -63,28 +65,117 @@ __device__ void inverse16(const float *Nm, float *Em) {
     __syncthreads();
 }
 
-// ------------------------------------------------------------------ kernel A
-// Products run as warp-tiled blocks (warp_gemm.cuh): tf32 tensor-core MMAs for
-// bf16 inputs (TF32), exact float32 for float32 inputs.
-template <int DK, typename Tin, typename Tg, bool TF32>
-__global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
+// ------------------------------------------------------------------ chunk records
+// Everything of a chunk that does not depend on the state (float32), written
+// once by the prep kernel: W = E B<-, K~ = K-> Diag(gamma^C), A~ = A-> Diag(gamma^C),
+// Q<-, C = -E (B<- K->^T * M_{-1}) V, E, N_bk = B<- K->^T * M_{-1}, P_k, P_a and gamma^C.
+__host__ __device__ constexpr size_t bwd_rec_floats(int dk, int dv) {
+    return (size_t)4 * kC * dk + (size_t)kC * dv + (size_t)4 * kC * kC + dk;
+}
+template <int DK, int DV>
+struct BRec {
+    static constexpr int W = 0, KG = kC * DK, AG = 2 * kC * DK, QL = 3 * kC * DK, CC = 4 * kC * DK,
+                         E = CC + kC * DV, NK = E + kC * kC, PK = NK + kC * kC, PA = PK + kC * kC,
+                         GC = PA + kC * kC;
+    static_assert(bwd_rec_floats(DK, DV) == (size_t)GC + DK && bwd_rec_floats(DK, DV) % 4 == 0, "record");
+};
+
+// ------------------------------------------------------------------ prep kernel
+// One CTA per (chunk, head, batch).  Products run as warp-tiled blocks
+// (warp_gemm.cuh): tf32 tensor-core MMAs for bf16 inputs (TF32), exact float32
+// for float32 inputs.
+template <int DK, int DV, typename Tin, typename Tg, bool TF32>
+__global__ void __launch_bounds__(kThreads) dplr_bwd_prep_kernel(const DplrParams p) {
+    constexpr int SK = pad4(DK), SV = pad4(DV), SC = kSC4;
+    using R = BRec<DK, DV>;
     extern __shared__ float smem[];
     float4 *rows = reinterpret_cast<float4 *>(smem);      // [C]
-    float *Gm = smem + 4 * kC;           // [C][SK]  gate scratch
-    float *Kr = Gm + kC * SK;
+    float *Gm = smem + 4 * kC;           // [C][SK]  raw gate, then Gamma
+    float *Ql = Gm + kC * SK;
+    float *Kr = Ql + kC * SK;
     float *Ar = Kr + kC * SK;
     float *Bl = Ar + kC * SK;
-    float *Wm = Bl + kC * SK;
-    float *Sm = Wm + kC * SK;            // [DVS][SK]
-    float *Nm = Sm + kDVS * SK;          // [C][SC]  B<- A->^T * M_{-1}
+    float *Vm = Bl + kC * SK;            // [C][SV]
+    float *T1 = Vm + kC * SV;            // [C][SV]  N_bk V
+    float *Nm = T1 + kC * SV;            // [C][SC]
     float *Em = Nm + kC * SC;
-    float *Nk = Em + kC * SC;            // B<- K->^T * M_{-1}
-    float *Vm = Nk + kC * SC;            // [C][SV]
-    float *T1 = Vm + kC * SV;
-    float *Xm = T1 + kC * SV;
-    float *gam = Xm + kC * SV;           // [DK]
+    float *Nk = Em + kC * SC;
+    float *gam = Nk + kC * SC;           // [DK]
     float *gsc = gam + DK;               // [C]
+
+    const int tid = threadIdx.x;
+    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
+    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    float *rec = p.ws_prep + (((size_t)b * H + h) * N + n) * bwd_rec_floats(DK, DV);
+
+    if (p.clip) {
+        dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
+        __syncthreads();
+    }
+    wg::load_tile<kC, DV, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * DV, (size_t)H * DV, nvalid, Vm);
+    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
+    __syncthreads();
+    {
+        auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
+        auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
+        auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
+        auto aQl = [&](int i, int d) { return Ql[i * SK + d]; };
+        wg::gemm16_pair<kC, TF32>(DK, aBl, bAr, DK, aBl, bKr, [&](int i, int j, float x, float y) {
+            Nm[i * SC + j] = j < i ? x : 0.f;
+            const float nk = j < i ? y : 0.f;
+            Nk[i * SC + j] = nk;
+            rec[R::NK + i * kC + j] = nk;
+        });
+        wg::gemm16_pair<kC, TF32>(DK, aQl, bKr, DK, aQl, bAr, [&](int i, int j, float x, float y) {
+            rec[R::PK + i * kC + j] = j <= i ? x : 0.f;
+            rec[R::PA + i * kC + j] = j <= i ? y : 0.f;
+        });
+    }
+    for (int idx = tid; idx < kC * DK; idx += kThreads) {
+        const int i = idx / DK, d = idx % DK;
+        rec[R::KG + idx] = Kr[i * SK + d] * gam[d];
+        rec[R::AG + idx] = Ar[i * SK + d] * gam[d];
+        rec[R::QL + idx] = Ql[i * SK + d];
+    }
+    for (int d = tid; d < DK; d += kThreads) rec[R::GC + d] = gam[d];
+    __syncthreads();
+    inverse16<SC>(Nm, Em);
+    for (int idx = tid; idx < kC * kC; idx += kThreads) rec[R::E + idx] = Em[(idx / kC) * SC + idx % kC];
+    wg::gemm16<DK, TF32>(
+        kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
+        [&](int i, int d, float x) { rec[R::W + i * DK + d] = x; });
+    wg::gemm16<DV, TF32>(
+        kC, [&](int i, int j) { return Nk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
+        [&](int i, int e, float x) { T1[i * SV + e] = x; });
+    __syncthreads();
+    wg::gemm16<DV, TF32>(
+        kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int e) { return T1[j * SV + e]; },
+        [&](int i, int e, float x) { rec[R::CC + i * DV + e] = -x; });
+}
+
+template <int DK, int DV>
+constexpr size_t prep_smem_bytes() {
+    return sizeof(float) * ((size_t)4 * kC + 5 * kC * pad4(DK) + 2 * kC * pad4(DV) + 3 * kC * kSC4 + DK + kC);
+}
+
+// ------------------------------------------------------------------ kernel A
+// The forward state scan from the records: X = C - W S^T (kept for the
+// gradient kernel), S <- S Diag(gamma^C) + V^T K~ + X^T A~.
+template <int DK, int DV, typename Tin, bool TF32>
+__global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrParams p) {
+    constexpr int SK = pad4(DK), SV = pad4(kDVS);
+    using R = BRec<DK, DV>;
+    extern __shared__ float smem[];
+    float *Wm = smem;                    // [C][SK]
+    float *KG = Wm + kC * SK;
+    float *AG = KG + kC * SK;
+    float *Sm = AG + kC * SK;            // [DVS][SK]
+    float *Cs = Sm + kDVS * SK;          // [C][SV]
+    float *Vm = Cs + kC * SV;
+    float *Xm = Vm + kC * SV;
+    float *gam = Xm + kC * SV;           // [DK]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -92,6 +183,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
     const Tin *v = static_cast<const Tin *>(p.v);
     const size_t head = (size_t)b * H + h;
     float *Sws = p.ws_S + head * (size_t)(N + 1) * dv * DK;
+    const float *recs = p.ws_prep + head * N * bwd_rec_floats(DK, DV);
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
@@ -99,49 +191,33 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
     }
     for (int n = 0; n < N; ++n) {
         const int t0 = n * kC, nvalid = min(kC, T - t0);
+        const float *rec = recs + (size_t)n * bwd_rec_floats(DK, DV);
         __syncthreads();
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
         }
-        if (p.clip) {
-            dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
-            __syncthreads();
-        }
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KG, DK, kC, KG);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::AG, DK, kC, AG);
+        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, kC, Cs);
         wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
                                               Vm);
-        dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, nullptr, Kr, Ar, Bl, gam, gsc);
+        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
         __syncthreads();
-        {
-            auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
-            wg::gemm16_pair<kC, TF32>(
-                DK, aBl, [&](int d, int j) { return Ar[j * SK + d]; }, DK, aBl,
-                [&](int d, int j) { return Kr[j * SK + d]; }, [&](int i, int j, float x, float y) {
-                    Nm[i * SC + j] = j < i ? x : 0.f;
-                    Nk[i * SC + j] = j < i ? y : 0.f;
-                });
-        }
-        __syncthreads();
-        inverse16<SC>(Nm, Em);
-        // W = E B<- ; Nk V
-        wg::gemm16<DK, TF32>(
-            kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
-            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+        float *xs = p.ws_x + ((head * N + n) * kC) * (size_t)dv + e0;
         wg::gemm16<kDVS, TF32>(
-            kC, [&](int i, int j) { return Nk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
-            [&](int i, int e, float x) { T1[i * SV + e] = x; });
+            DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
+            [&](int i, int e, float x) {
+                const float y = Cs[i * SV + e] - x;
+                Xm[i * SV + e] = y;
+                xs[(size_t)i * dv + e] = y;
+            });
         __syncthreads();
-        // V_2 = -E (Nk V) - W S^T
-        wg::gemm16_2<kDVS, TF32>(
-            kC, [&](int i, int j) { return -Em[i * SC + j]; }, [&](int j, int e) { return T1[j * SV + e]; }, DK,
-            [&](int i, int d) { return -Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
-            [&](int i, int e, float x) { Xm[i * SV + e] = x; });
-        __syncthreads();
-        // S <- (S + V^T K-> + V_2^T A->) Diag(gamma^C)
         wg::gemm2<DK, TF32>(
-            kC, [&](int e, int c) { return Vm[c * SV + e]; }, [&](int c, int d) { return Kr[c * SK + d]; }, kC,
-            [&](int e, int c) { return Xm[c * SV + e]; }, [&](int c, int d) { return Ar[c * SK + d]; },
-            [&](int e, int d, float x) { Sm[e * SK + d] = (Sm[e * SK + d] + x) * gam[d]; });
+            kC, [&](int e, int c) { return Vm[c * SV + e]; }, [&](int c, int d) { return KG[c * SK + d]; }, kC,
+            [&](int e, int c) { return Xm[c * SV + e]; }, [&](int c, int d) { return AG[c * SK + d]; },
+            [&](int e, int d, float x) { Sm[e * SK + d] = Sm[e * SK + d] * gam[d] + x; });
     }
     __syncthreads();
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
@@ -151,24 +227,21 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
 }
 
 // ------------------------------------------------------------------ kernel B
-template <int DK, typename Tin, typename Tg, bool TF32>
+// The reverse scan from the records: dC = A~ dS^T + P_a^T dO (kept for the
+// gradient kernel), dS <- dS Diag(gamma^C) + dO^T Q<- - dC^T W.
+template <int DK, int DV, typename Tin, bool TF32>
 __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrParams p) {
     constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
+    using R = BRec<DK, DV>;
     extern __shared__ float smem[];
-    float4 *rows = reinterpret_cast<float4 *>(smem);
-    float *Gm = smem + 4 * kC;           // [C][SK]  gate scratch
-    float *Ql = Gm + kC * SK;
-    float *Ar = Ql + kC * SK;
-    float *Bl = Ar + kC * SK;
-    float *Wm = Bl + kC * SK;
-    float *dS = Wm + kC * SK;            // [DVS][SK]
-    float *Nm = dS + kDVS * SK;          // [C][SC]
-    float *Em = Nm + kC * SC;
-    float *Pa = Em + kC * SC;
+    float *Wm = smem;                    // [C][SK]
+    float *AG = Wm + kC * SK;
+    float *QL = AG + kC * SK;
+    float *dS = QL + kC * SK;            // [DVS][SK]
+    float *Pa = dS + kDVS * SK;          // [C][SC]
     float *dO = Pa + kC * SC;            // [C][SV]
     float *dC = dO + kC * SV;
     float *gam = dC + kC * SV;           // [DK]
-    float *gsc = gam + DK;               // [C]
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -176,6 +249,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
     const Tin *dop = static_cast<const Tin *>(p.grad_o);
     const size_t head = (size_t)b * H + h;
     float *dSws = p.ws_dS + head * (size_t)N * dv * DK;
+    const float *recs = p.ws_prep + head * N * bwd_rec_floats(DK, DV);
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
@@ -183,42 +257,31 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
     }
     for (int n = N - 1; n >= 0; --n) {
         const int t0 = n * kC, nvalid = min(kC, T - t0);
+        const float *rec = recs + (size_t)n * bwd_rec_floats(DK, DV);
         __syncthreads();
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             dSws[((size_t)n * dv + e0 + e) * DK + d] = dS[e * SK + d];
         }
-        if (p.clip) {
-            dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
-            __syncthreads();
-        }
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::AG, DK, kC, AG);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::QL, DK, kC, QL);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::PA, kC, kC, Pa);
         wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv,
                                               nvalid, dO);
-        dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, nullptr, Ar, Bl, gam, gsc);
+        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
         __syncthreads();
-        {
-            auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
-            wg::gemm16_pair<kC, TF32>(
-                DK, [&](int i, int d) { return Bl[i * SK + d]; }, bAr, DK, [&](int i, int d) { return Ql[i * SK + d]; },
-                bAr, [&](int i, int j, float x, float y) {
-                    Nm[i * SC + j] = j < i ? x : 0.f;
-                    Pa[i * SC + j] = j <= i ? y : 0.f;
-                });
-        }
-        __syncthreads();
-        inverse16<SC>(Nm, Em);
-        // W = E B<- ; dC = A-> Diag(gamma^C) dS^T + P_a^T dO
-        wg::gemm16<DK, TF32>(
-            kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
-            [&](int i, int d, float x) { Wm[i * SK + d] = x; });
+        float *dcs = p.ws_dc + ((head * N + n) * kC) * (size_t)dv + e0;
         wg::gemm16_2<kDVS, TF32>(
-            DK, [&](int i, int d) { return Ar[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[e * SK + d]; },
-            kC, [&](int i, int j) { return Pa[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
-            [&](int i, int e, float x) { dC[i * SV + e] = x; });
+            DK, [&](int i, int d) { return AG[i * SK + d]; }, [&](int d, int e) { return dS[e * SK + d]; }, kC,
+            [&](int i, int j) { return Pa[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
+            [&](int i, int e, float x) {
+                dC[i * SV + e] = x;
+                dcs[(size_t)i * dv + e] = x;
+            });
         __syncthreads();
-        // dS <- dS Diag(gamma^C) + dO^T Q<- - dC^T W
         wg::gemm2<DK, TF32>(
-            kC, [&](int e, int c) { return dO[c * SV + e]; }, [&](int c, int d) { return Ql[c * SK + d]; }, kC,
+            kC, [&](int e, int c) { return dO[c * SV + e]; }, [&](int c, int d) { return QL[c * SK + d]; }, kC,
             [&](int e, int c) { return -dC[c * SV + e]; }, [&](int c, int d) { return Wm[c * SK + d]; },
             [&](int e, int d, float x) { dS[e * SK + d] = dS[e * SK + d] * gam[d] + x; });
     }
@@ -297,40 +360,18 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     }
     dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
     __syncthreads();
-    // Grams: N_ab, N_bk, P_k, P_a
+    // E, N_bk, P_k, P_a and W from the chunk record; V_2 (= X) and dC from the scans
     {
-        auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
-        auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
-        auto aBl = [&](int i, int d) { return Bl[i * SK + d]; };
-        auto aQl = [&](int i, int d) { return Ql[i * SK + d]; };
-        wg::gemm16_pair<kC, TF32>(DK, aBl, bAr, DK, aBl, bKr, [&](int i, int j, float x, float y) {
-            Nm[i * SC + j] = j < i ? x : 0.f;
-            Nk[i * SC + j] = j < i ? y : 0.f;
-        });
-        wg::gemm16_pair<kC, TF32>(DK, aQl, bKr, DK, aQl, bAr, [&](int i, int j, float x, float y) {
-            Pk[i * SC + j] = j <= i ? x : 0.f;
-            Pa[i * SC + j] = j <= i ? y : 0.f;
-        });
+        using R = BRec<DK, DV>;
+        const float *rec = p.ws_prep + (head * N + n) * bwd_rec_floats(DK, DV);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::E, kC, kC, Em);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::NK, kC, kC, Nk);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::PK, kC, kC, Pk);
+        wg::load_tile<kC, kC, SC, kThreads>(rec + R::PA, kC, kC, Pa);
+        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
+        wg::load_tile<kC, DV, SV, kThreads>(p.ws_x + (head * N + n) * (size_t)kC * DV, DV, kC, V2);
+        wg::load_tile<kC, DV, SV, kThreads>(p.ws_dc + (head * N + n) * (size_t)kC * DV, DV, kC, dC);
     }
-    __syncthreads();
-    inverse16<SC>(Nm, Em);
-    // W = E B<- ; Nk V
-    wg::gemm16<DK, TF32>(
-        kC, [&](int i, int j) { return Em[i * SC + j]; }, [&](int j, int d) { return Bl[j * SK + d]; },
-        [&](int i, int d, float x) { Wm[i * SK + d] = x; });
-    wg::gemm16<DV, TF32>(
-        kC, [&](int i, int j) { return Nk[i * SC + j]; }, [&](int j, int e) { return Vm[j * SV + e]; },
-        [&](int i, int e, float x) { Ym[i * SV + e] = x; });
-    __syncthreads();
-    // V_2 = -E (Nk V) - W S_prev^T ; dC = A-> Diag(gamma^C) dS^T + P_a^T dO
-    wg::gemm16_2<DV, TF32>(
-        kC, [&](int i, int j) { return -Em[i * SC + j]; }, [&](int j, int e) { return Ym[j * SV + e]; }, DK,
-        [&](int i, int d) { return -Wm[i * SK + d]; }, [&](int d, int e) { return Sp[(size_t)e * DK + d]; },
-        [&](int i, int e, float x) { V2[i * SV + e] = x; });
-    wg::gemm16_2<DV, TF32>(
-        DK, [&](int i, int d) { return Ar[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[(size_t)e * DK + d]; },
-        kC, [&](int i, int j) { return Pa[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
-        [&](int i, int e, float x) { dC[i * SV + e] = x; });
     __syncthreads();
     // O1 = dO V^T * M ; O2 = dO V_2^T * M ; Z1 = dC V^T
     {
@@ -518,13 +559,11 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
 
 template <int DK>
 constexpr size_t states_smem_bytes() {
-    return sizeof(float) * ((size_t)4 * kC + 5 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * kSC4 +
-                            3 * kC * pad4(kDVS) + DK + kC);
+    return sizeof(float) * ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * pad4(kDVS) + DK);
 }
 template <int DK>
 constexpr size_t dstate_smem_bytes() {
-    return sizeof(float) * ((size_t)4 * kC + 5 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * kSC4 +
-                            2 * kC * pad4(kDVS) + DK + kC);
+    return sizeof(float) * ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + kC * kSC4 + 2 * kC * pad4(kDVS) + DK);
 }
 
 template <typename F>
@@ -537,16 +576,18 @@ cudaError_t launch_all(const DplrParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const int N = (p.T + kC - 1) / kC;
     cudaError_t e;
-    const size_t sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
+    const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
     static_assert(sizeof(float) * grad_smem_floats<128, 128>() <= 227 * 1024, "kernel C shared memory");
-    if ((e = set_smem(dplr_bwd_states_kernel<DK, Tin, Tg, kTf32>, sa)) != cudaSuccess) return e;
-    if ((e = set_smem(dplr_bwd_dstate_kernel<DK, Tin, Tg, kTf32>, sb)) != cudaSuccess) return e;
+    if ((e = set_smem(dplr_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32>, sp)) != cudaSuccess) return e;
+    if ((e = set_smem(dplr_bwd_states_kernel<DK, DV, Tin, kTf32>, sa)) != cudaSuccess) return e;
+    if ((e = set_smem(dplr_bwd_dstate_kernel<DK, DV, Tin, kTf32>, sb)) != cudaSuccess) return e;
     if ((e = set_smem(dplr_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
-    const dim3 gscan(p.dv / kDVS, p.H, p.B), ggrad(N, p.H, p.B);
-    dplr_bwd_states_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sa, s>>>(p);
-    dplr_bwd_dstate_kernel<DK, Tin, Tg, kTf32><<<gscan, kThreads, sb, s>>>(p);
-    dplr_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<ggrad, kThreads, sc, s>>>(p);
+    const dim3 gscan(p.dv / kDVS, p.H, p.B), gchunk(N, p.H, p.B);
+    dplr_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sp, s>>>(p);
+    dplr_bwd_states_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sa, s>>>(p);
+    dplr_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sb, s>>>(p);
+    dplr_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sc, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -563,7 +604,7 @@ cudaError_t launch_typed(const DplrParams &p, cudaStream_t s) {
 
 size_t dplr_bwd_state_bytes(int B, int T, int H, int dk, int dv) {
     const size_t N = (T + kC - 1) / kC;
-    return sizeof(float) * (size_t)B * H * (2 * N + 1) * dv * dk;
+    return sizeof(float) * (size_t)B * H * ((2 * N + 1) * dv * dk + N * bwd_rec_floats(dk, dv) + 2 * N * kC * dv);
 }
 
 cudaError_t launch_dplr_bwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s) {

@@ -293,9 +293,13 @@ kda_status dplr_chunk_bwd(const dplr_bwd_args *args, kda_stream_t stream) {
     unsigned char *ws = static_cast<unsigned char *>(args->workspace);
     const size_t N = (size_t)(args->T + 15) / 16;
     const size_t per_state = (size_t)args->B * args->H * args->dv * args->dk;
+    const size_t bh = (size_t)args->B * args->H;
     p.status = reinterpret_cast<int *>(ws);
     p.ws_S = reinterpret_cast<float *>(ws + kStatusBytes);
     p.ws_dS = p.ws_S + (N + 1) * per_state;
+    p.ws_prep = p.ws_dS + N * per_state;
+    p.ws_x = p.ws_prep + N * bh * (4 * 16 * (size_t)args->dk + 16 * (size_t)args->dv + 4 * 16 * 16 + args->dk);
+    p.ws_dc = p.ws_x + N * bh * 16 * args->dv;
     return from_cuda(kda::launch_dplr_bwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -39,7 +39,9 @@ struct DplrParams {
     float *grad_h0;
     float *ws_S;            // [B, H, N + 1, dv, dk] states before each chunk, then the final state
     float *ws_dS;           // [B, H, N, dv, dk] gradients of the state after each chunk
-    float *ws_prep;         // forward: [B, H, N] chunk records (state-independent operands)
+    float *ws_prep;         // [B, H, N] chunk records (state-independent operands)
+    float *ws_x;            // backward: [B, H, N, C, dv] X of every chunk
+    float *ws_dc;           // backward: [B, H, N, C, dv] dC of every chunk
 };
 
 // Device-side copy of the validated backward arguments.

@@ -297,7 +297,13 @@ typedef struct {
     size_t workspace_bytes;
 } dplr_bwd_args;
 
-/* Workspace bytes for dplr_chunk_bwd: 256 + (2 ceil(T/16) + 1) B H dv dk 4 (0 on bad args). */
+/*
+ * Workspace bytes for dplr_chunk_bwd (0 on bad args): 256, the float32 chunk
+ * states and state gradients (2 N + 1) B H dv dk 4 with N = ceil(T/16), one
+ * record of state-independent chunk operands per chunk,
+ * N B H (4 16 dk + 16 dv + 4 16 16 + dk) 4, and the chunk products X and dC,
+ * 2 N B H 16 dv 4.
+ */
 size_t dplr_chunk_bwd_workspace(const dplr_bwd_args *args);
 
 /* Backward of the general gated DPLR recurrence; float32 CUDA-core kernels. */

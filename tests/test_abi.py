@@ -204,7 +204,8 @@ def _dplr_bwd_args(**over):
 def test_dplr_bwd_workspace_query(lib):
     need = lib.dplr_chunk_bwd_workspace(ctypes.byref(_dplr_bwd_args()))
     n_chunks = (100 + 15) // 16
-    assert need == 256 + 4 * 2 * 4 * (2 * n_chunks + 1) * 128 * 128
+    record = 4 * 16 * 128 + 16 * 128 + 4 * 16 * 16 + 128
+    assert need == 256 + 4 * 2 * 4 * ((2 * n_chunks + 1) * 128 * 128 + n_chunks * record + 2 * n_chunks * 16 * 128)
     assert lib.dplr_chunk_bwd_workspace(ctypes.byref(_dplr_bwd_args(dv=32))) == 0
 
 
