@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
 template <int DK, int DV>
 constexpr size_t grad_smem_floats() {
     return (size_t)4 * kC + (size_t)10 * kC * pad4(DK) + (size_t)5 * kC * pad4(DV) + (size_t)12 * kC * kSC4 + DK +
-           3 * kC;
+           3 * kC + DK + 32 * pad4(DK) + kC * pad4(DV);
 }
 
 template <int DK, int DV, typename Tin, typename Tg, bool TF32>
@@ -337,6 +337,9 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     float *rsum = gam + DK;              // [C] row sums / dL/d(-log rho)
     float *aux = rsum + kC;              // [C]
     float *gsc = aux + kC;               // [C]
+    float *lastrow = gsc + kC;           // [DK] diag(S_next^T dS)
+    float *slab = lastrow + DK;          // [32][SK] staged state rows
+    float *dVs = slab + 32 * SK;         // [C][SV] K-> Diag(gamma^C) dS^T
 
     const int tid = threadIdx.x;
     const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -386,23 +389,53 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
                              [&](int i, int j, float x) { Z1[i * SC + j] = x; });
     }
     __syncthreads();
-    // dW = -dC S_prev ; dQ<- ; dK-> and dA-> without their F/G terms ; Y = E^T dC
+    // dW = -dC S_prev ; dQ<- ; dK-> and dA-> without their F/G terms ; the dS term of dV ;
+    // diag(S_next^T dS) for the gamma^C row.  The stored states stream through
+    // shared memory 32 rows at a time (16-byte loads).
     {
-        auto bSp = [&](int e, int d) { return Sp[(size_t)e * DK + d]; };
-        auto bdS = [&](int e, int d) { return dS[(size_t)e * DK + d]; };
-        wg::gemm16<DK, TF32>(
-            DV, [&](int i, int e) { return dC[i * SV + e]; }, bSp, [&](int i, int d, float x) { Wm[i * SK + d] = -x; });
-        wg::gemm16_3<DK, TF32>(
-            DV, [&](int i, int e) { return dO[i * SV + e]; }, bSp, kC, [&](int i, int j) { return O1[i * SC + j]; },
-            [&](int j, int d) { return Kr[j * SK + d]; }, kC, [&](int i, int j) { return O2[i * SC + j]; },
-            [&](int j, int d) { return Ar[j * SK + d]; }, [&](int i, int d, float x) { dQl[i * SK + d] = x; });
+        constexpr int NT = wg::nt16<DK>();
+        int c0;
+        wg::origin16<DK>(c0);
+        float aW[NT][4] = {}, aQ[NT][4] = {}, aK[NT][4] = {}, aA[NT][4] = {}, aK2[NT][4] = {}, aA2[NT][4] = {};
+        for (int s0 = 0; s0 < DV; s0 += 32) {
+            wg::load_tile<32, DK, SK, kThreads>(Sp + (size_t)s0 * DK, DK, 32, slab);
+            __syncthreads();
+            auto bS = [&](int e, int d) { return slab[e * SK + d]; };
+            wg::tile<NT, TF32>(aW, 0, c0, 32, [&](int i, int e) { return dC[i * SV + s0 + e]; }, bS);
+            wg::tile<NT, TF32>(aQ, 0, c0, 32, [&](int i, int e) { return dO[i * SV + s0 + e]; }, bS);
+            __syncthreads();
+        }
+        float last = 0.f;                    // diag(S_next^T dS), column tid
+        for (int s0 = 0; s0 < DV; s0 += 32) {
+            wg::load_tile<32, DK, SK, kThreads>(dS + (size_t)s0 * DK, DK, 32, slab);
+            float sn[32];
+            if (tid < DK)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sn[e] = Sn[(size_t)(s0 + e) * DK + tid];
+            __syncthreads();
+            auto bS = [&](int e, int d) { return slab[e * SK + d]; };
+            wg::tile<NT, TF32>(aK, 0, c0, 32, [&](int i, int e) { return Vm[i * SV + s0 + e]; }, bS);
+            wg::tile<NT, TF32>(aA, 0, c0, 32, [&](int i, int e) { return V2[i * SV + s0 + e]; }, bS);
+            wg::gemm16<32, TF32>(
+                DK, [&](int i, int d) { return Kr[i * SK + d] * gam[d]; }, [&](int d, int e) { return slab[e * SK + d]; },
+                [&](int i, int e, float x) { dVs[i * SV + s0 + e] = x; });
+            if (tid < DK)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) last += sn[e] * slab[e * SK + tid];
+            __syncthreads();
+        }
+        if (tid < DK) lastrow[tid] = last;
+        wg::tile<NT, TF32>(aQ, 0, c0, kC, [&](int i, int j) { return O1[i * SC + j]; },
+                           [&](int j, int d) { return Kr[j * SK + d]; });
+        wg::tile<NT, TF32>(aQ, 0, c0, kC, [&](int i, int j) { return O2[i * SC + j]; },
+                           [&](int j, int d) { return Ar[j * SK + d]; });
         auto bQl = [&](int j, int d) { return Ql[j * SK + d]; };
-        wg::gemm16_pair<DK, TF32>(
-            DV, [&](int i, int e) { return Vm[i * SV + e]; }, bdS, kC, [&](int i, int j) { return O1[j * SC + i]; }, bQl,
-            [&](int i, int d, float x1, float x2) { dKr[i * SK + d] = x1 * gam[d] + x2; });
-        wg::gemm16_pair<DK, TF32>(
-            DV, [&](int i, int e) { return V2[i * SV + e]; }, bdS, kC, [&](int i, int j) { return O2[j * SC + i]; }, bQl,
-            [&](int i, int d, float x1, float x2) { dAr[i * SK + d] = x1 * gam[d] + x2; });
+        wg::tile<NT, TF32>(aK2, 0, c0, kC, [&](int i, int j) { return O1[j * SC + i]; }, bQl);
+        wg::tile<NT, TF32>(aA2, 0, c0, kC, [&](int i, int j) { return O2[j * SC + i]; }, bQl);
+        wg::store<NT>(aW, 0, c0, [&](int i, int d, float x) { Wm[i * SK + d] = -x; });
+        wg::store<NT>(aQ, 0, c0, [&](int i, int d, float x) { dQl[i * SK + d] = x; });
+        wg::store_pair<NT>(aK, aK2, 0, c0, [&](int i, int d, float x1, float x2) { dKr[i * SK + d] = x1 * gam[d] + x2; });
+        wg::store_pair<NT>(aA, aA2, 0, c0, [&](int i, int d, float x1, float x2) { dAr[i * SK + d] = x1 * gam[d] + x2; });
     }
     wg::gemm16<DV, TF32>(
         kC, [&](int i, int j) { return Em[j * SC + i]; }, [&](int j, int e) { return dC[j * SV + e]; },
@@ -444,12 +477,11 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     // dV = K-> Diag(gamma^C) dS^T + P_k^T dO - Nk^T (E^T dC)
     {
         Tin *gv = static_cast<Tin *>(p.grad_v);
-        wg::gemm16_3<DV, TF32>(
-            DK, [&](int i, int d) { return Kr[i * SK + d] * gam[d]; }, [&](int d, int e) { return dS[(size_t)e * DK + d]; },
+        wg::gemm16_2<DV, TF32>(
             kC, [&](int i, int j) { return Pk[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; }, kC,
             [&](int i, int j) { return -Nk[j * SC + i]; }, [&](int j, int e) { return Ym[j * SV + e]; },
             [&](int i, int e, float x) {
-                if (i < nvalid) stf(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, x);
+                if (i < nvalid) stf(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, x + dVs[i * SV + e]);
             });
     }
     __syncthreads();
@@ -471,8 +503,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     // dg' = in-chunk suffix sums of dlogGamma, the gamma^C row adding diag(S_next^T dS)
     const bool channel = p.gate_kind == KDA_GATE_CHANNEL;
     for (int d = tid; d < DK; d += kThreads) {
-        float run = 0.f;
-        for (int e = 0; e < DV; ++e) run += Sn[(size_t)e * DK + d] * dS[(size_t)e * DK + d];
+        float run = lastrow[d];              // diag(S_next^T dS), from the state pass above
         for (int i = kC - 1; i >= 0; --i) {
             run += dQl[i * SK + d];
             dQl[i * SK + d] = run;
