@@ -228,7 +228,8 @@ extern "C" {
 
 size_t kda_chunk_fwd_workspace(const kda_fwd_args *args) {
     if (validate(args) != KDA_OK) return 0;
-    return kStatusBytes;
+    if (args->dtype != KDA_BF16) return kStatusBytes;
+    return kStatusBytes + kda::fwd_zrec_bytes(args->B, args->T, args->H, args->cu_seqlens != nullptr);
 }
 
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
@@ -245,6 +246,15 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
     p.h0 = args->h0; p.o = args->o; p.ht = args->ht;
     p.status = static_cast<int *>(args->workspace);
     p.cu_seqlens = args->cu_seqlens;
+    if (args->dtype == KDA_BF16) {
+        // the full workspace holds the Z records of the two-kernel path; the status word alone
+        // selects the single-kernel path
+        const size_t zbytes = kda::fwd_zrec_bytes(args->B, args->T, args->H, args->cu_seqlens != nullptr);
+        if (args->workspace_bytes >= kStatusBytes + zbytes) {
+            if (!aligned16(args->workspace)) return KDA_ERR_INVALID_ARG;
+            p.zrec = static_cast<uint8_t *>(args->workspace) + kStatusBytes;
+        }
+    }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int g_bf16 = args->g_dtype == KDA_BF16;
@@ -371,7 +381,8 @@ kda_status kda_status_read(void *workspace, kda_stream_t stream) {
         return KDA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
     if (word != kda::kDevOk) {
-        if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return KDA_ERR_CUDA;
+        // the status word and the words after it that locate the first wait that ran out
+        if (cudaMemsetAsync(workspace, 0, 8 * sizeof(int), s) != cudaSuccess) return KDA_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     return word == kda::kDevOk ? KDA_OK : word == kda::kDevTimeout ? KDA_ERR_TIMEOUT : KDA_ERR_CUDA;

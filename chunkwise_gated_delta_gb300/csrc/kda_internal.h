@@ -20,6 +20,7 @@ struct FwdParams {
     float *ht;
     int *status;            // first word of the workspace
     const int *cu_seqlens;  // packed sequences: [B + 1] row offsets into a [1, T, H, d] batch, or null
+    uint8_t *zrec;          // bf16 path: Z records (fwd_zrec_bytes), or null to build Z in the scan kernel
 };
 
 // Device-side copy of the validated DPLR arguments.
@@ -72,6 +73,8 @@ cudaError_t launch_fwd_simt_f32(const FwdParams &p, int g_is_bf16, cudaStream_t 
 
 // bf16 tcgen05 path; returns cudaErrorNotSupported for shapes it does not take.
 cudaError_t launch_fwd_tc_bf16(const FwdParams &p, int g_is_bf16, cudaStream_t s);
+// Bytes of Z records the bf16 forward uses (16 KB per chunk slot and head).
+size_t fwd_zrec_bytes(int B, int T, int H, bool packed);
 
 // float32 CUDA-core DPLR chunk forward (inputs float32 or bf16) and the bytes
 // of chunk records it keeps in the workspace.

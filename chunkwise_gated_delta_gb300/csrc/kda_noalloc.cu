@@ -1,14 +1,16 @@
 // kda_chunk_fwd_noalloc: the forward for callers that cannot allocate device
 // memory at the point of the call.
 //
-// kda_chunk_fwd needs one piece of memory besides its inputs and outputs: a
-// workspace whose first word the kernels use to report a device-side error.
-// Callers that cannot provide it -- code running while a stream is captured
-// into a CUDA graph, frameworks whose allocator forbids allocations outside
-// its own arenas, hosts that only hand over the input and output tensors --
-// use this entry point instead.  The workspace then lives in a small array
-// owned by the library, defined below; every GPU that loads the library
-// holds it until the process exits.
+// kda_chunk_fwd needs a workspace besides its inputs and outputs: its first
+// word is where the kernels report a device-side error, and on the bf16 path
+// the rest, when given, holds the Z records of the two-kernel form.  Callers
+// that cannot provide one -- code running while a stream is captured into a
+// CUDA graph, frameworks whose allocator forbids allocations outside its own
+// arenas, hosts that only hand over the input and output tensors -- use this
+// entry point instead.  The status word then lives in a small array owned by
+// the library, defined below (every GPU that loads the library holds it until
+// the process exits), and the forward runs its single-kernel form, which
+// builds each chunk's Z inside the scan kernel and needs no records.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -17,8 +19,8 @@
 
 namespace {
 
-// Library-owned replacement for the caller's workspace (the forward needs
-// 256 bytes: its status word, padded to an aligned block).
+// Library-owned replacement for the caller's workspace: the status word,
+// padded to an aligned block (all the single-kernel forward needs).
 constexpr size_t kNoAllocScratchBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -48,9 +50,8 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const kda_fwd_args *args, kda_stream
     kda_fwd_args a = *args;
     a.workspace = nullptr;          // the caller's workspace fields are ignored
     a.workspace_bytes = 0;
-    const size_t need = kda_chunk_fwd_workspace(&a);
-    if (need == 0) return kda_chunk_fwd(&a, stream);          // reports the argument error, launches nothing
-    if (need > kNoAllocScratchBytes) return KDA_ERR_WORKSPACE;  // more scratch than the library array holds
+    if (kda_chunk_fwd_workspace(&a) == 0) return kda_chunk_fwd(&a, stream);   // reports the argument error
+    const size_t need = kNoAllocScratchBytes;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
     void *scratch = nullptr;

@@ -33,7 +33,10 @@
  *     detected on the host before anything is launched and nothing is
  *     written; the return value says which.  Errors found on the device
  *     (a bounded wait that ran out) are recorded in the first word of the
- *     workspace and read back with kda_status_read.
+ *     workspace and read back with kda_status_read.  The forward also leaves,
+ *     in words 1-6 of the workspace, where the first wait ran out (barrier,
+ *     phase, thread, block, and the barriers its two issuing threads were on)
+ *     for diagnosis; kda_status_read clears them with the status word.
  *   - Outputs must not alias inputs.
  */
 #ifndef KDA_H_
@@ -100,20 +103,36 @@ typedef struct {
     const int32_t *cu_seqlens;
 } kda_fwd_args;
 
-/* Bytes of workspace kda_chunk_fwd needs for these arguments (0 on bad args). */
+/*
+ * Bytes of workspace kda_chunk_fwd runs fastest with for these arguments (0
+ * on bad args): 256 for the status word, plus, for bfloat16 inputs, one
+ * 66048-byte chunk record per chunk slot and head -- B * ceil(T / 64) slots,
+ * or B + ceil(T / 64) with cu_seqlens.
+ */
 size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
 
 /*
  * Chunkwise forward of the gated delta rule (KDA and its special cases).
  * Writes o, and ht when non-NULL.  float32 inputs run a float32 CUDA-core
- * kernel; bfloat16 inputs run the tcgen05 tensor-core kernel (bf16 operands,
+ * kernel; bfloat16 inputs run the tcgen05 tensor-core path (bf16 operands,
  * fp32 accumulation, fp32 state).
+ *
+ * The workspace must be at least 256 bytes (KDA_ERR_WORKSPACE otherwise).
+ * For bfloat16 inputs with workspace_bytes >= kda_chunk_fwd_workspace(args)
+ * the forward takes two kernels: a chunk-parallel one writes every chunk's
+ * record into the workspace -- Z = [T ; P T] (T = (I + L)^{-1} Diag(beta)
+ * with L the masked beta K<- K->^T, P the masked Q<- K->^T: the forward recap
+ * of page "Kimi Delta Attention backward"), the rescaled tiles Q<-, K<-, K->
+ * and gamma^C -- then the scan kernel reads them; the
+ * workspace must then be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
+ * With a smaller workspace the scan kernel builds Z itself (one kernel,
+ * slower); both forms compute the same values.
  */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 
 /*
- * kda_chunk_fwd without a workspace from the caller.  The papers have no
- * counterpart: this is library plumbing.
+ * kda_chunk_fwd without a workspace from the caller, in its single-kernel
+ * form.  The papers have no counterpart: this is library plumbing.
  *
  * Some callers cannot allocate device memory where they call the forward:
  * code running while a stream is being captured into a CUDA graph,
@@ -127,8 +146,7 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  *   - Every call clears the array's status word on `stream`, then launches.
  *     All calls share the array, so calls that overlap on the GPU (unordered
  *     streams) race on it.
- *   - Returns KDA_ERR_WORKSPACE if the forward would need more scratch than
- *     the array holds (the current kernels need all of 256 bytes, no more).
+ *   - Runs the single-kernel form of kda_chunk_fwd (no chunk records).
  *   - A device-side wait that runs out is recorded in the shared array and
  *     cleared by the next call; to observe it, use kda_chunk_fwd with your
  *     own workspace and kda_status_read.

@@ -259,3 +259,58 @@ def test_varlen_noalloc_and_many_sequences():
         if lens[i]:
             assert rel(o[:, starts[i]:starts[i + 1]], ro) <= 5e-3, i
         assert rel(ht[i], rh[0]) <= 5e-3, i
+
+
+# ---------------------------------------------------------------- single-kernel form (status-word workspace)
+def _small_workspace():
+    return torch.zeros(256, dtype=torch.uint8, device=DEV)
+
+
+@pytest.mark.parametrize("variant,dv", [("kda", 128), ("kda", 64), ("gdn", 128), ("deltanet", 128), ("gla", 128)])
+def test_bf16_single_kernel_form(variant, dv):
+    """With only the status word as workspace the scan kernel builds Z itself; same tolerance
+    against the oracle, and it agrees with the two-kernel form (Z records) to rounding."""
+    w = custom(variant, 2, 300, 3, 128, dv, dtype=torch.bfloat16, h0=True)
+    x = make_inputs(w, seed=6)
+    d = {k_: (v_.to(DEV) if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    gate = {"kda": "channel", "gla": "channel", "gdn": "scalar", "deltanet": "none"}[variant]
+    args = (d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"))
+    o1, h1 = kda_chunk_fwd(*args, gate=gate, scale_v=x["scale_v"], workspace=_small_workspace())
+    o2, h2 = kda_chunk_fwd(*args, gate=gate, scale_v=x["scale_v"])
+    torch.cuda.synchronize()
+    ro, rh = run_oracle(x, variant)
+    o1, h1, o2, h2 = (t.double().cpu().numpy() for t in (o1, h1, o2, h2))
+    assert rel(o1, ro) <= 5e-3 and rel(h1, rh) <= 5e-3, (rel(o1, ro), rel(h1, rh))
+    assert rel(o2, o1) <= 1e-5 and rel(h2, h1) <= 1e-5, (rel(o2, o1), rel(h2, h1))
+
+
+def test_bf16_single_kernel_form_varlen():
+    lens = [100, 0, 1, 193, 64]
+    x, cu, refs, scale_v = _varlen_case(torch.bfloat16, lens, 128, 128, seed=30)
+    d = {k_: v_.to(DEV) for k_, v_ in x.items()}
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], gate="channel", scale_v=scale_v,
+                          cu_seqlens=cu.to(DEV), workspace=_small_workspace())
+    torch.cuda.synchronize()
+    o, ht = o.double().cpu().numpy(), ht.double().cpu().numpy()
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    for i, (ro, rh) in enumerate(refs):
+        if lens[i]:
+            assert rel(o[:, starts[i]:starts[i + 1]], ro) <= 5e-3, i
+        assert rel(ht[i], rh[0]) <= 5e-3, i
+
+
+def test_bf16_workspace_sizes():
+    """kda_chunk_fwd_workspace: the status word plus a 66048-byte record per chunk slot and head."""
+    import ctypes
+    from chunkwise_gated_delta_gb300 import _lib, api
+    lib = _lib.load()
+    w = custom("kda", 3, 200, 2, 128, 128, dtype=torch.bfloat16, h0=True)
+    x = make_inputs(w, seed=0)
+    d = {k_: v_.to(DEV) for k_, v_ in x.items() if isinstance(v_, torch.Tensor)}
+    o = torch.empty_like(d["v"])
+    a = api.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o)
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(a)) == 256 + 3 * 4 * 2 * 66048
+    cu = torch.tensor([0, 50, 200], dtype=torch.int32, device=DEV)
+    a = api.make_args(d["q"][:1], d["k"][:1], d["v"][:1], d["g"][:1], d["beta"][:1], d["h0"][:2], o[:1],
+                      cu_seqlens=cu)
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(a)) == 256 + (2 + 4) * 2 * 66048
