@@ -222,14 +222,21 @@ kda_status from_cuda(cudaError_t e) {
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Chunk-record bytes of the two-kernel bf16 forward, 0 where the single kernel is the faster
+// form: float32 inputs, and GLA (beta = 0, v unscaled), which has no inverse to hoist.
+size_t fwd_record_bytes(const kda_fwd_args *a) {
+    const bool gla = !(a->flags & KDA_FLAG_BETA_SCALES_V);
+    if (a->dtype != KDA_BF16 || gla) return 0;
+    return kda::fwd_zrec_bytes(a->B, a->T, a->H, a->cu_seqlens != nullptr);
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t kda_chunk_fwd_workspace(const kda_fwd_args *args) {
     if (validate(args) != KDA_OK) return 0;
-    if (args->dtype != KDA_BF16) return kStatusBytes;
-    return kStatusBytes + kda::fwd_zrec_bytes(args->B, args->T, args->H, args->cu_seqlens != nullptr);
+    return kStatusBytes + fwd_record_bytes(args);
 }
 
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
@@ -246,10 +253,9 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
     p.h0 = args->h0; p.o = args->o; p.ht = args->ht;
     p.status = static_cast<int *>(args->workspace);
     p.cu_seqlens = args->cu_seqlens;
-    if (args->dtype == KDA_BF16) {
-        // the full workspace holds the Z records of the two-kernel path; the status word alone
-        // selects the single-kernel path
-        const size_t zbytes = kda::fwd_zrec_bytes(args->B, args->T, args->H, args->cu_seqlens != nullptr);
+    if (const size_t zbytes = fwd_record_bytes(args)) {
+        // the full workspace holds the chunk records of the two-kernel form; the status word
+        // alone selects the single-kernel form
         if (args->workspace_bytes >= kStatusBytes + zbytes) {
             if (!aligned16(args->workspace)) return KDA_ERR_INVALID_ARG;
             p.zrec = static_cast<uint8_t *>(args->workspace) + kStatusBytes;

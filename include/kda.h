@@ -105,9 +105,10 @@ typedef struct {
 
 /*
  * Bytes of workspace kda_chunk_fwd runs fastest with for these arguments (0
- * on bad args): 256 for the status word, plus, for bfloat16 inputs, one
- * 66048-byte chunk record per chunk slot and head -- B * ceil(T / 64) slots,
- * or B + ceil(T / 64) with cu_seqlens.
+ * on bad args): 256 for the status word, plus, for bfloat16 inputs with the
+ * delta term (every variant but GLA), one 66048-byte chunk record per chunk
+ * slot and head -- B * ceil(T / 64) slots, or B + ceil(T / 64) with
+ * cu_seqlens.
  */
 size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
 
@@ -118,15 +119,16 @@ size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
  * fp32 accumulation, fp32 state).
  *
  * The workspace must be at least 256 bytes (KDA_ERR_WORKSPACE otherwise).
- * For bfloat16 inputs with workspace_bytes >= kda_chunk_fwd_workspace(args)
- * the forward takes two kernels: a chunk-parallel one writes every chunk's
- * record into the workspace -- Z = [T ; P T] (T = (I + L)^{-1} Diag(beta)
- * with L the masked beta K<- K->^T, P the masked Q<- K->^T: the forward recap
- * of page "Kimi Delta Attention backward"), the rescaled tiles Q<-, K<-, K->
- * and gamma^C -- then the scan kernel reads them; the
- * workspace must then be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
- * With a smaller workspace the scan kernel builds Z itself (one kernel,
- * slower); both forms compute the same values.
+ * For bfloat16 inputs with the delta term and workspace_bytes >=
+ * kda_chunk_fwd_workspace(args) the forward takes two kernels: a
+ * chunk-parallel one writes every chunk's record into the workspace --
+ * Z = [T ; P T] (T = (I + L)^{-1} Diag(beta) with L the masked
+ * beta K<- K->^T, P the masked Q<- K->^T: the forward recap of page "Kimi
+ * Delta Attention backward"), the rescaled tiles Q<-, K<-, K-> and gamma^C
+ * -- then the scan kernel reads them; the workspace must then be 16-byte
+ * aligned (KDA_ERR_INVALID_ARG otherwise).  With a smaller workspace the
+ * scan kernel builds Z itself (one kernel, slower); both forms compute the
+ * same values.
  */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 
