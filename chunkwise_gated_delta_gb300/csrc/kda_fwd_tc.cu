@@ -1115,7 +1115,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     if (wt == 0) {
         bulk_store(rec + REC_Z, base + OFF_KR, 16384u);
         tma_store_commit();
-        tma_store_wait_all0();
+        tma_store_wait_read0();             // shared memory may go once the copy has read it
     }
     __syncwarp();
     tc_fence_before();
