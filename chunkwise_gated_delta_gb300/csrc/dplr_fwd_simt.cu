@@ -162,23 +162,23 @@ constexpr size_t prep_smem_bytes() {
 }
 
 // One CTA per (32-wide value slice, head, batch): the serial scan over the
-// chunk records.
+// chunk records.  The records (and v) of chunk n + 1 travel by cp.async into a
+// second buffer while chunk n computes.
+template <int DK, typename Tin>
+__host__ __device__ constexpr int scan_buf_floats() {
+    // W, Qt, K~, A~ [C][SK]; C and O_loc slices [C][SV]; gamma^C [DK]; raw v rows [C][DVS] of Tin
+    return 4 * kC * pad4(DK) + 2 * kC * pad4(kDVS) + DK + (kC * kDVS * (int)sizeof(Tin) + 3) / 4;
+}
 template <int DK, int DV, typename Tin, bool TF32>
 __global__ void __launch_bounds__(kThreads)
 dplr_fwd_simt_kernel(const DplrParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS);
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), BUF = scan_buf_floats<DK, Tin>();
     using R = DRec<DK, DV>;
     extern __shared__ float smem[];
-    float *Wm = smem;                 // [C][SK]
-    float *QT = Wm + kC * SK;         // [C][SK]
-    float *KG = QT + kC * SK;         // [C][SK]
-    float *AG = KG + kC * SK;         // [C][SK]
-    float *Sm = AG + kC * SK;         // [DVS][SK] state slice
-    float *Cs = Sm + kDVS * SK;       // [C][SV]  C slice
-    float *Os = Cs + kC * SV;         // [C][SV]  O_loc slice
-    float *Vm = Os + kC * SV;         // [C][SV]  v slice
+    float *Sm = smem;                 // [DVS][SK] state slice
+    float *Vm = Sm + kDVS * SK;       // [C][SV]  v slice (float)
     float *Xm = Vm + kC * SV;         // [C][SV]  X
-    float *gC = Xm + kC * SV;         // [DK]
+    float *bufs = Xm + kC * SV;       // 2 x BUF
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS;
@@ -187,24 +187,38 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
     const float *recs = p.ws_prep + ((size_t)b * H + h) * N * dplr_rec_floats(DK, DV);
+    auto issue = [&](int n) {
+        const float *rec = recs + (size_t)n * dplr_rec_floats(DK, DV);
+        float *bf = bufs + (n & 1) * BUF;
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::W, DK, bf);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::QT, DK, bf + kC * SK);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::KG, DK, bf + 2 * kC * SK);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::AG, DK, bf + 3 * kC * SK);
+        wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, bf + 4 * kC * SK);
+        wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::OL + e0, DV, bf + 4 * kC * SK + kC * SV);
+        wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 4 * kC * SK + 2 * kC * SV);
+        wg::load_raw_async<kC, kDVS, Tin, kThreads>(v + (((size_t)b * T + n * kC) * H + h) * dv + e0, (size_t)H * dv,
+                                                    min(kC, T - n * kC),
+                                                    reinterpret_cast<Tin *>(bf + 4 * kC * SK + 2 * kC * SV + DK));
+    };
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         Sm[e * SK + d] = p.h0 ? p.h0[(((size_t)b * H + h) * dv + e0 + e) * DK + d] : 0.f;
     }
+    issue(0);
+    wg::cp_async_commit();
     for (int n = 0; n < N; ++n) {
         const int t0 = n * kC, nvalid = min(kC, T - t0);
-        const float *rec = recs + (size_t)n * dplr_rec_floats(DK, DV);
+        float *Wm = bufs + (n & 1) * BUF, *QT = Wm + kC * SK, *KG = QT + kC * SK, *AG = KG + kC * SK;
+        float *Cs = AG + kC * SK, *Os = Cs + kC * SV, *gC = Os + kC * SV;
+        const Tin *vraw = reinterpret_cast<const Tin *>(gC + DK);
+        __syncthreads();                  // chunk n - 1 is done with the other buffer
+        if (n + 1 < N) issue(n + 1);
+        wg::cp_async_commit();            // (an empty group on the last chunk keeps the count)
+        wg::cp_async_wait<1>();           // chunk n's copies (this thread's) have landed
         __syncthreads();
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::QT, DK, kC, QT);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KG, DK, kC, KG);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::AG, DK, kC, AG);
-        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, kC, Cs);
-        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::OL + e0, DV, kC, Os);
-        wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
-                                              Vm);
-        for (int d = tid; d < DK; d += kThreads) gC[d] = rec[R::GC + d];
+        wg::to_f32<kC, kDVS, SV, Tin, kThreads>(vraw, Vm);
         __syncthreads();
         // X = C - W S^T ; O = Qt S^T + O_loc
         {
@@ -232,16 +246,17 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     }
 }
 
-template <int DK>
+template <int DK, typename Tin>
 constexpr size_t dplr_smem_bytes() {
-    return sizeof(float) * (size_t)(4 * kC * pad4(DK) + kDVS * pad4(DK) + 4 * kC * pad4(kDVS) + DK);
+    return sizeof(float) * (size_t)(kDVS * pad4(DK) + 2 * kC * pad4(kDVS) + 2 * scan_buf_floats<DK, Tin>());
 }
 
 template <int DK, int DV, typename Tin, typename Tg>
 cudaError_t launch_dkv(const DplrParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const int N = (p.T + kC - 1) / kC;
-    const size_t sp = prep_smem_bytes<DK, DV>(), sm = dplr_smem_bytes<DK>();
+    const size_t sp = prep_smem_bytes<DK, DV>(), sm = dplr_smem_bytes<DK, Tin>();
+    static_assert(dplr_smem_bytes<128, float>() <= 227 * 1024, "scan shared memory");
     static_assert(prep_smem_bytes<128, 256>() <= 227 * 1024, "shared memory");
     cudaError_t e = cudaFuncSetAttribute(dplr_fwd_prep_kernel<DK, DV, Tin, Tg, kTf32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);

@@ -283,6 +283,7 @@ kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream) {
     if (st != KDA_OK) return st;
     const size_t need = kStatusBytes + kda::dplr_fwd_record_bytes(args->B, args->T, args->H, args->dk, args->dv);
     if (!args->workspace || args->workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(args->workspace)) return KDA_ERR_INVALID_ARG;   // vector and async copies into it
     kda::DplrParams p = dplr_params(args);
     p.ws_prep = reinterpret_cast<float *>(static_cast<unsigned char *>(args->workspace) + kStatusBytes);
     return from_cuda(kda::launch_dplr_fwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
@@ -298,6 +299,7 @@ kda_status dplr_chunk_bwd(const dplr_bwd_args *args, kda_stream_t stream) {
     kda_status st = validate_dplr_bwd(args);
     if (st != KDA_OK) return st;
     if (!args->workspace || args->workspace_bytes < dplr_bwd_workspace_bytes(args)) return KDA_ERR_WORKSPACE;
+    if (!aligned16(args->workspace)) return KDA_ERR_INVALID_ARG;   // vector and async copies into it
     kda::DplrParams p{};
     p.B = args->B; p.T = args->T; p.H = args->H; p.dk = args->dk; p.dv = args->dv;
     p.gate_kind = args->gate_kind;
@@ -355,6 +357,7 @@ kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream) {
     kda_status st = validate_bwd(args);
     if (st != KDA_OK) return st;
     if (!args->workspace || args->workspace_bytes < bwd_workspace_bytes(args)) return KDA_ERR_WORKSPACE;
+    if (!aligned16(args->workspace)) return KDA_ERR_INVALID_ARG;   // vector and async copies into it
     kda::BwdParams p{};
     p.B = args->B; p.T = args->T; p.H = args->H; p.dk = args->dk; p.dv = args->dv;
     p.gate_kind = args->gate_kind;

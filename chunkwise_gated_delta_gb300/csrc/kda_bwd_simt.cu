@@ -227,16 +227,18 @@ constexpr size_t prep_smem_bytes() {
 // ------------------------------------------------------------------ kernel A
 // The forward state scan from the chunk records: V_new = U - W S^T,
 // S <- S Diag(gamma^C) + V_new^T K~.  One CTA per (32-wide value slice, head, batch).
+// The records of chunk n + 1 travel (cp.async, double buffer) while chunk n computes.
+template <int DK>
+__host__ __device__ constexpr int states_buf_floats() {
+    return 2 * kC * pad4(DK) + kC * pad4(kDVS) + DK;       // W, K~, U (then V_new), gamma^C
+}
 template <int DK, int DV, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS);
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), BUF = states_buf_floats<DK>();
     using R = Rec<DK, DV>;
     extern __shared__ float smem[];
-    float *Wm = smem;                  // [C][SK]
-    float *KT = Wm + kC * SK;          // [C][SK]
-    float *Sm = KT + kC * SK;          // [DVS][SK]
-    float *Um = Sm + kDVS * SK;        // [C][SV]  U, then V_new
-    float *gam = Um + kC * SV;         // [DK]
+    float *Sm = smem;                  // [DVS][SK]
+    float *bufs = Sm + kDVS * SK;      // 2 x BUF
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -244,23 +246,32 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
     const size_t head = (size_t)b * H + h;
     float *Sws = p.ws_S + head * (size_t)(N + 1) * dv * DK;
     const float *recs = p.ws_prep + head * N * rec_floats(DK, DV);
+    auto issue = [&](int n) {
+        const float *rec = recs + (size_t)n * rec_floats(DK, DV);
+        float *bf = bufs + (n & 1) * BUF;
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::W, DK, bf);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::KT, DK, bf + kC * SK);
+        wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::U + e0, DV, bf + 2 * kC * SK);
+        wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 2 * kC * SK + kC * SV);
+    };
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         Sm[e * SK + d] = p.h0 ? p.h0[(head * dv + e0 + e) * DK + d] : 0.f;
     }
+    issue(0);
+    wg::cp_async_commit();
     for (int n = 0; n < N; ++n) {
-        const float *rec = recs + (size_t)n * rec_floats(DK, DV);
-        __syncthreads();
+        float *Wm = bufs + (n & 1) * BUF, *KT = Wm + kC * SK, *Um = KT + kC * SK, *gam = Um + kC * SV;
+        __syncthreads();               // S is final for chunk n; chunk n - 1's buffer is free
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
         }
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KT, DK, kC, KT);
-        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::U + e0, DV, kC, Um);
-        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
-        __syncthreads();
+        if (n + 1 < N) issue(n + 1);
+        wg::cp_async_commit();         // (an empty group on the last chunk keeps the count)
+        wg::cp_async_wait<1>();        // chunk n's tiles have landed (this thread's copies)
+        __syncthreads();               // ... and everyone's
         float *vn = p.ws_vnew + ((head * N + n) * kC) * (size_t)dv + e0;     // V_new rows of this chunk
         wg::gemm<kDVS, TF32>(
             DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
@@ -583,7 +594,7 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
 
 template <int DK>
 constexpr size_t states_smem_bytes() {
-    return sizeof(float) * ((size_t)2 * kC * pad4(DK) + kDVS * pad4(DK) + kC * pad4(kDVS) + DK);
+    return sizeof(float) * ((size_t)kDVS * pad4(DK) + 2 * states_buf_floats<DK>());
 }
 template <int DK>
 constexpr size_t dstate_smem_bytes() {

@@ -202,6 +202,8 @@ __device__ __forceinline__ void gemm16_pair(int K1, const FA1 &A1, const FB1 &B1
 
 // ---- staging of [rows][D] tiles from global memory
 // 8 consecutive elements as floats: one 16-byte load for bf16, two for fp32.
+__device__ __forceinline__ float ldf1(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float ldf1(float x) { return x; }
 __device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float (&x)[8]) {
     const uint4 u = *reinterpret_cast<const uint4 *>(p);
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -246,6 +248,46 @@ __device__ __forceinline__ void load_tile(const T *src, size_t rs, int nvalid, f
             q[1] = make_float4(x[it][4], x[it][5], x[it][6], x[it][7]);
         }
     }
+}
+
+// Asynchronous copy of an R x D float32 tile (global row stride rs floats, shared row stride SD;
+// every row start 16-byte aligned) by cp.async, 16 bytes per request, NT threads.  Completes
+// through cp_async_commit / cp_async_wait, so the next chunk's tiles can travel while the
+// current chunk computes.
+template <int R, int D, int SD, int NT>
+__device__ __forceinline__ void load_tile_async(const float *src, size_t rs, float *dst) {
+    static_assert(D % 4 == 0 && SD % 4 == 0, "tile shape");
+    constexpr int V = D / 4, TOT = R * V;
+    for (int idx = threadIdx.x; idx < TOT; idx += NT) {
+        const int c = idx / V, d0 = (idx % V) * 4;
+        const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(dst + c * SD + d0));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(src + (size_t)c * rs + d0)
+                     : "memory");
+    }
+}
+// The raw rows of an R x D tile of T (bf16 or float) into a shared staging tile with row stride D,
+// rows at or past nvalid zero-filled; every row start 16-byte aligned.  to_f32 converts it.
+template <int R, int D, typename T, int NT>
+__device__ __forceinline__ void load_raw_async(const T *src, size_t rs, int nvalid, T *dst) {
+    constexpr int E = 16 / sizeof(T), V = D / E, TOT = R * V;   // elements per request, requests per row
+    static_assert(D % E == 0, "tile shape");
+    for (int idx = threadIdx.x; idx < TOT; idx += NT) {
+        const int c = idx / V, d0 = (idx % V) * E;
+        const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(dst + c * D + d0));
+        const int bytes = c < nvalid ? 16 : 0;                   // 0: the request writes zeros
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s),
+                     "l"(src + (size_t)min(c, max(nvalid - 1, 0)) * rs + d0), "r"(bytes)
+                     : "memory");
+    }
+}
+template <int R, int D, int SD, typename T, int NT>
+__device__ __forceinline__ void to_f32(const T *stage, float *dst) {
+    for (int idx = threadIdx.x; idx < R * D; idx += NT) dst[(idx / D) * SD + idx % D] = ldf1(stage[idx]);
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 }  // namespace wg

@@ -28,7 +28,8 @@
  *   - Sequence tensors are contiguous [B, T, H, d] (d fastest); the state
  *     tensors h0 / ht are contiguous [B, H, dv, dk] float32 (row = value
  *     channel, column = key channel).  Device pointers must be 16-byte
- *     aligned.
+ *     aligned, workspaces included (KDA_ERR_INVALID_ARG otherwise, where the
+ *     entry point reads its workspace with vector or asynchronous copies).
  *   - Calls are asynchronous on the given stream.  Argument errors are
  *     detected on the host before anything is launched and nothing is
  *     written; the return value says which.  Errors found on the device
