@@ -160,22 +160,28 @@ constexpr size_t prep_smem_bytes() {
     return sizeof(float) * ((size_t)4 * kC + 5 * kC * pad4(DK) + 2 * kC * pad4(DV) + 3 * kC * kSC4 + DK + kC);
 }
 
+// The two scans read each chunk's record tiles (and v or dO) through a ring of
+// kRing buffers filled by cp.async: chunk n computes while chunks n + 1 and n + 2
+// are in flight.
+constexpr int kRing = 3;
+
 // ------------------------------------------------------------------ kernel A
 // The forward state scan from the records: X = C - W S^T (kept for the
 // gradient kernel), S <- S Diag(gamma^C) + V^T K~ + X^T A~.
+template <int DK, typename Tin>
+__host__ __device__ constexpr int states_buf_floats() {
+    // W, K~, A~ [C][SK]; C slice [C][SV]; gamma^C [DK]; raw v rows [C][DVS] of Tin
+    return 3 * kC * pad4(DK) + kC * pad4(kDVS) + DK + (kC * kDVS * (int)sizeof(Tin) + 3) / 4;
+}
 template <int DK, int DV, typename Tin, bool TF32>
 __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS);
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), BUF = states_buf_floats<DK, Tin>();
     using R = BRec<DK, DV>;
     extern __shared__ float smem[];
-    float *Wm = smem;                    // [C][SK]
-    float *KG = Wm + kC * SK;
-    float *AG = KG + kC * SK;
-    float *Sm = AG + kC * SK;            // [DVS][SK]
-    float *Cs = Sm + kDVS * SK;          // [C][SV]
-    float *Vm = Cs + kC * SV;
-    float *Xm = Vm + kC * SV;
-    float *gam = Xm + kC * SV;           // [DK]
+    float *Sm = smem;                    // [DVS][SK]
+    float *Vm = Sm + kDVS * SK;          // [C][SV]
+    float *Xm = Vm + kC * SV;            // [C][SV]
+    float *ring = Xm + kC * SV;          // kRing x BUF
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -184,27 +190,41 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
     const size_t head = (size_t)b * H + h;
     float *Sws = p.ws_S + head * (size_t)(N + 1) * dv * DK;
     const float *recs = p.ws_prep + head * N * bwd_rec_floats(DK, DV);
+    auto issue = [&](int n) {
+        const float *rec = recs + (size_t)n * bwd_rec_floats(DK, DV);
+        float *bf = ring + (n % kRing) * BUF;
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::W, DK, bf);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::KG, DK, bf + kC * SK);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::AG, DK, bf + 2 * kC * SK);
+        wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, bf + 3 * kC * SK);
+        wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 3 * kC * SK + kC * SV);
+        wg::load_raw_async<kC, kDVS, Tin, kThreads>(v + (((size_t)b * T + n * kC) * H + h) * dv + e0, (size_t)H * dv,
+                                                    min(kC, T - n * kC),
+                                                    reinterpret_cast<Tin *>(bf + 3 * kC * SK + kC * SV + DK));
+    };
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         Sm[e * SK + d] = p.h0 ? p.h0[(head * dv + e0 + e) * DK + d] : 0.f;
     }
+    for (int n = 0; n < kRing - 1; ++n) {
+        if (n < N) issue(n);
+        wg::cp_async_commit();
+    }
     for (int n = 0; n < N; ++n) {
-        const int t0 = n * kC, nvalid = min(kC, T - t0);
-        const float *rec = recs + (size_t)n * bwd_rec_floats(DK, DV);
-        __syncthreads();
+        float *Wm = ring + (n % kRing) * BUF, *KG = Wm + kC * SK, *AG = KG + kC * SK, *Cs = AG + kC * SK;
+        float *gam = Cs + kC * SV;
+        const Tin *vraw = reinterpret_cast<const Tin *>(gam + DK);
+        __syncthreads();                 // S is final for chunk n; chunk n - 1's buffer is free
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
         }
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KG, DK, kC, KG);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::AG, DK, kC, AG);
-        wg::load_tile<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, kC, Cs);
-        wg::load_tile<kC, kDVS, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv, nvalid,
-                                              Vm);
-        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
+        if (n + kRing - 1 < N) issue(n + kRing - 1);
+        wg::cp_async_commit();           // (empty groups at the end keep the count)
+        wg::cp_async_wait<kRing - 1>();  // chunk n's copies (this thread's) have landed
         __syncthreads();
+        wg::to_f32<kC, kDVS, SV, Tin, kThreads>(vraw, Vm);
         float *xs = p.ws_x + ((head * N + n) * kC) * (size_t)dv + e0;
         wg::gemm16<kDVS, TF32>(
             DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
@@ -229,19 +249,20 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
 // ------------------------------------------------------------------ kernel B
 // The reverse scan from the records: dC = A~ dS^T + P_a^T dO (kept for the
 // gradient kernel), dS <- dS Diag(gamma^C) + dO^T Q<- - dC^T W.
+template <int DK, typename Tin>
+__host__ __device__ constexpr int dstate_buf_floats() {
+    // W, A~, Q<- [C][SK]; P_a [C][SC]; gamma^C [DK]; raw dO rows [C][DVS] of Tin
+    return 3 * kC * pad4(DK) + kC * kSC4 + DK + (kC * kDVS * (int)sizeof(Tin) + 3) / 4;
+}
 template <int DK, int DV, typename Tin, bool TF32>
 __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
+    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4, BUF = dstate_buf_floats<DK, Tin>();
     using R = BRec<DK, DV>;
     extern __shared__ float smem[];
-    float *Wm = smem;                    // [C][SK]
-    float *AG = Wm + kC * SK;
-    float *QL = AG + kC * SK;
-    float *dS = QL + kC * SK;            // [DVS][SK]
-    float *Pa = dS + kDVS * SK;          // [C][SC]
-    float *dO = Pa + kC * SC;            // [C][SV]
-    float *dC = dO + kC * SV;
-    float *gam = dC + kC * SV;           // [DK]
+    float *dS = smem;                    // [DVS][SK]
+    float *dO = dS + kDVS * SK;          // [C][SV]
+    float *dC = dO + kC * SV;            // [C][SV]
+    float *ring = dC + kC * SV;          // kRing x BUF
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
@@ -250,34 +271,52 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
     const size_t head = (size_t)b * H + h;
     float *dSws = p.ws_dS + head * (size_t)N * dv * DK;
     const float *recs = p.ws_prep + head * N * bwd_rec_floats(DK, DV);
+    // step i handles chunk N - 1 - i (the scan runs backwards)
+    auto issue = [&](int i) {
+        const int n = N - 1 - i;
+        const float *rec = recs + (size_t)n * bwd_rec_floats(DK, DV);
+        float *bf = ring + (i % kRing) * BUF;
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::W, DK, bf);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::AG, DK, bf + kC * SK);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::QL, DK, bf + 2 * kC * SK);
+        wg::load_tile_async<kC, kC, SC, kThreads>(rec + R::PA, kC, bf + 3 * kC * SK);
+        wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 3 * kC * SK + kC * SC);
+        wg::load_raw_async<kC, kDVS, Tin, kThreads>(dop + (((size_t)b * T + n * kC) * H + h) * dv + e0,
+                                                    (size_t)H * dv, min(kC, T - n * kC),
+                                                    reinterpret_cast<Tin *>(bf + 3 * kC * SK + kC * SC + DK));
+    };
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         dS[e * SK + d] = p.grad_ht ? p.grad_ht[(head * dv + e0 + e) * DK + d] : 0.f;
     }
-    for (int n = N - 1; n >= 0; --n) {
-        const int t0 = n * kC, nvalid = min(kC, T - t0);
-        const float *rec = recs + (size_t)n * bwd_rec_floats(DK, DV);
-        __syncthreads();
+    for (int i = 0; i < kRing - 1; ++i) {
+        if (i < N) issue(i);
+        wg::cp_async_commit();
+    }
+    for (int i = 0; i < N; ++i) {
+        const int n = N - 1 - i;
+        float *Wm = ring + (i % kRing) * BUF, *AG = Wm + kC * SK, *QL = AG + kC * SK, *Pa = QL + kC * SK;
+        float *gam = Pa + kC * SC;
+        const Tin *draw = reinterpret_cast<const Tin *>(gam + DK);
+        __syncthreads();                 // dS is final for chunk n; the previous step's buffer is free
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             dSws[((size_t)n * dv + e0 + e) * DK + d] = dS[e * SK + d];
         }
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::AG, DK, kC, AG);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::QL, DK, kC, QL);
-        wg::load_tile<kC, kC, SC, kThreads>(rec + R::PA, kC, kC, Pa);
-        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv,
-                                              nvalid, dO);
-        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
+        if (i + kRing - 1 < N) issue(i + kRing - 1);
+        wg::cp_async_commit();
+        wg::cp_async_wait<kRing - 1>();
+        __syncthreads();
+        wg::to_f32<kC, kDVS, SV, Tin, kThreads>(draw, dO);
         __syncthreads();
         float *dcs = p.ws_dc + ((head * N + n) * kC) * (size_t)dv + e0;
         wg::gemm16_2<kDVS, TF32>(
-            DK, [&](int i, int d) { return AG[i * SK + d]; }, [&](int d, int e) { return dS[e * SK + d]; }, kC,
-            [&](int i, int j) { return Pa[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
-            [&](int i, int e, float x) {
-                dC[i * SV + e] = x;
-                dcs[(size_t)i * dv + e] = x;
+            DK, [&](int r, int d) { return AG[r * SK + d]; }, [&](int d, int e) { return dS[e * SK + d]; }, kC,
+            [&](int r, int j) { return Pa[j * SC + r]; }, [&](int j, int e) { return dO[j * SV + e]; },
+            [&](int r, int e, float x) {
+                dC[r * SV + e] = x;
+                dcs[(size_t)r * dv + e] = x;
             });
         __syncthreads();
         wg::gemm2<DK, TF32>(
@@ -588,13 +627,13 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     }
 }
 
-template <int DK>
+template <int DK, typename Tin>
 constexpr size_t states_smem_bytes() {
-    return sizeof(float) * ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + 3 * kC * pad4(kDVS) + DK);
+    return sizeof(float) * ((size_t)kDVS * pad4(DK) + 2 * kC * pad4(kDVS) + kRing * states_buf_floats<DK, Tin>());
 }
-template <int DK>
+template <int DK, typename Tin>
 constexpr size_t dstate_smem_bytes() {
-    return sizeof(float) * ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + kC * kSC4 + 2 * kC * pad4(kDVS) + DK);
+    return sizeof(float) * ((size_t)kDVS * pad4(DK) + 2 * kC * pad4(kDVS) + kRing * dstate_buf_floats<DK, Tin>());
 }
 
 template <typename F>
@@ -607,7 +646,7 @@ cudaError_t launch_all(const DplrParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const int N = (p.T + kC - 1) / kC;
     cudaError_t e;
-    const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
+    const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK, Tin>(), sb = dstate_smem_bytes<DK, Tin>();
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
     static_assert(sizeof(float) * grad_smem_floats<128, 128>() <= 227 * 1024, "kernel C shared memory");
     if ((e = set_smem(dplr_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32>, sp)) != cudaSuccess) return e;
