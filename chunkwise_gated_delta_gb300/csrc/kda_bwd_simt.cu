@@ -407,6 +407,25 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
     const float *dS = p.ws_dS + (head * N + n) * (size_t)DV * DK;           // gradient of the state after
     const bool sv = p.scale_v != 0;
 
+    // The stored states stream through a ring of four tile buffers that are free until the
+    // state products below end (W, dQ<-, dK<-, dK->): slabs of 32 rows, in the order they are
+    // consumed -- S_prev slabs, then (dS, S_next) slab pairs -- by cp.async, the first four
+    // issued now so that they travel during the loads and the first product.
+    constexpr int NS = DV / kC, NL = 3 * NS;
+    float *ring[4] = {Wm, dKl, dQl, dKr};
+    auto slab_src = [&](int k) -> const float * {
+        if (k < NS) return Sp + (size_t)k * kC * DK;
+        return (((k - NS) & 1) ? Sn : dS) + (size_t)((k - NS) >> 1) * kC * DK;
+    };
+    int issued = 0;
+    auto issue_upto = [&](int end) {
+        for (; issued < end && issued < NL; ++issued) {
+            wg::load_tile_async<kC, DK, SK, kThreadsC>(slab_src(issued), DK, ring[issued & 3]);
+            wg::cp_async_commit();
+        }
+    };
+    issue_upto(4);
+
     // ---- loads: Gamma and the rescaled tiles, v, dO, beta
     load_rescaled_par<DK, SK, Tin, Tg, kThreadsC>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, dbeta);
     load_beta<Tin>(p, b, h, t0, nvalid, beta);
@@ -416,14 +435,13 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
         wg::load_tile<kC, DV, SV, kThreadsC>(dop + r0, rs, nvalid, dO);
     }
     __syncthreads();
-    // ---- A~, P, N, W and U from the chunk record
+    // ---- A~, P and N from the chunk record
     {
         using R = Rec<DK, DV>;
         const float *rec = p.ws_prep + (head * N + n) * rec_floats(DK, DV);
         wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::A, kC, kC, Am);
         wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::P, kC, kC, Pm);
         wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::N, kC, kC, Nm);
-        wg::load_tile<kC, DK, SK, kThreadsC>(rec + R::W, DK, kC, Wm);
         // V_new and dU of this chunk, from the two scans
         wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_vnew + (head * N + n) * (size_t)kC * DV, DV, kC, Vn);
         wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_du + (head * N + n) * (size_t)kC * DV, DV, kC, dU);
@@ -436,35 +454,39 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
     __syncthreads();
     // ---- dW = -dU S_prev ; dQ<- = dO S_prev + (dO V_new^T * M) K-> ;
     //      dK-> = V_new dS Diag(gamma^C) + (dO V_new^T * M)^T Q<- ; and diag(S_next^T dS)
-    //      for the gamma^C row.  The stored states stream through shared memory 32
-    //      rows at a time (16-byte loads into the dK<- tile, free until A~^T dW).
+    //      for the gamma^C row, from the slab ring.  A unit consumes slabs a..bl; before it,
+    //      the buffers of every earlier slab are free, so slabs up to a + 3 may be in flight.
     {
         constexpr int NT = wg::ntiles<DK, 16>();
         int r0, c0;
         wg::origin<DK, 16>(r0, c0);
         float aW[NT][4] = {}, aQ[NT][4] = {}, aK[NT][4] = {}, aK2[NT][4] = {};
-        float *slab = dKl;
-        for (int s0 = 0; s0 < DV; s0 += kC) {
-            wg::load_tile<kC, DK, SK, kThreadsC>(Sp + (size_t)s0 * DK, DK, kC, slab);
-            __syncthreads();
-            auto bS = [&](int e, int d) { return slab[e * SK + d]; };
-            wg::tile<NT, TF32>(aW, r0, c0, kC, [&](int i, int e) { return dU[i * SV + s0 + e]; }, bS);
-            wg::tile<NT, TF32>(aQ, r0, c0, kC, [&](int i, int e) { return dO[i * SV + s0 + e]; }, bS);
-            __syncthreads();
-        }
         float last = 0.f;                  // diag(S_next^T dS), column tid
-        for (int s0 = 0; s0 < DV; s0 += kC) {
-            wg::load_tile<kC, DK, SK, kThreadsC>(dS + (size_t)s0 * DK, DK, kC, slab);
-            float sn[kC];
-            if (tid < DK)
-#pragma unroll
-                for (int e = 0; e < kC; ++e) sn[e] = Sn[(size_t)(s0 + e) * DK + tid];
+        for (int u = 0; u < 2 * NS; ++u) {
+            const int a = u < NS ? u : NS + 2 * (u - NS), bl = u < NS ? a : a + 1;
+            issue_upto(a + 4);
+            switch (issued - 1 - bl) {     // this thread's copies of slabs <= bl have landed
+                case 0: wg::cp_async_wait<0>(); break;
+                case 1: wg::cp_async_wait<1>(); break;
+                case 2: wg::cp_async_wait<2>(); break;
+                default: wg::cp_async_wait<3>(); break;
+            }
             __syncthreads();
-            wg::tile<NT, TF32>(aK, r0, c0, kC, [&](int i, int e) { return Vn[i * SV + s0 + e]; },
-                               [&](int e, int d) { return slab[e * SK + d]; });
-            if (tid < DK)
-#pragma unroll
-                for (int e = 0; e < kC; ++e) last += sn[e] * slab[e * SK + tid];
+            if (u < NS) {
+                const int s0 = u * kC;
+                const float *slab = ring[a & 3];
+                auto bS = [&](int e, int d) { return slab[e * SK + d]; };
+                wg::tile<NT, TF32>(aW, r0, c0, kC, [&](int i, int e) { return dU[i * SV + s0 + e]; }, bS);
+                wg::tile<NT, TF32>(aQ, r0, c0, kC, [&](int i, int e) { return dO[i * SV + s0 + e]; }, bS);
+            } else {
+                const int s0 = (u - NS) * kC;
+                const float *dsl = ring[a & 3], *snl = ring[(a + 1) & 3];
+                wg::tile<NT, TF32>(aK, r0, c0, kC, [&](int i, int e) { return Vn[i * SV + s0 + e]; },
+                                   [&](int e, int d) { return dsl[e * SK + d]; });
+                if (tid < DK)
+#pragma unroll 4
+                    for (int e = 0; e < kC; ++e) last += snl[e * SK + tid] * dsl[e * SK + tid];
+            }
             __syncthreads();
         }
         if (tid < DK) lastrow[tid] = last;
