@@ -62,6 +62,9 @@ struct DRec {
     static_assert(dplr_rec_floats(DK, DV) == (size_t)GC + DK && dplr_rec_floats(DK, DV) % 4 == 0, "record");
 };
 
+template <int DK>
+__host__ __device__ constexpr bool prep_aliases() { return 3 * kC * pad4(kC) <= kC * pad4(DK); }
+
 // One CTA per (chunk, head, batch).  Products run as warp-tiled 32 x N blocks
 // (warp_gemm.cuh): tf32 tensor-core MMAs for bf16 inputs (TF32), exact float32
 // for float32 inputs.
@@ -71,6 +74,11 @@ dplr_fwd_prep_kernel(const DplrParams p) {
     constexpr int SK = pad4(DK), SC = pad4(kC), SV = pad4(DV);
     using R = DRec<DK, DV>;
     extern __shared__ float smem[];
+    // Where three C x C tiles fit a key-wide tile (dk = 128), tiles that die early hand their
+    // space on, so two CTAs fit an SM for dv <= 128: Gamma's tile holds three Gram tiles once
+    // the rescaled tiles exist, and K->'s holds E, the inverse's scratch and M1 once the K~
+    // and A~ records are written.
+    constexpr bool kAlias = prep_aliases<DK>();
     float4 *rows = reinterpret_cast<float4 *>(smem);   // [C] eq. (4) data per row (clip)
     float *Gm = smem + 4 * kC;        // [C][SK]  raw gate, then Gamma
     float *Ql = Gm + kC * SK;         // [C][SK]
@@ -78,15 +86,16 @@ dplr_fwd_prep_kernel(const DplrParams p) {
     float *Ar = Kr + kC * SK;         // [C][SK]
     float *Bl = Ar + kC * SK;         // [C][SK]
     float *Vm = Bl + kC * SK;         // [C][SV]
-    float *Lab = Vm + kC * SV;        // [C][SC]  B<- A->^T * M_{-1}
+    float *Pa = Vm + kC * SV;         // [C][SC]  Q<- A->^T * M
+    float *gam = Pa + kC * SC;        // [DK]
+    float *gsc = gam + DK;            // [C]
+    float *extra = gsc + kC;          // 6 x [C][SC] when the tiles do not alias
+    float *Lab = kAlias ? Gm : extra; // [C][SC]  B<- A->^T * M_{-1}   (Gamma's tile, after the rescaling)
     float *Lbk = Lab + kC * SC;       // [C][SC]  B<- K->^T * M_{-1}
     float *Pk = Lbk + kC * SC;        // [C][SC]  Q<- K->^T * M
-    float *Pa = Pk + kC * SC;         // [C][SC]  Q<- A->^T * M
-    float *Em = Pa + kC * SC;         // [C][SC]  E
+    float *Em = kAlias ? Kr : Pk + kC * SC;   // [C][SC]  E           (K->'s tile, after the records)
     float *Ts = Em + kC * SC;         // [C][SC]  scratch of the inverse, then P_a E
     float *M1 = Ts + kC * SC;         // [C][SC]  E (B<- K->^T * M_{-1})
-    float *gam = M1 + kC * SC;        // [DK]
-    float *gsc = gam + DK;            // [C]
 
     const int tid = threadIdx.x;
     const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -158,7 +167,8 @@ dplr_fwd_prep_kernel(const DplrParams p) {
 
 template <int DK, int DV>
 constexpr size_t prep_smem_bytes() {
-    return sizeof(float) * (size_t)(4 * kC + 5 * kC * pad4(DK) + kC * pad4(DV) + 7 * kC * pad4(kC) + DK + kC);
+    return sizeof(float) * (size_t)(4 * kC + 5 * kC * pad4(DK) + kC * pad4(DV) + kC * pad4(kC) + DK + kC +
+                                    (prep_aliases<DK>() ? 0 : 6 * kC * pad4(kC)));
 }
 
 // One CTA per (32-wide value slice, head, batch): the serial scan over the
