@@ -225,3 +225,26 @@ def test_dplr_bwd_rejects_bad_arguments_before_launch(lib, over, code):
 
 def test_dplr_fwd_rejects_unknown_flags(lib):
     assert lib.dplr_chunk_fwd(ctypes.byref(_dplr_args(flags=4)), None) == _lib.KDA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- workspace alignment
+MISALIGNED = (1 << 40) + 40 * (1 << 32) + 8       # 8-byte aligned only, clear of every other fake pointer
+
+
+def test_fwd_records_need_an_aligned_workspace(lib):
+    """With room for the chunk records the forward copies them asynchronously: 16-byte alignment."""
+    need = lib.kda_chunk_fwd_workspace(ctypes.byref(_args()))
+    assert need > 256                                   # bf16 KDA: status word plus records
+    assert _call(lib, _args(workspace=MISALIGNED, workspace_bytes=need)) == _lib.KDA_ERR_INVALID_ARG
+    # GLA (flags cleared, no beta) keeps the single kernel: no records
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(flags=0, beta=None))) == 256
+
+
+def test_bwd_and_dplr_need_an_aligned_workspace(lib):
+    a = _bwd_args(workspace=MISALIGNED)
+    a.workspace_bytes = lib.kda_chunk_bwd_workspace(ctypes.byref(_bwd_args()))
+    assert lib.kda_chunk_bwd(ctypes.byref(a), None) == _lib.KDA_ERR_INVALID_ARG
+    d = _dplr_args(workspace=MISALIGNED, workspace_bytes=1 << 31)
+    assert lib.dplr_chunk_fwd(ctypes.byref(d), None) == _lib.KDA_ERR_INVALID_ARG
+    e = _dplr_bwd_args(workspace=MISALIGNED)
+    assert lib.dplr_chunk_bwd(ctypes.byref(e), None) == _lib.KDA_ERR_INVALID_ARG
