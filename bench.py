@@ -12,7 +12,9 @@ call per step; the line also carries the transition-norm report).
 
 --impl ours (default): the CUDA library through its C ABI.  `value` is tokens/s
 with the inputs resident in HBM; `e2e` is the same metric with pinned host
-inputs copied in and o / ht copied out inside the timed region; `roofline`
+inputs copied in and o / ht copied out inside the timed region, every step
+(the host runner overlaps one step's copies with the previous step's call on
+separate streams, as a serving loop would); `roofline`
 compares the kernel's algorithmic bytes per launch against the measured HBM
 copy bandwidth; `cpu_baseline` times the float64 oracle on a bounded sample
 of the same workload on the host cores.
@@ -387,8 +389,10 @@ def run_ours(args, rank, world, local):
     if not args.no_e2e:
         runner = HostRunner(x, device=dev, scale_v=x["scale_v"], gate=gate,
                             kind=kind_of(w) if kind_of(w) in ("dplr", "kda_bwd", "dplr_bwd") else "kda")
+        runner.begin(stream)
         for _ in range(max(3, min(args.warmup, 10))):
             runner.run(stream)
+        runner.finish(stream)
         torch.cuda.synchronize()
         e2e_steps = max(3, min(args.steps, 50))
         barrier(world)
@@ -396,8 +400,10 @@ def run_ours(args, rank, world, local):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        runner.begin(stream)            # the copy streams start after e0 ...
         for _ in range(e2e_steps):
-            runner.run(stream)
+            runner.run(stream)          # every step copies its inputs in and its results out
+        runner.finish(stream)           # ... and e1 waits for the last read-back
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps

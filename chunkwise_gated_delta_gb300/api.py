@@ -370,62 +370,103 @@ def gla_fwd(q, k, v, g, h0=None, **kw):
 
 
 class HostRunner:
-    """End-to-end call from pinned host buffers.
+    """End-to-end calls from pinned host buffers, pipelined across calls.
 
     Each :meth:`run` copies the inputs host->device, runs the call
     (``kda_chunk_fwd``; ``dplr_chunk_fwd`` when ``kind="dplr"``;
     ``kda_chunk_bwd`` / ``dplr_chunk_bwd`` when ``kind="kda_bwd"`` / ``"dplr_bwd"``) and copies its results back
-    device->host (o and ht, or every gradient), all on one stream.  Device
-    buffers are allocated once and reused.
+    device->host (o and ht, or every gradient).  Copies in run on one stream,
+    the call on the caller's stream, copies out on a third, and ``depth`` sets
+    of device buffers rotate between calls, so the inputs of one call travel
+    while the previous call computes and its results drain; events keep each
+    set's copies, call and read-back in order.  Bracket a run of calls with
+    :meth:`begin` and :meth:`finish` to order the copy streams after, and the
+    caller's stream after, everything they do.  Every call still copies all of
+    its inputs in and all of its results out.
     """
 
     _INPUTS = ("q", "k", "v", "g", "beta", "h0", "a", "b", "do", "dht")
 
-    def __init__(self, host: dict, device="cuda", scale_v=True, gate=None, kind="kda"):
+    def __init__(self, host: dict, device="cuda", scale_v=True, gate=None, kind="kda", depth=2):
         if kind not in ("kda", "dplr", "kda_bwd", "dplr_bwd"):
             raise ValueError(f"unknown kind {kind}")
         self.host = {k: v.pin_memory() for k, v in host.items() if k in self._INPUTS and isinstance(v, torch.Tensor)}
-        self.dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()}
-        q = self.dev["q"]
-        B, T, H, dk = q.shape
-        dv = self.dev["v"].shape[-1]
         self.scale_v, self.gate, self.kind = scale_v, gate, kind
-        if kind in ("kda_bwd", "dplr_bwd"):
-            d = self.dev
-            self.outs = {"dq": torch.empty_like(q), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
-                         "dh0": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
-            if "g" in d:
-                self.outs["dg"] = torch.empty_like(d["g"])
-            if "beta" in d and kind == "kda_bwd":
-                self.outs["dbeta"] = torch.empty_like(d["beta"])
-            if kind == "dplr_bwd":
-                self.outs["da"], self.outs["db"] = torch.empty_like(d["a"]), torch.empty_like(d["b"])
+        self.sets = [self._buffers(device) for _ in range(max(1, depth))]
+        self.outs_host = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in self.sets[0][1].items()}
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.sets[0][0].values())
+        self.d2h_bytes = sum(v.numel() * v.element_size() for v in self.sets[0][1].values())
+        self.copy_in = torch.cuda.Stream(device=device)
+        self.copy_out = torch.cuda.Stream(device=device)
+        ev = lambda: [torch.cuda.Event() for _ in self.sets]
+        self.ev_ready, self.ev_done, self.ev_drained = ev(), ev(), ev()
+        self.calls = 0
+
+    def _buffers(self, device):
+        dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()}
+        q = dev["q"]
+        B, T, H, dk = q.shape
+        dv = dev["v"].shape[-1]
+        if self.kind in ("kda_bwd", "dplr_bwd"):
+            outs = {"dq": torch.empty_like(q), "dk": torch.empty_like(dev["k"]), "dv": torch.empty_like(dev["v"]),
+                    "dh0": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
+            if "g" in dev:
+                outs["dg"] = torch.empty_like(dev["g"])
+            if "beta" in dev and self.kind == "kda_bwd":
+                outs["dbeta"] = torch.empty_like(dev["beta"])
+            if self.kind == "dplr_bwd":
+                outs["da"], outs["db"] = torch.empty_like(dev["a"]), torch.empty_like(dev["b"])
         else:
-            self.outs = {"o": torch.empty(B, T, H, dv, dtype=q.dtype, device=device),
-                         "ht": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
-        self.outs_host = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in self.outs.items()}
-        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.dev.values())
-        self.d2h_bytes = sum(v.numel() * v.element_size() for v in self.outs.values())
+            outs = {"o": torch.empty(B, T, H, dv, dtype=q.dtype, device=device),
+                    "ht": torch.empty(B, H, dv, dk, dtype=torch.float32, device=device)}
+        return dev, outs
+
+    def begin(self, stream=None):
+        """Order the copy streams after everything already on ``stream``."""
+        stream = stream or torch.cuda.current_stream()
+        self.copy_in.wait_stream(stream)
+        self.copy_out.wait_stream(stream)
+
+    def finish(self, stream=None):
+        """Order ``stream`` after every copy issued so far; returns the host results of the last call."""
+        stream = stream or torch.cuda.current_stream()
+        stream.wait_stream(self.copy_in)
+        stream.wait_stream(self.copy_out)
+        return self.outs_host
 
     def run(self, stream=None):
         stream = stream or torch.cuda.current_stream()
-        with torch.cuda.stream(stream):
-            for k, v in self.dev.items():
+        i = self.calls % len(self.sets)
+        reuse = self.calls >= len(self.sets)
+        self.calls += 1
+        d, outs = self.sets[i]
+        with torch.cuda.stream(self.copy_in):
+            if reuse:
+                self.copy_in.wait_event(self.ev_done[i])         # the last call on this set has read it
+            for k, v in d.items():
                 v.copy_(self.host[k], non_blocking=True)
-            d = self.dev
+            self.ev_ready[i].record(self.copy_in)
+        stream.wait_event(self.ev_ready[i])
+        if reuse:
+            stream.wait_event(self.ev_drained[i])                 # its results have been copied out
+        with torch.cuda.stream(stream):
             if self.kind == "dplr":
                 dplr_chunk_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"),
-                               gate=self.gate, o=self.outs["o"], ht=self.outs["ht"], stream=stream)
+                               gate=self.gate, o=outs["o"], ht=outs["ht"], stream=stream)
             elif self.kind == "dplr_bwd":
                 dplr_chunk_bwd(d["q"], d["k"], d["v"], d["a"], d["b"], d.get("g"), d.get("h0"), d["do"],
-                               d.get("dht"), gate=self.gate, grads=self.outs, stream=stream)
+                               d.get("dht"), gate=self.gate, grads=outs, stream=stream)
             elif self.kind == "kda_bwd":
                 kda_chunk_bwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), d["do"],
-                              d.get("dht"), gate=self.gate, scale_v=self.scale_v, grads=self.outs, stream=stream)
+                              d.get("dht"), gate=self.gate, scale_v=self.scale_v, grads=outs, stream=stream)
             else:
                 kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"),
-                              gate=self.gate, scale_v=self.scale_v, o=self.outs["o"], ht=self.outs["ht"],
+                              gate=self.gate, scale_v=self.scale_v, o=outs["o"], ht=outs["ht"],
                               stream=stream)
-            for k, v in self.outs.items():
+            self.ev_done[i].record(stream)
+        with torch.cuda.stream(self.copy_out):
+            self.copy_out.wait_event(self.ev_done[i])
+            for k, v in outs.items():
                 self.outs_host[k].copy_(v, non_blocking=True)
+            self.ev_drained[i].record(self.copy_out)
         return self.outs_host
