@@ -68,85 +68,17 @@ __device__ void row_rho(const DplrParams &p, int b, int h, int t0, int nvalid, f
     }
 }
 
-// The (optionally clipped) log-decay of token row `row` (flattened (b, t, h)), channel d.
-template <typename Tg>
-__device__ __forceinline__ float gate_of(const DplrParams &p, size_t row, int d, int dk, const float4 *rows, int c) {
-    const Tg *g = static_cast<const Tg *>(p.g);
-    float gv = 0.f;
-    if (p.gate_kind == KDA_GATE_CHANNEL) gv = ldf(g, row * dk + d);
-    else if (p.gate_kind == KDA_GATE_SCALAR) gv = ldf(g, row);
-    if (p.clip) gv = fminf(gv, rows[c].w);
-    return gv;
-}
 
-// Gamma and the rescaled tiles of one chunk, one key channel per thread
-// (rows past nvalid are zero, Gamma held at its last value); any tile pointer
-// may be null; gam[d] = gamma^C.  `rows` comes from row_rho when p.clip is set
-// (a barrier must separate the two).
-template <int DK, int C, typename Tin, typename Tg>
-__device__ void load_rescaled(const DplrParams &p, int b, int h, int t0, int nvalid, const float4 *rows, float *Gm,
-                              float *Ql, float *Kr, float *Ar, float *Bl, float *gam) {
-    constexpr int SK = DK + 1;
-    const Tin *q = static_cast<const Tin *>(p.q);
-    const Tin *k = static_cast<const Tin *>(p.k);
-    const Tin *a = static_cast<const Tin *>(p.a);
-    const Tin *bb = static_cast<const Tin *>(p.b);
-    for (int d = threadIdx.x; d < DK; d += blockDim.x) {
-        float G = 0.f, gm = 1.f;
-        for (int c = 0; c < C; ++c) {
-            float qv = 0.f, kv = 0.f, av = 0.f, bv = 0.f;
-            if (c < nvalid) {
-                const size_t row = ((size_t)b * p.T + t0 + c) * p.H + h;
-                if (Ql) qv = ldf(q, row * DK + d);
-                if (Kr) kv = ldf(k, row * DK + d);
-                if (Ar) av = ldf(a, row * DK + d);
-                if (Bl) bv = ldf(bb, row * DK + d);
-                G += gate_of<Tg>(p, row, d, DK, rows, c);
-                gm = expf(G);
-            }
-            if (Gm) Gm[c * SK + d] = gm;
-            if (Ql) Ql[c * SK + d] = qv * gm;
-            if (Kr) Kr[c * SK + d] = kv / gm;
-            if (Ar) Ar[c * SK + d] = av / gm;
-            if (Bl) Bl[c * SK + d] = bv * gm;
-        }
-        gam[d] = gm;
-    }
-}
 
-// E = (I + (B<- A->^T * M_{-1}))^{-1}: the strict-lower Gram into Nm, then
-// forward substitution, one column per thread of the first warp.  Starts and
-// ends with a barrier.
-template <int DK, int C>
-__device__ void inverse_e(const float *Bl, const float *Ar, float *Nm, float *Em) {
-    constexpr int SK = DK + 1, SC = C + 1;
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
-        const int i = idx / C, j = idx % C;
-        float acc = 0.f;
-        if (j < i)
-            for (int d = 0; d < DK; ++d) acc += Bl[i * SK + d] * Ar[j * SK + d];
-        Nm[i * SC + j] = acc;
-    }
-    __syncthreads();
-    if (threadIdx.x < C) {
-        const int c = threadIdx.x;
-        for (int i = 0; i < C; ++i) {
-            float y = 0.f;
-            if (i == c) y = 1.f;
-            else if (i > c)
-                for (int j = c; j < i; ++j) y -= Nm[i * SC + j] * Em[j * SC + c];
-            Em[i * SC + c] = y;
-        }
-    }
-    __syncthreads();
-}
 
-// load_rescaled with all threads loading the raw tiles first (16-byte vector
-// loads, 256 threads), then one thread per key channel running the cumsum down
-// its column in shared memory.  Gm is required here (it holds the raw gate in
-// between); Ql, Kr, Ar, Bl may be null; gsc holds C floats (scalar gates).
-// Contains one barrier; the caller synchronises before reading the tiles.
+// Gamma and the rescaled tiles of one chunk (rows past nvalid zero, Gamma held
+// at its last value; gam[d] = gamma^C): all threads load the raw tiles first
+// (16-byte vector loads, 256 threads), then one thread per key channel runs the
+// (optionally clipped) cumsum down its column in shared memory.  Gm is required
+// (it holds the raw gate in between); Ql, Kr, Ar, Bl may be null; gsc holds C
+// floats (scalar gates); `rows` comes from row_rho when p.clip is set (a
+// barrier must separate the two).  Contains one barrier; the caller
+// synchronises before reading the tiles.
 template <int DK, int SK, int C, typename Tin, typename Tg>
 __device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int nvalid, const float4 *rows,
                                   float *Gm, float *Ql, float *Kr, float *Ar, float *Bl, float *gam, float *gsc) {

@@ -38,15 +38,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait on phase `parity`.  Each try_wait already suspends the thread
-// for a hardware-defined window, so the bound is generous in time.  Returns
-// false when the bound ran out; the caller records the error and unwinds.
+// Iterations of try_wait a bounded wait takes before it gives up.  Each try_wait
+// already suspends the thread for a hardware-defined window, so the bound is
+// generous in time; the kernels' wait helpers then record the error and unwind.
 constexpr uint32_t kWaitBound = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitBound; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
 
 // Cluster-scope wait: used on barriers that the peer CTA of a cluster
 // completes (remote arrive or a bulk copy into this CTA's shared memory).
@@ -88,23 +83,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_remote, const voi
             dst_remote),
         "r"(smem_u32(src)), "r"(bytes), "r"(bar_remote)
         : "memory");
-}
-// Stores into another CTA's shared memory (address from map_to_rank).
-__device__ __forceinline__ void st_cluster_u128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-__device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint32_t a, uint32_t b) {
-    asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
-}
-// Orders this thread's generic-proxy writes to cluster shared memory before
-// later async-proxy (tensor core) reads of them.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-// Arrive on a barrier of another CTA, releasing this thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 // Arrive on another CTA's barrier and raise its expected transaction bytes
 // (relaxed: the bytes themselves are published by the bulk copies).
@@ -201,23 +179,7 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                      smem_u32(bar))
                  : "memory");
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 32 bit, 16 consecutive columns, followed by the wait in the same
-// asm statement so no use of the registers can be scheduled before the data
-// has arrived.  Thread i of the warp gets lane (base lane + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
-    uint32_t *u = reinterpret_cast<uint32_t *>(r);
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-        "%14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
-          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
-        : "r"(taddr)
-        : "memory");
-}
 
 // 32 lanes x 32 bit, 32 consecutive columns (load and wait in one statement).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
