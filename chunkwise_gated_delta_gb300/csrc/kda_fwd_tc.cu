@@ -1,10 +1,9 @@
-// Fused tcgen05 kernel for the chunkwise KDA forward (bf16 in, fp32 accumulate,
+// tcgen05 kernels for the chunkwise KDA forward (bf16 in, fp32 accumulate,
 // fp32 state), GB300 / sm_103a.
 //
-// One CTA owns one (batch, head, 64-wide value slice) and walks its chunks in
-// order.  The chunk form it evaluates is the one recapped on page "Kimi Delta
-// Attention backward" ("forward recap"), regrouped so every tensor-core
-// product has M = 128 rows:
+// The chunk form evaluated is the one recapped on page "Kimi Delta Attention
+// backward" ("forward recap"), regrouped so every tensor-core product has
+// M = 128 rows:
 //
 //   [beta K<- ; Q<-] K->^T      = [L ; P]          (Gram, one MMA)
 //   Z' (I + L_{strict}) = [I ; P],  Z = Z' Diag(beta) = [T ; P T]
@@ -21,28 +20,25 @@
 // is why the output rides in the lower half of the state-dependent product;
 // the state step uses the factored form of page "Gated Linear Attention" 5.2.
 //
-// Warp roles (384 threads):
-//   warps 0-3  "chain": the serial part -- the state S^T (128 key channels x
-//              64 values) in fp32 registers, one key channel per thread.
-//   warps 4-11 "WY": everything that does not depend on S.
-//
 // Two forms.
-//   Records (two kernels, when the caller's workspace holds them): a
-//   chunk-parallel kernel computes, for every chunk, Gamma, the rescaled tiles
-//   and Z -- the Gram, the inverse and the back-substitution, which dominate
-//   the state-independent work -- and writes them as a chunk record (the bf16
-//   tile images Z, Q<-, K<-, K-> and gamma^C).  The scan kernel then runs one
-//   CTA per (batch, head, 64-wide value slice); its WY warps only form
-//   [W ; P W] = Z K<-, [U ; P U] = Z V and A_chain, with Z and K<- double
-//   buffered, while the chain warps load Q<- (into A_chain's slot), K-> and
-//   gamma^C two chunks ahead.
-//   Single kernel (a 256-byte workspace): the WY warps build Z themselves.
-//   With dv = 128 the two value-slice CTAs of a head form a cluster and split
-//   that work by chunk parity: CTA r builds the chunks n with n % 2 == r and
-//   copies their slot tiles (A_chain, K->, gamma^C) and Z into the other CTA's
-//   shared memory; each CTA still runs the state scan of every chunk for its
-//   own value slice and forms its own [U ; P U] = Z V.  With dv = 64 one CTA
-//   does it all.
+//   Records (two kernels, when the caller's workspace holds them): the
+//   chunk-parallel Z kernel computes, for every chunk, Gamma, the rescaled
+//   tiles, Z, [W ; P W] and A_chain = [-W ; Q<- - P W] -- everything that
+//   does not depend on the state -- and writes the bf16 tile images of Z,
+//   A_chain and K-> and gamma^C as the chunk's record.  The record scan
+//   kernel then runs one CTA per (batch, head, 64-wide value slice) and takes
+//   three products per chunk (Z V, A_chain S^T, K->^T V_new).
+//   Single kernel (a 256-byte workspace, and GLA, which has no inverse): one
+//   CTA per (batch, head, 64-wide value slice) walks its chunks in order with
+//   two warp roles (384 threads): warps 0-3 "chain", the serial part -- the
+//   state S^T (128 key channels x 64 values) in fp32 registers, one key
+//   channel per thread; warps 4-11 "WY", everything that does not depend on
+//   S, Z included.  With dv = 128 the two value-slice CTAs of a head form a
+//   cluster and split the WY work by chunk parity: CTA r builds the chunks n
+//   with n % 2 == r and copies their slot tiles (A_chain, K->, gamma^C) and Z
+//   into the other CTA's shared memory; each CTA still runs the state scan of
+//   every chunk for its own value slice and forms its own [U ; P U] = Z V.
+//   With dv = 64 one CTA does it all.
 //
 // Warps reach every aligned instruction (bar.sync, tcgen05.ld) converged: each
 // block that only the issuing thread runs is followed by __syncwarp().
@@ -108,11 +104,11 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // bytes one CTA of a pair sends the other per chunk it builds: Z (st.async) and the slot tiles
 // (bulk copies)
 constexpr uint32_t kPushBytes = 16384 + 32768 + 16384 + 512;
-// One chunk's record (Z kernel -> scan kernel): images of the bf16 tiles the scan kernel reads.
-constexpr uint32_t REC_Z = 0;            // Z, K-major 128 x 64
-constexpr uint32_t REC_Q = 16384;        // Q<-, 64 x 128 (rows 64-127 of the A_G tile)
-constexpr uint32_t REC_KL = 32768;       // K<-, MN-major 64 x 128
-constexpr uint32_t REC_KR = 49152;       // K->, 64 x 128 (the slot tile)
+// One chunk's record (Z kernel -> record scan kernel): images of the bf16 tiles whose
+// products the scan forms, plus gamma^C.
+constexpr uint32_t REC_Z = 0;            // Z = [T ; P T], K-major 128 x 64 (A of Z V)
+constexpr uint32_t REC_A = 16384;        // A_chain = [-W ; Q<- - P W], K-major 128 x 128 (A of A_chain S^T)
+constexpr uint32_t REC_KR = 49152;       // K->, 64 x 128 (MN-major A of K->^T V_new)
 constexpr uint32_t REC_GC = 65536;       // gamma^C [128] f32
 constexpr uint32_t kRecBytes = 66048;
 
@@ -126,7 +122,7 @@ constexpr uint32_t kTmemCols = 512;
 // mbarrier indices
 enum {
     B_RAW = 0, B_V0, B_V1, B_GRAM, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
-    B_RX, B_PFREE, B_FIN0, B_FIN1, B_ZK0, B_ZK1, B_SL0, B_SL1, kNumBars
+    B_RX, B_PFREE, B_FIN0, B_FIN1, kNumBars
 };
 static_assert(kNumBars <= 24, "mbarrier slots");
 
@@ -300,8 +296,10 @@ __device__ __forceinline__ void frag_c_to_a(const float (&x)[2][4], uint32_t (&a
 // (4 columns) come back for the chunk's slot.  Rows at or past `live_rows`
 // are zero; `bet` and `gs` hold the chunk's beta and scalar gate.  The 256 WY
 // threads (index wt), 4 columns x 8 rows each; one barrier inside.
-//   With `rec` non-null, Q<-, K<-, K-> and gamma^C also go to that chunk record.
-template <int GATE, bool GRAM, bool SCAN>
+//   REC (the Z kernel of the record form): A_G rows 0-63 get K<- itself (beta is
+// applied to the rows of L instead, so the tile is also the B operand of Z K<-),
+// and K-> and gamma^C go straight to the chunk record `rec`.
+template <int GATE, bool GRAM, bool SCAN, bool REC = false>
 __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int wt, int live_rows, const float *bet,
                                               const float *gs, float *tot, uint2 (&krv)[8], float4 &gcv,
                                               uint8_t *rec = nullptr) {
@@ -337,7 +335,7 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
         }
     }
     gcv = make_float4(__expf(all[0]), __expf(all[1]), __expf(all[2]), __expf(all[3]));
-    if (rec && rg == 0) *reinterpret_cast<float4 *>(rec + REC_GC + 4 * col) = gcv;
+    if (REC && rg == 0) *reinterpret_cast<float4 *>(rec + REC_GC + 4 * col) = gcv;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         const int row = rg * 8 + r;
@@ -347,7 +345,7 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
         const float4 q4 = live ? ld_bf16x4(base + OFF_AG + obot) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 k4 = live ? ld_bf16x4(base + kraw + o64) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-        const float bb = bet[row];
+        const float bb = REC ? 1.f : bet[row];
         float kl[4], kr4[4], ql[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -363,11 +361,7 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
         if (GRAM) st_u64(base + OFF_KR + o64, kr);
         if (SCAN) st_u64(base + OFF_KL + o64, pack4(kl[0], kl[1], kl[2], kl[3]));
         krv[r] = kr;
-        if (rec) {
-            st_u64(rec + REC_Q + o64, pack4(ql[0], ql[1], ql[2], ql[3]));
-            st_u64(rec + REC_KL + o64, pack4(kl[0], kl[1], kl[2], kl[3]));
-            st_u64(rec + REC_KR + o64, kr);
-        }
+        if (REC) st_u64(rec + REC_KR + o64, kr);
     }
 }
 
@@ -378,8 +372,12 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
 // barrier that follows their stores of the rescaled tiles; `ph` is the parity
 // of the Gram barrier.  Returns the first of the 16 Z rows this warp wrote;
 // ends without a barrier.
-template <bool GLA>
-__device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph) {
+//   REC: rows 0-63 of the Gram are K<- K->^T (A_G holds K<-, not beta K<-), so
+// beta scales them as they leave TMEM; the inverses of the diagonal blocks go
+// to `yfrag` (4 KB) in the order of the MMA B fragments that read them, and
+// A_G is left alone.
+template <bool GLA, bool REC = false>
+__device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, float *yfrag = nullptr) {
     uint8_t *base = c.base;
     const int ww = wt >> 5, lane = wt & 31;
     const int quarter = ww & 3, half = ww >> 2;
@@ -408,6 +406,11 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph) {
         if (quarter < 2) {
             float v[32];
             tmem_ld32(c.tmem + TM_G + lane_base + half * 32, v);
+            if (REC) {
+                const float br = bet[row];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] *= br;
+            }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int col = half * 32 + 4 * q;
@@ -439,10 +442,20 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph) {
                     }
                 }
                 const int o = quarter * 32 + seg * 16;
+                if (REC) {
+                    // element (r, cc) of block bb is entry (r >> 2) & 1 of lane 4 (cc & 7) + (r & 3)
+                    // in the fragment of (bb, k-step r >> 3, column half cc >> 3)
+                    const int bb = o >> 4;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    *reinterpret_cast<float4 *>(sc.Y(row, o + 4 * c4)) =
-                        make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
+                    for (int cc = 0; cc < 16; ++cc)
+                        yfrag[(((bb * 2 + (r >> 3)) * 2 + (cc >> 3)) * 32 + 4 * (cc & 7) + (r & 3)) * 2 +
+                              ((r >> 2) & 1)] = y[cc];
+                } else {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        *reinterpret_cast<float4 *>(sc.Y(row, o + 4 * c4)) =
+                            make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
+                }
             }
         }
         named_sync(2, kWyThreads);
@@ -498,8 +511,16 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph) {
                 for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
-                        const uint32_t bf[2] = {to_tf32(*sc.Y(16 * bb + 8 * ks + t, 16 * bb + 8 * nh + g)),
-                                                to_tf32(*sc.Y(16 * bb + 8 * ks + t + 4, 16 * bb + 8 * nh + g))};
+                        uint32_t bf[2];
+                        if (REC) {
+                            const float2 y2 =
+                                *reinterpret_cast<const float2 *>(yfrag + (((bb * 2 + ks) * 2 + nh) * 32 + lane) * 2);
+                            bf[0] = to_tf32(y2.x);
+                            bf[1] = to_tf32(y2.y);
+                        } else {
+                            bf[0] = to_tf32(*sc.Y(16 * bb + 8 * ks + t, 16 * bb + 8 * nh + g));
+                            bf[1] = to_tf32(*sc.Y(16 * bb + 8 * ks + t + 4, 16 * bb + 8 * nh + g));
+                        }
                         mma_tf32_16x8x8(zb[bb][nh], af[ks], bf);
                     }
                 if (bb > 0) frag_c_to_a(zb[bb], za[bb], lane, -1.f);
@@ -539,7 +560,7 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph) {
 // ============================================================================
 // WY warps: everything of a chunk that does not depend on the state.
 // ============================================================================
-template <int GATE, bool GLA, bool PAIR, bool ZREC, typename Tg>
+template <int GATE, bool GLA, bool PAIR, typename Tg>
 __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                         const CUtensorMap *tm_g, const CUtensorMap *tm_v, int e0, int h, Seq sq, int nchunks) {
     uint8_t *base = c.base;
@@ -575,17 +596,6 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 tma_load_4d(base + OFF_AG + blk * 16384, tm_g, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
         }
     };
-    // With records: Z and K<- of chunk n, the operands of its products, into buffer n & 1 --
-    // (the K-> tile, the K<- tile) or (the Z-in tile, A_G rows 0-127 of column block 0), which
-    // nothing else uses without a pair.  The chain loads the rest of the record into the slot.
-    auto issue_zk = [&](int n) {
-        const uint8_t *r = c.zrec + (size_t)n * c.zstride;
-        const int bf = n & 1;
-        uint64_t *bar = c.bars + B_ZK0 + bf;
-        mbar_arrive_expect_tx(bar, 32768u);
-        bulk_load(base + (bf ? OFF_ZIN : OFF_KR), r + REC_Z, 16384u, bar);
-        bulk_load(base + (bf ? OFF_AG : OFF_KL), r + REC_KL, 16384u, bar);
-    };
     auto issue_v = [&](int n) {
         const int s = n & 1;
         mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
@@ -603,17 +613,12 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     };
 
     if (leader) {
-        if (ZREC) {
-            issue_zk(0);
-            if (nchunks > 1) issue_zk(1);
-        } else if (first < nchunks) {
-            issue_raw(first);
-        }
+        if (first < nchunks) issue_raw(first);
         issue_v(0);                          // nchunks >= 1: empty sequences return before the roles
         if (nchunks > 1) issue_v(1);
     }
     __syncwarp();
-    if (!ZREC) {
+    {
         float bv, gv;
         load_scalars(first, bv, gv);
         if (wt < kC) { betas[wt] = bv; gss[wt] = gv; }
@@ -637,7 +642,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         float4 gcv;
         int r0 = 0;                                          // first of the 16 Z rows this warp built
 
-        if constexpr (!ZREC) {
+        {
             if (n + step < nchunks) load_scalars(n + step, nb, ng);   // prefetch next built chunk's scalars
             wait_bar(c, B_RAW, phm);
             // ---------------- prologue: Gamma and the rescaled tiles, in place.  K-> and gamma^C also
@@ -655,12 +660,11 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         // ---------------- Z K<- -> [W ; P W],  Z V -> D1[s] = [U ; P U]
         if (leader) {
             wait_bar(c, B_V0 + s, ph2);
-            if (ZREC) wait_bar(c, B_ZK0 + s, ph2);               // buffer n & 1 holds Z and K<-
             if (n >= 2) wait_bar(c, B_E10 + s, (uint32_t)(((n - 2) >> 1) & 1));   // D1[s] drained
             tc_fence_after();
-            const uint32_t a0 = smem_u32(base + (ZREC && s ? OFF_ZIN : OFF_KR));
+            const uint32_t a0 = smem_u32(base + OFF_KR);
             if (!GLA) {
-                const uint32_t bk = smem_u32(base + (ZREC && s ? OFF_AG : OFF_KL));
+                const uint32_t bk = smem_u32(base + OFF_KL);
                 const uint32_t id = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -677,13 +681,11 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         wait_bar(c, B_W2, phm);
         tc_fence_after();
         if (leader && n + 2 < nchunks) issue_v(n + 2);           // v[s] consumed
-        if (ZREC && leader && n + 2 < nchunks) issue_zk(n + 2);      // buffer n & 1: its products are done
         __syncwarp();
         if (n >= 2) wait_bar(c, B_C20 + s, (uint32_t)(((n - 2) >> 1) & 1));   // own scan done with slot s
         // the other CTA of a pair is done with chunk n - 2, whose slot tiles and Z it received from
         // here: the slot and its Z-in tile may be rewritten
         if (PAIR && m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));
-        if (ZREC) wait_bar(c, B_SL0 + s, ph2);                 // Q<- (in A_chain[s]), K->, gamma^C of chunk n
         __syncwarp();
         if (PAIR) {
             // the other CTA forms its own [U ; P U] = Z V: send this warp's 16 rows of Z (the
@@ -718,8 +720,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        // Q<-: rows 64-127 of A_G, or (records) of A_chain[s] itself, replaced in place
-                        const uint4 u = *reinterpret_cast<const uint4 *>((ZREC ? ach : base + OFF_AG) +
+                        // Q<-: rows 64-127 of A_G
+                        const uint4 u = *reinterpret_cast<const uint4 *>(base + OFF_AG +
                                                                          sw128_offset(128, row, col + 8 * q));
                         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -734,7 +736,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             }
         }
         // ---------------- K-> and gamma^C into slot s (and the other CTA's slot s)
-        if constexpr (!ZREC) {
+        {
             const int cg = wt & 31, rg = wt >> 5;
             const int col = 4 * cg;
             uint8_t *kt = base + off_kt(s);
@@ -745,7 +747,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             }
             if (rg == 0) *reinterpret_cast<float4 *>(gC + s * kDK + col) = gcv;
         }
-        if (!ZREC && wt < kC && n + step < nchunks) {
+        if (wt < kC && n + step < nchunks) {
             betas[(sb ^ 1) * kC + wt] = nb;
             gss[(sb ^ 1) * kC + wt] = ng;
         }
@@ -754,7 +756,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         named_sync(2, kWyThreads);
         if (leader) {
             mbar_arrive(c.bars + B_WYR0 + s);
-            if (!ZREC && n + step < nchunks) issue_raw(n + step);   // A_G and the K<- tile are free again
+            if (n + step < nchunks) issue_raw(n + step);   // A_G and the K<- tile are free again
             if (PAIR) {
                 // the slot buffers go to the other CTA's slot s by bulk copy (it is done with
                 // chunk n - 2: checked above)
@@ -779,7 +781,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 // ============================================================================
 // Chain warps: the serial state scan and the output.
 // ============================================================================
-template <bool PAIR, bool ZREC>
+template <bool PAIR>
 __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_v, const CUtensorMap *tm_o,
                            int e0, int h, int b, Seq sq, int nchunks) {
     uint8_t *base = c.base;
@@ -808,24 +810,6 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     };
     write_state();
 
-    // With records the slot inputs of chunk n come straight from its record into slot n & 1:
-    // Q<- into rows 64-127 of A_chain (the WY warps turn it into Q<- - P W in place), K-> and
-    // gamma^C.  Issued once the slot's previous chunk is done with it, two chunks ahead.
-    auto issue_slot = [&](int n) {
-        const uint8_t *r = c.zrec + (size_t)n * c.zstride;
-        const int sl = n & 1;
-        uint64_t *bar = c.bars + B_SL0 + sl;
-        mbar_arrive_expect_tx(bar, 2u * 16384u + 512u);
-        for (int blk = 0; blk < 2; ++blk)
-            bulk_load(base + off_ach(sl) + blk * 16384 + 8192, r + REC_Q + blk * 8192, 8192u, bar);
-        bulk_load(base + off_kt(sl), r + REC_KR, 16384u, bar);
-        bulk_load(base + OFF_MISC + MISC_GC + sl * 512, r + REC_GC, 512u, bar);
-    };
-    if (ZREC && leader) {
-        issue_slot(0);
-        if (nchunks > 1) issue_slot(1);
-    }
-    __syncwarp();
 
     for (int n = 0; n < nchunks; ++n) {
         const int s = n & 1;
@@ -840,7 +824,6 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
             fence_proxy_async_smem();    // the received tiles are read by the tensor core next
         } else {
             wait_bar(c, B_WYR0 + s, ph2);
-            if (ZREC) wait_bar(c, B_SL0 + s, ph2);      // gamma^C and K-> of the slot, loaded here
         }
         tc_fence_after();
         const float gam = gC[s * kDK + j];
@@ -926,8 +909,6 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
         __syncwarp();
         wait_bar(c, B_C20 + s, ph2);
         tc_fence_after();
-        if (ZREC && leader && n + 2 < nchunks) issue_slot(n + 2);   // slot s: both products are done
-        __syncwarp();
         {
             float v[32];
 #pragma unroll
@@ -955,12 +936,11 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     __syncwarp();
 }
 
-template <int GATE, bool GLA, bool PAIR, bool ZREC, typename Tg>
+template <int GATE, bool GLA, bool PAIR, typename Tg>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o) {
-    static_assert(!(PAIR && ZREC), "with records each value slice builds every chunk itself");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctx c;
@@ -974,8 +954,8 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
     const Seq sq = seq_of(p, b);
     const int nchunks = (sq.len + kC - 1) / kC;
-    c.zrec = ZREC ? p.zrec + ((size_t)zslot0(p, b, sq) * p.H + h) * kRecBytes : nullptr;
-    c.zstride = (size_t)p.H * kRecBytes;
+    c.zrec = nullptr;
+    c.zstride = 0;
     if (nchunks == 0) {                     // empty sequence: ht = h0; nothing else is set up
         if (p.ht)
             for (int i = threadIdx.x; i < kDVS * kDK; i += kThreads) {
@@ -1002,9 +982,9 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     c.tmem = *tslot;
 
     if (threadIdx.x < kChainThreads)
-        chain_role<PAIR, ZREC>(c, p, &tm_v, &tm_o, e0, h, b, sq, nchunks);
+        chain_role<PAIR>(c, p, &tm_v, &tm_o, e0, h, b, sq, nchunks);
     else
-        wy_role<GATE, GLA, PAIR, ZREC, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, sq, nchunks);
+        wy_role<GATE, GLA, PAIR, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, sq, nchunks);
 
     tc_fence_before();
     __syncthreads();
@@ -1014,16 +994,17 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
 }
 
 // ============================================================================
-// Z records: the part of every chunk that needs the Gram and the inverse,
-// chunk-parallel ahead of the scan kernel.
+// Chunk records: every state-independent operand of a chunk, chunk-parallel
+// ahead of the record scan kernel.
 // ============================================================================
 // One CTA per (chunk, head, sequence) computes Gamma, the rescaled tiles and
-// Z = [T ; P T] (GLA: [I ; P]) with the scan kernel's own code (rescale_tiles,
-// build_z) and stores Z as the 16 KB image of the bf16 tile that the scan
-// kernel's products read, so that kernel loads it with one bulk copy instead
-// of building it.  Shared memory: the A_G and K-> tiles at the scan kernel's
-// offsets (raw k lands in the K-> tile and becomes K-> in place), then the
-// scalars, the cumsum partials and the barriers.
+// Z = [T ; P T] with the single kernel's code (rescale_tiles, build_z), then
+// [W ; P W] = Z K<- on the tensor core and A_chain = [-W ; Q<- - P W], and
+// stores the images of the bf16 tiles Z, A_chain and K-> (and gamma^C) as the
+// chunk's record, which the scan kernel loads with bulk copies.  Shared
+// memory: the A_G and K-> tiles at the single kernel's offsets (raw k lands in
+// the K-> tile and becomes K-> in place; A_G becomes [K<- ; Q<-], then
+// A_chain), then the scalars, the cumsum partials and the barriers.
 constexpr uint32_t OFF_WMISC = 49152;
 constexpr uint32_t WM_BETA = 0;          // beta [64] f32
 constexpr uint32_t WM_GS = 256;          // scalar gate [64] f32
@@ -1033,12 +1014,12 @@ constexpr uint32_t WM_TSLOT = 4800;      // TMEM base address
 constexpr uint32_t WM_ABORT = 4804;      // abort flag
 constexpr uint32_t kWMiscBytes = 4864;
 constexpr uint32_t kZSmemBytes = OFF_WMISC + kWMiscBytes + 1024;
-constexpr uint32_t kZTmemCols = 64;      // the Gram [L ; P]
+constexpr uint32_t kZTmemCols = 128;     // the Gram [L ; P] (64), then [W ; P W] (128)
 static_assert(OFF_KR + 16384 <= OFF_WMISC, "Z kernel tile layout");
 static_assert(WM_BAR + kNumBars * 8 <= WM_TSLOT, "Z kernel misc layout");
 static_assert(WM_ABORT + 4 <= kWMiscBytes, "Z kernel misc layout");
 
-template <int GATE, bool GLA, typename Tg>
+template <int GATE, typename Tg>
 __global__ void __launch_bounds__(kWyThreads, 4)
 kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_g) {
@@ -1106,22 +1087,371 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     uint8_t *rec = p.zrec + ((size_t)(zslot0(p, b, sq) + n) * H + h) * kRecBytes;
     uint2 krv[8];
     float4 gcv;
-    rescale_tiles<GATE, true, false>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gcv, rec);
+    rescale_tiles<GATE, true, false, true>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gcv, rec);
     fence_proxy_async_smem();
     __syncthreads();
-    build_z<GLA>(c, wt, betas, 0);
-    fence_proxy_async_smem();               // the Z stores, before the bulk copy reads them
-    __syncthreads();
+    // the cumsum partials are dead: their 4 KB hold the diagonal-block inverses
+    build_z<false, true>(c, wt, betas, 0, tot);
+    fence_proxy_async_smem();               // the Z stores, before the bulk copy and the tensor core read them
+    tc_fence_before();
+    __syncthreads();                        // and every warp is done with the Gram's TMEM columns
+    tc_fence_after();
     if (wt == 0) {
         bulk_store(rec + REC_Z, base + OFF_KR, 16384u);
         tma_store_commit();
-        tma_store_wait_read0();             // shared memory may go once the copy has read it
+        // [W ; P W] = Z K<-  (M128 N128 K64) over the Gram's columns.  K<- is rows 0-63 of A_G,
+        // read as an MN-major B tile: 16 K rows per step, its two 64-wide N blocks 16 KB apart.
+        const uint32_t a0 = smem_u32(base + OFF_KR), b0 = smem_u32(base + OFF_AG);
+        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(c.tmem + TM_G, desc_kmajor(a0, 128, ks), sdesc_sw128(b0 + ks * 2048u, 16384u, 1024u), id,
+                     ks > 0);
+        mma_commit(c.bars + B_GRAM);
+    }
+    __syncwarp();
+    wait_bar(c, B_GRAM, 1);
+    tc_fence_after();
+    // A_chain = [-W ; Q<- - P W] in place over A_G = [K<- ; Q<-] (the product has read K<-):
+    // TMEM lane quarter ww & 3, 64 columns per warp
+    {
+        const int ww = wt >> 5, quarter = ww & 3, half = ww >> 2;
+        const int row = quarter * 32 + (wt & 31);
+        uint8_t *ag = base + OFF_AG;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int col = half * 64 + cc * 32;
+            float v[32];
+            tmem_ld32(c.tmem + TM_G + ((uint32_t)(quarter * 32) << 16) + col, v);
+            if (quarter < 2) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = -v[e];
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(ag + sw128_offset(128, row, col + 8 * q));
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                        v[8 * q + 2 * e] = f.x - v[8 * q + 2 * e];
+                        v[8 * q + 2 * e + 1] = f.y - v[8 * q + 2 * e + 1];
+                    }
+                }
+            }
+            store_row32_bf16(ag, 128, row, col, v);
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (wt == 0) {
+        bulk_store(rec + REC_A, base + OFF_AG, 32768u);
+        tma_store_commit();
+        tma_store_wait_read0();             // shared memory may go once the copies have read it
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (wt < 32) tmem_dealloc(c.tmem, kZTmemCols);
+}
+
+// ============================================================================
+// Record scan kernel: the state recursion over the chunk records.
+// ============================================================================
+// One CTA per (64-wide value slice, head, sequence).  The records carry every
+// state-independent operand, so a chunk takes three products:
+//   D1 = Z V = [U ; P U]                  (issued by the loader, one chunk ahead)
+//   D1 += A_chain S^T = [V_new ; O]       (the state product)
+//   dS^T = K->^T V_new,   S <- (S + dS) Diag(gamma^C)
+// The slice's values are split into NH halves of W = 64 / NH, each a chain of
+// four warps with its own accumulator columns, S^T and V_new tiles and
+// barriers, so the halves can run out of step.  Warp 4 NH loads the records
+// (bulk copies) and the v tiles (TMA) and issues Z V.  A record takes about a
+// chunk's time to arrive, so A_chain, K->, gamma^C and v of chunk n go to entry
+// n % 3 of a three-deep ring, loaded three chunks ahead, and Z V of chunk n
+// runs two chunks ahead into accumulator slot n % 3, its Z from entry n % 2 of
+// a two-deep ring.  V_new takes the front of the half's S^T tile, which the
+// state product has read by then.
+// NH = 2 (two 32-wide halves, MN-major B tiles with 64-byte swizzle) gives the same
+// values and measured no faster: the halves run in step, the products' latency
+// dominates, not the register work between them.
+constexpr int kScanHalves = 1;
+template <int NH> struct ScanCfg {
+    static constexpr int W = 64 / NH;                    // values per half
+    static constexpr int kThreads = 128 * NH + 32;
+    static constexpr uint32_t R_SLOT = 57344;            // ring entry: A_chain, K->, v
+    static constexpr uint32_t R_ACH = 0, R_KT = 32768, R_V = 49152;
+    static constexpr uint32_t OFF_Z = 3 * R_SLOT;        // two entries: Z
+    static constexpr uint32_t OFF_ST = OFF_Z + 2 * 16384;    // S^T (then V_new) of each half, 16 KB in all
+    static constexpr uint32_t OFF_GC = OFF_ST + 16384;   // gamma^C [3][128] f32
+    static constexpr uint32_t OFF_BAR = OFF_GC + 1536;   // mbarriers
+    static constexpr uint32_t OFF_TSLOT = OFF_BAR + 256;
+    static constexpr uint32_t OFF_ABORT = OFF_TSLOT + 4;
+    static constexpr uint32_t kSmem = OFF_ABORT + 60 + 1024;   // + alignment slack of the dynamic base
+    static constexpr uint32_t kRTx = 32768u + 16384u + 512u + 8192u, kZTx = 16384u;
+};
+static_assert(ScanCfg<2>::kSmem <= 232448 && ScanCfg<1>::kSmem <= 232448, "shared memory per CTA");
+constexpr uint32_t kScanTmemCols = 256;
+constexpr uint32_t TS_D1 = 0;      // [U ; P U] -> [V_new ; O], 3 slots x 64 columns (half h: + h W)
+constexpr uint32_t TS_DS = 192;    // dS^T, half h at + h W
+
+// Ring entry / accumulator slot n % 3: FULLR, RFREE (one arrival per half), ZV, D1FREE (one
+// arrival per half); Z entry n % 2: FULLZ; C1 / C2: [half][chunk parity].
+enum { SB_FULLR = 0, SB_RFREE = 3, SB_ZV = 6, SB_D1FREE = 9, SB_FULLZ = 12, SB_C1 = 14, SB_C2 = 18, kScanBars = 22 };
+static_assert(kScanBars * 8 <= 256, "scan barriers");
+
+// 64-byte swizzle (MN-major operand tiles of 32 bf16 columns, one 64-byte row
+// each, 512-byte atoms of 8 rows): byte offset of column c < 32 of row r.
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t r, uint32_t c) {
+    return r * 64u + ((((c >> 3) ^ (r >> 1)) & 3u) << 4) + ((c & 7u) << 1);
+}
+// Descriptor of K-step ks (16 K rows) of such a tile: 8-row groups 512 bytes apart.
+__device__ __forceinline__ uint64_t desc_mn32(uint32_t base, uint32_t ks) {
+    uint64_t d = 0;
+    const uint32_t saddr = base + ks * 1024u;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((8192u >> 4) & 0x3FFFu) << 16;   // stride between 32-wide blocks (one block: unused)
+    d |= (uint64_t)((512u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;                         // descriptor version for tcgen05
+    d |= (uint64_t)4u << 61;                         // 64-byte swizzle
+    return d;
+}
+
+// W bf16 values of one row of a half's MN-major tile (SW128 with 64 columns, SW64 with 32).
+template <int W>
+__device__ __forceinline__ void store_half_row(uint8_t *tile, uint32_t rows, uint32_t r, const float *v) {
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+        const uint32_t off = W == 64 ? sw128_offset(rows, r, 8 * q) : sw64_offset(r, 8 * q);
+        st_u128(tile + off, pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+    }
+}
+template <int W>
+__device__ __forceinline__ uint64_t desc_half(uint32_t base, uint32_t krows, uint32_t ks) {
+    return W == 64 ? desc_mnmajor(base, krows, ks) : desc_mn32(base, ks);
+}
+template <int W> __device__ __forceinline__ void tmem_ld_half(uint32_t taddr, float (&v)[W]) {
+    tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(&v[0]));
+    if constexpr (W == 64) tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+}
+
+// One half's chain: thread t of the half owns key channel t (its TMEM lane) and
+// the W state values S[ev0 .. ev0 + W)[t] in registers.
+template <int NH>
+__device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, int h, int b, Seq sq,
+                           int nchunks) {
+    using G = ScanCfg<NH>;
+    constexpr int W = G::W;
+    uint8_t *base = c.base;
+    const int t = threadIdx.x - 128 * half;
+    const int warp = t >> 5;                             // TMEM lane quarter
+    const bool leader = t == 0;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int ev0 = e0 + half * W;
+    const int H = p.H, dv = p.dv;
+    const int bar_id = 1 + half;
+    uint8_t *st = base + G::OFF_ST + half * 8192;
+    uint8_t *vn = st;                                    // V_new: 64 rows at the front of the S^T tile
+    const float *gc = reinterpret_cast<const float *>(base + G::OFF_GC);
+    const uint32_t col = (uint32_t)(half * W);
+
+    float S[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) S[e] = p.h0 ? p.h0[(((size_t)b * H + h) * dv + ev0 + e) * kDK + t] : 0.f;
+
+    auto write_state = [&]() {
+        store_half_row<W>(st, 128, t, S);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(bar_id, 128);
+    };
+    write_state();
+
+    const uint32_t id1 = idesc_bf16(128, W, 0, 1), id2 = idesc_bf16(128, W, 1, 1);
+    for (int n = 0; n < nchunks; ++n) {
+        const int s = n & 1, ri = n % 3;
+        const uint32_t ph = (uint32_t)((n >> 1) & 1), phr = (uint32_t)((n / 3) & 1);
+        uint8_t *slot = base + ri * G::R_SLOT;
+        wait_bar(c, SB_FULLR + ri, phr);                 // A_chain, K-> and gamma^C of the record
+        wait_bar(c, SB_ZV + ri, phr);                    // D1[ri] = [U ; P U]
+        tc_fence_after();
+        const float gam = gc[ri * kDK + t];
+
+        // ---- D1[s] += A_chain S^T   (M128 N=W K128)
+        if (leader) {
+            const uint32_t a0 = smem_u32(slot + G::R_ACH), b0 = smem_u32(st);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(c.tmem + TS_D1 + ri * 64 + col, desc_kmajor(a0, 128, ks), desc_half<W>(b0, 128, ks), id1, 1);
+            mma_commit(c.bars + SB_C1 + half * 2 + s);
+        }
+        __syncwarp();
+        wait_bar(c, SB_C1 + half * 2 + s, ph);
+        tc_fence_after();
+
+        // ---- rows 0-63 (warps 0, 1): V_new -> the half's V_new tile; rows 64-127: O -> o
+        {
+            float v[W];
+            tmem_ld_half<W>(c.tmem + TS_D1 + ri * 64 + col + lane_base, v);
+            const int r = (warp & 1) * 32 + (t & 31);
+            if (warp < 2) {
+                store_half_row<W>(vn, 64, r, v);
+            } else if (n * kC + r < sq.len) {
+                __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
+                                      (((size_t)sq.bt * p.T + sq.t0 + n * kC + r) * H + h) * dv + ev0;
+#pragma unroll
+                for (int q = 0; q < W / 8; ++q)
+                    *reinterpret_cast<uint4 *>(orow + 8 * q) =
+                        make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_sync(bar_id, 128);
+        // ---- dS^T = K->^T V_new   (M128 N=W K64)
+        if (leader) {
+            tc_fence_after();
+            mbar_arrive(c.bars + SB_D1FREE + ri);        // this half's columns of D1[ri] are drained
+            const uint32_t a0 = smem_u32(slot + G::R_KT), b0 = smem_u32(vn);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(c.tmem + TS_DS + col, desc_mnmajor(a0, 64, ks), desc_half<W>(b0, 64, ks), id2, ks > 0);
+            mma_commit(c.bars + SB_C2 + half * 2 + s);
+        }
+        __syncwarp();
+        wait_bar(c, SB_C2 + half * 2 + s, ph);
+        tc_fence_after();
+        if (leader) mbar_arrive(c.bars + SB_RFREE + ri);  // this half is done with ring entry ri
+        __syncwarp();
+        {
+            float v[W];
+            tmem_ld_half<W>(c.tmem + TS_DS + col + lane_base, v);
+#pragma unroll
+            for (int e = 0; e < W; ++e) S[e] = gam * (S[e] + v[e]);
+        }
+        write_state();
+    }
+    if (p.ht) {
+#pragma unroll
+        for (int e = 0; e < W; ++e) p.ht[(((size_t)b * H + h) * dv + ev0 + e) * kDK + t] = S[e];
+    }
+}
+
+// The loader (one thread): chunk n's A_chain, K->, gamma^C and v tile into ring
+// entry n % 3, its Z into entry n % 2 of the Z ring, and D1[n % 3] = Z V as
+// soon as those are in and chunk n - 3 has drained the slot.
+template <int NH>
+__device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_v, int e0, int h, Seq sq,
+                            int nchunks) {
+    using G = ScanCfg<NH>;
+    uint8_t *base = c.base;
+    auto issue_r = [&](int n) {
+        const uint8_t *r = c.zrec + (size_t)n * c.zstride;
+        const int ri = n % 3;
+        uint8_t *slot = base + ri * G::R_SLOT;
+        uint64_t *bar = c.bars + SB_FULLR + ri;
+        mbar_arrive_expect_tx(bar, G::kRTx);
+        bulk_load(slot + G::R_ACH, r + REC_A, 32768u, bar);
+        bulk_load(slot + G::R_KT, r + REC_KR, 16384u, bar);
+        bulk_load(base + G::OFF_GC + ri * 512, r + REC_GC, 512u, bar);
+        tma_load_4d(slot + G::R_V, tm_v, bar, e0, h, sq.t0 + n * kC, sq.bt);
+    };
+    auto issue_z = [&](int n) {
+        const uint8_t *r = c.zrec + (size_t)n * c.zstride;
+        uint64_t *bar = c.bars + SB_FULLZ + (n & 1);
+        mbar_arrive_expect_tx(bar, G::kZTx);
+        bulk_load(base + G::OFF_Z + (n & 1) * 16384, r + REC_Z, 16384u, bar);
+    };
+    auto zv = [&](int n) {
+        const int ri = n % 3;
+        wait_bar(c, SB_FULLR + ri, (uint32_t)((n / 3) & 1));                 // v
+        wait_bar(c, SB_FULLZ + (n & 1), (uint32_t)((n >> 1) & 1));           // Z
+        if (n >= 3) wait_bar(c, SB_D1FREE + ri, (uint32_t)(((n - 3) / 3) & 1));   // chunk n - 3 drained D1[ri]
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(base + G::OFF_Z + (n & 1) * 16384), b0 = smem_u32(base + ri * G::R_SLOT + G::R_V);
+        const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(c.tmem + TS_D1 + ri * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
+        mma_commit(c.bars + SB_ZV + ri);
+    };
+    if ((threadIdx.x & 31) == 0) {
+        for (int n = 0; n < 3 && n < nchunks; ++n) {
+            issue_r(n);
+            if (n < 2) issue_z(n);
+        }
+        zv(0);
+        if (nchunks > 1) zv(1);
+        for (int n = 0; n < nchunks; ++n) {
+            if (n + 2 < nchunks) {
+                wait_bar(c, SB_ZV + n % 3, (uint32_t)((n / 3) & 1));     // Z V of chunk n has read its Z
+                issue_z(n + 2);
+            }
+            if (n + 3 < nchunks) {
+                wait_bar(c, SB_RFREE + n % 3, (uint32_t)((n / 3) & 1));  // chunk n is done with its entry
+                issue_r(n + 3);
+            }
+            if (n + 2 < nchunks) zv(n + 2);
+        }
+    }
+    __syncwarp();
+}
+
+template <int NH>
+__global__ void __launch_bounds__(ScanCfg<NH>::kThreads, 1)
+kda_fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_v) {
+    using G = ScanCfg<NH>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctx c;
+    c.base = base;
+    c.bars = reinterpret_cast<uint64_t *>(base + G::OFF_BAR);
+    c.abort = reinterpret_cast<volatile int *>(base + G::OFF_ABORT);
+    c.status = p.status;
+    c.rank = 0;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + G::OFF_TSLOT);
+    const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
+    const Seq sq = seq_of(p, b);
+    const int nchunks = (sq.len + kC - 1) / kC;
+    c.zrec = p.zrec + ((size_t)zslot0(p, b, sq) * p.H + h) * kRecBytes;
+    c.zstride = (size_t)p.H * kRecBytes;
+    if (nchunks == 0) {                     // empty sequence: ht = h0; nothing else is set up
+        if (p.ht)
+            for (int i = threadIdx.x; i < kDVS * kDK; i += G::kThreads) {
+                const size_t off = (((size_t)b * p.H + h) * p.dv + e0 + i / kDK) * kDK + i % kDK;
+                p.ht[off] = p.h0 ? p.h0[off] : 0.f;
+            }
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kScanBars; ++i)
+            mbar_init(c.bars + i, ((i >= SB_RFREE && i < SB_ZV) || (i >= SB_D1FREE && i < SB_FULLZ))
+                                      ? (uint32_t)NH : 1u);   // RFREE, D1FREE: one arrival per half
+        *c.abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(tslot, kScanTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    c.tmem = *tslot;
+
+    if (threadIdx.x < 128 * NH)
+        scan_chain<NH>(c, p, threadIdx.x >> 7, e0, h, b, sq, nchunks);
+    else
+        scan_loader<NH>(c, p, &tm_v, e0, h, sq, nchunks);
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x < 32) tmem_dealloc(c.tmem, kScanTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1152,15 +1482,14 @@ bool make_map(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int GATE, bool GLA, bool ZREC, typename Tg>
-cudaError_t launch_scan(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
-                        const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
-    // Without records the two value slices of a head split the chunks they build (a pair);
-    // with records building a chunk is light, and each slice builds every chunk itself.
+template <int GATE, bool GLA, typename Tg>
+cudaError_t launch_single(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
+                          const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
+    // The two value slices of a head (dv = 128) split the chunks they build (a pair).
     dim3 grid(p.dv / kDVS, p.H, p.B);
-    if constexpr (!ZREC) {
+    {
       if (p.dv == 2 * kDVS) {
-        auto kern = kda_fwd_tc_kernel<GATE, GLA, true, false, Tg>;
+        auto kern = kda_fwd_tc_kernel<GATE, GLA, true, Tg>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -1178,26 +1507,39 @@ cudaError_t launch_scan(const FwdParams &p, const CUtensorMap &q, const CUtensor
         return cudaLaunchKernelEx(&cfg, kern, p, q, k, g, v, o);
       }
     }
-    auto kern = kda_fwd_tc_kernel<GATE, GLA, false, ZREC, Tg>;
+    auto kern = kda_fwd_tc_kernel<GATE, GLA, false, Tg>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, kSmemBytes, s>>>(p, q, k, g, v, o);
     return cudaGetLastError();
 }
 
-// With Z records (p.zrec set): the chunk-parallel Z kernel, then the scan
-// kernel that loads Z; otherwise the scan kernel alone, building Z itself.
+template <int NH>
+cudaError_t launch_record_scan(const FwdParams &p, const CUtensorMap &v, cudaStream_t s) {
+    auto kern = kda_fwd_scan_kernel<NH>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ScanCfg<NH>::kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(p.dv / kDVS, p.H, p.B), ScanCfg<NH>::kThreads, ScanCfg<NH>::kSmem, s>>>(p, v);
+    return cudaGetLastError();
+}
+
+// With chunk records (p.zrec set): the chunk-parallel Z kernel, then the record
+// scan kernel; otherwise the single kernel, building Z itself.
 template <int GATE, bool GLA, typename Tg>
 cudaError_t launch_variant(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
                            const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
-    if (!p.zrec) return launch_scan<GATE, GLA, false, Tg>(p, q, k, g, v, o, s);
-    auto zk = kda_fwd_z_kernel<GATE, GLA, Tg>;
-    cudaError_t e = cudaFuncSetAttribute(zk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kZSmemBytes);
-    if (e != cudaSuccess) return e;
-    zk<<<dim3((p.T + kC - 1) / kC, p.H, p.B), kWyThreads, kZSmemBytes, s>>>(p, q, k, g);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_scan<GATE, GLA, true, Tg>(p, q, k, g, v, o, s);
+    if constexpr (GLA) {
+        return launch_single<GATE, GLA, Tg>(p, q, k, g, v, o, s);    // no inverse: no records
+    } else {
+        if (!p.zrec) return launch_single<GATE, GLA, Tg>(p, q, k, g, v, o, s);
+        auto zk = kda_fwd_z_kernel<GATE, Tg>;
+        cudaError_t e = cudaFuncSetAttribute(zk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kZSmemBytes);
+        if (e != cudaSuccess) return e;
+        zk<<<dim3((p.T + kC - 1) / kC, p.H, p.B), kWyThreads, kZSmemBytes, s>>>(p, q, k, g);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_record_scan<kScanHalves>(p, v, s);
+    }
 }
 
 }  // namespace

@@ -125,11 +125,13 @@ size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
  * chunk-parallel one writes every chunk's record into the workspace --
  * Z = [T ; P T] (T = (I + L)^{-1} Diag(beta) with L the masked
  * beta K<- K->^T, P the masked Q<- K->^T: the forward recap of page "Kimi
- * Delta Attention backward"), the rescaled tiles Q<-, K<-, K-> and gamma^C
- * -- then the scan kernel reads them; the workspace must then be 16-byte
- * aligned (KDA_ERR_INVALID_ARG otherwise).  With a smaller workspace the
- * scan kernel builds Z itself (one kernel, slower); both forms compute the
- * same values.
+ * Delta Attention backward"), A_chain = [-W ; Q<- - P W] with W = T K<-,
+ * the rescaled K-> and gamma^C -- then the scan kernel reads them; the
+ * workspace must then be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
+ * With a smaller workspace the scan kernel builds Z itself (one kernel,
+ * slower); both forms compute the same values up to bf16 rounding (the
+ * record form applies beta to the rows of L after the Gram product, the
+ * single kernel to the bf16 K<- operand before it).
  */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 

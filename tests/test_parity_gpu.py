@@ -269,7 +269,9 @@ def _small_workspace():
 @pytest.mark.parametrize("variant,dv", [("kda", 128), ("kda", 64), ("gdn", 128), ("deltanet", 128), ("gla", 128)])
 def test_bf16_single_kernel_form(variant, dv):
     """With only the status word as workspace the scan kernel builds Z itself; same tolerance
-    against the oracle, and it agrees with the two-kernel form (Z records) to rounding."""
+    against the oracle for both forms, and they agree with each other within it (the record form
+    scales the Gram rows by beta after the product, the single kernel scales the bf16 K<- operand,
+    so the two round differently)."""
     w = custom(variant, 2, 300, 3, 128, dv, dtype=torch.bfloat16, h0=True)
     x = make_inputs(w, seed=6)
     d = {k_: (v_.to(DEV) if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
@@ -281,7 +283,8 @@ def test_bf16_single_kernel_form(variant, dv):
     ro, rh = run_oracle(x, variant)
     o1, h1, o2, h2 = (t.double().cpu().numpy() for t in (o1, h1, o2, h2))
     assert rel(o1, ro) <= 5e-3 and rel(h1, rh) <= 5e-3, (rel(o1, ro), rel(h1, rh))
-    assert rel(o2, o1) <= 1e-5 and rel(h2, h1) <= 1e-5, (rel(o2, o1), rel(h2, h1))
+    assert rel(o2, ro) <= 5e-3 and rel(h2, rh) <= 5e-3, (rel(o2, ro), rel(h2, rh))
+    assert rel(o2, o1) <= 5e-3 and rel(h2, h1) <= 5e-3, (rel(o2, o1), rel(h2, h1))
 
 
 def test_bf16_single_kernel_form_varlen():
