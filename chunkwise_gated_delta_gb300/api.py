@@ -126,9 +126,10 @@ def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, sca
                           output_final_state=True, o=None, ht=None, stream=None, cu_seqlens=None):
     """``kda_chunk_fwd_noalloc`` of the C ABI: the forward without a workspace.
 
-    For callers that cannot allocate device memory at the call (for instance
-    inside CUDA-graph capture): the library uses its own 256-byte array in
-    place of the workspace.  o / ht may be passed in preallocated; when they
+    For callers that cannot allocate device memory at the call (an allocator
+    that owns all device memory, a host that hands over only the tensors):
+    the library uses its own 256-byte array in place of the workspace.
+    o / ht may be passed in preallocated; when they
     are not, this binding allocates them with torch before the call (the C
     entry point itself allocates nothing).  Calls sharing the library array
     must not overlap on the GPU.

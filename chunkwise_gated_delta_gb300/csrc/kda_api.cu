@@ -334,7 +334,7 @@ kda_status dplr_factor_norms(const dplr_fwd_args *args, float *rho, float *norm,
     const size_t g_bytes = args->gate_kind == KDA_GATE_CHANNEL ? nbt * args->dk * dtype_size(args->g_dtype)
                            : args->gate_kind == KDA_GATE_SCALAR ? nbt * dtype_size(args->g_dtype) : 0;
     struct R { const void *p; size_t n; } outr[] = {{rho, rho ? nbt * 4 : 0}, {norm, norm ? nbt * 4 : 0},
-                                                     {maxes, maxes ? 8 : 0}};
+                                                     {maxes, maxes ? size_t{8} : size_t{0}}};
     for (const R &o : outr) {
         if (overlaps(o.p, o.n, args->a, in_bytes) || overlaps(o.p, o.n, args->b, in_bytes) ||
             overlaps(o.p, o.n, args->g, g_bytes))

@@ -3,11 +3,11 @@
 //
 // kda_chunk_fwd needs a workspace besides its inputs and outputs: its first
 // word is where the kernels report a device-side error, and on the bf16 path
-// the rest, when given, holds the Z records of the two-kernel form.  Callers
-// that cannot provide one -- code running while a stream is captured into a
-// CUDA graph, frameworks whose allocator forbids allocations outside its own
-// arenas, hosts that only hand over the input and output tensors -- use this
-// entry point instead.  The status word then lives in a small array owned by
+// the rest, when given, holds the chunk records of the two-kernel form.
+// Callers that cannot provide one -- frameworks whose caching allocator owns
+// all device memory, plugins and embedded hosts that only hand over the input
+// and output tensors, latency-critical paths that cannot afford a cudaMalloc
+// (which may synchronise the device) -- use this entry point instead.  The status word then lives in a small array owned by
 // the library, defined below (every GPU that loads the library holds it until
 // the process exits), and the forward runs its single-kernel form, which
 // builds each chunk's Z inside the scan kernel and needs no records.
@@ -20,7 +20,8 @@
 namespace {
 
 // Library-owned replacement for the caller's workspace: the status word,
-// padded to an aligned block (all the single-kernel forward needs).
+// padded to an aligned block -- all the single-kernel forward needs, at any
+// problem size, so no size is rejected for want of scratch.
 constexpr size_t kNoAllocScratchBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -140,9 +140,10 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  * form.  The papers have no counterpart: this is library plumbing.
  *
  * Some callers cannot allocate device memory where they call the forward:
- * code running while a stream is being captured into a CUDA graph,
- * frameworks whose allocator forbids allocations outside its own arenas, or
- * hosts that hand the library nothing but the input and output tensors.
+ * frameworks whose caching allocator owns all device memory and forbids
+ * allocations outside its own arenas, plugins and embedded hosts that hand
+ * the library nothing but the input and output tensors, and latency-critical
+ * paths that cannot afford cudaMalloc, which may synchronise the device.
  * This entry point takes the same arguments as kda_chunk_fwd (workspace and
  * workspace_bytes are ignored) and uses instead an array owned by the
  * library: 256 bytes per device, held from library load until process exit.
@@ -151,7 +152,9 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  *   - Every call clears the array's status word on `stream`, then launches.
  *     All calls share the array, so calls that overlap on the GPU (unordered
  *     streams) race on it.
- *   - Runs the single-kernel form of kda_chunk_fwd (no chunk records).
+ *   - Runs the single-kernel form of kda_chunk_fwd (no chunk records), whose
+ *     scratch is the 256-byte status block at any problem size, so no size
+ *     that kda_chunk_fwd accepts is too large for the array.
  *   - A device-side wait that runs out is recorded in the shared array and
  *     cleared by the next call; to observe it, use kda_chunk_fwd with your
  *     own workspace and kda_status_read.

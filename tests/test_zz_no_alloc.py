@@ -1,9 +1,9 @@
 """kda_chunk_fwd_noalloc: the forward for callers that cannot allocate device memory.
 
-Callers such as code running during CUDA-graph capture, or frameworks whose
-allocator forbids allocations at the call site, cannot supply the workspace
-that kda_chunk_fwd needs; the no-allocation entry point replaces it with a
-small array owned by the library.  Its results must equal those of
+Callers such as frameworks whose caching allocator owns all device memory,
+or plugins handed only the input and output tensors, cannot supply the
+workspace that kda_chunk_fwd needs; the no-allocation entry point replaces it
+with a small array owned by the library.  Its results must equal those of
 kda_chunk_fwd on the same inputs, on every call (the library array keeps the
 previous call's contents, so two calls in a row are checked).  This file is
 collected last so that a run stopping at the first failure has already run
