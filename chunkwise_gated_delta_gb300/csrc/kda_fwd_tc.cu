@@ -1025,7 +1025,12 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
                  const __grid_constant__ CUtensorMap tm_g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // one-dimensional grid, chunk-major with the last chunk first: the records the scan reads
+    // first are written last and are still in L2 when it starts
+    const int nch = (p.T + kC - 1) / kC;
+    const int per_chunk = p.H * p.B;
+    const int h = (int)(blockIdx.x % (unsigned)p.H), b = (int)((blockIdx.x / (unsigned)p.H) % (unsigned)p.B);
+    const int n = nch - 1 - (int)(blockIdx.x / (unsigned)per_chunk);
     const Seq sq = seq_of(p, b);
     if (n * kC >= sq.len) return;           // past the end of this sequence (or an empty one)
     const int wt = threadIdx.x;
@@ -1291,14 +1296,28 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
         wait_bar(c, SB_C1 + half * 2 + s, ph);
         tc_fence_after();
 
-        // ---- rows 0-63 (warps 0, 1): V_new -> the half's V_new tile; rows 64-127: O -> o
+        // ---- rows 0-63 (warps 0, 1): V_new -> the half's V_new tile, then dS^T = K->^T V_new;
+        //      rows 64-127 (warps 2, 3): O -> o, stored while that product runs
         {
             float v[W];
             tmem_ld_half<W>(c.tmem + TS_D1 + ri * 64 + col + lane_base, v);
             const int r = (warp & 1) * 32 + (t & 31);
-            if (warp < 2) {
-                store_half_row<W>(vn, 64, r, v);
-            } else if (n * kC + r < sq.len) {
+            if (warp < 2) store_half_row<W>(vn, 64, r, v);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(bar_id, 128);
+            // ---- dS^T = K->^T V_new   (M128 N=W K64)
+            if (leader) {
+                tc_fence_after();
+                mbar_arrive(c.bars + SB_D1FREE + ri);    // this half's columns of D1[ri] are drained
+                const uint32_t a0 = smem_u32(slot + G::R_KT), b0 = smem_u32(vn);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(c.tmem + TS_DS + col, desc_mnmajor(a0, 64, ks), desc_half<W>(b0, 64, ks), id2, ks > 0);
+                mma_commit(c.bars + SB_C2 + half * 2 + s);
+            }
+            __syncwarp();
+            if (warp >= 2 && n * kC + r < sq.len) {
                 __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
                                       (((size_t)sq.bt * p.T + sq.t0 + n * kC + r) * H + h) * dv + ev0;
 #pragma unroll
@@ -1308,20 +1327,6 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
                                    pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_sync(bar_id, 128);
-        // ---- dS^T = K->^T V_new   (M128 N=W K64)
-        if (leader) {
-            tc_fence_after();
-            mbar_arrive(c.bars + SB_D1FREE + ri);        // this half's columns of D1[ri] are drained
-            const uint32_t a0 = smem_u32(slot + G::R_KT), b0 = smem_u32(vn);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(c.tmem + TS_DS + col, desc_mnmajor(a0, 64, ks), desc_half<W>(b0, 64, ks), id2, ks > 0);
-            mma_commit(c.bars + SB_C2 + half * 2 + s);
-        }
-        __syncwarp();
         wait_bar(c, SB_C2 + half * 2 + s, ph);
         tc_fence_after();
         if (leader) mbar_arrive(c.bars + SB_RFREE + ri);  // this half is done with ring entry ri
@@ -1535,7 +1540,9 @@ cudaError_t launch_variant(const FwdParams &p, const CUtensorMap &q, const CUten
         auto zk = kda_fwd_z_kernel<GATE, Tg>;
         cudaError_t e = cudaFuncSetAttribute(zk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kZSmemBytes);
         if (e != cudaSuccess) return e;
-        zk<<<dim3((p.T + kC - 1) / kC, p.H, p.B), kWyThreads, kZSmemBytes, s>>>(p, q, k, g);
+        const long long nblk = (long long)((p.T + kC - 1) / kC) * p.H * p.B;
+        if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
+        zk<<<dim3((unsigned)nblk), kWyThreads, kZSmemBytes, s>>>(p, q, k, g);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return launch_record_scan<kScanHalves>(p, v, s);
