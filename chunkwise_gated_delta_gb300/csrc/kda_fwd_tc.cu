@@ -137,7 +137,7 @@ struct Ctx {
     int *status;
     uint32_t tmem;
     uint32_t rank;     // rank in the pair (0 without a pair)
-    const uint8_t *zrec;   // Z record of chunk 0 of this (sequence, head); chunk n at zrec + n * zstride
+    const uint8_t *zrec;   // record of chunk 0 of this (sequence, head); chunk n at zrec + n * zstride
     size_t zstride;
 };
 
@@ -261,7 +261,7 @@ __device__ __forceinline__ Seq seq_of(const FwdParams &p, int b) {
     const int hi = min(max(p.cu_seqlens[b + 1], lo), p.T);
     return Seq{0, lo, hi - lo};
 }
-// Z record slot of chunk 0 of sequence b.  Dense: b * ceil(T / C).  Packed:
+// Record slot of chunk 0 of sequence b.  Dense: b * ceil(T / C).  Packed:
 // b + floor(t0 / C), which never collides with the next sequence's slots
 // (floor(t0 / C) + ceil(len / C) <= floor((t0 + len) / C) + 1), so B + ceil(T / C)
 // slots per head cover every packing.
