@@ -1196,7 +1196,7 @@ template <int NH> struct ScanCfg {
     static constexpr uint32_t kSmem = OFF_ABORT + 60 + 1024;   // + alignment slack of the dynamic base
     static constexpr uint32_t kRTx = 32768u + 16384u + 512u + 8192u, kZTx = 16384u;
 };
-static_assert(ScanCfg<2>::kSmem <= 232448 && ScanCfg<1>::kSmem <= 232448, "shared memory per CTA");
+static_assert(ScanCfg<kScanHalves>::kSmem <= 232448, "shared memory per CTA");   // the same for NH = 1, 2
 constexpr uint32_t kScanTmemCols = 256;
 constexpr uint32_t TS_D1 = 0;      // [U ; P U] -> [V_new ; O], 3 slots x 64 columns (half h: + h W)
 constexpr uint32_t TS_DS = 192;    // dS^T, half h at + h W
