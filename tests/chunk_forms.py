@@ -53,6 +53,51 @@ def kda_chunk_form(q, k, v, g, beta, h0=None, C=64, scale_v=True):
     return o, S
 
 
+def kda_record_form(q, k, v, g, beta, h0=None, C=64, blk=16, scale_v=True):
+    """The regrouping of the KDA chunk form that the tensor-core kernels evaluate.
+
+    Derived from the recap on page "Kimi Delta Attention backward": per chunk,
+    with L = Diag(beta)(K<- K->^T * M_{-1}) and P = Q<- K->^T * M,
+      Z' (I + L) = [I ; P]   solved by back-substitution over blk-column blocks
+                             (page "DeltaNet" 4.2, block form, on the
+                             transposed system): Z'_c = ([I ; P]_c -
+                             sum_{c' > c} Z'_{c'} L_{c'c}) (I + L_cc)^{-1};
+      Z = Z' Diag(beta) = [T ; P T]  with T = A~ Diag(beta);
+      [W ; P W] = Z K<-,   A = [-W ; Q<- - P W];
+      D1 = Z V + A S^T = [U - W S^T ; P U + (Q<- - P W) S^T] = [V_new ; O];
+      S <- (S + V_new^T K->) Diag(gamma^C).
+    With scale_v False (beta does not scale v) U = A~ V: V is multiplied by
+    Z' instead of Z.  Inputs as kda_chunk_form.
+    """
+    T, dk = q.shape
+    dv = v.shape[1]
+    g = np.zeros((T, dk)) if g is None else g
+    beta = np.zeros(T) if beta is None else beta
+    S = np.zeros((dv, dk)) if h0 is None else h0.copy()
+    o = np.zeros((T, dv))
+    for s in range(0, T, C):
+        e = min(s + C, T)
+        n = e - s
+        M, M1 = _masks(n)
+        Gam = np.exp(np.cumsum(g[s:e], axis=0))
+        Ql, Kl, Kr = q[s:e] * Gam, k[s:e] * Gam, k[s:e] / Gam
+        L = np.diag(beta[s:e]) @ ((Kl @ Kr.T) * M1)
+        P = (Ql @ Kr.T) * M
+        R = np.vstack([np.eye(n), P])
+        Zp = np.zeros((2 * n, n))
+        for c0 in reversed(range(0, n, blk)):
+            c1 = min(c0 + blk, n)
+            rhs = R[:, c0:c1] - Zp[:, c1:] @ L[c1:, c0:c1]
+            Zp[:, c0:c1] = rhs @ np.linalg.inv(np.eye(c1 - c0) + L[c0:c1, c0:c1])
+        Z = Zp @ np.diag(beta[s:e])
+        WP = Z @ Kl
+        A = np.vstack([-WP[:n], Ql - WP[n:]])
+        D1 = (Z if scale_v else Zp) @ v[s:e] + A @ S.T
+        o[s:e] = D1[n:]
+        S = (S + D1[:n].T @ Kr) * Gam[-1][None, :]
+    return o, S
+
+
 def dplr_chunk_form(q, k, v, a, b, g, h0=None, C=64):
     """Gated DPLR chunk forward of page "Diagonal Plus Low Rank", section 2.
 

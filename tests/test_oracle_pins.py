@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 
 import oracle
-from chunk_forms import dplr_chunk_form, dplr_wy_product, kda_chunk_form
+from chunk_forms import dplr_chunk_form, dplr_wy_product, kda_chunk_form, kda_record_form
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 rng = np.random.default_rng
@@ -162,6 +162,33 @@ def test_kda_chunk_form_equals_recurrence(C):
                                 beta[0, :, h], h0[0, h], C=C)
         scale = np.abs(o[0, :, h]).max()
         np.testing.assert_allclose(oc, o[0, :, h], rtol=0, atol=1e-12 * scale)
+        np.testing.assert_allclose(Sc, ht[0, h], rtol=0, atol=1e-12 * np.abs(ht).max())
+
+
+@pytest.mark.parametrize("C,blk", [(64, 16), (64, 8), (32, 16), (16, 16)])
+@pytest.mark.parametrize("variant", ["kda", "gdn", "deltanet", "gla"])
+def test_record_form_equals_recurrence(C, blk, variant):
+    """The regrouped products of the tensor-core kernels ([L ; P], the block back-substitution
+    of Z'(I + L) = [I ; P], A = [-W ; Q<- - P W], D1 = Z V + A S^T = [V_new ; O]) reach the
+    recurrence's result: the regrouping is exact, whatever the chunk and block sizes."""
+    q, k, v, beta, g, h0 = _rand(11, B=1, T=150, H=2, dk=16, dv=12)
+    scale_v = True
+    if variant == "kda":
+        o, ht = oracle.kda_fwd(q, k, v, g, beta, h0)
+    elif variant == "gdn":
+        o, ht = oracle.gdn_fwd(q, k, v, g[..., 0], beta, h0)
+        g = np.repeat(g[..., :1], g.shape[-1], axis=-1)
+    elif variant == "deltanet":
+        o, ht = oracle.deltanet_fwd(q, k, v, beta, h0)
+        g = np.zeros_like(g)
+    else:
+        o, ht = oracle.gla_fwd(q, k, v, g, h0)
+        beta = np.zeros_like(beta)
+        scale_v = False
+    for h in range(2):
+        oc, Sc = kda_record_form(q[0, :, h], k[0, :, h], v[0, :, h], g[0, :, h], beta[0, :, h], h0[0, h],
+                                 C=C, blk=blk, scale_v=scale_v)
+        np.testing.assert_allclose(oc, o[0, :, h], rtol=0, atol=1e-12 * np.abs(o).max())
         np.testing.assert_allclose(Sc, ht[0, h], rtol=0, atol=1e-12 * np.abs(ht).max())
 
 
