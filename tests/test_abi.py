@@ -248,3 +248,27 @@ def test_bwd_and_dplr_need_an_aligned_workspace(lib):
     assert lib.dplr_chunk_fwd(ctypes.byref(d), None) == _lib.KDA_ERR_INVALID_ARG
     e = _dplr_bwd_args(workspace=MISALIGNED)
     assert lib.dplr_chunk_bwd(ctypes.byref(e), None) == _lib.KDA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- no CPU path
+def test_missing_library_raises(monkeypatch, tmp_path):
+    """Without libkda.so the binding raises instead of computing anything itself."""
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libkda.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError, match="missing"):
+        _lib.load()
+
+
+@pytest.mark.parametrize("entry", ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_bwd"])
+def test_host_tensors_are_rejected(lib, entry):
+    """Every compute call takes device tensors only: host tensors raise, they are not run on the CPU."""
+    import torch
+
+    from chunkwise_gated_delta_gb300 import api
+    q = torch.zeros(1, 64, 1, 128, dtype=torch.bfloat16)
+    beta = torch.zeros(1, 64, 1, dtype=torch.bfloat16)
+    args = (q, q, q, q, beta)
+    if entry == "kda_chunk_bwd":
+        args = args + (None, q)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        getattr(api, entry)(*args)
