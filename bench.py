@@ -453,6 +453,23 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def relaunch_ranks(n_gpus: int, argv) -> int:
+    """`--gpus N` (N > 1) started without a rank environment: run N ranks of this same command.
+
+    One process per GPU through torch.distributed.run on 127.0.0.1; rank 0 prints the line and
+    the return code is the launcher's."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n_gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -460,12 +477,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["kda_bf16_b4t4096h16d128", "gdn_bf16_b8t2048h32d128", "deltanet_bf16_b8t2048h32d128",
+                    choices=["kda_fp32_b1t256h1d64", "kda_bf16_b4t4096h16d128", "gdn_bf16_b8t2048h32d128", "deltanet_bf16_b8t2048h32d128",
                              "gla_bf16_b8t2048h32d128", "dplr_bf16_b2t8192h16d128", "kda_bwd_bf16_b4t4096h16d128",
                              "dplr_bwd_bf16_b2t8192h16d128"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(relaunch_ranks(args.gpus, sys.argv[1:]))
+    if int(os.environ.get("WORLD_SIZE", "1")) != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={os.environ.get('WORLD_SIZE', '1')}")
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -147,7 +147,8 @@ def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, sca
     args = make_args(q, k, v, g, beta, h0, o, ht, gate=gate, scale_v=scale_v, cu_seqlens=cu_seqlens)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+    with torch.cuda.device(q.device):   # the C entry point uses the current device's array
+        rc = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_noalloc")
     return o, ht

@@ -1,5 +1,6 @@
-// Backward of the general gated DPLR recurrence, float32 arithmetic on CUDA
-// cores, chunk length C = 16.
+// Backward of the general gated DPLR recurrence, chunk length C = 16, float32
+// accumulation: the chunk products are warp-level tf32 tensor-core MMAs for
+// bf16 inputs and exact float32 products on the CUDA cores for fp32 inputs.
 //
 // Page "Diagonal Plus Low Rank", section 3 derives, per chunk [t], with
 // F = I + (B<- A->^T * M_{-1}), E = F^{-1}, W = E B<-,

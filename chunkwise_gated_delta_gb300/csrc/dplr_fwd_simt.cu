@@ -1,4 +1,5 @@
-// float32 CUDA-core kernels for the general gated DPLR recurrence
+// Kernels for the general gated DPLR recurrence, float32 accumulation (warp-level
+// tf32 tensor-core products for bf16 inputs, exact float32 products for fp32)
 //
 //     S_t = S_{t-1} Diag(alpha_t) (I - b_t a_t^T) + v_t k_t^T,   o_t = S_t q_t
 //

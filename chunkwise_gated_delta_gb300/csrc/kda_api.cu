@@ -41,6 +41,11 @@ kda_status validate(const kda_fwd_args *a) {
     if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
     if (a->dv != 64 && a->dv != 128) return KDA_ERR_UNSUPPORTED;
     if (a->chunk != 0 && a->chunk != 64) return KDA_ERR_UNSUPPORTED;
+    // the tensor-core forward is laid out for 128 key channels (fp32 inputs take 64 too)
+    if (a->dtype == KDA_BF16 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
+    // the bf16 forward reads a per-channel gate as bf16 tiles
+    if (a->dtype == KDA_BF16 && a->gate_kind == KDA_GATE_CHANNEL && a->g_dtype != KDA_BF16)
+        return KDA_ERR_UNSUPPORTED;
     // outputs must not alias inputs (packed sequences: one [1, T, H, d] batch)
     const size_t es = dtype_size(a->dtype);
     const size_t nbt = (size_t)(a->cu_seqlens ? 1 : a->B) * a->T * a->H;

@@ -1,5 +1,7 @@
 // Backward of the chunkwise gated delta rule (KDA and its special cases),
-// float32 arithmetic on CUDA cores, chunk length C = 32.
+// chunk length C = 32, float32 accumulation: the chunk products are warp-level
+// tf32 tensor-core MMAs for bf16 inputs and exact float32 products on the CUDA
+// cores for fp32 inputs.
 //
 // Page "Kimi Delta Attention backward" derives, per chunk [t] and with dS the
 // gradient of the state after the chunk:

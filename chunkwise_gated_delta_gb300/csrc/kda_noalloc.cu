@@ -13,8 +13,6 @@
 // builds each chunk's Z inside the scan kernel and needs no records.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "kda.h"
 
 namespace {
@@ -26,21 +24,16 @@ constexpr size_t kNoAllocScratchBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // In host code `g_noalloc_scratch` names a host-side stand-in, not the device
-// array, so its device address is looked up once per device, with that
-// device current, and cached here.
-constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-cudaError_t scratch_address(int dev, void **out) {
-    std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+// array.  Its device address belongs to the CUDA context that is current, not
+// to the device number: after cudaDeviceReset, or under a driver-API context
+// other than the primary one, an address kept from an earlier call would point
+// at freed memory.  So every call looks it up again, with the caller's device
+// current; the lookup allocates nothing.
+cudaError_t scratch_address(void **out) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    *out = p;
     return cudaSuccess;
 }
 
@@ -54,11 +47,18 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const kda_fwd_args *args, kda_stream
     if (kda_chunk_fwd_workspace(&a) == 0) return kda_chunk_fwd(&a, stream);   // reports the argument error
     const size_t need = kNoAllocScratchBytes;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (s != nullptr) {
+        // the array of the current device is cleared and used on `stream`: both must be on it
+        int sdev = -1;
+        if (cudaStreamGetDevice(s, &sdev) != cudaSuccess) return KDA_ERR_CUDA;
+        if (sdev != dev) return KDA_ERR_INVALID_ARG;
+    }
     void *scratch = nullptr;
-    if (scratch_address(dev, &scratch) != cudaSuccess) return KDA_ERR_CUDA;
+    if (scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
     // The array keeps the previous call's contents: the status word must start at zero.
-    if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess)
         return KDA_ERR_CUDA;
     a.workspace = scratch;
     a.workspace_bytes = kNoAllocScratchBytes;

@@ -74,7 +74,9 @@ typedef enum {
 
 typedef struct {
     int B, T, H;           /* batch, sequence length (any T >= 1), heads */
-    int dk, dv;            /* key / value head dims: 64 or 128 each */
+    int dk, dv;            /* key / value head dims: 64 or 128 each; bfloat16 inputs need
+                              dk = 128 (dk = 64 returns KDA_ERR_UNSUPPORTED: the tensor-core
+                              kernels are laid out for 128 key channels; float32 inputs take 64) */
     int chunk;             /* chunk length C; 64 (0 selects 64) */
     kda_dtype dtype;       /* dtype of q, k, v, beta and o */
     kda_gate gate_kind;
@@ -147,8 +149,12 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
  * This entry point takes the same arguments as kda_chunk_fwd (workspace and
  * workspace_bytes are ignored) and uses instead an array owned by the
  * library: 256 bytes per device, held from library load until process exit.
- *   - The first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - Every call looks up the device address of the current device's array
+ *     (a lookup, not an allocation: the address belongs to the current CUDA
+ *     context, so none is kept between calls); the first call on a device may
+ *     load the library's device code, so make it before any stream capture.
+ *     `stream` must belong to the current device (KDA_ERR_INVALID_ARG
+ *     otherwise).
  *   - Every call clears the array's status word on `stream`, then launches.
  *     All calls share the array, so calls that overlap on the GPU (unordered
  *     streams) race on it.
@@ -209,7 +215,12 @@ typedef struct {
  */
 size_t kda_chunk_bwd_workspace(const kda_bwd_args *args);
 
-/* Backward of the chunkwise gated delta rule; float32 CUDA-core kernels. */
+/*
+ * Backward of the chunkwise gated delta rule: four kernels with float32
+ * accumulation.  For bfloat16 inputs the chunk products run as warp-level
+ * tf32 tensor-core MMAs (operands rounded to tf32); float32 inputs take exact
+ * float32 products on the CUDA cores.
+ */
 kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream);
 
 /* ------------------------------------------------------------------ DPLR */
@@ -332,7 +343,11 @@ typedef struct {
  */
 size_t dplr_chunk_bwd_workspace(const dplr_bwd_args *args);
 
-/* Backward of the general gated DPLR recurrence; float32 CUDA-core kernels. */
+/*
+ * Backward of the general gated DPLR recurrence: four kernels with float32
+ * accumulation; tf32 warp-level tensor-core products for bfloat16 inputs,
+ * exact float32 products for float32 inputs.
+ */
 kda_status dplr_chunk_bwd(const dplr_bwd_args *args, kda_stream_t stream);
 
 /*

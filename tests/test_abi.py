@@ -58,6 +58,9 @@ def _call(lib, a):
 def test_workspace_query(lib):
     assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args())) >= 4
     assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(dk=96))) == 0
+    # bf16 with dk = 64 is documented as unsupported (the fp32 path takes it): no workspace size
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(dk=64))) == 0
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(dk=64, dtype=_lib.KDA_F32, g_dtype=_lib.KDA_F32))) == 256
     assert lib.kda_chunk_fwd_workspace(None) == 0
 
 
@@ -77,6 +80,8 @@ def test_workspace_query(lib):
     (dict(dk=96), _lib.KDA_ERR_UNSUPPORTED),
     (dict(dv=32), _lib.KDA_ERR_UNSUPPORTED),
     (dict(chunk=32), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dk=64), _lib.KDA_ERR_UNSUPPORTED),                             # bf16 needs dk = 128
+    (dict(g_dtype=_lib.KDA_F32), _lib.KDA_ERR_UNSUPPORTED),              # bf16 channel gate in fp32
     (dict(workspace=None, workspace_bytes=0), _lib.KDA_ERR_WORKSPACE),
     (dict(workspace_bytes=16), _lib.KDA_ERR_WORKSPACE),
 ])

@@ -7,8 +7,11 @@ max_over_ranks) in two processes with the gloo backend, and check that the
 reference arm does its work on rank 0 only.
 """
 import argparse
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch.multiprocessing as mp
@@ -73,3 +76,28 @@ def test_replicas_draw_different_inputs(rank):
     w = custom("kda", 1, 64, 1, 64, 64, dtype=torch.float32, h0=False)
     mine, other = make_inputs(w, seed=rank), make_inputs(w, seed=1 - rank)
     assert not torch.equal(mine["q"], other["q"])
+
+
+def test_gpus_two_entry_launches_two_ranks():
+    """`bench.py --gpus 2` with no rank environment starts two ranks itself (gloo on CPU) and
+    rank 0 prints one line with n_gpus = 2 (the reference arm, on the small fp32 workload)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--workload", "kda_fp32_b1t256h1d64", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, env=env, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["impl"] == "reference"
+
+
+def test_gpus_mismatch_with_world_size_fails_loudly():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--workload", "kda_fp32_b1t256h1d64", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, env=env, timeout=300, cwd=root)
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr

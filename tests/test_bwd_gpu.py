@@ -108,13 +108,19 @@ def test_bf16_deterministic():
         assert np.array_equal(a[key], b[key]), key
 
 
-def test_full_kda_bwd_b4t4096h16d128_sampled_heads():
-    """The backward workload B4 T4096 H16 d128 bf16: every gradient of three sampled heads."""
+def test_full_kda_bwd_b4t4096h16d128_every_head():
+    """The backward workload B4 T4096 H16 d128 bf16: every gradient of every (batch, head) pair."""
     w = WORKLOADS["kda_bwd_bf16_b4t4096h16d128"]
     x = make_inputs(w, seed=0)
     got = run_gpu(x, "kda")
-    heads = [(0, 0), (2, 9), (3, 15)]
-    ref = run_oracle(x, "kda", heads=heads)
-    compare(got, ref, 5e-3, heads=heads)
     for v in got.values():
         assert np.isfinite(v).all()
+    ref = run_oracle(x, "kda")
+    worst = {}
+    for b in range(w.B):
+        for h in range(w.H):
+            errs = compare(got, ref, 5e-3, heads=[(b, h)])
+            for k, e in errs.items():
+                worst[k] = max(worst.get(k, 0.0), e)
+    print("parity: kda_bwd_bf16_b4t4096h16d128 worst head per gradient:",
+          {k: f"{e:.3e}" for k, e in worst.items()})

@@ -122,16 +122,17 @@ def test_deterministic():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_full_dplr_b2t8192h16d128_sampled_heads():
+def test_full_dplr_b2t8192h16d128_every_head():
     w = WORKLOADS["dplr_bf16_b2t8192h16d128"]
     x = make_inputs(w, seed=0)
     o, ht = run_gpu(x)
-    heads = [(0, 0), (1, 15)]
-    ro, rh = run_oracle(x, heads=heads)
-    for (b, h) in heads:
-        eo, eh = rel(o[b, :, h], ro[b, :, h]), rel(ht[b, h], rh[b, h])
-        assert eo <= 5e-3 and eh <= 5e-3, f"head {(b, h)}: o {eo:.3e} ht {eh:.3e}"
     assert np.isfinite(o).all() and np.isfinite(ht).all()
+    ro, rh = run_oracle(x)
+    eo = np.array([[rel(o[b, :, h], ro[b, :, h]) for h in range(w.H)] for b in range(w.B)])
+    eh = np.array([[rel(ht[b, h], rh[b, h]) for h in range(w.H)] for b in range(w.B)])
+    summary = f"dplr_bf16_b2t8192h16d128: worst head o {eo.max():.3e}, ht {eh.max():.3e}"
+    print("parity:", summary)
+    assert eo.max() <= 5e-3 and eh.max() <= 5e-3, summary
 
 
 # ---------------------------------------------------------------- transition norms

@@ -153,26 +153,55 @@ def test_bf16_deterministic():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-# ---------------------------------------------------------------- full-size workloads, sampled heads
-def _full(name, heads):
+# ---------------------------------------------------------------- full-size workloads, every head
+def chunk_errors(o, ro, C=64):
+    """Relative Frobenius error of every C-token chunk of every (batch, head) sequence: [B, H, N].
+
+    A diagnostic beside the per-head bound: one bad chunk (a ragged tail, a wrong slot) barely
+    moves the norm over thousands of rows, but stands out here."""
+    B, T, H = o.shape[:3]
+    n = -(-T // C)
+    out = np.zeros((B, H, n))
+    for c in range(n):
+        sl = slice(c * C, min(T, (c + 1) * C))
+        num = np.linalg.norm(o[:, sl] - ro[:, sl], axis=(1, 3))
+        den = np.maximum(np.linalg.norm(ro[:, sl], axis=(1, 3)), 1e-300)
+        out[:, :, c] = num / den
+    return out
+
+
+def _full(name, seed=0):
+    """Every (batch, head) pair of a full-size workload against the oracle, one bound per head."""
     w = WORKLOADS[name]
-    x = make_inputs(w, seed=0)
+    x = make_inputs(w, seed=seed)
     o, ht = run_gpu(x, w.variant)
-    ro, rh = run_oracle(x, w.variant, heads=heads)
-    for (b, h) in heads:
-        eo, eh = rel(o[b, :, h], ro[b, :, h]), rel(ht[b, h], rh[b, h])
-        assert eo <= 5e-3 and eh <= 5e-3, f"{name} head {(b, h)}: o {eo:.3e} ht {eh:.3e}"
+    ro, rh = run_oracle(x, w.variant)
     assert np.isfinite(o).all() and np.isfinite(ht).all()
+    eo = np.array([[rel(o[b, :, h], ro[b, :, h]) for h in range(w.H)] for b in range(w.B)])
+    eh = np.array([[rel(ht[b, h], rh[b, h]) for h in range(w.H)] for b in range(w.B)])
+    ec = chunk_errors(o, ro)
+    summary = (f"{name} seed {seed}: worst head o {eo.max():.3e} at {np.unravel_index(eo.argmax(), eo.shape)}, "
+               f"ht {eh.max():.3e}; median head o {np.median(eo):.3e}; worst 64-token chunk o {ec.max():.3e}")
+    print("parity:", summary)
+    bad = [(b, h) for b in range(w.B) for h in range(w.H) if not (eo[b, h] <= 5e-3 and eh[b, h] <= 5e-3)]
+    assert not bad, f"{len(bad)} heads over 5e-3, first {bad[:4]}; {summary}"
+    return eo, eh
 
 
-def test_full_kda_b4t4096h16d128_sampled_heads():
-    _full("kda_bf16_b4t4096h16d128", [(0, 0), (1, 7), (3, 15)])
+def test_full_kda_b4t4096h16d128_every_head():
+    _full("kda_bf16_b4t4096h16d128")
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3, 4])
+def test_full_kda_b4t4096h16d128_seed_spread(seed):
+    """Seeds 1-4 beside seed 0: the spread of the worst-head error over five seeds."""
+    _full("kda_bf16_b4t4096h16d128", seed=seed)
 
 
 @pytest.mark.parametrize("name", ["gdn_bf16_b8t2048h32d128", "deltanet_bf16_b8t2048h32d128",
                                   "gla_bf16_b8t2048h32d128"])
-def test_full_special_cases_sampled_heads(name):
-    _full(name, [(0, 0), (7, 31)])
+def test_full_special_cases_every_head(name):
+    _full(name)
 
 
 # ---------------------------------------------------------------- packed variable-length batches
