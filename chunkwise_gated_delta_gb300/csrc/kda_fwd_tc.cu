@@ -193,16 +193,6 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 __device__ __forceinline__ void st_u128(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
-__device__ __forceinline__ void st_u64(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
-__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
-    return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
-}
-__device__ __forceinline__ float4 ld_bf16x4(const uint8_t *p) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(p);
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-    return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
 // 32 fp32 values -> 64 bytes of bf16 at (row, col .. col+31) of a SW128 tile with `rows` rows.
 __device__ __forceinline__ void store_row32_bf16(uint8_t *tile, uint32_t rows, uint32_t row, uint32_t col,
                                                  const float *v) {
@@ -234,21 +224,6 @@ template <> __device__ __forceinline__ float ldg_f<__nv_bfloat16>(const __nv_bfl
 }
 template <> __device__ __forceinline__ float ldg_f<float>(const float *p) { return *p; }
 
-// ---- fp32 [64][64] scratch for the inverse, with an XOR swizzle on column
-// bits 2-4: float4 groups stay contiguous, and row walks spread over the banks.
-__device__ __forceinline__ uint32_t sidx(uint32_t i, uint32_t j) { return i * 64u + (j ^ ((i & 7u) << 2)); }
-
-struct Scratch {
-    uint8_t *base;
-    __device__ __forceinline__ float *L(uint32_t i, uint32_t j) const {
-        return reinterpret_cast<float *>(base + OFF_KR) + sidx(i, j);
-    }
-    // Y lives in the dead beta K<- rows of the A_G tile: rows 0-31 at +0, rows 32-63 at +16 KB.
-    __device__ __forceinline__ float *Y(uint32_t i, uint32_t j) const {
-        return reinterpret_cast<float *>(base + OFF_AG + (i >= 32 ? 16384u : 0u)) + sidx(i & 31u, j);
-    }
-};
-
 // Where a (batch, head) sequence lives: tensor-map batch coordinate, first row
 // and length.  Dense batches: (b, 0, T).  Packed variable-length batches
 // (cu_seqlens): (0, cu_seqlens[b], cu_seqlens[b + 1] - cu_seqlens[b]).
@@ -269,100 +244,183 @@ __device__ __forceinline__ int zslot0(const FwdParams &p, int b, const Seq &sq) 
     return p.cu_seqlens ? b + sq.t0 / kC : b * ((p.T + kC - 1) / kC);
 }
 
-// Accumulator fragments of a 16x16 block (two 16x8 halves) -> tf32 A fragments of the
-// same block (k-steps 0 and 1), times `sign`, by shuffles within the warp.
-__device__ __forceinline__ void frag_c_to_a(const float (&x)[2][4], uint32_t (&a)[2][4], int lane, float sign) {
-    const int g = lane >> 2, t = lane & 3;
-    const int s0 = 4 * g + (t >> 1), s1 = s0 + 2;
-    const bool odd = (t & 1) != 0;
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        const float v0 = __shfl_sync(0xffffffffu, x[ks][0], s0), v1 = __shfl_sync(0xffffffffu, x[ks][1], s0);
-        const float v2 = __shfl_sync(0xffffffffu, x[ks][2], s0), v3 = __shfl_sync(0xffffffffu, x[ks][3], s0);
-        const float w0 = __shfl_sync(0xffffffffu, x[ks][0], s1), w1 = __shfl_sync(0xffffffffu, x[ks][1], s1);
-        const float w2 = __shfl_sync(0xffffffffu, x[ks][2], s1), w3 = __shfl_sync(0xffffffffu, x[ks][3], s1);
-        a[ks][0] = to_tf32(sign * (odd ? v1 : v0));
-        a[ks][1] = to_tf32(sign * (odd ? v3 : v2));
-        a[ks][2] = to_tf32(sign * (odd ? w1 : w0));
-        a[ks][3] = to_tf32(sign * (odd ? w3 : w2));
-    }
-}
-
 // ---- Gamma and the rescaled tiles of one chunk, in place.  Raw g (channel
 // gate) sits in A_G rows 0-63, raw q in A_G rows 64-127 and raw k in the
 // 64-row tile at `kraw`.  Q<- replaces the raw q; GRAM: beta K<- goes to A_G
 // rows 0-63 and K-> to the K-> tile (the Gram's operands); SCAN: K<- goes to
-// the K<- tile.  K-> (packed bf16, 8 rows x 4 columns per thread) and gamma^C
-// (4 columns) come back for the chunk's slot.  Rows at or past `live_rows`
-// are zero; `bet` and `gs` hold the chunk's beta and scalar gate.  The 256 WY
-// threads (index wt), 4 columns x 8 rows each; one barrier inside.
+// the K<- tile.  Rows at or past `live_rows` are zero; `bet` and `gs` hold the
+// chunk's beta and scalar gate.  The 256 WY threads (index wt): warp w owns
+// rows 8w .. 8w + 7, its lanes 16 column groups of 8 (one 16-byte piece of a
+// swizzled row) by 2 row halves, so every load and store moves 16 bytes and
+// the in-chunk cumsum is a 4-row sum, one shuffle and one exchange of warp
+// totals through `tot` (one barrier).  K-> of the thread's 4 rows comes back in
+// `krv` for the chunk's slot; the thread holding row 63 also returns gamma^C of
+// its 8 columns in `gam` (`has_gam`).
 //   REC (the Z kernel of the record form): A_G rows 0-63 get K<- itself (beta is
 // applied to the rows of L instead, so the tile is also the B operand of Z K<-),
 // and K-> and gamma^C go straight to the chunk record `rec`.
+__device__ __forceinline__ void unpack_bf16x8(const uint4 u, float (&x)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8]) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+
 template <int GATE, bool GRAM, bool SCAN, bool REC = false>
 __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int wt, int live_rows, const float *bet,
-                                              const float *gs, float *tot, uint2 (&krv)[8], float4 &gcv,
-                                              uint8_t *rec = nullptr) {
-    const int cg = wt & 31, rg = wt >> 5;
-    const int col = 4 * cg;
-    float G[8][4];
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
+                                              const float *gs, float *tot, uint4 (&krv)[4], float (&gam)[8],
+                                              bool &has_gam, uint8_t *rec = nullptr) {
+    const int w = wt >> 5, lane = wt & 31;
+    const int cq = lane & 15, rsub = lane >> 4;
+    const int r0 = 8 * w + 4 * rsub;                 // first of the thread's 4 rows
+    const int col = 8 * cq;                          // first of its 8 columns
+    // byte offset of (r0 + i, col) in a 64-row / 128-row swizzled tile: r0 & 7 == 4 rsub
+    const uint32_t sw = (uint32_t)((cq & 7) ^ (4 * rsub));
+    const uint32_t o64 = (uint32_t)(cq >> 3) * 8192u + (uint32_t)r0 * 128u;
+    const uint32_t o128 = (uint32_t)(cq >> 3) * 16384u + (uint32_t)r0 * 128u;
+    auto off64 = [&](int i) { return o64 + (uint32_t)i * 128u + ((sw ^ (uint32_t)i) << 4); };
+    auto off128 = [&](int i) { return o128 + (uint32_t)i * 128u + ((sw ^ (uint32_t)i) << 4); };
+
+    float G[4][8];                                   // in-chunk cumsum of g, base-2 units, this thread's rows
+    has_gam = (w == 7 && rsub == 1);
+    if constexpr (GATE == KDA_GATE_NONE) {
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int row = rg * 8 + r;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (row >= live_rows) {
-        } else if (GATE == KDA_GATE_CHANNEL) {
-            const float4 gg = ld_bf16x4(base + OFF_AG + sw128_offset(128, row, col));
-            x[0] = gg.x; x[1] = gg.y; x[2] = gg.z; x[3] = gg.w;
-        } else if (GATE == KDA_GATE_SCALAR) {
-            x[0] = x[1] = x[2] = x[3] = gs[row];
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) G[i][e] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gam[e] = 1.f;
+    } else {
+        float a[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = r0 + i;
+            float x[8];
+            if (GATE == KDA_GATE_CHANNEL) {
+                const uint4 u = row < live_rows ? *reinterpret_cast<const uint4 *>(base + OFF_AG + off128(i))
+                                                : make_uint4(0u, 0u, 0u, 0u);
+                unpack_bf16x8(u, x);
+            } else {
+                const float s = row < live_rows ? gs[row] : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = s;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { a[e] += x[e]; G[i][e] = a[e]; }
+        }
+        // the lower half-warp (rows + 4) adds the upper half's 4-row total; lanes 16-31 then hold
+        // the warp's 8-row total, which goes to the other warps through `tot`
+        float pre[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float up = __shfl_up_sync(0xffffffffu, a[e], 16);
+            pre[e] = rsub ? up : 0.f;
+            a[e] += pre[e];
+        }
+        if (rsub) {
+            *reinterpret_cast<float4 *>(tot + w * kDK + col) = make_float4(a[0], a[1], a[2], a[3]);
+            *reinterpret_cast<float4 *>(tot + w * kDK + col + 4) = make_float4(a[4], a[5], a[6], a[7]);
+        }
+        named_sync(2, kWyThreads);
+        for (int q = 0; q < w; ++q) {                // warp-uniform bound
+            const float4 t0 = *reinterpret_cast<const float4 *>(tot + q * kDK + col);
+            const float4 t1 = *reinterpret_cast<const float4 *>(tot + q * kDK + col + 4);
+            pre[0] += t0.x; pre[1] += t0.y; pre[2] += t0.z; pre[3] += t0.w;
+            pre[4] += t1.x; pre[5] += t1.y; pre[6] += t1.z; pre[7] += t1.w;
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) { a[e] += x[e]; G[r][e] = a[e]; }
-    }
-    *reinterpret_cast<float4 *>(tot + rg * kDK + col) = make_float4(a[0], a[1], a[2], a[3]);
-    named_sync(2, kWyThreads);
-    float pre[4] = {0.f, 0.f, 0.f, 0.f}, all[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int e = 0; e < 8; ++e) {
+            const float p2 = pre[e] * kLog2e;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 t4 = *reinterpret_cast<const float4 *>(tot + q * kDK + col);
-        const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (q < rg) pre[e] += tv[e];
-            all[e] += tv[e];
+            for (int i = 0; i < 4; ++i) G[i][e] = fmaf(G[i][e], kLog2e, p2);
+            gam[e] = ex2_approx(G[3][e]);            // meaningful on the thread that holds row 63
         }
     }
-    gcv = make_float4(__expf(all[0]), __expf(all[1]), __expf(all[2]), __expf(all[3]));
-    if (REC && rg == 0) *reinterpret_cast<float4 *>(rec + REC_GC + 4 * col) = gcv;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int row = rg * 8 + r;
-        const uint32_t o64 = sw128_offset(64, row, col);
-        const uint32_t otop = sw128_offset(128, row, col), obot = sw128_offset(128, 64 + row, col);
-        const bool live = row < live_rows;
-        const float4 q4 = live ? ld_bf16x4(base + OFF_AG + obot) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 k4 = live ? ld_bf16x4(base + kraw + o64) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-        const float bb = REC ? 1.f : bet[row];
-        float kl[4], kr4[4], ql[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float g2 = (G[r][e] + pre[e]) * kLog2e;   // G in base-2 units
-            const float ev = ex2_approx(g2), iv = ex2_approx(-g2);
-            kl[e] = kv[e] * ev;
-            kr4[e] = kv[e] * iv;
-            ql[e] = qv[e] * ev;
-        }
-        const uint2 kr = pack4(kr4[0], kr4[1], kr4[2], kr4[3]);
-        if (GRAM) st_u64(base + OFF_AG + otop, pack4(bb * kl[0], bb * kl[1], bb * kl[2], bb * kl[3]));
-        st_u64(base + OFF_AG + obot, pack4(ql[0], ql[1], ql[2], ql[3]));
-        if (GRAM) st_u64(base + OFF_KR + o64, kr);
-        if (SCAN) st_u64(base + OFF_KL + o64, pack4(kl[0], kl[1], kl[2], kl[3]));
-        krv[r] = kr;
-        if (REC) st_u64(rec + REC_KR + o64, kr);
+    if (REC && has_gam) {
+        *reinterpret_cast<float4 *>(rec + REC_GC + 4 * col) = make_float4(gam[0], gam[1], gam[2], gam[3]);
+        *reinterpret_cast<float4 *>(rec + REC_GC + 4 * col + 16) = make_float4(gam[4], gam[5], gam[6], gam[7]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool live = r0 + i < live_rows;
+        const uint4 uq = live ? *reinterpret_cast<const uint4 *>(base + OFF_AG + off128(i) + 8192u)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 uk = live ? *reinterpret_cast<const uint4 *>(base + kraw + off64(i)) : make_uint4(0u, 0u, 0u, 0u);
+        float qv[8], kv[8], kl[8], kr[8], ql[8];
+        unpack_bf16x8(uq, qv);
+        unpack_bf16x8(uk, kv);
+        const float bb = (REC || !GRAM) ? 1.f : bet[r0 + i];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if constexpr (GATE == KDA_GATE_NONE) {
+                kl[e] = kv[e]; kr[e] = kv[e]; ql[e] = qv[e];
+            } else {
+                const float ev = ex2_approx(G[i][e]), iv = ex2_approx(-G[i][e]);
+                kl[e] = kv[e] * ev;
+                kr[e] = kv[e] * iv;
+                ql[e] = qv[e] * ev;
+            }
+        }
+        const uint4 krp = pack_bf16x8(kr);
+        *reinterpret_cast<uint4 *>(base + OFF_AG + off128(i) + 8192u) = pack_bf16x8(ql);
+        if (GRAM) {
+            float bk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bk[e] = bb * kl[e];
+            *reinterpret_cast<uint4 *>(base + OFF_AG + off128(i)) = pack_bf16x8(bk);
+            *reinterpret_cast<uint4 *>(base + OFF_KR + off64(i)) = krp;
+        }
+        if (SCAN) *reinterpret_cast<uint4 *>(base + OFF_KL + off64(i)) = pack_bf16x8(kl);
+        krv[i] = krp;
+        if (REC) *reinterpret_cast<uint4 *>(rec + REC_KR + off64(i)) = krp;
+    }
+}
+// Slot image of the K-> rows a thread of rescale_tiles produced (its 4 rows x 8 columns) and,
+// from the thread that holds row 63, gamma^C of its 8 columns.
+__device__ __forceinline__ void store_kr_slot(uint8_t *kt, float *gc, int wt, const uint4 (&krv)[4],
+                                              const float (&gam)[8], bool has_gam) {
+    const int w = wt >> 5, lane = wt & 31;
+    const int cq = lane & 15, rsub = lane >> 4;
+    const int r0 = 8 * w + 4 * rsub;
+    const uint32_t sw = (uint32_t)((cq & 7) ^ (4 * rsub));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4 *>(kt + (uint32_t)(cq >> 3) * 8192u + (uint32_t)(r0 + i) * 128u +
+                                   ((sw ^ (uint32_t)i) << 4)) = krv[i];
+    if (has_gam) {
+        *reinterpret_cast<float4 *>(gc + 8 * cq) = make_float4(gam[0], gam[1], gam[2], gam[3]);
+        *reinterpret_cast<float4 *>(gc + 8 * cq + 4) = make_float4(gam[4], gam[5], gam[6], gam[7]);
+    }
+}
+
+// ---- Fragment images of the block back-substitution's B operands: tf32
+// values in the order the warp MMAs read them, 256 floats per 16x16 block
+// ([k-step][n-half][lane][2]).  The k index of every 8-wide k-step is taken
+// in the order 0, 2, 4, 6 | 1, 3, 5, 7 (slot t holds k = 2t, slot t + 4 holds
+// k = 2t + 1), which makes an accumulator fragment (row g, columns 2t, 2t + 1)
+// the A fragment of the next product as it stands: no shuffles.
+__device__ __forceinline__ int frag_pos(int r, int cc) {   // element (r, cc) of a 16x16 block
+    return (((r >> 3) * 2 + (cc >> 3)) * 32 + 4 * (cc & 7) + ((r & 7) >> 1)) * 2 + (r & 1);
+}
+// Accumulator fragment of a 16x8 half (columns 2t, 2t + 1 of rows g, g + 8) as the
+// k-permuted tf32 A fragment of one k-step, times `sign`.
+__device__ __forceinline__ void acc_as_a(const float (&x)[4], uint32_t (&a)[4], float sign) {
+    a[0] = to_tf32(sign * x[0]);
+    a[1] = to_tf32(sign * x[2]);
+    a[2] = to_tf32(sign * x[1]);
+    a[3] = to_tf32(sign * x[3]);
+}
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
 }
 
 // ---- Z = [T ; P T] of one chunk (GLA: [I ; P]) from its rescaled tiles, as a
@@ -370,19 +428,19 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
 // into TMEM, L and the inverses of its 16x16 diagonal blocks, the block
 // back-substitution, the beta scaling.  The 256 WY threads enter after the
 // barrier that follows their stores of the rescaled tiles; `ph` is the parity
-// of the Gram barrier.  Returns the first of the 16 Z rows this warp wrote;
+// of the Gram barrier.  `yfrag` (4 KB, free by then) receives the diagonal-block
+// inverses and the K-> tile, dead after the Gram, the off-diagonal blocks of L,
+// both as fragment images.  Returns the first of the 16 Z rows this warp wrote;
 // ends without a barrier.
 //   REC: rows 0-63 of the Gram are K<- K->^T (A_G holds K<-, not beta K<-), so
-// beta scales them as they leave TMEM; the inverses of the diagonal blocks go
-// to `yfrag` (4 KB) in the order of the MMA B fragments that read them, and
-// A_G is left alone.
+// beta scales them as they leave TMEM.
 template <bool GLA, bool REC = false>
-__device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, float *yfrag = nullptr) {
+__device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, float *yfrag) {
     uint8_t *base = c.base;
     const int ww = wt >> 5, lane = wt & 31;
     const int quarter = ww & 3, half = ww >> 2;
     const bool leader = wt == 0;
-    const Scratch sc{base};
+    float *lfrag = reinterpret_cast<float *>(base + OFF_KR);
     // ---------------- Gram: D_G = [beta K<- ; Q<-] K->^T   (M128 N64 K128)
     if (leader) {
         tc_fence_after();
@@ -402,7 +460,8 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, floa
     const int row = quarter * 32 + lane;   // TMEM lane owned by this thread
 
     if (!GLA) {
-        // ---- L (strictly lower, rows carry beta) to fp32 scratch in the K-> tile (dead now)
+        // ---- L (strictly lower, rows carry beta): the off-diagonal blocks as fragment images in
+        //      the (dead) K-> tile; the two diagonal blocks of the warps on the diagonal inverted
         if (quarter < 2) {
             float v[32];
             tmem_ld32(c.tmem + TM_G + lane_base + half * 32, v);
@@ -411,15 +470,16 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, floa
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] *= br;
             }
+            const int brow = row >> 4, rr = row & 15;
+            // the Gram barrier above has ordered the tensor core's reads of the K-> tile
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int col = half * 32 + 4 * q;
-                float4 f;
-                f.x = col + 0 < row ? v[4 * q + 0] : 0.f;
-                f.y = col + 1 < row ? v[4 * q + 1] : 0.f;
-                f.z = col + 2 < row ? v[4 * q + 2] : 0.f;
-                f.w = col + 3 < row ? v[4 * q + 3] : 0.f;
-                *reinterpret_cast<float4 *>(sc.L(row, col)) = f;
+            for (int hb = 0; hb < 2; ++hb) {
+                const int bc = 2 * half + hb;
+                if (bc < brow) {
+                    float *dst = lfrag + (brow * (brow - 1) / 2 + bc) * 256;
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) dst[frag_pos(rr, cc)] = __uint_as_float(to_tf32(v[16 * hb + cc]));
+                }
             }
             if (quarter == half) {
                 // Level 0 of the inverse: this warp holds the two 16x16 diagonal blocks of its
@@ -441,21 +501,9 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, floa
                         y[cc] -= lj * yj;
                     }
                 }
-                const int o = quarter * 32 + seg * 16;
-                if (REC) {
-                    // element (r, cc) of block bb is entry (r >> 2) & 1 of lane 4 (cc & 7) + (r & 3)
-                    // in the fragment of (bb, k-step r >> 3, column half cc >> 3)
-                    const int bb = o >> 4;
+                float *yb = yfrag + ((quarter * 32 + seg * 16) >> 4) * 256;
 #pragma unroll
-                    for (int cc = 0; cc < 16; ++cc)
-                        yfrag[(((bb * 2 + (r >> 3)) * 2 + (cc >> 3)) * 32 + 4 * (cc & 7) + (r & 3)) * 2 +
-                              ((r >> 2) & 1)] = y[cc];
-                } else {
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-                        *reinterpret_cast<float4 *>(sc.Y(row, o + 4 * c4)) =
-                            make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
-                }
+                for (int cc = 0; cc < 16; ++cc) yb[frag_pos(r, cc)] = __uint_as_float(to_tf32(y[cc]));
             }
         }
         named_sync(2, kWyThreads);
@@ -464,95 +512,103 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, floa
     // ---------------- Z' (I + L) = [I ; P] by block back-substitution over 16-column blocks,
     // 16 rows of Z' per warp: Z'_b = ([I ; P]_b - sum_{b' > b} Z'_{b'} L_{b'b}) Y_bb with
     // Y_bb = (I + L_bb)^{-1} (block form 2 of page "DeltaNet" 4.2, on the transposed system).
-    // Then Z = Z' Diag(beta) = [T ; P T].  For GLA (beta = 0, v unscaled) Z = [I ; P].
-    float zb[4][2][4];                                     // Z' blocks, accumulator-fragment layout
+    // Z' = [T' ; P T'] with T' lower triangular and P lower triangular, so the blocks right of
+    // the warp's own row block R are zero and are skipped.  Then Z = Z' Diag(beta) = [T ; P T],
+    // kept as packed bf16 in the stmatrix register order.  For GLA (beta = 0, v unscaled)
+    // Z = [I ; P].
     const int r0 = quarter * 32 + half * 16;               // first row of Z' owned by this warp
+    const int R = (r0 & 63) >> 4;
+    uint32_t zp[4][4];                                     // Z blocks, bf16 pairs, stmatrix order
     {
         const int g = lane >> 2, t = lane & 3;
-        uint32_t za[4][2][4];                              // -Z' blocks as tf32 A fragments
+        uint32_t za[4][2][4];                              // -Z' blocks as k-permuted tf32 A fragments
 #pragma unroll
         for (int bb = 3; bb >= 0; --bb) {
+            if (bb > R) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) zp[bb][m] = 0u;
+                continue;
+            }
             float acc[2][4];
             if (quarter < 2) {                             // identity rows
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        acc[nh][e] = (r0 + g + 8 * (e >> 1) == 16 * bb + 8 * nh + 2 * t + (e & 1)) ? 1.f : 0.f;
+                        acc[nh][e] = (bb == R && g + 8 * (e >> 1) == 8 * nh + 2 * t + (e & 1)) ? 1.f : 0.f;
             } else {                                       // rows of P = Q<- K->^T * M (inclusive)
                 float pv[8];
                 tmem_ld16x256b_x2(c.tmem + TM_G + ((uint32_t)r0 << 16) + 16 * bb, pv);
-                const int i0 = r0 - 64;
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        acc[nh][e] = (16 * bb + 8 * nh + 2 * t + (e & 1) <= i0 + g + 8 * (e >> 1)) ? pv[4 * nh + e]
-                                                                                                  : 0.f;
+                        acc[nh][e] = (bb < R || 8 * nh + 2 * t + (e & 1) <= g + 8 * (e >> 1)) ? pv[4 * nh + e] : 0.f;
             }
+            float zb[2][4];
             if (!GLA) {
 #pragma unroll
-                for (int bp = bb + 1; bp < 4; ++bp)
+                for (int bp = bb + 1; bp < 4; ++bp) {
+                    if (bp > R) continue;
+                    const float *lb = lfrag + (bp * (bp - 1) / 2 + bb) * 256;
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
                         for (int nh = 0; nh < 2; ++nh) {
-                            const uint32_t bf[2] = {to_tf32(*sc.L(16 * bp + 8 * ks + t, 16 * bb + 8 * nh + g)),
-                                                    to_tf32(*sc.L(16 * bp + 8 * ks + t + 4, 16 * bb + 8 * nh + g))};
+                            const float2 lf = *reinterpret_cast<const float2 *>(lb + ((ks * 2 + nh) * 32 + lane) * 2);
+                            const uint32_t bf[2] = {__float_as_uint(lf.x), __float_as_uint(lf.y)};
                             mma_tf32_16x8x8(acc[nh], za[bp][ks], bf);
                         }
+                }
                 uint32_t af[2][4];
-                frag_c_to_a(acc, af, lane, 1.f);
+                acc_as_a(acc[0], af[0], 1.f);
+                acc_as_a(acc[1], af[1], 1.f);
+                const float *yb = yfrag + bb * 256;
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) zb[bb][nh][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) zb[nh][e] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
-                        uint32_t bf[2];
-                        if (REC) {
-                            const float2 y2 =
-                                *reinterpret_cast<const float2 *>(yfrag + (((bb * 2 + ks) * 2 + nh) * 32 + lane) * 2);
-                            bf[0] = to_tf32(y2.x);
-                            bf[1] = to_tf32(y2.y);
-                        } else {
-                            bf[0] = to_tf32(*sc.Y(16 * bb + 8 * ks + t, 16 * bb + 8 * nh + g));
-                            bf[1] = to_tf32(*sc.Y(16 * bb + 8 * ks + t + 4, 16 * bb + 8 * nh + g));
-                        }
-                        mma_tf32_16x8x8(zb[bb][nh], af[ks], bf);
+                        const float2 yf = *reinterpret_cast<const float2 *>(yb + ((ks * 2 + nh) * 32 + lane) * 2);
+                        const uint32_t bf[2] = {__float_as_uint(yf.x), __float_as_uint(yf.y)};
+                        mma_tf32_16x8x8(zb[nh], af[ks], bf);
                     }
-                if (bb > 0) frag_c_to_a(zb[bb], za[bb], lane, -1.f);
+                if (bb > 0) {
+                    acc_as_a(zb[0], za[bb][0], -1.f);
+                    acc_as_a(zb[1], za[bb][1], -1.f);
+                }
             } else {
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) zb[bb][nh][e] = acc[nh][e];
+                    for (int e = 0; e < 4; ++e) zb[nh][e] = acc[nh][e];
+            }
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+                float b0 = 1.f, b1 = 1.f;
+                if (!GLA) {
+                    const float2 b2 = *reinterpret_cast<const float2 *>(bet + 16 * bb + 8 * nh + 2 * t);
+                    b0 = b2.x;
+                    b1 = b2.y;
+                }
+                zp[bb][2 * nh] = pack_bf16(zb[nh][0] * b0, zb[nh][1] * b1);       // rows g
+                zp[bb][2 * nh + 1] = pack_bf16(zb[nh][2] * b0, zb[nh][3] * b1);   // rows g + 8
             }
         }
     }
     if (!GLA) named_sync(2, kWyThreads);                   // every warp is done with L in the K-> tile
-    // ---------------- Z = Z' Diag(beta) -> bf16 K-major 128 x 64 tile in the K-> tile
+    // ---------------- Z -> bf16 K-major 128 x 64 tile in the K-> tile: one stmatrix per 16x16 block,
+    // lane l giving the address of row l & 7 of 8x8 matrix l >> 3 (rows + 8 for odd matrices,
+    // columns + 8 for the last two)
     {
-        const int g = lane >> 2, t = lane & 3;
-        uint8_t *zt = base + OFF_KR;
+        const uint32_t zt = smem_u32(base + OFF_KR);
+        const int mi = lane >> 3;
+        const uint32_t zrow = (uint32_t)(r0 + (lane & 7) + 8 * (mi & 1));
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb)
-#pragma unroll
-            for (int nh = 0; nh < 2; ++nh) {
-                const int c0 = 16 * bb + 8 * nh + 2 * t;
-                float b0 = 1.f, b1 = 1.f;
-                if (!GLA) {
-                    const float2 b2 = *reinterpret_cast<const float2 *>(bet + c0);
-                    b0 = b2.x;
-                    b1 = b2.y;
-                }
-                *reinterpret_cast<uint32_t *>(zt + sw128_offset(128, r0 + g, c0)) =
-                    pack_bf16(zb[bb][nh][0] * b0, zb[bb][nh][1] * b1);
-                *reinterpret_cast<uint32_t *>(zt + sw128_offset(128, r0 + g + 8, c0)) =
-                    pack_bf16(zb[bb][nh][2] * b0, zb[bb][nh][3] * b1);
-            }
+        for (int bb = 0; bb < 4; ++bb) stmatrix_x4(zt + sw128_offset(128, zrow, 16 * bb + 8 * (mi >> 1)), zp[bb]);
     }
     return r0;
 }
@@ -580,7 +636,6 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     const __nv_bfloat16 *betag = static_cast<const __nv_bfloat16 *>(p.beta);
     const Tg *gsg = static_cast<const Tg *>(p.g);
     const uint32_t raw_bytes = (GATE == KDA_GATE_CHANNEL ? 3u : 2u) * 16384u;
-    const Scratch sc{base};
     const int step = PAIR ? 2 : 1;                       // distance between chunks this CTA builds
     const int first = PAIR ? (int)c.rank : 0;
     auto owns = [&](int n) { return !PAIR || (n & 1) == (int)c.rank; };
@@ -638,8 +693,9 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         const float *bet = betas + sb * kC;
         float nb = 0.f, ng = 0.f;
         const uint32_t peer_base = PAIR ? map_to_rank(smem_u32(base), c.rank ^ 1u) : 0u;
-        uint2 krv[8];
-        float4 gcv;
+        uint4 krv[4];
+        float gam[8];
+        bool has_gam;
         int r0 = 0;                                          // first of the 16 Z rows this warp built
 
         {
@@ -647,11 +703,12 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             wait_bar(c, B_RAW, phm);
             // ---------------- prologue: Gamma and the rescaled tiles, in place.  K-> and gamma^C also
             // go to the chunk's slot, written at the end (the slot may still be in use).
-            rescale_tiles<GATE, true, true>(base, OFF_KL, wt, sq.len - n * kC, bet, gss + sb * kC, tot, krv, gcv);
+            rescale_tiles<GATE, true, true>(base, OFF_KL, wt, sq.len - n * kC, bet, gss + sb * kC, tot, krv, gam,
+                                            has_gam);
             fence_proxy_async_smem();
             named_sync(2, kWyThreads);
 
-            r0 = build_z<GLA>(c, wt, bet, phm);
+            r0 = build_z<GLA>(c, wt, bet, phm, tot);
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(2, kWyThreads);
@@ -736,17 +793,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             }
         }
         // ---------------- K-> and gamma^C into slot s (and the other CTA's slot s)
-        {
-            const int cg = wt & 31, rg = wt >> 5;
-            const int col = 4 * cg;
-            uint8_t *kt = base + off_kt(s);
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const uint32_t o64 = sw128_offset(64, rg * 8 + r, col);
-                st_u64(kt + o64, krv[r]);
-            }
-            if (rg == 0) *reinterpret_cast<float4 *>(gC + s * kDK + col) = gcv;
-        }
+        store_kr_slot(base + off_kt(s), gC + s * kDK, wt, krv, gam, has_gam);
         if (wt < kC && n + step < nchunks) {
             betas[(sb ^ 1) * kC + wt] = nb;
             gss[(sb ^ 1) * kC + wt] = ng;
@@ -1090,9 +1137,11 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     __syncthreads();                        // the scalars
 
     uint8_t *rec = p.zrec + ((size_t)(zslot0(p, b, sq) + n) * H + h) * kRecBytes;
-    uint2 krv[8];
-    float4 gcv;
-    rescale_tiles<GATE, true, false, true>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gcv, rec);
+    uint4 krv[4];
+    float gam[8];
+    bool has_gam;
+    rescale_tiles<GATE, true, false, true>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gam, has_gam,
+                                           rec);
     fence_proxy_async_smem();
     __syncthreads();
     // the cumsum partials are dead: their 4 KB hold the diagonal-block inverses
