@@ -52,7 +52,18 @@ KERNELS = {"kda": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gdn": ("kda_fwd_tc", "kda_fw
            "dplr": ("dplr_fwd_simt", "dplr_fwd_simt.cu"), "kda_bwd": ("kda_bwd_simt", "kda_bwd_simt.cu"),
            "dplr_bwd": ("dplr_bwd_simt", "dplr_bwd_simt.cu")}
 LAUNCHES_PER_STEP = {"kda": 2, "gdn": 2, "deltanet": 2, "gla": 1, "dplr": 2, "kda_bwd": 4,
-                     "dplr_bwd": 4}   # kernels one step launches
+                     "dplr_bwd": 4}   # kernels one step launches (bf16 forward: its two-kernel form)
+
+
+def forward_form(w, d, o, ht, gate, scale_v):
+    """Which form the library runs for this forward: 'single' (one kernel, the status word as
+    workspace) or 'records' (chunk-record kernel + scan), read from its workspace query."""
+    import ctypes
+
+    from chunkwise_gated_delta_gb300 import _lib, api
+    a = api.make_args(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), o, ht, gate=gate,
+                      scale_v=scale_v)
+    return "single" if _lib.load().kda_chunk_fwd_workspace(ctypes.byref(a)) <= 256 else "records"
 
 
 def kind_of(w) -> str:
@@ -356,6 +367,12 @@ def run_ours(args, rank, world, local):
             kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), gate=gate,
                           scale_v=x["scale_v"], o=o, ht=ht, stream=stream)
 
+    launches = LAUNCHES_PER_STEP.get(kind_of(w), 1)
+    form = None
+    if kind_of(w) in ("kda", "gdn", "deltanet", "gla"):
+        form = forward_form(w, d, o, ht, gate, x["scale_v"])
+        launches = 1 if form == "single" else 2
+
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -432,12 +449,13 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_per_launch(w),
                      "kernel": KERNELS[kind_of(w)][0],
-                     "scope": f"whole step: {LAUNCHES_PER_STEP.get(kind_of(w), 1)} kernel launch(es) per step, "
+                     "form": form,
+                     "scope": f"whole step: {launches} kernel launch(es) per step, "
                               "timed together between CUDA events",
                      "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                      "algorithmic_bytes_per_launch": abytes, "kernel_ms_per_launch": launch_ms},
         "e2e": e2e,
-        "gpu_launches": args.steps * LAUNCHES_PER_STEP.get(kind_of(w), 1),
+        "gpu_launches": args.steps * launches,
         "clocks": clk,
     }
     if kind_of(w) == "dplr":

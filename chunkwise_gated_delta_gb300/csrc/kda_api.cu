@@ -227,11 +227,26 @@ kda_status from_cuda(cudaError_t e) {
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Streaming multiprocessors of the current device (0 if the query fails).
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
 // Chunk-record bytes of the two-kernel bf16 forward, 0 where the single kernel is the faster
-// form: float32 inputs, and GLA (beta = 0, v unscaled), which has no inverse to hoist.
+// form: float32 inputs; GLA (beta = 0, v unscaled), which has no inverse to hoist; and batches
+// whose single-kernel CTAs (one per 64-value slice of each sequence and head) fill between half
+// and all of the SMs in one wave -- there every SM builds its own chunks' operands next to its
+// scan and no records travel through HBM, while fewer CTAs leave most SMs idle and more CTAs
+// take several waves, where the chunk-parallel record kernel on every SM wins.
 size_t fwd_record_bytes(const kda_fwd_args *a) {
     const bool gla = !(a->flags & KDA_FLAG_BETA_SCALES_V);
     if (a->dtype != KDA_BF16 || gla) return 0;
+    const long long ctas = (long long)a->B * a->H * (a->dv / 64);
+    const int sms = sm_count();
+    if (sms > 0 && 2 * ctas > sms && ctas <= sms) return 0;
     return kda::fwd_zrec_bytes(a->B, a->T, a->H, a->cu_seqlens != nullptr);
 }
 

@@ -108,7 +108,7 @@ constexpr uint32_t kPushBytes = 16384 + 32768 + 16384 + 512;
 // products the scan forms, plus gamma^C.
 constexpr uint32_t REC_Z = 0;            // Z = [T ; P T], K-major 128 x 64 (A of Z V)
 constexpr uint32_t REC_A = 16384;        // A_chain = [-W ; Q<- - P W], K-major 128 x 128 (A of A_chain S^T)
-constexpr uint32_t REC_KR = 49152;       // K->, 64 x 128 (MN-major A of K->^T V_new)
+constexpr uint32_t REC_KR = 49152;       // K~ = K exp(G_C - G), 64 x 128 (MN-major A of K~^T V_new)
 constexpr uint32_t REC_GC = 65536;       // gamma^C [128] f32
 constexpr uint32_t kRecBytes = 66048;
 
@@ -122,7 +122,7 @@ constexpr uint32_t kTmemCols = 512;
 // mbarrier indices
 enum {
     B_RAW = 0, B_V0, B_V1, B_GRAM, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
-    B_RX, B_PFREE, B_FIN0, B_FIN1, kNumBars
+    B_RX, B_PFREE, B_FIN0, B_FIN1, B_RAWK, B_RAWQ, kNumBars
 };
 static_assert(kNumBars <= 24, "mbarrier slots");
 
@@ -161,8 +161,10 @@ __device__ __forceinline__ void note_abort(const Ctx &c, int idx, uint32_t parit
     if (threadIdx.x == kChainThreads) atomicCAS(c.status + 6, 0, idx + 1 + 256 * (int)parity);
 }
 
-// Bounded wait that becomes a no-op once any thread of the CTA has given up.
-__device__ __noinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
+// Bounded wait that becomes a no-op once any thread of the CTA has given up.  The
+// first probe is inline: most waits find their phase already complete, and a call
+// to the out-of-line loop would move the caller's live registers through local memory.
+__device__ __noinline__ void wait_bar_slow(const Ctx &c, int idx, uint32_t parity) {
     uint64_t *bar = c.bars + idx;
     for (uint32_t i = 0; i < kWaitBound; ++i) {
         if (mbar_try_wait(bar, parity)) return;
@@ -173,8 +175,11 @@ __device__ __noinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
     }
     record_timeout(c, idx, parity);
 }
+__device__ __forceinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
+    if (!mbar_try_wait(c.bars + idx, parity)) wait_bar_slow(c, idx, parity);
+}
 // The same for barriers completed from the other CTA of the pair.
-__device__ __noinline__ void wait_bar_cluster(const Ctx &c, int idx, uint32_t parity) {
+__device__ __noinline__ void wait_bar_cluster_slow(const Ctx &c, int idx, uint32_t parity) {
     uint64_t *bar = c.bars + idx;
     for (uint32_t i = 0; i < kWaitBound; ++i) {
         if (mbar_try_wait_cluster(bar, parity)) return;
@@ -184,6 +189,9 @@ __device__ __noinline__ void wait_bar_cluster(const Ctx &c, int idx, uint32_t pa
         }
     }
     record_timeout(c, idx, parity);
+}
+__device__ __forceinline__ void wait_bar_cluster(const Ctx &c, int idx, uint32_t parity) {
+    if (!mbar_try_wait_cluster(c.bars + idx, parity)) wait_bar_cluster_slow(c, idx, parity);
 }
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -271,10 +279,10 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8]) {
     return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
 }
 
-template <int GATE, bool GRAM, bool SCAN, bool REC = false>
+template <int GATE, bool GRAM, bool SCAN, bool REC = false, typename PreQK>
 __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int wt, int live_rows, const float *bet,
                                               const float *gs, float *tot, uint4 (&krv)[4], float (&gam)[8],
-                                              bool &has_gam, uint8_t *rec = nullptr) {
+                                              bool &has_gam, PreQK &&pre_qk, uint8_t *rec = nullptr) {
     const int w = wt >> 5, lane = wt & 31;
     const int cq = lane & 15, rsub = lane >> 4;
     const int r0 = 8 * w + 4 * rsub;                 // first of the thread's 4 rows
@@ -317,12 +325,17 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
         }
         // the lower half-warp (rows + 4) adds the upper half's 4-row total; lanes 16-31 then hold
         // the warp's 8-row total, which goes to the other warps through `tot`
-        float pre[8];
+        float pre[8], rest[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float up = __shfl_up_sync(0xffffffffu, a[e], 16);
+            const float own = a[e];                  // this thread's 4-row sum
+            const float up = __shfl_up_sync(0xffffffffu, own, 16);
             pre[e] = rsub ? up : 0.f;
-            a[e] += pre[e];
+            a[e] = own + pre[e];                     // lanes 16-31: the warp's 8-row total
+            // REC: what the chunk adds after this thread's last row, starting with the lower
+            // half-warp's rows for the upper half (the warp total from lanes 16-31 less its own)
+            const float dn = __shfl_down_sync(0xffffffffu, a[e], 16);
+            rest[e] = rsub ? 0.f : dn - own;
         }
         if (rsub) {
             *reinterpret_cast<float4 *>(tot + w * kDK + col) = make_float4(a[0], a[1], a[2], a[3]);
@@ -335,37 +348,49 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
             pre[0] += t0.x; pre[1] += t0.y; pre[2] += t0.z; pre[3] += t0.w;
             pre[4] += t1.x; pre[5] += t1.y; pre[6] += t1.z; pre[7] += t1.w;
         }
+        if (REC) {
+            for (int q = w + 1; q < 8; ++q) {        // warp-uniform bound
+                const float4 t0 = *reinterpret_cast<const float4 *>(tot + q * kDK + col);
+                const float4 t1 = *reinterpret_cast<const float4 *>(tot + q * kDK + col + 4);
+                rest[0] += t0.x; rest[1] += t0.y; rest[2] += t0.z; rest[3] += t0.w;
+                rest[4] += t1.x; rest[5] += t1.y; rest[6] += t1.z; rest[7] += t1.w;
+            }
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float p2 = pre[e] * kLog2e;
+            // G_C, the chunk's total log-decay (base 2): this thread's running sum plus the rest
+            const float gc2 = fmaf(G[3][e] + rest[e], kLog2e, p2);
 #pragma unroll
             for (int i = 0; i < 4; ++i) G[i][e] = fmaf(G[i][e], kLog2e, p2);
-            gam[e] = ex2_approx(G[3][e]);            // meaningful on the thread that holds row 63
+            gam[e] = ex2_approx(REC ? gc2 : G[3][e]);    // REC: every thread; else the one holding row 63
         }
     }
     if (REC && has_gam) {
         *reinterpret_cast<float4 *>(rec + REC_GC + 4 * col) = make_float4(gam[0], gam[1], gam[2], gam[3]);
         *reinterpret_cast<float4 *>(rec + REC_GC + 4 * col + 16) = make_float4(gam[4], gam[5], gam[6], gam[7]);
     }
+    pre_qk();                                        // q and k may land later than g
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const bool live = r0 + i < live_rows;
         const uint4 uq = live ? *reinterpret_cast<const uint4 *>(base + OFF_AG + off128(i) + 8192u)
                               : make_uint4(0u, 0u, 0u, 0u);
         const uint4 uk = live ? *reinterpret_cast<const uint4 *>(base + kraw + off64(i)) : make_uint4(0u, 0u, 0u, 0u);
-        float qv[8], kv[8], kl[8], kr[8], ql[8];
+        float qv[8], kv[8], kl[8], kr[8], ql[8], kt[8];
         unpack_bf16x8(uq, qv);
         unpack_bf16x8(uk, kv);
         const float bb = (REC || !GRAM) ? 1.f : bet[r0 + i];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             if constexpr (GATE == KDA_GATE_NONE) {
-                kl[e] = kv[e]; kr[e] = kv[e]; ql[e] = qv[e];
+                kl[e] = kv[e]; kr[e] = kv[e]; ql[e] = qv[e]; kt[e] = kv[e];
             } else {
                 const float ev = ex2_approx(G[i][e]), iv = ex2_approx(-G[i][e]);
                 kl[e] = kv[e] * ev;
                 kr[e] = kv[e] * iv;
                 ql[e] = qv[e] * ev;
+                if (REC) kt[e] = kr[e] * gam[e];           // K~ = K exp(G_C - G) = K-> gamma^C
             }
         }
         const uint4 krp = pack_bf16x8(kr);
@@ -379,7 +404,7 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
         }
         if (SCAN) *reinterpret_cast<uint4 *>(base + OFF_KL + off64(i)) = pack_bf16x8(kl);
         krv[i] = krp;
-        if (REC) *reinterpret_cast<uint4 *>(rec + REC_KR + off64(i)) = krp;
+        if (REC) *reinterpret_cast<uint4 *>(rec + REC_KR + off64(i)) = pack_bf16x8(kt);
     }
 }
 // Slot image of the K-> rows a thread of rescale_tiles produced (its 4 rows x 8 columns) and,
@@ -635,24 +660,32 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     float *tot = reinterpret_cast<float *>(base + OFF_MISC + MISC_TOT);
     const __nv_bfloat16 *betag = static_cast<const __nv_bfloat16 *>(p.beta);
     const Tg *gsg = static_cast<const Tg *>(p.g);
-    const uint32_t raw_bytes = (GATE == KDA_GATE_CHANNEL ? 3u : 2u) * 16384u;
     const int step = PAIR ? 2 : 1;                       // distance between chunks this CTA builds
     const int first = PAIR ? (int)c.rank : 0;
     auto owns = [&](int n) { return !PAIR || (n & 1) == (int)c.rank; };
 
-    // raw tiles land where their rescaled versions go: g -> A_G rows 0-63,
-    // q -> A_G rows 64-127, k -> K<- tile
-    auto issue_raw = [&](int n) {
-        mbar_arrive_expect_tx(c.bars + B_RAW, raw_bytes);
-        for (int blk = 0; blk < 2; ++blk) {
-            tma_load_4d(base + OFF_AG + blk * 16384 + 8192, tm_q, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
-            tma_load_4d(base + OFF_KL + blk * 8192, tm_k, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
-            if (GATE == KDA_GATE_CHANNEL)
-                tma_load_4d(base + OFF_AG + blk * 16384, tm_g, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
-        }
+    // raw tiles land where their rescaled versions go: g -> A_G rows 0-63 (free once the Gram
+    // has read beta K<-), k -> the K<- tile (free once Z K<- has read it), q -> A_G rows 64-127
+    // (free once A_chain has read Q<-); each is fetched for the next chunk as soon as its tile frees
+    auto issue_g = [&](int n) {
+        if (GATE != KDA_GATE_CHANNEL) return;
+        mbar_arrive_expect_tx(c.bars + B_RAW, 16384u);
+        for (int blk = 0; blk < 2; ++blk)
+            tma_load_4d(base + OFF_AG + blk * 16384, tm_g, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
+    };
+    auto issue_k = [&](int n) {
+        mbar_arrive_expect_tx(c.bars + B_RAWK, 16384u);
+        for (int blk = 0; blk < 2; ++blk)
+            tma_load_4d(base + OFF_KL + blk * 8192, tm_k, c.bars + B_RAWK, blk * 64, h, sq.t0 + n * kC, sq.bt);
+    };
+    auto issue_q = [&](int n) {
+        mbar_arrive_expect_tx(c.bars + B_RAWQ, 16384u);
+        for (int blk = 0; blk < 2; ++blk)
+            tma_load_4d(base + OFF_AG + blk * 16384 + 8192, tm_q, c.bars + B_RAWQ, blk * 64, h, sq.t0 + n * kC,
+                        sq.bt);
     };
     auto issue_v = [&](int n) {
-        const int s = n & 1;
+        const int s = (n & 1) ^ (int)c.rank;
         mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
         tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, sq.t0 + n * kC, sq.bt);
     };
@@ -668,7 +701,11 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     };
 
     if (leader) {
-        if (first < nchunks) issue_raw(first);
+        if (first < nchunks) {
+            issue_g(first);
+            issue_k(first);
+            issue_q(first);
+        }
         issue_v(0);                          // nchunks >= 1: empty sequences return before the roles
         if (nchunks > 1) issue_v(1);
     }
@@ -681,7 +718,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     named_sync(2, kWyThreads);
 
     for (int n = 0; n < nchunks; ++n) {
-        const int s = n & 1;
+        // slot of chunk n: a pair keeps the chunks it builds in slot 0 and the other CTA's in slot 1
+        const int s = (n & 1) ^ (int)c.rank;
         const uint32_t ph2 = (uint32_t)((n >> 1) & 1);
 
         if (!owns(n)) continue;              // the chain warps take the other CTA's chunks
@@ -700,15 +738,20 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 
         {
             if (n + step < nchunks) load_scalars(n + step, nb, ng);   // prefetch next built chunk's scalars
-            wait_bar(c, B_RAW, phm);
+            if (GATE == KDA_GATE_CHANNEL) wait_bar(c, B_RAW, phm);
             // ---------------- prologue: Gamma and the rescaled tiles, in place.  K-> and gamma^C also
             // go to the chunk's slot, written at the end (the slot may still be in use).
             rescale_tiles<GATE, true, true>(base, OFF_KL, wt, sq.len - n * kC, bet, gss + sb * kC, tot, krv, gam,
-                                            has_gam);
+                                            has_gam, [&] {
+                                                wait_bar(c, B_RAWQ, phm);
+                                                wait_bar(c, B_RAWK, phm);
+                                            });
             fence_proxy_async_smem();
             named_sync(2, kWyThreads);
 
             r0 = build_z<GLA>(c, wt, bet, phm, tot);
+            // the Gram has read beta K<-: the next chunk's g may land in its rows
+            if (leader && n + step < nchunks) issue_g(n + step);
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(2, kWyThreads);
@@ -720,24 +763,36 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             if (n >= 2) wait_bar(c, B_E10 + s, (uint32_t)(((n - 2) >> 1) & 1));   // D1[s] drained
             tc_fence_after();
             const uint32_t a0 = smem_u32(base + OFF_KR);
-            if (!GLA) {
-                const uint32_t bk = smem_u32(base + OFF_KL);
-                const uint32_t id = idesc_bf16(128, 128, 0, 1);
+            const uint32_t bk = smem_u32(base + OFF_KL);
+            if (!GLA && s == 0) {
+                // slot 0: the v tile directly follows the two 64-column blocks of K<-, and D1[0] the
+                // [W ; P W] columns, so Z [K<- | V] = [[W ; P W] | [U ; P U]] is one N = 192 product
+                static_assert(OFF_V0 == OFF_KL + 16384 && TM_D1 == TM_WQ + 128, "merged Z [K<- | V] layout");
+                const uint32_t id = idesc_bf16(128, 192, 0, 1);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(c.tmem + TM_WQ, desc_kmajor(a0, 128, ks), desc_mnmajor(bk, 64, ks), id, ks > 0);
-            }
-            const uint32_t bv = smem_u32(base + off_v(s));
-            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+            } else {
+                if (!GLA) {
+                    const uint32_t id = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(c.tmem + TM_D1 + s * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(bv, 64, ks), id, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(c.tmem + TM_WQ, desc_kmajor(a0, 128, ks), desc_mnmajor(bk, 64, ks), id, ks > 0);
+                }
+                const uint32_t bv = smem_u32(base + off_v(s));
+                const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(c.tmem + TM_D1 + s * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(bv, 64, ks), id,
+                             ks > 0);
+            }
             mma_commit(c.bars + B_W2);
         }
         __syncwarp();                        // aligned TMEM loads and barriers below need whole warps
         wait_bar(c, B_W2, phm);
         tc_fence_after();
         if (leader && n + 2 < nchunks) issue_v(n + 2);           // v[s] consumed
+        if (leader && n + step < nchunks) issue_k(n + step);     // the K<- tile is consumed
         __syncwarp();
         if (n >= 2) wait_bar(c, B_C20 + s, (uint32_t)(((n - 2) >> 1) & 1));   // own scan done with slot s
         // the other CTA of a pair is done with chunk n - 2, whose slot tiles and Z it received from
@@ -803,16 +858,18 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         named_sync(2, kWyThreads);
         if (leader) {
             mbar_arrive(c.bars + B_WYR0 + s);
-            if (n + step < nchunks) issue_raw(n + step);   // A_G and the K<- tile are free again
+            if (n + step < nchunks) issue_q(n + step);     // A_chain has read Q<-
             if (PAIR) {
-                // the slot buffers go to the other CTA's slot s by bulk copy (it is done with
-                // chunk n - 2: checked above)
+                // the slot buffers go to slot 1 of the other CTA, which keeps the chunks built here
+                // there, by bulk copy (it is done with chunk n - 2: checked above)
+                const int ps = s ^ 1;
                 const uint32_t rbar = peer_base + OFF_MISC + MISC_BAR + 8u * B_RX;
-                const uint32_t gc_off = OFF_MISC + MISC_GC + (uint32_t)s * 512u;
+                const uint32_t gc_src = OFF_MISC + MISC_GC + (uint32_t)s * 512u;
+                const uint32_t gc_dst = OFF_MISC + MISC_GC + (uint32_t)ps * 512u;
                 mbar_arrive_expect_tx_remote(rbar, kPushBytes);
-                bulk_copy_to_peer(peer_base + off_ach(s), base + off_ach(s), 32768u, rbar);
-                bulk_copy_to_peer(peer_base + off_kt(s), base + off_kt(s), 16384u, rbar);
-                bulk_copy_to_peer(peer_base + gc_off, base + gc_off, 512u, rbar);
+                bulk_copy_to_peer(peer_base + off_ach(ps), base + off_ach(s), 32768u, rbar);
+                bulk_copy_to_peer(peer_base + off_kt(ps), base + off_kt(s), 16384u, rbar);
+                bulk_copy_to_peer(peer_base + gc_dst, base + gc_src, 512u, rbar);
             }
         }
         __syncwarp();                        // the leader's warp reaches the next barrier converged
@@ -859,7 +916,7 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
 
 
     for (int n = 0; n < nchunks; ++n) {
-        const int s = n & 1;
+        const int s = (n & 1) ^ (int)c.rank;   // a pair: own chunks in slot 0, the other CTA's in slot 1
         const uint32_t ph2 = (uint32_t)((n >> 1) & 1);
         const bool peer_chunk = PAIR && (n & 1) != (int)c.rank;
         if (peer_chunk) {
@@ -1141,7 +1198,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     float gam[8];
     bool has_gam;
     rescale_tiles<GATE, true, false, true>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gam, has_gam,
-                                           rec);
+                                           [] {}, rec);
     fence_proxy_async_smem();
     __syncthreads();
     // the cumsum partials are dead: their 4 KB hold the diagonal-block inverses
@@ -1384,7 +1441,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
             float v[W];
             tmem_ld_half<W>(c.tmem + TS_DS + col + lane_base, v);
 #pragma unroll
-            for (int e = 0; e < W; ++e) S[e] = gam * (S[e] + v[e]);
+            for (int e = 0; e < W; ++e) S[e] = fmaf(gam, S[e], v[e]);   // S Diag(gamma^C) + dS, dS^T = K~^T V_new
         }
         write_state();
     }
