@@ -13,6 +13,7 @@ KDA_ERR_UNSUPPORTED = -2
 KDA_ERR_WORKSPACE = -3
 KDA_ERR_CUDA = -4
 KDA_ERR_TIMEOUT = -5
+KDA_ERR_RANGE = -6
 
 KDA_BF16 = 0
 KDA_F32 = 1

@@ -410,11 +410,18 @@ kda_status kda_status_read(void *workspace, kda_stream_t stream) {
         return KDA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
     if (word != kda::kDevOk) {
-        // the status word and the words after it that locate the first wait that ran out
-        if (cudaMemsetAsync(workspace, 0, 8 * sizeof(int), s) != cudaSuccess) return KDA_ERR_CUDA;
+        // the status word and the words after it that locate the first wait that ran out (the
+        // wait budget in word kStatusBoundWord is the caller's and stays)
+        if (cudaMemsetAsync(workspace, 0, kda::kStatusBoundWord * sizeof(int), s) != cudaSuccess)
+            return KDA_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
     }
-    return word == kda::kDevOk ? KDA_OK : word == kda::kDevTimeout ? KDA_ERR_TIMEOUT : KDA_ERR_CUDA;
+    switch (word) {
+    case kda::kDevOk: return KDA_OK;
+    case kda::kDevTimeout: return KDA_ERR_TIMEOUT;
+    case kda::kDevDecayRange: return KDA_ERR_RANGE;
+    default: return KDA_ERR_CUDA;
+    }
 }
 
 const char *kda_status_string(kda_status status) {
@@ -425,6 +432,7 @@ const char *kda_status_string(kda_status status) {
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "device-side wait timed out";
+    case KDA_ERR_RANGE: return "in-chunk log-decay outside the range of the bf16 path";
     }
     return "unknown status";
 }

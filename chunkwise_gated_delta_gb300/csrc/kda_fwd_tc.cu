@@ -136,6 +136,8 @@ struct Ctx {
     volatile int *abort;
     int *status;
     uint32_t tmem;
+    uint32_t bound;    // polling iterations a bounded wait takes before it gives up
+    bool short_polls;  // a caller's budget: each poll suspends for at most kShortPollNs
     uint32_t rank;     // rank in the pair (0 without a pair)
     const uint8_t *zrec;   // record of chunk 0 of this (sequence, head); chunk n at zrec + n * zstride
     size_t zstride;
@@ -145,53 +147,79 @@ struct Ctx {
 // first wait to run out in the launch also leaves where it was in the next
 // words of the status block: barrier index + 1, parity, thread, block (x, y, z
 // in bytes 0-2).
-__device__ __forceinline__ void record_timeout(const Ctx &c, int idx, uint32_t parity) {
-    *c.abort = 1;
-    atomicCAS(c.status, kDevOk, kDevTimeout);
-    if (atomicCAS(c.status + 1, 0, idx + 1) == 0) {
-        c.status[2] = (int)parity;
-        c.status[3] = (int)threadIdx.x;
-        c.status[4] = (int)(blockIdx.x | (blockIdx.y << 8) | (blockIdx.z << 16));
+__device__ __forceinline__ void record_timeout(volatile int *abort, int *status, int idx, uint32_t parity) {
+    *abort = 1;
+    atomicCAS(status, kDevOk, kDevTimeout);
+    if (atomicCAS(status + 1, 0, idx + 1) == 0) {
+        status[2] = (int)parity;
+        status[3] = (int)threadIdx.x;
+        status[4] = (int)(blockIdx.x | (blockIdx.y << 8) | (blockIdx.z << 16));
     }
 }
 // A wait given up because another thread of the CTA gave up: the two issuing threads (chain
 // leader 0, WY leader 128) leave the barrier they were on in words 5 and 6.
-__device__ __forceinline__ void note_abort(const Ctx &c, int idx, uint32_t parity) {
-    if (threadIdx.x == 0) atomicCAS(c.status + 5, 0, idx + 1 + 256 * (int)parity);
-    if (threadIdx.x == kChainThreads) atomicCAS(c.status + 6, 0, idx + 1 + 256 * (int)parity);
+__device__ __forceinline__ void note_abort(int *status, int idx, uint32_t parity) {
+    if (threadIdx.x == 0) atomicCAS(status + 5, 0, idx + 1 + 256 * (int)parity);
+    if (threadIdx.x == kChainThreads) atomicCAS(status + 6, 0, idx + 1 + 256 * (int)parity);
 }
 
 // Bounded wait that becomes a no-op once any thread of the CTA has given up.  The
-// first probe is inline: most waits find their phase already complete, and a call
-// to the out-of-line loop would move the caller's live registers through local memory.
-__device__ __noinline__ void wait_bar_slow(const Ctx &c, int idx, uint32_t parity) {
+// first probe is inline: most waits end within it, and a call to the out-of-line
+// loop would move the caller's live registers through local memory.  Probes use
+// try_wait, which suspends the thread until the phase completes or a hardware time
+// limit passes; under a caller's budget the first probe does not block and each
+// later poll suspends for at most kShortPollNs, so the budget counts short polls.
+// The out-of-line loops take plain values, not the context: a reference to it would
+// keep the context in local memory for every inline use.
+constexpr uint32_t kShortPollNs = 32;
+// Returns whether the phase completed (false: the wait gave up, or another thread had).
+__device__ __noinline__ bool wait_bar_slow(uint64_t *bars, volatile int *abort, int *status, uint32_t bound,
+                                           bool short_polls, int idx, uint32_t parity) {
+    uint64_t *bar = bars + idx;
+    for (uint32_t i = 0; i < bound; ++i) {
+        if (short_polls ? mbar_try_wait_for(bar, parity, kShortPollNs) : mbar_try_wait(bar, parity)) return true;
+        if (*abort) {
+            note_abort(status, idx, parity);
+            return false;
+        }
+    }
+    record_timeout(abort, status, idx, parity);
+    return false;
+}
+__device__ __forceinline__ bool wait_bar(const Ctx &c, int idx, uint32_t parity) {
     uint64_t *bar = c.bars + idx;
-    for (uint32_t i = 0; i < kWaitBound; ++i) {
+    if (c.short_polls ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(c.bars, c.abort, c.status, c.bound, c.short_polls, idx, parity);
+}
+
+// Wait for a phase that an asynchronous operation this thread started completes -- a copy into
+// shared memory, a commit of tensor-core products -- whatever the abort flag says: nothing may
+// still write this CTA's shared memory or TMEM when it frees TMEM or exits.  These operations
+// complete by themselves, so the library's default bound applies (never the caller's budget);
+// running out is recorded like any other timeout.
+__device__ __noinline__ void drain_bar_slow(uint64_t *bar, volatile int *abort, int *status, int idx,
+                                            uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitBound; ++i)
         if (mbar_try_wait(bar, parity)) return;
-        if (*c.abort) {
-            note_abort(c, idx, parity);
-            return;
-        }
-    }
-    record_timeout(c, idx, parity);
+    record_timeout(abort, status, idx, parity);
 }
-__device__ __forceinline__ void wait_bar(const Ctx &c, int idx, uint32_t parity) {
-    if (!mbar_try_wait(c.bars + idx, parity)) wait_bar_slow(c, idx, parity);
+__device__ __forceinline__ void drain_bar(const Ctx &c, int idx, uint32_t parity) {
+    if (!mbar_try_wait(c.bars + idx, parity)) drain_bar_slow(c.bars + idx, c.abort, c.status, idx, parity);
 }
-// The same for barriers completed from the other CTA of the pair.
-__device__ __noinline__ void wait_bar_cluster_slow(const Ctx &c, int idx, uint32_t parity) {
-    uint64_t *bar = c.bars + idx;
-    for (uint32_t i = 0; i < kWaitBound; ++i) {
+__device__ __noinline__ void drain_bar_cluster_slow(uint64_t *bar, volatile int *abort, int *status, int idx,
+                                                    uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitBound; ++i)
         if (mbar_try_wait_cluster(bar, parity)) return;
-        if (*c.abort) {
-            note_abort(c, idx, parity);
-            return;
-        }
-    }
-    record_timeout(c, idx, parity);
+    record_timeout(abort, status, idx, parity);
 }
-__device__ __forceinline__ void wait_bar_cluster(const Ctx &c, int idx, uint32_t parity) {
-    if (!mbar_try_wait_cluster(c.bars + idx, parity)) wait_bar_cluster_slow(c, idx, parity);
+__device__ __forceinline__ void drain_bar_cluster(const Ctx &c, int idx, uint32_t parity) {
+    if (!mbar_try_wait_cluster(c.bars + idx, parity))
+        drain_bar_cluster_slow(c.bars + idx, c.abort, c.status, idx, parity);
+}
+// The budget of the bounded waits: word kStatusBoundWord of the status block, or the default.
+__device__ __forceinline__ uint32_t wait_bound_of(const int *status) {
+    const int b = status[kStatusBoundWord];
+    return b > 0 ? (uint32_t)b : kWaitBound;
 }
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -279,10 +307,14 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8]) {
     return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
 }
 
+// Largest in-chunk log-decay magnitude (base 2) the rescaled tiles represent: K-> = K 2^{-G}
+// and the products of K-> stay finite in fp32 with a margin of 2^28 for the sums.
+constexpr float kDecayLimit2 = 100.f;
+
 template <int GATE, bool GRAM, bool SCAN, bool REC = false, typename PreQK>
 __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int wt, int live_rows, const float *bet,
                                               const float *gs, float *tot, uint4 (&krv)[4], float (&gam)[8],
-                                              bool &has_gam, PreQK &&pre_qk, uint8_t *rec = nullptr) {
+                                              bool &has_gam, int *status, PreQK &&pre_qk, uint8_t *rec = nullptr) {
     const int w = wt >> 5, lane = wt & 31;
     const int cq = lane & 15, rsub = lane >> 4;
     const int r0 = 8 * w + 4 * rsub;                 // first of the thread's 4 rows
@@ -364,6 +396,14 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
 #pragma unroll
             for (int i = 0; i < 4; ++i) G[i][e] = fmaf(G[i][e], kLog2e, p2);
             gam[e] = ex2_approx(REC ? gc2 : G[3][e]);    // REC: every thread; else the one holding row 63
+        }
+        if (has_gam) {
+            // the chunk's total log-decay (the extreme of G for g <= 0) past the limit: the tiles
+            // would overflow; the status word says so instead of the outputs turning to inf / NaN
+            bool bad = false;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bad |= !(fabsf(G[3][e]) < kDecayLimit2);
+            if (bad) atomicCAS(status, kDevOk, kDevDecayRange);
         }
     }
     if (REC && has_gam) {
@@ -667,18 +707,30 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     // raw tiles land where their rescaled versions go: g -> A_G rows 0-63 (free once the Gram
     // has read beta K<-), k -> the K<- tile (free once Z K<- has read it), q -> A_G rows 64-127
     // (free once A_chain has read Q<-); each is fetched for the next chunk as soon as its tile frees
-    auto issue_g = [&](int n) {
-        if (GATE != KDA_GATE_CHANNEL) return;
+    // A barrier is re-armed only after the issuing thread's own wait on its previous phase has
+    // ended with the phase complete: while `clean` (every wait of this thread so far did, kept in
+    // a register), it issues; after a wait gave up it issues no more copies.  So each barrier has
+    // at most one copy in flight, and the last phase it issued on each is drained at the end.
+    // `mi` is the index, among the chunks this CTA builds, of the chunk fetched.
+    bool clean = true;
+    int last_g = -1, last_k = -1, last_q = -1, last_v[2] = {-1, -1};
+    auto issue_g = [&](int n, int mi) {
+        if (GATE != KDA_GATE_CHANNEL || !clean) return;
+        last_g = mi;
         mbar_arrive_expect_tx(c.bars + B_RAW, 16384u);
         for (int blk = 0; blk < 2; ++blk)
             tma_load_4d(base + OFF_AG + blk * 16384, tm_g, c.bars + B_RAW, blk * 64, h, sq.t0 + n * kC, sq.bt);
     };
-    auto issue_k = [&](int n) {
+    auto issue_k = [&](int n, int mi) {
+        if (!clean) return;
+        last_k = mi;
         mbar_arrive_expect_tx(c.bars + B_RAWK, 16384u);
         for (int blk = 0; blk < 2; ++blk)
             tma_load_4d(base + OFF_KL + blk * 8192, tm_k, c.bars + B_RAWK, blk * 64, h, sq.t0 + n * kC, sq.bt);
     };
-    auto issue_q = [&](int n) {
+    auto issue_q = [&](int n, int mi) {
+        if (!clean) return;
+        last_q = mi;
         mbar_arrive_expect_tx(c.bars + B_RAWQ, 16384u);
         for (int blk = 0; blk < 2; ++blk)
             tma_load_4d(base + OFF_AG + blk * 16384 + 8192, tm_q, c.bars + B_RAWQ, blk * 64, h, sq.t0 + n * kC,
@@ -686,6 +738,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     };
     auto issue_v = [&](int n) {
         const int s = (n & 1) ^ (int)c.rank;
+        if (!clean) return;
+        last_v[s] = n;
         mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
         tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, sq.t0 + n * kC, sq.bt);
     };
@@ -702,9 +756,9 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 
     if (leader) {
         if (first < nchunks) {
-            issue_g(first);
-            issue_k(first);
-            issue_q(first);
+            issue_g(first, 0);
+            issue_k(first, 0);
+            issue_q(first, 0);
         }
         issue_v(0);                          // nchunks >= 1: empty sequences return before the roles
         if (nchunks > 1) issue_v(1);
@@ -738,20 +792,20 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 
         {
             if (n + step < nchunks) load_scalars(n + step, nb, ng);   // prefetch next built chunk's scalars
-            if (GATE == KDA_GATE_CHANNEL) wait_bar(c, B_RAW, phm);
+            if (GATE == KDA_GATE_CHANNEL) clean &= wait_bar(c, B_RAW, phm);
             // ---------------- prologue: Gamma and the rescaled tiles, in place.  K-> and gamma^C also
             // go to the chunk's slot, written at the end (the slot may still be in use).
             rescale_tiles<GATE, true, true>(base, OFF_KL, wt, sq.len - n * kC, bet, gss + sb * kC, tot, krv, gam,
-                                            has_gam, [&] {
-                                                wait_bar(c, B_RAWQ, phm);
-                                                wait_bar(c, B_RAWK, phm);
+                                            has_gam, c.status, [&] {
+                                                clean &= wait_bar(c, B_RAWQ, phm);
+                                                clean &= wait_bar(c, B_RAWK, phm);
                                             });
             fence_proxy_async_smem();
             named_sync(2, kWyThreads);
 
             r0 = build_z<GLA>(c, wt, bet, phm, tot);
             // the Gram has read beta K<-: the next chunk's g may land in its rows
-            if (leader && n + step < nchunks) issue_g(n + step);
+            if (leader && n + step < nchunks) issue_g(n + step, m + 1);
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(2, kWyThreads);
@@ -759,7 +813,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 
         // ---------------- Z K<- -> [W ; P W],  Z V -> D1[s] = [U ; P U]
         if (leader) {
-            wait_bar(c, B_V0 + s, ph2);
+            clean &= wait_bar(c, B_V0 + s, ph2);
             if (n >= 2) wait_bar(c, B_E10 + s, (uint32_t)(((n - 2) >> 1) & 1));   // D1[s] drained
             tc_fence_after();
             const uint32_t a0 = smem_u32(base + OFF_KR);
@@ -792,12 +846,15 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         wait_bar(c, B_W2, phm);
         tc_fence_after();
         if (leader && n + 2 < nchunks) issue_v(n + 2);           // v[s] consumed
-        if (leader && n + step < nchunks) issue_k(n + step);     // the K<- tile is consumed
+        if (leader && n + step < nchunks) issue_k(n + step, m + 1);    // the K<- tile is consumed
         __syncwarp();
         if (n >= 2) wait_bar(c, B_C20 + s, (uint32_t)(((n - 2) >> 1) & 1));   // own scan done with slot s
-        // the other CTA of a pair is done with chunk n - 2, whose slot tiles and Z it received from
-        // here: the slot and its Z-in tile may be rewritten
-        if (PAIR && m >= 1) wait_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));
+        // the other CTA of a pair is done with the chunk sent before, whose slot tiles and Z it
+        // received here: its slot 1 and Z-in tile may be rewritten.  The two waits of the exchange
+        // between the CTAs of a pair (this one, and the receiver's for the chunk) are drain waits:
+        // both CTAs run every chunk whatever their other waits did, so every chunk is sent and
+        // received, at most one is in flight towards a CTA, and none is when it exits.
+        if (PAIR && m >= 1) drain_bar_cluster(c, B_PFREE, (uint32_t)((m - 1) & 1));
         __syncwarp();
         if (PAIR) {
             // the other CTA forms its own [U ; P U] = Z V: send this warp's 16 rows of Z (the
@@ -858,7 +915,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         named_sync(2, kWyThreads);
         if (leader) {
             mbar_arrive(c.bars + B_WYR0 + s);
-            if (n + step < nchunks) issue_q(n + step);     // A_chain has read Q<-
+            if (n + step < nchunks) issue_q(n + step, m + 1);      // A_chain has read Q<-
             if (PAIR) {
                 // the slot buffers go to slot 1 of the other CTA, which keeps the chunks built here
                 // there, by bulk copy (it is done with chunk n - 2: checked above)
@@ -874,10 +931,19 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         }
         __syncwarp();                        // the leader's warp reaches the next barrier converged
     }
-    // drain: every MMA this thread issued has completed before TMEM is freed
+    // drain, also after a wait gave up: every product issued here is done and the newest copy
+    // into each raw tile has landed before TMEM is freed and the CTA exits
     if (leader) {
         mma_commit(c.bars + B_FIN1);
-        wait_bar(c, B_FIN1, 0);
+        drain_bar(c, B_FIN1, 0);
+        if (last_g >= 0) drain_bar(c, B_RAW, (uint32_t)(last_g & 1));
+        if (last_k >= 0) drain_bar(c, B_RAWK, (uint32_t)(last_k & 1));
+        if (last_q >= 0) drain_bar(c, B_RAWQ, (uint32_t)(last_q & 1));
+        // v slots: a pair's slot 1 (the other CTA's chunks) is drained by the chain leader, which
+        // arms its later phases (an earlier phase than the last one would alias by parity with
+        // a phase that is still open)
+        for (int sl = 0; sl < (PAIR ? 1 : 2); ++sl)
+            if (last_v[sl] >= 0) drain_bar(c, B_V0 + sl, (uint32_t)((last_v[sl] >> 1) & 1));
     }
     __syncwarp();
 }
@@ -895,6 +961,8 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float *gC = reinterpret_cast<const float *>(base + OFF_MISC + MISC_GC);
     const int H = p.H, dv = p.dv;
+    bool clean = true;                          // every wait of this thread has ended complete
+    int last_v = -1;                            // newest v copy this thread issued (chunk index)
 
     float S[kDVS];
 #pragma unroll
@@ -922,9 +990,9 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
         if (peer_chunk) {
             // built by the other CTA: wait until its WY warps have written A_chain, K->, gamma^C
             // and Z here, and for this slice's v; [U ; P U] = Z V goes right before the state product
-            if (leader) wait_bar(c, B_V0 + s, ph2);
+            if (leader) clean &= wait_bar(c, B_V0 + s, ph2);
             __syncwarp();
-            wait_bar_cluster(c, B_RX, (uint32_t)((n >> 1) & 1));
+            drain_bar_cluster(c, B_RX, (uint32_t)((n >> 1) & 1));   // an exchange wait (see the WY warps)
             fence_proxy_async_smem();    // the received tiles are read by the tensor core next
         } else {
             wait_bar(c, B_WYR0 + s, ph2);
@@ -951,8 +1019,10 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
         __syncwarp();
         wait_bar(c, B_C10 + s, ph2);
         tc_fence_after();
-        if (peer_chunk && leader && n + 2 < nchunks) {
-            // v[s] has been read: fetch the slice of chunk n + 2
+        if (peer_chunk && leader && n + 2 < nchunks && clean) {
+            // v[s] has been read: fetch the slice of chunk n + 2 (its wait on chunk n's copy above
+            // ended complete; after a wait gave up no more copies are issued)
+            last_v = n + 2;
             mbar_arrive_expect_tx(c.bars + B_V0 + s, 8192u);
             tma_load_4d(base + off_v(s), tm_v, c.bars + B_V0 + s, e0, h, sq.t0 + (n + 2) * kC, sq.bt);
         }
@@ -1035,7 +1105,14 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     if (leader) {
         tma_store_wait_all0();
         mma_commit(c.bars + B_FIN0);
-        wait_bar(c, B_FIN0, 0);
+        drain_bar(c, B_FIN0, 0);
+        if (PAIR) {
+            // slot 1 of a pair: the newest v copy into it, issued here or, when the chain issued
+            // none, by the WY leader at the start (the first of the other CTA's chunks)
+            const int first_peer = c.rank ? 0 : 1;
+            const int lv = last_v >= 0 ? last_v : (first_peer < nchunks ? first_peer : -1);
+            if (lv >= 0) drain_bar(c, B_V1, (uint32_t)((lv >> 1) & 1));
+        }
     }
     __syncwarp();
 }
@@ -1052,6 +1129,8 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     c.bars = reinterpret_cast<uint64_t *>(base + OFF_MISC + MISC_BAR);
     c.abort = reinterpret_cast<volatile int *>(base + OFF_MISC + MISC_ABORT);
     c.status = p.status;
+    c.bound = wait_bound_of(p.status);
+    c.short_polls = c.bound != kWaitBound;
     c.rank = PAIR ? cluster_ctarank() : 0u;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + OFF_MISC + MISC_TSLOT);
 
@@ -1143,6 +1222,8 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     c.bars = reinterpret_cast<uint64_t *>(base + OFF_WMISC + WM_BAR);
     c.abort = reinterpret_cast<volatile int *>(base + OFF_WMISC + WM_ABORT);
     c.status = p.status;
+    c.bound = wait_bound_of(p.status);
+    c.short_polls = c.bound != kWaitBound;
     c.rank = 0;
     c.zrec = nullptr;
     c.zstride = 0;
@@ -1155,6 +1236,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     if (wt == 0) {
         mbar_init(c.bars + B_RAW, 1);
         mbar_init(c.bars + B_GRAM, 1);
+        mbar_init(c.bars + B_FIN0, 1);
         *c.abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -1198,7 +1280,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     float gam[8];
     bool has_gam;
     rescale_tiles<GATE, true, false, true>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gam, has_gam,
-                                           [] {}, rec);
+                                           c.status, [] {}, rec);
     fence_proxy_async_smem();
     __syncthreads();
     // the cumsum partials are dead: their 4 KB hold the diagonal-block inverses
@@ -1259,6 +1341,10 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
         bulk_store(rec + REC_A, base + OFF_AG, 32768u);
         tma_store_commit();
         tma_store_wait_read0();             // shared memory may go once the copies have read it
+        // drain, also after a wait gave up: the products are done and the tiles have landed
+        mma_commit(c.bars + B_FIN0);
+        drain_bar(c, B_FIN0, 0);
+        drain_bar(c, B_RAW, 0);
     }
     __syncwarp();
     tc_fence_before();
@@ -1309,7 +1395,8 @@ constexpr uint32_t TS_DS = 192;    // dS^T, half h at + h W
 
 // Ring entry / accumulator slot n % 3: FULLR, RFREE (one arrival per half), ZV, D1FREE (one
 // arrival per half); Z entry n % 2: FULLZ; C1 / C2: [half][chunk parity].
-enum { SB_FULLR = 0, SB_RFREE = 3, SB_ZV = 6, SB_D1FREE = 9, SB_FULLZ = 12, SB_C1 = 14, SB_C2 = 18, kScanBars = 22 };
+enum { SB_FULLR = 0, SB_RFREE = 3, SB_ZV = 6, SB_D1FREE = 9, SB_FULLZ = 12, SB_C1 = 14, SB_C2 = 18, SB_FINL = 22,
+       SB_FINC = 23, kScanBars = 25 };
 static_assert(kScanBars * 8 <= 256, "scan barriers");
 
 // 64-byte swizzle (MN-major operand tiles of 32 bf16 columns, one 64-byte row
@@ -1449,6 +1536,11 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
 #pragma unroll
         for (int e = 0; e < W; ++e) p.ht[(((size_t)b * H + h) * dv + ev0 + e) * kDK + t] = S[e];
     }
+    if (leader) {                                       // every product issued here is done
+        mma_commit(c.bars + SB_FINC + half);
+        drain_bar(c, SB_FINC + half, 0);
+    }
+    __syncwarp();
 }
 
 // The loader (one thread): chunk n's A_chain, K->, gamma^C and v tile into ring
@@ -1459,11 +1551,19 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
                             int nchunks) {
     using G = ScanCfg<NH>;
     uint8_t *base = c.base;
+    // A ring entry is re-armed only after this thread's own wait on its previous copy (in zv)
+    // ended with it landed: while `clean` (every wait of this thread so far did) it issues, after
+    // a wait gave up it issues no more copies.  One copy in flight per barrier, the newest drained
+    // at the end.
+    int last_r = -1, last_z = -1;                        // newest record / Z copy issued
+    bool clean = true;
     auto issue_r = [&](int n) {
         const uint8_t *r = c.zrec + (size_t)n * c.zstride;
         const int ri = n % 3;
         uint8_t *slot = base + ri * G::R_SLOT;
         uint64_t *bar = c.bars + SB_FULLR + ri;
+        if (!clean) return;
+        last_r = n;
         mbar_arrive_expect_tx(bar, G::kRTx);
         bulk_load(slot + G::R_ACH, r + REC_A, 32768u, bar);
         bulk_load(slot + G::R_KT, r + REC_KR, 16384u, bar);
@@ -1473,13 +1573,15 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
     auto issue_z = [&](int n) {
         const uint8_t *r = c.zrec + (size_t)n * c.zstride;
         uint64_t *bar = c.bars + SB_FULLZ + (n & 1);
+        if (!clean) return;
+        last_z = n;
         mbar_arrive_expect_tx(bar, G::kZTx);
         bulk_load(base + G::OFF_Z + (n & 1) * 16384, r + REC_Z, 16384u, bar);
     };
     auto zv = [&](int n) {
         const int ri = n % 3;
-        wait_bar(c, SB_FULLR + ri, (uint32_t)((n / 3) & 1));                 // v
-        wait_bar(c, SB_FULLZ + (n & 1), (uint32_t)((n >> 1) & 1));           // Z
+        clean &= wait_bar(c, SB_FULLR + ri, (uint32_t)((n / 3) & 1));        // v
+        clean &= wait_bar(c, SB_FULLZ + (n & 1), (uint32_t)((n >> 1) & 1));  // Z
         if (n >= 3) wait_bar(c, SB_D1FREE + ri, (uint32_t)(((n - 3) / 3) & 1));   // chunk n - 3 drained D1[ri]
         tc_fence_after();
         const uint32_t a0 = smem_u32(base + G::OFF_Z + (n & 1) * 16384), b0 = smem_u32(base + ri * G::R_SLOT + G::R_V);
@@ -1507,6 +1609,12 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
             }
             if (n + 2 < nchunks) zv(n + 2);
         }
+        // drain, also after a wait gave up: the newest copy into every entry has landed and every
+        // product issued here is done before the CTA frees TMEM and exits
+        for (int m = last_r; m >= 0 && m > last_r - 3; --m) drain_bar(c, SB_FULLR + m % 3, (uint32_t)((m / 3) & 1));
+        for (int m = last_z; m >= 0 && m > last_z - 2; --m) drain_bar(c, SB_FULLZ + (m & 1), (uint32_t)((m >> 1) & 1));
+        mma_commit(c.bars + SB_FINL);
+        drain_bar(c, SB_FINL, 0);
     }
     __syncwarp();
 }
@@ -1522,6 +1630,8 @@ kda_fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_v)
     c.bars = reinterpret_cast<uint64_t *>(base + G::OFF_BAR);
     c.abort = reinterpret_cast<volatile int *>(base + G::OFF_ABORT);
     c.status = p.status;
+    c.bound = wait_bound_of(p.status);
+    c.short_polls = c.bound != kWaitBound;
     c.rank = 0;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + G::OFF_TSLOT);
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;

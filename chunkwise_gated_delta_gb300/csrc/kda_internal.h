@@ -66,7 +66,10 @@ struct BwdParams {
 };
 
 // Device status codes written into the workspace word (first error wins).
-enum : int { kDevOk = 0, kDevTimeout = 1 };
+enum : int { kDevOk = 0, kDevTimeout = 1, kDevDecayRange = 2 };
+// Word of the 256-byte status block that holds the polling budget of the bounded waits
+// (iterations before a wait gives up; 0 = the library default).
+constexpr int kStatusBoundWord = 7;
 
 // float32 CUDA-core path (any gate kind; inputs float32).
 cudaError_t launch_fwd_simt_f32(const FwdParams &p, int g_is_bf16, cudaStream_t s);

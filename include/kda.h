@@ -38,6 +38,15 @@
  *     in words 1-6 of the workspace, where the first wait ran out (barrier,
  *     phase, thread, block, and the barriers its two issuing threads were on)
  *     for diagnosis; kda_status_read clears them with the status word.
+ *   - Word 7 of the workspace (bytes 28-31, int32) is read by the bf16
+ *     forward's kernels: when positive, the number of short polls (each
+ *     suspends the waiting thread for at most about 32 ns) a bounded wait
+ *     makes before it gives up (0: the library's default, far above any wait
+ *     that ends).  It exists to exercise the failure path: a
+ *     budget too small for the waits makes the launch end early with
+ *     KDA_ERR_TIMEOUT recorded and its outputs undefined, after every copy
+ *     and tensor-core product the kernels started has completed, so the next
+ *     call runs normally.  kda_status_read leaves it as it is.
  *   - Outputs must not alias inputs.
  */
 #ifndef KDA_H_
@@ -58,7 +67,9 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. dk = 96) */
     KDA_ERR_WORKSPACE = -3,    /* workspace missing or smaller than the query */
     KDA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
-    KDA_ERR_TIMEOUT = -5       /* a device-side bounded wait gave up */
+    KDA_ERR_TIMEOUT = -5,      /* a device-side bounded wait gave up */
+    KDA_ERR_RANGE = -6         /* bf16 forward: a chunk's total log-decay beyond the range its
+                                  rescaled tiles represent (see kda_chunk_fwd) */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -130,10 +141,19 @@ size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
  * Delta Attention backward"), A_chain = [-W ; Q<- - P W] with W = T K<-,
  * the rescaled K-> and gamma^C -- then the scan kernel reads them; the
  * workspace must then be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
- * With a smaller workspace the scan kernel builds Z itself (one kernel,
- * slower); both forms compute the same values up to bf16 rounding (the
- * record form applies beta to the rows of L after the Gram product, the
- * single kernel to the bf16 K<- operand before it).
+ * With a smaller workspace, or where the query returns 256 (a batch whose
+ * single-kernel CTAs, one per 64 values of each sequence and head, fill
+ * between half of the GPU's SMs and all of them: there that form is faster),
+ * the scan kernel builds Z itself in one kernel; both forms compute the same
+ * values up to bf16 rounding (the record form applies beta to the rows of L
+ * after the Gram product, the single kernel to the bf16 K<- operand before it).
+ *
+ * The bf16 path rescales each chunk's tiles by Gamma and 1/Gamma in float32
+ * (page "Gated Linear Attention", section 5.2), so a chunk's total log-decay,
+ * sum of g over its 64 tokens, must stay above -100 ln 2 (about -69); a chunk
+ * past that is detected on the device and recorded as KDA_ERR_RANGE for
+ * kda_status_read (its outputs are then undefined).  float32 inputs have no
+ * such limit (their Gram is formed in the log domain, section 5.3).
  */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 

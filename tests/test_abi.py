@@ -33,9 +33,11 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.kda_status_string(code)
     assert _lib.status_string(_lib.KDA_ERR_TIMEOUT) == "device-side wait timed out"
+    assert "decay" in _lib.status_string(_lib.KDA_ERR_RANGE)
+    assert _lib.status_string(-99) == "unknown status"
 
 
 def _args(**over):
