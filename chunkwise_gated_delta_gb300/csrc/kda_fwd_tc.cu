@@ -308,13 +308,18 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8]) {
 }
 
 // Largest in-chunk log-decay magnitude (base 2) the rescaled tiles represent: K-> = K 2^{-G}
-// and the products of K-> stay finite in fp32 with a margin of 2^28 for the sums.
-constexpr float kDecayLimit2 = 100.f;
+// and the products of K-> stay finite in fp32 with a margin of 2^28 for the sums.  The chain
+// checks it on gamma^C = 2^{G_C} (G_C, the chunk's total, is the extreme of G for g <= 0): a
+// chunk past it is recorded in the status word instead of inf / NaN reaching the outputs
+// unreported.
+constexpr float kGammaMin = 7.8886091e-31f;   // 2^-100
+constexpr float kGammaMax = 1.2676506e+30f;   // 2^100
+__device__ __forceinline__ bool gamma_in_range(float gam) { return gam > kGammaMin && gam < kGammaMax; }
 
 template <int GATE, bool GRAM, bool SCAN, bool REC = false, typename PreQK>
 __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int wt, int live_rows, const float *bet,
                                               const float *gs, float *tot, uint4 (&krv)[4], float (&gam)[8],
-                                              bool &has_gam, int *status, PreQK &&pre_qk, uint8_t *rec = nullptr) {
+                                              bool &has_gam, PreQK &&pre_qk, uint8_t *rec = nullptr) {
     const int w = wt >> 5, lane = wt & 31;
     const int cq = lane & 15, rsub = lane >> 4;
     const int r0 = 8 * w + 4 * rsub;                 // first of the thread's 4 rows
@@ -396,14 +401,6 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
 #pragma unroll
             for (int i = 0; i < 4; ++i) G[i][e] = fmaf(G[i][e], kLog2e, p2);
             gam[e] = ex2_approx(REC ? gc2 : G[3][e]);    // REC: every thread; else the one holding row 63
-        }
-        if (has_gam) {
-            // the chunk's total log-decay (the extreme of G for g <= 0) past the limit: the tiles
-            // would overflow; the status word says so instead of the outputs turning to inf / NaN
-            bool bad = false;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) bad |= !(fabsf(G[3][e]) < kDecayLimit2);
-            if (bad) atomicCAS(status, kDevOk, kDevDecayRange);
         }
     }
     if (REC && has_gam) {
@@ -796,7 +793,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             // ---------------- prologue: Gamma and the rescaled tiles, in place.  K-> and gamma^C also
             // go to the chunk's slot, written at the end (the slot may still be in use).
             rescale_tiles<GATE, true, true>(base, OFF_KL, wt, sq.len - n * kC, bet, gss + sb * kC, tot, krv, gam,
-                                            has_gam, c.status, [&] {
+                                            has_gam, [&] {
                                                 clean &= wait_bar(c, B_RAWQ, phm);
                                                 clean &= wait_bar(c, B_RAWK, phm);
                                             });
@@ -963,6 +960,7 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     const int H = p.H, dv = p.dv;
     bool clean = true;                          // every wait of this thread has ended complete
     int last_v = -1;                            // newest v copy this thread issued (chunk index)
+    bool in_range = true;                       // every chunk's gamma^C within the decay limit
 
     float S[kDVS];
 #pragma unroll
@@ -999,6 +997,7 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
         }
         tc_fence_after();
         const float gam = gC[s * kDK + j];
+        in_range &= gamma_in_range(gam);
 
         // ---- D1[s] (+)= [-W ; Q'] S^T   (M128 N64 K128)
         if (leader) {
@@ -1102,6 +1101,7 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
 #pragma unroll
         for (int e = 0; e < kDVS; ++e) p.ht[(((size_t)b * H + h) * dv + e0 + e) * kDK + j] = S[e];
     }
+    if (!in_range) atomicCAS(c.status, kDevOk, kDevDecayRange);
     if (leader) {
         tma_store_wait_all0();
         mma_commit(c.bars + B_FIN0);
@@ -1280,7 +1280,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     float gam[8];
     bool has_gam;
     rescale_tiles<GATE, true, false, true>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gam, has_gam,
-                                           c.status, [] {}, rec);
+                                           [] {}, rec);
     fence_proxy_async_smem();
     __syncthreads();
     // the cumsum partials are dead: their 4 KB hold the diagonal-block inverses
@@ -1453,6 +1453,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
     uint8_t *st = base + G::OFF_ST + half * 8192;
     uint8_t *vn = st;                                    // V_new: 64 rows at the front of the S^T tile
     const float *gc = reinterpret_cast<const float *>(base + G::OFF_GC);
+    bool in_range = true;                                // every chunk's gamma^C within the decay limit
     const uint32_t col = (uint32_t)(half * W);
 
     float S[W];
@@ -1476,6 +1477,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
         wait_bar(c, SB_ZV + ri, phr);                    // D1[ri] = [U ; P U]
         tc_fence_after();
         const float gam = gc[ri * kDK + t];
+        in_range &= gamma_in_range(gam);
 
         // ---- D1[s] += A_chain S^T   (M128 N=W K128)
         if (leader) {
@@ -1536,6 +1538,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
 #pragma unroll
         for (int e = 0; e < W; ++e) p.ht[(((size_t)b * H + h) * dv + ev0 + e) * kDK + t] = S[e];
     }
+    if (!in_range) atomicCAS(c.status, kDevOk, kDevDecayRange);
     if (leader) {                                       // every product issued here is done
         mma_commit(c.bars + SB_FINC + half);
         drain_bar(c, SB_FINC + half, 0);
