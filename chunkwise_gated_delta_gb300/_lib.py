@@ -58,6 +58,7 @@ class KdaBwdArgs(ctypes.Structure):
         ("grad_q", ctypes.c_void_p), ("grad_k", ctypes.c_void_p), ("grad_v", ctypes.c_void_p),
         ("grad_g", ctypes.c_void_p), ("grad_beta", ctypes.c_void_p), ("grad_h0", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("cu_seqlens", ctypes.c_void_p),
     ]
 
 
@@ -71,6 +72,7 @@ class DplrFwdArgs(ctypes.Structure):
         ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("g", ctypes.c_void_p),
         ("h0", ctypes.c_void_p), ("o", ctypes.c_void_p), ("ht", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("cu_seqlens", ctypes.c_void_p),
     ]
 
 
@@ -87,6 +89,7 @@ class DplrBwdArgs(ctypes.Structure):
         ("grad_a", ctypes.c_void_p), ("grad_b", ctypes.c_void_p), ("grad_g", ctypes.c_void_p),
         ("grad_h0", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("cu_seqlens", ctypes.c_void_p),
     ]
 
 

@@ -155,10 +155,16 @@ def kda_chunk_fwd_noalloc(q, k, v, g=None, beta=None, h0=None, *, gate=None, sca
 
 
 def make_bwd_args(q, k, v, g, beta, h0, do, dht, grads: dict, *, gate=None, scale_v=True,
-                  workspace=None) -> _lib.KdaBwdArgs:
-    """Fill the C backward argument struct (grads: dq, dk, dv, dg, dbeta, dh0 tensors or None)."""
+                  workspace=None, cu_seqlens=None) -> _lib.KdaBwdArgs:
+    """Fill the C backward argument struct (grads: dq, dk, dv, dg, dbeta, dh0 tensors or None).
+
+    With ``cu_seqlens`` (int32 device tensor [N + 1]) the batch is packed as in
+    :func:`make_args`.
+    """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
     if gate is None:
         gate = "none" if g is None else ("scalar" if g.dim() == 3 else "channel")
     x = _lib.KdaBwdArgs()
@@ -171,6 +177,7 @@ def make_bwd_args(q, k, v, g, beta, h0, do, dht, grads: dict, *, gate=None, scal
     x.grad_o, x.grad_ht = _ptr(do), _ptr(dht)
     x.grad_q, x.grad_k, x.grad_v = _ptr(grads.get("dq")), _ptr(grads.get("dk")), _ptr(grads.get("dv"))
     x.grad_g, x.grad_beta, x.grad_h0 = _ptr(grads.get("dg")), _ptr(grads.get("dbeta")), _ptr(grads.get("dh0"))
+    x.cu_seqlens = _ptr(cu_seqlens)
     if workspace is not None:
         x.workspace = _ptr(workspace)
         x.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -178,20 +185,26 @@ def make_bwd_args(q, k, v, g, beta, h0, do, dht, grads: dict, *, gate=None, scal
 
 
 def kda_chunk_bwd(q, k, v, g, beta, h0, do, dht=None, *, gate=None, scale_v=True, grads=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, cu_seqlens=None):
     """Backward of :func:`kda_chunk_fwd` through ``kda_chunk_bwd`` of the C ABI.
 
     Inputs are those of the forward plus do [B, T, H, dv] (dtype of q) and dht
     [B, H, dv, dk] fp32 or None.  Returns a dict with dq, dk, dv (dtype of q),
     dg (dtype and layout of g) when g is given, dbeta when beta is given, and
     dh0 (fp32).  ``grads`` may supply preallocated output tensors by those names.
+    cu_seqlens: int32 CUDA tensor [N + 1] for a packed batch of N sequences
+    (then q is [1, T, H, dk], h0 / dht / dh0 are [N, H, dv, dk]), or None.
     """
     lib = _lib.load()
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (h0, "h0"), (do, "do"),
-                    (dht, "dht")):
+                    (dht, "dht"), (cu_seqlens, "cu_seqlens")):
         _check(t, name)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
     out = dict(grads or {})
     out.setdefault("dq", torch.empty_like(q))
     out.setdefault("dk", torch.empty_like(k))
@@ -201,7 +214,7 @@ def kda_chunk_bwd(q, k, v, g, beta, h0, do, dht=None, *, gate=None, scale_v=True
     if beta is not None:
         out.setdefault("dbeta", torch.empty_like(beta))
     out.setdefault("dh0", torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device))
-    args = make_bwd_args(q, k, v, g, beta, h0, do, dht, out, gate=gate, scale_v=scale_v)
+    args = make_bwd_args(q, k, v, g, beta, h0, do, dht, out, gate=gate, scale_v=scale_v, cu_seqlens=cu_seqlens)
     need = lib.kda_chunk_bwd_workspace(ctypes.byref(args))
     if need == 0:
         rc = lib.kda_chunk_bwd(ctypes.byref(args), None)
@@ -219,9 +232,14 @@ def kda_chunk_bwd(q, k, v, g, beta, h0, do, dht=None, *, gate=None, scale_v=True
 
 
 def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None, clip=False,
-                   workspace=None) -> _lib.DplrFwdArgs:
-    """Fill the C DPLR argument struct from tensors (q, k, v, o may be None for the norm report)."""
+                   workspace=None, cu_seqlens=None) -> _lib.DplrFwdArgs:
+    """Fill the C DPLR argument struct from tensors (q, k, v, o may be None for the norm report).
+
+    With ``cu_seqlens`` the batch is packed as in :func:`make_args`.
+    """
     B, T, H, dk = a.shape
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
     dv = v.shape[-1] if v is not None else 0
     if gate is None:
         gate = "none" if g is None else ("scalar" if g.dim() == 3 else "channel")
@@ -233,6 +251,7 @@ def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None
     x.flags = _lib.DPLR_FLAG_CLIP_GATE if clip else 0
     x.q, x.k, x.v, x.a, x.b, x.g = _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(g)
     x.h0, x.o, x.ht = _ptr(h0), _ptr(o), _ptr(ht)
+    x.cu_seqlens = _ptr(cu_seqlens)
     if workspace is not None:
         x.workspace = _ptr(workspace)
         x.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -240,24 +259,30 @@ def make_dplr_args(q, k, v, a, b, g=None, h0=None, o=None, ht=None, *, gate=None
 
 
 def dplr_chunk_fwd(q, k, v, a, b, g=None, h0=None, *, gate=None, clip=False, output_final_state=True,
-                   o=None, ht=None, workspace=None, stream=None):
+                   o=None, ht=None, workspace=None, stream=None, cu_seqlens=None):
     """General gated DPLR forward through ``dplr_chunk_fwd`` of the C ABI.
 
     q, k, a, b: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, one dtype);
     g: log-decay [B, T, H, dk], [B, T, H] or None; h0: [B, H, dv, dk] fp32 or None.
     clip=True applies the eq. (7) gate clip (``DPLR_FLAG_CLIP_GATE``).
+    cu_seqlens: int32 CUDA tensor [N + 1] for a packed batch of N sequences
+    (then the inputs are [1, T, H, d], h0 / ht [N, H, dv, dk]), or None.
     Returns (o [B, T, H, dv] in q's dtype, ht [B, H, dv, dk] fp32 or None).
     """
     lib = _lib.load()
-    for t, name in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (g, "g"), (h0, "h0")):
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (g, "g"), (h0, "h0"),
+                    (cu_seqlens, "cu_seqlens")):
         _check(t, name)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    nseq = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if o is None:
         o = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
     if ht is None and output_final_state:
-        ht = torch.empty(B, H, dv, dk, dtype=torch.float32, device=q.device)
-    args = make_dplr_args(q, k, v, a, b, g, h0, o, ht, gate=gate, clip=clip)
+        ht = torch.empty(nseq, H, dv, dk, dtype=torch.float32, device=q.device)
+    args = make_dplr_args(q, k, v, a, b, g, h0, o, ht, gate=gate, clip=clip, cu_seqlens=cu_seqlens)
     need = lib.dplr_chunk_fwd_workspace(ctypes.byref(args))
     if need == 0:
         rc = lib.dplr_chunk_fwd(ctypes.byref(args), None)
@@ -299,19 +324,23 @@ def dplr_factor_norms(a, b, g=None, *, gate=None, clip=False, stream=None):
 
 
 def dplr_chunk_bwd(q, k, v, a, b, g, h0, do, dht=None, *, gate=None, clip=False, grads=None,
-                   workspace=None, stream=None):
+                   workspace=None, stream=None, cu_seqlens=None):
     """Backward of :func:`dplr_chunk_fwd` through ``dplr_chunk_bwd`` of the C ABI.
 
     Returns a dict with dq, dk, dv, da, db (dtype of q), dg (dtype and layout
     of g) when g is given, and dh0 (fp32).  ``grads`` may supply preallocated
-    outputs by those names.
+    outputs by those names.  cu_seqlens as for :func:`dplr_chunk_fwd`.
     """
     lib = _lib.load()
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (g, "g"), (h0, "h0"), (do, "do"),
-                    (dht, "dht")):
+                    (dht, "dht"), (cu_seqlens, "cu_seqlens")):
         _check(t, name)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
     out = dict(grads or {})
     for name, like in (("dq", q), ("dk", k), ("dv", v), ("da", a), ("db", b)):
         out.setdefault(name, torch.empty_like(like))
@@ -330,6 +359,7 @@ def dplr_chunk_bwd(q, k, v, a, b, g, h0, do, dht=None, *, gate=None, clip=False,
     x.grad_o, x.grad_ht = _ptr(do), _ptr(dht)
     x.grad_q, x.grad_k, x.grad_v = _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"])
     x.grad_a, x.grad_b, x.grad_g, x.grad_h0 = _ptr(out["da"]), _ptr(out["db"]), _ptr(out.get("dg")), _ptr(out["dh0"])
+    x.cu_seqlens = _ptr(cu_seqlens)
     need = lib.dplr_chunk_bwd_workspace(ctypes.byref(x))
     if need == 0:
         rc = lib.dplr_chunk_bwd(ctypes.byref(x), None)

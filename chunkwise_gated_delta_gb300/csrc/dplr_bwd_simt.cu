@@ -27,12 +27,13 @@
 // Four kernels, as for the KDA backward: a chunk-parallel prep kernel writes the
 // state-independent operands of every chunk (W, K-> and A-> times gamma^C,
 // Q<-, C, E, N_bk, P_k, P_a) once; the forward state scan and the reverse dS
-// scan per (32-wide value slice, head, batch) keep X and dC; then one CTA per
-// (chunk, head, batch) for every other gradient.
+// scan per (32-wide value slice, head, sequence) keep X and dC; then one CTA per
+// (chunk, head, sequence) for every other gradient.
 #include <cuda_bf16.h>
 
 #include "dplr_common.cuh"
 #include "kda_internal.h"
+#include "packed_seq.cuh"
 #include "warp_gemm.cuh"
 
 namespace kda {
@@ -82,7 +83,7 @@ struct BRec {
 };
 
 // ------------------------------------------------------------------ prep kernel
-// One CTA per (chunk, head, batch).  Products run as warp-tiled blocks
+// One CTA per (chunk, head, sequence).  Products run as warp-tiled blocks
 // (warp_gemm.cuh): tf32 tensor-core MMAs for bf16 inputs (TF32), exact float32
 // for float32 inputs.
 template <int DK, int DV, typename Tin, typename Tg, bool TF32>
@@ -104,19 +105,22 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_prep_kernel(const DplrParam
     float *gam = Nk + kC * SC;           // [DK]
     float *gsc = gam + DK;               // [C]
 
-    const int tid = threadIdx.x;
-    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
-    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const int tid = threadIdx.x, h = blockIdx.y;
+    int b, n;
+    seq::Seq sq;
+    if (!seq::chunk_of<kC>(p, b, n, sq)) return;
+    const int H = p.H;
+    const int t0 = n * kC, nvalid = min(kC, sq.len - t0);
+    const size_t row = (size_t)sq.row0 + t0;
     const Tin *v = static_cast<const Tin *>(p.v);
-    float *rec = p.ws_prep + (((size_t)b * H + h) * N + n) * bwd_rec_floats(DK, DV);
+    float *rec = p.ws_prep + seq::chunk_index<kC>(p, sq, h, n) * bwd_rec_floats(DK, DV);
 
     if (p.clip) {
-        dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
+        dplr::row_rho<DK, kC, Tin>(p, row, h, nvalid, rows);
         __syncthreads();
     }
-    wg::load_tile<kC, DV, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * DV, (size_t)H * DV, nvalid, Vm);
-    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
+    wg::load_tile<kC, DV, SV, kThreads>(v + (row * H + h) * DV, (size_t)H * DV, nvalid, Vm);
+    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, row, h, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
     __syncthreads();
     {
         auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
@@ -186,11 +190,14 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, dv = p.dv, N = (T + kC - 1) / kC;
+    const int H = p.H, dv = p.dv;
+    const seq::Seq sq = seq::seq_of<kC>(p, b);
+    const int N = sq.nch, T = sq.len;
+    const size_t row0 = sq.row0, ci0 = seq::chunk_index<kC>(p, sq, h, 0);
     const Tin *v = static_cast<const Tin *>(p.v);
     const size_t head = (size_t)b * H + h;
-    float *Sws = p.ws_S + head * (size_t)(N + 1) * dv * DK;
-    const float *recs = p.ws_prep + head * N * bwd_rec_floats(DK, DV);
+    float *Sws = p.ws_S + seq::state_index<kC>(p, sq, b, h, 0) * dv * DK;
+    const float *recs = p.ws_prep + ci0 * bwd_rec_floats(DK, DV);
     auto issue = [&](int n) {
         const float *rec = recs + (size_t)n * bwd_rec_floats(DK, DV);
         float *bf = ring + (n % kRing) * BUF;
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
         wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::AG, DK, bf + 2 * kC * SK);
         wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, bf + 3 * kC * SK);
         wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 3 * kC * SK + kC * SV);
-        wg::load_raw_async<kC, kDVS, Tin, kThreads>(v + (((size_t)b * T + n * kC) * H + h) * dv + e0, (size_t)H * dv,
+        wg::load_raw_async<kC, kDVS, Tin, kThreads>(v + ((row0 + n * kC) * H + h) * dv + e0, (size_t)H * dv,
                                                     min(kC, T - n * kC),
                                                     reinterpret_cast<Tin *>(bf + 3 * kC * SK + kC * SV + DK));
     };
@@ -226,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_states_kernel(const DplrPar
         wg::cp_async_wait<kRing - 1>();  // chunk n's copies (this thread's) have landed
         __syncthreads();
         wg::to_f32<kC, kDVS, SV, Tin, kThreads>(vraw, Vm);
-        float *xs = p.ws_x + ((head * N + n) * kC) * (size_t)dv + e0;
+        float *xs = p.ws_x + ((ci0 + n) * kC) * (size_t)dv + e0;
         wg::gemm16<kDVS, TF32>(
             DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
             [&](int i, int e, float x) {
@@ -267,11 +274,14 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, dv = p.dv, N = (T + kC - 1) / kC;
+    const int H = p.H, dv = p.dv;
+    const seq::Seq sq = seq::seq_of<kC>(p, b);
+    const int N = sq.nch, T = sq.len;
+    const size_t row0 = sq.row0, ci0 = seq::chunk_index<kC>(p, sq, h, 0);
     const Tin *dop = static_cast<const Tin *>(p.grad_o);
     const size_t head = (size_t)b * H + h;
-    float *dSws = p.ws_dS + head * (size_t)N * dv * DK;
-    const float *recs = p.ws_prep + head * N * bwd_rec_floats(DK, DV);
+    float *dSws = p.ws_dS + ci0 * dv * DK;
+    const float *recs = p.ws_prep + ci0 * bwd_rec_floats(DK, DV);
     // step i handles chunk N - 1 - i (the scan runs backwards)
     auto issue = [&](int i) {
         const int n = N - 1 - i;
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
         wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::QL, DK, bf + 2 * kC * SK);
         wg::load_tile_async<kC, kC, SC, kThreads>(rec + R::PA, kC, bf + 3 * kC * SK);
         wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 3 * kC * SK + kC * SC);
-        wg::load_raw_async<kC, kDVS, Tin, kThreads>(dop + (((size_t)b * T + n * kC) * H + h) * dv + e0,
+        wg::load_raw_async<kC, kDVS, Tin, kThreads>(dop + ((row0 + n * kC) * H + h) * dv + e0,
                                                     (size_t)H * dv, min(kC, T - n * kC),
                                                     reinterpret_cast<Tin *>(bf + 3 * kC * SK + kC * SC + DK));
     };
@@ -311,7 +321,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_dstate_kernel(const DplrPar
         __syncthreads();
         wg::to_f32<kC, kDVS, SV, Tin, kThreads>(draw, dO);
         __syncthreads();
-        float *dcs = p.ws_dc + ((head * N + n) * kC) * (size_t)dv + e0;
+        float *dcs = p.ws_dc + ((ci0 + n) * kC) * (size_t)dv + e0;
         wg::gemm16_2<kDVS, TF32>(
             DK, [&](int r, int d) { return AG[r * SK + d]; }, [&](int d, int e) { return dS[e * SK + d]; }, kC,
             [&](int r, int j) { return Pa[j * SC + r]; }, [&](int j, int e) { return dO[j * SV + e]; },
@@ -381,39 +391,41 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     float *slab = lastrow + DK;          // [32][SK] staged state rows
     float *dVs = slab + 32 * SK;         // [C][SV] K-> Diag(gamma^C) dS^T
 
-    const int tid = threadIdx.x;
-    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
-    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const int tid = threadIdx.x, h = blockIdx.y;
+    int b, n;
+    seq::Seq sq;
+    if (!seq::chunk_of<kC>(p, b, n, sq)) return;
+    const int H = p.H;
+    const int t0 = n * kC, nvalid = min(kC, sq.len - t0);
+    const size_t row = (size_t)sq.row0 + t0, ci = seq::chunk_index<kC>(p, sq, h, n);
     const Tin *v = static_cast<const Tin *>(p.v);
     const Tin *dop = static_cast<const Tin *>(p.grad_o);
-    const size_t head = (size_t)b * H + h;
-    const float *Sp = p.ws_S + (head * (N + 1) + n) * (size_t)DV * DK;
+    const float *Sp = p.ws_S + seq::state_index<kC>(p, sq, b, h, n) * DV * DK;
     const float *Sn = Sp + (size_t)DV * DK;
-    const float *dS = p.ws_dS + (head * N + n) * (size_t)DV * DK;
+    const float *dS = p.ws_dS + ci * DV * DK;
 
     if (p.clip) {
-        dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
+        dplr::row_rho<DK, kC, Tin>(p, row, h, nvalid, rows);
         __syncthreads();
     }
     {
-        const size_t r0 = (((size_t)b * T + t0) * H + h) * DV, rs = (size_t)H * DV;
+        const size_t r0 = (row * H + h) * DV, rs = (size_t)H * DV;
         wg::load_tile<kC, DV, SV, kThreads>(v + r0, rs, nvalid, Vm);
         wg::load_tile<kC, DV, SV, kThreads>(dop + r0, rs, nvalid, dO);
     }
-    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
+    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, row, h, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
     __syncthreads();
     // E, N_bk, P_k, P_a and W from the chunk record; V_2 (= X) and dC from the scans
     {
         using R = BRec<DK, DV>;
-        const float *rec = p.ws_prep + (head * N + n) * bwd_rec_floats(DK, DV);
+        const float *rec = p.ws_prep + ci * bwd_rec_floats(DK, DV);
         wg::load_tile<kC, kC, SC, kThreads>(rec + R::E, kC, kC, Em);
         wg::load_tile<kC, kC, SC, kThreads>(rec + R::NK, kC, kC, Nk);
         wg::load_tile<kC, kC, SC, kThreads>(rec + R::PK, kC, kC, Pk);
         wg::load_tile<kC, kC, SC, kThreads>(rec + R::PA, kC, kC, Pa);
         wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
-        wg::load_tile<kC, DV, SV, kThreads>(p.ws_x + (head * N + n) * (size_t)kC * DV, DV, kC, V2);
-        wg::load_tile<kC, DV, SV, kThreads>(p.ws_dc + (head * N + n) * (size_t)kC * DV, DV, kC, dC);
+        wg::load_tile<kC, DV, SV, kThreads>(p.ws_x + ci * kC * DV, DV, kC, V2);
+        wg::load_tile<kC, DV, SV, kThreads>(p.ws_dc + ci * kC * DV, DV, kC, dC);
     }
     __syncthreads();
     // O1 = dO V^T * M ; O2 = dO V_2^T * M ; Z1 = dC V^T
@@ -521,7 +533,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
             kC, [&](int i, int j) { return Pk[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; }, kC,
             [&](int i, int j) { return -Nk[j * SC + i]; }, [&](int j, int e) { return Ym[j * SV + e]; },
             [&](int i, int e, float x) {
-                if (i < nvalid) stf(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, x + dVs[i * SV + e]);
+                if (i < nvalid) stf(gv, ((row + i) * H + h) * DV + e, x + dVs[i * SV + e]);
             });
     }
     __syncthreads();
@@ -532,7 +544,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
         const int i = idx / DK, d = idx % DK;
         const float gm = Gm[i * SK + d], dq = dQl[i * SK + d];
         if (i < nvalid) {
-            const size_t off = (((size_t)b * T + t0 + i) * H + h) * DK + d;
+            const size_t off = ((row + i) * H + h) * DK + d;
             stf(gq, off, dq * gm);
             stf(gk, off, dKr[i * SK + d] / gm);
         }
@@ -557,11 +569,11 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
         for (int i = warp; i < kC; i += kThreads / 32) {
             float lost = 0.f;
             if (i < nvalid) {
-                const size_t row = ((size_t)b * T + t0 + i) * H + h;
+                const size_t tok = (row + i) * H + h;
                 for (int d = lane; d < DK; d += 32) {
                     const float dgp = dQl[i * SK + d];
-                    const bool keep = !p.clip || ldf(graw, row * DK + d) < rows[i].w;
-                    stf(gg, row * DK + d, keep ? dgp : 0.f);
+                    const bool keep = !p.clip || ldf(graw, tok * DK + d) < rows[i].w;
+                    stf(gg, tok * DK + d, keep ? dgp : 0.f);
                     if (!keep) lost += dgp;
                 }
             }
@@ -577,10 +589,10 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
             if (lane == 0) {
                 float lost = 0.f;
                 if (i < nvalid) {
-                    const size_t row = ((size_t)b * T + t0 + i) * H + h;
-                    const float g0 = p.gate_kind == KDA_GATE_SCALAR ? ldf(graw, row) : 0.f;
+                    const size_t tok = (row + i) * H + h;
+                    const float g0 = p.gate_kind == KDA_GATE_SCALAR ? ldf(graw, tok) : 0.f;
                     const bool keep = !p.clip || g0 < rows[i].w;
-                    if (p.gate_kind == KDA_GATE_SCALAR) stf(gg, row, keep ? acc : 0.f);
+                    if (p.gate_kind == KDA_GATE_SCALAR) stf(gg, tok, keep ? acc : 0.f);
                     if (!keep) lost = acc;
                 }
                 rsum[i] = lost;
@@ -615,7 +627,7 @@ __global__ void __launch_bounds__(kThreads) dplr_bwd_grad_kernel(const DplrParam
     for (int idx = tid; idx < kC * DK; idx += kThreads) {
         const int i = idx / DK, d = idx % DK;
         if (i >= nvalid) continue;
-        const size_t off = (((size_t)b * T + t0 + i) * H + h) * DK + d;
+        const size_t off = ((row + i) * H + h) * DK + d;
         const float gm = Gm[i * SK + d];
         float da = dAr[i * SK + d] / gm, db = dBl[i * SK + d] * gm;
         if (p.clip) {
@@ -645,7 +657,6 @@ cudaError_t set_smem(F *fn, size_t bytes) {
 template <int DK, int DV, typename Tin, typename Tg>
 cudaError_t launch_all(const DplrParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
-    const int N = (p.T + kC - 1) / kC;
     cudaError_t e;
     const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK, Tin>(), sb = dstate_smem_bytes<DK, Tin>();
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
@@ -654,7 +665,7 @@ cudaError_t launch_all(const DplrParams &p, cudaStream_t s) {
     if ((e = set_smem(dplr_bwd_states_kernel<DK, DV, Tin, kTf32>, sa)) != cudaSuccess) return e;
     if ((e = set_smem(dplr_bwd_dstate_kernel<DK, DV, Tin, kTf32>, sb)) != cudaSuccess) return e;
     if ((e = set_smem(dplr_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
-    const dim3 gscan(p.dv / kDVS, p.H, p.B), gchunk(N, p.H, p.B);
+    const dim3 gscan(p.dv / kDVS, p.H, p.B), gchunk = seq::chunk_grid<kC>(p.B, p.T, p.H, p.cu_seqlens != nullptr);
     dplr_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sp, s>>>(p);
     dplr_bwd_states_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sa, s>>>(p);
     dplr_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sb, s>>>(p);
@@ -673,9 +684,19 @@ cudaError_t launch_typed(const DplrParams &p, cudaStream_t s) {
 
 }  // namespace
 
-size_t dplr_bwd_state_bytes(int B, int T, int H, int dk, int dv) {
-    const size_t N = (T + kC - 1) / kC;
-    return sizeof(float) * (size_t)B * H * ((2 * N + 1) * dv * dk + N * bwd_rec_floats(dk, dv) + 2 * N * kC * dv);
+size_t dplr_bwd_state_bytes(int B, int T, int H, int dk, int dv, bool packed) {
+    const size_t NS = seq::chunk_slots<kC>(B, T, packed);
+    return sizeof(float) * (size_t)H * ((2 * NS + B) * dv * dk + NS * bwd_rec_floats(dk, dv) + 2 * NS * kC * dv);
+}
+
+void dplr_bwd_carve(DplrParams &p, float *ws) {
+    const size_t NS = seq::chunk_slots<kC>(p.B, p.T, p.cu_seqlens != nullptr), H = p.H;
+    const size_t st = (size_t)p.dv * p.dk;
+    p.ws_S = ws;                                     // [H][NS + B state slots][dv][dk]
+    p.ws_dS = p.ws_S + H * (NS + p.B) * st;          // [H][NS][dv][dk]
+    p.ws_prep = p.ws_dS + H * NS * st;               // [H][NS] records
+    p.ws_x = p.ws_prep + H * NS * bwd_rec_floats(p.dk, p.dv);
+    p.ws_dc = p.ws_x + H * NS * kC * p.dv;           // [H][NS][C][dv] each
 }
 
 cudaError_t launch_dplr_bwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s) {

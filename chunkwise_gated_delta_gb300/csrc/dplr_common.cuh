@@ -43,17 +43,17 @@ __device__ __forceinline__ float rho_eq4(float na2, float nb2, float ab) {
     return 0.5f * (eta + sqrtf(fmaxf(eta * eta - 4.f * eta * cosv + 4.f, 0.f)));
 }
 
-// Per row c < C of the chunk starting at t0: rows[c] = (|a|^2, |b|^2, a.b, -log rho)
-// (zeros past nvalid).  One warp per row; no barrier inside.
+// Per row c < C of the chunk starting at row `row0` of its batch: rows[c] = (|a|^2, |b|^2,
+// a.b, -log rho) (zeros past nvalid).  One warp per row; no barrier inside.
 template <int DK, int C, typename Tin>
-__device__ void row_rho(const DplrParams &p, int b, int h, int t0, int nvalid, float4 *rows) {
+__device__ void row_rho(const DplrParams &p, size_t row0, int h, int nvalid, float4 *rows) {
     const Tin *a = static_cast<const Tin *>(p.a);
     const Tin *bb = static_cast<const Tin *>(p.b);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     for (int c = warp; c < C; c += nwarps) {
         float na2 = 0.f, nb2 = 0.f, ab = 0.f;
         if (c < nvalid) {
-            const size_t row = (((size_t)b * p.T + t0 + c) * p.H + h) * DK;
+            const size_t row = ((row0 + c) * p.H + h) * DK;
             for (int d = lane; d < DK; d += 32) {
                 const float av = ldf(a, row + d), bv = ldf(bb, row + d);
                 na2 += av * av;
@@ -71,7 +71,8 @@ __device__ void row_rho(const DplrParams &p, int b, int h, int t0, int nvalid, f
 
 
 
-// Gamma and the rescaled tiles of one chunk (rows past nvalid zero, Gamma held
+// Gamma and the rescaled tiles of the chunk starting at row `row0` of its batch (rows
+// past nvalid zero, Gamma held
 // at its last value; gam[d] = gamma^C): all threads load the raw tiles first
 // (16-byte vector loads, 256 threads), then one thread per key channel runs the
 // (optionally clipped) cumsum down its column in shared memory.  Gm is required
@@ -80,7 +81,7 @@ __device__ void row_rho(const DplrParams &p, int b, int h, int t0, int nvalid, f
 // barrier must separate the two).  Contains one barrier; the caller
 // synchronises before reading the tiles.
 template <int DK, int SK, int C, typename Tin, typename Tg>
-__device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int nvalid, const float4 *rows,
+__device__ void load_rescaled_par(const DplrParams &p, size_t row0, int h, int nvalid, const float4 *rows,
                                   float *Gm, float *Ql, float *Kr, float *Ar, float *Bl, float *gam, float *gsc) {
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
@@ -88,7 +89,7 @@ __device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int
     const Tin *bb = static_cast<const Tin *>(p.b);
     const Tg *g = static_cast<const Tg *>(p.g);
     const int tid = threadIdx.x, nt = blockDim.x;
-    const size_t r0 = (((size_t)b * p.T + t0) * p.H + h) * DK, rs = (size_t)p.H * DK;
+    const size_t r0 = (row0 * p.H + h) * DK, rs = (size_t)p.H * DK;
     if (Ql) wg::load_tile<C, DK, SK, 256>(q + r0, rs, nvalid, Ql);
     if (Kr) wg::load_tile<C, DK, SK, 256>(k + r0, rs, nvalid, Kr);
     if (Ar) wg::load_tile<C, DK, SK, 256>(a + r0, rs, nvalid, Ar);
@@ -96,7 +97,7 @@ __device__ void load_rescaled_par(const DplrParams &p, int b, int h, int t0, int
     if (p.gate_kind == KDA_GATE_CHANNEL) wg::load_tile<C, DK, SK, 256>(g + r0, rs, nvalid, Gm);
     if (tid < C) {
         float gv = 0.f;
-        if (tid < nvalid && p.gate_kind == KDA_GATE_SCALAR) gv = ldf(g, ((size_t)b * p.T + t0 + tid) * p.H + h);
+        if (tid < nvalid && p.gate_kind == KDA_GATE_SCALAR) gv = ldf(g, (row0 + tid) * p.H + h);
         gsc[tid] = gv;
     }
     __syncthreads();

@@ -28,6 +28,7 @@
 
 #include "dplr_common.cuh"
 #include "kda_internal.h"
+#include "packed_seq.cuh"
 #include "warp_gemm.cuh"
 
 namespace kda {
@@ -66,7 +67,7 @@ struct DRec {
 template <int DK>
 __host__ __device__ constexpr bool prep_aliases() { return 3 * kC * pad4(kC) <= kC * pad4(DK); }
 
-// One CTA per (chunk, head, batch).  Products run as warp-tiled 32 x N blocks
+// One CTA per (chunk, head, sequence).  Products run as warp-tiled 32 x N blocks
 // (warp_gemm.cuh): tf32 tensor-core MMAs for bf16 inputs (TF32), exact float32
 // for float32 inputs.
 template <int DK, int DV, typename Tin, typename Tg, bool TF32>
@@ -98,19 +99,22 @@ dplr_fwd_prep_kernel(const DplrParams p) {
     float *Ts = Em + kC * SC;         // [C][SC]  scratch of the inverse, then P_a E
     float *M1 = Ts + kC * SC;         // [C][SC]  E (B<- K->^T * M_{-1})
 
-    const int tid = threadIdx.x;
-    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
-    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const int tid = threadIdx.x, h = blockIdx.y;
+    int b, n;
+    seq::Seq sq;
+    if (!seq::chunk_of<kC>(p, b, n, sq)) return;
+    const int H = p.H;
+    const int t0 = n * kC, nvalid = min(kC, sq.len - t0);
+    const size_t row = (size_t)sq.row0 + t0;
     const Tin *v = static_cast<const Tin *>(p.v);
-    float *rec = p.ws_prep + (((size_t)b * H + h) * N + n) * dplr_rec_floats(DK, DV);
+    float *rec = p.ws_prep + seq::chunk_index<kC>(p, sq, h, n) * dplr_rec_floats(DK, DV);
 
     if (p.clip) {
-        dplr::row_rho<DK, kC, Tin>(p, b, h, t0, nvalid, rows);
+        dplr::row_rho<DK, kC, Tin>(p, row, h, nvalid, rows);
         __syncthreads();
     }
-    wg::load_tile<kC, DV, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * DV, (size_t)H * DV, nvalid, Vm);
-    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, b, h, t0, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
+    wg::load_tile<kC, DV, SV, kThreads>(v + (row * H + h) * DV, (size_t)H * DV, nvalid, Vm);
+    dplr::load_rescaled_par<DK, SK, kC, Tin, Tg>(p, row, h, nvalid, rows, Gm, Ql, Kr, Ar, Bl, gam, gsc);
     __syncthreads();
     {
         auto bAr = [&](int d, int j) { return Ar[j * SK + d]; };
@@ -194,10 +198,13 @@ dplr_fwd_simt_kernel(const DplrParams p) {
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS;
     const int h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, dv = p.dv, N = (T + kC - 1) / kC;
+    const int H = p.H, dv = p.dv;
+    const seq::Seq sq = seq::seq_of<kC>(p, b);
+    const int N = sq.nch, T = sq.len;
+    const size_t row0 = sq.row0;
     const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
-    const float *recs = p.ws_prep + ((size_t)b * H + h) * N * dplr_rec_floats(DK, DV);
+    const float *recs = p.ws_prep + seq::chunk_index<kC>(p, sq, h, 0) * dplr_rec_floats(DK, DV);
     auto issue = [&](int n) {
         const float *rec = recs + (size_t)n * dplr_rec_floats(DK, DV);
         float *bf = bufs + (n & 1) * BUF;
@@ -208,7 +215,7 @@ dplr_fwd_simt_kernel(const DplrParams p) {
         wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::CC + e0, DV, bf + 4 * kC * SK);
         wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::OL + e0, DV, bf + 4 * kC * SK + kC * SV);
         wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 4 * kC * SK + 2 * kC * SV);
-        wg::load_raw_async<kC, kDVS, Tin, kThreads>(v + (((size_t)b * T + n * kC) * H + h) * dv + e0, (size_t)H * dv,
+        wg::load_raw_async<kC, kDVS, Tin, kThreads>(v + ((row0 + n * kC) * H + h) * dv + e0, (size_t)H * dv,
                                                     min(kC, T - n * kC),
                                                     reinterpret_cast<Tin *>(bf + 4 * kC * SK + 2 * kC * SV + DK));
     };
@@ -238,7 +245,7 @@ dplr_fwd_simt_kernel(const DplrParams p) {
                 DK, [&](int i, int d) { return Wm[i * SK + d]; }, bS, DK, [&](int i, int d) { return QT[i * SK + d]; },
                 bS, [&](int i, int e, float ws, float qs) {
                     Xm[i * SV + e] = Cs[i * SV + e] - ws;
-                    if (i < nvalid) o[(((size_t)b * T + t0 + i) * H + h) * dv + e0 + e] = from_f<Tin>(Os[i * SV + e] + qs);
+                    if (i < nvalid) o[((row0 + t0 + i) * H + h) * dv + e0 + e] = from_f<Tin>(Os[i * SV + e] + qs);
                 });
         }
         __syncthreads();
@@ -265,7 +272,6 @@ constexpr size_t dplr_smem_bytes() {
 template <int DK, int DV, typename Tin, typename Tg>
 cudaError_t launch_dkv(const DplrParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
-    const int N = (p.T + kC - 1) / kC;
     const size_t sp = prep_smem_bytes<DK, DV>(), sm = dplr_smem_bytes<DK, Tin>();
     static_assert(dplr_smem_bytes<128, float>() <= 227 * 1024, "scan shared memory");
     static_assert(prep_smem_bytes<128, 256>() <= 227 * 1024, "shared memory");
@@ -275,7 +281,8 @@ cudaError_t launch_dkv(const DplrParams &p, cudaStream_t s) {
     e = cudaFuncSetAttribute(dplr_fwd_simt_kernel<DK, DV, Tin, kTf32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
-    dplr_fwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<dim3(N, p.H, p.B), kThreads, sp, s>>>(p);
+    dplr_fwd_prep_kernel<DK, DV, Tin, Tg, kTf32>
+        <<<seq::chunk_grid<kC>(p.B, p.T, p.H, p.cu_seqlens != nullptr), kThreads, sp, s>>>(p);
     dplr_fwd_simt_kernel<DK, DV, Tin, kTf32><<<dim3(p.dv / kDVS, p.H, p.B), kThreads, sm, s>>>(p);
     return cudaGetLastError();
 }
@@ -380,7 +387,7 @@ __global__ void __launch_bounds__(256)
 dplr_factor_norm_kernel(const DplrParams p, float *rho, float *nrm, float *maxes) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const long ntok = (long)p.B * p.T * p.H;
+    const long ntok = (long)(p.cu_seqlens ? 1 : p.B) * p.T * p.H;   // packed: one [1, T] batch
     if (warp >= ntok) return;
     const int dk = p.dk;
     const Tin *a = static_cast<const Tin *>(p.a);
@@ -421,8 +428,8 @@ dplr_factor_norm_kernel(const DplrParams p, float *rho, float *nrm, float *maxes
 
 }  // namespace
 
-size_t dplr_fwd_record_bytes(int B, int T, int H, int dk, int dv) {
-    return sizeof(float) * (size_t)B * H * ((T + kC - 1) / kC) * dplr_rec_floats(dk, dv);
+size_t dplr_fwd_record_bytes(int B, int T, int H, int dk, int dv, bool packed) {
+    return sizeof(float) * (size_t)H * seq::chunk_slots<kC>(B, T, packed) * dplr_rec_floats(dk, dv);
 }
 
 cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s) {
@@ -433,7 +440,7 @@ cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16
 
 cudaError_t launch_dplr_factor_norms(const DplrParams &p, int in_bf16, int g_is_bf16, float *rho, float *nrm,
                                      float *maxes, cudaStream_t s) {
-    const long ntok = (long)p.B * p.T * p.H;
+    const long ntok = (long)(p.cu_seqlens ? 1 : p.B) * p.T * p.H;
     const long blocks = (ntok * 32 + 255) / 256;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
     if (maxes) {

@@ -81,6 +81,7 @@ kda_status validate_dplr_common(const dplr_fwd_args *a) {
     const void *ptrs[] = {a->q, a->k, a->v, a->a, a->b, a->g, a->h0, a->o, a->ht, a->workspace};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (a->cu_seqlens && (reinterpret_cast<uintptr_t>(a->cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
     const double elems = (double)a->B * a->T * a->H * (a->dk > 256 ? a->dk : 256);
     if (elems > 9.0e18 / 8 || (double)a->B * a->T * a->H > 2.0e9) return KDA_ERR_INVALID_ARG;
     if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
@@ -94,7 +95,7 @@ kda_status validate_dplr(const dplr_fwd_args *a) {
     if (a->dv % 32 != 0 || a->dv > 256) return KDA_ERR_UNSUPPORTED;
     if (a->chunk != 0 && a->chunk != 32) return KDA_ERR_UNSUPPORTED;
     const size_t es = dtype_size(a->dtype);
-    const size_t nbt = (size_t)a->B * a->T * a->H;
+    const size_t nbt = (size_t)(a->cu_seqlens ? 1 : a->B) * a->T * a->H;   // packed: one [1, T, H, d] batch
     const size_t o_bytes = nbt * a->dv * es;
     const size_t state_bytes = (size_t)a->B * a->H * a->dv * a->dk * 4;
     const size_t ht_bytes = a->ht ? state_bytes : 0;
@@ -103,7 +104,8 @@ kda_status validate_dplr(const dplr_fwd_args *a) {
     struct R { const void *p; size_t n; } ins[] = {
         {a->q, nbt * a->dk * es}, {a->k, nbt * a->dk * es}, {a->v, nbt * a->dv * es},
         {a->a, nbt * a->dk * es}, {a->b, nbt * a->dk * es}, {a->g, g_bytes},
-        {a->h0, a->h0 ? state_bytes : 0}, {a->workspace, a->workspace_bytes}};
+        {a->h0, a->h0 ? state_bytes : 0}, {a->workspace, a->workspace_bytes},
+        {a->cu_seqlens, a->cu_seqlens ? (size_t)(a->B + 1) * 4 : 0}};
     for (const R &r : ins) {
         if (overlaps(a->o, o_bytes, r.p, r.n)) return KDA_ERR_INVALID_ARG;
         if (overlaps(a->ht, ht_bytes, r.p, r.n)) return KDA_ERR_INVALID_ARG;
@@ -130,13 +132,14 @@ kda_status validate_bwd(const kda_bwd_args *a) {
                           a->grad_k, a->grad_v, a->grad_g, a->grad_beta, a->grad_h0, a->workspace};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (a->cu_seqlens && (reinterpret_cast<uintptr_t>(a->cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
     const double elems = (double)a->B * a->T * a->H * (a->dk > a->dv ? a->dk : a->dv);
     if (elems > 9.0e18 / 8 || (double)a->B * a->T * a->H > 2.0e9) return KDA_ERR_INVALID_ARG;
     if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
     if (a->dv != 64 && a->dv != 128) return KDA_ERR_UNSUPPORTED;
     if (a->chunk != 0 && a->chunk != 32) return KDA_ERR_UNSUPPORTED;
     const size_t es = dtype_size(a->dtype);
-    const size_t nbt = (size_t)a->B * a->T * a->H;
+    const size_t nbt = (size_t)(a->cu_seqlens ? 1 : a->B) * a->T * a->H;   // packed: one [1, T, H, d] batch
     const size_t state_bytes = (size_t)a->B * a->H * a->dv * a->dk * 4;
     const size_t g_bytes = a->gate_kind == KDA_GATE_CHANNEL ? nbt * a->dk * dtype_size(a->g_dtype)
                            : a->gate_kind == KDA_GATE_SCALAR ? nbt * dtype_size(a->g_dtype) : 0;
@@ -144,7 +147,8 @@ kda_status validate_bwd(const kda_bwd_args *a) {
     const R ins[] = {{a->q, nbt * a->dk * es}, {a->k, nbt * a->dk * es}, {a->v, nbt * a->dv * es},
                      {a->g, g_bytes}, {a->beta, a->beta ? nbt * es : 0}, {a->h0, a->h0 ? state_bytes : 0},
                      {a->grad_o, nbt * a->dv * es}, {a->grad_ht, a->grad_ht ? state_bytes : 0},
-                     {a->workspace, a->workspace_bytes}};
+                     {a->workspace, a->workspace_bytes},
+                     {a->cu_seqlens, a->cu_seqlens ? (size_t)(a->B + 1) * 4 : 0}};
     const R outs[] = {{a->grad_q, nbt * a->dk * es}, {a->grad_k, nbt * a->dk * es},
                       {a->grad_v, nbt * a->dv * es}, {a->grad_g, g_bytes},
                       {a->grad_beta, a->grad_beta ? nbt * es : 0}, {a->grad_h0, a->grad_h0 ? state_bytes : 0}};
@@ -158,7 +162,7 @@ kda_status validate_bwd(const kda_bwd_args *a) {
 }
 
 size_t bwd_workspace_bytes(const kda_bwd_args *a) {
-    return kStatusBytes + kda::bwd_state_bytes(a->B, a->T, a->H, a->dk, a->dv);
+    return kStatusBytes + kda::bwd_state_bytes(a->B, a->T, a->H, a->dk, a->dv, a->cu_seqlens != nullptr);
 }
 
 kda::DplrParams dplr_params(const dplr_fwd_args *args) {
@@ -169,6 +173,7 @@ kda::DplrParams dplr_params(const dplr_fwd_args *args) {
     p.q = args->q; p.k = args->k; p.v = args->v; p.a = args->a; p.b = args->b; p.g = args->g;
     p.h0 = args->h0; p.o = args->o; p.ht = args->ht;
     p.status = static_cast<int *>(args->workspace);
+    p.cu_seqlens = args->cu_seqlens;
     return p;
 }
 
@@ -190,13 +195,14 @@ kda_status validate_dplr_bwd(const dplr_bwd_args *a) {
                           a->grad_v, a->grad_a, a->grad_b, a->grad_g, a->grad_h0, a->workspace};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (a->cu_seqlens && (reinterpret_cast<uintptr_t>(a->cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
     const double elems = (double)a->B * a->T * a->H * (a->dk > a->dv ? a->dk : a->dv);
     if (elems > 9.0e18 / 8 || (double)a->B * a->T * a->H > 2.0e9) return KDA_ERR_INVALID_ARG;
     if (a->dk != 64 && a->dk != 128) return KDA_ERR_UNSUPPORTED;
     if (a->dv != 64 && a->dv != 128) return KDA_ERR_UNSUPPORTED;
     if (a->chunk != 0 && a->chunk != 16) return KDA_ERR_UNSUPPORTED;
     const size_t es = dtype_size(a->dtype);
-    const size_t nbt = (size_t)a->B * a->T * a->H;
+    const size_t nbt = (size_t)(a->cu_seqlens ? 1 : a->B) * a->T * a->H;   // packed: one [1, T, H, d] batch
     const size_t state_bytes = (size_t)a->B * a->H * a->dv * a->dk * 4;
     const size_t g_bytes = a->gate_kind == KDA_GATE_CHANNEL ? nbt * a->dk * dtype_size(a->g_dtype)
                            : a->gate_kind == KDA_GATE_SCALAR ? nbt * dtype_size(a->g_dtype) : 0;
@@ -204,7 +210,8 @@ kda_status validate_dplr_bwd(const dplr_bwd_args *a) {
     const R ins[] = {{a->q, nbt * a->dk * es}, {a->k, nbt * a->dk * es}, {a->v, nbt * a->dv * es},
                      {a->a, nbt * a->dk * es}, {a->b, nbt * a->dk * es}, {a->g, g_bytes},
                      {a->h0, a->h0 ? state_bytes : 0}, {a->grad_o, nbt * a->dv * es},
-                     {a->grad_ht, a->grad_ht ? state_bytes : 0}, {a->workspace, a->workspace_bytes}};
+                     {a->grad_ht, a->grad_ht ? state_bytes : 0}, {a->workspace, a->workspace_bytes},
+                     {a->cu_seqlens, a->cu_seqlens ? (size_t)(a->B + 1) * 4 : 0}};
     const R outs[] = {{a->grad_q, nbt * a->dk * es}, {a->grad_k, nbt * a->dk * es},
                       {a->grad_v, nbt * a->dv * es}, {a->grad_a, nbt * a->dk * es},
                       {a->grad_b, nbt * a->dk * es}, {a->grad_g, g_bytes},
@@ -219,7 +226,7 @@ kda_status validate_dplr_bwd(const dplr_bwd_args *a) {
 }
 
 size_t dplr_bwd_workspace_bytes(const dplr_bwd_args *a) {
-    return kStatusBytes + kda::dplr_bwd_state_bytes(a->B, a->T, a->H, a->dk, a->dv);
+    return kStatusBytes + kda::dplr_bwd_state_bytes(a->B, a->T, a->H, a->dk, a->dv, a->cu_seqlens != nullptr);
 }
 
 kda_status from_cuda(cudaError_t e) {
@@ -295,13 +302,15 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
 
 size_t dplr_chunk_fwd_workspace(const dplr_fwd_args *args) {
     if (validate_dplr(args) != KDA_OK) return 0;
-    return kStatusBytes + kda::dplr_fwd_record_bytes(args->B, args->T, args->H, args->dk, args->dv);
+    return kStatusBytes + kda::dplr_fwd_record_bytes(args->B, args->T, args->H, args->dk, args->dv,
+                                                     args->cu_seqlens != nullptr);
 }
 
 kda_status dplr_chunk_fwd(const dplr_fwd_args *args, kda_stream_t stream) {
     kda_status st = validate_dplr(args);
     if (st != KDA_OK) return st;
-    const size_t need = kStatusBytes + kda::dplr_fwd_record_bytes(args->B, args->T, args->H, args->dk, args->dv);
+    const size_t need = kStatusBytes + kda::dplr_fwd_record_bytes(args->B, args->T, args->H, args->dk, args->dv,
+                                                                  args->cu_seqlens != nullptr);
     if (!args->workspace || args->workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(args->workspace)) return KDA_ERR_INVALID_ARG;   // vector and async copies into it
     kda::DplrParams p = dplr_params(args);
@@ -328,16 +337,10 @@ kda_status dplr_chunk_bwd(const dplr_bwd_args *args, kda_stream_t stream) {
     p.grad_o = args->grad_o; p.grad_ht = args->grad_ht;
     p.grad_q = args->grad_q; p.grad_k = args->grad_k; p.grad_v = args->grad_v;
     p.grad_a = args->grad_a; p.grad_b = args->grad_b; p.grad_g = args->grad_g; p.grad_h0 = args->grad_h0;
+    p.cu_seqlens = args->cu_seqlens;
     unsigned char *ws = static_cast<unsigned char *>(args->workspace);
-    const size_t N = (size_t)(args->T + 15) / 16;
-    const size_t per_state = (size_t)args->B * args->H * args->dv * args->dk;
-    const size_t bh = (size_t)args->B * args->H;
     p.status = reinterpret_cast<int *>(ws);
-    p.ws_S = reinterpret_cast<float *>(ws + kStatusBytes);
-    p.ws_dS = p.ws_S + (N + 1) * per_state;
-    p.ws_prep = p.ws_dS + N * per_state;
-    p.ws_x = p.ws_prep + N * bh * (4 * 16 * (size_t)args->dk + 16 * (size_t)args->dv + 4 * 16 * 16 + args->dk);
-    p.ws_dc = p.ws_x + N * bh * 16 * args->dv;
+    kda::dplr_bwd_carve(p, reinterpret_cast<float *>(ws + kStatusBytes));
     return from_cuda(kda::launch_dplr_bwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -346,7 +349,7 @@ kda_status dplr_factor_norms(const dplr_fwd_args *args, float *rho, float *norm,
                              kda_stream_t stream) {
     kda_status st = validate_dplr_common(args);
     if (st != KDA_OK) return st;
-    const size_t nbt = (size_t)args->B * args->T * args->H;
+    const size_t nbt = (size_t)(args->cu_seqlens ? 1 : args->B) * args->T * args->H;
     const void *outs[] = {rho, norm, maxes};
     for (const void *p : outs)
         if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
@@ -387,17 +390,10 @@ kda_status kda_chunk_bwd(const kda_bwd_args *args, kda_stream_t stream) {
     p.grad_o = args->grad_o; p.grad_ht = args->grad_ht;
     p.grad_q = args->grad_q; p.grad_k = args->grad_k; p.grad_v = args->grad_v;
     p.grad_g = args->grad_g; p.grad_beta = args->grad_beta; p.grad_h0 = args->grad_h0;
+    p.cu_seqlens = args->cu_seqlens;
     unsigned char *ws = static_cast<unsigned char *>(args->workspace);
-    const size_t N = (size_t)(args->T + 31) / 32;
-    const size_t per_state = (size_t)args->B * args->H * args->dv * args->dk;
     p.status = reinterpret_cast<int *>(ws);
-    p.ws_S = reinterpret_cast<float *>(ws + kStatusBytes);
-    p.ws_dS = p.ws_S + (N + 1) * per_state;
-    p.ws_prep = p.ws_dS + N * per_state;
-    const size_t recs = N * (size_t)args->B * args->H * (3 * 32 * 32 + 3 * 32 * (size_t)args->dk + 32 * (size_t)args->dv +
-                                                          args->dk);
-    p.ws_vnew = p.ws_prep + recs;
-    p.ws_du = p.ws_vnew + N * (size_t)args->B * args->H * 32 * args->dv;
+    kda::bwd_carve(p, reinterpret_cast<float *>(ws + kStatusBytes));
     return from_cuda(kda::launch_bwd_simt(p, args->dtype == KDA_BF16, args->g_dtype == KDA_BF16,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }

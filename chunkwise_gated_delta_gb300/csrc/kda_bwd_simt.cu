@@ -20,19 +20,20 @@
 //
 // (dW against S_[t-1]; dK-> with the output term the page's final
 // combination carries.)  Four kernels:
-//   prep  one CTA per (chunk, head, batch): everything of a chunk that does
+//   prep  one CTA per (chunk, head, sequence): everything of a chunk that does
 //         not depend on the state (A~, P, N, W, U, K~, Q<-, gamma^C) into a
 //         chunk record in the workspace;
-//   A     forward scan per (value slice, head, batch) from the records: the
+//   A     forward scan per (value slice, head, sequence) from the records: the
 //         state before every chunk, the final state and V_new, into the
 //         workspace;
-//   B     reverse scan per (value slice, head, batch) from the records: dS
+//   B     reverse scan per (value slice, head, sequence) from the records: dS
 //         after every chunk and dU into the workspace, and dh0;
-//   C     one CTA per (chunk, head, batch): every other gradient of the chunk,
+//   C     one CTA per (chunk, head, sequence): every other gradient of the chunk,
 //         from its record, V_new, dU and the stored S_prev, S_next and dS.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
+#include "packed_seq.cuh"
 #include "warp_gemm.cuh"
 
 namespace kda {
@@ -42,6 +43,21 @@ constexpr int kC = 32;       // chunk length
 constexpr int kDVS = 32;     // value rows per CTA in the scans
 constexpr int kThreads = 256;
 constexpr int kThreadsC = 512;   // the gradient kernel: 16 warps to hide the latency of its L2 reads
+
+using seq::Seq;
+__host__ __device__ __forceinline__ int chunk_slots(int B, int T, bool packed) {
+    return seq::chunk_slots<kC>(B, T, packed);
+}
+__device__ __forceinline__ Seq seq_of(const BwdParams &p, int b) { return seq::seq_of<kC>(p, b); }
+__device__ __forceinline__ bool chunk_of(const BwdParams &p, int &b, int &n, Seq &sq) {
+    return seq::chunk_of<kC>(p, b, n, sq);
+}
+__device__ __forceinline__ size_t chunk_index(const BwdParams &p, const Seq &sq, int h, int n) {
+    return seq::chunk_index<kC>(p, sq, h, n);
+}
+__device__ __forceinline__ size_t state_index(const BwdParams &p, const Seq &sq, int b, int h, int n) {
+    return seq::state_index<kC>(p, sq, b, h, n);
+}
 
 template <typename T> __device__ __forceinline__ float ld(const T *p, size_t i);
 template <> __device__ __forceinline__ float ld<float>(const float *p, size_t i) { return p[i]; }
@@ -55,32 +71,33 @@ template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, 
 }
 
 template <typename Tin>
-__device__ void load_beta(const BwdParams &p, int b, int h, int t0, int nvalid, float *beta) {
+__device__ void load_beta(const BwdParams &p, size_t row, int h, int nvalid, float *beta) {
     const Tin *bp = static_cast<const Tin *>(p.beta);
     const int tid = threadIdx.x;
-    if (tid < kC) beta[tid] = (p.has_beta && tid < nvalid) ? ld(bp, ((size_t)b * p.T + t0 + tid) * p.H + h) : 0.f;
+    if (tid < kC) beta[tid] = (p.has_beta && tid < nvalid) ? ld(bp, (row + tid) * p.H + h) : 0.f;
 }
 
-// Gamma, Q<-, K<-, K-> of one chunk with row stride SK: all threads load the raw
+// Gamma, Q<-, K<-, K-> of the chunk starting at row `row` of its batch, with row stride
+// SK: all threads load the raw
 // tiles, then one thread per key channel runs the in-chunk cumsum of g down
 // its column in shared memory (rows past nvalid are zero, Gamma held at its
 // last value); gam[d] = gamma^C.  Gm and Ql may be null (the raw g then waits
 // in Kr); gsc holds C floats (scalar gates).  Contains one barrier; the
 // caller synchronises before reading the tiles.
 template <int DK, int SK, typename Tin, typename Tg, int NT = kThreads>
-__device__ void load_rescaled_par(const BwdParams &p, int b, int h, int t0, int nvalid, float *Gm, float *Ql,
+__device__ void load_rescaled_par(const BwdParams &p, size_t row, int h, int nvalid, float *Gm, float *Ql,
                                   float *Kl, float *Kr, float *gam, float *gsc) {
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tg *g = static_cast<const Tg *>(p.g);
     const int tid = threadIdx.x;
     float *graw = Gm ? Gm : Kr;
-    const size_t r0 = (((size_t)b * p.T + t0) * p.H + h) * DK, rs = (size_t)p.H * DK;
+    const size_t r0 = (row * p.H + h) * DK, rs = (size_t)p.H * DK;
     wg::load_tile<kC, DK, SK, NT>(k + r0, rs, nvalid, Kl);
     if (Ql) wg::load_tile<kC, DK, SK, NT>(q + r0, rs, nvalid, Ql);
     if (p.gate_kind == KDA_GATE_CHANNEL) wg::load_tile<kC, DK, SK, NT>(g + r0, rs, nvalid, graw);
     if (p.gate_kind == KDA_GATE_SCALAR && tid < kC)
-        gsc[tid] = tid < nvalid ? ld(g, ((size_t)b * p.T + t0 + tid) * p.H + h) : 0.f;
+        gsc[tid] = tid < nvalid ? ld(g, (row + tid) * p.H + h) : 0.f;
     __syncthreads();
     if (tid < DK) {
         const int d = tid;
@@ -163,7 +180,7 @@ struct Rec {
 };
 
 // ------------------------------------------------------------------ prep kernel
-// One CTA per (chunk, head, batch).
+// One CTA per (chunk, head, sequence).
 template <int DK, int DV, typename Tin, typename Tg, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_prep_kernel(const BwdParams p) {
     constexpr int SK = pad4(DK), SV = pad4(DV), SC = kSC4;
@@ -181,17 +198,20 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_prep_kernel(const BwdParams 
     float *gsc = beta + kC;            // [C]
     float *gam = gsc + kC;             // [DK]
 
-    const int tid = threadIdx.x;
-    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
-    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const int tid = threadIdx.x, h = blockIdx.y;
+    int b, n;
+    Seq sq;
+    if (!chunk_of(p, b, n, sq)) return;
+    const int H = p.H;
+    const int t0 = n * kC, nvalid = min(kC, sq.len - t0);
+    const size_t row = (size_t)sq.row0 + t0;
     const Tin *v = static_cast<const Tin *>(p.v);
-    float *rec = p.ws_prep + (((size_t)b * H + h) * N + n) * rec_floats(DK, DV);
+    float *rec = p.ws_prep + chunk_index(p, sq, h, n) * rec_floats(DK, DV);
     const bool sv = p.scale_v != 0;
 
-    load_beta<Tin>(p, b, h, t0, nvalid, beta);
-    wg::load_tile<kC, DV, SV, kThreads>(v + (((size_t)b * T + t0) * H + h) * DV, (size_t)H * DV, nvalid, Vm);
-    load_rescaled_par<DK, SK, Tin, Tg>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, gsc);
+    load_beta<Tin>(p, row, h, nvalid, beta);
+    wg::load_tile<kC, DV, SV, kThreads>(v + (row * H + h) * DV, (size_t)H * DV, nvalid, Vm);
+    load_rescaled_par<DK, SK, Tin, Tg>(p, row, h, nvalid, Gm, Ql, Kl, Kr, gam, gsc);
     __syncthreads();
     {
         auto bKr = [&](int d, int j) { return Kr[j * SK + d]; };
@@ -228,7 +248,7 @@ constexpr size_t prep_smem_bytes() {
 
 // ------------------------------------------------------------------ kernel A
 // The forward state scan from the chunk records: V_new = U - W S^T,
-// S <- S Diag(gamma^C) + V_new^T K~.  One CTA per (32-wide value slice, head, batch).
+// S <- S Diag(gamma^C) + V_new^T K~.  One CTA per (32-wide value slice, head, sequence).
 // The records of chunk n + 1 travel (cp.async, double buffer) while chunk n computes.
 template <int DK>
 __host__ __device__ constexpr int states_buf_floats() {
@@ -244,10 +264,13 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, dv = p.dv, N = (T + kC - 1) / kC;
+    const int H = p.H, dv = p.dv;
+    const Seq sq = seq_of(p, b);
+    const int N = sq.nch;
     const size_t head = (size_t)b * H + h;
-    float *Sws = p.ws_S + head * (size_t)(N + 1) * dv * DK;
-    const float *recs = p.ws_prep + head * N * rec_floats(DK, DV);
+    float *Sws = p.ws_S + state_index(p, sq, b, h, 0) * dv * DK;
+    const float *recs = p.ws_prep + chunk_index(p, sq, h, 0) * rec_floats(DK, DV);
+    float *vnew = p.ws_vnew + chunk_index(p, sq, h, 0) * kC * dv;
     auto issue = [&](int n) {
         const float *rec = recs + (size_t)n * rec_floats(DK, DV);
         float *bf = bufs + (n & 1) * BUF;
@@ -274,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
         wg::cp_async_commit();         // (an empty group on the last chunk keeps the count)
         wg::cp_async_wait<1>();        // chunk n's tiles have landed (this thread's copies)
         __syncthreads();               // ... and everyone's
-        float *vn = p.ws_vnew + ((head * N + n) * kC) * (size_t)dv + e0;     // V_new rows of this chunk
+        float *vn = vnew + (size_t)n * kC * dv + e0;     // V_new rows of this chunk
         wg::gemm<kDVS, TF32>(
             DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
             [&](int i, int e, float x) {
@@ -313,18 +336,21 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, dv = p.dv, N = (T + kC - 1) / kC;
+    const int H = p.H, dv = p.dv;
+    const Seq sq = seq_of(p, b);
+    const int N = sq.nch;
     const Tin *dop = static_cast<const Tin *>(p.grad_o);
     const size_t head = (size_t)b * H + h;
-    float *dSws = p.ws_dS + head * (size_t)N * dv * DK;
-    const float *recs = p.ws_prep + head * N * rec_floats(DK, DV);
+    float *dSws = p.ws_dS + chunk_index(p, sq, h, 0) * dv * DK;
+    const float *recs = p.ws_prep + chunk_index(p, sq, h, 0) * rec_floats(DK, DV);
+    float *dus = p.ws_du + chunk_index(p, sq, h, 0) * kC * dv;
 
     for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         dS[e * SK + d] = p.grad_ht ? p.grad_ht[(head * dv + e0 + e) * DK + d] : 0.f;
     }
     for (int n = N - 1; n >= 0; --n) {
-        const int t0 = n * kC, nvalid = min(kC, T - t0);
+        const int t0 = n * kC, nvalid = min(kC, sq.len - t0);
         const float *rec = recs + (size_t)n * rec_floats(DK, DV);
         __syncthreads();
         for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
@@ -335,11 +361,11 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
         wg::load_tile<kC, DK, SK, kThreads>(rec + R::QL, DK, kC, QL);
         wg::load_tile<kC, DK, SK, kThreads>(rec + R::KT, DK, kC, KT);
         wg::load_tile<kC, kC, SC, kThreads>(rec + R::P, kC, kC, Pm);
-        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)b * T + t0) * H + h) * dv + e0, (size_t)H * dv,
+        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)sq.row0 + t0) * H + h) * dv + e0, (size_t)H * dv,
                                               nvalid, dO);
         for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
         __syncthreads();
-        float *du = p.ws_du + ((head * N + n) * kC) * (size_t)dv + e0;       // dU rows of this chunk
+        float *du = dus + (size_t)n * kC * dv + e0;       // dU rows of this chunk
         wg::gemm2<kDVS, TF32>(
             DK, [&](int i, int d) { return KT[i * SK + d]; }, [&](int d, int e) { return dS[e * SK + d]; }, kC,
             [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
@@ -397,16 +423,19 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
     float *gam = dbeta + kC;           // [DK]
     float *lastrow = gam + DK;         // [DK] diag(S_next^T dS)
 
-    const int tid = threadIdx.x;
-    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int T = p.T, H = p.H, N = (T + kC - 1) / kC;
-    const int t0 = n * kC, nvalid = min(kC, T - t0);
+    const int tid = threadIdx.x, h = blockIdx.y;
+    int b, n;
+    Seq sq;
+    if (!chunk_of(p, b, n, sq)) return;
+    const int H = p.H;
+    const int t0 = n * kC, nvalid = min(kC, sq.len - t0);
+    const size_t row = (size_t)sq.row0 + t0;
     const Tin *v = static_cast<const Tin *>(p.v);
     const Tin *dop = static_cast<const Tin *>(p.grad_o);
-    const size_t head = (size_t)b * H + h;
-    const float *Sp = p.ws_S + (head * (N + 1) + n) * (size_t)DV * DK;      // state before the chunk
+    const size_t ci = chunk_index(p, sq, h, n);
+    const float *Sp = p.ws_S + state_index(p, sq, b, h, n) * DV * DK;     // state before the chunk
     const float *Sn = Sp + (size_t)DV * DK;                                 // state after the chunk
-    const float *dS = p.ws_dS + (head * N + n) * (size_t)DV * DK;           // gradient of the state after
+    const float *dS = p.ws_dS + ci * DV * DK;                               // gradient of the state after
     const bool sv = p.scale_v != 0;
 
     // The stored states stream through a ring of four tile buffers that are free until the
@@ -429,10 +458,10 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
     issue_upto(4);
 
     // ---- loads: Gamma and the rescaled tiles, v, dO, beta
-    load_rescaled_par<DK, SK, Tin, Tg, kThreadsC>(p, b, h, t0, nvalid, Gm, Ql, Kl, Kr, gam, dbeta);
-    load_beta<Tin>(p, b, h, t0, nvalid, beta);
+    load_rescaled_par<DK, SK, Tin, Tg, kThreadsC>(p, row, h, nvalid, Gm, Ql, Kl, Kr, gam, dbeta);
+    load_beta<Tin>(p, row, h, nvalid, beta);
     {
-        const size_t r0 = (((size_t)b * T + t0) * H + h) * DV, rs = (size_t)H * DV;
+        const size_t r0 = (row * H + h) * DV, rs = (size_t)H * DV;
         wg::load_tile<kC, DV, SV, kThreadsC>(v + r0, rs, nvalid, Vm);
         wg::load_tile<kC, DV, SV, kThreadsC>(dop + r0, rs, nvalid, dO);
     }
@@ -440,13 +469,13 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
     // ---- A~, P and N from the chunk record
     {
         using R = Rec<DK, DV>;
-        const float *rec = p.ws_prep + (head * N + n) * rec_floats(DK, DV);
+        const float *rec = p.ws_prep + ci * rec_floats(DK, DV);
         wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::A, kC, kC, Am);
         wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::P, kC, kC, Pm);
         wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::N, kC, kC, Nm);
         // V_new and dU of this chunk, from the two scans
-        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_vnew + (head * N + n) * (size_t)kC * DV, DV, kC, Vn);
-        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_du + (head * N + n) * (size_t)kC * DV, DV, kC, dU);
+        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_vnew + ci * kC * DV, DV, kC, Vn);
+        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_du + ci * kC * DV, DV, kC, dU);
     }
     __syncthreads();
     // ---- dO V_new^T * M (into Pm)
@@ -563,7 +592,7 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
     for (int idx = tid; idx < kC * DK; idx += kThreadsC) {
         const int i = idx / DK, d = idx % DK;
         if (i < nvalid) {
-            const size_t off = (((size_t)b * T + t0 + i) * H + h) * DK + d;
+            const size_t off = ((row + i) * H + h) * DK + d;
             const float gm = Gm[i * SK + d];
             st(gq, off, dQl[i * SK + d] * gm);
             st(gk, off, dKl[i * SK + d] * gm + dKr[i * SK + d] / gm);
@@ -572,10 +601,10 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
     for (int idx = tid; idx < kC * DV; idx += kThreadsC) {
         const int i = idx / DV, e = idx % DV;
         if (i < nvalid)
-            st(gv, (((size_t)b * T + t0 + i) * H + h) * DV + e, (sv ? beta[i] : 1.f) * Vn[i * SV + e]);
+            st(gv, ((row + i) * H + h) * DV + e, (sv ? beta[i] : 1.f) * Vn[i * SV + e]);
     }
     if (p.has_beta && tid < nvalid)
-        st(static_cast<Tin *>(p.grad_beta), ((size_t)b * T + t0 + tid) * H + h, dbeta[tid]);
+        st(static_cast<Tin *>(p.grad_beta), (row + tid) * H + h, dbeta[tid]);
     if (p.gate_kind != KDA_GATE_NONE) {
         // diag(S_next^T dS) for the gamma^C row, then suffix sums down each channel
         Tg *gg = static_cast<Tg *>(p.grad_g);
@@ -586,7 +615,7 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
                 for (int i = kC - 1; i >= 0; --i) {
                     run += dQl[i * SK + d] * Ql[i * SK + d] + dKl[i * SK + d] * Kl[i * SK + d] -
                            dKr[i * SK + d] * Kr[i * SK + d];
-                    if (i < nvalid) st(gg, (((size_t)b * T + t0 + i) * H + h) * DK + d, run);
+                    if (i < nvalid) st(gg, ((row + i) * H + h) * DK + d, run);
                 }
             }
         } else {
@@ -609,7 +638,7 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
                 for (int d = 0; d < DK; ++d) run += acc_last[d];
                 for (int i = kC - 1; i >= 0; --i) {
                     run += rowsum[i];
-                    if (i < nvalid) st(gg, ((size_t)b * T + t0 + i) * H + h, run);
+                    if (i < nvalid) st(gg, (row + i) * H + h, run);
                 }
             }
         }
@@ -633,7 +662,7 @@ cudaError_t set_smem(F *fn, size_t bytes) {
 template <int DK, int DV, typename Tin, typename Tg>
 cudaError_t launch_all(const BwdParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
-    const int N = (p.T + kC - 1) / kC;
+    const bool packed = p.cu_seqlens != nullptr;
     cudaError_t e;
     const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
@@ -642,7 +671,7 @@ cudaError_t launch_all(const BwdParams &p, cudaStream_t s) {
     if ((e = set_smem(kda_bwd_states_kernel<DK, DV, kTf32>, sa)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_dstate_kernel<DK, DV, Tin, kTf32>, sb)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
-    const dim3 gscan(p.dv / kDVS, p.H, p.B), gchunk(N, p.H, p.B);
+    const dim3 gscan(p.dv / kDVS, p.H, p.B), gchunk = seq::chunk_grid<kC>(p.B, p.T, p.H, packed);
     kda_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sp, s>>>(p);
     kda_bwd_states_kernel<DK, DV, kTf32><<<gscan, kThreads, sa, s>>>(p);
     kda_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sb, s>>>(p);
@@ -661,9 +690,18 @@ cudaError_t launch_typed(const BwdParams &p, cudaStream_t s) {
 
 }  // namespace
 
-size_t bwd_state_bytes(int B, int T, int H, int dk, int dv) {
-    const size_t N = (T + kC - 1) / kC;
-    return sizeof(float) * (size_t)B * H * ((2 * N + 1) * dv * dk + N * rec_floats(dk, dv) + 2 * N * kC * dv);
+size_t bwd_state_bytes(int B, int T, int H, int dk, int dv, bool packed) {
+    const size_t NS = chunk_slots(B, T, packed);
+    return sizeof(float) * (size_t)H * ((2 * NS + B) * dv * dk + NS * rec_floats(dk, dv) + 2 * NS * kC * dv);
+}
+
+void bwd_carve(BwdParams &p, float *ws) {
+    const size_t NS = chunk_slots(p.B, p.T, p.cu_seqlens != nullptr), H = p.H, st = (size_t)p.dv * p.dk;
+    p.ws_S = ws;                                     // [H][NS + B state slots][dv][dk]
+    p.ws_dS = p.ws_S + H * (NS + p.B) * st;          // [H][NS][dv][dk]
+    p.ws_prep = p.ws_dS + H * NS * st;               // [H][NS] records
+    p.ws_vnew = p.ws_prep + H * NS * rec_floats(p.dk, p.dv);
+    p.ws_du = p.ws_vnew + H * NS * kC * p.dv;        // [H][NS][C][dv] each
 }
 
 cudaError_t launch_bwd_simt(const BwdParams &p, int in_bf16, int g_is_bf16, cudaStream_t s) {

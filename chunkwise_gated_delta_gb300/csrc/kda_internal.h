@@ -38,11 +38,14 @@ struct DplrParams {
     const float *grad_ht;
     void *grad_q, *grad_k, *grad_v, *grad_a, *grad_b, *grad_g;
     float *grad_h0;
-    float *ws_S;            // [B, H, N + 1, dv, dk] states before each chunk, then the final state
-    float *ws_dS;           // [B, H, N, dv, dk] gradients of the state after each chunk
-    float *ws_prep;         // [B, H, N] chunk records (state-independent operands)
-    float *ws_x;            // backward: [B, H, N, C, dv] X of every chunk
-    float *ws_dc;           // backward: [B, H, N, C, dv] dC of every chunk
+    // workspace arrays, by head, then chunk slot: NS = B ceil(T / C) slots for dense
+    // batches, B + ceil(T / C) for packed sequences (dplr_bwd_carve)
+    float *ws_S;            // [H, NS + B, dv, dk] states before each chunk, then the final state
+    float *ws_dS;           // [H, NS, dv, dk] gradients of the state after each chunk
+    float *ws_prep;         // [H, NS] chunk records (state-independent operands)
+    float *ws_x;            // backward: [H, NS, C, dv] X of every chunk
+    float *ws_dc;           // backward: [H, NS, C, dv] dC of every chunk
+    const int *cu_seqlens;  // packed sequences: [B + 1] row offsets into a [1, T, H, d] batch, or null
 };
 
 // Device-side copy of the validated backward arguments.
@@ -57,12 +60,15 @@ struct BwdParams {
     const float *grad_ht;   // [B, H, dv, dk] or null
     void *grad_q, *grad_k, *grad_v, *grad_g, *grad_beta;
     float *grad_h0;
-    float *ws_S;            // [B, H, N + 1, dv, dk] states before each chunk, then the final state
-    float *ws_dS;           // [B, H, N, dv, dk] gradients of the state after each chunk
-    float *ws_prep;         // [B, H, N] chunk records (state-independent operands)
-    float *ws_vnew;         // [B, H, N, C, dv] V_new of every chunk
-    float *ws_du;           // [B, H, N, C, dv] dU of every chunk
+    // workspace arrays, by head, then chunk slot (bwd_carve): NS = B ceil(T / 32) slots for
+    // dense batches, B + ceil(T / 32) for packed sequences
+    float *ws_S;            // [H, NS + B, dv, dk] states before each chunk, then the final state
+    float *ws_dS;           // [H, NS, dv, dk] gradients of the state after each chunk
+    float *ws_prep;         // [H, NS] chunk records (state-independent operands)
+    float *ws_vnew;         // [H, NS, C, dv] V_new of every chunk
+    float *ws_du;           // [H, NS, C, dv] dU of every chunk
     int *status;
+    const int *cu_seqlens;  // packed sequences: [B + 1] row offsets into a [1, T, H, d] batch, or null
 };
 
 // Device status codes written into the workspace word (first error wins).
@@ -81,19 +87,23 @@ size_t fwd_zrec_bytes(int B, int T, int H, bool packed);
 
 // float32 CUDA-core DPLR chunk forward (inputs float32 or bf16) and the bytes
 // of chunk records it keeps in the workspace.
-size_t dplr_fwd_record_bytes(int B, int T, int H, int dk, int dv);
+size_t dplr_fwd_record_bytes(int B, int T, int H, int dk, int dv, bool packed);
 cudaError_t launch_dplr_fwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s);
 
-// float32 CUDA-core DPLR backward (inputs float32 or bf16) and its workspace bytes.
+// float32 CUDA-core DPLR backward (inputs float32 or bf16), its workspace bytes and the
+// carving of those bytes (at ws, 16-byte aligned) into p's ws_* arrays.
 cudaError_t launch_dplr_bwd_simt(const DplrParams &p, int in_bf16, int g_is_bf16, cudaStream_t s);
-size_t dplr_bwd_state_bytes(int B, int T, int H, int dk, int dv);
+size_t dplr_bwd_state_bytes(int B, int T, int H, int dk, int dv, bool packed);
+void dplr_bwd_carve(DplrParams &p, float *ws);
 
 // Per-token transition norms; maxes (2 floats) is cleared on the stream first.
 cudaError_t launch_dplr_factor_norms(const DplrParams &p, int in_bf16, int g_is_bf16, float *rho, float *nrm,
                                      float *maxes, cudaStream_t s);
 
-// Backward: bytes of chunk states the three kernels keep in the workspace.
-size_t bwd_state_bytes(int B, int T, int H, int dk, int dv);
+// Backward: bytes of chunk states, records and chunk products the kernels keep in the
+// workspace, and the carving of those bytes (at ws, 16-byte aligned) into p's ws_* arrays.
+size_t bwd_state_bytes(int B, int T, int H, int dk, int dv, bool packed);
+void bwd_carve(BwdParams &p, float *ws);
 
 // float32 CUDA-core backward (inputs float32 or bf16).
 cudaError_t launch_bwd_simt(const BwdParams &p, int in_bf16, int g_is_bf16, cudaStream_t s);

@@ -223,15 +223,23 @@ typedef struct {
     void *workspace;       /* device buffer of kda_chunk_bwd_workspace bytes; its first 256
                               bytes zero-filled before the first use */
     size_t workspace_bytes;
+    /*
+     * Packed variable-length batches, or NULL: as in kda_fwd_args (B sequences back
+     * to back in [1, T, H, d] tensors -- q, k, v, g, beta, grad_o and the gradients of
+     * those -- h0, grad_ht and grad_h0 one [H, dv, dk] state per sequence, a DEVICE
+     * array of B + 1 int32 offsets, clamped into [0, T] by the kernels).  Gradients
+     * do not cross a sequence boundary; an empty sequence's grad_h0 is its grad_ht.
+     */
+    const int32_t *cu_seqlens;
 } kda_bwd_args;
 
 /*
  * Bytes of workspace kda_chunk_bwd needs (0 on bad args): 256 for the status
- * word, the float32 chunk states and state gradients,
- * (2 N + 1) B H dv dk 4 bytes with N = ceil(T/32), and one float32 record of
- * state-independent chunk operands per chunk,
- * N B H (3 32 32 + 3 32 dk + 32 dv + dk) 4 bytes, and the chunk products
- * V_new and dU, 2 N B H 32 dv 4 bytes.
+ * word, then, with NS chunk slots per head (B ceil(T/32); B + ceil(T/32) with
+ * cu_seqlens), the float32 chunk states and state gradients,
+ * (2 NS + B) H dv dk 4 bytes, one float32 record of state-independent chunk
+ * operands per slot, NS H (3 32 32 + 3 32 dk + 32 dv + dk) 4 bytes, and the
+ * chunk products V_new and dU, 2 NS H 32 dv 4 bytes.
  */
 size_t kda_chunk_bwd_workspace(const kda_bwd_args *args);
 
@@ -287,12 +295,17 @@ typedef struct {
     float *ht;             /* [B, H, dv, dk] final state, or NULL (not written) */
     void *workspace;       /* device buffer, zero-filled before its first use */
     size_t workspace_bytes;
+    /* Packed variable-length batches, or NULL: as in kda_fwd_args (q, k, v, a, b, g and o
+       [1, T, H, d]; h0 / ht one state per sequence; B + 1 int32 device offsets).
+       dplr_factor_norms reads it only to count the T H tokens of the packed batch. */
+    const int32_t *cu_seqlens;
 } dplr_fwd_args;
 
 /*
  * Bytes of workspace dplr_chunk_fwd needs for these arguments (0 on bad args):
  * 256 for the status word plus one float32 record of state-independent chunk
- * operands per 32-token chunk, ceil(T/32) B H (4 32 dk + 2 32 dv + dk) 4 bytes.
+ * operands per 32-token chunk slot, NS H (4 32 dk + 2 32 dv + dk) 4 bytes with
+ * NS = B ceil(T/32) (B + ceil(T/32) with cu_seqlens).
  */
 size_t dplr_chunk_fwd_workspace(const dplr_fwd_args *args);
 
@@ -352,14 +365,16 @@ typedef struct {
     float *grad_h0;        /* [B, H, dv, dk] out, or NULL */
     void *workspace;       /* dplr_chunk_bwd_workspace bytes; first 256 zero-filled before first use */
     size_t workspace_bytes;
+    /* Packed variable-length batches, or NULL: as in kda_bwd_args. */
+    const int32_t *cu_seqlens;
 } dplr_bwd_args;
 
 /*
- * Workspace bytes for dplr_chunk_bwd (0 on bad args): 256, the float32 chunk
- * states and state gradients (2 N + 1) B H dv dk 4 with N = ceil(T/16), one
- * record of state-independent chunk operands per chunk,
- * N B H (4 16 dk + 16 dv + 4 16 16 + dk) 4, and the chunk products X and dC,
- * 2 N B H 16 dv 4.
+ * Workspace bytes for dplr_chunk_bwd (0 on bad args): 256, then, with NS chunk
+ * slots per head (B ceil(T/16); B + ceil(T/16) with cu_seqlens), the float32
+ * chunk states and state gradients (2 NS + B) H dv dk 4, one record of
+ * state-independent chunk operands per slot, NS H (4 16 dk + 16 dv + 4 16 16 + dk) 4,
+ * and the chunk products X and dC, 2 NS H 16 dv 4.
  */
 size_t dplr_chunk_bwd_workspace(const dplr_bwd_args *args);
 

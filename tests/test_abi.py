@@ -173,6 +173,19 @@ def test_bwd_workspace_query(lib):
     assert lib.kda_chunk_bwd_workspace(None) == 0
 
 
+def test_bwd_workspace_query_packed(lib):
+    """Packed sequences: B + ceil(T / 32) chunk slots per head, and one more state slot per sequence."""
+    cu = (1 << 40) + 20 * (1 << 32)
+    need = lib.kda_chunk_bwd_workspace(ctypes.byref(_bwd_args(B=5, cu_seqlens=cu)))
+    slots = 5 + (100 + 31) // 32
+    record = 3 * 32 * 32 + 3 * 32 * 128 + 32 * 128 + 128
+    assert need == 256 + 4 * 4 * ((2 * slots + 5) * 128 * 128 + slots * record + 2 * slots * 32 * 128)
+    # a misaligned offsets array, and one that overlaps an output
+    assert lib.kda_chunk_bwd(ctypes.byref(_bwd_args(cu_seqlens=cu + 2)), None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_bwd(ctypes.byref(_bwd_args(cu_seqlens=(1 << 40) + 8 * (1 << 32))), None) == \
+        _lib.KDA_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("over,code", [
     (dict(grad_o=None), _lib.KDA_ERR_INVALID_ARG),
     (dict(grad_q=None), _lib.KDA_ERR_INVALID_ARG),
@@ -214,6 +227,19 @@ def test_dplr_bwd_workspace_query(lib):
     record = 4 * 16 * 128 + 16 * 128 + 4 * 16 * 16 + 128
     assert need == 256 + 4 * 2 * 4 * ((2 * n_chunks + 1) * 128 * 128 + n_chunks * record + 2 * n_chunks * 16 * 128)
     assert lib.dplr_chunk_bwd_workspace(ctypes.byref(_dplr_bwd_args(dv=32))) == 0
+
+
+def test_dplr_workspace_queries_packed(lib):
+    """Packed sequences: B + ceil(T / C) chunk slots per head (C = 32 forward, 16 backward)."""
+    cu = (1 << 40) + 30 * (1 << 32)
+    fwd = lib.dplr_chunk_fwd_workspace(ctypes.byref(_dplr_args(B=5, cu_seqlens=cu)))
+    assert fwd == 256 + 4 * 4 * (5 + (100 + 31) // 32) * (4 * 32 * 128 + 2 * 32 * 128 + 128)
+    need = lib.dplr_chunk_bwd_workspace(ctypes.byref(_dplr_bwd_args(B=5, cu_seqlens=cu)))
+    slots = 5 + (100 + 15) // 16
+    record = 4 * 16 * 128 + 16 * 128 + 4 * 16 * 16 + 128
+    assert need == 256 + 4 * 4 * ((2 * slots + 5) * 128 * 128 + slots * record + 2 * slots * 16 * 128)
+    assert lib.dplr_chunk_bwd(ctypes.byref(_dplr_bwd_args(cu_seqlens=cu + 2)), None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.dplr_chunk_fwd(ctypes.byref(_dplr_args(cu_seqlens=cu + 2)), None) == _lib.KDA_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("over,code", [

@@ -124,3 +124,64 @@ def test_full_kda_bwd_b4t4096h16d128_every_head():
                 worst[k] = max(worst.get(k, 0.0), e)
     print("parity: kda_bwd_bf16_b4t4096h16d128 worst head per gradient:",
           {k: f"{e:.3e}" for k, e in worst.items()})
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+def _packed_bwd(variant, dtype, lens, dk, dv, seed=20):
+    """Sequences of the given lengths packed into one [1, T, H, d] batch: the packed backward
+    against the oracle's backward of each sequence on its own (an empty sequence's dh0 is its dht)."""
+    H = 2
+    parts = [make_inputs(custom(variant, 1, max(n, 1), H, dk, dv, dtype=dtype, h0=True, grads=True),
+                         seed=seed + i) for i, n in enumerate(lens)]
+    rows = ("q", "k", "v", "g", "beta", "do")
+    x = {name: torch.cat([p_[name][:, :n] for p_, n in zip(parts, lens)], 1).contiguous()
+         for name in rows if name in parts[0]}
+    for name in ("h0", "dht"):
+        x[name] = torch.cat([p_[name] for p_ in parts], 0).contiguous()
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=DEV)
+    d = {k_: v_.to(DEV) for k_, v_ in x.items()}
+    out = kda_chunk_bwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d["h0"], d["do"], d["dht"],
+                        gate=GATE[variant], scale_v=parts[0]["scale_v"], cu_seqlens=cu)
+    torch.cuda.synchronize()
+    got = {k_: v_.double().cpu().numpy() for k_, v_ in out.items()}
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    worst = {}
+    for i, (p_, n) in enumerate(zip(parts, lens)):
+        if n == 0:
+            assert rel(got["dh0"][i], f64(p_["dht"])[0]) <= 1e-6, i
+            continue
+        sub = {name: (p_[name][:, :n] if name in rows else p_[name]) for name in p_ if name != "scale_v"}
+        sub["scale_v"] = p_["scale_v"]
+        ref = run_oracle(sub, variant)
+        mine = {k_: (v_[i:i + 1] if k_ == "dh0" else v_[:, starts[i]:starts[i + 1]]) for k_, v_ in got.items()}
+        for k_, e in compare(mine, ref, TOL[dtype]).items():
+            worst[k_] = max(worst.get(k_, 0.0), e)
+    return worst
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.float32, 64, 64), (torch.bfloat16, 128, 128),
+                                         (torch.bfloat16, 128, 64)])
+def test_packed_kda_bwd(dtype, dk, dv):
+    """cu_seqlens: ragged lengths below, at and above a 32-token chunk, an empty sequence and a
+    one-token one; no gradient crosses a boundary."""
+    _packed_bwd("kda", dtype, [100, 32, 0, 1, 193, 37], dk, dv)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "gla"])
+def test_packed_special_cases_bwd(variant):
+    _packed_bwd(variant, torch.bfloat16, [70, 0, 130, 33], 128, 128)
+
+
+def test_packed_bwd_equals_dense_on_equal_lengths():
+    """Equal lengths packed with cu_seqlens give the same gradients as the dense [B, T] batch
+    (bit for bit: the same chunks, products and sums in the same order)."""
+    x = make_inputs(custom("kda", 3, 96, 2, 128, 128, dtype=torch.bfloat16, h0=True, grads=True), seed=23)
+    d = {k_: (v_.to(DEV) if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    dense = kda_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], d["do"], d["dht"], gate="channel")
+    flat = {k_: d[k_].reshape(1, -1, *d[k_].shape[2:]).contiguous() for k_ in ("q", "k", "v", "g", "beta", "do")}
+    cu = torch.tensor([0, 96, 192, 288], dtype=torch.int32, device=DEV)
+    packed = kda_chunk_bwd(flat["q"], flat["k"], flat["v"], flat["g"], flat["beta"], d["h0"], flat["do"],
+                           d["dht"], gate="channel", cu_seqlens=cu)
+    torch.cuda.synchronize()
+    for key, t in dense.items():
+        assert torch.equal(packed[key].reshape(t.shape), t), key

@@ -158,3 +158,32 @@ def test_full_dplr_bwd_b2t8192h16d128_every_head():
                 worst[k] = max(worst.get(k, 0.0), e)
     print("parity: dplr_bwd_bf16_b2t8192h16d128 worst head per gradient:",
           {k: f"{e:.3e}" for k, e in worst.items()})
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+@pytest.mark.parametrize("dtype,clip", [(torch.float32, False), (torch.float32, True), (torch.bfloat16, False)])
+def test_packed_sequences(dtype, clip):
+    """cu_seqlens: ragged lengths below, at and above a 16-token chunk, an empty sequence and a
+    one-token one, against the oracle's backward of each sequence alone (an empty sequence's dh0
+    is its dht)."""
+    lens, H, dk, dv = [40, 16, 0, 1, 70, 17], 2, 128, 64
+    parts = [_inputs(dtype, 1, max(n, 1), H, dk, dv, seed=40 + i, eta_scale=1.5 if clip else 1.0)
+             for i, n in enumerate(lens)]
+    rows = ("q", "k", "v", "a", "b", "g", "do")
+    x = {name: torch.cat([p_[name][:, :n] for p_, n in zip(parts, lens)], 1).contiguous() for name in rows}
+    for name in ("h0", "dht"):
+        x[name] = torch.cat([p_[name] for p_ in parts], 0).contiguous()
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=DEV)
+    d = {k: v.to(DEV) for k, v in x.items()}
+    out = dplr_chunk_bwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["g"], d["h0"], d["do"], d["dht"],
+                         gate="channel", clip=clip, cu_seqlens=cu)
+    torch.cuda.synchronize()
+    got = {k: v.double().cpu().numpy() for k, v in out.items()}
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    for i, (p_, n) in enumerate(zip(parts, lens)):
+        if n == 0:
+            assert rel(got["dh0"][i], f64(p_["dht"])[0]) <= 1e-6, i
+            continue
+        sub = {name: (p_[name][:, :n] if name in rows else p_[name]) for name in p_}
+        mine = {k: (v[i:i + 1] if k == "dh0" else v[:, starts[i]:starts[i + 1]]) for k, v in got.items()}
+        compare(mine, oracle_bwd(sub, clip), TOL[dtype])

@@ -186,3 +186,30 @@ def test_factor_norms_full_workload():
     sample = [(rng.integers(2), rng.integers(8192), rng.integers(16)) for _ in range(32)]
     rho, nrm, mx = _check_norms(x, sample)
     assert mx[0] > 1.0 and mx[1] > 1.0
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.float32, 64, 64), (torch.bfloat16, 128, 128)])
+def test_packed_sequences(dtype, dk, dv):
+    """cu_seqlens: ragged lengths below, at and above a 32-token chunk, an empty sequence and a
+    one-token one, against the oracle on each sequence alone; no state crosses a boundary."""
+    lens, H = [100, 32, 0, 1, 193, 37], 2
+    parts = [make_inputs(custom("dplr", 1, max(n, 1), H, dk, dv, dtype=dtype, h0=True), seed=30 + i)
+             for i, n in enumerate(lens)]
+    rows = ("q", "k", "v", "a", "b", "g")
+    x = {name: torch.cat([p_[name][:, :n] for p_, n in zip(parts, lens)], 1).contiguous() for name in rows}
+    x["h0"] = torch.cat([p_["h0"] for p_ in parts], 0).contiguous()
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=DEV)
+    d = {k: v.to(DEV) for k, v in x.items()}
+    o, ht = dplr_chunk_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["g"], d["h0"], cu_seqlens=cu)
+    torch.cuda.synchronize()
+    o, ht = o.double().cpu().numpy(), ht.double().cpu().numpy()
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    for i, (p_, n) in enumerate(zip(parts, lens)):
+        if n == 0:
+            assert np.array_equal(ht[i], f64(p_["h0"])[0]), i
+            continue
+        ro, rh = run_oracle({name: (p_[name][:, :n] if name in rows else p_[name]) for name in p_})
+        assert rel(o[:, starts[i]:starts[i + 1]], ro) <= TOL[dtype], i
+        assert rel(ht[i], rh[0]) <= TOL[dtype], i
+
