@@ -371,7 +371,9 @@ def run_ours(args, rank, world, local):
     form = None
     if kind_of(w) in ("kda", "gdn", "deltanet", "gla"):
         form = forward_form(w, d, o, ht, gate, x["scale_v"])
-        launches = 1 if form == "single" else 2
+        # single: the kernel, then (gated variants) the launch that redoes a call whose decay
+        # passed the one-product Gram's range and otherwise exits at once; records: Z + scan
+        launches = (1 if gate == "none" else 2) if form == "single" else 2
 
     for _ in range(max(3, args.warmup)):
         step()

@@ -2,6 +2,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kda.h"
 #include "kda_internal.h"
 
@@ -280,6 +282,12 @@ kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream) {
     p.h0 = args->h0; p.o = args->o; p.ht = args->ht;
     p.status = static_cast<int *>(args->workspace);
     p.cu_seqlens = args->cu_seqlens;
+    {
+        static std::atomic<unsigned> calls{0};
+        unsigned t = ++calls;
+        if ((int)t == 0) t = ++calls;                // never 0, the status block's initial value
+        p.strong_token = (int)t;
+    }
     if (const size_t zbytes = fwd_record_bytes(args)) {
         // the full workspace holds the chunk records of the two-kernel form; the status word
         // alone selects the single-kernel form
@@ -428,7 +436,7 @@ const char *kda_status_string(kda_status status) {
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "device-side wait timed out";
-    case KDA_ERR_RANGE: return "in-chunk log-decay outside the range of the bf16 path";
+    case KDA_ERR_RANGE: return "log-decay outside the range of a kernel";
     }
     return "unknown status";
 }

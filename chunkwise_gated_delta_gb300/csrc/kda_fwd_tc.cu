@@ -5,7 +5,9 @@
 // backward" ("forward recap"), regrouped so every tensor-core product has
 // M = 128 rows:
 //
-//   [beta K<- ; Q<-] K->^T      = [L ; P]          (Gram, one MMA)
+//   [beta K<- ; Q<-] K->^T      = [L ; P]          (Gram, one MMA; a chunk whose decay
+//                                                    K-> cannot represent takes the sub-chunk
+//                                                    form of "Gated Linear Attention" 5.3)
 //   Z' (I + L_{strict}) = [I ; P],  Z = Z' Diag(beta) = [T ; P T]
 //        with T = (I + L)^{-1} Diag(beta): block back-substitution over
 //        16-column blocks (page "DeltaNet" 4.2, block form 2), the 16x16
@@ -14,20 +16,23 @@
 //   Z K<-                       = [W ; P W]
 //   Z V                         = [U ; P U]        (into the accumulator D1)
 //   D1 += [-W ; Q<- - P W] S^T  = [V_new ; O]      (state-dependent, one MMA)
-//   K->^T V_new                 = dS^T,  S <- (S + dS) Diag(gamma^C)
+//   K->^T V_new                 = dS^T,  S <- (S + dS) Diag(gamma^C)   (single kernel)
+//   K~^T V_new                  = dS^T,  S <- S Diag(gamma^C) + dS     (records, and a chunk
+//                                        past K->'s range),  K~ = K-> Diag(gamma^C)
 //
 // O = Q<- S^T + (Q<- K->^T * M) V_new expands to (Q<- - P W) S^T + P U, which
 // is why the output rides in the lower half of the state-dependent product;
-// the state step uses the factored form of page "Gated Linear Attention" 5.2.
+// the state step uses the factored form of page "Gated Linear Attention" 5.2
+// (K~ = K exp(G_C - G) is bounded by |K| at any decay).
 //
 // Two forms.
 //   Records (two kernels, when the caller's workspace holds them): the
 //   chunk-parallel Z kernel computes, for every chunk, Gamma, the rescaled
 //   tiles, Z, [W ; P W] and A_chain = [-W ; Q<- - P W] -- everything that
 //   does not depend on the state -- and writes the bf16 tile images of Z,
-//   A_chain and K-> and gamma^C as the chunk's record.  The record scan
+//   A_chain and K~ and gamma^C as the chunk's record.  The record scan
 //   kernel then runs one CTA per (batch, head, 64-wide value slice) and takes
-//   three products per chunk (Z V, A_chain S^T, K->^T V_new).
+//   three products per chunk (Z V, A_chain S^T, K~^T V_new).
 //   Single kernel (a 256-byte workspace, and GLA, which has no inverse): one
 //   CTA per (batch, head, 64-wide value slice) walks its chunks in order with
 //   two warp roles (384 threads): warps 0-3 "chain", the serial part -- the
@@ -76,7 +81,7 @@ constexpr uint32_t OFF_V0 = 65536;       // v slice [64][64] (MN-major B), slot 
 constexpr uint32_t OFF_V1 = 73728;       // slot 1
 constexpr uint32_t OFF_ACH0 = 81920;     // [-W ; Q'] 128 x 128 K-major, slot 0
 constexpr uint32_t OFF_ACH1 = 114688;    // slot 1
-constexpr uint32_t OFF_KT0 = 147456;     // K-> 64 x 128 (MN-major A of dS), slot 0
+constexpr uint32_t OFF_KT0 = 147456;     // K-> (or K~) 64 x 128 (MN-major A of dS), slot 0
 constexpr uint32_t OFF_KT1 = 163840;     // slot 1
 constexpr uint32_t OFF_ZIN = 180224;     // Z received from the other CTA of the pair
 constexpr uint32_t OFF_ST = 196608;      // S^T 128 x 64 (MN-major B); V_new in its first 8 KB
@@ -122,7 +127,7 @@ constexpr uint32_t kTmemCols = 512;
 // mbarrier indices
 enum {
     B_RAW = 0, B_V0, B_V1, B_GRAM, B_W2, B_WYR0, B_WYR1, B_C10, B_C11, B_C20, B_C21, B_E10, B_E11,
-    B_RX, B_PFREE, B_FIN0, B_FIN1, B_RAWK, B_RAWQ, kNumBars
+    B_RX, B_PFREE, B_FIN0, B_FIN1, B_RAWK, B_RAWQ, B_STRONG, kNumBars
 };
 static_assert(kNumBars <= 24, "mbarrier slots");
 
@@ -225,6 +230,19 @@ __device__ __forceinline__ uint32_t wait_bound_of(const int *status) {
 __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+// A named barrier that also returns whether `pred` held in any of its threads.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ void st_u128(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
@@ -289,12 +307,17 @@ __device__ __forceinline__ int zslot0(const FwdParams &p, int b, const Seq &sq) 
 // rows 8w .. 8w + 7, its lanes 16 column groups of 8 (one 16-byte piece of a
 // swizzled row) by 2 row halves, so every load and store moves 16 bytes and
 // the in-chunk cumsum is a 4-row sum, one shuffle and one exchange of warp
-// totals through `tot` (one barrier).  K-> of the thread's 4 rows comes back in
-// `krv` for the chunk's slot; the thread holding row 63 also returns gamma^C of
-// its 8 columns in `gam` (`has_gam`).
+// totals through `tot` (one barrier).  SCAN: K-> of the thread's 4 rows comes
+// back in `krv` for the chunk's slot; the thread holding row 63 (`has_gam`)
+// also returns gamma^C of its 8 columns in `gam`.
 //   REC (the Z kernel of the record form): A_G rows 0-63 get K<- itself (beta is
 // applied to the rows of L instead, so the tile is also the B operand of Z K<-),
-// and K-> and gamma^C go straight to the chunk record `rec`.
+// and K~ = K exp(G_C - G) and gamma^C go straight to the chunk record `rec`.
+//   Returns whether this thread saw a column whose decay K-> cannot represent
+// (G_C below -kFastLog2): the callers vote on it at their next barrier, and a
+// chunk so marked is done again by strong_prologue.  STRONG (that second pass):
+// K-> is not formed (its tile gets zeros), K~ is formed directly and goes to
+// `krv` in place of K->, and every thread returns gamma^C in `gam`.
 __device__ __forceinline__ void unpack_bf16x8(const uint4 u, float (&x)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -307,17 +330,14 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8]) {
     return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
 }
 
-// Largest in-chunk log-decay magnitude (base 2) the rescaled tiles represent: K-> = K 2^{-G}
-// and the products of K-> stay finite in fp32 with a margin of 2^28 for the sums.  The chain
-// checks it on gamma^C = 2^{G_C} (G_C, the chunk's total, is the extreme of G for g <= 0): a
-// chunk past it is recorded in the status word instead of inf / NaN reaching the outputs
-// unreported.
-constexpr float kGammaMin = 7.8886091e-31f;   // 2^-100
-constexpr float kGammaMax = 1.2676506e+30f;   // 2^100
-__device__ __forceinline__ bool gamma_in_range(float gam) { return gam > kGammaMin && gam < kGammaMax; }
+// Largest in-chunk log-decay magnitude (base 2) the rescaled tiles of the one-product Gram
+// represent: K-> = K 2^{-G} and the products of K-> stay finite in fp32 with a margin of 2^28
+// for the sums.  G_C, the chunk's total, is the extreme of G for g <= 0; a chunk whose G_C is
+// below -kFastLog2 in any channel takes the sub-chunk Gram (strong_gram) instead.
+constexpr float kFastLog2 = 100.f;
 
-template <int GATE, bool GRAM, bool SCAN, bool REC = false, typename PreQK>
-__device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int wt, int live_rows, const float *bet,
+template <int GATE, bool GRAM, bool SCAN, bool REC, bool STRONG, typename PreQK>
+__device__ __forceinline__ bool rescale_tiles(uint8_t *base, uint32_t kraw, int wt, int live_rows, const float *bet,
                                               const float *gs, float *tot, uint4 (&krv)[4], float (&gam)[8],
                                               bool &has_gam, PreQK &&pre_qk, uint8_t *rec = nullptr) {
     const int w = wt >> 5, lane = wt & 31;
@@ -331,7 +351,10 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
     auto off64 = [&](int i) { return o64 + (uint32_t)i * 128u + ((sw ^ (uint32_t)i) << 4); };
     auto off128 = [&](int i) { return o128 + (uint32_t)i * 128u + ((sw ^ (uint32_t)i) << 4); };
 
+    constexpr bool ALLGC = REC || STRONG;            // every thread needs G_C of its columns
     float G[4][8];                                   // in-chunk cumsum of g, base-2 units, this thread's rows
+    float gc2[8];                                    // ALLGC: G_C of this thread's columns, base 2
+    bool strong_here = false;                        // a column of this thread past the fast form's range
     has_gam = (w == 7 && rsub == 1);
     if constexpr (GATE == KDA_GATE_NONE) {
 #pragma unroll
@@ -339,7 +362,7 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
 #pragma unroll
             for (int e = 0; e < 8; ++e) G[i][e] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) gam[e] = 1.f;
+        for (int e = 0; e < 8; ++e) { gam[e] = 1.f; gc2[e] = 0.f; }
     } else {
         float a[8];
 #pragma unroll
@@ -369,7 +392,7 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
             const float up = __shfl_up_sync(0xffffffffu, own, 16);
             pre[e] = rsub ? up : 0.f;
             a[e] = own + pre[e];                     // lanes 16-31: the warp's 8-row total
-            // REC: what the chunk adds after this thread's last row, starting with the lower
+            // what the chunk adds after this thread's last row, starting with the lower
             // half-warp's rows for the upper half (the warp total from lanes 16-31 less its own)
             const float dn = __shfl_down_sync(0xffffffffu, a[e], 16);
             rest[e] = rsub ? 0.f : dn - own;
@@ -385,7 +408,7 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
             pre[0] += t0.x; pre[1] += t0.y; pre[2] += t0.z; pre[3] += t0.w;
             pre[4] += t1.x; pre[5] += t1.y; pre[6] += t1.z; pre[7] += t1.w;
         }
-        if (REC) {
+        if (ALLGC) {
             for (int q = w + 1; q < 8; ++q) {        // warp-uniform bound
                 const float4 t0 = *reinterpret_cast<const float4 *>(tot + q * kDK + col);
                 const float4 t1 = *reinterpret_cast<const float4 *>(tot + q * kDK + col + 4);
@@ -397,10 +420,13 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
         for (int e = 0; e < 8; ++e) {
             const float p2 = pre[e] * kLog2e;
             // G_C, the chunk's total log-decay (base 2): this thread's running sum plus the rest
-            const float gc2 = fmaf(G[3][e] + rest[e], kLog2e, p2);
+            gc2[e] = fmaf(G[3][e] + rest[e], kLog2e, p2);
 #pragma unroll
             for (int i = 0; i < 4; ++i) G[i][e] = fmaf(G[i][e], kLog2e, p2);
-            gam[e] = ex2_approx(REC ? gc2 : G[3][e]);    // REC: every thread; else the one holding row 63
+            // ALLGC: every thread; else the one holding row 63, whose G[3] is G_C
+            const float gce = ALLGC ? gc2[e] : G[3][e];
+            gam[e] = ex2_approx(gce);
+            strong_here |= (ALLGC || has_gam) && gce < -kFastLog2;
         }
     }
     if (REC && has_gam) {
@@ -423,11 +449,17 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
             if constexpr (GATE == KDA_GATE_NONE) {
                 kl[e] = kv[e]; kr[e] = kv[e]; ql[e] = qv[e]; kt[e] = kv[e];
             } else {
-                const float ev = ex2_approx(G[i][e]), iv = ex2_approx(-G[i][e]);
+                const float ev = ex2_approx(G[i][e]);
                 kl[e] = kv[e] * ev;
-                kr[e] = kv[e] * iv;
                 ql[e] = qv[e] * ev;
-                if (REC) kt[e] = kr[e] * gam[e];           // K~ = K exp(G_C - G) = K-> gamma^C
+                // K~ = K exp(G_C - G): K-> gamma^C where K-> is finite, else directly
+                if (!STRONG) {
+                    kr[e] = kv[e] * ex2_approx(-G[i][e]);
+                    if (REC) kt[e] = kr[e] * gam[e];
+                } else {
+                    kr[e] = 0.f;
+                    kt[e] = kv[e] * ex2_approx(gc2[e] - G[i][e]);
+                }
             }
         }
         const uint4 krp = pack_bf16x8(kr);
@@ -440,14 +472,17 @@ __device__ __forceinline__ void rescale_tiles(uint8_t *base, uint32_t kraw, int 
             *reinterpret_cast<uint4 *>(base + OFF_KR + off64(i)) = krp;
         }
         if (SCAN) *reinterpret_cast<uint4 *>(base + OFF_KL + off64(i)) = pack_bf16x8(kl);
-        krv[i] = krp;
+        if (SCAN) krv[i] = STRONG ? pack_bf16x8(kt) : krp;
         if (REC) *reinterpret_cast<uint4 *>(rec + REC_KR + off64(i)) = pack_bf16x8(kt);
     }
+    return strong_here;
 }
-// Slot image of the K-> rows a thread of rescale_tiles produced (its 4 rows x 8 columns) and,
-// from the thread that holds row 63, gamma^C of its 8 columns.
+// Slot image of the rows a thread of rescale_tiles produced (its 4 rows x 8 columns) and, from
+// the thread that holds row 63, gamma^C of its 8 columns.  The rows are K->, or K~ for a chunk
+// that took the sub-chunk Gram (`strong`), which the chain learns from the sign bit of gamma^C
+// (stored negated; -0 where gamma^C underflows).
 __device__ __forceinline__ void store_kr_slot(uint8_t *kt, float *gc, int wt, const uint4 (&krv)[4],
-                                              const float (&gam)[8], bool has_gam) {
+                                              const float (&gam)[8], bool has_gam, bool strong) {
     const int w = wt >> 5, lane = wt & 31;
     const int cq = lane & 15, rsub = lane >> 4;
     const int r0 = 8 * w + 4 * rsub;
@@ -457,8 +492,10 @@ __device__ __forceinline__ void store_kr_slot(uint8_t *kt, float *gc, int wt, co
         *reinterpret_cast<uint4 *>(kt + (uint32_t)(cq >> 3) * 8192u + (uint32_t)(r0 + i) * 128u +
                                    ((sw ^ (uint32_t)i) << 4)) = krv[i];
     if (has_gam) {
-        *reinterpret_cast<float4 *>(gc + 8 * cq) = make_float4(gam[0], gam[1], gam[2], gam[3]);
-        *reinterpret_cast<float4 *>(gc + 8 * cq + 4) = make_float4(gam[4], gam[5], gam[6], gam[7]);
+        const float sg = strong ? -1.f : 1.f;
+        *reinterpret_cast<float4 *>(gc + 8 * cq) = make_float4(sg * gam[0], sg * gam[1], sg * gam[2], sg * gam[3]);
+        *reinterpret_cast<float4 *>(gc + 8 * cq + 4) =
+            make_float4(sg * gam[4], sg * gam[5], sg * gam[6], sg * gam[7]);
     }
 }
 
@@ -496,8 +533,10 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t addr, const uint32_t (&r)[4
 // ends without a barrier.
 //   REC: rows 0-63 of the Gram are K<- K->^T (A_G holds K<-, not beta K<-), so
 // beta scales them as they leave TMEM.
+//   strong: the sub-chunk Gram is already in TMEM; the Gram barrier is committed with no product,
+// so that its phases stay one per chunk.
 template <bool GLA, bool REC = false>
-__device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, float *yfrag) {
+__device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, float *yfrag, bool strong) {
     uint8_t *base = c.base;
     const int ww = wt >> 5, lane = wt & 31;
     const int quarter = ww & 3, half = ww >> 2;
@@ -506,11 +545,13 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, floa
     // ---------------- Gram: D_G = [beta K<- ; Q<-] K->^T   (M128 N64 K128)
     if (leader) {
         tc_fence_after();
-        const uint32_t a0 = smem_u32(base + OFF_AG), b0 = smem_u32(base + OFF_KR);
-        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+        if (!strong) {
+            const uint32_t a0 = smem_u32(base + OFF_AG), b0 = smem_u32(base + OFF_KR);
+            const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-            mma_bf16(c.tmem + TM_G, desc_kmajor(a0, 128, ks), desc_kmajor(b0, 64, ks), id, ks > 0);
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(c.tmem + TM_G, desc_kmajor(a0, 128, ks), desc_kmajor(b0, 64, ks), id, ks > 0);
+        }
         mma_commit(c.bars + B_GRAM);
     }
     __syncwarp();
@@ -676,9 +717,265 @@ __device__ int build_z(const Ctx &c, int wt, const float *bet, uint32_t ph, floa
 }
 
 // ============================================================================
+// Chunks past the one-product Gram's range: the sub-chunk Gram.
+// ============================================================================
+// [beta K<- ; Q<-] K->^T factors exp(G_i - G_j) as Gamma_i / Gamma_j, whose 1 / Gamma_j overflows
+// once a chunk's log-decay passes -kFastLog2 (base 2).  Such a chunk takes the secondary chunking
+// of page "Gated Linear Attention", section 5.3, with 16-token sub-chunks:
+//   - pairs of different sub-chunks (I > J) as bf16 tensor-core products, with the end of
+//     sub-chunk I - 1 as reference, R_I = G at row 16 I - 1: rows i of sub-chunk I scaled by
+//     2^{G_i - R_I} <= 1 (one A tile serves every I) and rows j < 16 I of K by 2^{R_I - G_j} <= 1
+//     (a B tile per I), so no factor exceeds 1;
+//   - pairs within a sub-chunk element by element in fp32, sum_d x_id k_jd 2^{G_id - G_jd}, at
+//     full precision.
+// The result lands in the Gram's TMEM columns as the one-product Gram leaves it (rows 0-63:
+// [beta] K<- K->^T, rows 64-127: Q<- K->^T; the parts build_z reads), with no limit on the decay.
+// The 256 WY threads enter after the prologue has written its tiles and with no copy into A_G,
+// the K-> tile or the raw k tile in flight; they read q, k and g from global memory (L2), use
+// A_G, the K-> tile, `scratch` (4 KB) and TMEM columns kStrongCol .. kStrongCol + 63 as scratch,
+// and end with the raw g, q and k tiles fetched back into place for the prologue, which then
+// runs again.  Returns the completed-phase count of B_STRONG.
+constexpr uint32_t kStrongCol = 64;      // TMEM columns 64-127: free while the Gram is formed
+struct StrongArgs {
+    const __nv_bfloat16 *q, *k;         // [.., H, 128] rows of the batch
+    const void *g;                      // channel gate, same layout (type Tg), or null
+    const float *gs;                    // scalar gate of the chunk's rows (shared memory), or null
+    const float *bet;                   // beta of the chunk's rows for rows 0-63, or null (unscaled)
+    float *scratch;                     // 4 KB of shared memory
+    size_t row0;                        // global row (b T + t) of the chunk's first token
+    int H, h, live;                     // heads, this head, valid rows of the chunk
+    const CUtensorMap *tm_q, *tm_k, *tm_g;   // tm_g: null unless the gate is per channel
+    int tma_t, tma_b;                   // TMA token and batch coordinates of the chunk
+    uint32_t kraw;                      // offset of the raw k tile
+};
+
+template <int GATE, typename Tg>
+__device__ __forceinline__ uint32_t strong_gram(const Ctx &c, const StrongArgs &a, int wt, uint32_t sph) {
+    uint8_t *base = c.base;
+    const int d = wt & 127, part = wt >> 7;          // key channel; part 0: k side, part 1: q side
+    const int ww = wt >> 5, lane = wt & 31, quarter = ww & 3, half = ww >> 2;
+    const bool leader = wt == 0;
+    bool ok = true;                                  // every wait here ended complete
+    int armed = -1;                                  // leader: phase count of the newest phase it armed
+    auto grow = [&](int r) -> float {                // log-decay of row r, channel d, base 2
+        if (r >= a.live) return 0.f;
+        const float x = GATE == KDA_GATE_CHANNEL
+                            ? ldg_f<Tg>(static_cast<const Tg *>(a.g) + ((a.row0 + r) * a.H + a.h) * kDK + d)
+                            : a.gs[r];
+        return x * kLog2e;
+    };
+    auto raw = [&](const __nv_bfloat16 *t, int r) -> __nv_bfloat16 {
+        return r < a.live ? t[((a.row0 + r) * a.H + a.h) * kDK + d] : __float2bfloat16_rn(0.f);
+    };
+
+    // ---- the A tile in A_G: row i of sub-chunk I scaled by 2^{G_i - R_I}; rows 0-63 from k
+    //      (times beta), rows 64-127 from q.  R keeps R_I of channel d.
+    float R[4];
+    {
+        const __nv_bfloat16 *x = part ? a.q : a.k;
+        float G = 0.f;
+#pragma unroll
+        for (int I = 0; I < 4; ++I) {
+            R[I] = G;
+#pragma unroll 1
+            for (int r0 = 16 * I; r0 < 16 * I + 16; r0 += 8) {
+                float gv[8], xv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    gv[i] = grow(r0 + i);
+                    xv[i] = __bfloat162float(raw(x, r0 + i));
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + i;
+                    G += gv[i];
+                    float v = xv[i] * ex2_approx(G - R[I]);
+                    if (!part && a.bet) v *= a.bet[r];
+                    *reinterpret_cast<__nv_bfloat16 *>(base + OFF_AG + sw128_offset(128, part * 64 + r, d)) =
+                        __float2bfloat16_rn(v);
+                }
+            }
+        }
+    }
+    auto ref = [&](int I) { return I == 0 ? R[0] : I == 1 ? R[1] : I == 2 ? R[2] : R[3]; };
+
+    // ---- sub-chunk pairs I > J: B = rows j < 16 I of k scaled by 2^{R_I - G_j} in the K-> tile,
+    //      D = A B^T (N = 16 I) into the spare columns, whose rows of sub-chunk I go to the Gram's
+#pragma unroll 1
+    for (int I = 1; I < 4; ++I) {
+        if (part == 0) {
+            const float RI = ref(I);
+            float G = 0.f;
+#pragma unroll 1
+            for (int j0 = 0; j0 < 16 * I; j0 += 8) {
+                float gv[8], kv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    gv[i] = grow(j0 + i);
+                    kv[i] = __bfloat162float(raw(a.k, j0 + i));
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    G += gv[i];
+                    *reinterpret_cast<__nv_bfloat16 *>(base + OFF_KR + sw128_offset(64, j0 + i, d)) =
+                        __float2bfloat16_rn(kv[i] * ex2_approx(RI - G));
+                }
+            }
+        }
+        fence_proxy_async_smem();                    // A and B, before the tensor core reads them
+        named_sync(2, kWyThreads);
+        if (leader && ok) {
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(base + OFF_AG), b0 = smem_u32(base + OFF_KR);
+            const uint32_t id = idesc_bf16(128, 16 * I, 0, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(c.tmem + kStrongCol, desc_kmajor(a0, 128, ks), desc_kmajor(b0, 64, ks), id, ks > 0);
+            mma_commit(c.bars + B_STRONG);
+            armed = (int)sph;
+        }
+        __syncwarp();
+        ok &= wait_bar(c, B_STRONG, sph & 1u);
+        ++sph;
+        tc_fence_after();
+        // rows of sub-chunk I: lanes 16 (I & 1) .. of quarter I / 2 (rows of L) and 2 + I / 2 (of P)
+        if (half == 0 && (quarter == (I >> 1) || quarter == 2 + (I >> 1))) {
+            const uint32_t lb = (uint32_t)(quarter * 32) << 16;
+            const bool mine = (lane >> 4) == (I & 1);
+#pragma unroll 1
+            for (int cc = 0; cc * 32 < 16 * I; ++cc) {
+                float o[32], nw[32];
+                __syncwarp();
+                tmem_ld32(c.tmem + TM_G + lb + 32 * cc, o);
+                tmem_ld32(c.tmem + kStrongCol + lb + 32 * cc, nw);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = mine ? nw[e] : o[e];
+                tmem_st32(c.tmem + TM_G + lb + 32 * cc, o);
+            }
+        }
+        tc_fence_before();
+        named_sync(2, kWyThreads);                   // the B tile and the spare columns are free again
+    }
+
+    // ---- pairs within sub-chunk I, in fp32.  G, k, q of its 16 rows go to the K-> tile as
+    //      [channel][row] arrays (a warp's threads read distinct rows of one channel: distinct
+    //      banks); one thread per entry: 136 of P (i >= j), 120 of L (i > j).
+    float *sG = reinterpret_cast<float *>(base + OFF_KR);                       // [128][16] f32
+    __nv_bfloat16 *sk = reinterpret_cast<__nv_bfloat16 *>(base + OFF_KR + 8192);   // [128][16]
+    __nv_bfloat16 *sq = sk + 128 * 16;                                              // [128][16]
+    int ei, ej;                                      // this thread's entry
+    const bool isP = wt < 136;
+    {
+        int e = isP ? wt : wt - 136, i = isP ? 0 : 1;
+        while (e >= (isP ? i + 1 : i)) {             // row i holds i + 1 (P) or i (L) entries
+            e -= isP ? i + 1 : i;
+            ++i;
+        }
+        ei = i;
+        ej = e;
+    }
+#pragma unroll 1
+    for (int I = 0; I < 4; ++I) {
+        if (part == 0) {
+            float G = ref(I);
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                G += grow(16 * I + j);
+                sG[d * 16 + j] = G;
+            }
+        } else {
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                sk[d * 16 + j] = raw(a.k, 16 * I + j);
+                sq[d * 16 + j] = raw(a.q, 16 * I + j);
+            }
+        }
+        named_sync(2, kWyThreads);
+        {
+            const __nv_bfloat16 *xs = isP ? sq : sk;
+            float acc = 0.f;
+#pragma unroll 4
+            for (int dd = 0; dd < kDK; ++dd)
+                acc = fmaf(__bfloat162float(xs[dd * 16 + ei]) * __bfloat162float(sk[dd * 16 + ej]),
+                           ex2_approx(sG[dd * 16 + ei] - sG[dd * 16 + ej]), acc);
+            if (!isP && a.bet) acc *= a.bet[16 * I + ei];
+            a.scratch[(isP ? 256 : 0) + ei * 16 + ej] = acc;
+        }
+        named_sync(2, kWyThreads);
+        // into columns 16 I .. 16 I + 15 of the sub-chunk's rows (entries above the diagonal: 0)
+        if (half == 0 && (quarter == (I >> 1) || quarter == 2 + (I >> 1))) {
+            const uint32_t lb = (uint32_t)(quarter * 32) << 16;
+            const bool mine = (lane >> 4) == (I & 1), pq = quarter >= 2;
+            const int ii = lane & 15;
+            const uint32_t cc = (uint32_t)(16 * I) & ~31u;
+            const float *src = a.scratch + (pq ? 256 : 0) + ii * 16;
+            float o[32];
+            __syncwarp();
+            tmem_ld32(c.tmem + TM_G + lb + cc, o);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const float val = (pq ? jj <= ii : jj < ii) ? src[jj] : 0.f;
+                if (I & 1) o[16 + jj] = mine ? val : o[16 + jj];   // I & 1: the same in the whole warp
+                else o[jj] = mine ? val : o[jj];
+            }
+            tmem_st32(c.tmem + TM_G + lb + cc, o);
+        }
+        tc_fence_before();
+        named_sync(2, kWyThreads);                   // the staged rows and `scratch` are free again
+    }
+
+    // ---- the raw tiles back into place: g into A_G rows 0-63, q into rows 64-127, k into its tile
+    fence_proxy_async_smem();
+    named_sync(2, kWyThreads);
+    if (leader && ok) {
+        mbar_arrive_expect_tx(c.bars + B_STRONG, (a.tm_g ? 3u : 2u) * 16384u);
+        for (int blk = 0; blk < 2; ++blk) {
+            tma_load_4d(base + OFF_AG + blk * 16384 + 8192, a.tm_q, c.bars + B_STRONG, blk * 64, a.h, a.tma_t,
+                        a.tma_b);
+            if (a.tm_g)
+                tma_load_4d(base + OFF_AG + blk * 16384, a.tm_g, c.bars + B_STRONG, blk * 64, a.h, a.tma_t, a.tma_b);
+            tma_load_4d(base + a.kraw + blk * 8192, a.tm_k, c.bars + B_STRONG, blk * 64, a.h, a.tma_t, a.tma_b);
+        }
+        armed = (int)sph;
+    }
+    __syncwarp();
+    ok &= wait_bar(c, B_STRONG, sph & 1u);
+    ++sph;
+    // a wait gave up: the newest product or copy issued here completes before the tiles are
+    // touched again (the phases before it completed first)
+    if (leader && !ok && armed >= 0) drain_bar(c, B_STRONG, (uint32_t)armed & 1u);
+    return sph;
+}
+
+// A chunk the prologue marked: the sub-chunk Gram, then the prologue again over the refetched
+// raw tiles in its STRONG form.  Out of line, so that the rarely taken path does not weigh on the
+// registers of the loops around it; returns what the prologue returns in registers (K~ rows for
+// the chunk's slot, gamma^C) and the completed-phase count of B_STRONG.  Ends, like the ordinary
+// prologue and its barrier, with the tiles written and visible to the tensor core.
+struct StrongOut {
+    uint4 krv[4];
+    float gam[8];
+    uint32_t sph;
+};
+template <int GATE, bool SCAN, bool REC, typename Tg>
+__device__ __noinline__ StrongOut strong_prologue(const Ctx c, const StrongArgs a, int wt, uint32_t sph,
+                                                  const float *bet, uint8_t *rec) {
+    StrongOut out;
+    out.sph = strong_gram<GATE, Tg>(c, a, wt, sph);
+    bool has_gam;
+    rescale_tiles<GATE, true, SCAN, REC, true>(c.base, a.kraw, wt, a.live, bet, a.gs, a.scratch, out.krv, out.gam,
+                                               has_gam, [] {}, rec);
+    fence_proxy_async_smem();
+    named_sync(2, kWyThreads);
+    return out;
+}
+
+// ============================================================================
 // WY warps: everything of a chunk that does not depend on the state.
 // ============================================================================
-template <int GATE, bool GLA, bool PAIR, typename Tg>
+// STRONG: the instance that takes the sub-chunk Gram for a chunk past the one-product Gram's
+// range; the other instance only notes such a chunk (kStatusStrongWord) for the launch that follows.
+template <int GATE, bool GLA, bool PAIR, bool STRONG, typename Tg>
 __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                         const CUtensorMap *tm_g, const CUtensorMap *tm_v, int e0, int h, Seq sq, int nchunks) {
     uint8_t *base = c.base;
@@ -711,6 +1008,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
     // `mi` is the index, among the chunks this CTA builds, of the chunk fetched.
     bool clean = true;
     int last_g = -1, last_k = -1, last_q = -1, last_v[2] = {-1, -1};
+    uint32_t sph = 0;                                    // completed phases of the sub-chunk Gram's barrier
     auto issue_g = [&](int n, int mi) {
         if (GATE != KDA_GATE_CHANNEL || !clean) return;
         last_g = mi;
@@ -784,7 +1082,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
         const uint32_t peer_base = PAIR ? map_to_rank(smem_u32(base), c.rank ^ 1u) : 0u;
         uint4 krv[4];
         float gam[8];
-        bool has_gam;
+        bool has_gam, strong;
         int r0 = 0;                                          // first of the 16 Z rows this warp built
 
         {
@@ -792,15 +1090,47 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
             if (GATE == KDA_GATE_CHANNEL) clean &= wait_bar(c, B_RAW, phm);
             // ---------------- prologue: Gamma and the rescaled tiles, in place.  K-> and gamma^C also
             // go to the chunk's slot, written at the end (the slot may still be in use).
-            rescale_tiles<GATE, true, true>(base, OFF_KL, wt, sq.len - n * kC, bet, gss + sb * kC, tot, krv, gam,
-                                            has_gam, [&] {
-                                                clean &= wait_bar(c, B_RAWQ, phm);
-                                                clean &= wait_bar(c, B_RAWK, phm);
-                                            });
+            auto pre_qk = [&] {
+                clean &= wait_bar(c, B_RAWQ, phm);
+                clean &= wait_bar(c, B_RAWK, phm);
+            };
+            const bool mark = rescale_tiles<GATE, true, true, false, false>(
+                base, OFF_KL, wt, sq.len - n * kC, bet, gss + sb * kC, tot, krv, gam, has_gam, pre_qk);
             fence_proxy_async_smem();
-            named_sync(2, kWyThreads);
+            if constexpr (!STRONG) {
+                // outputs of this call are redone by the STRONG launch: note it, go on
+                if (mark) p.status[kStatusStrongWord] = p.strong_token;
+                named_sync(2, kWyThreads);
+                strong = false;
+            } else {
+                strong = named_sync_or(2, kWyThreads, mark);
+            }
+            if (STRONG && strong) {
+                const StrongArgs sa{static_cast<const __nv_bfloat16 *>(p.q),
+                                    static_cast<const __nv_bfloat16 *>(p.k),
+                                    GATE == KDA_GATE_CHANNEL ? p.g : nullptr,
+                                    gss + sb * kC,
+                                    bet,
+                                    tot,
+                                    (size_t)sq.bt * T + sq.t0 + n * kC,
+                                    H,
+                                    h,
+                                    sq.len - n * kC,
+                                    tm_q,
+                                    tm_k,
+                                    GATE == KDA_GATE_CHANNEL ? tm_g : nullptr,
+                                    sq.t0 + n * kC,
+                                    sq.bt,
+                                    OFF_KL};
+                const StrongOut so = strong_prologue<GATE, true, false, Tg>(c, sa, wt, sph, bet, nullptr);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) krv[i] = so.krv[i];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gam[e] = so.gam[e];
+                sph = so.sph;
+            }
 
-            r0 = build_z<GLA>(c, wt, bet, phm, tot);
+            r0 = build_z<GLA>(c, wt, bet, phm, tot, strong);
             // the Gram has read beta K<-: the next chunk's g may land in its rows
             if (leader && n + step < nchunks) issue_g(n + step, m + 1);
             fence_proxy_async_smem();
@@ -901,8 +1231,8 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
                 store_row32_bf16(ach, 128, row, col, v);
             }
         }
-        // ---------------- K-> and gamma^C into slot s (and the other CTA's slot s)
-        store_kr_slot(base + off_kt(s), gC + s * kDK, wt, krv, gam, has_gam);
+        // ---------------- K-> (K~) and gamma^C into slot s (and the other CTA's slot s)
+        store_kr_slot(base + off_kt(s), gC + s * kDK, wt, krv, gam, has_gam, strong);
         if (wt < kC && n + step < nchunks) {
             betas[(sb ^ 1) * kC + wt] = nb;
             gss[(sb ^ 1) * kC + wt] = ng;
@@ -948,7 +1278,7 @@ __device__ void wy_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_
 // ============================================================================
 // Chain warps: the serial state scan and the output.
 // ============================================================================
-template <bool PAIR>
+template <bool PAIR, bool STRONG>
 __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_v, const CUtensorMap *tm_o,
                            int e0, int h, int b, Seq sq, int nchunks) {
     uint8_t *base = c.base;
@@ -960,7 +1290,6 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     const int H = p.H, dv = p.dv;
     bool clean = true;                          // every wait of this thread has ended complete
     int last_v = -1;                            // newest v copy this thread issued (chunk index)
-    bool in_range = true;                       // every chunk's gamma^C within the decay limit
 
     float S[kDVS];
 #pragma unroll
@@ -996,8 +1325,10 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
             wait_bar(c, B_WYR0 + s, ph2);
         }
         tc_fence_after();
-        const float gam = gC[s * kDK + j];
-        in_range &= gamma_in_range(gam);
+        // gamma^C; its sign bit marks a chunk whose slot holds K~ instead of K-> (same in every thread)
+        const float gsg = gC[s * kDK + j];
+        const bool ktilde = STRONG && signbit(gsg);
+        const float gam = STRONG ? fabsf(gsg) : gsg;
 
         // ---- D1[s] (+)= [-W ; Q'] S^T   (M128 N64 K128)
         if (leader) {
@@ -1087,8 +1418,13 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 tmem_ld32(c.tmem + TM_S + lane_base + cc * 32, v);
+                if (!ktilde) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) S[cc * 32 + e] = gam * (S[cc * 32 + e] + v[e]);
+                    for (int e = 0; e < 32; ++e) S[cc * 32 + e] = gam * (S[cc * 32 + e] + v[e]);   // dS^T = K->^T V_new
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) S[cc * 32 + e] = fmaf(gam, S[cc * 32 + e], v[e]);   // dS^T = K~^T V_new
+                }
             }
         }
         if (leader) tma_store_wait_read0();                       // staging tile free for the next chunk
@@ -1101,7 +1437,6 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
 #pragma unroll
         for (int e = 0; e < kDVS; ++e) p.ht[(((size_t)b * H + h) * dv + e0 + e) * kDK + j] = S[e];
     }
-    if (!in_range) atomicCAS(c.status, kDevOk, kDevDecayRange);
     if (leader) {
         tma_store_wait_all0();
         mma_commit(c.bars + B_FIN0);
@@ -1117,11 +1452,15 @@ __device__ void chain_role(const Ctx &c, const FwdParams &p, const CUtensorMap *
     __syncwarp();
 }
 
-template <int GATE, bool GLA, bool PAIR, typename Tg>
+// STRONG: the second launch of a call, which redoes the call with the sub-chunk Gram when the
+// first noted a chunk past the one-product Gram's range, and exits at once otherwise (both CTAs of
+// a pair read the same word, so they decide alike).
+template <int GATE, bool GLA, bool PAIR, bool STRONG, typename Tg>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o) {
+    if (STRONG && *reinterpret_cast<volatile const int *>(p.status + kStatusStrongWord) != p.strong_token) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctx c;
@@ -1165,9 +1504,9 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
     c.tmem = *tslot;
 
     if (threadIdx.x < kChainThreads)
-        chain_role<PAIR>(c, p, &tm_v, &tm_o, e0, h, b, sq, nchunks);
+        chain_role<PAIR, STRONG>(c, p, &tm_v, &tm_o, e0, h, b, sq, nchunks);
     else
-        wy_role<GATE, GLA, PAIR, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, sq, nchunks);
+        wy_role<GATE, GLA, PAIR, STRONG, Tg>(c, p, &tm_q, &tm_k, &tm_g, &tm_v, e0, h, sq, nchunks);
 
     tc_fence_before();
     __syncthreads();
@@ -1183,7 +1522,7 @@ kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
 // One CTA per (chunk, head, sequence) computes Gamma, the rescaled tiles and
 // Z = [T ; P T] with the single kernel's code (rescale_tiles, build_z), then
 // [W ; P W] = Z K<- on the tensor core and A_chain = [-W ; Q<- - P W], and
-// stores the images of the bf16 tiles Z, A_chain and K-> (and gamma^C) as the
+// stores the images of the bf16 tiles Z, A_chain and K~ (and gamma^C) as the
 // chunk's record, which the scan kernel loads with bulk copies.  Shared
 // memory: the A_G and K-> tiles at the single kernel's offsets (raw k lands in
 // the K-> tile and becomes K-> in place; A_G becomes [K<- ; Q<-], then
@@ -1237,6 +1576,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
         mbar_init(c.bars + B_RAW, 1);
         mbar_init(c.bars + B_GRAM, 1);
         mbar_init(c.bars + B_FIN0, 1);
+        mbar_init(c.bars + B_STRONG, 1);
         *c.abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -1279,12 +1619,31 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     uint4 krv[4];
     float gam[8];
     bool has_gam;
-    rescale_tiles<GATE, true, false, true>(base, OFF_KR, wt, sq.len - n * kC, betas, gss, tot, krv, gam, has_gam,
-                                           [] {}, rec);
+    const bool mark = rescale_tiles<GATE, true, false, true, false>(base, OFF_KR, wt, sq.len - n * kC, betas, gss,
+                                                                    tot, krv, gam, has_gam, [] {}, rec);
     fence_proxy_async_smem();
-    __syncthreads();
+    const bool strong = __syncthreads_or(mark) != 0;
+    if (strong) {
+        const StrongArgs sa{static_cast<const __nv_bfloat16 *>(p.q),
+                            static_cast<const __nv_bfloat16 *>(p.k),
+                            GATE == KDA_GATE_CHANNEL ? p.g : nullptr,
+                            gss,
+                            nullptr,
+                            tot,
+                            (size_t)sq.bt * T + sq.t0 + n * kC,
+                            H,
+                            h,
+                            sq.len - n * kC,
+                            &tm_q,
+                            &tm_k,
+                            GATE == KDA_GATE_CHANNEL ? &tm_g : nullptr,
+                            sq.t0 + n * kC,
+                            sq.bt,
+                            OFF_KR};
+        strong_prologue<GATE, false, true, Tg>(c, sa, wt, 0u, betas, rec);
+    }
     // the cumsum partials are dead: their 4 KB hold the diagonal-block inverses
-    build_z<false, true>(c, wt, betas, 0, tot);
+    build_z<false, true>(c, wt, betas, 0, tot, strong);
     fence_proxy_async_smem();               // the Z stores, before the bulk copy and the tensor core read them
     tc_fence_before();
     __syncthreads();                        // and every warp is done with the Gram's TMEM columns
@@ -1360,12 +1719,12 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
 // state-independent operand, so a chunk takes three products:
 //   D1 = Z V = [U ; P U]                  (issued by the loader, one chunk ahead)
 //   D1 += A_chain S^T = [V_new ; O]       (the state product)
-//   dS^T = K->^T V_new,   S <- (S + dS) Diag(gamma^C)
+//   dS^T = K~^T V_new,   S <- S Diag(gamma^C) + dS
 // The slice's values are split into NH halves of W = 64 / NH, each a chain of
 // four warps with its own accumulator columns, S^T and V_new tiles and
 // barriers, so the halves can run out of step.  Warp 4 NH loads the records
 // (bulk copies) and the v tiles (TMA) and issues Z V.  A record takes about a
-// chunk's time to arrive, so A_chain, K->, gamma^C and v of chunk n go to entry
+// chunk's time to arrive, so A_chain, K~, gamma^C and v of chunk n go to entry
 // n % 3 of a three-deep ring, loaded three chunks ahead, and Z V of chunk n
 // runs two chunks ahead into accumulator slot n % 3, its Z from entry n % 2 of
 // a two-deep ring.  V_new takes the front of the half's S^T tile, which the
@@ -1377,7 +1736,7 @@ constexpr int kScanHalves = 1;
 template <int NH> struct ScanCfg {
     static constexpr int W = 64 / NH;                    // values per half
     static constexpr int kThreads = 128 * NH + 32;
-    static constexpr uint32_t R_SLOT = 57344;            // ring entry: A_chain, K->, v
+    static constexpr uint32_t R_SLOT = 57344;            // ring entry: A_chain, K~, v
     static constexpr uint32_t R_ACH = 0, R_KT = 32768, R_V = 49152;
     static constexpr uint32_t OFF_Z = 3 * R_SLOT;        // two entries: Z
     static constexpr uint32_t OFF_ST = OFF_Z + 2 * 16384;    // S^T (then V_new) of each half, 16 KB in all
@@ -1453,7 +1812,6 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
     uint8_t *st = base + G::OFF_ST + half * 8192;
     uint8_t *vn = st;                                    // V_new: 64 rows at the front of the S^T tile
     const float *gc = reinterpret_cast<const float *>(base + G::OFF_GC);
-    bool in_range = true;                                // every chunk's gamma^C within the decay limit
     const uint32_t col = (uint32_t)(half * W);
 
     float S[W];
@@ -1473,11 +1831,10 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
         const int s = n & 1, ri = n % 3;
         const uint32_t ph = (uint32_t)((n >> 1) & 1), phr = (uint32_t)((n / 3) & 1);
         uint8_t *slot = base + ri * G::R_SLOT;
-        wait_bar(c, SB_FULLR + ri, phr);                 // A_chain, K-> and gamma^C of the record
+        wait_bar(c, SB_FULLR + ri, phr);                 // A_chain, K~ and gamma^C of the record
         wait_bar(c, SB_ZV + ri, phr);                    // D1[ri] = [U ; P U]
         tc_fence_after();
         const float gam = gc[ri * kDK + t];
-        in_range &= gamma_in_range(gam);
 
         // ---- D1[s] += A_chain S^T   (M128 N=W K128)
         if (leader) {
@@ -1491,7 +1848,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
         wait_bar(c, SB_C1 + half * 2 + s, ph);
         tc_fence_after();
 
-        // ---- rows 0-63 (warps 0, 1): V_new -> the half's V_new tile, then dS^T = K->^T V_new;
+        // ---- rows 0-63 (warps 0, 1): V_new -> the half's V_new tile, then dS^T = K~^T V_new;
         //      rows 64-127 (warps 2, 3): O -> o, stored while that product runs
         {
             float v[W];
@@ -1501,7 +1858,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(bar_id, 128);
-            // ---- dS^T = K->^T V_new   (M128 N=W K64)
+            // ---- dS^T = K~^T V_new   (M128 N=W K64)
             if (leader) {
                 tc_fence_after();
                 mbar_arrive(c.bars + SB_D1FREE + ri);    // this half's columns of D1[ri] are drained
@@ -1538,7 +1895,6 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
 #pragma unroll
         for (int e = 0; e < W; ++e) p.ht[(((size_t)b * H + h) * dv + ev0 + e) * kDK + t] = S[e];
     }
-    if (!in_range) atomicCAS(c.status, kDevOk, kDevDecayRange);
     if (leader) {                                       // every product issued here is done
         mma_commit(c.bars + SB_FINC + half);
         drain_bar(c, SB_FINC + half, 0);
@@ -1546,7 +1902,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
     __syncwarp();
 }
 
-// The loader (one thread): chunk n's A_chain, K->, gamma^C and v tile into ring
+// The loader (one thread): chunk n's A_chain, K~, gamma^C and v tile into ring
 // entry n % 3, its Z into entry n % 2 of the Z ring, and D1[n % 3] = Z V as
 // soon as those are in and chunk n - 3 has drained the slot.
 template <int NH>
@@ -1706,14 +2062,14 @@ bool make_map(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int GATE, bool GLA, typename Tg>
-cudaError_t launch_single(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
-                          const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
+template <int GATE, bool GLA, bool STRONG, typename Tg>
+cudaError_t launch_single_one(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
+                              const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
     // The two value slices of a head (dv = 128) split the chunks they build (a pair).
     dim3 grid(p.dv / kDVS, p.H, p.B);
     {
       if (p.dv == 2 * kDVS) {
-        auto kern = kda_fwd_tc_kernel<GATE, GLA, true, Tg>;
+        auto kern = kda_fwd_tc_kernel<GATE, GLA, true, STRONG, Tg>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -1731,11 +2087,24 @@ cudaError_t launch_single(const FwdParams &p, const CUtensorMap &q, const CUtens
         return cudaLaunchKernelEx(&cfg, kern, p, q, k, g, v, o);
       }
     }
-    auto kern = kda_fwd_tc_kernel<GATE, GLA, false, Tg>;
+    auto kern = kda_fwd_tc_kernel<GATE, GLA, false, STRONG, Tg>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, kSmemBytes, s>>>(p, q, k, g, v, o);
     return cudaGetLastError();
+}
+
+// The single kernel as two launches: the first, with only the one-product Gram, notes a chunk
+// whose decay is past its range; the second redoes the whole call with the sub-chunk Gram if the
+// first noted one, and exits at once otherwise.  (The sub-chunk path compiled into the first
+// kernel would cost it registers in its chunk loop; the second launch costs a few microseconds.)
+// GATE_NONE has no decay: one launch.
+template <int GATE, bool GLA, typename Tg>
+cudaError_t launch_single(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
+                          const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
+    cudaError_t e = launch_single_one<GATE, GLA, false, Tg>(p, q, k, g, v, o, s);
+    if (e != cudaSuccess || GATE == KDA_GATE_NONE) return e;
+    return launch_single_one<GATE, GLA, true, Tg>(p, q, k, g, v, o, s);
 }
 
 template <int NH>

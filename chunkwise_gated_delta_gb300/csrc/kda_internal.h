@@ -21,6 +21,7 @@ struct FwdParams {
     int *status;            // first word of the workspace
     const int *cu_seqlens;  // packed sequences: [B + 1] row offsets into a [1, T, H, d] batch, or null
     uint8_t *zrec;          // bf16 path: Z records (fwd_zrec_bytes), or null to build Z in the scan kernel
+    int strong_token;       // nonzero, new for every call: see kStatusStrongWord
 };
 
 // Device-side copy of the validated DPLR arguments.
@@ -76,6 +77,10 @@ enum : int { kDevOk = 0, kDevTimeout = 1, kDevDecayRange = 2 };
 // Word of the 256-byte status block that holds the polling budget of the bounded waits
 // (iterations before a wait gives up; 0 = the library default).
 constexpr int kStatusBoundWord = 7;
+// Word where the single-kernel bf16 forward notes the call's strong_token when a chunk's decay
+// is past the one-product Gram's range; a second launch then redoes the call with the sub-chunk
+// Gram, and exits at once when the word holds another call's token.
+constexpr int kStatusStrongWord = 8;
 
 // float32 CUDA-core path (any gate kind; inputs float32).
 cudaError_t launch_fwd_simt_f32(const FwdParams &p, int g_is_bf16, cudaStream_t s);

@@ -68,8 +68,8 @@ typedef enum {
     KDA_ERR_WORKSPACE = -3,    /* workspace missing or smaller than the query */
     KDA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
     KDA_ERR_TIMEOUT = -5,      /* a device-side bounded wait gave up */
-    KDA_ERR_RANGE = -6         /* bf16 forward: a chunk's total log-decay beyond the range its
-                                  rescaled tiles represent (see kda_chunk_fwd) */
+    KDA_ERR_RANGE = -6         /* reserved: a log-decay beyond a kernel's range (no kernel of
+                                  this version has such a limit; see kda_chunk_fwd) */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -148,12 +148,18 @@ size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
  * values up to bf16 rounding (the record form applies beta to the rows of L
  * after the Gram product, the single kernel to the bf16 K<- operand before it).
  *
- * The bf16 path rescales each chunk's tiles by Gamma and 1/Gamma in float32
- * (page "Gated Linear Attention", section 5.2), so a chunk's total log-decay,
- * sum of g over its 64 tokens, must stay above -100 ln 2 (about -69); a chunk
- * past that is detected on the device and recorded as KDA_ERR_RANGE for
- * kda_status_read (its outputs are then undefined).  float32 inputs have no
- * such limit (their Gram is formed in the log domain, section 5.3).
+ * The decay has no range limit.  The bf16 path forms a chunk's Gram with one
+ * tensor-core product over tiles rescaled by Gamma and 1/Gamma (page "Gated
+ * Linear Attention", section 5.2) while the chunk's total log-decay, sum of g
+ * over its 64 tokens, stays above -100 ln 2 (about -69) in every channel; a
+ * chunk past that (detected on the device, chunk by chunk) takes that page's
+ * secondary chunking (section 5.3): 16-token sub-chunks, products between
+ * sub-chunks against a per-sub-chunk reference, pairs within a sub-chunk
+ * element by element in float32.  float32 inputs form every Gram in the log
+ * domain.  In the single-kernel form such a chunk makes the call take a
+ * second launch (the first notes the call in word 8 of the status block, the
+ * second redoes the call with the sub-chunk Gram; without such a chunk the
+ * second launch exits at once); a captured graph replays both.
  */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 

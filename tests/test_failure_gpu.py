@@ -8,8 +8,6 @@
   (default budget) must match the oracle: the context and the library are
   unharmed.  Both forms (chunk records + scan; the single kernel, with and
   without the two-CTA pair) are covered.
-* A chunk whose total log-decay is past the range of the rescaled bf16 tiles:
-  recorded as KDA_ERR_RANGE instead of inf / NaN outputs going unreported.
 """
 import ctypes
 
@@ -83,20 +81,9 @@ def test_generous_budget_changes_nothing():
 
 
 @pytest.mark.parametrize("form", ["records", "single"])
-def test_strong_decay_is_reported_not_silent(form):
-    """g = -3 softplus(N(0, 1)): a 64-token chunk's log-decay reaches about -150, past the bf16 tiles'
-    range; the status word says so (the float32 path handles this case, see the parity tests)."""
-    lib = _lib.load()
-    x = _inputs(256, 128, seed=23, g_scale=30.0)
-    assert float(x["g"].double()[:, :64].sum(1).min()) < -100.0
-    st, _, _ = _call(lib, x, form, budget=0)
-    assert st == _lib.KDA_ERR_RANGE, _lib.status_string(st)
-
-
-@pytest.mark.parametrize("form", ["records", "single"])
 def test_decay_within_range_matches_oracle(form):
-    """Stronger decay than the workloads' (g = -0.6 softplus(N(0, 1)), about -31 per chunk on average)
-    but inside the range: no status, and parity with the oracle."""
+    """Stronger decay than the workloads' (g = -0.6 softplus(N(0, 1)), about -31 per chunk on average),
+    still within the one-product Gram's range: no status, and parity with the oracle."""
     lib = _lib.load()
     x = _inputs(512, 128, seed=24, g_scale=6.0)
     chunk_sums = x["g"].double().reshape(2, 8, 64, 2, 128).sum(2)

@@ -98,6 +98,66 @@ def test_fp32_strong_decay(variant):
     assert rel(o, ro) <= 1e-5 and rel(ht, rh) <= 1e-5
 
 
+# ---------------------------------------------------------------- bf16: decay past the one-product Gram
+def _run_form(x, variant, form):
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    gate = {"kda": "channel", "gla": "channel", "gdn": "scalar", "deltanet": "none"}[variant]
+    ws = _small_workspace() if form == "single" else None
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d.get("g"), d.get("beta"), d.get("h0"), gate=gate,
+                          scale_v=x["scale_v"], workspace=ws)
+    torch.cuda.synchronize()
+    return o.double().cpu().numpy(), ht.double().cpu().numpy()
+
+
+def _scaled_gate(x, chunk_scales):
+    """g times chunk_scales[n] on the rows of 64-token chunk n (the last scale holds to the end)."""
+    g = x["g"].double()
+    T = g.shape[1]
+    for n in range(0, T, 64):
+        g[:, n:n + 64] *= chunk_scales[min(n // 64, len(chunk_scales) - 1)]
+    x["g"] = g.to(x["g"].dtype)
+    return x
+
+
+@pytest.mark.parametrize("form", ["records", "single"])
+@pytest.mark.parametrize("variant", ["kda", "gdn", "gla"])
+def test_bf16_strong_decay(variant, form):
+    """g = -3 softplus(N(0,1)), T = 300 (a ragged tail): a 64-token chunk's log-decay reaches about
+    -150, where the one-product Gram's K / Gamma overflows; those chunks take the sub-chunk Gram
+    (GLA page, section 5.3) and match the oracle within the bf16 tolerance."""
+    x = _scaled_gate(make_inputs(custom(variant, 2, 300, 2, 128, 128, dtype=torch.bfloat16, h0=True), seed=25),
+                     [30.0])
+    assert float(x["g"].double()[:, :64].sum(1).min()) < -100.0
+    o, ht = _run_form(x, variant, form)
+    ro, rh = run_oracle(x, variant)
+    assert np.isfinite(o).all() and np.isfinite(ht).all()
+    assert rel(o, ro) <= 5e-3 and rel(ht, rh) <= 5e-3, (rel(o, ro), rel(ht, rh))
+
+
+@pytest.mark.parametrize("form,dv", [("records", 128), ("single", 128), ("single", 64)])
+def test_bf16_mixed_decay_chunks(form, dv):
+    """Strong and ordinary chunks interleaved in one sequence (each chunk picks its Gram form; with
+    dv = 128 the two CTAs of a pair build alternate chunks), T = 450."""
+    x = _scaled_gate(make_inputs(custom("kda", 2, 450, 2, 128, dv, dtype=torch.bfloat16, h0=True), seed=26),
+                     [30.0, 1.0, 1.0, 30.0, 30.0, 1.0, 30.0, 1.0])
+    o, ht = _run_form(x, "kda", form)
+    ro, rh = run_oracle(x, "kda")
+    assert rel(o, ro) <= 5e-3 and rel(ht, rh) <= 5e-3, (rel(o, ro), rel(ht, rh))
+
+
+@pytest.mark.parametrize("form", ["records", "single"])
+@pytest.mark.parametrize("variant", ["kda", "gdn"])
+def test_bf16_extreme_decay(variant, form):
+    """g = -20 on every token and channel: a 16-token sub-chunk alone spans -320, so even the
+    sub-chunk references cannot factor the diagonal blocks; those are formed element by element."""
+    x = make_inputs(custom(variant, 1, 200, 2, 128, 128, dtype=torch.bfloat16, h0=True), seed=27)
+    x["g"] = torch.full_like(x["g"], -20.0)
+    o, ht = _run_form(x, variant, form)
+    ro, rh = run_oracle(x, variant)
+    assert np.isfinite(o).all() and np.isfinite(ht).all()
+    assert rel(o, ro) <= 5e-3 and rel(ht, rh) <= 5e-3, (rel(o, ro), rel(ht, rh))
+
+
 # ---------------------------------------------------------------- bf16 tensor-core path
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 200, 512])
 def test_bf16_kda_lengths(T):
