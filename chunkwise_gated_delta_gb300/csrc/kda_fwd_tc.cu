@@ -1460,7 +1460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o) {
-    if (STRONG && *reinterpret_cast<volatile const int *>(p.status + kStatusStrongWord) != p.strong_token) return;
+    if (STRONG) {
+        grid_dep_wait();                    // the first launch of the call is done and visible
+        if (*reinterpret_cast<volatile const int *>(p.status + kStatusStrongWord) != p.strong_token) return;
+    } else {
+        grid_dep_launch();                  // the second launch may take SMs as this one's blocks finish
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctx c;
@@ -2077,28 +2082,40 @@ cudaError_t launch_single_one(const FwdParams &p, const CUtensorMap &q, const CU
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = kSmemBytes;
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = STRONG ? 2 : 1;
         return cudaLaunchKernelEx(&cfg, kern, p, q, k, g, v, o);
       }
     }
     auto kern = kda_fwd_tc_kernel<GATE, GLA, false, STRONG, Tg>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, s>>>(p, q, k, g, v, o);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = STRONG ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p, q, k, g, v, o);
 }
 
 // The single kernel as two launches: the first, with only the one-product Gram, notes a chunk
 // whose decay is past its range; the second redoes the whole call with the sub-chunk Gram if the
 // first noted one, and exits at once otherwise.  (The sub-chunk path compiled into the first
-// kernel would cost it registers in its chunk loop; the second launch costs a few microseconds.)
-// GATE_NONE has no decay: one launch.
+// kernel would cost it registers in its chunk loop; the second launch costs a few microseconds,
+// fewer as a programmatic dependent launch, whose blocks take SMs as the first launch's finish
+// and wait for its completion in the hardware.)  GATE_NONE has no decay: one launch.
 template <int GATE, bool GLA, typename Tg>
 cudaError_t launch_single(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
                           const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
