@@ -319,23 +319,27 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
 
 // ------------------------------------------------------------------ kernel B
 // The reverse scan from the chunk records: dU = K~ dS^T + P^T dO,
-// dS <- dS Diag(gamma^C) + dO^T Q<- - dU^T W.
+// dS <- dS Diag(gamma^C) + dO^T Q<- - dU^T W.  One CTA per (64-wide value slice, head,
+// sequence): the records of a head are read by dv / 64 CTAs, and the records and dO rows of
+// chunk n - 1 travel (cp.async, double buffer) while chunk n computes.
+constexpr int kDVD = 64;     // value rows per CTA in the reverse scan
+template <int DK, typename Tin>
+__host__ __device__ constexpr int dstate_buf_floats() {
+    // W, Q<-, K~ [C][SK]; P [C][SC]; gamma^C [DK]; raw dO rows [C][DVD] of Tin
+    return 3 * kC * pad4(DK) + kC * kSC4 + DK + (kC * kDVD * (int)sizeof(Tin) + 3) / 4;
+}
 template <int DK, int DV, typename Tin, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS), SC = kSC4;
+    constexpr int SK = pad4(DK), SV = pad4(kDVD), SC = kSC4, BUF = dstate_buf_floats<DK, Tin>();
     using R = Rec<DK, DV>;
     extern __shared__ float smem[];
-    float *Wm = smem;                  // [C][SK]
-    float *QL = Wm + kC * SK;          // [C][SK]
-    float *KT = QL + kC * SK;          // [C][SK]
-    float *dS = KT + kC * SK;          // [DVS][SK]
-    float *Pm = dS + kDVS * SK;        // [C][SC]
-    float *dO = Pm + kC * SC;          // [C][SV]
+    float *dS = smem;                  // [DVD][SK]
+    float *dO = dS + kDVD * SK;        // [C][SV]
     float *dU = dO + kC * SV;          // [C][SV]
-    float *gam = dU + kC * SV;         // [DK]
+    float *bufs = dU + kC * SV;        // 2 x BUF
 
     const int tid = threadIdx.x;
-    const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
+    const int e0 = blockIdx.x * kDVD, h = blockIdx.y, b = blockIdx.z;
     const int H = p.H, dv = p.dv;
     const Seq sq = seq_of(p, b);
     const int N = sq.nch;
@@ -344,29 +348,44 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
     float *dSws = p.ws_dS + chunk_index(p, sq, h, 0) * dv * DK;
     const float *recs = p.ws_prep + chunk_index(p, sq, h, 0) * rec_floats(DK, DV);
     float *dus = p.ws_du + chunk_index(p, sq, h, 0) * kC * dv;
+    // buffer (n & 1) holds chunk n's tiles
+    auto issue = [&](int n) {
+        const float *rec = recs + (size_t)n * rec_floats(DK, DV);
+        float *bf = bufs + (n & 1) * BUF;
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::W, DK, bf);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::QL, DK, bf + kC * SK);
+        wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::KT, DK, bf + 2 * kC * SK);
+        wg::load_tile_async<kC, kC, SC, kThreads>(rec + R::P, kC, bf + 3 * kC * SK);
+        wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 3 * kC * SK + kC * SC);
+        const int t0 = n * kC;
+        wg::load_raw_async<kC, kDVD, Tin, kThreads>(dop + (((size_t)sq.row0 + t0) * H + h) * dv + e0,
+                                                    (size_t)H * dv, min(kC, sq.len - t0),
+                                                    reinterpret_cast<Tin *>(bf + 3 * kC * SK + kC * SC + DK));
+    };
 
-    for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+    for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         dS[e * SK + d] = p.grad_ht ? p.grad_ht[(head * dv + e0 + e) * DK + d] : 0.f;
     }
+    if (N > 0) issue(N - 1);
+    wg::cp_async_commit();
     for (int n = N - 1; n >= 0; --n) {
-        const int t0 = n * kC, nvalid = min(kC, sq.len - t0);
-        const float *rec = recs + (size_t)n * rec_floats(DK, DV);
-        __syncthreads();
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+        float *Wm = bufs + (n & 1) * BUF, *QL = Wm + kC * SK, *KT = QL + kC * SK, *Pm = KT + kC * SK;
+        float *gam = Pm + kC * SC;
+        const Tin *draw = reinterpret_cast<const Tin *>(gam + DK);
+        __syncthreads();               // dS is final for chunk n; chunk n + 1's buffer is free
+        for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             dSws[((size_t)n * dv + e0 + e) * DK + d] = dS[e * SK + d];
         }
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::W, DK, kC, Wm);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::QL, DK, kC, QL);
-        wg::load_tile<kC, DK, SK, kThreads>(rec + R::KT, DK, kC, KT);
-        wg::load_tile<kC, kC, SC, kThreads>(rec + R::P, kC, kC, Pm);
-        wg::load_tile<kC, kDVS, SV, kThreads>(dop + (((size_t)sq.row0 + t0) * H + h) * dv + e0, (size_t)H * dv,
-                                              nvalid, dO);
-        for (int d = tid; d < DK; d += kThreads) gam[d] = rec[R::GC + d];
+        if (n > 0) issue(n - 1);
+        wg::cp_async_commit();         // (an empty group on the last step keeps the count)
+        wg::cp_async_wait<1>();        // chunk n's tiles have landed (this thread's copies)
+        __syncthreads();               // ... and everyone's
+        wg::to_f32<kC, kDVD, SV, Tin, kThreads>(draw, dO);
         __syncthreads();
         float *du = dus + (size_t)n * kC * dv + e0;       // dU rows of this chunk
-        wg::gemm2<kDVS, TF32>(
+        wg::gemm2<kDVD, TF32>(
             DK, [&](int i, int d) { return KT[i * SK + d]; }, [&](int d, int e) { return dS[e * SK + d]; }, kC,
             [&](int i, int j) { return Pm[j * SC + i]; }, [&](int j, int e) { return dO[j * SV + e]; },
             [&](int i, int e, float x) {
@@ -374,14 +393,17 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
                 du[(size_t)i * dv + e] = x;
             });
         __syncthreads();
-        wg::gemm2<DK, TF32>(
-            kC, [&](int e, int c) { return dO[c * SV + e]; }, [&](int c, int d) { return QL[c * SK + d]; }, kC,
-            [&](int e, int c) { return -dU[c * SV + e]; }, [&](int c, int d) { return Wm[c * SK + d]; },
-            [&](int e, int d, float x) { dS[e * SK + d] = dS[e * SK + d] * gam[d] + x; });
+        // dS rows e of the slice, 32 at a time
+#pragma unroll
+        for (int eo = 0; eo < kDVD; eo += 32)
+            wg::gemm2<DK, TF32>(
+                kC, [&](int e, int c) { return dO[c * SV + eo + e]; }, [&](int c, int d) { return QL[c * SK + d]; },
+                kC, [&](int e, int c) { return -dU[c * SV + eo + e]; }, [&](int c, int d) { return Wm[c * SK + d]; },
+                [&](int e, int d, float x) { dS[(eo + e) * SK + d] = dS[(eo + e) * SK + d] * gam[d] + x; });
     }
     __syncthreads();
     if (p.grad_h0) {
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+        for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             p.grad_h0[(head * dv + e0 + e) * DK + d] = dS[e * SK + d];
         }
@@ -649,9 +671,9 @@ template <int DK>
 constexpr size_t states_smem_bytes() {
     return sizeof(float) * ((size_t)kDVS * pad4(DK) + 2 * states_buf_floats<DK>());
 }
-template <int DK>
+template <int DK, typename Tin>
 constexpr size_t dstate_smem_bytes() {
-    return sizeof(float) * ((size_t)3 * kC * pad4(DK) + kDVS * pad4(DK) + kC * kSC4 + 2 * kC * pad4(kDVS) + DK);
+    return sizeof(float) * ((size_t)kDVD * pad4(DK) + 2 * kC * pad4(kDVD) + 2 * dstate_buf_floats<DK, Tin>());
 }
 
 template <typename F>
@@ -664,17 +686,19 @@ cudaError_t launch_all(const BwdParams &p, cudaStream_t s) {
     constexpr bool kTf32 = sizeof(Tin) == 2;        // bf16 inputs: tf32 tensor-core products
     const bool packed = p.cu_seqlens != nullptr;
     cudaError_t e;
-    const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK>();
+    const size_t sp = prep_smem_bytes<DK, DV>(), sa = states_smem_bytes<DK>(), sb = dstate_smem_bytes<DK, Tin>();
+    static_assert(dstate_smem_bytes<128, float>() <= 227 * 1024, "kernel B shared memory");
     const size_t sc = sizeof(float) * grad_smem_floats<DK, DV>();
     static_assert(sizeof(float) * grad_smem_floats<128, 128>() <= 227 * 1024, "kernel C shared memory");
     if ((e = set_smem(kda_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32>, sp)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_states_kernel<DK, DV, kTf32>, sa)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_dstate_kernel<DK, DV, Tin, kTf32>, sb)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
-    const dim3 gscan(p.dv / kDVS, p.H, p.B), gchunk = seq::chunk_grid<kC>(p.B, p.T, p.H, packed);
+    const dim3 gscan(p.dv / kDVS, p.H, p.B), gback(p.dv / kDVD, p.H, p.B);
+    const dim3 gchunk = seq::chunk_grid<kC>(p.B, p.T, p.H, packed);
     kda_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sp, s>>>(p);
     kda_bwd_states_kernel<DK, DV, kTf32><<<gscan, kThreads, sa, s>>>(p);
-    kda_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sb, s>>>(p);
+    kda_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gback, kThreads, sb, s>>>(p);
     kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreadsC, sc, s>>>(p);
     return cudaGetLastError();
 }
