@@ -40,7 +40,6 @@ namespace kda {
 namespace {
 
 constexpr int kC = 32;       // chunk length
-constexpr int kDVS = 32;     // value rows per CTA in the scans
 constexpr int kThreads = 256;
 constexpr int kThreadsC = 512;   // the gradient kernel: 16 warps to hide the latency of its L2 reads
 
@@ -248,22 +247,23 @@ constexpr size_t prep_smem_bytes() {
 
 // ------------------------------------------------------------------ kernel A
 // The forward state scan from the chunk records: V_new = U - W S^T,
-// S <- S Diag(gamma^C) + V_new^T K~.  One CTA per (32-wide value slice, head, sequence).
+// S <- S Diag(gamma^C) + V_new^T K~.  One CTA per (64-wide value slice, head, sequence).
 // The records of chunk n + 1 travel (cp.async, double buffer) while chunk n computes.
+constexpr int kDVD = 64;     // value rows per CTA in the two scans
 template <int DK>
 __host__ __device__ constexpr int states_buf_floats() {
-    return 2 * kC * pad4(DK) + kC * pad4(kDVS) + DK;       // W, K~, U (then V_new), gamma^C
+    return 2 * kC * pad4(DK) + kC * pad4(kDVD) + DK;       // W, K~, U (then V_new), gamma^C
 }
 template <int DK, int DV, bool TF32>
 __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParams p) {
-    constexpr int SK = pad4(DK), SV = pad4(kDVS), BUF = states_buf_floats<DK>();
+    constexpr int SK = pad4(DK), SV = pad4(kDVD), BUF = states_buf_floats<DK>();
     using R = Rec<DK, DV>;
     extern __shared__ float smem[];
     float *Sm = smem;                  // [DVS][SK]
-    float *bufs = Sm + kDVS * SK;      // 2 x BUF
+    float *bufs = Sm + kDVD * SK;      // 2 x BUF
 
     const int tid = threadIdx.x;
-    const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
+    const int e0 = blockIdx.x * kDVD, h = blockIdx.y, b = blockIdx.z;
     const int H = p.H, dv = p.dv;
     const Seq sq = seq_of(p, b);
     const int N = sq.nch;
@@ -276,11 +276,11 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
         float *bf = bufs + (n & 1) * BUF;
         wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::W, DK, bf);
         wg::load_tile_async<kC, DK, SK, kThreads>(rec + R::KT, DK, bf + kC * SK);
-        wg::load_tile_async<kC, kDVS, SV, kThreads>(rec + R::U + e0, DV, bf + 2 * kC * SK);
+        wg::load_tile_async<kC, kDVD, SV, kThreads>(rec + R::U + e0, DV, bf + 2 * kC * SK);
         wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 2 * kC * SK + kC * SV);
     };
 
-    for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+    for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         Sm[e * SK + d] = p.h0 ? p.h0[(head * dv + e0 + e) * DK + d] : 0.f;
     }
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
     for (int n = 0; n < N; ++n) {
         float *Wm = bufs + (n & 1) * BUF, *KT = Wm + kC * SK, *Um = KT + kC * SK, *gam = Um + kC * SV;
         __syncthreads();               // S is final for chunk n; chunk n - 1's buffer is free
-        for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+        for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
             const int e = idx / DK, d = idx % DK;
             Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
         }
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
         wg::cp_async_wait<1>();        // chunk n's tiles have landed (this thread's copies)
         __syncthreads();               // ... and everyone's
         float *vn = vnew + (size_t)n * kC * dv + e0;     // V_new rows of this chunk
-        wg::gemm<kDVS, TF32>(
+        wg::gemm<kDVD, TF32>(
             DK, [&](int i, int d) { return Wm[i * SK + d]; }, [&](int d, int e) { return Sm[e * SK + d]; },
             [&](int i, int e, float x) {
                 const float y = Um[i * SV + e] - x;
@@ -306,12 +306,15 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
                 vn[(size_t)i * dv + e] = y;
             });
         __syncthreads();
-        wg::gemm<DK, TF32>(
-            kC, [&](int e, int c) { return Um[c * SV + e]; }, [&](int c, int d) { return KT[c * SK + d]; },
-            [&](int e, int d, float x) { Sm[e * SK + d] = Sm[e * SK + d] * gam[d] + x; });
+        // S rows e of the slice, 32 at a time
+#pragma unroll
+        for (int eo = 0; eo < kDVD; eo += 32)
+            wg::gemm<DK, TF32>(
+                kC, [&](int e, int c) { return Um[c * SV + eo + e]; }, [&](int c, int d) { return KT[c * SK + d]; },
+                [&](int e, int d, float x) { Sm[(eo + e) * SK + d] = Sm[(eo + e) * SK + d] * gam[d] + x; });
     }
     __syncthreads();
-    for (int idx = tid; idx < kDVS * DK; idx += kThreads) {
+    for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
         const int e = idx / DK, d = idx % DK;
         Sws[((size_t)N * dv + e0 + e) * DK + d] = Sm[e * SK + d];
     }
@@ -322,7 +325,6 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
 // dS <- dS Diag(gamma^C) + dO^T Q<- - dU^T W.  One CTA per (64-wide value slice, head,
 // sequence): the records of a head are read by dv / 64 CTAs, and the records and dO rows of
 // chunk n - 1 travel (cp.async, double buffer) while chunk n computes.
-constexpr int kDVD = 64;     // value rows per CTA in the reverse scan
 template <int DK, typename Tin>
 __host__ __device__ constexpr int dstate_buf_floats() {
     // W, Q<-, K~ [C][SK]; P [C][SC]; gamma^C [DK]; raw dO rows [C][DVD] of Tin
@@ -669,7 +671,7 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
 
 template <int DK>
 constexpr size_t states_smem_bytes() {
-    return sizeof(float) * ((size_t)kDVS * pad4(DK) + 2 * states_buf_floats<DK>());
+    return sizeof(float) * ((size_t)kDVD * pad4(DK) + 2 * states_buf_floats<DK>());
 }
 template <int DK, typename Tin>
 constexpr size_t dstate_smem_bytes() {
@@ -694,11 +696,11 @@ cudaError_t launch_all(const BwdParams &p, cudaStream_t s) {
     if ((e = set_smem(kda_bwd_states_kernel<DK, DV, kTf32>, sa)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_dstate_kernel<DK, DV, Tin, kTf32>, sb)) != cudaSuccess) return e;
     if ((e = set_smem(kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32>, sc)) != cudaSuccess) return e;
-    const dim3 gscan(p.dv / kDVS, p.H, p.B), gback(p.dv / kDVD, p.H, p.B);
+    const dim3 gscan(p.dv / kDVD, p.H, p.B);
     const dim3 gchunk = seq::chunk_grid<kC>(p.B, p.T, p.H, packed);
     kda_bwd_prep_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreads, sp, s>>>(p);
     kda_bwd_states_kernel<DK, DV, kTf32><<<gscan, kThreads, sa, s>>>(p);
-    kda_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gback, kThreads, sb, s>>>(p);
+    kda_bwd_dstate_kernel<DK, DV, Tin, kTf32><<<gscan, kThreads, sb, s>>>(p);
     kda_bwd_grad_kernel<DK, DV, Tin, Tg, kTf32><<<gchunk, kThreadsC, sc, s>>>(p);
     return cudaGetLastError();
 }
