@@ -1720,42 +1720,48 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
 // ============================================================================
 // Record scan kernel: the state recursion over the chunk records.
 // ============================================================================
-// One CTA per (64-wide value slice, head, sequence).  The records carry every
+// One CTA per (value slice, head, sequence).  The records carry every
 // state-independent operand, so a chunk takes three products:
 //   D1 = Z V = [U ; P U]                  (issued by the loader, one chunk ahead)
 //   D1 += A_chain S^T = [V_new ; O]       (the state product)
 //   dS^T = K~^T V_new,   S <- S Diag(gamma^C) + dS
-// The slice's values are split into NH halves of W = 64 / NH, each a chain of
-// four warps with its own accumulator columns, S^T and V_new tiles and
-// barriers, so the halves can run out of step.  Warp 4 NH loads the records
-// (bulk copies) and the v tiles (TMA) and issues Z V.  A record takes about a
-// chunk's time to arrive, so A_chain, K~, gamma^C and v of chunk n go to entry
-// n % 3 of a three-deep ring, loaded three chunks ahead, and Z V of chunk n
-// runs two chunks ahead into accumulator slot n % 3, its Z from entry n % 2 of
-// a two-deep ring.  V_new takes the front of the half's S^T tile, which the
-// state product has read by then.
-// NH = 2 (two 32-wide halves, MN-major B tiles with 64-byte swizzle) gives the same
-// values and measured no faster: the halves run in step, the products' latency
-// dominates, not the register work between them.
-constexpr int kScanHalves = 1;
-template <int NH> struct ScanCfg {
-    static constexpr int W = 64 / NH;                    // values per half
+// The CTA's SV = NH W values are split into NH halves of W, each a chain of four
+// warps with its own accumulator columns, S^T and V_new tiles and barriers, so
+// the halves can run out of step.  Warp 4 NH loads the records (bulk copies)
+// and the v tiles (TMA) and issues Z V for the whole slice.  A record takes
+// about a chunk's time to arrive, so A_chain, K~, gamma^C and v of chunk n go
+// to entry n % RD of an RD-deep ring, loaded RD chunks ahead, and Z V of chunk
+// n runs up to two chunks ahead into accumulator slot n % RD, its Z from entry
+// n % 2 of a two-deep ring.  V_new takes the front of the half's S^T tile,
+// which the state product has read by then.
+//   Configurations: one 64-wide slice (NH = 1, W = 64, RD = 3); both slices of
+// a dv = 128 head in one CTA (NH = 2, W = 64, RD = 2: the record and Z tiles
+// serve both halves, half the CTAs, for batches of more heads than one wave
+// of SMs holds).  Two 32-wide halves of a 64-wide slice (NH = 2, W = 32, RD =
+// 3, MN-major B tiles with 64-byte swizzle) give the same values and measured
+// no faster: the halves run in step, the products' latency dominates.
+template <int NH_, int W_, int RD_> struct ScanCfg {
+    static constexpr int NH = NH_, W = W_, RD = RD_;
+    static constexpr int SV = NH * W;                    // values per CTA
     static constexpr int kThreads = 128 * NH + 32;
-    static constexpr uint32_t R_SLOT = 57344;            // ring entry: A_chain, K~, v
     static constexpr uint32_t R_ACH = 0, R_KT = 32768, R_V = 49152;
-    static constexpr uint32_t OFF_Z = 3 * R_SLOT;        // two entries: Z
-    static constexpr uint32_t OFF_ST = OFF_Z + 2 * 16384;    // S^T (then V_new) of each half, 16 KB in all
-    static constexpr uint32_t OFF_GC = OFF_ST + 16384;   // gamma^C [3][128] f32
+    static constexpr uint32_t R_SLOT = R_V + 128u * SV;  // ring entry: A_chain, K~, v (64 rows x SV)
+    static constexpr uint32_t OFF_Z = RD * R_SLOT;       // two entries: Z
+    static constexpr uint32_t OFF_ST = OFF_Z + 2 * 16384;    // S^T (then V_new) of each half, 256 SV bytes in all
+    static constexpr uint32_t OFF_GC = OFF_ST + 256u * SV;   // gamma^C [RD][128] f32
     static constexpr uint32_t OFF_BAR = OFF_GC + 1536;   // mbarriers
     static constexpr uint32_t OFF_TSLOT = OFF_BAR + 256;
     static constexpr uint32_t OFF_ABORT = OFF_TSLOT + 4;
     static constexpr uint32_t kSmem = OFF_ABORT + 60 + 1024;   // + alignment slack of the dynamic base
-    static constexpr uint32_t kRTx = 32768u + 16384u + 512u + 8192u, kZTx = 16384u;
+    static constexpr uint32_t kRTx = 32768u + 16384u + 512u + 128u * SV, kZTx = 16384u;
+    // TMEM: [U ; P U] -> [V_new ; O] in RD slots of SV columns (half h at + h W), then dS^T
+    static constexpr uint32_t TS_D1 = 0, TS_DS = RD * SV;
+    static constexpr uint32_t kTmemCols = (RD + 1) * SV <= 256 ? 256 : 512;
+    static_assert(RD >= 2 && RD <= 3 && (RD + 1) * SV <= 512, "scan configuration");
+    static_assert(kSmem <= 232448, "shared memory per CTA");
 };
-static_assert(ScanCfg<kScanHalves>::kSmem <= 232448, "shared memory per CTA");   // the same for NH = 1, 2
-constexpr uint32_t kScanTmemCols = 256;
-constexpr uint32_t TS_D1 = 0;      // [U ; P U] -> [V_new ; O], 3 slots x 64 columns (half h: + h W)
-constexpr uint32_t TS_DS = 192;    // dS^T, half h at + h W
+using ScanSlice = ScanCfg<1, 64, 3>;     // one 64-wide value slice per CTA
+using ScanHead = ScanCfg<2, 64, 2>;      // both slices of a dv = 128 head per CTA
 
 // Ring entry / accumulator slot n % 3: FULLR, RFREE (one arrival per half), ZV, D1FREE (one
 // arrival per half); Z entry n % 2: FULLZ; C1 / C2: [half][chunk parity].
@@ -1801,11 +1807,11 @@ template <int W> __device__ __forceinline__ void tmem_ld_half(uint32_t taddr, fl
 
 // One half's chain: thread t of the half owns key channel t (its TMEM lane) and
 // the W state values S[ev0 .. ev0 + W)[t] in registers.
-template <int NH>
+template <class G>
 __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, int h, int b, Seq sq,
                            int nchunks) {
-    using G = ScanCfg<NH>;
-    constexpr int W = G::W;
+    constexpr int W = G::W, RD = G::RD, SV = G::SV;
+    constexpr int PW = G::NH == 2 && W == 64 ? 32 : W;   // columns per TMEM load
     uint8_t *base = c.base;
     const int t = threadIdx.x - 128 * half;
     const int warp = t >> 5;                             // TMEM lane quarter
@@ -1814,7 +1820,7 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
     const int ev0 = e0 + half * W;
     const int H = p.H, dv = p.dv;
     const int bar_id = 1 + half;
-    uint8_t *st = base + G::OFF_ST + half * 8192;
+    uint8_t *st = base + G::OFF_ST + half * 128 * W * 2;
     uint8_t *vn = st;                                    // V_new: 64 rows at the front of the S^T tile
     const float *gc = reinterpret_cast<const float *>(base + G::OFF_GC);
     const uint32_t col = (uint32_t)(half * W);
@@ -1833,8 +1839,8 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
 
     const uint32_t id1 = idesc_bf16(128, W, 0, 1), id2 = idesc_bf16(128, W, 1, 1);
     for (int n = 0; n < nchunks; ++n) {
-        const int s = n & 1, ri = n % 3;
-        const uint32_t ph = (uint32_t)((n >> 1) & 1), phr = (uint32_t)((n / 3) & 1);
+        const int s = n & 1, ri = n % RD;
+        const uint32_t ph = (uint32_t)((n >> 1) & 1), phr = (uint32_t)((n / RD) & 1);
         uint8_t *slot = base + ri * G::R_SLOT;
         wait_bar(c, SB_FULLR + ri, phr);                 // A_chain, K~ and gamma^C of the record
         wait_bar(c, SB_ZV + ri, phr);                    // D1[ri] = [U ; P U]
@@ -1846,7 +1852,8 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
             const uint32_t a0 = smem_u32(slot + G::R_ACH), b0 = smem_u32(st);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(c.tmem + TS_D1 + ri * 64 + col, desc_kmajor(a0, 128, ks), desc_half<W>(b0, 128, ks), id1, 1);
+                mma_bf16(c.tmem + G::TS_D1 + ri * SV + col, desc_kmajor(a0, 128, ks), desc_half<W>(b0, 128, ks), id1,
+                         1);
             mma_commit(c.bars + SB_C1 + half * 2 + s);
         }
         __syncwarp();
@@ -1856,10 +1863,35 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
         // ---- rows 0-63 (warps 0, 1): V_new -> the half's V_new tile, then dS^T = K~^T V_new;
         //      rows 64-127 (warps 2, 3): O -> o, stored while that product runs
         {
-            float v[W];
-            tmem_ld_half<W>(c.tmem + TS_D1 + ri * 64 + col + lane_base, v);
+            // in pieces of PW columns: with two 64-wide halves a whole row would not fit the registers
             const int r = (warp & 1) * 32 + (t & 31);
-            if (warp < 2) store_half_row<W>(vn, 64, r, v);
+            float v[W];
+            if constexpr (PW == W) {
+                tmem_ld_half<W>(c.tmem + G::TS_D1 + ri * SV + col + lane_base, v);
+                if (warp < 2) store_half_row<W>(vn, 64, r, v);
+            } else {
+                // the O rows (warps 2, 3) go out piece by piece at once
+#pragma unroll
+                for (int pc = 0; pc < W / PW; ++pc) {
+                    float u[PW];
+                    tmem_ld32(c.tmem + G::TS_D1 + ri * SV + col + pc * PW + lane_base, u);
+                    if (warp < 2) {
+#pragma unroll
+                        for (int q = 0; q < PW / 8; ++q)
+                            st_u128(vn + sw128_offset(64, r, pc * PW + 8 * q), pack_bf16(u[8 * q], u[8 * q + 1]),
+                                    pack_bf16(u[8 * q + 2], u[8 * q + 3]), pack_bf16(u[8 * q + 4], u[8 * q + 5]),
+                                    pack_bf16(u[8 * q + 6], u[8 * q + 7]));
+                    } else if (n * kC + r < sq.len) {
+                        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
+                                              (((size_t)sq.bt * p.T + sq.t0 + n * kC + r) * H + h) * dv + ev0 + pc * PW;
+#pragma unroll
+                        for (int q = 0; q < PW / 8; ++q)
+                            *reinterpret_cast<uint4 *>(orow + 8 * q) =
+                                make_uint4(pack_bf16(u[8 * q], u[8 * q + 1]), pack_bf16(u[8 * q + 2], u[8 * q + 3]),
+                                           pack_bf16(u[8 * q + 4], u[8 * q + 5]), pack_bf16(u[8 * q + 6], u[8 * q + 7]));
+                    }
+                }
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(bar_id, 128);
@@ -1870,11 +1902,11 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
                 const uint32_t a0 = smem_u32(slot + G::R_KT), b0 = smem_u32(vn);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(c.tmem + TS_DS + col, desc_mnmajor(a0, 64, ks), desc_half<W>(b0, 64, ks), id2, ks > 0);
+                    mma_bf16(c.tmem + G::TS_DS + col, desc_mnmajor(a0, 64, ks), desc_half<W>(b0, 64, ks), id2, ks > 0);
                 mma_commit(c.bars + SB_C2 + half * 2 + s);
             }
             __syncwarp();
-            if (warp >= 2 && n * kC + r < sq.len) {
+            if (PW == W && warp >= 2 && n * kC + r < sq.len) {
                 __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
                                       (((size_t)sq.bt * p.T + sq.t0 + n * kC + r) * H + h) * dv + ev0;
 #pragma unroll
@@ -1888,11 +1920,14 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
         tc_fence_after();
         if (leader) mbar_arrive(c.bars + SB_RFREE + ri);  // this half is done with ring entry ri
         __syncwarp();
-        {
-            float v[W];
-            tmem_ld_half<W>(c.tmem + TS_DS + col + lane_base, v);
 #pragma unroll
-            for (int e = 0; e < W; ++e) S[e] = fmaf(gam, S[e], v[e]);   // S Diag(gamma^C) + dS, dS^T = K~^T V_new
+        for (int pc = 0; pc < W / PW; ++pc) {
+            float v[PW];
+            if constexpr (PW == W) tmem_ld_half<W>(c.tmem + G::TS_DS + col + lane_base, v);
+            else tmem_ld32(c.tmem + G::TS_DS + col + pc * PW + lane_base, v);
+#pragma unroll
+            for (int e = 0; e < PW; ++e)                // S Diag(gamma^C) + dS, dS^T = K~^T V_new
+                S[pc * PW + e] = fmaf(gam, S[pc * PW + e], v[e]);
         }
         write_state();
     }
@@ -1908,12 +1943,12 @@ __device__ void scan_chain(const Ctx &c, const FwdParams &p, int half, int e0, i
 }
 
 // The loader (one thread): chunk n's A_chain, K~, gamma^C and v tile into ring
-// entry n % 3, its Z into entry n % 2 of the Z ring, and D1[n % 3] = Z V as
-// soon as those are in and chunk n - 3 has drained the slot.
-template <int NH>
+// entry n % RD, its Z into entry n % 2 of the Z ring, and D1[n % RD] = Z V as
+// soon as those are in and chunk n - RD has drained the slot.
+template <class G>
 __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap *tm_v, int e0, int h, Seq sq,
                             int nchunks) {
-    using G = ScanCfg<NH>;
+    constexpr int RD = G::RD, SV = G::SV;
     uint8_t *base = c.base;
     // A ring entry is re-armed only after this thread's own wait on its previous copy (in zv)
     // ended with it landed: while `clean` (every wait of this thread so far did) it issues, after
@@ -1923,7 +1958,7 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
     bool clean = true;
     auto issue_r = [&](int n) {
         const uint8_t *r = c.zrec + (size_t)n * c.zstride;
-        const int ri = n % 3;
+        const int ri = n % RD;
         uint8_t *slot = base + ri * G::R_SLOT;
         uint64_t *bar = c.bars + SB_FULLR + ri;
         if (!clean) return;
@@ -1932,7 +1967,8 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
         bulk_load(slot + G::R_ACH, r + REC_A, 32768u, bar);
         bulk_load(slot + G::R_KT, r + REC_KR, 16384u, bar);
         bulk_load(base + G::OFF_GC + ri * 512, r + REC_GC, 512u, bar);
-        tma_load_4d(slot + G::R_V, tm_v, bar, e0, h, sq.t0 + n * kC, sq.bt);
+        for (int vb = 0; vb < SV / 64; ++vb)           // 64-wide column blocks of the v tile
+            tma_load_4d(slot + G::R_V + vb * 8192, tm_v, bar, e0 + 64 * vb, h, sq.t0 + n * kC, sq.bt);
     };
     auto issue_z = [&](int n) {
         const uint8_t *r = c.zrec + (size_t)n * c.zstride;
@@ -1943,20 +1979,20 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
         bulk_load(base + G::OFF_Z + (n & 1) * 16384, r + REC_Z, 16384u, bar);
     };
     auto zv = [&](int n) {
-        const int ri = n % 3;
-        clean &= wait_bar(c, SB_FULLR + ri, (uint32_t)((n / 3) & 1));        // v
+        const int ri = n % RD;
+        clean &= wait_bar(c, SB_FULLR + ri, (uint32_t)((n / RD) & 1));       // v
         clean &= wait_bar(c, SB_FULLZ + (n & 1), (uint32_t)((n >> 1) & 1));  // Z
-        if (n >= 3) wait_bar(c, SB_D1FREE + ri, (uint32_t)(((n - 3) / 3) & 1));   // chunk n - 3 drained D1[ri]
+        if (n >= RD) wait_bar(c, SB_D1FREE + ri, (uint32_t)(((n - RD) / RD) & 1));   // chunk n - RD drained D1[ri]
         tc_fence_after();
         const uint32_t a0 = smem_u32(base + G::OFF_Z + (n & 1) * 16384), b0 = smem_u32(base + ri * G::R_SLOT + G::R_V);
-        const uint32_t id = idesc_bf16(128, 64, 0, 1);
+        const uint32_t id = idesc_bf16(128, SV, 0, 1);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(c.tmem + TS_D1 + ri * 64, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
+            mma_bf16(c.tmem + G::TS_D1 + ri * SV, desc_kmajor(a0, 128, ks), desc_mnmajor(b0, 64, ks), id, ks > 0);
         mma_commit(c.bars + SB_ZV + ri);
     };
     if ((threadIdx.x & 31) == 0) {
-        for (int n = 0; n < 3 && n < nchunks; ++n) {
+        for (int n = 0; n < RD && n < nchunks; ++n) {
             issue_r(n);
             if (n < 2) issue_z(n);
         }
@@ -1964,18 +2000,19 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
         if (nchunks > 1) zv(1);
         for (int n = 0; n < nchunks; ++n) {
             if (n + 2 < nchunks) {
-                wait_bar(c, SB_ZV + n % 3, (uint32_t)((n / 3) & 1));     // Z V of chunk n has read its Z
+                wait_bar(c, SB_ZV + n % RD, (uint32_t)((n / RD) & 1));    // Z V of chunk n has read its Z
                 issue_z(n + 2);
             }
-            if (n + 3 < nchunks) {
-                wait_bar(c, SB_RFREE + n % 3, (uint32_t)((n / 3) & 1));  // chunk n is done with its entry
-                issue_r(n + 3);
+            if (n + RD < nchunks) {
+                wait_bar(c, SB_RFREE + n % RD, (uint32_t)((n / RD) & 1));  // chunk n is done with its entry
+                issue_r(n + RD);
             }
             if (n + 2 < nchunks) zv(n + 2);
         }
         // drain, also after a wait gave up: the newest copy into every entry has landed and every
         // product issued here is done before the CTA frees TMEM and exits
-        for (int m = last_r; m >= 0 && m > last_r - 3; --m) drain_bar(c, SB_FULLR + m % 3, (uint32_t)((m / 3) & 1));
+        for (int m = last_r; m >= 0 && m > last_r - RD; --m)
+            drain_bar(c, SB_FULLR + m % RD, (uint32_t)((m / RD) & 1));
         for (int m = last_z; m >= 0 && m > last_z - 2; --m) drain_bar(c, SB_FULLZ + (m & 1), (uint32_t)((m >> 1) & 1));
         mma_commit(c.bars + SB_FINL);
         drain_bar(c, SB_FINL, 0);
@@ -1983,10 +2020,10 @@ __device__ void scan_loader(const Ctx &c, const FwdParams &p, const CUtensorMap 
     __syncwarp();
 }
 
-template <int NH>
-__global__ void __launch_bounds__(ScanCfg<NH>::kThreads, 1)
+template <class G>
+__global__ void __launch_bounds__(G::kThreads, 1)
 kda_fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_v) {
-    using G = ScanCfg<NH>;
+    constexpr int NH = G::NH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctx c;
@@ -1998,14 +2035,14 @@ kda_fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_v)
     c.short_polls = c.bound != kWaitBound;
     c.rank = 0;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + G::OFF_TSLOT);
-    const int e0 = blockIdx.x * kDVS, h = blockIdx.y, b = blockIdx.z;
+    const int e0 = blockIdx.x * G::SV, h = blockIdx.y, b = blockIdx.z;
     const Seq sq = seq_of(p, b);
     const int nchunks = (sq.len + kC - 1) / kC;
     c.zrec = p.zrec + ((size_t)zslot0(p, b, sq) * p.H + h) * kRecBytes;
     c.zstride = (size_t)p.H * kRecBytes;
     if (nchunks == 0) {                     // empty sequence: ht = h0; nothing else is set up
         if (p.ht)
-            for (int i = threadIdx.x; i < kDVS * kDK; i += G::kThreads) {
+            for (int i = threadIdx.x; i < G::SV * kDK; i += G::kThreads) {
                 const size_t off = (((size_t)b * p.H + h) * p.dv + e0 + i / kDK) * kDK + i % kDK;
                 p.ht[off] = p.h0 ? p.h0[off] : 0.f;
             }
@@ -2020,7 +2057,7 @@ kda_fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_v)
         fence_proxy_async_smem();
     }
     if (threadIdx.x < 32) {
-        tmem_alloc(tslot, kScanTmemCols);
+        tmem_alloc(tslot, G::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -2029,14 +2066,14 @@ kda_fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_v)
     c.tmem = *tslot;
 
     if (threadIdx.x < 128 * NH)
-        scan_chain<NH>(c, p, threadIdx.x >> 7, e0, h, b, sq, nchunks);
+        scan_chain<G>(c, p, threadIdx.x >> 7, e0, h, b, sq, nchunks);
     else
-        scan_loader<NH>(c, p, &tm_v, e0, h, sq, nchunks);
+        scan_loader<G>(c, p, &tm_v, e0, h, sq, nchunks);
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (threadIdx.x < 32) tmem_dealloc(c.tmem, kScanTmemCols);
+    if (threadIdx.x < 32) tmem_dealloc(c.tmem, G::kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
@@ -2124,13 +2161,29 @@ cudaError_t launch_single(const FwdParams &p, const CUtensorMap &q, const CUtens
     return launch_single_one<GATE, GLA, true, Tg>(p, q, k, g, v, o, s);
 }
 
-template <int NH>
-cudaError_t launch_record_scan(const FwdParams &p, const CUtensorMap &v, cudaStream_t s) {
-    auto kern = kda_fwd_scan_kernel<NH>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ScanCfg<NH>::kSmem);
+template <class G>
+cudaError_t launch_record_scan_cfg(const FwdParams &p, const CUtensorMap &v, cudaStream_t s) {
+    auto kern = kda_fwd_scan_kernel<G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(p.dv / kDVS, p.H, p.B), ScanCfg<NH>::kThreads, ScanCfg<NH>::kSmem, s>>>(p, v);
+    kern<<<dim3(p.dv / G::SV, p.H, p.B), G::kThreads, G::kSmem, s>>>(p, v);
     return cudaGetLastError();
+}
+
+// The record scan's configuration: both value slices of a dv = 128 head in one CTA when one
+// CTA per 64-wide slice would take more than one wave of SMs (the head form halves the waves);
+// otherwise one CTA per slice, whose products run on a tensor pipe of their own.
+constexpr int kScanHeadPolicy = 1;       // 0: slices always, 1: heads for multi-wave batches, 2: heads always
+cudaError_t launch_record_scan(const FwdParams &p, const CUtensorMap &v, cudaStream_t s) {
+    if (p.dv == 2 * kDVS && kScanHeadPolicy != 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess)
+            sms = 0;
+        const long long slice_ctas = 2LL * p.B * p.H;
+        if (kScanHeadPolicy == 2 || (sms > 0 && slice_ctas > sms)) return launch_record_scan_cfg<ScanHead>(p, v, s);
+    }
+    return launch_record_scan_cfg<ScanSlice>(p, v, s);
 }
 
 // With chunk records (p.zrec set): the chunk-parallel Z kernel, then the record
@@ -2150,7 +2203,7 @@ cudaError_t launch_variant(const FwdParams &p, const CUtensorMap &q, const CUten
         zk<<<dim3((unsigned)nblk), kWyThreads, kZSmemBytes, s>>>(p, q, k, g);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        return launch_record_scan<kScanHalves>(p, v, s);
+        return launch_record_scan(p, v, s);
     }
 }
 
