@@ -245,14 +245,13 @@ int sm_count() {
 }
 
 // Chunk-record bytes of the two-kernel bf16 forward, 0 where the single kernel is the faster
-// form: float32 inputs; GLA (beta = 0, v unscaled), which has no inverse to hoist; and batches
-// whose single-kernel CTAs (one per 64-value slice of each sequence and head) fill between half
-// and all of the SMs in one wave -- there every SM builds its own chunks' operands next to its
-// scan and no records travel through HBM, while fewer CTAs leave most SMs idle and more CTAs
-// take several waves, where the chunk-parallel record kernel on every SM wins.
+// form: float32 inputs, and batches whose single-kernel CTAs (one per 64-value slice of each
+// sequence and head) fill between half and all of the SMs in one wave -- there every SM builds
+// its own chunks' operands next to its scan and no records travel through HBM, while fewer CTAs
+// leave most SMs idle and more CTAs take several waves, where the chunk-parallel record kernel
+// on every SM wins.
 size_t fwd_record_bytes(const kda_fwd_args *a) {
-    const bool gla = !(a->flags & KDA_FLAG_BETA_SCALES_V);
-    if (a->dtype != KDA_BF16 || gla) return 0;
+    if (a->dtype != KDA_BF16) return 0;
     const long long ctas = (long long)a->B * a->H * (a->dv / 64);
     const int sms = sm_count();
     if (sms > 0 && 2 * ctas > sms && ctas <= sms) return 0;

@@ -33,7 +33,7 @@
 //   A_chain and K~ and gamma^C as the chunk's record.  The record scan
 //   kernel then runs one CTA per (batch, head, 64-wide value slice) and takes
 //   three products per chunk (Z V, A_chain S^T, K~^T V_new).
-//   Single kernel (a 256-byte workspace, and GLA, which has no inverse): one
+//   Single kernel (a 256-byte workspace, or batches that fill one wave): one
 //   CTA per (batch, head, 64-wide value slice) walks its chunks in order with
 //   two warp roles (384 threads): warps 0-3 "chain", the serial part -- the
 //   state S^T (128 key channels x 64 values) in fp32 registers, one key
@@ -1546,7 +1546,7 @@ static_assert(OFF_KR + 16384 <= OFF_WMISC, "Z kernel tile layout");
 static_assert(WM_BAR + kNumBars * 8 <= WM_TSLOT, "Z kernel misc layout");
 static_assert(WM_ABORT + 4 <= kWMiscBytes, "Z kernel misc layout");
 
-template <int GATE, typename Tg>
+template <int GATE, bool GLA, typename Tg>
 __global__ void __launch_bounds__(kWyThreads, 4)
 kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_g) {
@@ -1627,7 +1627,9 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     const bool mark = rescale_tiles<GATE, true, false, true, false>(base, OFF_KR, wt, sq.len - n * kC, betas, gss,
                                                                     tot, krv, gam, has_gam, [] {}, rec);
     fence_proxy_async_smem();
-    const bool strong = __syncthreads_or(mark) != 0;
+    bool strong = false;                    // no gate: no decay, no sub-chunk path compiled
+    if constexpr (GATE == KDA_GATE_NONE) __syncthreads();
+    else strong = __syncthreads_or(mark) != 0;
     if (strong) {
         const StrongArgs sa{static_cast<const __nv_bfloat16 *>(p.q),
                             static_cast<const __nv_bfloat16 *>(p.k),
@@ -1648,7 +1650,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
         strong_prologue<GATE, false, true, Tg>(c, sa, wt, 0u, betas, rec);
     }
     // the cumsum partials are dead: their 4 KB hold the diagonal-block inverses
-    build_z<false, true>(c, wt, betas, 0, tot, strong);
+    build_z<GLA, true>(c, wt, betas, 0, tot, strong);
     fence_proxy_async_smem();               // the Z stores, before the bulk copy and the tensor core read them
     tc_fence_before();
     __syncthreads();                        // and every warp is done with the Gram's TMEM columns
@@ -1658,12 +1660,15 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
         tma_store_commit();
         // [W ; P W] = Z K<-  (M128 N128 K64) over the Gram's columns.  K<- is rows 0-63 of A_G,
         // read as an MN-major B tile: 16 K rows per step, its two 64-wide N blocks 16 KB apart.
-        const uint32_t a0 = smem_u32(base + OFF_KR), b0 = smem_u32(base + OFF_AG);
-        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+        // GLA (beta = 0): W = 0, no product.
+        if (!GLA) {
+            const uint32_t a0 = smem_u32(base + OFF_KR), b0 = smem_u32(base + OFF_AG);
+            const uint32_t id = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(c.tmem + TM_G, desc_kmajor(a0, 128, ks), sdesc_sw128(b0 + ks * 2048u, 16384u, 1024u), id,
-                     ks > 0);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(c.tmem + TM_G, desc_kmajor(a0, 128, ks), sdesc_sw128(b0 + ks * 2048u, 16384u, 1024u), id,
+                         ks > 0);
+        }
         mma_commit(c.bars + B_GRAM);
     }
     __syncwarp();
@@ -1679,7 +1684,12 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
         for (int cc = 0; cc < 2; ++cc) {
             const int col = half * 64 + cc * 32;
             float v[32];
-            tmem_ld32(c.tmem + TM_G + ((uint32_t)(quarter * 32) << 16) + col, v);
+            if (!GLA) {
+                tmem_ld32(c.tmem + TM_G + ((uint32_t)(quarter * 32) << 16) + col, v);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.f;
+            }
             if (quarter < 2) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = -v[e];
@@ -2191,11 +2201,9 @@ cudaError_t launch_record_scan(const FwdParams &p, const CUtensorMap &v, cudaStr
 template <int GATE, bool GLA, typename Tg>
 cudaError_t launch_variant(const FwdParams &p, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &g,
                            const CUtensorMap &v, const CUtensorMap &o, cudaStream_t s) {
-    if constexpr (GLA) {
-        return launch_single<GATE, GLA, Tg>(p, q, k, g, v, o, s);    // no inverse: no records
-    } else {
+    {
         if (!p.zrec) return launch_single<GATE, GLA, Tg>(p, q, k, g, v, o, s);
-        auto zk = kda_fwd_z_kernel<GATE, Tg>;
+        auto zk = kda_fwd_z_kernel<GATE, GLA, Tg>;
         cudaError_t e = cudaFuncSetAttribute(zk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kZSmemBytes);
         if (e != cudaSuccess) return e;
         const long long nblk = (long long)((p.T + kC - 1) / kC) * p.H * p.B;

@@ -119,10 +119,11 @@ typedef struct {
 
 /*
  * Bytes of workspace kda_chunk_fwd runs fastest with for these arguments (0
- * on bad args): 256 for the status word, plus, for bfloat16 inputs with the
- * delta term (every variant but GLA), one 66048-byte chunk record per chunk
- * slot and head -- B * ceil(T / 64) slots, or B + ceil(T / 64) with
- * cu_seqlens.
+ * on bad args): 256 for the status word, plus, for bfloat16 inputs, one
+ * 66048-byte chunk record per chunk slot and head -- B * ceil(T / 64) slots,
+ * or B + ceil(T / 64) with cu_seqlens -- except for batches whose
+ * single-kernel CTAs fill between half and all of the SMs (there the query
+ * returns 256 and the forward runs its single-kernel form).
  */
 size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
 

@@ -269,8 +269,10 @@ def test_fwd_records_need_an_aligned_workspace(lib):
     need = lib.kda_chunk_fwd_workspace(ctypes.byref(_args()))
     assert need > 256                                   # bf16 KDA: status word plus records
     assert _call(lib, _args(workspace=MISALIGNED, workspace_bytes=need)) == _lib.KDA_ERR_INVALID_ARG
-    # GLA (flags cleared, no beta) keeps the single kernel: no records
-    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(flags=0, beta=None))) == 256
+    # GLA (flags cleared, no beta) takes the same records (Z = [I ; P], A_chain = [0 ; Q<-])
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(flags=0, beta=None))) == need
+    # float32 inputs never do
+    assert lib.kda_chunk_fwd_workspace(ctypes.byref(_args(dtype=_lib.KDA_F32, dk=64))) == 256
 
 
 def test_bwd_and_dplr_need_an_aligned_workspace(lib):
