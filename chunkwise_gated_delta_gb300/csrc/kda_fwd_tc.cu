@@ -1559,6 +1559,7 @@ kda_fwd_z_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, co
     const int h = (int)(blockIdx.x % (unsigned)p.H), b = (int)((blockIdx.x / (unsigned)p.H) % (unsigned)p.B);
     const int n = nch - 1 - (int)(blockIdx.x / (unsigned)per_chunk);
     const Seq sq = seq_of(p, b);
+    grid_dep_launch();                      // the record scan may take SMs as this kernel's blocks finish
     if (n * kC >= sq.len) return;           // past the end of this sequence (or an empty one)
     const int wt = threadIdx.x;
     Ctx c;
@@ -2074,6 +2075,7 @@ kda_fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_v)
     __syncthreads();
     tc_fence_after();
     c.tmem = *tslot;
+    grid_dep_wait();                        // the Z kernel is done and its records are visible
 
     if (threadIdx.x < 128 * NH)
         scan_chain<G>(c, p, threadIdx.x >> 7, e0, h, b, sq, nchunks);
@@ -2176,8 +2178,18 @@ cudaError_t launch_record_scan_cfg(const FwdParams &p, const CUtensorMap &v, cud
     auto kern = kda_fwd_scan_kernel<G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(p.dv / G::SV, p.H, p.B), G::kThreads, G::kSmem, s>>>(p, v);
-    return cudaGetLastError();
+    // a programmatic dependent launch: its blocks set up while the Z kernel's last blocks run
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.dv / G::SV, p.H, p.B);
+    cfg.blockDim = dim3(G::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = G::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, v);
 }
 
 // The record scan's configuration: both value slices of a dv = 128 head in one CTA when one
