@@ -32,7 +32,7 @@ __host__ __device__ __forceinline__ int chunk_slots(int B, int T, bool packed) {
 
 // P: a parameter block with B, T and cu_seqlens (null for a dense batch).
 template <int C, class P>
-__device__ __forceinline__ Seq seq_of(const P &p, int b) {
+__host__ __device__ __forceinline__ Seq seq_of(const P &p, int b) {
     const int N = (p.T + C - 1) / C;
     if (!p.cu_seqlens) return Seq{b * p.T, p.T, b * N, N};
     const int lo = min(max(p.cu_seqlens[b], 0), p.T);
@@ -40,19 +40,10 @@ __device__ __forceinline__ Seq seq_of(const P &p, int b) {
     return Seq{lo, hi - lo, b + lo / C, (hi - lo + C - 1) / C};
 }
 
-// The sequence and chunk of a chunk-parallel CTA: grid (N, H, B) for dense batches;
-// (chunk slots, H, 1) for packed sequences, where the CTA bisects for the last sequence
-// whose first slot is at or before its own.  False for a slot no sequence uses (the
-// whole CTA then returns).
+// The sequence and chunk of chunk slot s of a packed batch: the last sequence whose first
+// slot is at or before s, by bisection.  False for a slot no sequence uses.
 template <int C, class P>
-__device__ __forceinline__ bool chunk_of(const P &p, int &b, int &n, Seq &sq) {
-    if (!p.cu_seqlens) {
-        b = blockIdx.z;
-        n = blockIdx.x;
-        sq = seq_of<C>(p, b);
-        return true;
-    }
-    const int s = blockIdx.x;
+__host__ __device__ __forceinline__ bool slot_of(const P &p, int s, int &b, int &n, Seq &sq) {
     int lo = 0, hi = p.B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -65,6 +56,20 @@ __device__ __forceinline__ bool chunk_of(const P &p, int &b, int &n, Seq &sq) {
     return n >= 0 && n < sq.nch;
 }
 
+// The sequence and chunk of a chunk-parallel CTA: grid (N, H, B) for dense batches;
+// (chunk slots, H, 1) for packed sequences (slot_of).  False for a slot no sequence uses
+// (the whole CTA then returns).
+template <int C, class P>
+__device__ __forceinline__ bool chunk_of(const P &p, int &b, int &n, Seq &sq) {
+    if (!p.cu_seqlens) {
+        b = blockIdx.z;
+        n = blockIdx.x;
+        sq = seq_of<C>(p, b);
+        return true;
+    }
+    return slot_of<C>(p, (int)blockIdx.x, b, n, sq);
+}
+
 // Grid of the chunk-parallel kernels.
 template <int C>
 inline dim3 chunk_grid(int B, int T, int H, bool packed) {
@@ -75,11 +80,11 @@ inline dim3 chunk_grid(int B, int T, int H, bool packed) {
 // slots (records and per-chunk products), and state slots (the state before each chunk,
 // then the final one).
 template <int C, class P>
-__device__ __forceinline__ size_t chunk_index(const P &p, const Seq &sq, int h, int n) {
+__host__ __device__ __forceinline__ size_t chunk_index(const P &p, const Seq &sq, int h, int n) {
     return (size_t)h * chunk_slots<C>(p.B, p.T, p.cu_seqlens != nullptr) + sq.slot0 + n;
 }
 template <int C, class P>
-__device__ __forceinline__ size_t state_index(const P &p, const Seq &sq, int b, int h, int n) {
+__host__ __device__ __forceinline__ size_t state_index(const P &p, const Seq &sq, int b, int h, int n) {
     return (size_t)h * (chunk_slots<C>(p.B, p.T, p.cu_seqlens != nullptr) + p.B) + sq.slot0 + b + n;
 }
 
