@@ -2,7 +2,7 @@
 
 Every step of the computation runs in the CUDA library (``libkda.so``); this
 module only turns torch tensors into pointers and sizes, picks the current
-stream and keeps a zero-filled workspace per device.  There is no CPU path:
+stream and keeps a zero-filled workspace per device and stream.  There is no CPU path:
 when the library is missing, :func:`_lib.load` raises.
 """
 from __future__ import annotations
@@ -39,14 +39,25 @@ def _check(t, name):
         raise ValueError(f"{name} must be contiguous")
 
 
-def workspace_for(device, nbytes: int) -> torch.Tensor:
-    """A cached, zero-filled workspace of at least ``nbytes`` on ``device``."""
+def workspace_for(device, nbytes: int, stream=None) -> torch.Tensor:
+    """A cached, zero-filled workspace of at least ``nbytes`` for calls on ``stream``
+    (default: the current stream of ``device``).
+
+    One per (device, stream): calls on different streams may run at the same time on
+    the GPU, and two such calls must not share chunk records or a status block.  The
+    workspace is allocated on its stream, so a replaced one goes back to the
+    allocator in that stream's order.
+    """
     dev = torch.device(device)
-    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    if stream is None:
+        stream = torch.cuda.current_stream(idx)
+    key = (idx, stream.cuda_stream)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
         _workspaces.pop(key, None)
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=torch.device("cuda", idx))
         _workspaces[key] = ws
     return ws
 
@@ -110,12 +121,12 @@ def kda_chunk_fwd(q, k, v, g=None, beta=None, h0=None, *, gate=None, scale_v=Tru
         # invalid arguments: let the launch entry point report which status
         rc = lib.kda_chunk_fwd(ctypes.byref(args), None)
         raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "kda_chunk_fwd")
-    if workspace is None:
-        workspace = workspace_for(q.device, need)
-    args.workspace = _ptr(workspace)
-    args.workspace_bytes = workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    if workspace is None:
+        workspace = workspace_for(q.device, need, stream)
+    args.workspace = _ptr(workspace)
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
     rc = lib.kda_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd")
@@ -219,12 +230,12 @@ def kda_chunk_bwd(q, k, v, g, beta, h0, do, dht=None, *, gate=None, scale_v=True
     if need == 0:
         rc = lib.kda_chunk_bwd(ctypes.byref(args), None)
         raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "kda_chunk_bwd")
-    if workspace is None:
-        workspace = workspace_for(q.device, need)
-    args.workspace = _ptr(workspace)
-    args.workspace_bytes = workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    if workspace is None:
+        workspace = workspace_for(q.device, need, stream)
+    args.workspace = _ptr(workspace)
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
     rc = lib.kda_chunk_bwd(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "kda_chunk_bwd")
@@ -287,12 +298,12 @@ def dplr_chunk_fwd(q, k, v, a, b, g=None, h0=None, *, gate=None, clip=False, out
     if need == 0:
         rc = lib.dplr_chunk_fwd(ctypes.byref(args), None)
         raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "dplr_chunk_fwd")
-    if workspace is None:
-        workspace = workspace_for(q.device, need)
-    args.workspace = _ptr(workspace)
-    args.workspace_bytes = workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    if workspace is None:
+        workspace = workspace_for(q.device, need, stream)
+    args.workspace = _ptr(workspace)
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
     rc = lib.dplr_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "dplr_chunk_fwd")
@@ -364,12 +375,12 @@ def dplr_chunk_bwd(q, k, v, a, b, g, h0, do, dht=None, *, gate=None, clip=False,
     if need == 0:
         rc = lib.dplr_chunk_bwd(ctypes.byref(x), None)
         raise KdaError(rc if rc != 0 else _lib.KDA_ERR_INVALID_ARG, "dplr_chunk_bwd")
-    if workspace is None:
-        workspace = workspace_for(q.device, need)
-    x.workspace = _ptr(workspace)
-    x.workspace_bytes = workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    if workspace is None:
+        workspace = workspace_for(q.device, need, stream)
+    x.workspace = _ptr(workspace)
+    x.workspace_bytes = workspace.numel() * workspace.element_size()
     rc = lib.dplr_chunk_bwd(ctypes.byref(x), ctypes.c_void_p(stream.cuda_stream))
     if rc != _lib.KDA_OK:
         raise KdaError(rc, "dplr_chunk_bwd")
@@ -377,12 +388,16 @@ def dplr_chunk_bwd(q, k, v, a, b, g, h0, do, dht=None, *, gate=None, clip=False,
 
 
 def status_read(workspace=None, device=None, stream=None) -> int:
-    """Device status word of the workspace (waits for the stream, then clears it)."""
+    """Device status word of the workspace (waits for the stream, then clears it); by
+    default the cached workspace of ``stream`` (default: the current stream of ``device``)."""
     lib = _lib.load()
-    if workspace is None:
-        workspace = workspace_for(device or torch.cuda.current_device(), 256)
+    if workspace is not None:
+        device = workspace.device
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     if stream is None:
-        stream = torch.cuda.current_stream(workspace.device)
+        stream = torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = workspace_for(dev, 256, stream)
     return lib.kda_status_read(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
 
 

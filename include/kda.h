@@ -160,7 +160,11 @@ size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
  * domain.  In the single-kernel form such a chunk makes the call take a
  * second launch (the first notes the call in word 8 of the status block, the
  * second redoes the call with the sub-chunk Gram; without such a chunk the
- * second launch exits at once); a captured graph replays both.
+ * second launch exits at once).  A captured graph replays both launches with
+ * the note of the capture: once a replay has met such a chunk, the second
+ * launch of every later replay on the same workspace redoes the call too
+ * (same results, at the sub-chunk form's cost) until the caller clears the
+ * status block.
  */
 kda_status kda_chunk_fwd(const kda_fwd_args *args, kda_stream_t stream);
 
