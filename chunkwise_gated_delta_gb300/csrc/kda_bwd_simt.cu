@@ -250,6 +250,26 @@ constexpr size_t prep_smem_bytes() {
 // S <- S Diag(gamma^C) + V_new^T K~.  One CTA per (64-wide value slice, head, sequence).
 // The records of chunk n + 1 travel (cp.async, double buffer) while chunk n computes.
 constexpr int kDVD = 64;     // value rows per CTA in the two scans
+
+// A scan's [kDVD][DK] state block between shared memory (row stride SK) and global rows of DK
+// floats, 16 bytes per access (rows 16-byte aligned on both sides); a null source reads zeros.
+template <int DK, int SK>
+__device__ __forceinline__ void block_to_shared(const float *src, float *dst) {
+    constexpr int V = DK / 4;
+    for (int idx = threadIdx.x; idx < kDVD * V; idx += kThreads) {
+        const int e = idx / V, d = (idx % V) * 4;
+        *reinterpret_cast<float4 *>(dst + e * SK + d) =
+            src ? *reinterpret_cast<const float4 *>(src + (size_t)e * DK + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+template <int DK, int SK>
+__device__ __forceinline__ void block_to_global(const float *src, float *dst) {
+    constexpr int V = DK / 4;
+    for (int idx = threadIdx.x; idx < kDVD * V; idx += kThreads) {
+        const int e = idx / V, d = (idx % V) * 4;
+        *reinterpret_cast<float4 *>(dst + (size_t)e * DK + d) = *reinterpret_cast<const float4 *>(src + e * SK + d);
+    }
+}
 template <int DK>
 __host__ __device__ constexpr int states_buf_floats() {
     return 2 * kC * pad4(DK) + kC * pad4(kDVD) + DK;       // W, K~, U (then V_new), gamma^C
@@ -280,19 +300,13 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
         wg::load_tile_async<1, DK, DK, kThreads>(rec + R::GC, DK, bf + 2 * kC * SK + kC * SV);
     };
 
-    for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
-        const int e = idx / DK, d = idx % DK;
-        Sm[e * SK + d] = p.h0 ? p.h0[(head * dv + e0 + e) * DK + d] : 0.f;
-    }
+    block_to_shared<DK, SK>(p.h0 ? p.h0 + (head * dv + e0) * DK : nullptr, Sm);
     issue(0);
     wg::cp_async_commit();
     for (int n = 0; n < N; ++n) {
         float *Wm = bufs + (n & 1) * BUF, *KT = Wm + kC * SK, *Um = KT + kC * SK, *gam = Um + kC * SV;
         __syncthreads();               // S is final for chunk n; chunk n - 1's buffer is free
-        for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            Sws[((size_t)n * dv + e0 + e) * DK + d] = Sm[e * SK + d];
-        }
+        block_to_global<DK, SK>(Sm, Sws + ((size_t)n * dv + e0) * DK);
         if (n + 1 < N) issue(n + 1);
         wg::cp_async_commit();         // (an empty group on the last chunk keeps the count)
         wg::cp_async_wait<1>();        // chunk n's tiles have landed (this thread's copies)
@@ -314,10 +328,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_states_kernel(const BwdParam
                 [&](int e, int d, float x) { Sm[(eo + e) * SK + d] = Sm[(eo + e) * SK + d] * gam[d] + x; });
     }
     __syncthreads();
-    for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
-        const int e = idx / DK, d = idx % DK;
-        Sws[((size_t)N * dv + e0 + e) * DK + d] = Sm[e * SK + d];
-    }
+    block_to_global<DK, SK>(Sm, Sws + ((size_t)N * dv + e0) * DK);
 }
 
 // ------------------------------------------------------------------ kernel B
@@ -365,10 +376,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
                                                     reinterpret_cast<Tin *>(bf + 3 * kC * SK + kC * SC + DK));
     };
 
-    for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
-        const int e = idx / DK, d = idx % DK;
-        dS[e * SK + d] = p.grad_ht ? p.grad_ht[(head * dv + e0 + e) * DK + d] : 0.f;
-    }
+    block_to_shared<DK, SK>(p.grad_ht ? p.grad_ht + (head * dv + e0) * DK : nullptr, dS);
     if (N > 0) issue(N - 1);
     wg::cp_async_commit();
     for (int n = N - 1; n >= 0; --n) {
@@ -376,10 +384,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
         float *gam = Pm + kC * SC;
         const Tin *draw = reinterpret_cast<const Tin *>(gam + DK);
         __syncthreads();               // dS is final for chunk n; chunk n + 1's buffer is free
-        for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            dSws[((size_t)n * dv + e0 + e) * DK + d] = dS[e * SK + d];
-        }
+        block_to_global<DK, SK>(dS, dSws + ((size_t)n * dv + e0) * DK);
         if (n > 0) issue(n - 1);
         wg::cp_async_commit();         // (an empty group on the last step keeps the count)
         wg::cp_async_wait<1>();        // chunk n's tiles have landed (this thread's copies)
@@ -404,12 +409,7 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_dstate_kernel(const BwdParam
                 [&](int e, int d, float x) { dS[(eo + e) * SK + d] = dS[(eo + e) * SK + d] * gam[d] + x; });
     }
     __syncthreads();
-    if (p.grad_h0) {
-        for (int idx = tid; idx < kDVD * DK; idx += kThreads) {
-            const int e = idx / DK, d = idx % DK;
-            p.grad_h0[(head * dv + e0 + e) * DK + d] = dS[e * SK + d];
-        }
-    }
+    if (p.grad_h0) block_to_global<DK, SK>(dS, p.grad_h0 + (head * dv + e0) * DK);
 }
 
 // ------------------------------------------------------------------ kernel C
@@ -479,6 +479,20 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
             wg::cp_async_commit();
         }
     };
+    // A~, P, N of the chunk record and the chunk's V_new and dU (float32, written by the prep kernel
+    // and the scans) by cp.async too: one group, committed before the slabs' and waited for after
+    // the loads below
+    {
+        using R = Rec<DK, DV>;
+        const float *rec = p.ws_prep + ci * rec_floats(DK, DV);
+        wg::load_tile_async<kC, kC, SC, kThreadsC>(rec + R::A, kC, Am);
+        wg::load_tile_async<kC, kC, SC, kThreadsC>(rec + R::P, kC, Pm);
+        wg::load_tile_async<kC, kC, SC, kThreadsC>(rec + R::N, kC, Nm);
+        wg::load_tile_async<kC, DV, SV, kThreadsC>(p.ws_vnew + ci * kC * DV, DV, Vn);
+        wg::load_tile_async<kC, DV, SV, kThreadsC>(p.ws_du + ci * kC * DV, DV, dU);
+        wg::cp_async_commit();
+    }
+    static_assert(NL >= 4, "four slab groups follow the tiles' group");
     issue_upto(4);
 
     // ---- loads: Gamma and the rescaled tiles, v, dO, beta
@@ -489,18 +503,7 @@ __global__ void __launch_bounds__(kThreadsC) kda_bwd_grad_kernel(const BwdParams
         wg::load_tile<kC, DV, SV, kThreadsC>(v + r0, rs, nvalid, Vm);
         wg::load_tile<kC, DV, SV, kThreadsC>(dop + r0, rs, nvalid, dO);
     }
-    __syncthreads();
-    // ---- A~, P and N from the chunk record
-    {
-        using R = Rec<DK, DV>;
-        const float *rec = p.ws_prep + ci * rec_floats(DK, DV);
-        wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::A, kC, kC, Am);
-        wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::P, kC, kC, Pm);
-        wg::load_tile<kC, kC, SC, kThreadsC>(rec + R::N, kC, kC, Nm);
-        // V_new and dU of this chunk, from the two scans
-        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_vnew + ci * kC * DV, DV, kC, Vn);
-        wg::load_tile<kC, DV, SV, kThreadsC>(p.ws_du + ci * kC * DV, DV, kC, dU);
-    }
+    wg::cp_async_wait<4>();            // the tiles' group (at most the four slab groups after it in flight)
     __syncthreads();
     // ---- dO V_new^T * M (into Pm)
     wg::gemm<kC, TF32, 16>(
