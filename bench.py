@@ -51,7 +51,7 @@ KERNELS = {"kda": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gdn": ("kda_fwd_tc", "kda_fw
            "deltanet": ("kda_fwd_tc", "kda_fwd_tc.cu"), "gla": ("kda_fwd_tc", "kda_fwd_tc.cu"),
            "dplr": ("dplr_fwd_simt", "dplr_fwd_simt.cu"), "kda_bwd": ("kda_bwd_simt", "kda_bwd_simt.cu"),
            "dplr_bwd": ("dplr_bwd_simt", "dplr_bwd_simt.cu")}
-LAUNCHES_PER_STEP = {"kda": 2, "gdn": 2, "deltanet": 2, "gla": 1, "dplr": 2, "kda_bwd": 4,
+LAUNCHES_PER_STEP = {"kda": 2, "gdn": 2, "deltanet": 2, "gla": 2, "dplr": 2, "kda_bwd": 4,
                      "dplr_bwd": 4}   # kernels one step launches (bf16 forward: its two-kernel form)
 
 
