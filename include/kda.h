@@ -47,6 +47,9 @@
  *     KDA_ERR_TIMEOUT recorded and its outputs undefined, after every copy
  *     and tensor-core product the kernels started has completed, so the next
  *     call runs normally.  kda_status_read leaves it as it is.
+ *   - Word 8 of the workspace (bytes 32-35) belongs to the bf16 forward's
+ *     single-kernel form, which notes there a call that needs its second
+ *     launch (see kda_chunk_fwd); callers do not write it.
  *   - Outputs must not alias inputs.
  */
 #ifndef KDA_H_
@@ -134,13 +137,14 @@ size_t kda_chunk_fwd_workspace(const kda_fwd_args *args);
  * fp32 accumulation, fp32 state).
  *
  * The workspace must be at least 256 bytes (KDA_ERR_WORKSPACE otherwise).
- * For bfloat16 inputs with the delta term and workspace_bytes >=
- * kda_chunk_fwd_workspace(args) the forward takes two kernels: a
+ * For bfloat16 inputs and workspace_bytes >= kda_chunk_fwd_workspace(args)
+ * (when that is more than 256) the forward takes two kernels: a
  * chunk-parallel one writes every chunk's record into the workspace --
  * Z = [T ; P T] (T = (I + L)^{-1} Diag(beta) with L the masked
  * beta K<- K->^T, P the masked Q<- K->^T: the forward recap of page "Kimi
- * Delta Attention backward"), A_chain = [-W ; Q<- - P W] with W = T K<-,
- * the rescaled K-> and gamma^C -- then the scan kernel reads them; the
+ * Delta Attention backward"), A_chain = [-W ; Q<- - P W] with W = T K<-
+ * (GLA, beta = 0: Z = [I ; P], A_chain = [0 ; Q<-]), the rescaled K-> and
+ * gamma^C -- then the scan kernel reads them; the
  * workspace must then be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
  * With a smaller workspace, or where the query returns 256 (a batch whose
  * single-kernel CTAs, one per 64 values of each sequence and head, fill
