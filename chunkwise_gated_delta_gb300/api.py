@@ -16,6 +16,7 @@ from ._lib import KdaError
 
 _GATES = {"none": _lib.KDA_GATE_NONE, "scalar": _lib.KDA_GATE_SCALAR, "channel": _lib.KDA_GATE_CHANNEL}
 _workspaces: dict = {}
+_MAX_WORKSPACES = 16   # cached (device, stream) workspaces; callers that make many streams evict the oldest
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -53,12 +54,14 @@ def workspace_for(device, nbytes: int, stream=None) -> torch.Tensor:
     if stream is None:
         stream = torch.cuda.current_stream(idx)
     key = (idx, stream.cuda_stream)
-    ws = _workspaces.get(key)
+    ws = _workspaces.pop(key, None)
     if ws is None or ws.numel() < nbytes:
-        _workspaces.pop(key, None)
         with torch.cuda.stream(stream):
             ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=torch.device("cuda", idx))
-        _workspaces[key] = ws
+    _workspaces[key] = ws                  # most recently used last
+    while len(_workspaces) > _MAX_WORKSPACES:
+        # the least recently used goes back to the allocator, in its own stream's order
+        _workspaces.pop(next(iter(_workspaces)))
     return ws
 
 
